@@ -1,0 +1,166 @@
+"""Seeded synthetic inputs for the W4 group-affine sparse-MoE layer.
+
+This module draws layers and token batches with the shapes and value
+distributions of the layer described in "Optimizing on-device inference for
+Apple Silicon" (section "Qwen creates three different workload shapes": 256
+experts, top-8, one shared expert; section "Dequantise weights during matrix
+multiplication": 4-bit codes, one bf16 scale and one bf16 bias per 64
+weights).  It implements none of the layer's arithmetic: no dequantisation,
+no top-k selection, no softmax, no expert projection.  The only arithmetic on
+drawn values is the input screen in `draw_tokens`, which recomputes the raw
+router scores x.W_r (+bias) in float64 solely to redraw tokens whose leading
+scores are closer than the required margin.
+
+Everything is numpy (PCG64) so the same seed gives the same bytes on any host.
+
+Layout of a drawn layer (all numpy, C-contiguous):
+  * gate/up codes   uint32 [E][I][H/8]   (row = output feature, words along input)
+  * down codes      uint32 [E][H][I/8]
+  * scales/biases   uint16 bf16 bit patterns [E][rows][cols/64]
+  * shared expert   same without the leading E
+  * router_w        float32 [H][E]; router_bias float32 [E] or None
+  * shared_gate     float32 [H]
+Eight 4-bit codes sit in each uint32, the lowest-index column in the lowest
+nibble.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+GROUP = 64          # weights sharing one scale and one bias
+MARGIN = 1e-2       # minimum gap between adjacent leading router scores
+
+# Workload table.  Each entry is a layer shape plus a batch description.
+CONFIGS = {
+    # tiny layer the oracle finishes in well under a second
+    "tiny_T4": dict(T=4, H=256, E=16, top_k=2, I=128, zipf=None, seed=0),
+    # batch-1 decode step on the full layer, uniform expert popularity
+    "decode_T1": dict(T=1, H=2048, E=256, top_k=8, I=512, zipf=None, seed=1),
+    # short prefill, Zipf(1.0)-skewed routing
+    "prefill_T512": dict(T=512, H=2048, E=256, top_k=8, I=512, zipf=1.0, seed=2),
+    # 4K-token prefill, Zipf(1.0)-skewed routing
+    "prefill_T4096": dict(T=4096, H=2048, E=256, top_k=8, I=512, zipf=1.0, seed=3),
+    # 16K-token prefill in four 4096-row chunks, then 64 batch-1 decode steps,
+    # Zipf(1.2)-skewed routing
+    "long_T16384": dict(T=16384, H=2048, E=256, top_k=8, I=512, zipf=1.2, seed=4,
+                        chunk=4096, decode_steps=64),
+}
+
+
+@dataclasses.dataclass
+class W4Matrix:
+    """One group-affine 4-bit matrix (or a stack of them along a leading E axis)."""
+    codes: np.ndarray      # uint32 [..., rows, cols/8]
+    scales: np.ndarray     # uint16 bf16 bits [..., rows, cols/64]
+    biases: np.ndarray     # uint16 bf16 bits [..., rows, cols/64]
+
+
+@dataclasses.dataclass
+class W4Layer:
+    H: int
+    E: int
+    I: int
+    top_k: int
+    router_w: np.ndarray               # float32 [H][E]
+    router_bias: Optional[np.ndarray]  # float32 [E] or None
+    shared_gate: np.ndarray            # float32 [H]
+    gate: W4Matrix                     # [E][I][H/8]
+    up: W4Matrix                       # [E][I][H/8]
+    down: W4Matrix                     # [E][H][I/8]
+    sh_gate: W4Matrix                  # [I][H/8]
+    sh_up: W4Matrix                    # [I][H/8]
+    sh_down: W4Matrix                  # [H][I/8]
+
+    def nbytes_expert(self) -> int:
+        """Bytes of one expert's three matrices (codes + scales + biases)."""
+        w = 3 * self.H * self.I
+        return w // 2 + 2 * 2 * (w // GROUP)
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (round to nearest, ties to even); return the bits."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _streams(seed: int, n: int):
+    return [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(n)]
+
+
+def _draw_matrix(rng: np.random.Generator, lead: tuple, rows: int, cols: int) -> W4Matrix:
+    """Codes uniform in [0,15] (a uniform 32-bit word is eight uniform nibbles);
+    s = bf16(|N(0,0.02)|); b = bf16(-8 s + N(0,0.002))."""
+    assert cols % GROUP == 0
+    codes = rng.integers(0, 1 << 32, size=lead + (rows, cols // 8), dtype=np.uint32)
+    shape_g = lead + (rows, cols // GROUP)
+    s_bits = f32_to_bf16_bits(np.abs(rng.normal(0.0, 0.02, size=shape_g)).astype(np.float32))
+    s = bf16_bits_to_f32(s_bits)
+    b_bits = f32_to_bf16_bits((-8.0 * s + rng.normal(0.0, 0.002, size=shape_g)).astype(np.float32))
+    return W4Matrix(codes, s_bits, b_bits)
+
+
+def zipf_bias(E: int, s: float) -> np.ndarray:
+    """Per-expert router offset -s*ln(rank), rank = e+1: multiplies expert e's
+    softmax odds by a Zipf(s) popularity weight."""
+    return (-s * np.log(np.arange(1, E + 1, dtype=np.float64))).astype(np.float32)
+
+
+def draw_layer(H: int, E: int, I: int, top_k: int, zipf: Optional[float], seed: int) -> W4Layer:
+    rw, rr, rs = _streams(seed, 3)
+    gate = _draw_matrix(rw, (E,), I, H)
+    up = _draw_matrix(rw, (E,), I, H)
+    down = _draw_matrix(rw, (E,), H, I)
+    sh_gate = _draw_matrix(rs, (), I, H)
+    sh_up = _draw_matrix(rs, (), I, H)
+    sh_down = _draw_matrix(rs, (), H, I)
+    router_w = rr.normal(0.0, 0.05, size=(H, E)).astype(np.float32)
+    shared_gate = rr.normal(0.0, 0.05, size=(H,)).astype(np.float32)
+    bias = zipf_bias(E, zipf) if zipf else None
+    return W4Layer(H, E, I, top_k, router_w, bias, shared_gate, gate, up, down,
+                   sh_gate, sh_up, sh_down)
+
+
+def _screen_ok(x_bits: np.ndarray, layer: W4Layer, margin: float) -> np.ndarray:
+    """Input screen: True for tokens whose top-(k+1) raw scores are pairwise
+    separated by at least `margin` (adjacent pairs after sorting)."""
+    x = bf16_bits_to_f32(x_bits).astype(np.float64)
+    sc = x @ layer.router_w.astype(np.float64)
+    if layer.router_bias is not None:
+        sc = sc + layer.router_bias.astype(np.float64)
+    kk = min(layer.top_k + 1, layer.E)
+    lead = -np.sort(-sc, axis=1)[:, :kk]
+    if kk < 2:
+        return np.ones(x.shape[0], dtype=bool)
+    return np.all(lead[:, :-1] - lead[:, 1:] >= margin, axis=1)
+
+
+def draw_tokens(layer: W4Layer, T: int, seed: int, stream: int = 0,
+                margin: Optional[float] = MARGIN) -> np.ndarray:
+    """x = bf16(N(0,1)) of shape [T][H] (bf16 bits).  With a margin, any token
+    failing the score screen is redrawn from the same stream until it passes."""
+    rng = _streams(seed * 1000003 + 17 + stream, 1)[0]
+    x = f32_to_bf16_bits(rng.normal(0.0, 1.0, size=(T, layer.H)).astype(np.float32))
+    if margin is None or T == 0:
+        return x
+    for _ in range(1000):
+        bad = np.nonzero(~_screen_ok(x, layer, margin))[0]
+        if bad.size == 0:
+            return x
+        x[bad] = f32_to_bf16_bits(rng.normal(0.0, 1.0, size=(bad.size, layer.H)).astype(np.float32))
+    raise RuntimeError("input screen did not converge")
+
+
+def draw_config(name: str, T: Optional[int] = None, stream: int = 0):
+    """Layer and token batch of a named workload; T overrides the batch size."""
+    c = CONFIGS[name]
+    layer = draw_layer(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], c["seed"])
+    x = draw_tokens(layer, c["T"] if T is None else T, c["seed"], stream)
+    return layer, x
