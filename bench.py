@@ -1,0 +1,427 @@
+"""Benchmark of the W4 group-affine sparse-MoE layer on GB300.
+
+Workload (one step): the long-prompt configuration -- a 16384-token prompt
+processed as four 4096-row prefill chunks, then 64 consecutive batch-1 decode
+steps; H=2048, E=256 experts, top-8, I=512, one shared expert, Zipf(1.2)-skewed
+routing; every input seeded and synthetic.  The prefill chunks use one layer
+(455 MB of packed weights, larger than L2).  The 64 decode steps cycle over 16
+layers of the same shape with distinct weights (7.3 GB), as a multi-layer model
+would, so a decode step never finds its layer's weights left in L2.
+
+Printed (rank 0, one JSON line): whole-step tokens/s, prefill and decode
+tokens/s, the roofline of the dominant kernel and of the decode step, the CPU
+oracle timed on this host, the end-to-end rate through host buffers, clocks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4g64 MoE layer tok/s at T=1 & T=4096; % of HBM / bf16 TC roofline"
+WORKLOAD = "long_T16384"
+N_REPLICAS = 16
+PREFILL_KERNELS = ["router_scores", "topk", "chunk_count", "scan", "assign", "gemm_gate_up", "gemm_down", "combine"]
+DECODE_KERNELS = ["decode_router", "decode_gate_up", "decode_down"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# multi-process plumbing (one process per GPU; replicas, no data-path exchange)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def reduce_max(value, dist, device):
+    """Max over ranks of a float (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank, world, seconds):
+    """Whole-job throughput: every rank processes the same units (weak scaling)."""
+    return units_per_rank * world / seconds
+
+
+# ---------------------------------------------------------------------------
+# measured peaks and clocks
+# ---------------------------------------------------------------------------
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def build_workload(torch, mw, S, device):
+    c = S.CONFIGS[WORKLOAD]
+    L0, x = S.draw_config(WORKLOAD)
+    xdec = S.draw_tokens(L0, c["decode_steps"], c["seed"], stream=1)
+    layers = [mw.DeviceLayer(L0, device)]
+    for r in range(1, N_REPLICAS):
+        Lr = S.draw_layer_torch(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], seed=1000 + r, device=device)
+        layers.append(mw.DeviceLayer(Lr, device))
+    return c, L0, x, xdec, layers
+
+
+def run_gpu(args, rank, local_rank, world, dist):
+    import torch
+    from bit_quantized_sparse_gb300 import moe_w4 as mw
+    from bit_quantized_sparse_gb300 import synthetic as S
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    c, L0, x_np, xdec_np, layers = build_workload(torch, mw, S, device)
+    T, chunk, ndec, H = c["T"], c["chunk"], c["decode_steps"], c["H"]
+    x = mw.tokens_to_device(x_np, device)
+    xdec = mw.tokens_to_device(xdec_np, device)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    outdec = torch.empty((ndec, H), dtype=torch.bfloat16, device=device)
+    ws = layers[0].workspace(chunk)
+    stream = torch.cuda.Stream(device)
+
+    def prefill_part():
+        for i in range(0, T, chunk):
+            mw.forward_prefill(layers[0], x[i:i + chunk], out=out[i:i + chunk], ws=ws)
+
+    def decode_part():
+        for i in range(ndec):
+            mw._check(mw.moe_w4_forward_decode(ctypes.byref(layers[i % N_REPLICAS].c), 1, xdec[i:i + 1].data_ptr(),
+                                               outdec[i:i + 1].data_ptr(), ws.data_ptr(), ws.numel(),
+                                               torch.cuda.current_stream().cuda_stream), "decode")
+
+    def step():
+        prefill_part()
+        decode_part()
+
+    # eager warm-up (first-call host set-up happens outside any capture)
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    if layers[0].status() != 0:
+        raise RuntimeError(f"device status {layers[0].status()} after warm-up")
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    g_step, g_pre, g_dec = capture(step), capture(prefill_part), capture(decode_part)
+
+    def timed(g, n):
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        return reduce_max(e0.elapsed_time(e1) / 1e3, dist, device)
+
+    with ClockSampler(local_rank) as clk:
+        t_step = timed(g_step, args.steps)
+    clocks = clk.summary()
+    t_pre = timed(g_pre, args.steps)
+    t_dec = timed(g_dec, args.steps)
+
+    # per-kernel durations: the library records events around its kernels
+    def traced(fn, names):
+        n = len(names) + 1
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for e in evs:
+                e.record(stream)
+        torch.cuda.synchronize()
+        arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in evs])
+        mw._check(mw.moe_w4_set_trace_events(arr, n), "trace")
+        try:
+            g = capture(fn)
+        finally:
+            mw.moe_w4_set_trace_events(None, 0)
+        acc = np.zeros(n - 1)
+        for _ in range(args.warmup):
+            g.replay()
+        for _ in range(args.steps):
+            g.replay()
+            torch.cuda.synchronize()
+            acc += [evs[i].elapsed_time(evs[i + 1]) / 1e3 for i in range(n - 1)]
+        return dict(zip(names, (acc / args.steps).tolist()))
+
+    xc = x[:chunk]
+    k_pre = traced(lambda: mw.forward_prefill(layers[0], xc, out=out[:chunk], ws=ws), PREFILL_KERNELS)
+    k_dec = traced(lambda: mw._check(mw.moe_w4_forward_decode(
+        ctypes.byref(layers[1].c), 1, xdec[:1].data_ptr(), outdec[:1].data_ptr(), ws.data_ptr(), ws.numel(),
+        torch.cuda.current_stream().cuda_stream), "decode"), DECODE_KERNELS)
+
+    # end to end through host buffers: copy in, run, copy out, every step
+    x_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(x.cpu())
+    xd_host = torch.empty((ndec, H), dtype=torch.bfloat16, pin_memory=True)
+    xd_host.copy_(xdec.cpu())
+    o_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    od_host = torch.empty((ndec, H), dtype=torch.bfloat16, pin_memory=True)
+
+    def e2e_steps(n):
+        with torch.cuda.stream(stream):
+            for _ in range(n):
+                x.copy_(x_host, non_blocking=True)
+                xdec.copy_(xd_host, non_blocking=True)
+                g_step.replay()
+                o_host.copy_(out, non_blocking=True)
+                od_host.copy_(outdec, non_blocking=True)
+
+    e2e_steps(args.warmup)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    e2e_steps(args.steps)
+    torch.cuda.synchronize()
+    t_e2e = reduce_max(time.perf_counter() - t0, dist, device)
+    status = layers[0].status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    return dict(c=c, L0=L0, x_np=x_np, xdec_np=xdec_np, t_step=t_step, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e,
+                clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device))
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work (per unit) for the roofline
+# ---------------------------------------------------------------------------
+def expert_bytes(H, I):
+    w = 3 * H * I
+    return w // 2 + 2 * 2 * (w // 64)
+
+
+def decode_bytes(c, T=1):
+    """Bytes one decode call must move: k+1 experts' packed weights, router
+    weights, shared gate, x and out."""
+    H, E, I, k = c["H"], c["E"], c["I"], c["top_k"]
+    return (k + 1) * expert_bytes(H, I) + H * E * 4 + H * 4 + T * H * 2 + T * H * 2
+
+
+def gemm_flops(c, T, which):
+    H, I, k = c["H"], c["I"], c["top_k"]
+    rows = T * k + T
+    return 2 * rows * H * 2 * I if which == "gate_up" else 2 * rows * I * H
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline arm and the cpu_baseline object)
+# ---------------------------------------------------------------------------
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def time_oracle(L0, x_np, n_prefill, n_decode, xdec_np):
+    import oracle as O
+    t0 = time.perf_counter()
+    O.moe_layer(L0, x_np[:n_prefill])
+    for i in range(n_decode):
+        O.moe_layer(L0, xdec_np[i:i + 1])
+    dt = time.perf_counter() - t0
+    return (n_prefill + n_decode) / dt, dt
+
+
+def run_reference(args):
+    """The oracle as it stands, on this host's cores: each step is a bounded
+    sample of the workload (8 prefill rows and one decode row)."""
+    from bit_quantized_sparse_gb300 import synthetic as S
+    c = S.CONFIGS[WORKLOAD]
+    L0, x = S.draw_config(WORKLOAD, T=64)
+    xdec = S.draw_tokens(L0, 4, c["seed"], stream=1)
+    for _ in range(args.warmup):
+        time_oracle(L0, x, 8, 1, xdec)
+    times = [time_oracle(L0, x, 8, 1, xdec)[1] for _ in range(args.steps)]
+    total = sum(times)
+    val = 9 * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tok/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: H=2048 E=256 top-8 I=512 Zipf(1.2); step = 8 prefill rows + 1 decode row"},
+            "cpu_baseline": {"value": val, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": "8 prefill rows + 1 decode row per step of the long_T16384 layer"},
+            "e2e": {"value": val, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+    import torch
+    dist = init_dist(world, "nccl")
+    r = run_gpu(args, rank, local_rank, world, dist)
+    c = r["c"]
+    pk = peaks()
+    T, ndec, chunk = c["T"], c["decode_steps"], c["chunk"]
+    units = T + ndec
+    value = job_value(units, world, r["t_step"] / args.steps)
+    pre_tok_s = job_value(T, world, r["t_pre"] / args.steps)
+    dec_tok_s = job_value(ndec, world, r["t_dec"] / args.steps)
+
+    # dominant kernel of the step: largest total time share (4 prefill calls + 64 decode calls)
+    share = {("prefill", n): 4 * t for n, t in r["k_pre"].items()}
+    share.update({("decode", n): ndec * t for n, t in r["k_dec"].items()})
+    total = sum(share.values())
+    dom = max(share, key=share.get)
+    t_dom = r["k_pre" if dom[0] == "prefill" else "k_dec"][dom[1]]
+    if dom[1] in ("gemm_gate_up", "gemm_down"):
+        f = gemm_flops(c, chunk, "gate_up" if dom[1] == "gemm_gate_up" else "down")
+        ach = f / t_dom / 1e12
+        roof = {"kernel": dom[1], "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": None,
+                "work_per_launch": f"{f:.4e} FLOP (fp16 operands, fp32 accumulate)",
+                "peak_note": f"dense bf16 sustained, {pk['source']}; fp16 has the same nominal rate"}
+    else:
+        b = decode_bytes(c)
+        ach = b / sum(r["k_dec"].values()) / 1e9
+        roof = {"kernel": "decode step", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / pk["hbm_gbs"], "traffic": None}
+    t_dec_call = sum(r["k_dec"].values())
+    dec_b = decode_bytes(c)
+    roof_dec = {"kernel": "decode call (3 kernels)", "bound": "hbm", "achieved": dec_b / t_dec_call / 1e9,
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": dec_b / t_dec_call / 1e9 / pk["hbm_gbs"],
+                "bytes_per_call": dec_b, "us_per_call_kernels": 1e6 * t_dec_call,
+                "us_per_call_in_step": 1e6 * r["t_dec"] / args.steps / ndec}
+    pre_flops = gemm_flops(c, chunk, "gate_up") + gemm_flops(c, chunk, "down")
+    t_chunk = r["t_pre"] / args.steps / (T // chunk)
+    line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * r["t_step"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp16-mma/fp32-acc (w4 codes, bf16 in/out)",
+            "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD}: T=16384 prefill in 4x4096 chunks + 64 decode steps; H=2048 E=256 "
+                                   f"top-8 I=512 shared expert, Zipf(1.2) routing",
+                       "l2": f"inputs larger than L2: 455 MB of weights per layer; decode cycles {N_REPLICAS} "
+                             f"distinct layers ({N_REPLICAS * 455} MB)",
+                       "parallelism": f"replicas x{world}", "timing": "CUDA graph replay, CUDA events"},
+            "prefill": {"tok_s": pre_tok_s, "ms_per_4096_chunk": 1e3 * t_chunk,
+                        "tensor_tflops": pre_flops / t_chunk / 1e12,
+                        "frac_of_peak": pre_flops / t_chunk / 1e12 / pk["bf16_tflops_sustained"]},
+            "decode": {"tok_s": dec_tok_s, "us_per_token": 1e6 * r["t_dec"] / args.steps / ndec,
+                       "roofline": roof_dec},
+            "roofline": roof,
+            "kernels_us": {"prefill_4096": {k: 1e6 * v for k, v in r["k_pre"].items()},
+                           "decode_T1": {k: 1e6 * v for k, v in r["k_dec"].items()}},
+            "kernel_share": {f"{a}:{b}": v / total for (a, b), v in sorted(share.items(), key=lambda kv: -kv[1])},
+            "gpu_launches": args.steps * (4 * len(PREFILL_KERNELS) + ndec * len(DECODE_KERNELS)),
+            "e2e": {"value": job_value(units, world, r["t_e2e"] / args.steps), "unit": "tok/s",
+                    "h2d_bytes_per_step": units * c["H"] * 2, "d2h_bytes_per_step": units * c["H"] * 2},
+            "clocks": r["clocks"], "gpu": r["gpu"],
+            "context": {"pages_whole_model_M5_Max": {"prefill_tok_s_4K": 5749.9, "decode_tok_s_4K": 186.6,
+                                                    "mlx_lm_prefill": 4737.5, "mlx_lm_decode": 140.9,
+                                                    "note": "whole 40-layer model on an Apple M5 Max; context only"}}}
+    if rank == 0 and not args.no_cpu_baseline:
+        val, dt = time_oracle(r["L0"], r["x_np"], 128, 2, r["xdec_np"])
+        line["cpu_baseline"] = {"value": val, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"128 prefill rows + 2 decode rows of the workload ({dt:.1f} s)"}
+    if rank == 0:
+        print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+// C ABI of libmoe_w4: argument validation, workspace layout and the three
+// entry points (route, decode, prefill).  Everything is enqueued on the
+// caller's stream; nothing here allocates, frees or synchronises.
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mw4 {
+
+static cudaEvent_t* g_trace = nullptr;
+static int g_ntrace = 0;
+
+void trace_mark(cudaStream_t st, int i) {
+    if (g_trace && i < g_ntrace) cudaEventRecordWithFlags(g_trace[i], st, cudaEventRecordExternal);
+}
+
+static size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
+
+WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
+    WsLayout w{};
+    const size_t E = L.E, k = L.top_k, H = L.H, I = L.I;
+    const size_t T = T_max < 1 ? 1 : (size_t)T_max;
+    const size_t Td = T < (size_t)kDecodeMaxT ? T : (size_t)kDecodeMaxT;
+    w.T_max = (int)T;
+    w.nchunk_max = (int)((T + kChunk - 1) / kChunk);
+    w.max_blocks = (int)((T * k + kBN - 1) / kBN + E + (T + kBN - 1) / kBN);
+    w.max_tiles_gu = w.max_blocks * (int)(I / kBM);
+    w.max_tiles_dn = w.max_blocks * (int)(H / kBM);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o += up256(bytes); return at; };
+    w.ctrl = take(sizeof(Ctrl));
+    w.logits = take(T * E * 4);
+    w.x16 = take(T * H * 2);
+    w.topk_idx = take(T * k * 4);
+    w.topk_w = take(T * k * 4);
+    w.gamma = take(T * 4);
+    w.chunk_base = take((size_t)w.nchunk_max * E * 4);
+    w.counts = take((E + 1) * 4);
+    w.offsets = take((E + 2) * 4);
+    w.perm = take(T * k * 4);
+    w.inv = take(T * k * 4);
+    w.tiles_gu = take((size_t)w.max_tiles_gu * sizeof(Tile));
+    w.tiles_dn = take((size_t)w.max_tiles_dn * sizeof(Tile));
+    w.ntiles = take(4 * sizeof(int32_t));
+    w.hh = take((T * k + T) * I * 2);
+    w.ys = take((T * k + T) * H * 2);
+    const size_t nslice = (H + kRouterRowsPerCta - 1) / kRouterRowsPerCta;
+    w.dec_part = take(nslice * Td * E * 4);
+    w.dec_idx = take(Td * k * 4);
+    w.dec_w = take(Td * k * 4);
+    w.dec_gamma = take(Td * 4);
+    w.dec_hh = take(Td * (k + 1) * I * 4);
+    w.total = o;
+    return w;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+static int check_mat(const moe_w4_mat& m) {
+    if (!m.codes || !m.scales || !m.biases) return MOE_W4_ERR_INVALID;
+    if (!aligned16(m.codes) || !aligned16(m.scales) || !aligned16(m.biases)) return MOE_W4_ERR_ALIGN;
+    return MOE_W4_OK;
+}
+
+static int check_layer(const moe_w4_layer* L) {
+    if (!L) return MOE_W4_ERR_INVALID;
+    if (L->E < 1 || L->top_k < 1 || L->top_k > 8 || L->top_k > L->E) return MOE_W4_ERR_INVALID;
+    if (L->H <= 0 || L->I <= 0) return MOE_W4_ERR_INVALID;
+    if (L->H % kBM || L->I % kBM || L->H > 4096 || L->I > 4096 || L->E > 1024) return MOE_W4_ERR_UNSUPPORTED;
+    if (!L->router_w || !L->shared_gate) return MOE_W4_ERR_INVALID;
+    if (!aligned16(L->router_w) || !aligned16(L->shared_gate) || (L->router_bias && !aligned16(L->router_bias)))
+        return MOE_W4_ERR_ALIGN;
+    const moe_w4_mat* ms[6] = {&L->gate, &L->up, &L->down, &L->sh_gate, &L->sh_up, &L->sh_down};
+    for (const moe_w4_mat* m : ms) {
+        const int r = check_mat(*m);
+        if (r) return r;
+    }
+    return MOE_W4_OK;
+}
+
+// Fits calls of T tokens?  The layout is recomputed for the T the workspace
+// was sized for: the largest T_max whose layout fits ws_bytes must be >= T.
+static int check_ws(const moe_w4_layer& L, int T, const void* ws, size_t ws_bytes, WsLayout* out) {
+    if (!ws) return MOE_W4_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MOE_W4_ERR_WORKSPACE;
+    const WsLayout w = ws_layout(L, T);
+    if (w.total > ws_bytes) return MOE_W4_ERR_WORKSPACE;
+    *out = w;
+    return MOE_W4_OK;
+}
+
+template <typename P>
+static P* at(void* ws, size_t off) { return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off); }
+
+static int launch_status(cudaError_t e) { return e == cudaSuccess ? MOE_W4_OK : MOE_W4_ERR_LAUNCH; }
+
+static RouteOut route_ws(void* ws, const WsLayout& w) {
+    RouteOut o{};
+    o.topk_idx = at<int32_t>(ws, w.topk_idx);
+    o.topk_w = at<float>(ws, w.topk_w);
+    o.gamma = at<float>(ws, w.gamma);
+    o.counts = at<int32_t>(ws, w.counts);
+    o.offsets = at<int32_t>(ws, w.offsets);
+    o.perm = at<int32_t>(ws, w.perm);
+    o.inv = at<int32_t>(ws, w.inv);
+    o.chunk_base = at<int32_t>(ws, w.chunk_base);
+    o.logits = at<float>(ws, w.logits);
+    o.x16 = at<uint16_t>(ws, w.x16);
+    o.tiles_gu = at<Tile>(ws, w.tiles_gu);
+    o.tiles_dn = at<Tile>(ws, w.tiles_dn);
+    o.ntiles = at<int32_t>(ws, w.ntiles);
+    o.status = &at<Ctrl>(ws, w.ctrl)->status;
+    return o;
+}
+
+}  // namespace mw4
+
+using namespace mw4;
+
+extern "C" {
+
+size_t moe_w4_workspace_size(const moe_w4_layer* L, int T_max) {
+    if (check_layer(L) != MOE_W4_OK || T_max < 0) return 0;
+    return ws_layout(*L, T_max).total;
+}
+
+int moe_w4_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!workspace || ws_bytes < sizeof(Ctrl)) return MOE_W4_ERR_WORKSPACE;
+    return launch_status(cudaMemsetAsync(workspace, 0, sizeof(Ctrl), stream));
+}
+
+size_t moe_w4_status_offset(void) { return offsetof(Ctrl, status); }
+
+int moe_w4_set_trace_events(cudaEvent_t* events, int n_events) {
+    if (events && n_events < 1) return MOE_W4_ERR_INVALID;
+    g_trace = events;
+    g_ntrace = events ? n_events : 0;
+    return MOE_W4_OK;
+}
+
+int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x, int32_t* topk_idx, float* topk_w,
+                 float* shared_gamma, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                 void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (T < 0) return MOE_W4_ERR_INVALID;
+    if (!topk_idx || !topk_w || !shared_gamma || !counts || !offsets || !perm || !inv)
+        return MOE_W4_ERR_INVALID;
+    if (T > 0 && !x) return MOE_W4_ERR_INVALID;
+    if (T > 0 && !aligned16(x)) return MOE_W4_ERR_ALIGN;
+    WsLayout w;
+    if ((r = check_ws(*L, T, workspace, ws_bytes, &w))) return r;
+    RouteOut o = route_ws(workspace, w);
+    o.topk_idx = topk_idx; o.topk_w = topk_w; o.gamma = shared_gamma;
+    o.counts = counts; o.offsets = offsets; o.perm = perm; o.inv = inv;
+    o.tiles_gu = nullptr; o.tiles_dn = nullptr; o.x16 = nullptr;
+    if (T == 0) {   // empty batch: zero counts and offsets, nothing else to write
+        cudaMemsetAsync(counts, 0, (size_t)L->E * 4, stream);
+        return launch_status(cudaMemsetAsync(offsets, 0, (size_t)(L->E + 1) * 4, stream));
+    }
+    cudaError_t e = launch_router_prefill(*L, T, x, o, stream);
+    if (e == cudaSuccess) e = launch_grouping(*L, T, o, stream);
+    return launch_status(e);
+}
+
+int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out, void* workspace,
+                          size_t ws_bytes, cudaStream_t stream) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (T < 0 || T > kDecodeMaxT) return T < 0 ? MOE_W4_ERR_INVALID : MOE_W4_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_W4_OK;
+    if (!x || !out) return MOE_W4_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(out)) return MOE_W4_ERR_ALIGN;
+    WsLayout w;
+    if ((r = check_ws(*L, T, workspace, ws_bytes, &w))) return r;
+    DecodeWs d{};
+    d.part = at<float>(workspace, w.dec_part);
+    d.idx = at<int32_t>(workspace, w.dec_idx);
+    d.w = at<float>(workspace, w.dec_w);
+    d.gamma = at<float>(workspace, w.dec_gamma);
+    d.hh = at<float>(workspace, w.dec_hh);
+    d.counter = &at<Ctrl>(workspace, w.ctrl)->decode_counter;
+    d.status = &at<Ctrl>(workspace, w.ctrl)->status;
+    trace_mark(stream, 0);
+    return launch_status(launch_decode(*L, T, x, out, d, stream));
+}
+
+int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out,
+                           void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (T < 0) return MOE_W4_ERR_INVALID;
+    if (T == 0) return MOE_W4_OK;
+    if (!x || !out) return MOE_W4_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(out)) return MOE_W4_ERR_ALIGN;
+    WsLayout w;
+    if ((r = check_ws(*L, T, workspace, ws_bytes, &w))) return r;
+    RouteOut o = route_ws(workspace, w);
+    trace_mark(stream, 0);
+    cudaError_t e = launch_router_prefill(*L, T, x, o, stream);
+    if (e == cudaSuccess) e = launch_grouping(*L, T, o, stream);
+    if (e != cudaSuccess) return MOE_W4_ERR_LAUNCH;
+    PrefillWs p{};
+    p.tiles_gu = o.tiles_gu; p.tiles_dn = o.tiles_dn; p.ntiles = o.ntiles;
+    p.offsets = o.offsets; p.perm = o.perm; p.inv = o.inv; p.topk_w = o.topk_w; p.gamma = o.gamma;
+    p.x16 = o.x16;
+    p.hh = at<uint16_t>(workspace, w.hh);
+    p.ys = at<uint16_t>(workspace, w.ys);
+    p.max_tiles_gu = w.max_tiles_gu;
+    p.max_tiles_dn = w.max_tiles_dn;
+    p.status = o.status;
+    return launch_status(launch_grouped_ffn(*L, T, x, out, p, stream));
+}
+
+const char* moe_w4_strerror(int status) {
+    switch (status) {
+        case MOE_W4_OK: return "ok";
+        case MOE_W4_ERR_INVALID: return "invalid argument (NULL pointer, negative T or top_k out of range)";
+        case MOE_W4_ERR_UNSUPPORTED: return "unsupported shape (H and I multiples of 128, H, I <= 4096, E <= 1024, decode T <= 16)";
+        case MOE_W4_ERR_WORKSPACE: return "workspace missing, smaller than moe_w4_workspace_size or not 256-byte aligned";
+        case MOE_W4_ERR_LAUNCH: return "a CUDA kernel launch failed";
+        case MOE_W4_ERR_DEVICE: return "a kernel reported a device-side error in the status word";
+        case MOE_W4_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,283 @@
+// Device helpers shared by the kernels of libmoe_w4: inline PTX for mbarriers
+// (every wait bounded), TMA bulk/tensor copies, cp.async, and the tcgen05
+// tensor-core instructions (TMEM alloc, MMA, commit, loads).  sm_103a only.
+#pragma once
+#include <cfloat>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "moe_w4.h"
+
+#define MW4_DEV __device__ __forceinline__
+
+namespace mw4 {
+
+// ---------------------------------------------------------------------------
+// status word (offset 0 of the workspace)
+// ---------------------------------------------------------------------------
+struct Ctrl {
+    unsigned int status;          // sticky MOE_W4_STATUS_* bits
+    unsigned int decode_counter;  // last-block-done counter of the decode router
+    unsigned int pad[62];
+};
+static_assert(sizeof(Ctrl) == 256, "control header is 256 bytes");
+
+MW4_DEV void raise_status(unsigned int* status, unsigned int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses
+// ---------------------------------------------------------------------------
+MW4_DEV uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+MW4_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+MW4_DEV void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+MW4_DEV void mbar_arrive(uint64_t* bar) {
+    asm volatile("{.reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0];}" :: "r"(smem_u32(bar)) : "memory");
+}
+MW4_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("{.reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;}"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+MW4_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{.reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p;}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Wall-clock bound for every wait: about two seconds of %globaltimer.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+MW4_DEV uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase.  On timeout it raises
+// MOE_W4_STATUS_WAIT_TIMEOUT, sets the CTA's abort flag and returns false.
+// Any thread that sees the abort flag set also gives up at once.
+MW4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// proxies and fences
+// ---------------------------------------------------------------------------
+// Generic-proxy writes to shared memory -> visible to the async proxy (TMA,
+// tensor cores).  Executed by the writing threads before they signal.
+MW4_DEV void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// TMA and bulk copies (async proxy; completion counted in bytes on an mbarrier)
+// ---------------------------------------------------------------------------
+MW4_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+// Contiguous global -> shared copy; size and both addresses multiples of 16.
+MW4_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+MW4_DEV void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// cp.async (16-byte, bypass L1)
+// ---------------------------------------------------------------------------
+MW4_DEV void cp_async_16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(dst)), "l"(src) : "memory");
+}
+MW4_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+MW4_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory and the 5th-generation tensor-core MMA
+// ---------------------------------------------------------------------------
+// Allocation by one full warp; the TMEM base address is written to smem.
+MW4_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+MW4_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+MW4_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+MW4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major operand stored as rows of 128
+// bytes (64 bf16) in the 128-byte swizzle pattern, 8-row atoms 1024 bytes
+// apart.  `addr` must be 1024-byte aligned, plus 32 bytes per K=16 slice.
+MW4_DEV uint64_t umma_desc_sw128(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);          // start address
+    d |= (uint64_t)(16 >> 4) << 16;                  // leading byte offset (unused here)
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: 8 rows * 128 B
+    d |= (uint64_t)1 << 46;                          // descriptor version (tcgen05)
+    d |= (uint64_t)2 << 61;                          // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (format 0, both K-major),
+// fp32 D.
+MW4_DEV uint32_t umma_idesc_f16(int M, int N) {
+    return (1u << 4)                     // D format fp32
+         | (0u << 7)                     // A format fp16
+         | (0u << 10)                    // B format fp16
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+MW4_DEV void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{.reg .pred p; setp.ne.b32 p, %4, 0;"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+MW4_DEV void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns; thread t of the warp gets lane
+// (base lane + t).  Must be followed by tmem_wait_ld before use.
+MW4_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+MW4_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// 4-bit code unpacking to fp16 pairs (exact)
+// ---------------------------------------------------------------------------
+// For a word holding codes n0..n7 (n0 lowest), returns four half2 values
+// (n0,n1), (n2,n3), (n4,n5), (n6,n7), each lane equal to 1024 + n: 0x64 is
+// the high byte of fp16(1024), whose unit in the last place is 1, so a code in
+// the low mantissa bits adds exactly n.
+MW4_DEV void unpack8_f16_plus1024(uint32_t w, uint32_t (&p)[4]) {
+    const uint32_t lo = w & 0x0F0F0F0Fu;          // bytes: n0 n2 n4 n6
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;   // bytes: n1 n3 n5 n7
+    const uint32_t a = __byte_perm(lo, hi, 0x5140); // bytes: n0 n1 n2 n3
+    const uint32_t b = __byte_perm(lo, hi, 0x7362); // bytes: n4 n5 n6 n7
+    const uint32_t c = 0x64646464u;
+    p[0] = __byte_perm(a, c, 0x4140);
+    p[1] = __byte_perm(a, c, 0x4342);
+    p[2] = __byte_perm(b, c, 0x4140);
+    p[3] = __byte_perm(b, c, 0x4342);
+}
+
+MW4_DEV __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+MW4_DEV uint32_t h2_as_u32(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+MW4_DEV uint32_t bf162_as_u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+// w = s*q + b for eight codes, s and b given as half2 pairs; the product and
+// sum are exact inside the fused multiply-add, so each weight is rounded to
+// fp16 once.
+MW4_DEV void dequant8_f16(uint32_t word, __half2 s2, __half2 b2, uint32_t (&o)[4]) {
+    uint32_t p[4];
+    unpack8_f16_plus1024(word, p);
+    const __half2 k1024 = u32_as_h2(0x64006400u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 q = __hsub2(u32_as_h2(p[i]), k1024);   // exact
+        o[i] = h2_as_u32(__hfma2(s2, q, b2));               // single rounding
+    }
+}
+
+MW4_DEV float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+MW4_DEV float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+MW4_DEV float sigmoid_f(float z) { return 1.0f / (1.0f + __expf(-z)); }
+
+// ---------------------------------------------------------------------------
+// warp-level selection (router)
+// ---------------------------------------------------------------------------
+// Best of (v, i) pairs: larger score, then lower expert index.
+MW4_DEV void warp_argmax(float& v, int& i) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+        if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+    }
+}
+
+// Selects the top-k of `sc` (E scores in shared memory, owned by this warp),
+// writes experts by descending score with softmax weights over the selection.
+MW4_DEV void select_topk_warp(float* sc, int E, int k, int32_t* idx_out, float* w_out) {
+    const int lane = threadIdx.x & 31;
+    float top_v[8];
+    int top_i[8];
+    for (int j = 0; j < k; ++j) {
+        float v = -FLT_MAX;
+        int i = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            const float s = sc[e];
+            if (s > v || (s == v && e < i)) { v = s; i = e; }
+        }
+        warp_argmax(v, i);
+        top_v[j] = v;
+        top_i[j] = i;
+        __syncwarp();
+        if (lane == 0) sc[i] = -INFINITY;   // taken
+        __syncwarp();
+    }
+    // softmax over the selection, relative to the largest (the first) score
+    float z = 0.f;
+    for (int j = 0; j < k; ++j) z += expf(top_v[j] - top_v[0]);
+    if (lane < k) {
+        float mine = 0.f;
+        int mi = 0;
+        for (int j = 0; j < k; ++j)
+            if (j == lane) { mine = top_v[j]; mi = top_i[j]; }
+        idx_out[lane] = mi;
+        w_out[lane] = expf(mine - top_v[0]) / z;
+    }
+}
+
+MW4_DEV float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+}  // namespace mw4

@@ -1,0 +1,167 @@
+// Expert grouping on the GPU: per-chunk histograms of the assignments, one
+// prefix scan to expert offsets (plus the block lists the grouped GEMMs walk),
+// and a stable scatter giving each assignment its grouped position.
+// ("Optimizing on-device inference for Apple Silicon", section "Keep expert
+// routing on the GPU": histogram -> prefix scan -> scatter -> block map, all
+// enqueued without a CPU round trip.)
+//
+// Determinism: the position of assignment (t, j) of expert e is
+// offsets[e] + #{t' < t : t' selected e}; chunks are scanned in token order
+// and, inside a chunk, one warp walks the tokens in order, so no result
+// depends on atomic ordering.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mw4 {
+
+// chunk_base[c][e] <- number of assignments to e in tokens [c*kChunk, (c+1)*kChunk)
+__global__ void __launch_bounds__(kChunk) chunk_count_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                                             int32_t* __restrict__ chunk_base,
+                                                             unsigned int* status) {
+    extern __shared__ int hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int t = blockIdx.x * kChunk + threadIdx.x;
+    if (t < T) {
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[(size_t)t * k + j];
+            if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+            else raise_status(status, MOE_W4_STATUS_BAD_INDEX);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_base[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+// Exclusive scan of n <= 2*blockDim values in shared memory `a` (in place);
+// returns the total.  blockDim is a multiple of 32.
+__device__ int block_exclusive_scan(int* a, int n, int* warp_tot) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int i0 = 2 * tid;
+    const int v0 = (i0 < n) ? a[i0] : 0, v1 = (i0 + 1 < n) ? a[i0 + 1] : 0;
+    int s = v0 + v1, incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = (lane < nw) ? warp_tot[lane] : 0, wi = wv;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, wi, off);
+            if (lane >= off) wi += o;
+        }
+        if (lane < nw) warp_tot[lane] = wi - wv;   // exclusive warp prefix
+        if (lane == 31) warp_tot[32] = wi;          // total
+    }
+    __syncthreads();
+    const int excl = warp_tot[warp] + incl - s;
+    if (i0 < n) a[i0] = excl;
+    if (i0 + 1 < n) a[i0 + 1] = excl + v0;
+    const int total = warp_tot[32];
+    __syncthreads();
+    return total;
+}
+
+// One CTA: per-expert totals over chunks (chunk_base becomes the absolute
+// start of each chunk inside its expert group), expert offsets, and the tile
+// lists of the grouped GEMMs (expert-major, then row block, then weight block).
+__global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nchunk, int32_t* __restrict__ chunk_base,
+                                                    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                    Tile* __restrict__ tiles_gu, Tile* __restrict__ tiles_dn,
+                                                    int32_t* __restrict__ ntiles, int MI, int MH) {
+    extern __shared__ int sm[];
+    int* cnt = sm;               // [E+1]
+    int* off = sm + (E + 1);     // [E+1]
+    int* blk = off + (E + 1);    // [E+1]
+    int* wt = blk + (E + 1);     // [33]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < nchunk; ++c) {
+            const int v = chunk_base[(size_t)c * E + e];
+            chunk_base[(size_t)c * E + e] = run;
+            run += v;
+        }
+        cnt[e] = run;
+        off[e] = run;
+        blk[e] = (run + kBN - 1) / kBN;
+    }
+    if (threadIdx.x == 0) {
+        cnt[E] = T;                        // shared expert: every token, in order
+        off[E] = T;
+        blk[E] = (T + kBN - 1) / kBN;
+    }
+    __syncthreads();
+    block_exclusive_scan(off, E + 1, wt);      // off[e] = start of group e; off[E] = T*k
+    const int nblk = block_exclusive_scan(blk, E + 1, wt);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        counts[e] = cnt[e];
+        offsets[e] = off[e];
+        for (int c = 0; c < nchunk; ++c) chunk_base[(size_t)c * E + e] += off[e];
+    }
+    if (threadIdx.x == 0) offsets[E] = off[E];
+    if (tiles_gu == nullptr) return;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        const int c = cnt[e];
+        for (int b = 0; b * kBN < c; ++b) {
+            const int r0 = b * kBN, nr = min(kBN, c - r0);
+            for (int m = 0; m < MI; ++m) tiles_gu[(size_t)(blk[e] + b) * MI + m] = Tile{e, m, r0, nr};
+            for (int m = 0; m < MH; ++m) tiles_dn[(size_t)(blk[e] + b) * MH + m] = Tile{e, m, r0, nr};
+        }
+    }
+    if (threadIdx.x == 0) {
+        ntiles[0] = nblk * MI;
+        ntiles[1] = nblk * MH;
+    }
+}
+
+// One warp per chunk walks its tokens in order and gives every assignment its
+// grouped position; lanes holding the same expert in one step are ranked by
+// lane order, which is token order.
+__global__ void __launch_bounds__(32) assign_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                                    const int32_t* __restrict__ chunk_base,
+                                                    int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    extern __shared__ int running[];
+    const int lane = threadIdx.x;
+    const int c = blockIdx.x;
+    for (int e = lane; e < E; e += 32) running[e] = chunk_base[(size_t)c * E + e];
+    __syncwarp();
+    const int per = 32 / k;                 // tokens per step
+    const int t_begin = c * kChunk, t_end = min(T, t_begin + kChunk);
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int t0 = t_begin; t0 < t_end; t0 += per) {
+        const int t = t0 + lane / k, j = lane % k;
+        const bool valid = (lane < per * k) && (t < t_end);
+        int e = valid ? idx[(size_t)t * k + j] : -1;
+        if (e < 0 || e >= E) e = -1;        // bad indices were reported by the count kernel
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        int pos = 0;
+        if (e >= 0) pos = running[e] + __popc(same & lt_mask);
+        __syncwarp();
+        if (e >= 0 && (same & lt_mask) == 0) running[e] += __popc(same);   // group leader
+        __syncwarp();
+        if (e >= 0) {
+            perm[pos] = t * k + j;
+            inv[(size_t)t * k + j] = pos;
+        }
+    }
+}
+
+cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cudaStream_t st) {
+    const int E = L.E, k = L.top_k;
+    const int nchunk = (T + kChunk - 1) / kChunk;
+    chunk_count_kernel<<<nchunk, kChunk, E * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.status);
+    trace_mark(st, 3);
+    const size_t scan_sm = (3 * (E + 1) + 33) * sizeof(int);
+    scan_kernel<<<1, 1024, scan_sm, st>>>(T, E, k, nchunk, o.chunk_base, o.counts, o.offsets, o.tiles_gu,
+                                          o.tiles_dn, o.ntiles, L.I / kBM, L.H / kBM);
+    trace_mark(st, 4);
+    assign_kernel<<<nchunk, 32, E * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.perm, o.inv);
+    trace_mark(st, 5);
+    return cudaGetLastError();
+}
+
+}  // namespace mw4

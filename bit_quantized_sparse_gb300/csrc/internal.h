@@ -1,0 +1,85 @@
+// Internal declarations of libmoe_w4: workspace layout, kernel parameter
+// blocks and the host-side launchers of each kernel family.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "moe_w4.h"
+
+namespace mw4 {
+
+constexpr int kGroup = 64;        // weights per scale/bias group
+constexpr int kChunk = 128;       // tokens per grouping chunk
+constexpr int kBM = 128;          // weight rows per tensor-core tile
+constexpr int kBN = 128;          // token rows per tensor-core tile
+constexpr int kBK = 64;           // reduction columns per pipeline stage (= one group)
+constexpr int kDecodeMaxT = 16;   // largest decode batch
+constexpr int kRouterRowsPerCta = 256;  // H rows per decode-router CTA
+
+struct Tile { int e, m, r0, nrows; };
+
+// Records trace event `i` on `st` when tracing is enabled (moe_w4_set_trace_events).
+void trace_mark(cudaStream_t st, int i);   // expert (E = shared), weight-row block, first row, rows
+
+// Byte offsets of every region of the workspace (all 256-byte aligned).
+struct WsLayout {
+    size_t ctrl, logits, x16, topk_idx, topk_w, gamma, chunk_base, counts, offsets, perm, inv;
+    size_t tiles_gu, tiles_dn, ntiles, hh, ys;
+    size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh;
+    size_t total;
+    int T_max, nchunk_max, max_blocks, max_tiles_gu, max_tiles_dn;
+};
+WsLayout ws_layout(const moe_w4_layer& L, int T_max);
+
+// ---------------------------------------------------------------------------
+// routing (router.cu, grouping.cu)
+// ---------------------------------------------------------------------------
+struct RouteOut {
+    int32_t* topk_idx; float* topk_w; float* gamma;
+    int32_t* counts;   // [E] routed (tile maps also need the shared group)
+    int32_t* offsets;  // [E+1]
+    int32_t* perm; int32_t* inv;
+    int32_t* chunk_base;
+    float* logits;
+    uint16_t* x16;     // fp16 copy of x written by the top-k kernel (NULL: not needed)
+    Tile* tiles_gu; Tile* tiles_dn; int32_t* ntiles;   // NULL: no tile maps
+    unsigned int* status;
+};
+cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* x, const RouteOut& o,
+                                  cudaStream_t st);
+cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// decode (decode.cu)
+// ---------------------------------------------------------------------------
+struct DecodeWs {
+    float* part;        // [H/256][T][E] partial scores
+    int32_t* idx;       // [T][k]
+    float* w;           // [T][k]
+    float* gamma;       // [T]
+    float* hh;          // [T][k+1][I]
+    unsigned int* counter;
+    unsigned int* status;
+};
+cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
+                          cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// grouped tensor-core GEMMs (grouped_gemm.cu)
+// ---------------------------------------------------------------------------
+struct PrefillWs {
+    const Tile* tiles_gu; const Tile* tiles_dn; const int32_t* ntiles;
+    const int32_t* offsets; const int32_t* perm; const int32_t* inv;
+    const float* topk_w; const float* gamma;
+    const uint16_t* x16;  // fp16 [T][H]
+    uint16_t* hh;   // fp16 [T*k + T][I]
+    uint16_t* ys;   // fp16 [T*k + T][H]
+    int max_tiles_gu, max_tiles_dn;
+    unsigned int* status;
+};
+cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out,
+                               const PrefillWs& p, cudaStream_t st);
+
+}  // namespace mw4

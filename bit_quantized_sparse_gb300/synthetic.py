@@ -164,3 +164,29 @@ def draw_config(name: str, T: Optional[int] = None, stream: int = 0):
     layer = draw_layer(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], c["seed"])
     x = draw_tokens(layer, c["T"] if T is None else T, c["seed"], stream)
     return layer, x
+
+
+def draw_layer_torch(H: int, E: int, I: int, top_k: int, zipf: Optional[float], seed: int, device="cuda"):
+    """Same recipe as draw_layer, drawn directly on a device with a seeded torch
+    generator (fast enough for many layer replicas; the values differ from the
+    numpy draw of the same seed).  Returns a W4Layer whose arrays are torch
+    tensors: codes int32 (bit patterns of the uint32 words), scales/biases
+    int16 (bf16 bit patterns), router float32."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+
+    def mat(lead, rows, cols):
+        codes = torch.randint(-(1 << 31), 1 << 31, lead + (rows, cols // 8), generator=g, device=device,
+                              dtype=torch.int64).to(torch.int32)
+        shape_g = lead + (rows, cols // GROUP)
+        s = (torch.randn(shape_g, generator=g, device=device) * 0.02).abs().to(torch.bfloat16)
+        b = (-8.0 * s.float() + torch.randn(shape_g, generator=g, device=device) * 0.002).to(torch.bfloat16)
+        return W4Matrix(codes, s.view(torch.int16), b.view(torch.int16))
+
+    gate, up, down = mat((E,), I, H), mat((E,), I, H), mat((E,), H, I)
+    sh_gate, sh_up, sh_down = mat((), I, H), mat((), I, H), mat((), H, I)
+    router_w = torch.randn((H, E), generator=g, device=device) * 0.05
+    shared_gate = torch.randn((H,), generator=g, device=device) * 0.05
+    bias = torch.from_numpy(zipf_bias(E, zipf)).to(device) if zipf else None
+    return W4Layer(H, E, I, top_k, router_w, bias, shared_gate, gate, up, down, sh_gate, sh_up, sh_down)

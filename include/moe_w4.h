@@ -1,0 +1,166 @@
+/*
+ * moe_w4.h -- C ABI of the GB300 (sm_103a) W4 group-affine sparse-MoE layer.
+ *
+ * One sparse mixture-of-experts feed-forward layer over 4-bit weights, as
+ * described in "Optimizing on-device inference for Apple Silicon"
+ * (perplexity.ai blog):
+ *   - section "Qwen creates three different workload shapes": the router
+ *     scores E = 256 experts per token and keeps the top k = 8; one shared
+ *     expert processes every token;
+ *   - section "Dequantise weights during matrix multiplication": each weight
+ *     is a 4-bit code q; every group of 64 weights shares one bf16 scale s and
+ *     one bf16 bias b, w = s*q + b; weights are rebuilt only at the point of
+ *     use, products accumulate in fp32 and the output is bf16;
+ *   - section "Keep expert routing on the GPU": histogram of assignments per
+ *     expert, prefix scan to offsets, scatter of rows into expert groups and
+ *     a block map, all without a CPU round trip;
+ *   - sections "Optimise the single-row weight path" and "Reduce intermediate
+ *     state and traffic": batch-1 decode is a fused GEMV (gate and up
+ *     projections with the gated activation; output projection with the
+ *     routing scores and the shared expert's result).
+ * Readings taken where the pages are silent (also used by the oracle):
+ *   routing weights = softmax over the k selected scores; equal scores pick
+ *   the lower expert index; the shared expert is scaled by sigmoid(x . g);
+ *   expert FFN = SwiGLU, y = Wd (silu(Wg x) * (Wu x)); rows of an expert
+ *   group are ordered by ascending token index.
+ *
+ * Conventions for every entry point
+ *   - All pointers except `L` itself are DEVICE pointers (the layer struct and
+ *     its dims live in host memory).  The caller owns every buffer; the library
+ *     never allocates, frees or synchronises.  All work is enqueued on
+ *     `stream` (a cudaStream_t; 0 = legacy default stream) and returns at once.
+ *   - bf16 values are passed as their 16-bit patterns (moe_w4_bf16).
+ *   - Return 0 on success or a negative MOE_W4_ERR_* code; on error nothing
+ *     has been enqueued, except MOE_W4_ERR_LAUNCH (a launch failed part-way;
+ *     outputs are undefined).  No exception or abort crosses the ABI.
+ *   - Results are deterministic: identical inputs give identical bytes, and
+ *     rows are independent (a batch split into chunks gives the same rows).
+ *   - Device-side faults of a bad pointer surface at the caller's next sync.
+ */
+#ifndef MOE_W4_H
+#define MOE_W4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_w4_bf16; /* IEEE bfloat16 bit pattern */
+
+/* One group-affine 4-bit matrix with `rows` output features and `cols` input
+ * features (cols % 64 == 0):
+ *   codes  uint32 [rows][cols/8]   eight 4-bit codes per word; input column
+ *                                  8*w + i is nibble i of word w (nibble 0 =
+ *                                  bits 0..3)
+ *   scales bf16   [rows][cols/64]  scale of input columns 64g .. 64g+63
+ *   biases bf16   [rows][cols/64]
+ * Routed experts stack E such matrices contiguously (leading [E] axis). */
+typedef struct {
+    const uint32_t*    codes;
+    const moe_w4_bf16* scales;
+    const moe_w4_bf16* biases;
+} moe_w4_mat;
+
+/* The layer.  H hidden size, E routed experts, I intermediate size (routed and
+ * shared), top_k experts kept per token.
+ * Supported: H % 128 == 0, I % 128 == 0, 64 <= H <= 16384, 128 <= I <= 4096,
+ * 1 <= E <= 1024, 1 <= top_k <= min(E, 8).  Every pointer 16-byte aligned. */
+typedef struct {
+    int H, E, I, top_k;
+    const float* router_w;     /* [H][E] fp32                                   */
+    const float* router_bias;  /* [E] fp32 added to the scores, or NULL         */
+    const float* shared_gate;  /* [H] fp32; shared expert scale sigmoid(x . g)  */
+    moe_w4_mat gate, up;       /* routed: [E][I][H/8] codes, [E][I][H/64] s, b  */
+    moe_w4_mat down;           /* routed: [E][H][I/8] codes, [E][H][I/64] s, b  */
+    moe_w4_mat sh_gate, sh_up; /* shared: [I][H/8] codes, [I][H/64] s, b        */
+    moe_w4_mat sh_down;        /* shared: [H][I/8] codes, [H][I/64] s, b        */
+} moe_w4_layer;
+
+enum {
+    MOE_W4_OK              = 0,
+    MOE_W4_ERR_INVALID     = -1, /* NULL pointer, T < 0, top_k out of range    */
+    MOE_W4_ERR_UNSUPPORTED = -2, /* shape outside the supported set            */
+    MOE_W4_ERR_WORKSPACE   = -3, /* workspace NULL, too small or misaligned    */
+    MOE_W4_ERR_LAUNCH      = -4, /* a CUDA launch failed (cudaGetLastError)    */
+    MOE_W4_ERR_DEVICE      = -5, /* reported by moe_w4_device_status: a kernel
+                                    gave up a bounded wait or saw a bad index  */
+    MOE_W4_ERR_ALIGN       = -6  /* a pointer is not 16-byte aligned           */
+};
+
+/* Bytes of workspace needed for calls with up to T_max tokens (0 if the layer
+ * is invalid).  The workspace holds routing intermediates, the grouped
+ * activations and a small control header at offset 0. */
+size_t moe_w4_workspace_size(const moe_w4_layer* L, int T_max);
+
+/* Clears the workspace control header (status word and completion counters).
+ * Call once after allocating a workspace, before its first use; every later
+ * call leaves the header as it found it, except the sticky status word. */
+int moe_w4_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Offset in bytes, within the workspace, of the int32 device status word:
+ * 0 = no device-side error; otherwise a bit set of MOE_W4_STATUS_* values.
+ * Kernels only OR into it; clear it with moe_w4_workspace_init. */
+size_t moe_w4_status_offset(void);
+#define MOE_W4_STATUS_WAIT_TIMEOUT 1u  /* a bounded wait gave up              */
+#define MOE_W4_STATUS_BAD_INDEX    2u  /* a routing index was out of range    */
+#define MOE_W4_STATUS_FP16_RANGE   4u  /* a prefill intermediate left the fp16
+                                          range (|v| > 65504): output not finite */
+
+/* Routing of T tokens (sections "Qwen creates three different workload
+ * shapes" and "Keep expert routing on the GPU").
+ *   x         bf16  [T][H]
+ *   topk_idx  int32 [T][top_k]  selected experts, by descending score
+ *   topk_w    fp32  [T][top_k]  softmax over the selected scores
+ *   shared_gamma fp32 [T]       sigmoid(x . shared_gate)
+ *   counts    int32 [E]         assignments per expert
+ *   offsets   int32 [E+1]       exclusive prefix sum of counts
+ *   perm      int32 [T*top_k]   perm[p] = t*top_k + j of the assignment at
+ *                               grouped position p (tokens ascending in a group)
+ *   inv       int32 [T*top_k]   inverse of perm
+ * Scores are fp32 sums of x . W_r (+bias). */
+int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
+                 int32_t* topk_idx, float* topk_w, float* shared_gamma,
+                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                 void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Layer output for a decode batch, 1 <= T <= 16 (section "Optimise the
+ * single-row weight path"): router, fused W4 GEMV for gate/up + SwiGLU, fused
+ * W4 GEMV for down weighted by the routing scores plus the gated shared
+ * expert.  out bf16 [T][H]. */
+int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
+                          moe_w4_bf16* out, void* workspace, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/* Layer output for a prefill batch, T >= 1 (section "Dequantise weights
+ * during matrix multiplication"): routing as moe_w4_route, then grouped W4
+ * GEMMs on the tensor cores (dequantised fp16 tiles in shared memory, fp16
+ * activations, fp32 accumulators in tensor memory) with a SwiGLU epilogue, and
+ * a weighted un-permute that adds the gated shared expert.  out bf16 [T][H].
+ * The activations x, the SwiGLU output and each expert's weighted output must
+ * stay within the fp16 range (|v| <= 65504); otherwise the status word gets
+ * MOE_W4_STATUS_FP16_RANGE. */
+int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
+                           moe_w4_bf16* out, void* workspace, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* Optional tracing for benchmarks: while set, every forward call records
+ * events[0..n_events) (cudaEvent_t, created by the caller) on its stream:
+ * event 0 before its first kernel and event i after its i-th kernel, so
+ * consecutive events bracket one kernel each (prefill: 8 kernels -- router
+ * scores, top-k, chunk counts, scan, assign, grouped gate/up GEMM, grouped
+ * down GEMM, combine; decode: 3 -- router, gate/up GEMV, down GEMV).  Extra
+ * kernels beyond n_events-1 are not traced.  Events are recorded with
+ * cudaEventRecordExternal, so they also fire inside a captured CUDA graph.
+ * Pass NULL to stop tracing.  Process-wide setting, not thread-safe. */
+int moe_w4_set_trace_events(cudaEvent_t* events, int n_events);
+
+/* Static description of a status code. */
+const char* moe_w4_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_W4_H */

@@ -1,0 +1,51 @@
+"""Host-side logic of bench.py: algorithmic work per unit and the multi-rank
+reduction (world size 2 over gloo on the CPU)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as tmp
+
+import bench
+
+
+def test_work_per_unit():
+    c = dict(H=2048, E=256, I=512, top_k=8)
+    # 8 routed + 1 shared expert at 1,769,472 B each, W_r, g, x, out
+    assert bench.expert_bytes(2048, 512) == 1769472
+    assert bench.decode_bytes(c) == 18038784
+    # 2 * 3 * H * I * (k + 1) FLOP per token = 56.6 MFLOP
+    per_tok = (bench.gemm_flops(c, 4096, "gate_up") + bench.gemm_flops(c, 4096, "down")) / 4096
+    assert per_tok == 2 * 3 * 2048 * 512 * 9
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist = bench.init_dist(world, "gloo")
+    t = bench.reduce_max(1.0 + rank, dist, "cpu")
+    v = bench.job_value(100, world, t)
+    q.put((rank, t, v))
+    dist.destroy_process_group()
+
+
+def test_reduce_max_two_ranks():
+    ctx = tmp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+    assert [r[1] for r in res] == [2.0, 2.0]           # every rank sees the slowest rank's time
+    assert [r[2] for r in res] == [100.0, 100.0]       # 2 ranks x 100 units / 2 s

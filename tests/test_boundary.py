@@ -1,0 +1,101 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every
+entry point the header declares, and rejects bad arguments on the host before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_w4.h")
+
+
+@pytest.fixture(scope="module")
+def mw():
+    from bit_quantized_sparse_gb300 import _build
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    from bit_quantized_sparse_gb300 import moe_w4
+    return moe_w4
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_w4_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_w4_route", "moe_w4_forward_decode", "moe_w4_forward_prefill", "moe_w4_workspace_size",
+              "moe_w4_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(mw):
+    lib = ctypes.CDLL(mw.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(declared_functions()) <= set(mw.EXPORTED)
+
+
+def _layer(mw, H=2048, E=256, I=512, k=8, ptr=1 << 20):
+    L = mw.MoeW4Layer()
+    L.H, L.E, L.I, L.top_k = H, E, I, k
+    L.router_w = L.shared_gate = ptr
+    L.router_bias = None
+    for n in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
+        setattr(L, n, mw.MoeW4Mat(ptr, ptr, ptr))
+    return L
+
+
+def test_workspace_size_host_only(mw):
+    L = _layer(mw)
+    w1 = mw.moe_w4_workspace_size(ctypes.byref(L), 1)
+    w4k = mw.moe_w4_workspace_size(ctypes.byref(L), 4096)
+    assert 0 < w1 < w4k
+    # grouped activations alone: (T*k + T) rows of I and H bf16 values
+    assert w4k >= (4096 * 9) * (512 + 2048) * 2
+    assert mw.moe_w4_workspace_size(None, 4) == 0
+    assert mw.moe_w4_status_offset() == 0
+
+
+@pytest.mark.parametrize("field,val,code", [
+    ("top_k", 0, -1), ("top_k", 9, -1), ("E", 0, -1), ("H", 100, -2), ("I", 192, -2), ("H", 8192, -2),
+    ("E", 2048, -2)])
+def test_bad_shapes_rejected(mw, field, val, code):
+    L = _layer(mw)
+    setattr(L, field, val)
+    assert mw.moe_w4_workspace_size(ctypes.byref(L), 8) == 0
+    ws = 1 << 12
+    assert mw.moe_w4_forward_prefill(ctypes.byref(L), 4, ws, ws, ws, 1 << 40, None) == code
+    assert mw.moe_w4_forward_decode(ctypes.byref(L), 1, ws, ws, ws, 1 << 40, None) == code
+
+
+def test_bad_arguments_rejected(mw):
+    L = _layer(mw)
+    p = ctypes.byref(L)
+    a = 1 << 12
+    assert mw.moe_w4_forward_prefill(None, 4, a, a, a, 1 << 40, None) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_forward_prefill(p, -1, a, a, a, 1 << 40, None) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_forward_prefill(p, 4, None, a, a, 1 << 40, None) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_forward_prefill(p, 4, a + 2, a, a, 1 << 40, None) == mw.MOE_W4_ERR_ALIGN
+    assert mw.moe_w4_forward_prefill(p, 4, a, a, None, 1 << 40, None) == mw.MOE_W4_ERR_WORKSPACE
+    assert mw.moe_w4_forward_prefill(p, 4, a, a, a, 1024, None) == mw.MOE_W4_ERR_WORKSPACE
+    assert mw.moe_w4_forward_prefill(p, 4, a, a, a + 16, 1 << 40, None) == mw.MOE_W4_ERR_WORKSPACE
+    assert mw.moe_w4_forward_decode(p, 17, a, a, a, 1 << 40, None) == mw.MOE_W4_ERR_UNSUPPORTED
+    assert mw.moe_w4_forward_decode(p, 0, a, a, a, 1 << 40, None) == mw.MOE_W4_OK      # empty batch: no work
+    assert mw.moe_w4_forward_prefill(p, 0, a, a, a, 1 << 40, None) == mw.MOE_W4_OK
+    z = [a] * 6
+    assert mw.moe_w4_route(p, 4, a, *z, None, a, 1 << 40, None) == mw.MOE_W4_ERR_INVALID   # inv missing
+    assert mw.moe_w4_route(p, 4, a, *z, a, None, 1 << 40, None) == mw.MOE_W4_ERR_WORKSPACE
+    L.gate = mw.MoeW4Mat(a + 4, a, a)
+    assert mw.moe_w4_forward_prefill(p, 4, a, a, a, 1 << 40, None) == mw.MOE_W4_ERR_ALIGN
+    L.gate = mw.MoeW4Mat(None, a, a)
+    assert mw.moe_w4_forward_prefill(p, 4, a, a, a, 1 << 40, None) == mw.MOE_W4_ERR_INVALID
+
+
+def test_strerror(mw):
+    for code in (0, -1, -2, -3, -4, -5, -6, 42):
+        assert isinstance(mw.moe_w4_strerror(code), str) and mw.moe_w4_strerror(code)

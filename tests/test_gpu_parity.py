@@ -1,0 +1,225 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.
+
+Bar: routing and grouping bit-exact (selected experts and their order,
+per-expert counts, offsets, perm, inv); routing weights and the shared gate
+within 1e-5; bf16 layer output within max|err| <= 2e-2 * rms(ref) and relative
+L2 error <= 5e-3 against the float64 oracle.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from bit_quantized_sparse_gb300 import synthetic as S
+from tests import tolerance as TOL
+
+pytestmark = pytest.mark.gpu
+
+W_TOL = 1e-5        # routing weights and shared gate
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+@pytest.fixture(scope="module")
+def mw(torch):
+    from bit_quantized_sparse_gb300 import _build
+    _build.build()
+    from bit_quantized_sparse_gb300 import moe_w4
+    return moe_w4
+
+
+_CACHE = {}
+
+
+def layer_of(mw, name, T=None):
+    key = (name, T)
+    if key not in _CACHE:
+        L, x = S.draw_config(name, T=T)
+        _CACHE[key] = (L, x, mw.DeviceLayer(L))
+    return _CACHE[key]
+
+
+def to_np_bits(t):
+    import torch
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def check_out(got_bits, ref):
+    """bf16 output against the float64 oracle (bar and its reading: tests/tolerance.py)."""
+    got = O.bf16_to_f64(got_bits)
+    assert got.shape == ref.shape
+    assert np.all(np.isfinite(got))
+    m = TOL.metrics(got, ref)
+    assert TOL.within(m), m
+    return m
+
+
+def check_route(dev, L, x_bits):
+    xf = O.bf16_to_f64(x_bits)
+    idx, w, gam, _ = O.route(xf, L.router_w, L.router_bias, L.shared_gate, L.top_k)
+    counts, offsets, perm, inv = O.group(idx, L.E)
+    g = {k: v.cpu().numpy() for k, v in dev.items()}
+    assert np.array_equal(g["topk_idx"], idx)
+    assert np.max(np.abs(g["topk_w"] - w)) <= W_TOL
+    assert np.max(np.abs(g["gamma"] - gam)) <= W_TOL
+    assert np.array_equal(g["counts"], counts)
+    assert np.array_equal(g["offsets"], offsets)
+    assert np.array_equal(g["perm"], perm)
+    assert np.array_equal(g["inv"], inv)
+
+
+# ---------------------------------------------------------------------------
+# routing and grouping: bit-exact at every configured size
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name,T", [("tiny_T4", None), ("decode_T1", None), ("prefill_T512", None),
+                                    ("prefill_T4096", None), ("long_T16384", 4096)])
+def test_route_bit_exact(mw, torch, name, T):
+    L, x, dl = layer_of(mw, name, T)
+    xd = mw.tokens_to_device(x)
+    r = mw.route(dl, xd)
+    torch.cuda.synchronize()
+    check_route(r, L, x)
+    assert dl.status() == 0
+
+
+# ---------------------------------------------------------------------------
+# prefill: grouped tensor-core path
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["tiny_T4", "prefill_T512"])
+def test_prefill_full(mw, torch, name):
+    L, x, dl = layer_of(mw, name)
+    out = mw.forward_prefill(dl, mw.tokens_to_device(x))
+    torch.cuda.synchronize()
+    ref = O.moe_layer(L, x)["out"]
+    check_out(to_np_bits(out), ref)
+    assert dl.status() == 0
+
+
+def _sample(T, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=n, replace=False)]))
+
+
+@pytest.mark.parametrize("name,T", [("prefill_T4096", None), ("long_T16384", 4096)])
+def test_prefill_sampled(mw, torch, name, T):
+    L, x, dl = layer_of(mw, name, T)
+    out = to_np_bits(mw.forward_prefill(dl, mw.tokens_to_device(x)))
+    rows = _sample(x.shape[0], 48, 7)
+    ref = O.moe_layer(L, x, tokens=rows)["out"]
+    check_out(out[rows], ref)
+    assert dl.status() == 0
+
+
+def test_prefill_single_token_and_ragged(mw, torch):
+    L, x, dl = layer_of(mw, "prefill_T512")
+    for T in (1, 3, 129, 333):
+        out = to_np_bits(mw.forward_prefill(dl, mw.tokens_to_device(x[:T])))
+        rows = _sample(T, min(T, 8), T)
+        check_out(out[rows], O.moe_layer(L, x[:T], tokens=rows)["out"])
+
+
+def test_prefill_chunked_equals_unchunked(mw, torch):
+    L, x, dl = layer_of(mw, "prefill_T4096")
+    xd = mw.tokens_to_device(x[:2048])
+    whole = mw.forward_prefill(dl, xd).clone()
+    parts = torch.cat([mw.forward_prefill(dl, xd[i:i + 512]).clone() for i in range(0, 2048, 512)])
+    torch.cuda.synchronize()
+    assert torch.equal(whole.view(torch.int16), parts.view(torch.int16))
+
+
+def test_prefill_deterministic(mw, torch):
+    L, x, dl = layer_of(mw, "prefill_T512")
+    xd = mw.tokens_to_device(x)
+    a = mw.forward_prefill(dl, xd).clone()
+    b = mw.forward_prefill(dl, xd).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_prefill_all_tokens_to_same_experts(mw, torch):
+    """Degenerate routing: a router bias makes every token pick experts 0..7,
+    so eight groups hold all T rows and the rest are empty."""
+    L, _, _ = layer_of(mw, "prefill_T512")
+    import copy
+    L2 = copy.copy(L)
+    bias = np.full(L.E, -50.0, np.float32)
+    bias[:L.top_k] = 5.0 * np.arange(L.top_k, 0, -1)
+    L2.router_bias = bias
+    x = S.draw_tokens(L2, 300, seed=11)
+    dl = mw.DeviceLayer(L2)
+    r = mw.route(dl, mw.tokens_to_device(x))
+    out = to_np_bits(mw.forward_prefill(dl, mw.tokens_to_device(x)))
+    torch.cuda.synchronize()
+    check_route(r, L2, x)
+    assert np.all(r["counts"].cpu().numpy()[:L.top_k] == 300) and r["counts"].cpu().numpy()[L.top_k:].sum() == 0
+    rows = _sample(300, 12, 3)
+    check_out(out[rows], O.moe_layer(L2, x, tokens=rows)["out"])
+
+
+def test_small_layer_top1(mw, torch):
+    """E = 16, top_k = 1: every routing weight is exactly 1."""
+    L = S.draw_layer(256, 16, 128, 1, None, seed=21)
+    x = S.draw_tokens(L, 64, seed=21)
+    dl = mw.DeviceLayer(L)
+    r = mw.route(dl, mw.tokens_to_device(x))
+    torch.cuda.synchronize()
+    check_route(r, L, x)
+    assert np.all(r["topk_w"].cpu().numpy() == 1.0)
+    ref = O.moe_layer(L, x)["out"]
+    check_out(to_np_bits(mw.forward_prefill(dl, mw.tokens_to_device(x))), ref)
+    check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[:16]))), ref[:16])
+
+
+# ---------------------------------------------------------------------------
+# decode: fused GEMV path
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name,T", [("decode_T1", None), ("tiny_T4", None), ("decode_T1", 16)])
+def test_decode(mw, torch, name, T):
+    L, x, dl = layer_of(mw, name, T)
+    out = mw.forward_decode(dl, mw.tokens_to_device(x))
+    torch.cuda.synchronize()
+    check_out(to_np_bits(out), O.moe_layer(L, x)["out"])
+    assert dl.status() == 0
+
+
+def test_decode_matches_prefill(mw, torch):
+    L, x, dl = layer_of(mw, "decode_T1", 16)
+    xd = mw.tokens_to_device(x)
+    a = O.bf16_to_f64(to_np_bits(mw.forward_decode(dl, xd)))
+    b = to_np_bits(mw.forward_prefill(dl, xd))
+    check_out(b, a)
+
+
+def test_decode_repeated_calls(mw, torch):
+    """The decode router's completion counter is reset by the last CTA, so
+    back-to-back calls give identical results."""
+    L, x, dl = layer_of(mw, "decode_T1")
+    xd = mw.tokens_to_device(x)
+    outs = [mw.forward_decode(dl, xd).clone() for _ in range(5)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert dl.status() == 0
+
+
+def test_gpu_workspace_errors(mw, torch):
+    import ctypes
+    L, x, dl = layer_of(mw, "tiny_T4")
+    xd = mw.tokens_to_device(x)
+    out = torch.empty((4, L.H), dtype=torch.bfloat16, device="cuda")
+    need = dl.workspace_size(4)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    assert mw.moe_w4_forward_prefill(ctypes.byref(dl.c), 4, xd.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                                     need - 1, st) == mw.MOE_W4_ERR_WORKSPACE
+    assert mw.moe_w4_forward_prefill(ctypes.byref(dl.c), 4, xd.data_ptr() + 2, out.data_ptr(), ws.data_ptr(),
+                                     need, st) == mw.MOE_W4_ERR_ALIGN
+    assert mw.moe_w4_forward_prefill(ctypes.byref(dl.c), 4, xd.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                                     need, st) == mw.MOE_W4_OK
+    torch.cuda.synchronize()
