@@ -222,6 +222,9 @@ const char* moe_w4_strerror(int status) {
         case MOE_W4_ERR_LAUNCH: return "a CUDA kernel launch failed";
         case MOE_W4_ERR_DEVICE: return "a kernel reported a device-side error in the status word";
         case MOE_W4_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case MOE_W4_ERR_SCRATCH:
+            return "the call needs more scratch than the fixed MOE_W4_NOALLOC_SCRATCH_BYTES array of "
+                   "moe_w4_forward_decode_noalloc";
         default: return "unknown status";
     }
 }

@@ -1,0 +1,100 @@
+// Decode entry point for callers that cannot allocate device memory.
+//
+// Some callers cannot hand the library a workspace: plugins inside an
+// inference engine that owns all device memory and forbids allocation once it
+// is serving, real-time loops that must never block on an allocator, or hosts
+// whose memory plan is fixed before they learn the layer's shape.  For them,
+// moe_w4_forward_decode_noalloc runs the same decode kernels as
+// moe_w4_forward_decode, with the scratch those kernels need (partial router
+// scores, selected experts and weights, the shared gate, the SwiGLU outputs and
+// a small control header) placed in one file-scope device array of
+// MOE_W4_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library keeps
+// until the process exits.  Nothing on this path calls cudaMalloc, cudaFree or
+// any allocating routine.
+//
+// In host code `g_noalloc_scratch` names a host-side stand-in, not the device
+// array, so its device address is looked up once per device with
+// cudaGetSymbolAddress (with that device current) and cached; the first call on
+// a device does this set-up.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mw4 {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_W4_NOALLOC_SCRATCH_BYTES];
+
+static constexpr int kMaxDevices = 64;
+static void* g_scratch_addr[kMaxDevices] = {};
+
+static size_t up256n(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Compact decode-only layout inside the fixed array: control header, partial
+// scores, selected experts, weights, shared gate, SwiGLU outputs.
+struct NoallocLayout { size_t ctrl, part, idx, w, gamma, hh, total; };
+
+static NoallocLayout noalloc_layout(const moe_w4_layer& L, int T) {
+    NoallocLayout n{};
+    const size_t E = L.E, k = L.top_k, H = L.H, I = L.I, Tz = (size_t)T;
+    const size_t nslice = (H + kRouterRowsPerCta - 1) / kRouterRowsPerCta;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o += up256n(bytes); return at; };
+    n.ctrl = take(sizeof(Ctrl));
+    n.part = take(nslice * Tz * E * 4);
+    n.idx = take(Tz * k * 4);
+    n.w = take(Tz * k * 4);
+    n.gamma = take(Tz * 4);
+    n.hh = take(Tz * (k + 1) * I * 4);
+    n.total = o;
+    return n;
+}
+
+// Device address of the scratch array on the current device (set-up on first use).
+static cudaError_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace mw4
+
+using namespace mw4;
+
+extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out,
+                                             cudaStream_t stream) {
+    if (!L || L->E < 1 || L->top_k < 1 || L->top_k > 8 || L->top_k > L->E || L->H <= 0 || L->I <= 0)
+        return MOE_W4_ERR_INVALID;
+    if (L->H % kBM || L->I % kBM || L->H > 4096 || L->I > 4096 || L->E > 1024) return MOE_W4_ERR_UNSUPPORTED;
+    if (T < 0) return MOE_W4_ERR_INVALID;
+    if (T > kDecodeMaxT) return MOE_W4_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_W4_OK;
+    if (!x || !out || !L->router_w || !L->shared_gate) return MOE_W4_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15) return MOE_W4_ERR_ALIGN;
+    const moe_w4_mat* ms[6] = {&L->gate, &L->up, &L->down, &L->sh_gate, &L->sh_up, &L->sh_down};
+    for (const moe_w4_mat* m : ms)
+        if (!m->codes || !m->scales || !m->biases) return MOE_W4_ERR_INVALID;
+    const NoallocLayout n = noalloc_layout(*L, T);
+    if (n.total > (size_t)MOE_W4_NOALLOC_SCRATCH_BYTES) return MOE_W4_ERR_SCRATCH;
+    void* base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return MOE_W4_ERR_LAUNCH;
+    uint8_t* b = static_cast<uint8_t*>(base);
+    // the completion counter must start at zero; clear the header every call
+    if (cudaMemsetAsync(b + n.ctrl, 0, sizeof(Ctrl), stream) != cudaSuccess) return MOE_W4_ERR_LAUNCH;
+    DecodeWs d{};
+    d.part = reinterpret_cast<float*>(b + n.part);
+    d.idx = reinterpret_cast<int32_t*>(b + n.idx);
+    d.w = reinterpret_cast<float*>(b + n.w);
+    d.gamma = reinterpret_cast<float*>(b + n.gamma);
+    d.hh = reinterpret_cast<float*>(b + n.hh);
+    d.counter = &reinterpret_cast<Ctrl*>(b + n.ctrl)->decode_counter;
+    d.status = &reinterpret_cast<Ctrl*>(b + n.ctrl)->status;
+    return launch_decode(*L, T, x, out, d, stream) == cudaSuccess ? MOE_W4_OK : MOE_W4_ERR_LAUNCH;
+}

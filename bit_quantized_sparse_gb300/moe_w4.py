@@ -36,6 +36,7 @@ MOE_W4_ERR_WORKSPACE = -3
 MOE_W4_ERR_LAUNCH = -4
 MOE_W4_ERR_DEVICE = -5
 MOE_W4_ERR_ALIGN = -6
+MOE_W4_ERR_SCRATCH = -7
 DECODE_MAX_T = 16
 
 
@@ -60,6 +61,7 @@ _SIGS = {
     "moe_w4_forward_decode": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_w4_forward_prefill": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_w4_set_trace_events": (c_int, [c_void_p, c_int]),
+    "moe_w4_forward_decode_noalloc": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_w4_strerror": (c_char_p, [c_int]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -75,6 +77,7 @@ moe_w4_route = _lib.moe_w4_route
 moe_w4_forward_decode = _lib.moe_w4_forward_decode
 moe_w4_forward_prefill = _lib.moe_w4_forward_prefill
 moe_w4_set_trace_events = _lib.moe_w4_set_trace_events
+moe_w4_forward_decode_noalloc = _lib.moe_w4_forward_decode_noalloc
 
 
 def moe_w4_strerror(status: int) -> str:

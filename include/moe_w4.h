@@ -87,7 +87,9 @@ enum {
     MOE_W4_ERR_LAUNCH      = -4, /* a CUDA launch failed (cudaGetLastError)    */
     MOE_W4_ERR_DEVICE      = -5, /* reported by moe_w4_device_status: a kernel
                                     gave up a bounded wait or saw a bad index  */
-    MOE_W4_ERR_ALIGN       = -6  /* a pointer is not 16-byte aligned           */
+    MOE_W4_ERR_ALIGN       = -6, /* a pointer is not 16-byte aligned           */
+    MOE_W4_ERR_SCRATCH     = -7  /* moe_w4_forward_decode_noalloc: the call
+                                    needs more than the fixed scratch array    */
 };
 
 /* Bytes of workspace needed for calls with up to T_max tokens (0 if the layer
@@ -145,6 +147,29 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
 int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
                            moe_w4_bf16* out, void* workspace, size_t ws_bytes,
                            cudaStream_t stream);
+
+/* Decode without any allocation, for callers that cannot allocate device
+ * memory where they run the layer (an engine plugin whose host owns all
+ * device memory, a real-time loop that must not wait on an allocator, a
+ * memory plan fixed before the layer's shape is known).  The pages have no
+ * counterpart: it is a deployment convenience of this library.
+ * Same arguments, kernels and results as moe_w4_forward_decode, minus the
+ * workspace: the scratch lives in one fixed device array of
+ * MOE_W4_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library keeps until the process exits.
+ *   - Calls needing more scratch than that (large H, E or I, or many tokens)
+ *     return MOE_W4_ERR_SCRATCH; the shapes used here (H=2048, E=256, I=512,
+ *     top-8) fit for every T <= 16.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call reuses the same array and clears its control header first;
+ *     calls that overlap on the GPU (other streams, other threads) race and
+ *     give wrong results: serialise them.
+ *   - It never calls cudaMalloc, cudaFree or any allocating routine. */
+#define MOE_W4_NOALLOC_SCRATCH_BYTES (2u << 20)
+int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
+                                  moe_w4_bf16* out, cudaStream_t stream);
 
 /* Optional tracing for benchmarks: while set, every forward call records
  * events[0..n_events) (cudaEvent_t, created by the caller) on its stream:
