@@ -42,7 +42,29 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["step", "prefill_chunk", "decode"], default="step",
+                    help="step: the timed benchmark; prefill_chunk / decode: run --calls plain library calls on "
+                         "one layer of the workload and exit (for profilers)")
+    ap.add_argument("--calls", type=int, default=2)
     return ap.parse_args()
+
+
+def run_case(args):
+    """Small untimed runs for profilers: one layer, `calls` library calls."""
+    import torch
+    from bit_quantized_sparse_gb300 import moe_w4 as mw
+    from bit_quantized_sparse_gb300 import synthetic as S
+    c = S.CONFIGS[WORKLOAD]
+    T = c["chunk"] if args.case == "prefill_chunk" else 1
+    L0, x = S.draw_config(WORKLOAD, T=T)
+    dl = mw.DeviceLayer(L0)
+    xd = mw.tokens_to_device(x)
+    for _ in range(args.calls):
+        (mw.forward_prefill if args.case == "prefill_chunk" else mw.forward_decode)(dl, xd)
+    torch.cuda.synchronize()
+    if dl.status() != 0:
+        raise RuntimeError(f"device status {dl.status()}")
+    print(json.dumps({"case": args.case, "calls": args.calls, "T": T, "ok": True}))
 
 
 # ---------------------------------------------------------------------------
@@ -352,6 +374,9 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+    if args.case != "step":
+        run_case(args)
         return
     import torch
     dist = init_dist(world, "nccl")
