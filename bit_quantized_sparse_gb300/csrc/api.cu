@@ -1,6 +1,8 @@
 // C ABI of libmoe_w4: argument validation, workspace layout and the three
 // entry points (route, decode, prefill).  Everything is enqueued on the
 // caller's stream; nothing here allocates, frees or synchronises.
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -10,9 +12,13 @@ namespace mw4 {
 
 static cudaEvent_t* g_trace = nullptr;
 static int g_ntrace = 0;
+static int g_traced_kernels = 0;
 
 void trace_mark(cudaStream_t st, int i) {
     if (g_trace && i < g_ntrace) cudaEventRecordWithFlags(g_trace[i], st, cudaEventRecordExternal);
+}
+void trace_kernels(int n) {
+    if (g_trace) g_traced_kernels = n;
 }
 
 static size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -51,6 +57,8 @@ WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     w.dec_w = take(Td * k * 4);
     w.dec_gamma = take(Td * 4);
     w.dec_hh = take(Td * (k + 1) * I * 4);
+    w.dec_cpart = take((k + 1) * E * 4);
+    w.dec_ybuf = take((k + 1) * H * 4);
     w.total = o;
     return w;
 }
@@ -93,7 +101,13 @@ static int check_ws(const moe_w4_layer& L, int T, const void* ws, size_t ws_byte
 template <typename P>
 static P* at(void* ws, size_t off) { return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off); }
 
-static int launch_status(cudaError_t e) { return e == cudaSuccess ? MOE_W4_OK : MOE_W4_ERR_LAUNCH; }
+// A failed launch returns MOE_W4_ERR_LAUNCH; with MOE_W4_DEBUG set in the
+// environment the CUDA error string also goes to stderr.
+static int launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_W4_OK;
+    if (std::getenv("MOE_W4_DEBUG")) std::fprintf(stderr, "moe_w4: CUDA error %d: %s\n", (int)e, cudaGetErrorString(e));
+    return MOE_W4_ERR_LAUNCH;
+}
 
 static RouteOut route_ws(void* ws, const WsLayout& w) {
     RouteOut o{};
@@ -131,6 +145,8 @@ int moe_w4_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream)
 }
 
 size_t moe_w4_status_offset(void) { return offsetof(Ctrl, status); }
+
+int moe_w4_last_traced_kernels(void) { return g_traced_kernels; }
 
 int moe_w4_set_trace_events(cudaEvent_t* events, int n_events) {
     if (events && n_events < 1) return MOE_W4_ERR_INVALID;
@@ -182,6 +198,9 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, mo
     d.hh = at<float>(workspace, w.dec_hh);
     d.counter = &at<Ctrl>(workspace, w.ctrl)->decode_counter;
     d.status = &at<Ctrl>(workspace, w.ctrl)->status;
+    d.ctrl = at<Ctrl>(workspace, w.ctrl);
+    d.fused_cpart = at<float>(workspace, w.dec_cpart);
+    d.fused_ybuf = at<float>(workspace, w.dec_ybuf);
     trace_mark(stream, 0);
     return launch_status(launch_decode(*L, T, x, out, d, stream));
 }
@@ -210,6 +229,7 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, m
     p.max_tiles_gu = w.max_tiles_gu;
     p.max_tiles_dn = w.max_tiles_dn;
     p.status = o.status;
+    trace_kernels(8);
     return launch_status(launch_grouped_ffn(*L, T, x, out, p, stream));
 }
 

@@ -25,6 +25,20 @@ struct Ctrl {
 };
 static_assert(sizeof(Ctrl) == 256, "control header is 256 bytes");
 
+// Release-ordered increment at GPU scope: after a CTA barrier, one thread's
+// release makes the whole CTA's earlier writes visible to whoever acquires
+// the counter (release ordering is cumulative over what the barrier ordered).
+MW4_DEV unsigned int atomic_add_release_gpu(unsigned int* p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+MW4_DEV unsigned int atomic_add_acq_rel_gpu(unsigned int* p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 MW4_DEV void raise_status(unsigned int* status, unsigned int bits) {
     if (status) atomicOr(status, bits);
 }
@@ -109,6 +123,11 @@ MW4_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+// Pull a contiguous global range into L2 (no completion tracking); size a
+// multiple of 16 bytes.
+MW4_DEV void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
 }
 MW4_DEV void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -241,36 +260,71 @@ MW4_DEV void warp_argmax(float& v, int& i) {
     }
 }
 
-// Selects the top-k of `sc` (E scores in shared memory, owned by this warp),
-// writes experts by descending score with softmax weights over the selection.
-MW4_DEV void select_topk_warp(float* sc, int E, int k, int32_t* idx_out, float* w_out) {
+// Selects the top-k of `sc` (E <= 1024 scores in shared memory, owned by this
+// warp), writes experts by descending score with softmax weights over the
+// selection.  Each lane keeps its (up to 32) scores in registers.
+MW4_DEV void select_topk_warp(const float* sc, int E, int k, int32_t* idx_out, float* w_out) {
     const int lane = threadIdx.x & 31;
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = (lane + 32 * i < E) ? sc[lane + 32 * i] : -INFINITY;
+    // all loops have compile-time bounds so that every array stays in registers
     float top_v[8];
     int top_i[8];
-    for (int j = 0; j < k; ++j) {
-        float v = -FLT_MAX;
-        int i = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-            const float s = sc[e];
-            if (s > v || (s == v && e < i)) { v = s; i = e; }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+        if (j < k) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)   // ascending index within the lane: strict > keeps the lower one
+                if (v[i] > bv) { bv = v[i]; bi = lane + 32 * i; }
         }
-        warp_argmax(v, i);
-        top_v[j] = v;
-        top_i[j] = i;
-        __syncwarp();
-        if (lane == 0) sc[i] = -INFINITY;   // taken
-        __syncwarp();
+        warp_argmax(bv, bi);
+        top_v[j] = bv;
+        top_i[j] = bi;
+        if (j < k) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)   // the owner marks it taken
+                if (lane + 32 * i == bi) v[i] = -INFINITY;
+        }
     }
     // softmax over the selection, relative to the largest (the first) score
-    float z = 0.f;
-    for (int j = 0; j < k; ++j) z += expf(top_v[j] - top_v[0]);
+    float z = 0.f, mine = 0.f;
+    int mi = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j < k) z += expf(top_v[j] - top_v[0]);
+        if (j == lane) { mine = top_v[j]; mi = top_i[j]; }
+    }
     if (lane < k) {
-        float mine = 0.f;
-        int mi = 0;
-        for (int j = 0; j < k; ++j)
-            if (j == lane) { mine = top_v[j]; mi = top_i[j]; }
         idx_out[lane] = mi;
         w_out[lane] = expf(mine - top_v[0]) / z;
+    }
+}
+
+// Block-wide top-k by rank counting: the rank of expert e is the number of
+// experts with a larger score, or an equal score and a lower index; the k
+// experts of rank < k land at their rank.  Two threads per expert (adjacent
+// lanes) split the comparisons.  Needs blockDim >= 2*E.  Writes sel_idx[k],
+// sel_val[k] (scores, descending); callers synchronise before reading.
+MW4_DEV void select_topk_block(const float* sc, int E, int k, int* sel_idx, float* sel_val) {
+    const int t = threadIdx.x, e = t >> 1, half = t & 1;
+    int r = 0;
+    float v = 0.f;
+    if (e < E) {
+        v = sc[e];
+        const int j0 = half ? E / 2 : 0, j1 = half ? E : E / 2;
+#pragma unroll 8
+        for (int j = j0; j < j1; ++j) {
+            const float u = sc[j];
+            r += (u > v) || (u == v && j < e);
+        }
+    }
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    if (e < E && half == 0 && r < k) {
+        sel_idx[r] = e;
+        sel_val[r] = v;
     }
 }
 

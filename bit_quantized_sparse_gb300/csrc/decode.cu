@@ -196,6 +196,14 @@ __global__ void __launch_bounds__(kDN_Warps * 32) decode_down_kernel(moe_w4_laye
 cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                           cudaStream_t st) {
     const int k = L.top_k;
+    if (T == 1 && decode_fused_supported(L)) {   // one launch for the whole layer
+        const cudaError_t e = launch_decode_fused(L, x, out, d, st);
+        trace_kernels(1);
+        trace_mark(st, 1);
+        trace_mark(st, 2);
+        trace_mark(st, 3);
+        return e == cudaSuccess ? cudaGetLastError() : e;
+    }
     static bool attrs_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -206,6 +214,7 @@ cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint1
         cudaFuncSetAttribute(decode_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 9 * 4096 * 4);
         attrs_set[dev] = true;
     }
+    trace_kernels(3);
     dim3 g1((L.E + 31) / 32, (L.H + kRouterRowsPerCta - 1) / kRouterRowsPerCta);
     decode_router_kernel<<<g1, 256, 8 * L.E * sizeof(float), st>>>(x, L.router_w, L.router_bias, L.shared_gate, T,
                                                                    L.H, L.E, k, d);

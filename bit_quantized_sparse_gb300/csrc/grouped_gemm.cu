@@ -43,7 +43,9 @@ struct GemmArgs {
     const float* gamma;        // [T] (down)
     const uint16_t* s0r; const uint16_t* b0r; const uint16_t* s1r; const uint16_t* b1r;   // routed
     const uint16_t* s0s; const uint16_t* b0s; const uint16_t* s1s; const uint16_t* b1s;   // shared
+    const uint32_t* c0r; const uint32_t* c1r; const uint32_t* c0s; const uint32_t* c1s;   // codes (L2 prefetch)
     uint16_t* out;             // hh [.][I] or ys [.][H]
+    const uint16_t* hh_rows;   // down: the B rows (hh), for the L2 prefetch
     int E, k, T, H;            // H: row length of x
     int K;                     // reduction length (H or I)
     int rows_e;                // weight rows per expert (I or H)
@@ -62,7 +64,7 @@ struct Smem {
     static constexpr uint32_t stage_bytes = NMAT * kTileBytes + kTileBytes + NMAT * kCodesBytes;
     static size_t bytes(int stages, int K) {
         const size_t sb = (size_t)NMAT * 2 * kBM * (K / kGroup) * 2;
-        return 1024 + (size_t)stages * stage_bytes + sb + (4 * stages + 2) * 8 + 16;
+        return 1024 + (size_t)stages * stage_bytes + sb + (4 * stages + 2) * 8 + 16 + kBN * 4;
     }
 };
 
@@ -104,6 +106,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     uint64_t* accum_full = bars + 4 * S + 1;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * S + 2);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * S + 2) + 1;
+    float* col_scale = reinterpret_cast<float*>(bars + 4 * S + 2) + 4;   // [kBN], 16-byte aligned
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     if (tid == 0) {
@@ -132,6 +135,13 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
             const CUtensorMap* m1 = shared_e ? &map1s : &map1r;
             prefetch_tensormap(m0);
             if (DUAL) prefetch_tensormap(m1); else prefetch_tensormap(&mapb);
+            // the tile's packed codes are one contiguous range per matrix: pull
+            // them into L2 now so the per-step TMA loads hit L2, not HBM
+            const size_t coff = (size_t)arow * (a.K / 8);
+            const uint32_t cbytes = kBM * (a.K / 2);
+            prefetch_l2((shared_e ? a.c0s : a.c0r) + coff, cbytes);
+            if (DUAL) prefetch_l2((shared_e ? a.c1s : a.c1r) + coff, cbytes);
+            else prefetch_l2(a.hh_rows + (size_t)p0 * a.K, (uint32_t)nrows * a.K * 2);
             const size_t goff = shared_e ? (size_t)tile.m * kBM * G : ((size_t)tile.e * a.rows_e + tile.m * kBM) * G;
             const uint32_t sbb = kBM * G * 2;
             mbar_arrive_expect_tx(sb_full, NMAT * 2 * sbb);
@@ -187,7 +197,11 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 tok[n] = -1;
                 if (row < nrows) tok[n] = shared_e ? tile.r0 + row : a.perm[p0 + row] / a.k;
             }
+            // up to `lag` gathers stay in flight; stage ks is signalled once its
+            // own copies have landed (cp.async.wait_group), after a proxy fence
+            const int lag = S - 1 < 2 ? S - 1 : 2;
             bool ok = true;
+            int signalled = 0;
             for (int ks = 0; ks < nK; ++ks) {
                 const int s = ks % S;
                 const uint32_t ph = (ks / S) & 1;
@@ -201,16 +215,17 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                                     a.x16 + (size_t)tok[n] * a.H + ks * kBK + c * 8);
                 }
                 cp_async_commit();
-                if (ks >= 1) {
-                    cp_async_wait<1>();
+                if (ks - signalled >= lag) {
+                    if (lag == 2) cp_async_wait<2>(); else cp_async_wait<1>();
                     fence_proxy_async_smem();
-                    mbar_arrive(&full_B[(ks - 1) % S]);
+                    mbar_arrive(&full_B[signalled % S]);
+                    ++signalled;
                 }
             }
             cp_async_wait<0>();
             if (ok) {
                 fence_proxy_async_smem();
-                mbar_arrive(&full_B[(nK - 1) % S]);
+                for (; signalled < nK; ++signalled) mbar_arrive(&full_B[signalled % S]);
             }
         }
     } else {
@@ -248,6 +263,11 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
             mbar_arrive(&full_A[s]);
         }
         // ------------------------------------------------------------ epilogue (warps 4-7)
+        if (!DUAL && warp < 8) {   // per-column output scale, fetched while the MMAs run
+            const int i = tid - 128;
+            if (i < nrows) col_scale[i] = shared_e ? a.gamma[tile.r0 + i] : a.topk_w[a.perm[p0 + i]];
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+        }
         if (warp < 8 && ok && mbar_wait(accum_full, 0, abort_flag, a.status)) {
             tc_fence_after();
             const int q = warp - 4;
@@ -266,8 +286,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                     if (DUAL) {
                         v = silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]);
                     } else {
-                        const float sc = shared_e ? a.gamma[tile.r0 + n] : a.topk_w[a.perm[p0 + n]];
-                        v = __uint_as_float(g[j]) * sc;
+                        v = __uint_as_float(g[j]) * col_scale[n];
                     }
                     if (!(fabsf(v) <= 65504.f)) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
                     a.out[(size_t)(p0 + n) * a.out_cols + ocol] = __half_as_ushort(__float2half_rn(v));
@@ -390,6 +409,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     a.tiles = p.tiles_gu;
     a.s0r = L.gate.scales; a.b0r = L.gate.biases; a.s1r = L.up.scales; a.b1r = L.up.biases;
     a.s0s = L.sh_gate.scales; a.b0s = L.sh_gate.biases; a.s1s = L.sh_up.scales; a.b1s = L.sh_up.biases;
+    a.c0r = L.gate.codes; a.c1r = L.up.codes; a.c0s = L.sh_gate.codes; a.c1s = L.sh_up.codes;
     a.out = p.hh; a.K = H; a.rows_e = I; a.out_cols = I; a.stages = s_gu;
     grouped_w4_gemm_kernel<true><<<p.max_tiles_gu, kThreads, sm_gu, st>>>(a, mg, mu, msg, msu, mh);
     trace_mark(st, 6);
@@ -399,6 +419,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     b.tiles = p.tiles_dn; b.ntiles = p.ntiles + 1;
     b.s0r = L.down.scales; b.b0r = L.down.biases; b.s1r = nullptr; b.b1r = nullptr;
     b.s0s = L.sh_down.scales; b.b0s = L.sh_down.biases; b.s1s = nullptr; b.b1s = nullptr;
+    b.c0r = L.down.codes; b.c1r = nullptr; b.c0s = L.sh_down.codes; b.c1s = nullptr; b.hh_rows = p.hh;
     b.out = p.ys; b.K = I; b.rows_e = H; b.out_cols = H; b.stages = s_dn;
     grouped_w4_gemm_kernel<false><<<p.max_tiles_dn, kThreads, sm_dn, st>>>(b, md, md, msd, msd, mh);
     trace_mark(st, 7);

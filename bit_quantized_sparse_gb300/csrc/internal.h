@@ -19,15 +19,18 @@ constexpr int kDecodeMaxT = 16;   // largest decode batch
 constexpr int kRouterRowsPerCta = 256;  // H rows per decode-router CTA
 
 struct Tile { int e, m, r0, nrows; };
+struct Ctrl;   // workspace control header (common.cuh)
 
 // Records trace event `i` on `st` when tracing is enabled (moe_w4_set_trace_events).
-void trace_mark(cudaStream_t st, int i);   // expert (E = shared), weight-row block, first row, rows
+void trace_mark(cudaStream_t st, int i);
+// Records how many kernels the current traced call launches.
+void trace_kernels(int n);   // expert (E = shared), weight-row block, first row, rows
 
 // Byte offsets of every region of the workspace (all 256-byte aligned).
 struct WsLayout {
     size_t ctrl, logits, x16, topk_idx, topk_w, gamma, chunk_base, counts, offsets, perm, inv;
     size_t tiles_gu, tiles_dn, ntiles, hh, ys;
-    size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh;
+    size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh, dec_cpart, dec_ybuf;
     size_t total;
     int T_max, nchunk_max, max_blocks, max_tiles_gu, max_tiles_dn;
 };
@@ -62,7 +65,13 @@ struct DecodeWs {
     float* hh;          // [T][k+1][I]
     unsigned int* counter;
     unsigned int* status;
+    Ctrl* ctrl;         // control header (counters of the fused kernel)
+    float* fused_cpart; // [k+1][E] cluster partial scores (fused T=1 kernel)
+    float* fused_ybuf;  // [k+1][H] weighted expert outputs (fused T=1 kernel)
 };
+bool decode_fused_supported(const moe_w4_layer& L);
+cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
+                                cudaStream_t st);
 cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                           cudaStream_t st);
 

@@ -30,7 +30,7 @@ static size_t up256n(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Compact decode-only layout inside the fixed array: control header, partial
 // scores, selected experts, weights, shared gate, SwiGLU outputs.
-struct NoallocLayout { size_t ctrl, part, idx, w, gamma, hh, total; };
+struct NoallocLayout { size_t ctrl, part, idx, w, gamma, hh, cpart, ybuf, total; };
 
 static NoallocLayout noalloc_layout(const moe_w4_layer& L, int T) {
     NoallocLayout n{};
@@ -44,6 +44,8 @@ static NoallocLayout noalloc_layout(const moe_w4_layer& L, int T) {
     n.w = take(Tz * k * 4);
     n.gamma = take(Tz * 4);
     n.hh = take(Tz * (k + 1) * I * 4);
+    n.cpart = take((k + 1) * E * 4);
+    n.ybuf = take((k + 1) * H * 4);
     n.total = o;
     return n;
 }
@@ -96,5 +98,8 @@ extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const
     d.hh = reinterpret_cast<float*>(b + n.hh);
     d.counter = &reinterpret_cast<Ctrl*>(b + n.ctrl)->decode_counter;
     d.status = &reinterpret_cast<Ctrl*>(b + n.ctrl)->status;
+    d.ctrl = reinterpret_cast<Ctrl*>(b + n.ctrl);
+    d.fused_cpart = reinterpret_cast<float*>(b + n.cpart);
+    d.fused_ybuf = reinterpret_cast<float*>(b + n.ybuf);
     return launch_decode(*L, T, x, out, d, stream) == cudaSuccess ? MOE_W4_OK : MOE_W4_ERR_LAUNCH;
 }

@@ -177,10 +177,15 @@ int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const moe_w4_bf1
  * consecutive events bracket one kernel each (prefill: 8 kernels -- router
  * scores, top-k, chunk counts, scan, assign, grouped gate/up GEMM, grouped
  * down GEMM, combine; decode: 3 -- router, gate/up GEMV, down GEMV).  Extra
- * kernels beyond n_events-1 are not traced.  Events are recorded with
+ * kernels beyond n_events-1 are not traced; a call that launches fewer
+ * kernels records its remaining events right after its last kernel (batch-1
+ * decode of the supported shapes is one fused kernel).  Events are recorded with
  * cudaEventRecordExternal, so they also fire inside a captured CUDA graph.
  * Pass NULL to stop tracing.  Process-wide setting, not thread-safe. */
 int moe_w4_set_trace_events(cudaEvent_t* events, int n_events);
+
+/* Number of kernels the most recent traced call launched (0 before any). */
+int moe_w4_last_traced_kernels(void);
 
 /* Static description of a status code. */
 const char* moe_w4_strerror(int status);

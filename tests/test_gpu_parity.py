@@ -188,6 +188,21 @@ def test_decode(mw, torch, name, T):
     assert dl.status() == 0
 
 
+@pytest.mark.parametrize("name", ["decode_T1", "prefill_T512"])
+def test_decode_single_tokens(mw, torch, name):
+    """Batch-1 decode (the one-kernel path for these shapes) on 12 tokens, one
+    call each, uniform and Zipf-skewed routing, against the oracle."""
+    L, x, dl = layer_of(mw, name)
+    xs = S.draw_tokens(L, 12, seed=99, stream=5)
+    outs = []
+    for t in range(12):
+        outs.append(mw.forward_decode(dl, mw.tokens_to_device(xs[t:t + 1])).clone())
+    torch.cuda.synchronize()
+    got = np.concatenate([to_np_bits(o) for o in outs])
+    check_out(got, O.moe_layer(L, xs)["out"])
+    assert dl.status() == 0
+
+
 def test_decode_matches_prefill(mw, torch):
     L, x, dl = layer_of(mw, "decode_T1", 16)
     xd = mw.tokens_to_device(x)
