@@ -50,21 +50,28 @@ struct GemmArgs {
     int K;                     // reduction length (H or I)
     int rows_e;                // weight rows per expert (I or H)
     int out_cols;              // I or H
-    int stages;
     unsigned int* status;
 };
 
-constexpr int kThreads = 384;
 constexpr uint32_t kCodesBytes = kBM * (kBK / 8) * 4;   // 4 KB of packed codes per matrix per step
-constexpr uint32_t kTileBytes = kBM * kBK * 2;          // 16 KB bf16 tile (A or B)
+constexpr uint32_t kTileBytes = kBM * kBK * 2;          // 16 KB fp16 tile (A or B)
 
+// Persistent-kernel geometry: warp roles and ring depths.
 template <bool DUAL>
-struct Smem {
+struct Geo {
     static constexpr int NMAT = DUAL ? 2 : 1;
-    static constexpr uint32_t stage_bytes = NMAT * kTileBytes + kTileBytes + NMAT * kCodesBytes;
-    static size_t bytes(int stages, int K) {
-        const size_t sb = (size_t)NMAT * 2 * kBM * (K / kGroup) * 2;
-        return 1024 + (size_t)stages * stage_bytes + sb + (4 * stages + 2) * 8 + 16 + kBN * 4;
+    static constexpr int kDeqWarps = 4 * NMAT;            // one thread per (matrix, weight row)
+    static constexpr int kDeqWarp0 = 4;
+    static constexpr int kEpiWarp0 = kDeqWarp0 + kDeqWarps;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+    static constexpr int SR = DUAL ? 4 : 6;               // codes (+B) ring
+    static constexpr int SA = DUAL ? 3 : 4;               // dequantised A ring
+    static constexpr uint32_t R_STAGE = kTileBytes + NMAT * kCodesBytes;   // B first (1024-aligned)
+    static constexpr uint32_t A_STAGE = NMAT * kTileBytes;
+    static constexpr uint32_t ACC_COLS = NMAT * 128;      // TMEM columns per accumulator buffer
+    static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;   // double-buffered
+    static constexpr size_t bytes() {
+        return 1024 + (size_t)SR * R_STAGE + (size_t)SA * A_STAGE + 2 * kBN * 4 + (3 * SR + 2 * SA + 4) * 8 + 16;
     }
 };
 
@@ -72,57 +79,69 @@ MW4_DEV uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
+struct TileInfo { int e, m, r0, nrows, p0, arow; bool sh; };
+
+MW4_DEV TileInfo tile_info(const GemmArgs& a, int t) {
+    const Tile tl = a.tiles[t];
+    TileInfo ti;
+    ti.e = tl.e; ti.m = tl.m; ti.r0 = tl.r0; ti.nrows = tl.nrows;
+    ti.sh = (tl.e == a.E);
+    ti.p0 = (ti.sh ? a.T * a.k : a.offsets[tl.e]) + tl.r0;
+    ti.arow = (ti.sh ? 0 : tl.e * a.rows_e) + tl.m * kBM;
+    return ti;
+}
+
 template <bool DUAL>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Geo<DUAL>::kThreads, 1)
 grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap map0r,
                        const __grid_constant__ CUtensorMap map1r, const __grid_constant__ CUtensorMap map0s,
                        const __grid_constant__ CUtensorMap map1s, const __grid_constant__ CUtensorMap mapb) {
-    constexpr int NMAT = Smem<DUAL>::NMAT;
-    constexpr uint32_t NCOLS = DUAL ? 256 : 128;
-    if ((int)blockIdx.x >= a.ntiles[0]) return;
-    const Tile tile = a.tiles[blockIdx.x];
-    const int S = a.stages, G = a.K / kGroup, nK = a.K / kBK;
-    const bool shared_e = (tile.e == a.E);
-    const int p0 = (shared_e ? a.T * a.k : a.offsets[tile.e]) + tile.r0;
-    const int arow = (shared_e ? 0 : tile.e * a.rows_e) + tile.m * kBM;
-    const int nrows = tile.nrows;
-    const int nmma = ((nrows + 15) / 16) * 16;
+    using GG = Geo<DUAL>;
+    constexpr int NMAT = GG::NMAT, SR = GG::SR, SA = GG::SA;
+    const int ntiles = a.ntiles[0];
+    const int G = a.K / kGroup, nK = a.K / kBK;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align1024(smem_raw);
-    auto A_of = [&](int s, int mat) { return base + (size_t)s * Smem<DUAL>::stage_bytes + mat * kTileBytes; };
-    auto B_of = [&](int s) { return base + (size_t)s * Smem<DUAL>::stage_bytes + NMAT * kTileBytes; };
+    uint8_t* rring = base;
+    uint8_t* aring = base + (size_t)SR * GG::R_STAGE;
+    auto B_of = [&](int s) { return rring + (size_t)s * GG::R_STAGE; };
     auto C_of = [&](int s, int mat) {
-        return reinterpret_cast<uint32_t*>(base + (size_t)s * Smem<DUAL>::stage_bytes + (NMAT + 1) * kTileBytes +
-                                           mat * kCodesBytes);
+        return reinterpret_cast<const uint8_t*>(rring + (size_t)s * GG::R_STAGE + kTileBytes + mat * kCodesBytes);
     };
-    uint16_t* sb = reinterpret_cast<uint16_t*>(base + (size_t)S * Smem<DUAL>::stage_bytes);   // [NMAT][2][128][G]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sb + (size_t)NMAT * 2 * kBM * G);
-    uint64_t* full_codes = bars;
-    uint64_t* full_B = bars + S;
-    uint64_t* full_A = bars + 2 * S;
-    uint64_t* empty = bars + 3 * S;
-    uint64_t* sb_full = bars + 4 * S;
-    uint64_t* accum_full = bars + 4 * S + 1;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4 * S + 2);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4 * S + 2) + 1;
-    float* col_scale = reinterpret_cast<float*>(bars + 4 * S + 2) + 4;   // [kBN], 16-byte aligned
+    auto A_of = [&](int s, int mat) { return aring + (size_t)s * GG::A_STAGE + mat * kTileBytes; };
+    float* col_scale = reinterpret_cast<float*>(aring + (size_t)SA * GG::A_STAGE);   // [2][kBN]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(col_scale + 2 * kBN);
+    uint64_t* r_full = bars;
+    uint64_t* r_fullb = bars + SR;
+    uint64_t* r_empty = bars + 2 * SR;
+    uint64_t* a_full = bars + 3 * SR;
+    uint64_t* a_empty = bars + 3 * SR + SA;
+    uint64_t* acc_full = bars + 3 * SR + 2 * SA;
+    uint64_t* acc_empty = acc_full + 2;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_empty + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2) + 1;
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full_codes[s], 1);
-            mbar_init(&full_B[s], 64);
-            mbar_init(&full_A[s], 256);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < SR; ++s) {
+            mbar_init(&r_full[s], 1);
+            mbar_init(&r_fullb[s], 64);
+            mbar_init(&r_empty[s], 1);
         }
-        mbar_init(sb_full, 1);
-        mbar_init(accum_full, 1);
+        for (int s = 0; s < SA; ++s) {
+            mbar_init(&a_full[s], 128 * NMAT);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 128);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, NCOLS);
+    if (warp == 1) tmem_alloc(tmem_slot, GG::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -131,149 +150,184 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const CUtensorMap* m0 = shared_e ? &map0s : &map0r;
-            const CUtensorMap* m1 = shared_e ? &map1s : &map1r;
-            prefetch_tensormap(m0);
-            if (DUAL) prefetch_tensormap(m1); else prefetch_tensormap(&mapb);
-            // the tile's packed codes are one contiguous range per matrix: pull
-            // them into L2 now so the per-step TMA loads hit L2, not HBM
-            const size_t coff = (size_t)arow * (a.K / 8);
-            const uint32_t cbytes = kBM * (a.K / 2);
-            prefetch_l2((shared_e ? a.c0s : a.c0r) + coff, cbytes);
-            if (DUAL) prefetch_l2((shared_e ? a.c1s : a.c1r) + coff, cbytes);
-            else prefetch_l2(a.hh_rows + (size_t)p0 * a.K, (uint32_t)nrows * a.K * 2);
-            const size_t goff = shared_e ? (size_t)tile.m * kBM * G : ((size_t)tile.e * a.rows_e + tile.m * kBM) * G;
-            const uint32_t sbb = kBM * G * 2;
-            mbar_arrive_expect_tx(sb_full, NMAT * 2 * sbb);
-            bulk_load(sb, (shared_e ? a.s0s : a.s0r) + goff, sbb, sb_full);
-            bulk_load(sb + kBM * G, (shared_e ? a.b0s : a.b0r) + goff, sbb, sb_full);
-            if (DUAL) {
-                bulk_load(sb + 2 * kBM * G, (shared_e ? a.s1s : a.s1r) + goff, sbb, sb_full);
-                bulk_load(sb + 3 * kBM * G, (shared_e ? a.b1s : a.b1r) + goff, sbb, sb_full);
-            }
-            for (int ks = 0; ks < nK; ++ks) {
-                const int s = ks % S;
-                const uint32_t ph = (ks / S) & 1;
-                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, a.status)) break;
-                mbar_arrive_expect_tx(&full_codes[s], NMAT * kCodesBytes + (DUAL ? 0 : kTileBytes));
-                tma_load_2d(C_of(s, 0), m0, ks * (kBK / 8), arow, &full_codes[s]);
-                if (DUAL) tma_load_2d(C_of(s, 1), m1, ks * (kBK / 8), arow, &full_codes[s]);
-                else tma_load_2d(B_of(s), &mapb, ks * kBK, p0, &full_codes[s]);
+            prefetch_tensormap(&map0r);
+            prefetch_tensormap(&map0s);
+            if (DUAL) { prefetch_tensormap(&map1r); prefetch_tensormap(&map1s); } else prefetch_tensormap(&mapb);
+            int gk = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileInfo ti = tile_info(a, t);
+                const CUtensorMap* m0 = ti.sh ? &map0s : &map0r;
+                const CUtensorMap* m1 = ti.sh ? &map1s : &map1r;
+                // the tile's packed codes are one contiguous range per matrix
+                prefetch_l2((ti.sh ? a.c0s : a.c0r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
+                if (DUAL) prefetch_l2((ti.sh ? a.c1s : a.c1r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
+                else prefetch_l2(a.hh_rows + (size_t)ti.p0 * a.K, (uint32_t)ti.nrows * a.K * 2);
+                for (int ks = 0; ks < nK; ++ks, ++gk) {
+                    const int s = gk % SR;
+                    if (!mbar_wait(&r_empty[s], ((gk / SR) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&r_full[s], NMAT * kCodesBytes + (DUAL ? 0 : kTileBytes));
+                    tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * (kBK / 8), ti.arow, &r_full[s]);
+                    if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * (kBK / 8), ti.arow, &r_full[s]);
+                    else tma_load_2d(B_of(s), &mapb, ks * kBK, ti.p0, &r_full[s]);
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = umma_idesc_f16(kBM, nmma);
+            int gk = 0, it = 0;
             bool ok = true;
-            for (int ks = 0; ks < nK && ok; ++ks) {
-                const int s = ks % S;
-                const uint32_t ph = (ks / S) & 1;
-                ok = mbar_wait(&full_A[s], ph, abort_flag, a.status) &&
-                     mbar_wait(DUAL ? &full_B[s] : &full_codes[s], ph, abort_flag, a.status);
-                if (!ok) break;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+                const TileInfo ti = tile_info(a, t);
+                const int nmma = ((ti.nrows + 15) / 16) * 16;
+                const uint32_t idesc = umma_idesc_f16(kBM, nmma);
+                const int b = it & 1;
+                if (!mbar_wait(&acc_empty[b], ((it >> 1) & 1) ^ 1, abort_flag, a.status)) break;
                 tc_fence_after();
+                const uint32_t dacc = taddr + b * GG::ACC_COLS;
+                for (int ks = 0; ks < nK; ++ks, ++gk) {
+                    const int sr = gk % SR, sa = gk % SA;
+                    ok = mbar_wait(&a_full[sa], (gk / SA) & 1, abort_flag, a.status) &&
+                         mbar_wait(DUAL ? &r_fullb[sr] : &r_full[sr], (gk / SR) & 1, abort_flag, a.status);
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
-                    const uint64_t bdesc = umma_desc_sw128(smem_u32(B_of(s)) + kk * 32);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t bdesc = umma_desc_sw128(smem_u32(B_of(sr)) + kk * 32);
 #pragma unroll
-                    for (int mat = 0; mat < NMAT; ++mat) {
-                        const uint64_t adesc = umma_desc_sw128(smem_u32(A_of(s, mat)) + kk * 32);
-                        umma_f16(taddr + mat * 128, adesc, bdesc, idesc, (ks | kk) != 0);
+                        for (int mat = 0; mat < NMAT; ++mat) {
+                            const uint64_t adesc = umma_desc_sw128(smem_u32(A_of(sa, mat)) + kk * 32);
+                            umma_f16(dacc + mat * 128, adesc, bdesc, idesc, (ks | kk) != 0);
+                        }
                     }
+                    umma_commit(&r_empty[sr]);
+                    umma_commit(&a_empty[sa]);
                 }
-                umma_commit(&empty[s]);
+                if (ok) umma_commit(&acc_full[b]);
             }
-            if (ok) umma_commit(accum_full);
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------ token-row gather (gate/up)
         if (DUAL) {
             const int tb = tid - 64, c = tb & 7;
-            int tok[16];
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                const int row = (tb >> 3) + 8 * n;
-                tok[n] = -1;
-                if (row < nrows) tok[n] = shared_e ? tile.r0 + row : a.perm[p0 + row] / a.k;
-            }
-            // up to `lag` gathers stay in flight; stage ks is signalled once its
-            // own copies have landed (cp.async.wait_group), after a proxy fence
-            const int lag = S - 1 < 2 ? S - 1 : 2;
+            const int lag = 2;   // <= SR - 1
+            int gk = 0, signalled = 0;
             bool ok = true;
-            int signalled = 0;
-            for (int ks = 0; ks < nK; ++ks) {
-                const int s = ks % S;
-                const uint32_t ph = (ks / S) & 1;
-                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, a.status)) { ok = false; break; }
-                uint8_t* dst = B_of(s);
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const TileInfo ti = tile_info(a, t);
+                int tok[16];
 #pragma unroll
                 for (int n = 0; n < 16; ++n) {
                     const int row = (tb >> 3) + 8 * n;
-                    if (tok[n] >= 0)
-                        cp_async_16(dst + row * 128 + ((c ^ (row & 7)) << 4),
-                                    a.x16 + (size_t)tok[n] * a.H + ks * kBK + c * 8);
+                    tok[n] = -1;
+                    if (row < ti.nrows) tok[n] = ti.sh ? ti.r0 + row : a.perm[ti.p0 + row] / a.k;
                 }
-                cp_async_commit();
-                if (ks - signalled >= lag) {
-                    if (lag == 2) cp_async_wait<2>(); else cp_async_wait<1>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(&full_B[signalled % S]);
-                    ++signalled;
+                for (int ks = 0; ks < nK; ++ks, ++gk) {
+                    const int s = gk % SR;
+                    if (!mbar_wait(&r_empty[s], ((gk / SR) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    uint8_t* dst = B_of(s);
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        const int row = (tb >> 3) + 8 * n;
+                        if (tok[n] >= 0)
+                            cp_async_16(dst + row * 128 + ((c ^ (row & 7)) << 4),
+                                        a.x16 + (size_t)tok[n] * a.H + ks * kBK + c * 8);
+                    }
+                    cp_async_commit();
+                    if (gk - signalled >= lag) {   // this stage's copies landed: proxy fence, signal
+                        cp_async_wait<2>();
+                        fence_proxy_async_smem();
+                        mbar_arrive(&r_fullb[signalled % SR]);
+                        ++signalled;
+                    }
                 }
             }
             cp_async_wait<0>();
             if (ok) {
                 fence_proxy_async_smem();
-                for (; signalled < nK; ++signalled) mbar_arrive(&full_B[signalled % S]);
+                for (; signalled < gk; ++signalled) mbar_arrive(&r_fullb[signalled % SR]);
+            }
+        }
+    } else if (warp < GG::kEpiWarp0) {
+        // ------------------------------------------------------------ dequantisation: one weight row per thread
+        const int td = tid - 32 * GG::kDeqWarp0, mat = td / 128, row = td % 128;
+        const int sw = (row >> 2) & 1;   // 32-byte swizzle phase of this row's codes
+        const bool chunked = (G % 8) == 0;
+        int gk = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const TileInfo ti = tile_info(a, t);
+            const uint16_t* sp = (mat == 0 ? (ti.sh ? a.s0s : a.s0r) : (ti.sh ? a.s1s : a.s1r)) + (size_t)(ti.arow + row) * G;
+            const uint16_t* bp = (mat == 0 ? (ti.sh ? a.b0s : a.b0r) : (ti.sh ? a.b1s : a.b1r)) + (size_t)(ti.arow + row) * G;
+            uint4 sq = make_uint4(0, 0, 0, 0), bq = sq, sqn = sq, bqn = sq;
+            if (chunked) {
+                sq = __ldg(reinterpret_cast<const uint4*>(sp));
+                bq = __ldg(reinterpret_cast<const uint4*>(bp));
+            }
+            for (int k8 = 0; k8 < nK; k8 += 8) {
+                if (chunked && k8 + 8 < nK) {   // next eight steps' scales and biases
+                    sqn = __ldg(reinterpret_cast<const uint4*>(sp + k8 + 8));
+                    bqn = __ldg(reinterpret_cast<const uint4*>(bp + k8 + 8));
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int ks = k8 + j;
+                    if (ks >= nK) break;
+                    uint32_t s16, b16;
+                    if (chunked) {
+                        const uint32_t sw2 = (j < 2 ? sq.x : j < 4 ? sq.y : j < 6 ? sq.z : sq.w);
+                        const uint32_t bw2 = (j < 2 ? bq.x : j < 4 ? bq.y : j < 6 ? bq.z : bq.w);
+                        s16 = (j & 1) ? (sw2 >> 16) : (sw2 & 0xFFFFu);
+                        b16 = (j & 1) ? (bw2 >> 16) : (bw2 & 0xFFFFu);
+                    } else {
+                        s16 = sp[ks];
+                        b16 = bp[ks];
+                    }
+                    const int sr = gk % SR, sa = gk % SA;
+                    ok = mbar_wait(&r_full[sr], (gk / SR) & 1, abort_flag, a.status) &&
+                         mbar_wait(&a_empty[sa], ((gk / SA) & 1) ^ 1, abort_flag, a.status);
+                    if (!ok) break;
+                    const uint8_t* cr = C_of(sr, mat) + row * 32;
+                    const uint4 w0 = *reinterpret_cast<const uint4*>(cr + ((0 ^ sw) << 4));
+                    const uint4 w1 = *reinterpret_cast<const uint4*>(cr + ((1 ^ sw) << 4));
+                    const __half s_h = __float2half_rn(bf16_bits_to_float((uint16_t)s16));
+                    const __half b_h = __float2half_rn(bf16_bits_to_float((uint16_t)b16));
+                    const __half2 s2 = __halves2half2(s_h, s_h), b2 = __halves2half2(b_h, b_h);
+                    uint8_t* At = A_of(sa, mat) + row * 128;
+                    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                    for (int wi = 0; wi < 8; ++wi) {
+                        uint32_t o[4];
+                        dequant8_f16(words[wi], s2, b2, o);
+                        *reinterpret_cast<uint4*>(At + ((wi ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(&a_full[sa]);
+                    ++gk;
+                }
+                if (!ok) break;
+                sq = sqn;
+                bq = bqn;
             }
         }
     } else {
-        // ------------------------------------------------------------ dequantisation
-        const int td = tid - 128, word = td & 7, rbase = td >> 3;
-        bool ok = mbar_wait(sb_full, 0, abort_flag, a.status);
-        // scales and biases arrive as bf16; convert the tile to fp16 once (exact
-        // for normal values), shared by the 256 dequantising threads
-        uint16_t* sb16 = sb;
-        for (int i = td; i < NMAT * 2 * kBM * G && ok; i += 256)
-            sb16[i] = __half_as_ushort(__float2half_rn(bf16_bits_to_float(sb[i])));
-        asm volatile("bar.sync 1, 256;" ::: "memory");
-        for (int ks = 0; ks < nK && ok; ++ks) {
-            const int s = ks % S;
-            const uint32_t ph = (ks / S) & 1;
-            if (!mbar_wait(&full_codes[s], ph, abort_flag, a.status)) { ok = false; break; }
-#pragma unroll
-            for (int mat = 0; mat < NMAT; ++mat) {
-                const uint32_t* cw = C_of(s, mat);
-                uint8_t* At = A_of(s, mat);
-                const uint16_t* ss = sb16 + (size_t)(2 * mat) * kBM * G;
-                const uint16_t* bb = ss + (size_t)kBM * G;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int row = rbase + 32 * j;
-                    const uint32_t w = cw[row * 8 + word];
-                    const uint32_t s16 = ss[row * G + ks], b16 = bb[row * G + ks];
-                    uint32_t o[4];
-                    dequant8_f16(w, u32_as_h2(s16 | (s16 << 16)), u32_as_h2(b16 | (b16 << 16)), o);
-                    *reinterpret_cast<uint4*>(At + row * 128 + ((word ^ (row & 7)) << 4)) =
-                        make_uint4(o[0], o[1], o[2], o[3]);
-                }
+        // ------------------------------------------------------------ epilogue: TMEM -> registers -> global
+        const int q = warp - GG::kEpiWarp0, et = tid - 32 * GG::kEpiWarp0;
+        int it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+            const TileInfo ti = tile_info(a, t);
+            const int b = it & 1;
+            if (!DUAL) {   // per-column output scale of this tile, fetched while the MMAs run
+                if (et < ti.nrows)
+                    col_scale[b * kBN + et] = ti.sh ? a.gamma[ti.r0 + et] : a.topk_w[a.perm[ti.p0 + et]];
+                asm volatile("bar.sync 2, 128;" ::: "memory");
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&full_A[s]);
-        }
-        // ------------------------------------------------------------ epilogue (warps 4-7)
-        if (!DUAL && warp < 8) {   // per-column output scale, fetched while the MMAs run
-            const int i = tid - 128;
-            if (i < nrows) col_scale[i] = shared_e ? a.gamma[tile.r0 + i] : a.topk_w[a.perm[p0 + i]];
-            asm volatile("bar.sync 2, 128;" ::: "memory");
-        }
-        if (warp < 8 && ok && mbar_wait(accum_full, 0, abort_flag, a.status)) {
+            if (!mbar_wait(&acc_full[b], (it >> 1) & 1, abort_flag, a.status)) break;
             tc_fence_after();
-            const int q = warp - 4;
-            const uint32_t lane_addr = taddr + ((uint32_t)(q * 32) << 16);
-            const int ocol = tile.m * kBM + q * 32 + lane;
-            for (int c0 = 0; c0 < nrows; c0 += 16) {
+            const uint32_t lane_addr = taddr + b * GG::ACC_COLS + ((uint32_t)(q * 32) << 16);
+            const int ocol = ti.m * kBM + q * 32 + lane;
+            for (int c0 = 0; c0 < ti.nrows; c0 += 16) {
                 uint32_t g[16], u[16];
                 tmem_ld16(lane_addr + c0, g);
                 if (DUAL) tmem_ld16(lane_addr + 128 + c0, u);
@@ -281,22 +335,21 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int n = c0 + j;
-                    if (n >= nrows) break;
+                    if (n >= ti.nrows) break;
                     float v;
-                    if (DUAL) {
-                        v = silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]);
-                    } else {
-                        v = __uint_as_float(g[j]) * col_scale[n];
-                    }
+                    if (DUAL) v = silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]);
+                    else v = __uint_as_float(g[j]) * col_scale[b * kBN + n];
                     if (!(fabsf(v) <= 65504.f)) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
-                    a.out[(size_t)(p0 + n) * a.out_cols + ocol] = __half_as_ushort(__float2half_rn(v));
+                    a.out[(size_t)(ti.p0 + n) * a.out_cols + ocol] = __half_as_ushort(__float2half_rn(v));
                 }
             }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[b]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(taddr, NCOLS);
+    if (warp == 1) tmem_dealloc(taddr, GG::TMEM_COLS);
 }
 
 // out[t] = bf16( sum_j ys[inv[t*k + j]] + ys[T*k + t] ) with ys in fp16 and
@@ -359,34 +412,31 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static int stages_for(bool dual, int K) {
-    const int budget = 227 * 1024;
-    for (int s = 4; s >= 2; --s) {
-        const size_t b = dual ? Smem<true>::bytes(s, K) : Smem<false>::bytes(s, K);
-        if (b <= (size_t)budget) return s;
-    }
-    return 0;
-}
-
 cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const PrefillWs& p,
                                cudaStream_t st) {
     const int H = L.H, I = L.I, E = L.E, k = L.top_k;
     const uint64_t rows_all = (uint64_t)T * k + T;
     CUtensorMap mg, mu, msg, msu, md, msd, mh;
     const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
-    bool ok = make_map(&mg, U32, 4, L.gate.codes, (uint64_t)E * I, H / 8, kBM, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&mu, U32, 4, L.up.codes, (uint64_t)E * I, H / 8, kBM, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&msg, U32, 4, L.sh_gate.codes, I, H / 8, kBM, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&msu, U32, 4, L.sh_up.codes, I, H / 8, kBM, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&md, U32, 4, L.down.codes, (uint64_t)E * H, I / 8, kBM, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-              make_map(&msd, U32, 4, L.sh_down.codes, H, I / 8, kBM, kBK / 8, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+    const auto SW32 = CU_TENSOR_MAP_SWIZZLE_32B;   // 32-byte code rows: bank-conflict-free per-row reads
+    bool ok = make_map(&mg, U32, 4, L.gate.codes, (uint64_t)E * I, H / 8, kBM, kBK / 8, SW32) &&
+              make_map(&mu, U32, 4, L.up.codes, (uint64_t)E * I, H / 8, kBM, kBK / 8, SW32) &&
+              make_map(&msg, U32, 4, L.sh_gate.codes, I, H / 8, kBM, kBK / 8, SW32) &&
+              make_map(&msu, U32, 4, L.sh_up.codes, I, H / 8, kBM, kBK / 8, SW32) &&
+              make_map(&md, U32, 4, L.down.codes, (uint64_t)E * H, I / 8, kBM, kBK / 8, SW32) &&
+              make_map(&msd, U32, 4, L.sh_down.codes, H, I / 8, kBM, kBK / 8, SW32) &&
               make_map(&mh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hh, rows_all, I, kBN, kBK,
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
 
-    const int s_gu = stages_for(true, H), s_dn = stages_for(false, I);
-    if (s_gu == 0 || s_dn == 0) return cudaErrorInvalidConfiguration;
-    const size_t sm_gu = Smem<true>::bytes(s_gu, H), sm_dn = Smem<false>::bytes(s_dn, I);
+    const size_t sm_gu = Geo<true>::bytes(), sm_dn = Geo<false>::bytes();
+    int nsm = 0;
+    {
+        int dv = 0;
+        cudaGetDevice(&dv);
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dv);
+        if (nsm <= 0) nsm = 148;
+    }
     static int set_gu[64] = {}, set_dn[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -410,8 +460,10 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     a.s0r = L.gate.scales; a.b0r = L.gate.biases; a.s1r = L.up.scales; a.b1r = L.up.biases;
     a.s0s = L.sh_gate.scales; a.b0s = L.sh_gate.biases; a.s1s = L.sh_up.scales; a.b1s = L.sh_up.biases;
     a.c0r = L.gate.codes; a.c1r = L.up.codes; a.c0s = L.sh_gate.codes; a.c1s = L.sh_up.codes;
-    a.out = p.hh; a.K = H; a.rows_e = I; a.out_cols = I; a.stages = s_gu;
-    grouped_w4_gemm_kernel<true><<<p.max_tiles_gu, kThreads, sm_gu, st>>>(a, mg, mu, msg, msu, mh);
+    a.out = p.hh; a.K = H; a.rows_e = I; a.out_cols = I;
+    // persistent: one CTA per SM (never more CTAs than the largest tile count)
+    const int grid_gu = p.max_tiles_gu < nsm ? p.max_tiles_gu : nsm;
+    grouped_w4_gemm_kernel<true><<<grid_gu, Geo<true>::kThreads, sm_gu, st>>>(a, mg, mu, msg, msu, mh);
     trace_mark(st, 6);
 
     // down: A = Wd rows (H per expert), K = I, B = hh rows, out = ys [.][H]
@@ -420,8 +472,9 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     b.s0r = L.down.scales; b.b0r = L.down.biases; b.s1r = nullptr; b.b1r = nullptr;
     b.s0s = L.sh_down.scales; b.b0s = L.sh_down.biases; b.s1s = nullptr; b.b1s = nullptr;
     b.c0r = L.down.codes; b.c1r = nullptr; b.c0s = L.sh_down.codes; b.c1s = nullptr; b.hh_rows = p.hh;
-    b.out = p.ys; b.K = I; b.rows_e = H; b.out_cols = H; b.stages = s_dn;
-    grouped_w4_gemm_kernel<false><<<p.max_tiles_dn, kThreads, sm_dn, st>>>(b, md, md, msd, msd, mh);
+    b.out = p.ys; b.K = I; b.rows_e = H; b.out_cols = H;
+    const int grid_dn = p.max_tiles_dn < nsm ? p.max_tiles_dn : nsm;
+    grouped_w4_gemm_kernel<false><<<grid_dn, Geo<false>::kThreads, sm_dn, st>>>(b, md, md, msd, msd, mh);
     trace_mark(st, 7);
 
     const size_t nthr = (size_t)T * (H / 8);
