@@ -37,6 +37,7 @@ WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     auto take = [&](size_t bytes) { const size_t at = o; o += up256(bytes); return at; };
     w.ctrl = take(sizeof(Ctrl));
     w.logits = take(T * E * 4);
+    w.router_a = take((E + kBM - 1) / kBM * kBM * 3 * H * 2);
     w.x16 = take(T * H * 2);
     w.topk_idx = take(T * k * 4);
     w.topk_w = take(T * k * 4);
@@ -120,6 +121,7 @@ static RouteOut route_ws(void* ws, const WsLayout& w) {
     o.inv = at<int32_t>(ws, w.inv);
     o.chunk_base = at<int32_t>(ws, w.chunk_base);
     o.logits = at<float>(ws, w.logits);
+    o.router_a = at<uint16_t>(ws, w.router_a);
     o.x16 = at<uint16_t>(ws, w.x16);
     o.tiles_gu = at<Tile>(ws, w.tiles_gu);
     o.tiles_dn = at<Tile>(ws, w.tiles_dn);

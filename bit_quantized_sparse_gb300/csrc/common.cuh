@@ -181,7 +181,14 @@ MW4_DEV uint32_t umma_idesc_f16(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+// Instruction descriptor, kind::f16: bf16 A and B (format 1, both K-major),
+// fp32 D.
+MW4_DEV uint32_t umma_idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread (kind::f16: the
+// instruction descriptor selects fp16 or bf16 operands).
 MW4_DEV void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{.reg .pred p; setp.ne.b32 p, %4, 0;"
@@ -260,14 +267,13 @@ MW4_DEV void warp_argmax(float& v, int& i) {
     }
 }
 
-// Selects the top-k of `sc` (E <= 1024 scores in shared memory, owned by this
-// warp), writes experts by descending score with softmax weights over the
-// selection.  Each lane keeps its (up to 32) scores in registers.
-MW4_DEV void select_topk_warp(const float* sc, int E, int k, int32_t* idx_out, float* w_out) {
+// Warp top-k with NV scores per lane kept in registers (E <= 32 NV).
+template <int NV>
+MW4_DEV void select_topk_warp_n(const float* sc, int E, int k, int32_t* idx_out, float* w_out) {
     const int lane = threadIdx.x & 31;
-    float v[32];
+    float v[NV];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = (lane + 32 * i < E) ? sc[lane + 32 * i] : -INFINITY;
+    for (int i = 0; i < NV; ++i) v[i] = (lane + 32 * i < E) ? sc[lane + 32 * i] : -INFINITY;
     // all loops have compile-time bounds so that every array stays in registers
     float top_v[8];
     int top_i[8];
@@ -277,7 +283,7 @@ MW4_DEV void select_topk_warp(const float* sc, int E, int k, int32_t* idx_out, f
         int bi = 0x7fffffff;
         if (j < k) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)   // ascending index within the lane: strict > keeps the lower one
+            for (int i = 0; i < NV; ++i)   // ascending index within the lane: strict > keeps the lower one
                 if (v[i] > bv) { bv = v[i]; bi = lane + 32 * i; }
         }
         warp_argmax(bv, bi);
@@ -285,7 +291,7 @@ MW4_DEV void select_topk_warp(const float* sc, int E, int k, int32_t* idx_out, f
         top_i[j] = bi;
         if (j < k) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)   // the owner marks it taken
+            for (int i = 0; i < NV; ++i)   // the owner marks it taken
                 if (lane + 32 * i == bi) v[i] = -INFINITY;
         }
     }
@@ -301,6 +307,17 @@ MW4_DEV void select_topk_warp(const float* sc, int E, int k, int32_t* idx_out, f
         idx_out[lane] = mi;
         w_out[lane] = expf(mine - top_v[0]) / z;
     }
+}
+
+// Selects the top-k of `sc` (E <= 1024 scores, owned by this warp), writes
+// experts by descending score with softmax weights over the selection.
+MW4_DEV void select_topk_warp(const float* sc, int E, int k, int32_t* idx_out, float* w_out) {
+    if (E <= 32) select_topk_warp_n<1>(sc, E, k, idx_out, w_out);
+    else if (E <= 64) select_topk_warp_n<2>(sc, E, k, idx_out, w_out);
+    else if (E <= 128) select_topk_warp_n<4>(sc, E, k, idx_out, w_out);
+    else if (E <= 256) select_topk_warp_n<8>(sc, E, k, idx_out, w_out);
+    else if (E <= 512) select_topk_warp_n<16>(sc, E, k, idx_out, w_out);
+    else select_topk_warp_n<32>(sc, E, k, idx_out, w_out);
 }
 
 // Block-wide top-k by rank counting: the rank of expert e is the number of

@@ -80,10 +80,15 @@ __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nch
     int* wt = blk + (E + 1);     // [33]
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
-        for (int c = 0; c < nchunk; ++c) {
-            const int v = chunk_base[(size_t)c * E + e];
-            chunk_base[(size_t)c * E + e] = run;
-            run += v;
+        for (int c0 = 0; c0 < nchunk; c0 += 8) {   // eight independent loads in flight
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = (c0 + j < nchunk) ? chunk_base[(size_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (c0 + j < nchunk) chunk_base[(size_t)(c0 + j) * E + e] = run;
+                run += v[j];
+            }
         }
         cnt[e] = run;
         off[e] = run;
@@ -104,13 +109,20 @@ __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nch
     }
     if (threadIdx.x == 0) offsets[E] = off[E];
     if (tiles_gu == nullptr) return;
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-        const int c = cnt[e];
-        for (int b = 0; b * kBN < c; ++b) {
-            const int r0 = b * kBN, nr = min(kBN, c - r0);
-            for (int m = 0; m < MI; ++m) tiles_gu[(size_t)(blk[e] + b) * MI + m] = Tile{e, m, r0, nr};
-            for (int m = 0; m < MH; ++m) tiles_dn[(size_t)(blk[e] + b) * MH + m] = Tile{e, m, r0, nr};
+    __syncthreads();
+    // tiles in parallel: block b belongs to the expert whose block range holds it
+    // (blk[] is the exclusive scan of blocks per expert; binary search)
+    for (int i = threadIdx.x; i < nblk * (MI + MH); i += blockDim.x) {
+        const bool gu = i < nblk * MI;
+        const int j = gu ? i : i - nblk * MI, M = gu ? MI : MH;
+        const int b = j / M, m = j % M;
+        int lo = 0, hi = E;   // largest e with blk[e] <= b
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (blk[mid] <= b) lo = mid; else hi = mid - 1;
         }
+        const int e = lo, r0 = (b - blk[e]) * kBN, nr = min(kBN, cnt[e] - r0);
+        (gu ? tiles_gu : tiles_dn)[j] = Tile{e, m, r0, nr};
     }
     if (threadIdx.x == 0) {
         ntiles[0] = nblk * MI;
@@ -124,18 +136,21 @@ __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nch
 __global__ void __launch_bounds__(32) assign_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                                     const int32_t* __restrict__ chunk_base,
                                                     int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
-    extern __shared__ int running[];
+    extern __shared__ int sm_assign[];
+    int* running = sm_assign;             // [E]
+    int* sel = sm_assign + E;             // [kChunk * k] the chunk's selections
     const int lane = threadIdx.x;
     const int c = blockIdx.x;
+    const int t_begin = c * kChunk, t_end = min(T, t_begin + kChunk);
     for (int e = lane; e < E; e += 32) running[e] = chunk_base[(size_t)c * E + e];
+    for (int i = lane; i < (t_end - t_begin) * k; i += 32) sel[i] = idx[(size_t)t_begin * k + i];
     __syncwarp();
     const int per = 32 / k;                 // tokens per step
-    const int t_begin = c * kChunk, t_end = min(T, t_begin + kChunk);
     const unsigned lt_mask = (1u << lane) - 1u;
     for (int t0 = t_begin; t0 < t_end; t0 += per) {
         const int t = t0 + lane / k, j = lane % k;
         const bool valid = (lane < per * k) && (t < t_end);
-        int e = valid ? idx[(size_t)t * k + j] : -1;
+        int e = valid ? sel[(t - t_begin) * k + j] : -1;
         if (e < 0 || e >= E) e = -1;        // bad indices were reported by the count kernel
         const unsigned same = __match_any_sync(0xffffffffu, e);
         int pos = 0;
@@ -159,7 +174,8 @@ cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cud
     scan_kernel<<<1, 1024, scan_sm, st>>>(T, E, k, nchunk, o.chunk_base, o.counts, o.offsets, o.tiles_gu,
                                           o.tiles_dn, o.ntiles, L.I / kBM, L.H / kBM);
     trace_mark(st, 4);
-    assign_kernel<<<nchunk, 32, E * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.perm, o.inv);
+    assign_kernel<<<nchunk, 32, (E + kChunk * k) * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.perm,
+                                                                     o.inv);
     trace_mark(st, 5);
     return cudaGetLastError();
 }

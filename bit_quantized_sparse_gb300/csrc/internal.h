@@ -28,7 +28,7 @@ void trace_kernels(int n);   // expert (E = shared), weight-row block, first row
 
 // Byte offsets of every region of the workspace (all 256-byte aligned).
 struct WsLayout {
-    size_t ctrl, logits, x16, topk_idx, topk_w, gamma, chunk_base, counts, offsets, perm, inv;
+    size_t ctrl, logits, router_a, x16, topk_idx, topk_w, gamma, chunk_base, counts, offsets, perm, inv;
     size_t tiles_gu, tiles_dn, ntiles, hh, ys;
     size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh, dec_cpart, dec_ybuf;
     size_t total;
@@ -46,6 +46,7 @@ struct RouteOut {
     int32_t* perm; int32_t* inv;
     int32_t* chunk_base;
     float* logits;
+    uint16_t* router_a;  // [Epad][3H] bf16 split router weights (tensor-core scores); NULL: CUDA cores
     uint16_t* x16;     // fp16 copy of x written by the top-k kernel (NULL: not needed)
     Tile* tiles_gu; Tile* tiles_dn; int32_t* ntiles;   // NULL: no tile maps
     unsigned int* status;

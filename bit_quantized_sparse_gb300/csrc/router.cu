@@ -72,6 +72,134 @@ __global__ void __launch_bounds__(256) router_scores_kernel(const uint16_t* __re
 }
 
 // ---------------------------------------------------------------------------
+// scores on the tensor cores with fp32 accuracy
+// ---------------------------------------------------------------------------
+// W_r (fp32) is split exactly into three bf16 terms, w = hi + mid + lo (8 + 8 +
+// 8 significant bits), stored transposed as A[e][k] for k in [0, 3H): hi, then
+// mid, then lo.  x is exact in bf16, every bf16 x bf16 product is exact in
+// fp32, and the tensor core accumulates in fp32, so A . [x, x, x] reproduces
+// the fp32 score x . W_r.  Rows e >= E are zero.
+__global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ Wr, int H, int E, int Epad,
+                                                           uint16_t* __restrict__ A) {
+    __shared__ float tile[32][33];
+    const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;   // 32 x 8
+    for (int r = ty; r < 32; r += 8) {
+        const int e = e0 + tx;
+        tile[r][tx] = (e < E) ? Wr[(size_t)(h0 + r) * E + e] : 0.f;
+    }
+    __syncthreads();
+    for (int r = ty; r < 32; r += 8) {   // r: expert within the tile, tx: row h within the tile
+        const int e = e0 + r;
+        if (e >= Epad) continue;
+        const float w = tile[tx][r];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const float r1 = w - __bfloat162float(hi);
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+        uint16_t* row = A + (size_t)e * 3 * H + h0 + tx;
+        row[0] = __bfloat16_as_ushort(hi);
+        row[H] = __bfloat16_as_ushort(mid);
+        row[2 * H] = __bfloat16_as_ushort(lo);
+    }
+}
+
+constexpr int kRtBN = 64;      // tokens per tile
+constexpr int kRtStages = 6;
+
+struct RouterTcArgs {
+    const float* bias;
+    float* logits;   // [T][E]
+    int T, H, E;
+    unsigned int* status;
+};
+
+// One CTA: 128 experts x 64 tokens, K = 3H in 64-column steps.  Warp 0 issues
+// TMA for A and B, warp 1 allocates TMEM and one thread issues the MMAs,
+// warps 4-7 write the scores (+ bias).
+__global__ void __launch_bounds__(256, 1)
+router_tc_kernel(const __grid_constant__ RouterTcArgs a, const __grid_constant__ CUtensorMap mapA,
+                 const __grid_constant__ CUtensorMap mapX) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr uint32_t A_BYTES = kBM * kBK * 2, B_BYTES = kRtBN * kBK * 2, STAGE = A_BYTES + B_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + kRtStages * STAGE);
+    uint64_t* empty = full + kRtStages;
+    uint64_t* accum = empty + kRtStages;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(accum + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1) + 1;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kRtBN;
+    const int nK = 3 * a.H / kBK, hsteps = a.H / kBK;
+    if (tid == 0) {
+        for (int s = 0; s < kRtStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(accum, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 4 * kRtBN);   // hi, mid, lo accumulators
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t taddr = *tmem_slot;
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&mapA);
+        prefetch_tensormap(&mapX);
+        for (int ks = 0; ks < nK; ++ks) {
+            const int s = ks % kRtStages;
+            if (!mbar_wait(&empty[s], ((ks / kRtStages) & 1) ^ 1, abort_flag, a.status)) break;
+            uint8_t* st = base + (size_t)s * STAGE;
+            mbar_arrive_expect_tx(&full[s], STAGE);
+            tma_load_2d(st, &mapA, ks * kBK, m0, &full[s]);
+            tma_load_2d(st + A_BYTES, &mapX, (ks % hsteps) * kBK, n0, &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        const uint32_t idesc = umma_idesc_bf16(kBM, kRtBN);
+        bool ok = true;
+        for (int ks = 0; ks < nK; ++ks) {
+            const int s = ks % kRtStages;
+            if (!(ok = mbar_wait(&full[s], (ks / kRtStages) & 1, abort_flag, a.status))) break;
+            tc_fence_after();
+            const uint32_t sa = smem_u32(base + (size_t)s * STAGE);
+            // one accumulator per term: products of very different magnitude are
+            // never summed inside the tensor core, only in fp32 in the epilogue
+            const int part = ks / hsteps, kp = ks % hsteps;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_f16(taddr + part * kRtBN, umma_desc_sw128(sa + kk * 32), umma_desc_sw128(sa + A_BYTES + kk * 32),
+                         idesc, (kp | kk) != 0);
+            umma_commit(&empty[s]);
+        }
+        if (ok) umma_commit(accum);
+    } else if (warp >= 4) {
+        const int q = warp - 4, e = m0 + q * 32 + lane;
+        if (mbar_wait(accum, 0, abort_flag, a.status)) {
+            tc_fence_after();
+            const float bias = (e < a.E && a.bias) ? a.bias[e] : 0.f;
+            for (int c0 = 0; c0 < kRtBN; c0 += 16) {
+                uint32_t vh[16], vm[16], vl[16];
+                const uint32_t ta = taddr + ((uint32_t)(q * 32) << 16) + c0;
+                tmem_ld16(ta, vh);
+                tmem_ld16(ta + kRtBN, vm);
+                tmem_ld16(ta + 2 * kRtBN, vl);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = n0 + c0 + j;
+                    const float v = __uint_as_float(vh[j]) + (__uint_as_float(vm[j]) + __uint_as_float(vl[j]));
+                    if (e < a.E && t < a.T) a.logits[(size_t)t * a.E + e] = v + bias;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(taddr, 4 * kRtBN);
+}
+
+size_t router_tc_smem() { return 1024 + (size_t)kRtStages * (kBM * kBK * 2 + kRtBN * kBK * 2) + 2 * kRtStages * 8 + 32; }
+
+// ---------------------------------------------------------------------------
 // per-token selection: one warp per token
 // ---------------------------------------------------------------------------
 constexpr int kTopkWarps = 8;
@@ -114,10 +242,53 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __re
     if (lane == 0) gamma[t] = 1.0f / (1.0f + expf(-d));
 }
 
+typedef CUresult (*EncodeTiledFnR)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static bool bf16_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    static EncodeTiledFnR fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess)
+            return false;
+        fn = reinterpret_cast<EncodeTiledFnR>(p);
+    }
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* x, const RouteOut& o,
                                   cudaStream_t st) {
-    dim3 grid((L.E + kRE - 1) / kRE, (T + kRT - 1) / kRT);
-    router_scores_kernel<<<grid, 256, 0, st>>>(x, L.router_w, L.router_bias, o.logits, T, L.H, L.E);
+    const int Epad = (L.E + kBM - 1) / kBM * kBM;
+    if (o.router_a) {   // tensor-core path
+        router_split_kernel<<<dim3(L.H / 32, Epad / 32), 256, 0, st>>>(L.router_w, L.H, L.E, Epad, o.router_a);
+        CUtensorMap mA, mX;
+        if (!bf16_map(&mA, o.router_a, Epad, 3 * (uint64_t)L.H, kBM) || !bf16_map(&mX, x, T, L.H, kRtBN))
+            return cudaErrorInvalidValue;
+        static size_t attr[64] = {};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (attr[dev] < router_tc_smem()) {
+            const cudaError_t e = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)router_tc_smem());
+            if (e != cudaSuccess) return e;
+            attr[dev] = router_tc_smem();
+        }
+        RouterTcArgs ra{L.router_bias, o.logits, T, L.H, L.E, o.status};
+        router_tc_kernel<<<dim3(Epad / kBM, (T + kRtBN - 1) / kRtBN), 256, router_tc_smem(), st>>>(ra, mA, mX);
+    } else {
+        dim3 grid((L.E + kRE - 1) / kRE, (T + kRT - 1) / kRT);
+        router_scores_kernel<<<grid, 256, 0, st>>>(x, L.router_w, L.router_bias, o.logits, T, L.H, L.E);
+    }
     trace_mark(st, 1);
     const size_t sm = (size_t)kTopkWarps * L.E * sizeof(float);
     topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, sm, st>>>(
