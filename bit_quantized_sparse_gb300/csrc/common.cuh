@@ -212,46 +212,66 @@ MW4_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 MW4_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// ---------------------------------------------------------------------------
-// 4-bit code unpacking to fp16 pairs (exact)
-// ---------------------------------------------------------------------------
-// For a word holding codes n0..n7 (n0 lowest), returns four half2 values
-// (n0,n1), (n2,n3), (n4,n5), (n6,n7), each lane equal to 1024 + n: 0x64 is
-// the high byte of fp16(1024), whose unit in the last place is 1, so a code in
-// the low mantissa bits adds exactly n.
-MW4_DEV void unpack8_f16_plus1024(uint32_t w, uint32_t (&p)[4]) {
-    const uint32_t lo = w & 0x0F0F0F0Fu;          // bytes: n0 n2 n4 n6
-    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;   // bytes: n1 n3 n5 n7
-    const uint32_t a = __byte_perm(lo, hi, 0x5140); // bytes: n0 n1 n2 n3
-    const uint32_t b = __byte_perm(lo, hi, 0x7362); // bytes: n4 n5 n6 n7
-    const uint32_t c = 0x64646464u;
-    p[0] = __byte_perm(a, c, 0x4140);
-    p[1] = __byte_perm(a, c, 0x4342);
-    p[2] = __byte_perm(b, c, 0x4140);
-    p[3] = __byte_perm(b, c, 0x4342);
+// 32 lanes x 32 consecutive 32-bit columns; thread t of the warp writes lane
+// (base lane + t).  Follow with tmem_wait_st before signalling a consumer.
+MW4_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+           "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+           "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+           "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+MW4_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem]^T: A is 128 lanes (rows) x K/2 columns of
+// 16-bit pairs; issued by one thread.
+MW4_DEV void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{.reg .pred p; setp.ne.b32 p, %4, 0;"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// 4-bit code unpacking to fp16 (exact), in "chunk order"
+// ---------------------------------------------------------------------------
+// A word holds the codes of 8 consecutive columns, n0 in the lowest nibble.
+// fp16(1024) has a unit in the last place of 1, so a nibble OR-ed into bits
+// 0..3 reads 1024 + q and one OR-ed into bits 4..7 reads 1024 + 16 q, both
+// exactly.  One bitwise op therefore yields two columns; the four pairs come
+// out as (n0,n4) (n1,n5) (n2,n6) (n3,n7), the second and fourth scaled by 16.
+// The columns inside every 8-column chunk are thus stored in the order
+//   kChunkOrder = {0, 4, 1, 5, 2, 6, 3, 7}
+// and the other operand of the product (x, h) is stored in the same order.
 MW4_DEV __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
 MW4_DEV uint32_t h2_as_u32(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
 MW4_DEV uint32_t bf162_as_u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 
-// w = s*q + b for eight codes, s and b given as half2 pairs; the product and
-// sum are exact inside the fused multiply-add, so each weight is rounded to
-// fp16 once.
-MW4_DEV void dequant8_f16(uint32_t word, __half2 s2, __half2 b2, uint32_t (&o)[4]) {
-    uint32_t p[4];
-    unpack8_f16_plus1024(word, p);
-    const __half2 k1024 = u32_as_h2(0x64006400u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __half2 q = __hsub2(u32_as_h2(p[i]), k1024);   // exact
-        o[i] = h2_as_u32(__hfma2(s2, q, b2));               // single rounding
-    }
+MW4_DEV int chunk_pos_of_col(int j) { return ((j & 3) << 1) | (j >> 2); }   // inverse of kChunkOrder
+
+// w = s*q + b for eight codes in chunk order; s2 = (s, s), s16 = (s/16, s/16),
+// b2 = (b, b).  q (or 16 q) is recovered exactly and the product and sum are
+// exact inside the fused multiply-add: each weight is rounded to fp16 once.
+MW4_DEV void dequant8_f16(uint32_t w, __half2 s2, __half2 s16, __half2 b2, uint32_t (&o)[4]) {
+    const uint32_t magic = 0x64006400u;
+    const uint32_t w8 = w >> 8;
+    const uint32_t p0 = (w & 0x000F000Fu) | magic;    // 1024 + (n0, n4)
+    const uint32_t p1 = (w & 0x00F000F0u) | magic;    // 1024 + 16 (n1, n5)
+    const uint32_t p2 = (w8 & 0x000F000Fu) | magic;   // 1024 + (n2, n6)
+    const uint32_t p3 = (w8 & 0x00F000F0u) | magic;   // 1024 + 16 (n3, n7)
+    const __half2 k1024 = u32_as_h2(magic);
+    o[0] = h2_as_u32(__hfma2(s2, __hsub2(u32_as_h2(p0), k1024), b2));
+    o[1] = h2_as_u32(__hfma2(s16, __hsub2(u32_as_h2(p1), k1024), b2));
+    o[2] = h2_as_u32(__hfma2(s2, __hsub2(u32_as_h2(p2), k1024), b2));
+    o[3] = h2_as_u32(__hfma2(s16, __hsub2(u32_as_h2(p3), k1024), b2));
 }
 
 MW4_DEV float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
-MW4_DEV float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+MW4_DEV float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 MW4_DEV float sigmoid_f(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
 // ---------------------------------------------------------------------------

@@ -1,4 +1,7 @@
 // Prefill expert FFN as grouped GEMMs on the 5th-generation tensor cores.
+// Along K every operand is stored in chunk order (common.cuh): the
+// dequantised weights come out that way, the fp16 copy of x and h are written
+// that way.
 // Operands are fp16 (weights rebuilt in fp16, activations and the intermediate
 // h in fp16), accumulation fp32: fp16 has the same tcgen05 rate as bf16 and
 // eight times its precision, which keeps the computation error an order of
@@ -56,24 +59,30 @@ struct GemmArgs {
 constexpr uint32_t kCodesBytes = kBM * (kBK / 8) * 4;   // 4 KB of packed codes per matrix per step
 constexpr uint32_t kTileBytes = kBM * kBK * 2;          // 16 KB fp16 tile (A or B)
 
-// Persistent-kernel geometry: warp roles and ring depths.
+// Persistent-kernel geometry: warp roles, ring depths and the TMEM map.
+// The dequantised weights (the A operand) live in tensor memory, written by
+// tcgen05.st and read by the MMA from there: no shared-memory round trip and
+// no proxy fence.  TMEM (512 columns) holds the accumulators and an A ring.
 template <bool DUAL>
 struct Geo {
     static constexpr int NMAT = DUAL ? 2 : 1;
     static constexpr int kDeqWarps = 4 * NMAT;            // one thread per (matrix, weight row)
     static constexpr int kDeqWarp0 = 4;
     static constexpr int kEpiWarp0 = kDeqWarp0 + kDeqWarps;
-    static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
-    static constexpr int SR = DUAL ? 4 : 6;               // codes (+B) ring
-    static constexpr int SA = DUAL ? 3 : 4;               // dequantised A ring
+    static constexpr int kEpiWarps = 8;                   // two per TMEM lane group, columns interleaved
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+    static constexpr int SR = DUAL ? 8 : 10;              // codes (+B) ring in shared memory
     static constexpr uint32_t R_STAGE = kTileBytes + NMAT * kCodesBytes;   // B first (1024-aligned)
-    static constexpr uint32_t A_STAGE = NMAT * kTileBytes;
     static constexpr uint32_t ACC_COLS = NMAT * 128;      // TMEM columns per accumulator buffer
-    static constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;   // double-buffered
+    static constexpr int ACC_BUFS = DUAL ? 1 : 2;
+    static constexpr uint32_t A_COLS = NMAT * (kBK / 2);  // TMEM columns per A stage (16-bit pairs)
+    static constexpr int SA = (512 - ACC_BUFS * ACC_COLS) / A_COLS;   // A ring in TMEM
+    static constexpr uint32_t A_TMEM0 = ACC_BUFS * ACC_COLS;
     static constexpr size_t bytes() {
-        return 1024 + (size_t)SR * R_STAGE + (size_t)SA * A_STAGE + 2 * kBN * 4 + (3 * SR + 2 * SA + 4) * 8 + 16;
+        return 1024 + (size_t)SR * R_STAGE + 2 * kBN * 4 + (3 * SR + 2 * SA + 4) * 8 + 16;
     }
 };
+static_assert(Geo<true>::SA == 4 && Geo<false>::SA == 8, "TMEM map");
 
 MW4_DEV uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -104,13 +113,11 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align1024(smem_raw);
     uint8_t* rring = base;
-    uint8_t* aring = base + (size_t)SR * GG::R_STAGE;
     auto B_of = [&](int s) { return rring + (size_t)s * GG::R_STAGE; };
     auto C_of = [&](int s, int mat) {
         return reinterpret_cast<const uint8_t*>(rring + (size_t)s * GG::R_STAGE + kTileBytes + mat * kCodesBytes);
     };
-    auto A_of = [&](int s, int mat) { return aring + (size_t)s * GG::A_STAGE + mat * kTileBytes; };
-    float* col_scale = reinterpret_cast<float*>(aring + (size_t)SA * GG::A_STAGE);   // [2][kBN]
+    float* col_scale = reinterpret_cast<float*>(rring + (size_t)SR * GG::R_STAGE);   // [2][kBN]
     uint64_t* bars = reinterpret_cast<uint64_t*>(col_scale + 2 * kBN);
     uint64_t* r_full = bars;
     uint64_t* r_fullb = bars + SR;
@@ -135,13 +142,13 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 128);
+            mbar_init(&acc_empty[b], 32 * GG::kEpiWarps);
         }
         *abort_flag = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, GG::TMEM_COLS);
+    if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -182,8 +189,8 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 const TileInfo ti = tile_info(a, t);
                 const int nmma = ((ti.nrows + 15) / 16) * 16;
                 const uint32_t idesc = umma_idesc_f16(kBM, nmma);
-                const int b = it & 1;
-                if (!mbar_wait(&acc_empty[b], ((it >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+                const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS;
+                if (!mbar_wait(&acc_empty[b], (use & 1) ^ 1, abort_flag, a.status)) break;
                 tc_fence_after();
                 const uint32_t dacc = taddr + b * GG::ACC_COLS;
                 for (int ks = 0; ks < nK; ++ks, ++gk) {
@@ -192,14 +199,14 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                          mbar_wait(DUAL ? &r_fullb[sr] : &r_full[sr], (gk / SR) & 1, abort_flag, a.status);
                     if (!ok) break;
                     tc_fence_after();
+                    const uint32_t atm = taddr + GG::A_TMEM0 + sa * GG::A_COLS;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t bdesc = umma_desc_sw128(smem_u32(B_of(sr)) + kk * 32);
 #pragma unroll
-                        for (int mat = 0; mat < NMAT; ++mat) {
-                            const uint64_t adesc = umma_desc_sw128(smem_u32(A_of(sa, mat)) + kk * 32);
-                            umma_f16(dacc + mat * 128, adesc, bdesc, idesc, (ks | kk) != 0);
-                        }
+                        for (int mat = 0; mat < NMAT; ++mat)
+                            umma_f16_ts(dacc + mat * 128, atm + mat * (kBK / 2) + kk * 8, bdesc, idesc,
+                                        (ks | kk) != 0);
                     }
                     umma_commit(&r_empty[sr]);
                     umma_commit(&a_empty[sa]);
@@ -291,18 +298,25 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                     const uint8_t* cr = C_of(sr, mat) + row * 32;
                     const uint4 w0 = *reinterpret_cast<const uint4*>(cr + ((0 ^ sw) << 4));
                     const uint4 w1 = *reinterpret_cast<const uint4*>(cr + ((1 ^ sw) << 4));
-                    const __half s_h = __float2half_rn(bf16_bits_to_float((uint16_t)s16));
+                    const float sf = bf16_bits_to_float((uint16_t)s16);
+                    const __half s_h = __float2half_rn(sf), s_h16 = __float2half_rn(sf * 0.0625f);
                     const __half b_h = __float2half_rn(bf16_bits_to_float((uint16_t)b16));
-                    const __half2 s2 = __halves2half2(s_h, s_h), b2 = __halves2half2(b_h, b_h);
-                    uint8_t* At = A_of(sa, mat) + row * 128;
+                    const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16);
+                    const __half2 b2 = __halves2half2(b_h, b_h);
+                    // this thread's weight row -> its TMEM lane, 32 columns of fp16 pairs
                     const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                    uint32_t o[32];
 #pragma unroll
                     for (int wi = 0; wi < 8; ++wi) {
-                        uint32_t o[4];
-                        dequant8_f16(words[wi], s2, b2, o);
-                        *reinterpret_cast<uint4*>(At + ((wi ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        uint32_t q4[4];
+                        dequant8_f16(words[wi], s2, s2_16, b2, q4);
+                        o[4 * wi] = q4[0]; o[4 * wi + 1] = q4[1]; o[4 * wi + 2] = q4[2]; o[4 * wi + 3] = q4[3];
                     }
-                    fence_proxy_async_smem();
+                    tc_fence_after();   // the MMAs that read this A slot have completed (a_empty)
+                    tmem_st32(taddr + ((uint32_t)(row & ~31) << 16) + GG::A_TMEM0 + sa * GG::A_COLS + mat * (kBK / 2),
+                              o);
+                    tmem_wait_st();
+                    tc_fence_before();
                     mbar_arrive(&a_full[sa]);
                     ++gk;
                 }
@@ -313,21 +327,24 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         }
     } else {
         // ------------------------------------------------------------ epilogue: TMEM -> registers -> global
-        const int q = warp - GG::kEpiWarp0, et = tid - 32 * GG::kEpiWarp0;
+        const int ew = warp - GG::kEpiWarp0, q = ew & 3, half = ew >> 2;
+        const int et = tid - 32 * GG::kEpiWarp0;
         int it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const TileInfo ti = tile_info(a, t);
-            const int b = it & 1;
+            const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS;
             if (!DUAL) {   // per-column output scale of this tile, fetched while the MMAs run
                 if (et < ti.nrows)
                     col_scale[b * kBN + et] = ti.sh ? a.gamma[ti.r0 + et] : a.topk_w[a.perm[ti.p0 + et]];
-                asm volatile("bar.sync 2, 128;" ::: "memory");
+                asm volatile("bar.sync 2, 256;" ::: "memory");
             }
-            if (!mbar_wait(&acc_full[b], (it >> 1) & 1, abort_flag, a.status)) break;
+            if (!mbar_wait(&acc_full[b], use & 1, abort_flag, a.status)) break;
             tc_fence_after();
             const uint32_t lane_addr = taddr + b * GG::ACC_COLS + ((uint32_t)(q * 32) << 16);
-            const int ocol = ti.m * kBM + q * 32 + lane;
-            for (int c0 = 0; c0 < ti.nrows; c0 += 16) {
+            // h is the K operand of the down projection: store it in chunk order
+            const int orow = ti.m * kBM + q * 32 + lane;
+            const int ocol = DUAL ? ((orow & ~7) | chunk_pos_of_col(orow & 7)) : orow;
+            for (int c0 = half * 16; c0 < ti.nrows; c0 += 32) {
                 uint32_t g[16], u[16];
                 tmem_ld16(lane_addr + c0, g);
                 if (DUAL) tmem_ld16(lane_addr + 128 + c0, u);
@@ -349,7 +366,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(taddr, GG::TMEM_COLS);
+    if (warp == 1) tmem_dealloc(taddr, 512);
 }
 
 // out[t] = bf16( sum_j ys[inv[t*k + j]] + ys[T*k + t] ) with ys in fp16 and

@@ -223,16 +223,21 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __re
     for (int h = lane * 8; h < H; h += 256) {
         const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h);
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-        uint32_t hv[4];
         bool fits = true;
+        float f[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float a = __uint_as_float(u[i] << 16), b = __uint_as_float(u[i] & 0xFFFF0000u);
             d = fmaf(a, g[h + 2 * i], d);
             d = fmaf(b, g[h + 2 * i + 1], d);
             fits = fits && fabsf(a) <= 65504.f && fabsf(b) <= 65504.f;
-            hv[i] = h2_as_u32(__floats2half2_rn(a, b));
+            f[2 * i] = a;
+            f[2 * i + 1] = b;
         }
+        // fp16 copy in chunk order {0,4,1,5,2,6,3,7} (the order the dequantised weights use)
+        uint32_t hv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hv[i] = h2_as_u32(__floats2half2_rn(f[i], f[i + 4]));
         if (x16) {
             *reinterpret_cast<uint4*>(x16 + (size_t)t * H + h) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             if (!fits) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
