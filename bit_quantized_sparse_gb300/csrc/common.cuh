@@ -99,6 +99,12 @@ MW4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
     }
 }
 
+// mbar_wait run by a whole converged warp; every lane gets lane 0's answer.
+MW4_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, status);
+    return __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+}
+
 // ---------------------------------------------------------------------------
 // proxies and fences
 // ---------------------------------------------------------------------------
@@ -199,6 +205,32 @@ MW4_DEV void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t 
 MW4_DEV void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  :: "r"(smem_u32(bar)) : "memory");
+}
+
+// Warp-level issue: the whole (converged) warp executes these with the same
+// operands and one elected lane issues the instruction.  Keeping the loop that
+// feeds tcgen05.mma warp-uniform, rather than running it in one lane of a
+// divergent branch, cuts the issue cost per MMA from about 44 cycles to about
+// 12 on sm_103a (measured), which decides the rate for narrow N.  elect.sync
+// elects the same lane every time for a full mask, so one thread issues both
+// the MMAs and the commits that track them.
+MW4_DEV void umma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{.reg .pred p, e; setp.ne.b32 p, %4, 0; elect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+MW4_DEV void umma_f16_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{.reg .pred p, e; setp.ne.b32 p, %4, 0; elect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;}"
+        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+MW4_DEV void umma_commit_elect(uint64_t* bar) {
+    asm volatile(
+        "{.reg .pred e; elect.sync _|e, 0xffffffff;\n"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];}"
+        :: "r"(smem_u32(bar)) : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns; thread t of the warp gets lane

@@ -181,38 +181,36 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int gk = 0, it = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
-                const TileInfo ti = tile_info(a, t);
-                const int nmma = ((ti.nrows + 15) / 16) * 16;
-                const uint32_t idesc = umma_idesc_f16(kBM, nmma);
-                const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS;
-                if (!mbar_wait(&acc_empty[b], (use & 1) ^ 1, abort_flag, a.status)) break;
+        // ------------------------------------------------------------ MMA issuer (warp-uniform, one lane issues)
+        int gk = 0, it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+            const TileInfo ti = tile_info(a, t);
+            const int nmma = ((ti.nrows + 15) / 16) * 16;
+            const uint32_t idesc = umma_idesc_f16(kBM, nmma);
+            const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS;
+            if (!mbar_wait_warp(&acc_empty[b], (use & 1) ^ 1, abort_flag, a.status)) break;
+            tc_fence_after();
+            const uint32_t dacc = taddr + b * GG::ACC_COLS;
+            for (int ks = 0; ks < nK; ++ks, ++gk) {
+                const int sr = gk % SR, sa = gk % SA;
+                ok = mbar_wait_warp(&a_full[sa], (gk / SA) & 1, abort_flag, a.status) &&
+                     mbar_wait_warp(DUAL ? &r_fullb[sr] : &r_full[sr], (gk / SR) & 1, abort_flag, a.status);
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t dacc = taddr + b * GG::ACC_COLS;
-                for (int ks = 0; ks < nK; ++ks, ++gk) {
-                    const int sr = gk % SR, sa = gk % SA;
-                    ok = mbar_wait(&a_full[sa], (gk / SA) & 1, abort_flag, a.status) &&
-                         mbar_wait(DUAL ? &r_fullb[sr] : &r_full[sr], (gk / SR) & 1, abort_flag, a.status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t atm = taddr + GG::A_TMEM0 + sa * GG::A_COLS;
+                const uint32_t atm = taddr + GG::A_TMEM0 + sa * GG::A_COLS;
+                const uint64_t bdesc0 = umma_desc_sw128(smem_u32(B_of(sr)));
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t bdesc = umma_desc_sw128(smem_u32(B_of(sr)) + kk * 32);
+                for (int kk = 0; kk < kBK / 16; ++kk) {
 #pragma unroll
-                        for (int mat = 0; mat < NMAT; ++mat)
-                            umma_f16_ts(dacc + mat * 128, atm + mat * (kBK / 2) + kk * 8, bdesc, idesc,
-                                        (ks | kk) != 0);
-                    }
-                    umma_commit(&r_empty[sr]);
-                    umma_commit(&a_empty[sa]);
+                    for (int mat = 0; mat < NMAT; ++mat)   // +32 bytes per K=16 slice: +2 in the address field
+                        umma_f16_ts_elect(dacc + mat * 128, atm + mat * (kBK / 2) + kk * 8, bdesc0 + 2 * kk, idesc,
+                                          (ks | kk) != 0);
                 }
-                if (ok) umma_commit(&acc_full[b]);
+                umma_commit_elect(&r_empty[sr]);
+                umma_commit_elect(&a_empty[sa]);
             }
+            if (ok) umma_commit_elect(&acc_full[b]);
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------ token-row gather (gate/up)

@@ -115,7 +115,7 @@ struct RouterTcArgs {
 };
 
 // One CTA: 128 experts x 64 tokens, K = 3H in 64-column steps.  Warp 0 issues
-// TMA for A and B, warp 1 allocates TMEM and one thread issues the MMAs,
+// TMA for A and B, warp 1 allocates TMEM and issues the MMAs,
 // warps 4-7 write the scores (+ bias).
 __global__ void __launch_bounds__(256, 1)
 router_tc_kernel(const __grid_constant__ RouterTcArgs a, const __grid_constant__ CUtensorMap mapA,
@@ -153,24 +153,24 @@ router_tc_kernel(const __grid_constant__ RouterTcArgs a, const __grid_constant__
             tma_load_2d(st, &mapA, ks * kBK, m0, &full[s]);
             tma_load_2d(st + A_BYTES, &mapX, (ks % hsteps) * kBK, n0, &full[s]);
         }
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {   // warp-uniform loop, one elected lane issues
         const uint32_t idesc = umma_idesc_bf16(kBM, kRtBN);
         bool ok = true;
         for (int ks = 0; ks < nK; ++ks) {
             const int s = ks % kRtStages;
-            if (!(ok = mbar_wait(&full[s], (ks / kRtStages) & 1, abort_flag, a.status))) break;
+            if (!(ok = mbar_wait_warp(&full[s], (ks / kRtStages) & 1, abort_flag, a.status))) break;
             tc_fence_after();
             const uint32_t sa = smem_u32(base + (size_t)s * STAGE);
+            const uint64_t adesc0 = umma_desc_sw128(sa), bdesc0 = umma_desc_sw128(sa + A_BYTES);
             // one accumulator per term: products of very different magnitude are
             // never summed inside the tensor core, only in fp32 in the epilogue
             const int part = ks / hsteps, kp = ks % hsteps;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-                umma_f16(taddr + part * kRtBN, umma_desc_sw128(sa + kk * 32), umma_desc_sw128(sa + A_BYTES + kk * 32),
-                         idesc, (kp | kk) != 0);
-            umma_commit(&empty[s]);
+            for (int kk = 0; kk < kBK / 16; ++kk)   // +32 bytes per K=16 slice: +2 in the address field
+                umma_f16_elect(taddr + part * kRtBN, adesc0 + 2 * kk, bdesc0 + 2 * kk, idesc, (kp | kk) != 0);
+            umma_commit_elect(&empty[s]);
         }
-        if (ok) umma_commit(accum);
+        if (ok) umma_commit_elect(accum);
     } else if (warp >= 4) {
         const int q = warp - 4, e = m0 + q * 32 + lane;
         if (mbar_wait(accum, 0, abort_flag, a.status)) {
