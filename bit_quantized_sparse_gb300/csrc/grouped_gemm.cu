@@ -14,21 +14,26 @@
 // "Match tile size to expert load": tiles of fixed size over each expert's
 // rows, listed in a block map.)
 //
-// One CTA computes one tile: 128 weight rows (output features) x up to 128
-// grouped token rows, reducing over K in 64-column steps (one quantisation
-// group per row per step).  Warp roles, 384 threads:
-//   warp 0      TMA: packed codes of the step (and, for the down projection,
-//               the activation rows), plus the tile's scales/biases once
-//   warp 1      TMEM allocation; one thread issues tcgen05.mma
-//   warps 2-3   gate/up only: gather the token rows of x with cp.async
-//   warps 4-11  dequantise codes -> bf16 A tiles (128-byte swizzle) in smem;
-//               warps 4-7 then run the epilogue out of TMEM
+// A tile is 128 weight rows (output features) x up to 128 grouped token rows,
+// reduced over K in 64-column steps (one quantisation group per row per step).
 // The weights are the M=128 operand ("swap AB"), so an expert with few rows
 // wastes only N columns, and N = rows rounded up to 16.
 //   gate/up:  D_g = Wg * X^T, D_u = Wu * X^T (two accumulators), epilogue
 //             h = silu(D_g) * D_u -> hh[p][i] fp16
 //   down:     D = Wd * H^T, epilogue scales column p by its routing weight
 //             (or the shared gate) -> ys[p][o] fp16
+// The kernel is persistent (one CTA per SM, tiles strided by the grid) and
+// warp-specialised:
+//   dequantisers  4 warps per matrix, one thread per weight row: codes from
+//                 shared memory -> fp16 -> tcgen05.st into an A ring in TMEM;
+//                 for gate/up they also gather the token rows of x16 (the B
+//                 operand) with cp.async a few steps ahead
+//   epilogue      8 warps, two per TMEM lane quarter: TMEM -> registers ->
+//                 global memory
+//   producer      1 warp, TMA: the step's packed codes (and, for down, the
+//                 contiguous B rows of hh), plus an L2 prefetch of the tile's codes
+//   MMA           1 warp: TMEM allocation and the MMA loop (warp-uniform, one
+//                 elected lane issues tcgen05.mma with A read from tensor memory)
 // combine_kernel then sums, per token, its k rows of ys and the shared row in
 // a fixed order.
 #include "common.cuh"
@@ -67,10 +72,12 @@ template <bool DUAL>
 struct Geo {
     static constexpr int NMAT = DUAL ? 2 : 1;
     static constexpr int kDeqWarps = 4 * NMAT;            // one thread per (matrix, weight row)
-    static constexpr int kDeqWarp0 = 4;
-    static constexpr int kEpiWarp0 = kDeqWarp0 + kDeqWarps;
+    static constexpr int kDeqWarp0 = 0;                   // warp w reaches TMEM lanes 32*(w%4)..+31, so the
+    static constexpr int kEpiWarp0 = kDeqWarp0 + kDeqWarps;   // dequantiser and epilogue groups start at w%4 == 0
     static constexpr int kEpiWarps = 8;                   // two per TMEM lane group, columns interleaved
-    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+    static constexpr int kProdWarp = kEpiWarp0 + kEpiWarps;   // TMA producer
+    static constexpr int kMmaWarp = kProdWarp + 1;            // TMEM owner and MMA issuer
+    static constexpr int kThreads = 32 * (kMmaWarp + 1);
     static constexpr int SR = DUAL ? 8 : 10;              // codes (+B) ring in shared memory
     static constexpr uint32_t R_STAGE = kTileBytes + NMAT * kCodesBytes;   // B first (1024-aligned)
     static constexpr uint32_t ACC_COLS = NMAT * 128;      // TMEM columns per accumulator buffer
@@ -79,10 +86,11 @@ struct Geo {
     static constexpr int SA = (512 - ACC_BUFS * ACC_COLS) / A_COLS;   // A ring in TMEM
     static constexpr uint32_t A_TMEM0 = ACC_BUFS * ACC_COLS;
     static constexpr size_t bytes() {
-        return 1024 + (size_t)SR * R_STAGE + 2 * kBN * 4 + (3 * SR + 2 * SA + 4) * 8 + 16;
+        return 1024 + (size_t)SR * R_STAGE + 2 * kBN * 4 + (2 * SR + SA + 4) * 8 + 16;
     }
 };
 static_assert(Geo<true>::SA == 4 && Geo<false>::SA == 8, "TMEM map");
+static_assert(Geo<true>::SA <= Geo<true>::SR && Geo<false>::SA <= Geo<false>::SR, "A slots are freed by the stage barriers");
 
 MW4_DEV uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -120,11 +128,9 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     float* col_scale = reinterpret_cast<float*>(rring + (size_t)SR * GG::R_STAGE);   // [2][kBN]
     uint64_t* bars = reinterpret_cast<uint64_t*>(col_scale + 2 * kBN);
     uint64_t* r_full = bars;
-    uint64_t* r_fullb = bars + SR;
-    uint64_t* r_empty = bars + 2 * SR;
-    uint64_t* a_full = bars + 3 * SR;
-    uint64_t* a_empty = bars + 3 * SR + SA;
-    uint64_t* acc_full = bars + 3 * SR + 2 * SA;
+    uint64_t* r_empty = bars + SR;
+    uint64_t* a_full = bars + 2 * SR;
+    uint64_t* acc_full = bars + 2 * SR + SA;
     uint64_t* acc_empty = acc_full + 2;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_empty + 2);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2) + 1;
@@ -133,12 +139,10 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     if (tid == 0) {
         for (int s = 0; s < SR; ++s) {
             mbar_init(&r_full[s], 1);
-            mbar_init(&r_fullb[s], 64);
             mbar_init(&r_empty[s], 1);
         }
         for (int s = 0; s < SA; ++s) {
             mbar_init(&a_full[s], 128 * NMAT);
-            mbar_init(&a_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -148,39 +152,46 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         fence_mbar_init();
         fence_proxy_async_smem();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 512);
+    if (warp == GG::kMmaWarp) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t taddr = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == GG::kProdWarp) {
+        // ------------------------------------------------------------ TMA producer (warp-uniform)
+        // Per step: the packed codes of each matrix and, for down, the tile's
+        // contiguous B rows of hh (gate/up B rows are gathered by the
+        // dequantisers).
         if (lane == 0) {
             prefetch_tensormap(&map0r);
             prefetch_tensormap(&map0s);
             if (DUAL) { prefetch_tensormap(&map1r); prefetch_tensormap(&map1s); } else prefetch_tensormap(&mapb);
-            int gk = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info(a, t);
-                const CUtensorMap* m0 = ti.sh ? &map0s : &map0r;
-                const CUtensorMap* m1 = ti.sh ? &map1s : &map1r;
-                // the tile's packed codes are one contiguous range per matrix
+        }
+        int gk = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const TileInfo ti = tile_info(a, t);
+            const CUtensorMap* m0 = ti.sh ? &map0s : &map0r;
+            const CUtensorMap* m1 = ti.sh ? &map1s : &map1r;
+            if (lane == 0) {   // the tile's packed codes are one contiguous range per matrix
                 prefetch_l2((ti.sh ? a.c0s : a.c0r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
                 if (DUAL) prefetch_l2((ti.sh ? a.c1s : a.c1r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
                 else prefetch_l2(a.hh_rows + (size_t)ti.p0 * a.K, (uint32_t)ti.nrows * a.K * 2);
-                for (int ks = 0; ks < nK; ++ks, ++gk) {
-                    const int s = gk % SR;
-                    if (!mbar_wait(&r_empty[s], ((gk / SR) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&r_full[s], NMAT * kCodesBytes + (DUAL ? 0 : kTileBytes));
+            }
+            const uint32_t bbytes = DUAL ? 0u : kTileBytes;
+            for (int ks = 0; ks < nK; ++ks, ++gk) {
+                const int s = gk % SR;
+                if (!mbar_wait_warp(&r_empty[s], ((gk / SR) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&r_full[s], NMAT * kCodesBytes + bbytes);
                     tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * (kBK / 8), ti.arow, &r_full[s]);
                     if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * (kBK / 8), ti.arow, &r_full[s]);
                     else tma_load_2d(B_of(s), &mapb, ks * kBK, ti.p0, &r_full[s]);
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == GG::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer (warp-uniform, one lane issues)
         int gk = 0, it = 0;
         bool ok = true;
@@ -194,8 +205,10 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
             const uint32_t dacc = taddr + b * GG::ACC_COLS;
             for (int ks = 0; ks < nK; ++ks, ++gk) {
                 const int sr = gk % SR, sa = gk % SA;
-                ok = mbar_wait_warp(&a_full[sa], (gk / SA) & 1, abort_flag, a.status) &&
-                     mbar_wait_warp(DUAL ? &r_fullb[sr] : &r_full[sr], (gk / SR) & 1, abort_flag, a.status);
+                // a_full certifies both operands: the dequantisers arrive only after
+                // the step's codes (and, for down, its B rows) landed and, for
+                // gate/up, after their own gathered B rows landed
+                ok = mbar_wait_warp(&a_full[sa], (gk / SA) & 1, abort_flag, a.status);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t atm = taddr + GG::A_TMEM0 + sa * GG::A_COLS;
@@ -207,52 +220,9 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         umma_f16_ts_elect(dacc + mat * 128, atm + mat * (kBK / 2) + kk * 8, bdesc0 + 2 * kk, idesc,
                                           (ks | kk) != 0);
                 }
-                umma_commit_elect(&r_empty[sr]);
-                umma_commit_elect(&a_empty[sa]);
+                umma_commit_elect(&r_empty[sr]);   // also frees A slot sa (see the dequantiser)
             }
             if (ok) umma_commit_elect(&acc_full[b]);
-        }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ token-row gather (gate/up)
-        if (DUAL) {
-            const int tb = tid - 64, c = tb & 7;
-            const int lag = 2;   // <= SR - 1
-            int gk = 0, signalled = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const TileInfo ti = tile_info(a, t);
-                int tok[16];
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    const int row = (tb >> 3) + 8 * n;
-                    tok[n] = -1;
-                    if (row < ti.nrows) tok[n] = ti.sh ? ti.r0 + row : a.perm[ti.p0 + row] / a.k;
-                }
-                for (int ks = 0; ks < nK; ++ks, ++gk) {
-                    const int s = gk % SR;
-                    if (!mbar_wait(&r_empty[s], ((gk / SR) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
-                    uint8_t* dst = B_of(s);
-#pragma unroll
-                    for (int n = 0; n < 16; ++n) {
-                        const int row = (tb >> 3) + 8 * n;
-                        if (tok[n] >= 0)
-                            cp_async_16(dst + row * 128 + ((c ^ (row & 7)) << 4),
-                                        a.x16 + (size_t)tok[n] * a.H + ks * kBK + c * 8);
-                    }
-                    cp_async_commit();
-                    if (gk - signalled >= lag) {   // this stage's copies landed: proxy fence, signal
-                        cp_async_wait<2>();
-                        fence_proxy_async_smem();
-                        mbar_arrive(&r_fullb[signalled % SR]);
-                        ++signalled;
-                    }
-                }
-            }
-            cp_async_wait<0>();
-            if (ok) {
-                fence_proxy_async_smem();
-                for (; signalled < gk; ++signalled) mbar_arrive(&r_fullb[signalled % SR]);
-            }
         }
     } else if (warp < GG::kEpiWarp0) {
         // ------------------------------------------------------------ dequantisation: one weight row per thread
@@ -261,6 +231,41 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         const bool chunked = (G % 8) == 0;
         int gk = 0;
         bool ok = true;
+        // gate/up: these threads also gather the B rows (token rows of x16), kGatherAhead
+        // steps ahead of the step they dequantise; thread td copies half of tile row
+        // td/2 (four 16-byte chunks, 128-byte swizzle).  A stage is reused only after
+        // the MMAs of the step SR earlier, signalled on r_empty.
+        constexpr int kGatherAhead = 4;
+        static_assert(kGatherAhead < SR, "the gather must not wait on a stage the MMA still needs");
+        const int grow = td >> 1, gc0 = (td & 1) * 4;
+        int g_t = blockIdx.x, g_ks = 0, g_gk = 0, g_tok = -1;
+        auto g_setup = [&]() {
+            g_tok = -1;
+            if (g_t < ntiles) {
+                const TileInfo tg = tile_info(a, g_t);
+                if (grow < tg.nrows) g_tok = tg.sh ? tg.r0 + grow : a.perm[tg.p0 + grow] / a.k;
+            }
+        };
+        auto gather_step = [&]() -> bool {   // copies of step g_gk (an empty group past the last tile)
+            if (g_t < ntiles) {
+                const int s = g_gk % SR;
+                if (!mbar_wait(&r_empty[s], ((g_gk / SR) & 1) ^ 1, abort_flag, a.status)) return false;
+                if (g_tok >= 0) {
+                    uint8_t* dst = B_of(s) + grow * 128;
+                    const uint16_t* src = a.x16 + (size_t)g_tok * a.H + g_ks * kBK;
+#pragma unroll
+                    for (int c = gc0; c < gc0 + 4; ++c) cp_async_16(dst + ((c ^ (grow & 7)) << 4), src + c * 8);
+                }
+                ++g_gk;
+                if (++g_ks == nK) { g_ks = 0; g_t += gridDim.x; g_setup(); }
+            }
+            cp_async_commit();
+            return true;
+        };
+        if (DUAL) {
+            g_setup();
+            for (int i = 0; i < kGatherAhead && ok; ++i) ok = gather_step();
+        }
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             const TileInfo ti = tile_info(a, t);
             const uint16_t* sp = (mat == 0 ? (ti.sh ? a.s0s : a.s0r) : (ti.sh ? a.s1s : a.s1r)) + (size_t)(ti.arow + row) * G;
@@ -289,31 +294,42 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         s16 = sp[ks];
                         b16 = bp[ks];
                     }
+                    if (DUAL && !(ok = gather_step())) break;   // B rows of step gk + kGatherAhead
                     const int sr = gk % SR, sa = gk % SA;
+                    // A slot sa last served step gk - SA; the commit on r_empty of that
+                    // step's stage fires once its MMAs are done (SA <= SR, so that
+                    // barrier cannot have moved on by a further phase meanwhile)
                     ok = mbar_wait(&r_full[sr], (gk / SR) & 1, abort_flag, a.status) &&
-                         mbar_wait(&a_empty[sa], ((gk / SA) & 1) ^ 1, abort_flag, a.status);
+                         (gk < SA || mbar_wait(&r_empty[(gk - SA) % SR], ((gk - SA) / SR) & 1, abort_flag, a.status));
                     if (!ok) break;
                     const uint8_t* cr = C_of(sr, mat) + row * 32;
-                    const uint4 w0 = *reinterpret_cast<const uint4*>(cr + ((0 ^ sw) << 4));
-                    const uint4 w1 = *reinterpret_cast<const uint4*>(cr + ((1 ^ sw) << 4));
                     const float sf = bf16_bits_to_float((uint16_t)s16);
                     const __half s_h = __float2half_rn(sf), s_h16 = __float2half_rn(sf * 0.0625f);
                     const __half b_h = __float2half_rn(bf16_bits_to_float((uint16_t)b16));
                     const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16);
                     const __half2 b2 = __halves2half2(b_h, b_h);
-                    // this thread's weight row -> its TMEM lane, 32 columns of fp16 pairs
-                    const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                    uint32_t o[32];
+                    tc_fence_after();   // the MMAs that read this A slot have completed
+                    // this thread's weight row -> its TMEM lane, 32 columns of fp16 pairs, in two halves
+                    const uint32_t tdst =
+                        taddr + ((uint32_t)(row & ~31) << 16) + GG::A_TMEM0 + sa * GG::A_COLS + mat * (kBK / 2);
 #pragma unroll
-                    for (int wi = 0; wi < 8; ++wi) {
-                        uint32_t q4[4];
-                        dequant8_f16(words[wi], s2, s2_16, b2, q4);
-                        o[4 * wi] = q4[0]; o[4 * wi + 1] = q4[1]; o[4 * wi + 2] = q4[2]; o[4 * wi + 3] = q4[3];
+                    for (int hlf = 0; hlf < 2; ++hlf) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(cr + ((hlf ^ sw) << 4));
+                        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+                        uint32_t o[16];
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            uint32_t q4[4];
+                            dequant8_f16(words[wi], s2, s2_16, b2, q4);
+                            o[4 * wi] = q4[0]; o[4 * wi + 1] = q4[1]; o[4 * wi + 2] = q4[2]; o[4 * wi + 3] = q4[3];
+                        }
+                        tmem_st16(tdst + 16 * hlf, o);
                     }
-                    tc_fence_after();   // the MMAs that read this A slot have completed (a_empty)
-                    tmem_st32(taddr + ((uint32_t)(row & ~31) << 16) + GG::A_TMEM0 + sa * GG::A_COLS + mat * (kBK / 2),
-                              o);
                     tmem_wait_st();
+                    if (DUAL) {   // this thread's B copies of step gk have landed; hand them to the async proxy
+                        cp_async_wait<kGatherAhead>();
+                        fence_proxy_async_smem();
+                    }
                     tc_fence_before();
                     mbar_arrive(&a_full[sa]);
                     ++gk;
@@ -323,6 +339,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 bq = bqn;
             }
         }
+        if (DUAL) cp_async_wait<0>();   // no copy in flight when the CTA leaves
     } else {
         // ------------------------------------------------------------ epilogue: TMEM -> registers -> global
         const int ew = warp - GG::kEpiWarp0, q = ew & 3, half = ew >> 2;
@@ -347,16 +364,26 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 tmem_ld16(lane_addr + c0, g);
                 if (DUAL) tmem_ld16(lane_addr + 128 + c0, u);
                 tmem_wait_ld();
+                // column n of the tile is grouped row p0 + n: one pointer per chunk, rows
+                // out_cols apart; a full chunk runs without per-element branches
+                uint16_t* op = a.out + (size_t)(ti.p0 + c0) * a.out_cols + ocol;
+                const float* cs = col_scale + b * kBN + c0;
+                bool bad = false;
+                auto emit = [&](int j) {
+                    const float v = DUAL ? silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j])
+                                         : __uint_as_float(g[j]) * cs[j];
+                    bad |= !(fabsf(v) <= 65504.f);
+                    op[(size_t)j * a.out_cols] = __half_as_ushort(__float2half_rn(v));
+                };
+                if (c0 + 16 <= ti.nrows) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int n = c0 + j;
-                    if (n >= ti.nrows) break;
-                    float v;
-                    if (DUAL) v = silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]);
-                    else v = __uint_as_float(g[j]) * col_scale[b * kBN + n];
-                    if (!(fabsf(v) <= 65504.f)) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
-                    a.out[(size_t)(ti.p0 + n) * a.out_cols + ocol] = __half_as_ushort(__float2half_rn(v));
+                    for (int j = 0; j < 16; ++j) emit(j);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (j < ti.nrows - c0) emit(j);
                 }
+                if (bad) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[b]);
@@ -364,7 +391,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(taddr, 512);
+    if (warp == GG::kMmaWarp) tmem_dealloc(taddr, 512);
 }
 
 // out[t] = bf16( sum_j ys[inv[t*k + j]] + ys[T*k + t] ) with ys in fp16 and
@@ -442,6 +469,10 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
               make_map(&msd, U32, 4, L.sh_down.codes, H, I / 8, kBM, kBK / 8, SW32) &&
               make_map(&mh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hh, rows_all, I, kBN, kBK,
                        CU_TENSOR_MAP_SWIZZLE_128B);
+    // x16 rows for tile::gather4: box one row high, 64 columns, 128-byte swizzle
+    CUtensorMap mx;
+    ok = ok && make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x16, (uint64_t)T, H, 1, kBK,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
 
     const size_t sm_gu = Geo<true>::bytes(), sm_dn = Geo<false>::bytes();
@@ -478,7 +509,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     a.out = p.hh; a.K = H; a.rows_e = I; a.out_cols = I;
     // persistent: one CTA per SM (never more CTAs than the largest tile count)
     const int grid_gu = p.max_tiles_gu < nsm ? p.max_tiles_gu : nsm;
-    grouped_w4_gemm_kernel<true><<<grid_gu, Geo<true>::kThreads, sm_gu, st>>>(a, mg, mu, msg, msu, mh);
+    grouped_w4_gemm_kernel<true><<<grid_gu, Geo<true>::kThreads, sm_gu, st>>>(a, mg, mu, msg, msu, mx);
     trace_mark(st, 6);
 
     // down: A = Wd rows (H per expert), K = I, B = hh rows, out = ys [.][H]
