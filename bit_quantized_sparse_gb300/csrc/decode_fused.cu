@@ -14,7 +14,8 @@
 //      through distributed shared memory, and the k+1 cluster sums are
 //      exchanged through global memory (bounded wait: all clusters are
 //      co-resident, one CTA per SM).  Each CTA then selects the top-k.
-//      The shared cluster does not wait: it starts loading its weights at once.
+//      The shared cluster does not wait for the routing: it starts loading its
+//      weights as soon as its own router reads are done.
 //   2. TMA loads the CTA's slices of the packed codes (128-byte swizzle) and
 //      its scales/biases; the gate/up slices are consumed box by box as they
 //      land.
@@ -258,6 +259,25 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     const bool shared_cluster = (slot == k);
     unsigned int* status = &a.ctrl->status;
 
+    // the router's loads go out first: thread (e, half) sums half of this CTA's
+    // slice of the H rows for expert e; its W_r column slice and the matching x
+    // values (the same for the whole warp) land while x is prepared below
+    const int rh0 = (int)((long)G * H / NG), rh1 = (int)((long)(G + 1) * H / NG);
+    const int rnh = rh1 - rh0, rhalf = rnh / 2;
+    const int r_e = tid % E, r_hb = (tid / E) ? rhalf : 0, r_he = (tid / E) ? rnh : rhalf;
+    float rw[32], rx[32];
+    if (tid < 2 * E) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const bool in = r_hb + j < r_he;
+            rw[j] = in ? __ldg(a.router_w + (size_t)(rh0 + r_hb + j) * E + r_e) : 0.f;
+            rx[j] = in ? bf16_bits_to_float(__ldg(a.x + rh0 + r_hb + j)) : 0.f;
+        }
+    }
+    if (tid == 32) {   // the descriptors are fetched once, early, off the critical path
+        prefetch_tensormap(&mg); prefetch_tensormap(&mu); prefetch_tensormap(&md);
+        prefetch_tensormap(&msg); prefetch_tensormap(&msu); prefetch_tensormap(&msd);
+    }
     if (tid == 0) {
         for (int b = 0; b < nbox_gu; ++b) mbar_init(&bar_gu[b], 1);
         mbar_init(bar_dn, 1);
@@ -289,7 +309,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     }
     __syncthreads();
 
-    // ---------------------------------------------------------------- loads of the shared expert start now
+    // ---------------------------------------------------------------- weight loads (routed: after the top-k)
     // called by all 32 lanes of warp 0: lane b issues box b, lanes 16.. the rest
     auto issue_loads = [&](int e) {
         const bool sh = (e >= E);
@@ -319,30 +339,20 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             bulk_load(dsb + RD * (I / 64), (sh ? a.sdb : a.db) + dO, dsz, bar_dn);
         }
     };
-    if (shared_cluster && warp == 0) issue_loads(E);
 
     // ---------------------------------------------------------------- 1. router partial sums
-    {
-        const int h0 = (int)((long)G * H / NG), h1 = (int)((long)(G + 1) * H / NG);
-        float* xs = reinterpret_cast<float*>(hperm);   // the CTA's x slice (hperm is free until step 4)
-        for (int h = h0 + tid; h < h1; h += kFThreads) xs[h - h0] = bf16_bits_to_float(a.x[h]);
-        __syncthreads();
-        // thread (e, half): half of the CTA's rows for expert e; loads issued before the sums
-        const int nh = h1 - h0, half = nh / 2;
-        for (int i = tid; i < 2 * E; i += kFThreads) {
-            const int e = i % E, hb = (i / E) ? half : 0, he = (i / E) ? nh : half;
-            float w[32];
+    if (tid < 2 * E) {
+        float sum = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] = (hb + j < he) ? __ldg(a.router_w + (size_t)(h0 + hb + j) * E + e) : 0.f;
-            float s = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) s = (hb + j < he) ? fmaf(xs[hb + j], w[j], s) : s;
-            if (i / E) logits[e] = s; else part[e] = s;
-        }
-        __syncthreads();
-        for (int e = tid; e < E; e += kFThreads) part[e] += logits[e];
-        __syncthreads();
+        for (int j = 0; j < 32; ++j) sum = fmaf(rx[j], rw[j], sum);
+        (tid / E ? logits : part)[r_e] = sum;
     }
+    __syncthreads();
+    for (int e = tid; e < E; e += kFThreads) part[e] += logits[e];
+    __syncthreads();
+    // the shared expert needs no routing: its loads start once this CTA's router
+    // reads are done, so that they do not delay the exchange everyone waits on
+    if (shared_cluster && warp == 0) issue_loads(E);
     cluster_sync();
     {   // cluster sum of the partials, ranks in order; CTA r reduces experts [r*E/kCS, (r+1)*E/kCS)
         const int e0 = rank * E / kCS, e1 = (rank + 1) * E / kCS;
@@ -412,13 +422,14 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             {
                 __shared__ int32_t idx_s[8];
                 __shared__ float v_s[8];
-                select_topk_block(logits, E, k, idx_s, v_s);
+                __shared__ __align__(16) uint32_t cand[128];
+                select_topk_block(logits, E, k, idx_s, v_s, cand);
                 __syncthreads();
-                if (warp == 0) {   // softmax over the selection (v_s[0] is the largest)
-                    float z = 0.f;
-                    for (int j = 0; j < k; ++j) z += expf(v_s[j] - v_s[0]);
+                if (warp == 0) {   // softmax over the selection (v_s[0] is the largest), one lane per slot
+                    const float ex = lane < k ? expf(v_s[lane] - v_s[0]) : 0.f;
+                    const float z = warp_sum(ex);
                     if (lane < k) {
-                        const float w = expf(v_s[lane] - v_s[0]) / z;
+                        const float w = ex / z;
                         if (lane == slot) { *sel_e = idx_s[lane]; *sel_w = w; }
                         if (G == 0) { a.idx_out[lane] = idx_s[lane]; a.w_out[lane] = w; }
                     }
@@ -573,9 +584,8 @@ static bool codes_map(CUtensorMap* m, const uint32_t* codes, uint64_t rows, uint
 bool decode_fused_supported(const moe_w4_layer& L) {
     if (L.H % 256 || L.I % 256 || L.H / kCS > 256 || L.I / kCS > 256) return false;
     if ((L.I / kCS) % 16 || (L.H / kCS) % 16 || L.H / 256 > 16) return false;
-    if (L.H > 8 * L.I) return false;   // the router's x slice borrows the h buffer
-    if (L.E < 128 || L.E > 256) return false;   // 2 threads per expert in the top-k; partials in 2E floats
-    if (L.H > 64 * kCS * (L.top_k + 1)) return false;   // <= 64 router rows per CTA
+    if (L.E < 128 || L.E > 256 || L.E % 32) return false;   // top-k: E/32 warps sort 32 scores each; 2E floats of partials
+    if (L.H > 64 * kCS * (L.top_k + 1)) return false;   // <= 64 router rows per CTA (32 per thread)
     const FusedSmem s(L.H, L.E, L.I);
     return s.total + 1024 + 256 <= 227 * 1024;   // + static shared memory of the kernel
 }
