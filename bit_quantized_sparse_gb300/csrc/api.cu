@@ -58,7 +58,7 @@ WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     w.dec_w = take(Td * k * 4);
     w.dec_gamma = take(Td * 4);
     w.dec_hh = take(Td * (k + 1) * I * 4);
-    w.dec_cpart = take((k + 1) * E * 4);
+    w.dec_cpart = take((size_t)kFusedClustersPerExpert * (k + 1) * E * 4);
     w.dec_ybuf = take((k + 1) * H * 4);
     w.total = o;
     return w;

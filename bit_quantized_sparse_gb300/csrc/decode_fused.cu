@@ -5,40 +5,50 @@
 // state and traffic" -- gate/up projections fused with the gated activation,
 // the output projection fused with the routing scores and the shared expert.)
 //
-// Grid: (k+1) clusters of kCS CTAs.  Cluster j < k serves the j-th selected
-// expert, cluster k the shared expert.  CTA r of a cluster owns gate/up rows
-// [r*I/kCS, (r+1)*I/kCS) and down rows [r*H/kCS, (r+1)*H/kCS) of its expert.
+// Grid: (k+1) experts x 16 CTAs, in clusters of 4 (one CTA per SM; the host
+// checks that every cluster fits on the GPU at once).  Expert slot j < k is
+// the j-th selected expert, slot k the shared expert.  CTA i (0..15) of an
+// expert owns gate/up rows [i*I/16, (i+1)*I/16) and down rows
+// [i*H/16, (i+1)*H/16) of it.
 //
-//   1. router: every CTA sums x . W_r over its own 1/((k+1) kCS) slice of the
-//      H rows for all E experts; the slices are reduced in each cluster
-//      through distributed shared memory, and the k+1 cluster sums are
-//      exchanged through global memory (bounded wait: all clusters are
-//      co-resident, one CTA per SM).  Each CTA then selects the top-k.
-//      The shared cluster does not wait for the routing: it starts loading its
-//      weights as soon as its own router reads are done.
+//   1. router: every CTA sums x . W_r over its own 1/(16 (k+1)) slice of the H
+//      rows for all E experts (these loads go out first); the 4 slices of a
+//      cluster are added through distributed shared memory, the cluster sums
+//      are published in global memory and, once all are in (bounded wait: all
+//      CTAs are co-resident), every routed CTA adds them in a fixed order and
+//      selects the top-k.  The shared expert does not wait for the routing: it
+//      starts loading its weights as soon as its own router reads are done.
 //   2. TMA loads the CTA's slices of the packed codes (128-byte swizzle) and
 //      its scales/biases; the gate/up slices are consumed box by box as they
 //      land.
 //   3. gate/up GEMV on the tensor cores as a dot-product engine: mma.sync
-//      m16n8k16 with A = bf16(128 + q) built from the codes by one bitwise op
-//      per pair, B = x (exact in bf16), fp32 accumulation per 64-column group;
-//      then w = s*(acc - 128*sum(x)) + b*sum(x).  SwiGLU in fp32.
-//   4. h is exchanged inside the cluster (distributed shared memory).
-//   5. down GEMV the same way with fp16 (1024 + q) x fp16 h, scaled by the
-//      routing weight (or the shared gate), written per expert.
+//      m16n8k16 with fp16 A = 1024 + q (even nibbles) or 1024 + 16 q (odd
+//      nibbles), one bitwise op per pair, and B = x in fp16 with the odd
+//      positions divided by 16; fp32 accumulation per 64-column group, then
+//      s*(acc - 1024*sum(B)) + b*sum(x).  SwiGLU in fp32.
+//   4. h: every CTA publishes its slice of h in global memory; the 16 CTAs of
+//      an expert wait (bounded) until all 16 slices are in and read all of h.
+//   5. down GEMV the same way with h in fp16, scaled by the routing weight
+//      (or the shared gate), written per expert.
 //   6. per block of output rows, the last of the k+1 CTAs to finish adds the
 //      k+1 expert outputs in slot order and writes bf16 out.
-// No step waits on another CTA except the bounded router exchange and the
-// hardware cluster barriers.
+// No step waits on another CTA except the bounded router and h exchanges and
+// the hardware cluster barriers.
 #include "common.cuh"
 #include "internal.h"
 
 namespace mw4 {
 
-constexpr int kCS = 8;          // CTAs per cluster
-constexpr int kFThreads = 512;  // 16 warps
+constexpr int kCS = 4;                                   // CTAs per cluster
+constexpr int kPE = kCS * kFusedClustersPerExpert;       // CTAs per expert (16)
+constexpr int kFThreads = 512;                           // 16 warps
 constexpr int kFWarps = kFThreads / 32;
-constexpr int kMaxSlots = 9;   // k + 1 <= 9
+constexpr int kMaxSlots = 9;                             // k + 1 <= 9
+// control-header words used by the kernel (Ctrl::pad)
+constexpr int kPadRows = 0;                 // [kPE] combine arrivals per block of output rows
+constexpr int kPadDone = kPadRows + kPE;    // row blocks combined
+constexpr int kPadH = kPadDone + 1;         // [k+1] h slices published per expert
+static_assert(kPadH + kMaxSlots <= 62, "control header");
 
 struct FusedArgs {
     const uint16_t* x;          // [H] bf16
@@ -49,7 +59,8 @@ struct FusedArgs {
     const uint16_t* ds; const uint16_t* db;                                             // routed down s, b
     const uint16_t* sgs; const uint16_t* sgb; const uint16_t* sus; const uint16_t* sub; // shared
     const uint16_t* sds; const uint16_t* sdb;
-    float* cpart;               // [k+1][E] cluster partial scores
+    float* cpart;               // [4(k+1)][E] cluster partial scores
+    float* hbuf;                // [k+1][I] h of every expert
     float* ybuf;                // [k+1][H] weighted expert outputs
     int32_t* idx_out;           // [k] (for inspection)
     float* w_out;               // [k]
@@ -61,12 +72,12 @@ struct FusedArgs {
 
 // smem carve-up (byte offsets from a 1024-aligned base), computed on both sides
 struct FusedSmem {
-    uint32_t gcodes, ucodes, dcodes, gsb, usb, dsb, xperm, xsum, part, logits, gsum, usum, hloc, hperm, hsum,
-        red, misc, total;
+    uint32_t gcodes, ucodes, dcodes, gsb, usb, dsb, xperm, xsum, xbs, part, logits, gsum, usum, hperm, hsum,
+        hbs, red, misc, total;
     int RG, RD;
     __host__ __device__ FusedSmem(int H, int E, int I) {
-        RG = I / kCS;
-        RD = H / kCS;
+        RG = I / kPE;
+        RD = H / kPE;
         uint32_t o = 0;
         auto take = [&](uint32_t bytes, uint32_t align) {
             o = (o + align - 1) / align * align;
@@ -82,13 +93,14 @@ struct FusedSmem {
         dsb = take(2 * RD * (I / 64) * 2, 16);
         xperm = take(H * 2, 16);
         xsum = take(H / 64 * 4, 16);
+        xbs = take(H / 64 * 4, 16);
         part = take(E * 4, 16);
         logits = take(E * 4, 16);
         gsum = take(RG * 4, 16);
         usum = take(RG * 4, 16);
-        hloc = take(RG * 4, 16);
         hperm = take(I * 2, 16);
         hsum = take(I / 64 * 4, 16);
+        hbs = take(I / 64 * 4, 16);
         red = part;   // K-split partials reuse the score buffers (part, logits: 2E floats) after routing
         misc = take(256, 16);
         total = o;
@@ -123,13 +135,6 @@ MW4_DEV uint32_t ld_acquire_u32(const unsigned int* p) {
 }
 
 // --------------------------------------------------------------------------- legacy-MMA dot engine
-MW4_DEV void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 MW4_DEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -146,15 +151,16 @@ MW4_DEV uint32_t sw_word(const uint8_t* base, int rows, int row, int wi) {
                                               w * 4);
 }
 
-// One warp: rows [r0, r0+16) of a swizzled codes tile set, 64-column groups
-// [grp0, grp1); B fragments from `bperm` (16 bytes per (32-column block,
-// lane%4)), column sums `gsum` (per 64 columns), scale/bias tables
-// [rows][ngrp_row].  Adds the dot products of rows r0+g and r0+g+8 (g =
-// lane/4) to acc0/acc1.  Two groups are in flight at a time so that the
-// chained MMAs of one group overlap the other's.
-MW4_DEV void w4_group_mma(const uint8_t* codes, int rows, int r0, int grp, const uint4* bperm, uint32_t magic,
-                          bool f16, float (&d)[4]) {
+// One warp: rows [r0, r0+16) of a swizzled codes tile set, one 64-column
+// group; adds the group's dot products of rows r0+g and r0+g+8 (g = lane/4)
+// to d[0] and d[2].  A holds fp16 1024 + q for the even nibbles of a code
+// byte and 1024 + 16 q for the odd ones (one bitwise op per pair, one shift
+// per word); B (`bperm`, 16 bytes per (32-column block, lane%4)) holds the
+// matching activations, the odd positions divided by 16, so that every
+// product is q * value + 1024 * (stored B value).
+MW4_DEV void w4_group_mma(const uint8_t* codes, int rows, int r0, int grp, const uint4* bperm, float (&d)[4]) {
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    constexpr uint32_t M = 0x64006400u;
     // both rows of the thread (r0+g, r0+g+8) share the swizzle phase g; a group
     // (2 blocks of 32 columns) lies inside one box of 8 blocks
     const int blk0 = grp * 2;
@@ -168,26 +174,28 @@ MW4_DEV void w4_group_mma(const uint8_t* codes, int rows, int r0, int grp, const
         const uint32_t wh = *reinterpret_cast<const uint32_t*>(row1 + off);
         const uint4 bv = bperm[blk * 4 + c];
         uint32_t a[4];
-        a[0] = (wg & 0x000F000Fu) | magic;
-        a[1] = (wh & 0x000F000Fu) | magic;
-        a[2] = ((wg >> 4) & 0x000F000Fu) | magic;
-        a[3] = ((wh >> 4) & 0x000F000Fu) | magic;
-        if (f16) mma_f16_16816(d, a, bv.x, bv.y); else mma_bf16_16816(d, a, bv.x, bv.y);
-        a[0] = ((wg >> 8) & 0x000F000Fu) | magic;
-        a[1] = ((wh >> 8) & 0x000F000Fu) | magic;
-        a[2] = ((wg >> 12) & 0x000F000Fu) | magic;
-        a[3] = ((wh >> 12) & 0x000F000Fu) | magic;
-        if (f16) mma_f16_16816(d, a, bv.z, bv.w); else mma_bf16_16816(d, a, bv.z, bv.w);
+        a[0] = (wg & 0x000F000Fu) | M;   // nibbles 0, 4
+        a[1] = (wh & 0x000F000Fu) | M;
+        a[2] = (wg & 0x00F000F0u) | M;   // nibbles 1, 5 (x16)
+        a[3] = (wh & 0x00F000F0u) | M;
+        mma_f16_16816(d, a, bv.x, bv.y);
+        const uint32_t wg8 = wg >> 8, wh8 = wh >> 8;
+        a[0] = (wg8 & 0x000F000Fu) | M;  // nibbles 2, 6
+        a[1] = (wh8 & 0x000F000Fu) | M;
+        a[2] = (wg8 & 0x00F000F0u) | M;  // nibbles 3, 7 (x16)
+        a[3] = (wh8 & 0x00F000F0u) | M;
+        mma_f16_16816(d, a, bv.z, bv.w);
     }
 }
 
-template <bool F16>
+// Rows r0+g and r0+g+8 dotted with the activation over groups [grp0, grp1):
+// per group w = s*q + b, so the dot is s * (sum of q*value) + b * (sum of
+// values); `bsum` holds per-group sums of the stored B values (for the 1024
+// offset), `tsum` the true sums of the activation.
 MW4_DEV bool w4_gemv16(const uint8_t* codes, int rows, int r0, int grp0, int grp1, const uint4* bperm,
-                       const float* gsum, const uint16_t* sc, const uint16_t* bi, int ngrp_row, float& acc0,
-                       float& acc1, uint64_t* box_bars, volatile int* abort_flag, unsigned int* status) {
+                       const float* bsum, const float* tsum, const uint16_t* sc, const uint16_t* bi, int ngrp_row,
+                       float& acc0, float& acc1, uint64_t* box_bars, volatile int* abort_flag, unsigned int* status) {
     const int lane = threadIdx.x & 31, g = lane >> 2;
-    const uint32_t magic = F16 ? 0x64006400u : 0x43004300u;
-    const float offs = F16 ? 1024.f : 128.f;
     constexpr int kIn = 4;   // groups in flight: independent MMA chains
     for (int grp = grp0; grp < grp1; grp += kIn) {
         if (box_bars) {   // 4 groups (256 columns) per TMA box
@@ -199,20 +207,20 @@ MW4_DEV bool w4_gemv16(const uint8_t* codes, int rows, int r0, int grp0, int grp
 #pragma unroll
         for (int q = 0; q < kIn; ++q) {
             d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
-            if (grp + q < grp1) w4_group_mma(codes, rows, r0, grp + q, bperm, magic, F16, d[q]);
+            if (grp + q < grp1) w4_group_mma(codes, rows, r0, grp + q, bperm, d[q]);
         }
         // every lane of a row group holds the same column sums (B is the same for all n)
 #pragma unroll
         for (int q = 0; q < kIn; ++q) {
             const int gg = grp + q;
             if (gg >= grp1) break;
-            const float xs = gsum[gg];
+            const float bs = bsum[gg], xs = tsum[gg];
             const float s0 = bf16_bits_to_float(sc[(r0 + g) * ngrp_row + gg]);
             const float b0 = bf16_bits_to_float(bi[(r0 + g) * ngrp_row + gg]);
             const float s1 = bf16_bits_to_float(sc[(r0 + g + 8) * ngrp_row + gg]);
             const float b1 = bf16_bits_to_float(bi[(r0 + g + 8) * ngrp_row + gg]);
-            acc0 = fmaf(s0, d[q][0] - offs * xs, fmaf(b0, xs, acc0));
-            acc1 = fmaf(s1, d[q][2] - offs * xs, fmaf(b1, xs, acc1));
+            acc0 = fmaf(s0, d[q][0] - 1024.f * bs, fmaf(b0, xs, acc0));
+            acc1 = fmaf(s1, d[q][2] - 1024.f * bs, fmaf(b1, xs, acc1));
         }
     }
     return true;
@@ -236,13 +244,14 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     uint16_t* dsb = reinterpret_cast<uint16_t*>(sm + L.dsb);
     uint32_t* xperm = reinterpret_cast<uint32_t*>(sm + L.xperm);
     float* xsum = reinterpret_cast<float*>(sm + L.xsum);
+    float* xbs = reinterpret_cast<float*>(sm + L.xbs);
     float* part = reinterpret_cast<float*>(sm + L.part);
     float* logits = reinterpret_cast<float*>(sm + L.logits);
     float* gsum = reinterpret_cast<float*>(sm + L.gsum);
     float* usum = reinterpret_cast<float*>(sm + L.usum);
-    float* hloc = reinterpret_cast<float*>(sm + L.hloc);
     uint32_t* hperm = reinterpret_cast<uint32_t*>(sm + L.hperm);
     float* hsum = reinterpret_cast<float*>(sm + L.hsum);
+    float* hbs = reinterpret_cast<float*>(sm + L.hbs);
     float* red = reinterpret_cast<float*>(sm + L.red);
     uint8_t* misc = sm + L.misc;
     const int nbox_gu = H / 256, nbox_dn = I / 256 > 0 ? I / 256 : 1;
@@ -254,8 +263,11 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     int* last_flag = reinterpret_cast<int*>(sel_e + 2);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rank = (int)cluster_rank(), slot = (int)cluster_id();
-    const int NC = k + 1, NG = NC * kCS, G = slot * kCS + rank;
+    // clusters are consecutive blocks: expert slot = block / kPE, CTA ei of the
+    // expert = block % kPE; cluster cid, rank inside the cluster for DSMEM
+    const int rank = (int)cluster_rank(), cid = (int)cluster_id();
+    const int G = blockIdx.x, slot = G / kPE, ei = G % kPE;
+    const int NC = k + 1, NG = NC * kPE, NCL = NC * kFusedClustersPerExpert;
     const bool shared_cluster = (slot == k);
     unsigned int* status = &a.ctrl->status;
 
@@ -284,28 +296,44 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // x as permuted bf16 pairs for the B fragments, and per-64-column sums
-    // (block of 32 columns, lane%4 = c): {x[8c], x[8c+4]}, {x[8c+1], x[8c+5]},
-    // {x[8c+2], x[8c+6]}, {x[8c+3], x[8c+7]}
+    // x as fp16 B fragments, one thread per 16-byte entry: entry i (32-column
+    // block i/4, lane%4 = i%4) holds {x[8i], x[8i+4]}, {x[8i+1], x[8i+5]}/16,
+    // {x[8i+2], x[8i+6]}, {x[8i+3], x[8i+7]}/16; plus the per-64-column group
+    // sums of the stored values (xbs) and of the values the products use
+    // (xsum), reduced over the 8 lanes of a group (H/8 is a multiple of 32, so
+    // the loop runs whole warps)
     for (int i = tid; i < H / 8; i += kFThreads) {
         const uint4 v = *reinterpret_cast<const uint4*>(a.x + i * 8);
         const uint32_t e[4] = {v.x, v.y, v.z, v.w};   // pairs (0,1) (2,3) (4,5) (6,7)
-        const uint32_t q0 = __byte_perm(e[0], e[2], 0x5410), q1 = __byte_perm(e[0], e[2], 0x7632);
-        const uint32_t q2 = __byte_perm(e[1], e[3], 0x5410), q3 = __byte_perm(e[1], e[3], 0x7632);
-        uint4* dst = reinterpret_cast<uint4*>(xperm) + i;   // i = blk*4 + c
-        *dst = make_uint4(q0, q1, q2, q3);
-    }
-    __syncthreads();
-    for (int gi = tid; gi < H / 64; gi += kFThreads) {   // 64 columns = 8 permuted 16-byte entries
-        float sx = 0.f;
+        float f[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint4 q = reinterpret_cast<const uint4*>(xperm)[gi * 8 + i];
-            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) sx += __uint_as_float(u[j] << 16) + __uint_as_float(u[j] & 0xFFFF0000u);
+        for (int j = 0; j < 4; ++j) {
+            f[2 * j] = __uint_as_float(e[j] << 16);
+            f[2 * j + 1] = __uint_as_float(e[j] & 0xFFFF0000u);
         }
-        xsum[gi] = sx;
+        float sb = 0.f, so = 0.f;   // sums of the stored even / odd entries
+        bool bad = false;
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float m = (j & 1) ? 0.0625f : 1.0f;
+            bad |= !(fabsf(f[j]) <= 65504.f) || !(fabsf(f[j + 4]) <= 65504.f);
+            const __half2 h2 = __floats2half2_rn(f[j] * m, f[j + 4] * m);
+            q[j] = h2_as_u32(h2);
+            const float2 back = __half22float2(h2);
+            if (j & 1) so += back.x + back.y; else sb += back.x + back.y;
+        }
+        reinterpret_cast<uint4*>(xperm)[i] = make_uint4(q[0], q[1], q[2], q[3]);
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) {
+            sb += __shfl_xor_sync(0xffffffffu, sb, off);
+            so += __shfl_xor_sync(0xffffffffu, so, off);
+        }
+        if ((i & 7) == 0) {
+            xbs[i / 8] = sb + so;
+            xsum[i / 8] = sb + 16.f * so;
+        }
+        if (bad) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
     }
     __syncthreads();
 
@@ -316,8 +344,8 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         const CUtensorMap* MG = sh ? &msg : &mg;
         const CUtensorMap* MU = sh ? &msu : &mu;
         const CUtensorMap* MD = sh ? &msd : &md;
-        const int grow = (sh ? 0 : e * I) + rank * RG;
-        const int drow = (sh ? 0 : e * H) + rank * RD;
+        const int grow = (sh ? 0 : e * I) + ei * RG;
+        const int drow = (sh ? 0 : e * H) + ei * RD;
         const uint32_t gsz = RG * (H / 64) * 2, dsz = RD * (I / 64) * 2;
         const size_t go = (size_t)grow * (H / 64), dO = (size_t)drow * (I / 64);
         if (lane < nbox_gu) {
@@ -350,9 +378,6 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     __syncthreads();
     for (int e = tid; e < E; e += kFThreads) part[e] += logits[e];
     __syncthreads();
-    // the shared expert needs no routing: its loads start once this CTA's router
-    // reads are done, so that they do not delay the exchange everyone waits on
-    if (shared_cluster && warp == 0) issue_loads(E);
     cluster_sync();
     {   // cluster sum of the partials, ranks in order; CTA r reduces experts [r*E/kCS, (r+1)*E/kCS)
         const int e0 = rank * E / kCS, e1 = (rank + 1) * E / kCS;
@@ -363,11 +388,14 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             float s = 0.f;
 #pragma unroll
             for (int r = 0; r < kCS; ++r) s += v[r];
-            a.cpart[(size_t)slot * E + e] = s;
+            a.cpart[(size_t)cid * E + e] = s;
         }
         __syncthreads();
         if (tid == 0) atomic_add_release_gpu(&a.ctrl->decode_counter, 1u);
     }
+    // the shared expert needs no routing: its loads start once its router sums are
+    // published, so that issuing them does not delay the exchange everyone waits on
+    if (shared_cluster && warp == 0) issue_loads(E);
     cluster_sync();   // every peer has read this CTA's partials; the buffers may be reused
     if (shared_cluster) {   // the shared cluster's gate sigmoid(x . g), all threads
         float d = 0.f;
@@ -391,7 +419,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             for (int w = 0; w < kFWarps; ++w) t += gsum[w];
             *sel_w = 1.0f / (1.0f + expf(-t));
             *sel_e = E;
-            if (rank == 0) *a.gamma_out = *sel_w;
+            if (ei == 0) *a.gamma_out = *sel_w;
         }
     }
     if (!shared_cluster) {
@@ -409,13 +437,14 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         }
         __syncthreads();
         if (!*abort_flag) {
-            for (int e = tid; e < E; e += kFThreads) {
-                float v[kMaxSlots];
+            for (int e = tid; e < E; e += kFThreads) {   // cluster sums added in cluster order, all loads in flight
+                constexpr int kMaxCl = kMaxSlots * kFusedClustersPerExpert;
+                float v[kMaxCl];
 #pragma unroll
-                for (int j = 0; j < kMaxSlots; ++j) v[j] = (j < NC) ? __ldcg(a.cpart + (size_t)j * E + e) : 0.f;
+                for (int j = 0; j < kMaxCl; ++j) v[j] = (j < NCL) ? __ldcg(a.cpart + (size_t)j * E + e) : 0.f;
                 float s = 0.f;
 #pragma unroll
-                for (int j = 0; j < kMaxSlots; ++j) s += v[j];
+                for (int j = 0; j < kMaxCl; ++j) s += v[j];
                 logits[e] = s + (a.router_bias ? a.router_bias[e] : 0.f);
             }
             __syncthreads();
@@ -448,7 +477,9 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
 
     // ---------------------------------------------------------------- 3. gate/up GEMV
     // 2*RG/16 row tiles (gate, then up) x KS splits of the 64-column groups
-    if (run && mbar_wait(&bar_gu[0], 0, abort_flag, status)) {   // box 0 also carries the scales/biases
+    // box 0 also carries the scales/biases; the block agrees on the outcome of the wait
+    const bool gu_ok = __syncthreads_and(run ? mbar_wait(&bar_gu[0], 0, abort_flag, status) : 0);
+    if (gu_ok) {
         const int ntile = 2 * (RG / 16), KS = kFWarps / ntile > 0 ? kFWarps / ntile : 1, ngrp = H / 64;
         for (int task = warp; task < ntile * KS; task += kFWarps) {
             const int t = task / KS, ks = task % KS;
@@ -456,9 +487,9 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             const int r0 = (up ? t - ntile / 2 : t) * 16;
             const uint16_t* sb = up ? usb : gsb;
             float acc0 = 0.f, acc1 = 0.f;
-            w4_gemv16<false>(up ? ucodes : gcodes, RG, r0, ks * ngrp / KS, (ks + 1) * ngrp / KS,
-                             reinterpret_cast<const uint4*>(xperm), xsum, sb, sb + RG * (H / 64), H / 64, acc0,
-                             acc1, bar_gu, abort_flag, status);
+            w4_gemv16(up ? ucodes : gcodes, RG, r0, ks * ngrp / KS, (ks + 1) * ngrp / KS,
+                      reinterpret_cast<const uint4*>(xperm), xbs, xsum, sb, sb + RG * (H / 64), H / 64, acc0, acc1,
+                      bar_gu, abort_flag, status);
             if ((lane & 3) == 0) {
                 red[task * 16 + (lane >> 2)] = acc0;
                 red[task * 16 + (lane >> 2) + 8] = acc1;
@@ -473,62 +504,91 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         }
     }
     __syncthreads();
-    if (run)
-        for (int i = tid; i < RG; i += kFThreads) hloc[i] = silu_f(gsum[i]) * usum[i];
-    // ---------------------------------------------------------------- 4. exchange h inside the cluster
-    cluster_sync();
-    if (run) {
-        // fp16 B fragments of h, permuted like x, and per-64-column sums
-        for (int i = tid; i < I / 8; i += kFThreads) {
-            float v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int col = i * 8 + j;
-                v[j] = ld_dsmem_f32(hloc + (col % RG), col / RG);
+    // ---------------------------------------------------------------- 4. h through global memory
+    if (gu_ok)
+        for (int i = tid; i < RG; i += kFThreads) a.hbuf[(size_t)slot * I + ei * RG + i] = silu_f(gsum[i]) * usum[i];
+    __syncthreads();
+    if (tid == 0) {
+        // published even after an abort, so that no CTA of the expert waits in vain
+        atomic_add_release_gpu(&a.ctrl->pad[kPadH + slot], 1u);
+        if (gu_ok) {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_u32(&a.ctrl->pad[kPadH + slot]) < (uint32_t)kPE) {
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
             }
-            const uint32_t q0 = h2_as_u32(__floats2half2_rn(v[0], v[4])), q1 = h2_as_u32(__floats2half2_rn(v[1], v[5]));
-            const uint32_t q2 = h2_as_u32(__floats2half2_rn(v[2], v[6])), q3 = h2_as_u32(__floats2half2_rn(v[3], v[7]));
+        }
+    }
+    __syncthreads();
+    const bool h_ok = gu_ok && !*abort_flag;
+    if (h_ok) {
+        // fp16 B fragments of h, laid out like x (odd entries divided by 16)
+        for (int i = tid; i < I / 8; i += kFThreads) {
+            const float* src = a.hbuf + (size_t)slot * I + i * 8;
+            const float4 v0 = __ldcg(reinterpret_cast<const float4*>(src));
+            const float4 v1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            bool bad = false;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) bad |= !(fabsf(v[j]) <= 65504.f);
+            if (bad) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
+            const uint32_t q0 = h2_as_u32(__floats2half2_rn(v[0], v[4]));
+            const uint32_t q1 = h2_as_u32(__floats2half2_rn(v[1] * 0.0625f, v[5] * 0.0625f));
+            const uint32_t q2 = h2_as_u32(__floats2half2_rn(v[2], v[6]));
+            const uint32_t q3 = h2_as_u32(__floats2half2_rn(v[3] * 0.0625f, v[7] * 0.0625f));
             reinterpret_cast<uint4*>(hperm)[i] = make_uint4(q0, q1, q2, q3);
         }
     }
-    cluster_sync();   // peers may leave once everyone has read their h
-    if (run) {
+    __syncthreads();
+    if (h_ok) {
         for (int gi = tid; gi < I / 64; gi += kFThreads) {
-            float s = 0.f;
+            float sb = 0.f, so = 0.f;
             for (int i = gi * 8; i < gi * 8 + 8; ++i) {
                 const uint4 q = reinterpret_cast<const uint4*>(hperm)[i];
                 const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float2 f = __half22float2(u32_as_h2(u[j]));
-                    s += f.x + f.y;
+                    if (j & 1) so += f.x + f.y; else sb += f.x + f.y;
                 }
             }
-            hsum[gi] = s;
+            hbs[gi] = sb + so;
+            hsum[gi] = sb + 16.f * so;
         }
     }
-    __syncthreads();
     // ---------------------------------------------------------------- 5. down GEMV
-    if (run && mbar_wait(bar_dn, 0, abort_flag, status)) {
-        const int ntile = RD / 16;
-        const float wsel = *sel_w;
-        for (int t = warp; t < ntile; t += kFWarps) {
+    // RD/16 row tiles x KS splits of the 64-column groups
+    const bool dn_ok = __syncthreads_and(h_ok ? mbar_wait(bar_dn, 0, abort_flag, status) : 0);
+    if (dn_ok) {
+        const int ntile = RD / 16, KS = kFWarps / ntile > 0 ? kFWarps / ntile : 1, ngrp = I / 64;
+        for (int task = warp; task < ntile * KS; task += kFWarps) {
+            const int t = task / KS, ks = task % KS;
             float acc0 = 0.f, acc1 = 0.f;
-            w4_gemv16<true>(dcodes, RD, t * 16, 0, I / 64, reinterpret_cast<const uint4*>(hperm), hsum, dsb,
-                            dsb + RD * (I / 64), I / 64, acc0, acc1, nullptr, abort_flag, status);
+            w4_gemv16(dcodes, RD, t * 16, ks * ngrp / KS, (ks + 1) * ngrp / KS, reinterpret_cast<const uint4*>(hperm),
+                      hbs, hsum, dsb, dsb + RD * (I / 64), I / 64, acc0, acc1, nullptr, abort_flag, status);
             if ((lane & 3) == 0) {
-                const int o = rank * RD + t * 16 + (lane >> 2);
-                a.ybuf[(size_t)slot * H + o] = acc0 * wsel;
-                a.ybuf[(size_t)slot * H + o + 8] = acc1 * wsel;
+                red[task * 16 + (lane >> 2)] = acc0;
+                red[task * 16 + (lane >> 2) + 8] = acc1;
             }
+        }
+        __syncthreads();
+        const float wsel = *sel_w;
+        for (int i = tid; i < RD; i += kFThreads) {   // sum the K splits in order
+            const int t = i / 16, r = i % 16;
+            float v = 0.f;
+            for (int ks = 0; ks < KS; ++ks) v += red[(t * KS + ks) * 16 + r];
+            a.ybuf[(size_t)slot * H + ei * RD + i] = v * wsel;
         }
     }
     // ---------------------------------------------------------------- 6. combine: last of the k+1 CTAs per row block
     __syncthreads();
-    if (tid == 0) *last_flag = (atomic_add_acq_rel_gpu(&a.ctrl->pad[rank], 1u) == (unsigned)(NC - 1));
+    if (tid == 0) *last_flag = (atomic_add_acq_rel_gpu(&a.ctrl->pad[kPadRows + ei], 1u) == (unsigned)(NC - 1));
     __syncthreads();
     if (*last_flag) {
-        for (int o = rank * RD + tid; o < (rank + 1) * RD; o += kFThreads) {
+        for (int o = ei * RD + tid; o < (ei + 1) * RD; o += kFThreads) {
             float v[kMaxSlots];
 #pragma unroll
             for (int j = 0; j < kMaxSlots; ++j) v[j] = (j < NC) ? __ldcg(a.ybuf + (size_t)j * H + o) : 0.f;
@@ -539,11 +599,13 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         }
         __syncthreads();
         if (tid == 0) {
-            a.ctrl->pad[rank] = 0;
-            // the last row block to finish resets the exchange counter for the next call
-            if (atomicAdd(&a.ctrl->pad[kCS], 1u) == (unsigned)(kCS - 1)) {
+            a.ctrl->pad[kPadRows + ei] = 0;
+            // the last row block to finish resets the exchange counters for the next
+            // call: by then every CTA has passed both exchanges
+            if (atomicAdd(&a.ctrl->pad[kPadDone], 1u) == (unsigned)(kPE - 1)) {
                 a.ctrl->decode_counter = 0;
-                a.ctrl->pad[kCS] = 0;
+                for (int j = 0; j < NC; ++j) a.ctrl->pad[kPadH + j] = 0;
+                a.ctrl->pad[kPadDone] = 0;
             }
         }
     }
@@ -581,23 +643,64 @@ static bool codes_map(CUtensorMap* m, const uint32_t* codes, uint64_t rows, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool decode_fused_supported(const moe_w4_layer& L) {
-    if (L.H % 256 || L.I % 256 || L.H / kCS > 256 || L.I / kCS > 256) return false;
-    if ((L.I / kCS) % 16 || (L.H / kCS) % 16 || L.H / 256 > 16) return false;
+static bool shape_ok(const moe_w4_layer& L) {
+    if (L.H % 256 || L.I % 256 || L.H > 4096 || L.I > 2048) return false;   // slices of 16 rows; <= 16 row tiles
+    if (L.H / 256 > 16) return false;                                         // gate/up box barriers
     if (L.E < 128 || L.E > 256 || L.E % 32) return false;   // top-k: E/32 warps sort 32 scores each; 2E floats of partials
-    if (L.H > 64 * kCS * (L.top_k + 1)) return false;   // <= 64 router rows per CTA (32 per thread)
+    if (L.top_k + 1 > kMaxSlots) return false;
+    if (L.H > 64 * kPE * (L.top_k + 1)) return false;   // <= 64 router rows per CTA (32 per thread)
     const FusedSmem s(L.H, L.E, L.I);
-    return s.total + 1024 + 256 <= 227 * 1024;   // + static shared memory of the kernel
+    return s.total + 1024 + 1024 <= 227 * 1024;   // + static shared memory of the kernel
 }
 
-size_t decode_fused_scratch(const moe_w4_layer& L) {
-    return ((size_t)(L.top_k + 1) * L.E + (size_t)(L.top_k + 1) * L.H) * 4;
+static size_t fused_smem(const moe_w4_layer& L) { return FusedSmem(L.H, L.E, L.I).total + 1024; }
+
+static cudaLaunchConfig_t fused_config(const moe_w4_layer& L, cudaLaunchAttribute* attr, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((L.top_k + 1) * kPE);
+    cfg.blockDim = dim3(kFThreads);
+    cfg.dynamicSmemBytes = fused_smem(L);
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+// The kernel's exchanges wait on other CTAs, so every cluster must be resident
+// at once: the answer of the occupancy calculator is checked (and cached per
+// device and launch shape) before the fused path is taken.
+bool decode_fused_supported(const moe_w4_layer& L) {
+    if (!shape_ok(L)) return false;
+    struct Entry { int dev, k; size_t smem; bool ok; };
+    static Entry cache[16] = {};
+    static int ncache = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const size_t smem = fused_smem(L);
+    for (int i = 0; i < ncache; ++i)
+        if (cache[i].dev == dev && cache[i].k == L.top_k && cache[i].smem == smem) return cache[i].ok;
+    bool ok = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+              cudaSuccess;
+    if (ok) {
+        cudaLaunchAttribute attr[1];
+        const cudaLaunchConfig_t cfg = fused_config(L, attr, nullptr);
+        int nclusters = 0;
+        ok = cudaOccupancyMaxActiveClusters(&nclusters, (void*)decode_fused_kernel, &cfg) == cudaSuccess &&
+             nclusters >= (L.top_k + 1) * kFusedClustersPerExpert;
+    }
+    cudaGetLastError();   // a refused query leaves no sticky error behind
+    if (ncache < 16) cache[ncache++] = Entry{dev, L.top_k, smem, ok};
+    return ok;
 }
 
 cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                                 cudaStream_t st) {
     const int H = L.H, E = L.E, I = L.I, k = L.top_k;
-    const int RG = I / kCS, RD = H / kCS;
+    const int RG = I / kPE, RD = H / kPE;
     CUtensorMap mg, mu, md, msg, msu, msd;
     bool ok = codes_map(&mg, L.gate.codes, (uint64_t)E * I, H, RG) && codes_map(&mu, L.up.codes, (uint64_t)E * I, H, RG) &&
               codes_map(&md, L.down.codes, (uint64_t)E * H, I, RD) && codes_map(&msg, L.sh_gate.codes, I, H, RG) &&
@@ -609,34 +712,12 @@ cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16
     a.ds = L.down.scales; a.db = L.down.biases;
     a.sgs = L.sh_gate.scales; a.sgb = L.sh_gate.biases; a.sus = L.sh_up.scales; a.sub = L.sh_up.biases;
     a.sds = L.sh_down.scales; a.sdb = L.sh_down.biases;
-    a.cpart = d.fused_cpart; a.ybuf = d.fused_ybuf;
+    a.cpart = d.fused_cpart; a.hbuf = d.hh; a.ybuf = d.fused_ybuf;
     a.idx_out = d.idx; a.w_out = d.w; a.gamma_out = d.gamma; a.out = out;
     a.ctrl = d.ctrl;
     a.H = H; a.E = E; a.I = I; a.k = k;
-    const FusedSmem s(H, E, I);
-    const size_t smem = s.total + 1024;
-    static size_t attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (attr_set[dev] < smem) {   // dynamic + static shared memory must stay within the opt-in limit
-        const cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = smem;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((k + 1) * kCS);
-    cfg.blockDim = dim3(kFThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const cudaLaunchConfig_t cfg = fused_config(L, attr, st);   // shared memory opt-in set by the support check
     return cudaLaunchKernelEx(&cfg, decode_fused_kernel, a, mg, mu, md, msg, msu, msd);
 }
 

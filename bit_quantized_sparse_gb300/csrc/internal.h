@@ -16,6 +16,7 @@ constexpr int kBM = 128;          // weight rows per tensor-core tile
 constexpr int kBN = 128;          // token rows per tensor-core tile
 constexpr int kBK = 64;           // reduction columns per pipeline stage (= one group)
 constexpr int kDecodeMaxT = 16;   // largest decode batch
+constexpr int kFusedClustersPerExpert = 4;   // fused T=1 decode: 16 CTAs per expert in clusters of 4
 constexpr int kRouterRowsPerCta = 256;  // H rows per decode-router CTA
 
 struct Tile { int e, m, r0, nrows; };
@@ -67,8 +68,9 @@ struct DecodeWs {
     unsigned int* counter;
     unsigned int* status;
     Ctrl* ctrl;         // control header (counters of the fused kernel)
-    float* fused_cpart; // [k+1][E] cluster partial scores (fused T=1 kernel)
-    float* fused_ybuf;  // [k+1][H] weighted expert outputs (fused T=1 kernel)
+    float* fused_cpart; // [kFusedClustersPerExpert*(k+1)][E] cluster partial scores (fused T=1 kernel)
+    float* fused_ybuf;  // [k+1][H] weighted expert outputs (fused T=1 kernel); the fused kernel
+                        // exchanges h through hh ([k+1][I] at T=1)
 };
 bool decode_fused_supported(const moe_w4_layer& L);
 cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,

@@ -44,7 +44,7 @@ static NoallocLayout noalloc_layout(const moe_w4_layer& L, int T) {
     n.w = take(Tz * k * 4);
     n.gamma = take(Tz * 4);
     n.hh = take(Tz * (k + 1) * I * 4);
-    n.cpart = take((k + 1) * E * 4);
+    n.cpart = take((size_t)kFusedClustersPerExpert * (k + 1) * E * 4);
     n.ybuf = take((k + 1) * H * 4);
     n.total = o;
     return n;
