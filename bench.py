@@ -109,6 +109,28 @@ def peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary table
+    (profiles/traffic.md), or None when the kernel's source files have changed
+    since that capture (their sha256 no longer matches) or it was never captured."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) < 4 or cells[0] != kernel:
+            continue
+        h = hashlib.sha256()
+        for f in cells[1].split():
+            fp = os.path.join(ROOT, "bit_quantized_sparse_gb300", f)
+            if not os.path.exists(fp):
+                return None
+            h.update(open(fp, "rb").read())
+        return int(cells[3]) if h.hexdigest() == cells[2] else None
+    return None
+
+
 class ClockSampler:
     """nvidia-smi sampled every 200 ms while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -402,15 +424,20 @@ def main():
     if dom[1] in ("gemm_gate_up", "gemm_down"):
         f = gemm_flops(c, chunk, "gate_up" if dom[1] == "gemm_gate_up" else "down")
         ach = f / t_dom / 1e12
+        gk = "grouped_w4_gemm_kernel<1>" if dom[1] == "gemm_gate_up" else "grouped_w4_gemm_kernel<0>"
         roof = {"kernel": dom[1], "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": None,
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": measured_traffic(gk),
                 "work_per_launch": f"{f:.4e} FLOP (fp16 operands, fp32 accumulate)",
                 "peak_note": f"dense bf16 sustained, {pk['source']}; fp16 has the same nominal rate"}
     else:
         b = decode_bytes(c)
         ach = b / sum(r["k_dec"].values()) / 1e9
-        roof = {"kernel": "decode step", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / pk["hbm_gbs"], "traffic": None}
+        fused_only = len(r["k_dec"]) == 1
+        roof = {"kernel": "decode_fused_kernel" if fused_only else "decode step", "bound": "hbm", "achieved": ach,
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                "traffic": measured_traffic("decode_fused_kernel") if fused_only else None,
+                "work_per_launch": f"{b} B (algorithmic bytes of one batch-1 call)",
+                "peak_note": f"measured copy bandwidth, {pk['source']}"}
     t_dec_call = sum(r["k_dec"].values())
     fused = len(r["k_dec"]) == 1
     dec_launches = len(r["k_dec"])
@@ -418,6 +445,7 @@ def main():
     roof_dec = {"kernel": "decode_fused_kernel" if fused else "decode call (3 kernels)", "bound": "hbm", "achieved": dec_b / t_dec_call / 1e9,
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": dec_b / t_dec_call / 1e9 / pk["hbm_gbs"],
                 "bytes_per_call": dec_b, "us_per_call_kernels": 1e6 * t_dec_call,
+                "traffic": measured_traffic("decode_fused_kernel") if fused else None,
                 "us_per_call_in_step": 1e6 * r["t_dec"] / args.steps / ndec}
     pre_flops = gemm_flops(c, chunk, "gate_up") + gemm_flops(c, chunk, "down")
     t_chunk = r["t_pre"] / args.steps / (T // chunk)

@@ -49,3 +49,21 @@ def test_reduce_max_two_ranks():
         p.join(timeout=60)
     assert [r[1] for r in res] == [2.0, 2.0]           # every rank sees the slowest rank's time
     assert [r[2] for r in res] == [100.0, 100.0]       # 2 ranks x 100 units / 2 s
+
+
+def test_measured_traffic_follows_the_sources(tmp_path, monkeypatch):
+    """A captured DRAM figure is reported only while the kernel's sources are unchanged."""
+    import hashlib
+    src = tmp_path / "bit_quantized_sparse_gb300" / "csrc"
+    src.mkdir(parents=True)
+    (src / "k.cu").write_text("kernel v1\n")
+    (tmp_path / "profiles").mkdir()
+    digest = hashlib.sha256(b"kernel v1\n").hexdigest()
+    (tmp_path / "profiles" / "traffic.md").write_text(
+        "| kernel | source files | sha256 | dram bytes per launch | from |\n|---|---|---|---|---|\n"
+        f"| my_kernel | csrc/k.cu | {digest} | 12345 | a capture |\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.measured_traffic("my_kernel") == 12345
+    assert bench.measured_traffic("other_kernel") is None
+    (src / "k.cu").write_text("kernel v2\n")          # the kernel changed after the capture
+    assert bench.measured_traffic("my_kernel") is None
