@@ -47,8 +47,7 @@ WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     w.offsets = take((E + 2) * 4);
     w.perm = take(T * k * 4);
     w.inv = take(T * k * 4);
-    w.tiles_gu = take((size_t)w.max_tiles_gu * sizeof(Tile));
-    w.tiles_dn = take((size_t)w.max_tiles_dn * sizeof(Tile));
+    w.blkinfo = take((size_t)w.max_blocks * sizeof(int4));
     w.ntiles = take(4 * sizeof(int32_t));
     w.hh = take((T * k + T) * I * 2);
     w.ys = take((T * k + T) * H * 2);
@@ -123,8 +122,7 @@ static RouteOut route_ws(void* ws, const WsLayout& w) {
     o.logits = at<float>(ws, w.logits);
     o.router_a = at<uint16_t>(ws, w.router_a);
     o.x16 = at<uint16_t>(ws, w.x16);
-    o.tiles_gu = at<Tile>(ws, w.tiles_gu);
-    o.tiles_dn = at<Tile>(ws, w.tiles_dn);
+    o.blkinfo = at<int4>(ws, w.blkinfo);
     o.ntiles = at<int32_t>(ws, w.ntiles);
     o.status = &at<Ctrl>(ws, w.ctrl)->status;
     return o;
@@ -172,7 +170,7 @@ int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x, int32_t* to
     RouteOut o = route_ws(workspace, w);
     o.topk_idx = topk_idx; o.topk_w = topk_w; o.gamma = shared_gamma;
     o.counts = counts; o.offsets = offsets; o.perm = perm; o.inv = inv;
-    o.tiles_gu = nullptr; o.tiles_dn = nullptr; o.x16 = nullptr;
+    o.blkinfo = nullptr; o.x16 = nullptr;
     if (T == 0) {   // empty batch: zero counts and offsets, nothing else to write
         cudaMemsetAsync(counts, 0, (size_t)L->E * 4, stream);
         return launch_status(cudaMemsetAsync(offsets, 0, (size_t)(L->E + 1) * 4, stream));
@@ -223,7 +221,7 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, m
     if (e == cudaSuccess) e = launch_grouping(*L, T, o, stream);
     if (e != cudaSuccess) return MOE_W4_ERR_LAUNCH;
     PrefillWs p{};
-    p.tiles_gu = o.tiles_gu; p.tiles_dn = o.tiles_dn; p.ntiles = o.ntiles;
+    p.blkinfo = o.blkinfo; p.ntiles = o.ntiles;
     p.offsets = o.offsets; p.perm = o.perm; p.inv = o.inv; p.topk_w = o.topk_w; p.gamma = o.gamma;
     p.x16 = o.x16;
     p.hh = at<uint16_t>(workspace, w.hh);

@@ -42,8 +42,9 @@
 namespace mw4 {
 
 struct GemmArgs {
-    const Tile* tiles;
+    const int4* blkinfo;       // per 128-row block: {group (E = shared), first row, rows, first grouped position}
     const int32_t* ntiles;     // tile count (device)
+    int M;                     // weight-row blocks per row block (tile = row block * M + weight-row block)
     const int32_t* offsets;    // expert group starts
     const int32_t* perm;       // grouped position -> t*k + j
     const uint16_t* x16;       // [T][H] fp16 copy of the activations (gate/up)
@@ -98,13 +99,18 @@ MW4_DEV uint8_t* align1024(uint8_t* p) {
 
 struct TileInfo { int e, m, r0, nrows, p0, arow; bool sh; };
 
+// Tile t = (row block t / M, weight-row block t % M); the row block's record
+// (group, first row, rows, first grouped position) was written by the scan.
 MW4_DEV TileInfo tile_info(const GemmArgs& a, int t) {
-    const Tile tl = a.tiles[t];
+    const int4 bi = __ldg(a.blkinfo + t / a.M);
     TileInfo ti;
-    ti.e = tl.e; ti.m = tl.m; ti.r0 = tl.r0; ti.nrows = tl.nrows;
-    ti.sh = (tl.e == a.E);
-    ti.p0 = (ti.sh ? a.T * a.k : a.offsets[tl.e]) + tl.r0;
-    ti.arow = (ti.sh ? 0 : tl.e * a.rows_e) + tl.m * kBM;
+    ti.e = bi.x;
+    ti.m = t % a.M;
+    ti.r0 = bi.y;
+    ti.nrows = bi.z;
+    ti.p0 = bi.w;
+    ti.sh = (ti.e == a.E);
+    ti.arow = (ti.sh ? 0 : ti.e * a.rows_e) + ti.m * kBM;
     return ti;
 }
 
@@ -502,7 +508,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     a.E = E; a.k = k; a.T = T; a.H = H; a.status = p.status;
 
     // gate/up: A = Wg, Wu rows (I per expert), K = H, out = hh [.][I]
-    a.tiles = p.tiles_gu;
+    a.blkinfo = p.blkinfo; a.M = I / kBM;
     a.s0r = L.gate.scales; a.b0r = L.gate.biases; a.s1r = L.up.scales; a.b1r = L.up.biases;
     a.s0s = L.sh_gate.scales; a.b0s = L.sh_gate.biases; a.s1s = L.sh_up.scales; a.b1s = L.sh_up.biases;
     a.c0r = L.gate.codes; a.c1r = L.up.codes; a.c0s = L.sh_gate.codes; a.c1s = L.sh_up.codes;
@@ -514,7 +520,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
 
     // down: A = Wd rows (H per expert), K = I, B = hh rows, out = ys [.][H]
     GemmArgs b = a;
-    b.tiles = p.tiles_dn; b.ntiles = p.ntiles + 1;
+    b.M = H / kBM; b.ntiles = p.ntiles + 1;
     b.s0r = L.down.scales; b.b0r = L.down.biases; b.s1r = nullptr; b.b1r = nullptr;
     b.s0s = L.sh_down.scales; b.b0s = L.sh_down.biases; b.s1s = nullptr; b.b1s = nullptr;
     b.c0r = L.down.codes; b.c1r = nullptr; b.c0s = L.sh_down.codes; b.c1s = nullptr; b.hh_rows = p.hh;

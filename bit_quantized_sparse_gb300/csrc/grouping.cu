@@ -69,25 +69,42 @@ __device__ int block_exclusive_scan(int* a, int n, int* warp_tot) {
 // One CTA: per-expert totals over chunks (chunk_base becomes the absolute
 // start of each chunk inside its expert group), expert offsets, and the tile
 // lists of the grouped GEMMs (expert-major, then row block, then weight block).
+constexpr int kScanRegChunks = 32;   // chunk counts held in registers (T <= 32 * kChunk)
+
 __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nchunk, int32_t* __restrict__ chunk_base,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                                    Tile* __restrict__ tiles_gu, Tile* __restrict__ tiles_dn,
+                                                    int4* __restrict__ blkinfo,
                                                     int32_t* __restrict__ ntiles, int MI, int MH) {
     extern __shared__ int sm[];
     int* cnt = sm;               // [E+1]
     int* off = sm + (E + 1);     // [E+1]
     int* blk = off + (E + 1);    // [E+1]
     int* wt = blk + (E + 1);     // [33]
+    // up to kScanRegChunks chunks: the counts of one expert stay in registers as
+    // exclusive prefixes and are written once, offset added, after the scan
+    const bool in_regs = nchunk <= kScanRegChunks;
+    int pre[kScanRegChunks];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
-        for (int c0 = 0; c0 < nchunk; c0 += 8) {   // eight independent loads in flight
-            int v[8];
+        if (in_regs) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = (c0 + j < nchunk) ? chunk_base[(size_t)(c0 + j) * E + e] : 0;
+            for (int j = 0; j < kScanRegChunks; ++j) pre[j] = (j < nchunk) ? chunk_base[(size_t)j * E + e] : 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (c0 + j < nchunk) chunk_base[(size_t)(c0 + j) * E + e] = run;
-                run += v[j];
+            for (int j = 0; j < kScanRegChunks; ++j) {
+                const int c = pre[j];
+                pre[j] = run;
+                run += c;
+            }
+        } else {
+            for (int c0 = 0; c0 < nchunk; c0 += 8) {   // eight independent loads in flight
+                int v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = (c0 + j < nchunk) ? chunk_base[(size_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (c0 + j < nchunk) chunk_base[(size_t)(c0 + j) * E + e] = run;
+                    run += v[j];
+                }
             }
         }
         cnt[e] = run;
@@ -105,24 +122,26 @@ __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nch
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         counts[e] = cnt[e];
         offsets[e] = off[e];
-        for (int c = 0; c < nchunk; ++c) chunk_base[(size_t)c * E + e] += off[e];
+        if (in_regs) {
+            // E <= 1024 = blockDim.x: each thread owns at most one expert, whose prefixes pre[] holds
+#pragma unroll
+            for (int j = 0; j < kScanRegChunks; ++j)
+                if (j < nchunk) chunk_base[(size_t)j * E + e] = pre[j] + off[e];
+        } else {
+            for (int c = 0; c < nchunk; ++c) chunk_base[(size_t)c * E + e] += off[e];
+        }
     }
     if (threadIdx.x == 0) offsets[E] = off[E];
-    if (tiles_gu == nullptr) return;
-    __syncthreads();
-    // tiles in parallel: block b belongs to the expert whose block range holds it
-    // (blk[] is the exclusive scan of blocks per expert; binary search)
-    for (int i = threadIdx.x; i < nblk * (MI + MH); i += blockDim.x) {
-        const bool gu = i < nblk * MI;
-        const int j = gu ? i : i - nblk * MI, M = gu ? MI : MH;
-        const int b = j / M, m = j % M;
-        int lo = 0, hi = E;   // largest e with blk[e] <= b
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (blk[mid] <= b) lo = mid; else hi = mid - 1;
+    if (blkinfo == nullptr) return;
+    // one record per 128-row block: the GEMMs read their tile's block in one load
+    // (tile = block * M + weight-row block); the shared group (e = E) comes last
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        const int b0 = blk[e], b1 = (e < E) ? blk[e + 1] : nblk;
+        const int rows = (e < E) ? cnt[e] : T, p_first = (e < E) ? off[e] : T * k;
+        for (int b = b0; b < b1; ++b) {
+            const int r0 = (b - b0) * kBN;
+            blkinfo[b] = make_int4(e, r0, min(kBN, rows - r0), p_first + r0);
         }
-        const int e = lo, r0 = (b - blk[e]) * kBN, nr = min(kBN, cnt[e] - r0);
-        (gu ? tiles_gu : tiles_dn)[j] = Tile{e, m, r0, nr};
     }
     if (threadIdx.x == 0) {
         ntiles[0] = nblk * MI;
@@ -133,30 +152,53 @@ __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nch
 // One warp per chunk walks its tokens in order and gives every assignment its
 // grouped position; lanes holding the same expert in one step are ranked by
 // lane order, which is token order.
-__global__ void __launch_bounds__(32) assign_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
-                                                    const int32_t* __restrict__ chunk_base,
-                                                    int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+// Four warps per chunk of kChunk tokens, warp w taking tokens [32w, 32w+32):
+// each warp first counts its tokens' selections per expert, the counts are
+// turned into per-warp starting positions (chunk base + earlier warps'
+// counts), then every warp places its own tokens in order.  Positions are
+// therefore the same as one warp walking the whole chunk in token order.
+constexpr int kAssignWarps = kChunk / 32;
+__global__ void __launch_bounds__(kChunk) assign_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                                        const int32_t* __restrict__ chunk_base,
+                                                        int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
     extern __shared__ int sm_assign[];
-    int* running = sm_assign;             // [E]
-    int* sel = sm_assign + E;             // [kChunk * k] the chunk's selections
-    const int lane = threadIdx.x;
+    int* running = sm_assign;                       // [kAssignWarps][E]
+    int* sel = sm_assign + kAssignWarps * E;        // [kChunk * k] the chunk's selections
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x;
     const int t_begin = c * kChunk, t_end = min(T, t_begin + kChunk);
-    for (int e = lane; e < E; e += 32) running[e] = chunk_base[(size_t)c * E + e];
-    for (int i = lane; i < (t_end - t_begin) * k; i += 32) sel[i] = idx[(size_t)t_begin * k + i];
-    __syncwarp();
+    for (int i = threadIdx.x; i < kAssignWarps * E; i += blockDim.x) running[i] = 0;
+    for (int i = threadIdx.x; i < (t_end - t_begin) * k; i += blockDim.x) sel[i] = idx[(size_t)t_begin * k + i];
+    __syncthreads();
+    const int w_begin = min(t_end, t_begin + 32 * warp), w_end = min(t_end, w_begin + 32);
+    int* run_w = running + warp * E;
+    for (int i = lane; i < (w_end - w_begin) * k; i += 32) {   // this warp's counts
+        const int e = sel[(w_begin - t_begin) * k + i];
+        if (e >= 0 && e < E) atomicAdd(&run_w[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {    // counts -> starting positions
+        int base = chunk_base[(size_t)c * E + e];
+#pragma unroll
+        for (int w = 0; w < kAssignWarps; ++w) {
+            const int n = running[w * E + e];
+            running[w * E + e] = base;
+            base += n;
+        }
+    }
+    __syncthreads();
     const int per = 32 / k;                 // tokens per step
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int t0 = t_begin; t0 < t_end; t0 += per) {
+    for (int t0 = w_begin; t0 < w_end; t0 += per) {
         const int t = t0 + lane / k, j = lane % k;
-        const bool valid = (lane < per * k) && (t < t_end);
+        const bool valid = (lane < per * k) && (t < w_end);
         int e = valid ? sel[(t - t_begin) * k + j] : -1;
         if (e < 0 || e >= E) e = -1;        // bad indices were reported by the count kernel
         const unsigned same = __match_any_sync(0xffffffffu, e);
         int pos = 0;
-        if (e >= 0) pos = running[e] + __popc(same & lt_mask);
+        if (e >= 0) pos = run_w[e] + __popc(same & lt_mask);
         __syncwarp();
-        if (e >= 0 && (same & lt_mask) == 0) running[e] += __popc(same);   // group leader
+        if (e >= 0 && (same & lt_mask) == 0) run_w[e] += __popc(same);   // group leader
         __syncwarp();
         if (e >= 0) {
             perm[pos] = t * k + j;
@@ -171,10 +213,10 @@ cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cud
     chunk_count_kernel<<<nchunk, kChunk, E * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.status);
     trace_mark(st, 3);
     const size_t scan_sm = (3 * (E + 1) + 33) * sizeof(int);
-    scan_kernel<<<1, 1024, scan_sm, st>>>(T, E, k, nchunk, o.chunk_base, o.counts, o.offsets, o.tiles_gu,
-                                          o.tiles_dn, o.ntiles, L.I / kBM, L.H / kBM);
+    scan_kernel<<<1, 1024, scan_sm, st>>>(T, E, k, nchunk, o.chunk_base, o.counts, o.offsets, o.blkinfo, o.ntiles,
+                                          L.I / kBM, L.H / kBM);
     trace_mark(st, 4);
-    assign_kernel<<<nchunk, 32, (E + kChunk * k) * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.perm,
+    assign_kernel<<<nchunk, kChunk, (kAssignWarps * E + kChunk * k) * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.perm,
                                                                      o.inv);
     trace_mark(st, 5);
     return cudaGetLastError();

@@ -19,18 +19,17 @@ constexpr int kDecodeMaxT = 16;   // largest decode batch
 constexpr int kFusedClustersPerExpert = 4;   // fused T=1 decode: 16 CTAs per expert in clusters of 4
 constexpr int kRouterRowsPerCta = 256;  // H rows per decode-router CTA
 
-struct Tile { int e, m, r0, nrows; };
 struct Ctrl;   // workspace control header (common.cuh)
 
 // Records trace event `i` on `st` when tracing is enabled (moe_w4_set_trace_events).
 void trace_mark(cudaStream_t st, int i);
 // Records how many kernels the current traced call launches.
-void trace_kernels(int n);   // expert (E = shared), weight-row block, first row, rows
+void trace_kernels(int n);
 
 // Byte offsets of every region of the workspace (all 256-byte aligned).
 struct WsLayout {
     size_t ctrl, logits, router_a, x16, topk_idx, topk_w, gamma, chunk_base, counts, offsets, perm, inv;
-    size_t tiles_gu, tiles_dn, ntiles, hh, ys;
+    size_t blkinfo, ntiles, hh, ys;
     size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh, dec_cpart, dec_ybuf;
     size_t total;
     int T_max, nchunk_max, max_blocks, max_tiles_gu, max_tiles_dn;
@@ -49,7 +48,7 @@ struct RouteOut {
     float* logits;
     uint16_t* router_a;  // [Epad][3H] bf16 split router weights (tensor-core scores); NULL: CUDA cores
     uint16_t* x16;     // fp16 copy of x written by the top-k kernel (NULL: not needed)
-    Tile* tiles_gu; Tile* tiles_dn; int32_t* ntiles;   // NULL: no tile maps
+    int4* blkinfo; int32_t* ntiles;   // per-block records [max blocks] and tile counts [2]; NULL: no tile maps
     unsigned int* status;
 };
 cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* x, const RouteOut& o,
@@ -82,7 +81,8 @@ cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint1
 // grouped tensor-core GEMMs (grouped_gemm.cu)
 // ---------------------------------------------------------------------------
 struct PrefillWs {
-    const Tile* tiles_gu; const Tile* tiles_dn; const int32_t* ntiles;
+    const int4* blkinfo;     // per 128-row block of the grouped rows: {group (E = shared), first row, rows, first position}
+    const int32_t* ntiles;   // [2] gate/up and down tile counts
     const int32_t* offsets; const int32_t* perm; const int32_t* inv;
     const float* topk_w; const float* gamma;
     const uint16_t* x16;  // fp16 [T][H]

@@ -204,45 +204,64 @@ size_t router_tc_smem() { return 1024 + (size_t)kRtStages * (kBM * kBK * 2 + kRt
 // ---------------------------------------------------------------------------
 constexpr int kTopkWarps = 8;
 
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(const float* __restrict__ logits,
+// NIT >= ceil(H/256): 16-byte loads of the x row per lane, held in registers.
+template <int NIT>
+__global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 3 : 2) topk_kernel(const float* __restrict__ logits,
                                                                const uint16_t* __restrict__ x,
                                                                const float* __restrict__ g, int T, int H, int E,
                                                                int k, int32_t* __restrict__ idx,
                                                                float* __restrict__ w, float* __restrict__ gamma,
                                                                uint16_t* __restrict__ x16,
                                                                unsigned int* status) {
-    extern __shared__ float sc_all[];
+    extern __shared__ float sm_topk[];
+    float* gs = sm_topk;                    // [H] shared-expert gate vector, staged once per block
+    float* sc_all = sm_topk + H;            // [kTopkWarps][E] scores
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    for (int i = threadIdx.x; i < H / 4; i += blockDim.x)
+        reinterpret_cast<float4*>(gs)[i] = reinterpret_cast<const float4*>(g)[i];
+    __syncthreads();
     const int t = blockIdx.x * kTopkWarps + warp;
     if (t >= T) return;
+    // the token's row of x is requested first, so that its latency hides behind the selection
+    uint4 xv[NIT];
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int h = it * 256 + lane * 8;
+        xv[it] = h < H ? *reinterpret_cast<const uint4*>(x + (size_t)t * H + h) : make_uint4(0, 0, 0, 0);
+    }
     float* sc = sc_all + warp * E;
     for (int e = lane; e < E; e += 32) sc[e] = logits[(size_t)t * E + e];
     __syncwarp();
     select_topk_warp(sc, E, k, idx + (size_t)t * k, w + (size_t)t * k);
     float d = 0.f;
-    for (int h = lane * 8; h < H; h += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-        bool fits = true;
+    bool fits = true;
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int h = it * 256 + lane * 8;
+        if (h >= H) break;
+        const uint32_t u[4] = {xv[it].x, xv[it].y, xv[it].z, xv[it].w};
+        const float4 g0 = *reinterpret_cast<const float4*>(gs + h), g1 = *reinterpret_cast<const float4*>(gs + h + 4);
+        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         float f[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float a = __uint_as_float(u[i] << 16), b = __uint_as_float(u[i] & 0xFFFF0000u);
-            d = fmaf(a, g[h + 2 * i], d);
-            d = fmaf(b, g[h + 2 * i + 1], d);
-            fits = fits && fabsf(a) <= 65504.f && fabsf(b) <= 65504.f;
-            f[2 * i] = a;
-            f[2 * i + 1] = b;
+            f[2 * i] = __uint_as_float(u[i] << 16);
+            f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            d = fmaf(f[i], gg[i], d);
+            fits = fits && fabsf(f[i]) <= 65504.f;
         }
         // fp16 copy in chunk order {0,4,1,5,2,6,3,7} (the order the dequantised weights use)
-        uint32_t hv[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) hv[i] = h2_as_u32(__floats2half2_rn(f[i], f[i + 4]));
         if (x16) {
+            uint32_t hv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) hv[i] = h2_as_u32(__floats2half2_rn(f[i], f[i + 4]));
             *reinterpret_cast<uint4*>(x16 + (size_t)t * H + h) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            if (!fits) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
         }
     }
+    if (x16 && !fits) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
     d = warp_sum(d);
     if (lane == 0) gamma[t] = 1.0f / (1.0f + expf(-d));
 }
@@ -295,9 +314,21 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
         router_scores_kernel<<<grid, 256, 0, st>>>(x, L.router_w, L.router_bias, o.logits, T, L.H, L.E);
     }
     trace_mark(st, 1);
-    const size_t sm = (size_t)kTopkWarps * L.E * sizeof(float);
-    topk_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, sm, st>>>(
-        o.logits, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w, o.gamma, o.x16, o.status);
+    const size_t sm = ((size_t)L.H + (size_t)kTopkWarps * L.E) * sizeof(float);
+    const dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
+    const int nit = (L.H + 255) / 256;   // H <= 4096
+    if (nit <= 2)
+        topk_kernel<2><<<grid, block, sm, st>>>(o.logits, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
+                                                o.gamma, o.x16, o.status);
+    else if (nit <= 4)
+        topk_kernel<4><<<grid, block, sm, st>>>(o.logits, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
+                                                o.gamma, o.x16, o.status);
+    else if (nit <= 8)
+        topk_kernel<8><<<grid, block, sm, st>>>(o.logits, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
+                                                o.gamma, o.x16, o.status);
+    else
+        topk_kernel<16><<<grid, block, sm, st>>>(o.logits, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
+                                                 o.gamma, o.x16, o.status);
     trace_mark(st, 2);
     return cudaGetLastError();
 }
