@@ -176,6 +176,25 @@ def test_small_layer_top1(mw, torch):
     check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[:16]))), ref[:16])
 
 
+def test_widths_not_multiple_of_256(mw, torch):
+    """H = I = 384: multiples of 128 (the supported granularity) but not of 256,
+    so rows of x and h end inside a 256-column block and the quantisation groups
+    per row (6) are not a multiple of 8.  Routing, prefill and decode against the
+    oracle."""
+    L = S.draw_layer(384, 32, 384, 4, 1.0, seed=31)
+    x = S.draw_tokens(L, 200, seed=31)
+    dl = mw.DeviceLayer(L)
+    xd = mw.tokens_to_device(x)
+    r = mw.route(dl, xd)
+    torch.cuda.synchronize()
+    check_route(r, L, x)
+    ref = O.moe_layer(L, x)["out"]
+    check_out(to_np_bits(mw.forward_prefill(dl, xd)), ref)
+    check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[:3]))), ref[:3])
+    check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[7:8]))), ref[7:8])
+    assert dl.status() == 0
+
+
 # ---------------------------------------------------------------------------
 # decode: fused GEMV path
 # ---------------------------------------------------------------------------
