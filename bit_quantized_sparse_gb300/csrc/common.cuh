@@ -105,6 +105,11 @@ MW4_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_
     return __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
 }
 
+// Programmatic dependent launch: wait until the preceding grid on the stream has
+// completed and its memory is visible; let the next grid start launching.
+MW4_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MW4_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // proxies and fences
 // ---------------------------------------------------------------------------

@@ -271,9 +271,12 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     const bool shared_cluster = (slot == k);
     unsigned int* status = &a.ctrl->status;
 
-    // the router's loads go out first: thread (e, half) sums half of this CTA's
-    // slice of the H rows for expert e; its W_r column slice and the matching x
-    // values (the same for the whole warp) land while x is prepared below
+    // The kernel may start before the previous kernel on the stream has finished
+    // (programmatic dependent launch): until griddep_wait() it touches only
+    // weights, its own shared memory and the tensor maps.
+    // The router's loads go out first: thread (e, half) sums half of this CTA's
+    // slice of the H rows for expert e; its W_r column slice is requested before
+    // the wait, the matching x values (the same for the whole warp) after it.
     const int rh0 = (int)((long)G * H / NG), rh1 = (int)((long)(G + 1) * H / NG);
     const int rnh = rh1 - rh0, rhalf = rnh / 2;
     const int r_e = tid % E, r_hb = (tid / E) ? rhalf : 0, r_he = (tid / E) ? rnh : rhalf;
@@ -283,7 +286,6 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         for (int j = 0; j < 32; ++j) {
             const bool in = r_hb + j < r_he;
             rw[j] = in ? __ldg(a.router_w + (size_t)(rh0 + r_hb + j) * E + r_e) : 0.f;
-            rx[j] = in ? bf16_bits_to_float(__ldg(a.x + rh0 + r_hb + j)) : 0.f;
         }
     }
     if (tid == 32) {   // the descriptors are fetched once, early, off the critical path
@@ -295,6 +297,11 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         mbar_init(bar_dn, 1);
         *abort_flag = 0;
         fence_mbar_init();
+    }
+    griddep_wait();   // from here on: x, the workspace and its counters
+    if (tid < 2 * E) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rx[j] = (r_hb + j < r_he) ? bf16_bits_to_float(__ldg(a.x + rh0 + r_hb + j)) : 0.f;
     }
     // x as fp16 B fragments, one thread per 16-byte entry: entry i (32-column
     // block i/4, lane%4 = i%4) holds {x[8i], x[8i+4]}, {x[8i+1], x[8i+5]}/16,
@@ -560,6 +567,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         }
     }
     // ---------------------------------------------------------------- 5. down GEMV
+    griddep_launch_dependents();   // the next kernel on the stream may start its prologue
     // RD/16 row tiles x KS splits of the 64-column groups
     const bool dn_ok = __syncthreads_and(h_ok ? mbar_wait(bar_dn, 0, abort_flag, status) : 0);
     if (dn_ok) {
@@ -655,7 +663,8 @@ static bool shape_ok(const moe_w4_layer& L) {
 
 static size_t fused_smem(const moe_w4_layer& L) { return FusedSmem(L.H, L.E, L.I).total + 1024; }
 
-static cudaLaunchConfig_t fused_config(const moe_w4_layer& L, cudaLaunchAttribute* attr, cudaStream_t st) {
+static cudaLaunchConfig_t fused_config(const moe_w4_layer& L, cudaLaunchAttribute* attr, cudaStream_t st,
+                                       bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((L.top_k + 1) * kPE);
     cfg.blockDim = dim3(kFThreads);
@@ -665,8 +674,10 @@ static cudaLaunchConfig_t fused_config(const moe_w4_layer& L, cudaLaunchAttribut
     attr[0].val.clusterDim.x = kCS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cfg;
 }
 
@@ -686,8 +697,8 @@ bool decode_fused_supported(const moe_w4_layer& L) {
     bool ok = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
               cudaSuccess;
     if (ok) {
-        cudaLaunchAttribute attr[1];
-        const cudaLaunchConfig_t cfg = fused_config(L, attr, nullptr);
+        cudaLaunchAttribute attr[2];
+        const cudaLaunchConfig_t cfg = fused_config(L, attr, nullptr, false);
         int nclusters = 0;
         ok = cudaOccupancyMaxActiveClusters(&nclusters, (void*)decode_fused_kernel, &cfg) == cudaSuccess &&
              nclusters >= (L.top_k + 1) * kFusedClustersPerExpert;
@@ -716,8 +727,9 @@ cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16
     a.idx_out = d.idx; a.w_out = d.w; a.gamma_out = d.gamma; a.out = out;
     a.ctrl = d.ctrl;
     a.H = H; a.E = E; a.I = I; a.k = k;
-    cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = fused_config(L, attr, st);   // shared memory opt-in set by the support check
+    cudaLaunchAttribute attr[2];
+    // programmatic dependent launch: the prologue may overlap the previous kernel's tail
+    const cudaLaunchConfig_t cfg = fused_config(L, attr, st, true);   // shared memory opt-in set by the support check
     return cudaLaunchKernelEx(&cfg, decode_fused_kernel, a, mg, mu, md, msg, msu, msd);
 }
 
