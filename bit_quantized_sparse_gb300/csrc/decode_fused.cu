@@ -303,46 +303,6 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
 #pragma unroll
         for (int j = 0; j < 32; ++j) rx[j] = (r_hb + j < r_he) ? bf16_bits_to_float(__ldg(a.x + rh0 + r_hb + j)) : 0.f;
     }
-    // x as fp16 B fragments, one thread per 16-byte entry: entry i (32-column
-    // block i/4, lane%4 = i%4) holds {x[8i], x[8i+4]}, {x[8i+1], x[8i+5]}/16,
-    // {x[8i+2], x[8i+6]}, {x[8i+3], x[8i+7]}/16; plus the per-64-column group
-    // sums of the stored values (xbs) and of the values the products use
-    // (xsum), reduced over the 8 lanes of a group (H/8 is a multiple of 32, so
-    // the loop runs whole warps)
-    for (int i = tid; i < H / 8; i += kFThreads) {
-        const uint4 v = *reinterpret_cast<const uint4*>(a.x + i * 8);
-        const uint32_t e[4] = {v.x, v.y, v.z, v.w};   // pairs (0,1) (2,3) (4,5) (6,7)
-        float f[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[2 * j] = __uint_as_float(e[j] << 16);
-            f[2 * j + 1] = __uint_as_float(e[j] & 0xFFFF0000u);
-        }
-        float sb = 0.f, so = 0.f;   // sums of the stored even / odd entries
-        bool bad = false;
-        uint32_t q[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float m = (j & 1) ? 0.0625f : 1.0f;
-            bad |= !(fabsf(f[j]) <= 65504.f) || !(fabsf(f[j + 4]) <= 65504.f);
-            const __half2 h2 = __floats2half2_rn(f[j] * m, f[j + 4] * m);
-            q[j] = h2_as_u32(h2);
-            const float2 back = __half22float2(h2);
-            if (j & 1) so += back.x + back.y; else sb += back.x + back.y;
-        }
-        reinterpret_cast<uint4*>(xperm)[i] = make_uint4(q[0], q[1], q[2], q[3]);
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1) {
-            sb += __shfl_xor_sync(0xffffffffu, sb, off);
-            so += __shfl_xor_sync(0xffffffffu, so, off);
-        }
-        if ((i & 7) == 0) {
-            xbs[i / 8] = sb + so;
-            xsum[i / 8] = sb + 16.f * so;
-        }
-        if (bad) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
-    }
-    __syncthreads();
 
     // ---------------------------------------------------------------- weight loads (routed: after the top-k)
     // called by all 32 lanes of warp 0: lane b issues box b, lanes 16.. the rest
@@ -404,6 +364,48 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     // published, so that issuing them does not delay the exchange everyone waits on
     if (shared_cluster && warp == 0) issue_loads(E);
     cluster_sync();   // every peer has read this CTA's partials; the buffers may be reused
+    // x for the GEMVs is prepared here, off the router's critical path, while the
+    // other CTAs' router sums come in
+    // x as fp16 B fragments, one thread per 16-byte entry: entry i (32-column
+    // block i/4, lane%4 = i%4) holds {x[8i], x[8i+4]}, {x[8i+1], x[8i+5]}/16,
+    // {x[8i+2], x[8i+6]}, {x[8i+3], x[8i+7]}/16; plus the per-64-column group
+    // sums of the stored values (xbs) and of the values the products use
+    // (xsum), reduced over the 8 lanes of a group (H/8 is a multiple of 32, so
+    // the loop runs whole warps)
+    for (int i = tid; i < H / 8; i += kFThreads) {
+        const uint4 v = *reinterpret_cast<const uint4*>(a.x + i * 8);
+        const uint32_t e[4] = {v.x, v.y, v.z, v.w};   // pairs (0,1) (2,3) (4,5) (6,7)
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f[2 * j] = __uint_as_float(e[j] << 16);
+            f[2 * j + 1] = __uint_as_float(e[j] & 0xFFFF0000u);
+        }
+        float sb = 0.f, so = 0.f;   // sums of the stored even / odd entries
+        bool bad = false;
+        uint32_t q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float m = (j & 1) ? 0.0625f : 1.0f;
+            bad |= !(fabsf(f[j]) <= 65504.f) || !(fabsf(f[j + 4]) <= 65504.f);
+            const __half2 h2 = __floats2half2_rn(f[j] * m, f[j + 4] * m);
+            q[j] = h2_as_u32(h2);
+            const float2 back = __half22float2(h2);
+            if (j & 1) so += back.x + back.y; else sb += back.x + back.y;
+        }
+        reinterpret_cast<uint4*>(xperm)[i] = make_uint4(q[0], q[1], q[2], q[3]);
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) {
+            sb += __shfl_xor_sync(0xffffffffu, sb, off);
+            so += __shfl_xor_sync(0xffffffffu, so, off);
+        }
+        if ((i & 7) == 0) {
+            xbs[i / 8] = sb + so;
+            xsum[i / 8] = sb + 16.f * so;
+        }
+        if (bad) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
+    }
+    __syncthreads();
     if (shared_cluster) {   // the shared cluster's gate sigmoid(x . g), all threads
         float d = 0.f;
         for (int h = tid * 8; h < H; h += kFThreads * 8) {
@@ -494,9 +496,13 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             const int r0 = (up ? t - ntile / 2 : t) * 16;
             const uint16_t* sb = up ? usb : gsb;
             float acc0 = 0.f, acc1 = 0.f;
-            w4_gemv16(up ? ucodes : gcodes, RG, r0, ks * ngrp / KS, (ks + 1) * ngrp / KS,
-                      reinterpret_cast<const uint4*>(xperm), xbs, xsum, sb, sb + RG * (H / 64), H / 64, acc0, acc1,
-                      bar_gu, abort_flag, status);
+            // split ks takes its share of each half of the columns, so that every warp
+            // starts on an early box and, once the last box lands, has one box left
+            const int half = ngrp / 2;
+            for (int hf = 0; hf < 2; ++hf)
+                w4_gemv16(up ? ucodes : gcodes, RG, r0, hf * half + ks * half / KS, hf * half + (ks + 1) * half / KS,
+                          reinterpret_cast<const uint4*>(xperm), xbs, xsum, sb, sb + RG * (H / 64), H / 64, acc0, acc1,
+                          bar_gu, abort_flag, status);
             if ((lane & 3) == 0) {
                 red[task * 16 + (lane >> 2)] = acc0;
                 red[task * 16 + (lane >> 2) + 8] = acc1;
