@@ -406,7 +406,7 @@ MW4_DEV bool topk_before(float v, int i, float u, int j) { return v > u || (v ==
 // other, one thread per candidate.  Needs E % 32 == 0, E <= blockDim.x,
 // (E/32) * k <= 64.  `cand` is scratch of 2 * 64 words in shared memory,
 // 16-byte aligned.
-MW4_DEV void select_topk_block(const float* sc, int E, int k, int* sel_idx, float* sel_val, uint32_t* cand) {
+static __device__ __noinline__ void select_topk_block(const float* sc, int E, int k, int* sel_idx, float* sel_val, uint32_t* cand) {
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     float* cv = reinterpret_cast<float*>(cand);
     int* ci = reinterpret_cast<int*>(cand + 64);
