@@ -395,57 +395,6 @@ MW4_DEV void select_topk_warp(const float* sc, int E, int k, int32_t* idx_out, f
     else select_topk_warp_n<32>(sc, E, k, idx_out, w_out);
 }
 
-// (v, i) ranks before (u, j) when v > u, or v == u and i < j: larger score
-// first, lower expert index on equal scores.
-MW4_DEV bool topk_before(float v, int i, float u, int j) { return v > u || (v == u && i < j); }
-
-// Top-k of the E scores in shared memory `sc`, by descending score, lower
-// index first on equal scores; the whole block calls it.  Each of the first
-// E/32 warps sorts its 32 scores (bitonic network over the lanes) and keeps
-// its first k as candidates; the candidates are then ranked against each
-// other, one thread per candidate.  Needs E % 32 == 0, E <= blockDim.x,
-// (E/32) * k <= 64.  `cand` is scratch of 2 * 64 words in shared memory,
-// 16-byte aligned.
-static __device__ __noinline__ void select_topk_block(const float* sc, int E, int k, int* sel_idx, float* sel_val, uint32_t* cand) {
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    float* cv = reinterpret_cast<float*>(cand);
-    int* ci = reinterpret_cast<int*>(cand + 64);
-    if (warp < E / 32) {
-        float v = sc[t];
-        int i = t;
-#pragma unroll
-        for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-            for (int j = kk >> 1; j > 0; j >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, v, j);
-                const int oi = __shfl_xor_sync(0xffffffffu, i, j);
-                // lanes with (lane & kk) == 0 build a descending run; the lower lane of a
-                // pair keeps the element that ranks first in a descending run
-                const bool desc = (lane & kk) == 0, lower = (lane & j) == 0;
-                const bool other_first = topk_before(ov, oi, v, i);
-                if (other_first == (lower == desc)) { v = ov; i = oi; }
-            }
-        }
-        if (lane < k) { cv[warp * k + lane] = v; ci[warp * k + lane] = i; }
-    }
-    const int nc = (E / 32) * k;
-    for (int c = nc + t; c < ((nc + 3) & ~3); c += blockDim.x) { cv[c] = -INFINITY; ci[c] = 0x7fffffff; }   // pad to 4
-    __syncthreads();
-    if (t < nc) {
-        const float v = cv[t];
-        const int i = ci[t];
-        int r = 0;
-#pragma unroll 4
-        for (int c = 0; c < nc; c += 4) {   // four candidates per 16-byte load; the padding ranks last
-            const float4 u = *reinterpret_cast<const float4*>(cv + c);
-            const int4 j = *reinterpret_cast<const int4*>(ci + c);
-            r += topk_before(u.x, j.x, v, i) + topk_before(u.y, j.y, v, i) + topk_before(u.z, j.z, v, i) +
-                 topk_before(u.w, j.w, v, i);
-        }
-        if (r < k) { sel_idx[r] = i; sel_val[r] = v; }
-    }
-}
-
 MW4_DEV float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);

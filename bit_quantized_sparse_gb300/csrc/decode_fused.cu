@@ -134,6 +134,41 @@ MW4_DEV uint32_t ld_acquire_u32(const unsigned int* p) {
     return v;
 }
 
+// Top-k of E <= 256 scores in shared memory by one warp, larger score first and
+// the lower expert index on equal scores: each lane holds 8 scores as
+// order-preserving integer keys; per round the warp maximum comes from
+// redux.sync, then the lowest index holding it.  Lane r < k returns the r-th
+// selection (index and score).
+MW4_DEV uint32_t order_key(float v) {
+    const uint32_t b = __float_as_uint(v);
+    return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);   // monotone: larger float, larger key
+}
+MW4_DEV void warp_topk_redux(const float* sc, int E, int k, int& sel_idx, float& sel_val) {
+    const int lane = threadIdx.x & 31;
+    uint32_t key[8];
+    unsigned live = 0;   // bit i: score lane + 32 i exists and is not taken
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < E ? order_key(sc[e]) : 0u;
+        if (e < E) live |= 1u << i;
+    }
+    sel_idx = -1;
+    sel_val = 0.f;
+    for (int r = 0; r < k; ++r) {
+        uint32_t bk = 0;
+        int bi = 0x7fffffff;
+        bool any = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)   // ascending index in the lane: strict > keeps the lower one
+            if (((live >> i) & 1u) && (!any || key[i] > bk)) { bk = key[i]; bi = lane + 32 * i; any = true; }
+        const uint32_t wmax = __reduce_max_sync(0xffffffffu, any ? bk : 0u);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, (any && bk == wmax) ? (uint32_t)bi : 0xffffffffu);
+        if ((int)(win & 31) == lane) live &= ~(1u << (win >> 5));
+        if (lane == r) { sel_idx = (int)win; sel_val = sc[win]; }
+    }
+}
+
 // --------------------------------------------------------------------------- legacy-MMA dot engine
 MW4_DEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -462,27 +497,24 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
                 logits[e] = s + (a.router_bias ? a.router_bias[e] : 0.f);
             }
             __syncthreads();
-            {
-                __shared__ int32_t idx_s[8];
-                __shared__ float v_s[8];
-                __shared__ __align__(16) uint32_t cand[128];
-                select_topk_block(logits, E, k, idx_s, v_s, cand);
-                __syncthreads();
-                if (warp == 0) {   // softmax over the selection (v_s[0] is the largest), one lane per slot
-                    const float ex = lane < k ? expf(v_s[lane] - v_s[0]) : 0.f;
-                    const float z = warp_sum(ex);
-                    if (lane < k) {
-                        const float w = ex / z;
-                        if (lane == slot) { *sel_e = idx_s[lane]; *sel_w = w; }
-                        if (G == 0) { a.idx_out[lane] = idx_s[lane]; a.w_out[lane] = w; }
-                    }
-                }
-            }
-            __syncthreads();
+            // one warp selects, weighs and issues the loads of this CTA's expert
             if (warp == 0) {
-                const int e = *sel_e;
-                if (e < 0 || e >= E) { if (lane == 0) { raise_status(status, MOE_W4_STATUS_BAD_INDEX); *abort_flag = 1; } }
-                else issue_loads(e);
+                int sidx;
+                float sval;
+                warp_topk_redux(logits, E, k, sidx, sval);
+                const float v0 = __shfl_sync(0xffffffffu, sval, 0);   // the largest selected score
+                const float ex = lane < k ? expf(sval - v0) : 0.f;
+                const float z = warp_sum(ex);
+                const float w = ex / z;   // softmax over the selection
+                const int e = __shfl_sync(0xffffffffu, sidx, slot);
+                const float we = __shfl_sync(0xffffffffu, w, slot);
+                if (lane == 0) { *sel_e = e; *sel_w = we; }
+                if (G == 0 && lane < k) { a.idx_out[lane] = sidx; a.w_out[lane] = w; }
+                if (e < 0 || e >= E) {
+                    if (lane == 0) { raise_status(status, MOE_W4_STATUS_BAD_INDEX); *abort_flag = 1; }
+                } else {
+                    issue_loads(e);
+                }
             }
         }
     }
