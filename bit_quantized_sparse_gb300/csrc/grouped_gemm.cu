@@ -24,7 +24,8 @@
 //             (or the shared gate) -> ys[p][o] fp16
 // The kernel is persistent (one CTA per SM, tiles strided by the grid) and
 // warp-specialised:
-//   dequantisers  4 warps per matrix, one thread per weight row: codes from
+//   dequantisers  8 warps (gate/up: one thread per matrix row; down: two threads
+//                 per row, half a step each): codes from
 //                 shared memory -> fp16 -> tcgen05.st into an A ring in TMEM;
 //                 for gate/up they also gather the token rows of x16 (the B
 //                 operand) with cp.async a few steps ahead
@@ -72,7 +73,10 @@ constexpr uint32_t kTileBytes = kBM * kBK * 2;          // 16 KB fp16 tile (A or
 template <bool DUAL>
 struct Geo {
     static constexpr int NMAT = DUAL ? 2 : 1;
-    static constexpr int kDeqWarps = 4 * NMAT;            // one thread per (matrix, weight row)
+    // 8 dequantiser warps: gate/up one thread per (matrix, weight row); down two
+    // threads per weight row, 32 of the step's 64 columns each (more threads in
+    // flight for the one matrix)
+    static constexpr int kDeqWarps = 8;
     static constexpr int kDeqWarp0 = 0;                   // warp w reaches TMEM lanes 32*(w%4)..+31, so the
     static constexpr int kEpiWarp0 = kDeqWarp0 + kDeqWarps;   // dequantiser and epilogue groups start at w%4 == 0
     static constexpr int kEpiWarps = 8;                   // two per TMEM lane group, columns interleaved
@@ -148,7 +152,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
             mbar_init(&r_empty[s], 1);
         }
         for (int s = 0; s < SA; ++s) {
-            mbar_init(&a_full[s], 128 * NMAT);
+            mbar_init(&a_full[s], 32 * GG::kDeqWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -232,7 +236,8 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         }
     } else if (warp < GG::kEpiWarp0) {
         // ------------------------------------------------------------ dequantisation: one weight row per thread
-        const int td = tid - 32 * GG::kDeqWarp0, mat = td / 128, row = td % 128;
+        const int td = tid - 32 * GG::kDeqWarp0, row = td % 128;
+        const int mat = DUAL ? td / 128 : 0, hsel = DUAL ? -1 : td / 128;   // down: which 32-column half
         const int sw = (row >> 2) & 1;   // 32-byte swizzle phase of this row's codes
         const bool chunked = (G % 8) == 0;
         int gk = 0;
@@ -320,6 +325,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         taddr + ((uint32_t)(row & ~31) << 16) + GG::A_TMEM0 + sa * GG::A_COLS + mat * (kBK / 2);
 #pragma unroll
                     for (int hlf = 0; hlf < 2; ++hlf) {
+                        if (!DUAL && hlf != hsel) continue;
                         const uint4 w = *reinterpret_cast<const uint4*>(cr + ((hlf ^ sw) << 4));
                         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
                         uint32_t o[16];
