@@ -329,58 +329,55 @@ MW4_DEV float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t
 MW4_DEV float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 MW4_DEV float sigmoid_f(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
+
+// Warp top-k with NV scores per lane kept in registers (E <= 32 NV).
 // ---------------------------------------------------------------------------
 // warp-level selection (router)
 // ---------------------------------------------------------------------------
-// Best of (v, i) pairs: larger score, then lower expert index.
-MW4_DEV void warp_argmax(float& v, int& i) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, i, off);
-        if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
-    }
+// Order-preserving 32-bit key of a float: larger float, larger key.
+MW4_DEV uint32_t order_key(float v) {
+    const uint32_t b = __float_as_uint(v);
+    return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
 }
 
-// Warp top-k with NV scores per lane kept in registers (E <= 32 NV).
+// Top-k (k <= 8) of E <= 32*NV scores of one warp: lane j holds scores
+// lane + 32 i as keys; each round takes the warp maximum (redux.sync) and, among
+// the lanes holding it, the lowest expert index, so equal scores go to the
+// lower index.  Writes the experts by descending score and their softmax
+// weights (over the selection, relative to the largest score).
 template <int NV>
 MW4_DEV void select_topk_warp_n(const float* sc, int E, int k, int32_t* idx_out, float* w_out) {
     const int lane = threadIdx.x & 31;
-    float v[NV];
+    uint32_t key[NV];
+    uint32_t live = 0;   // bit i: score lane + 32 i exists and is not taken
 #pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = (lane + 32 * i < E) ? sc[lane + 32 * i] : -INFINITY;
-    // all loops have compile-time bounds so that every array stays in registers
-    float top_v[8];
-    int top_i[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        float bv = -INFINITY;
+    for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < E ? order_key(sc[e]) : 0u;
+        if (e < E) live |= 1u << i;
+    }
+    int mine = 0;
+    float mval = 0.f;
+    for (int r = 0; r < k; ++r) {
+        uint32_t bk = 0;
         int bi = 0x7fffffff;
-        if (j < k) {
+        bool any = false;
 #pragma unroll
-            for (int i = 0; i < NV; ++i)   // ascending index within the lane: strict > keeps the lower one
-                if (v[i] > bv) { bv = v[i]; bi = lane + 32 * i; }
-        }
-        warp_argmax(bv, bi);
-        top_v[j] = bv;
-        top_i[j] = bi;
-        if (j < k) {
-#pragma unroll
-            for (int i = 0; i < NV; ++i)   // the owner marks it taken
-                if (lane + 32 * i == bi) v[i] = -INFINITY;
-        }
+        for (int i = 0; i < NV; ++i)   // ascending index in the lane: strict > keeps the lower one
+            if (((live >> i) & 1u) && (!any || key[i] > bk)) { bk = key[i]; bi = lane + 32 * i; any = true; }
+        const uint32_t wmax = __reduce_max_sync(0xffffffffu, any ? bk : 0u);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, (any && bk == wmax) ? (uint32_t)bi : 0xffffffffu);
+        if ((int)(win & 31) == lane) live &= ~(1u << (win >> 5));
+        if (lane == r) { mine = (int)win; mval = sc[win]; }
     }
-    // softmax over the selection, relative to the largest (the first) score
-    float z = 0.f, mine = 0.f;
-    int mi = 0;
+    const float v0 = __shfl_sync(0xffffffffu, mval, 0);
+    const float ex = lane < k ? expf(mval - v0) : 0.f;
+    float z = ex;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        if (j < k) z += expf(top_v[j] - top_v[0]);
-        if (j == lane) { mine = top_v[j]; mi = top_i[j]; }
-    }
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     if (lane < k) {
-        idx_out[lane] = mi;
-        w_out[lane] = expf(mine - top_v[0]) / z;
+        idx_out[lane] = mine;
+        w_out[lane] = ex / z;
     }
 }
 

@@ -139,10 +139,6 @@ MW4_DEV uint32_t ld_acquire_u32(const unsigned int* p) {
 // order-preserving integer keys; per round the warp maximum comes from
 // redux.sync, then the lowest index holding it.  Lane r < k returns the r-th
 // selection (index and score).
-MW4_DEV uint32_t order_key(float v) {
-    const uint32_t b = __float_as_uint(v);
-    return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);   // monotone: larger float, larger key
-}
 MW4_DEV void warp_topk_redux(const float* sc, int E, int k, int& sel_idx, float& sel_val) {
     const int lane = threadIdx.x & 31;
     uint32_t key[8];
