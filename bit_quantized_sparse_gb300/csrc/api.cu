@@ -36,7 +36,7 @@ WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o += up256(bytes); return at; };
     w.ctrl = take(sizeof(Ctrl));
-    w.logits = take(T * E * 4);
+    w.logits = take(kRouterSplit * T * E * 4);   // partial router scores
     w.router_a = take((E + kBM - 1) / kBM * kBM * 3 * H * 2);
     w.x16 = take(T * H * 2);
     w.topk_idx = take(T * k * 4);

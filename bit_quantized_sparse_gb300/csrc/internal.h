@@ -18,6 +18,7 @@ constexpr int kBK = 64;           // reduction columns per pipeline stage (= one
 constexpr int kDecodeMaxT = 16;   // largest decode batch
 constexpr int kFusedClustersPerExpert = 4;   // fused T=1 decode: 16 CTAs per expert in clusters of 4
 constexpr int kRouterRowsPerCta = 256;  // H rows per decode-router CTA
+constexpr int kRouterSplit = 2;         // prefill router: partial score arrays (halves of H)
 
 struct Ctrl;   // workspace control header (common.cuh)
 
@@ -45,7 +46,7 @@ struct RouteOut {
     int32_t* offsets;  // [E+1]
     int32_t* perm; int32_t* inv;
     int32_t* chunk_base;
-    float* logits;
+    float* logits;       // [kRouterSplit][T][E] partial router scores (tensor-core path), [T][E] otherwise
     uint16_t* router_a;  // [Epad][3H] bf16 split router weights (tensor-core scores); NULL: CUDA cores
     uint16_t* x16;     // fp16 copy of x written by the top-k kernel (NULL: not needed)
     int4* blkinfo; int32_t* ntiles;   // per-block records [max blocks] and tile counts [2]; NULL: no tile maps

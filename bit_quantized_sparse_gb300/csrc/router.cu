@@ -104,40 +104,45 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* __restri
     }
 }
 
-constexpr int kRtBN = 64;      // tokens per tile
-constexpr int kRtStages = 6;
+constexpr int kRtBN = 128;     // tokens per tile
+constexpr int kRtStages = 3;
+constexpr int kRtSplit = kRouterSplit;   // halves of H in separate CTAs; the top-k kernel adds the partial scores
 
 struct RouterTcArgs {
     const float* bias;
-    float* logits;   // [T][E]
+    float* logits;   // [kRtSplit][T][E] partial scores (the bias goes into the first)
     int T, H, E;
     unsigned int* status;
 };
 
-// One CTA: 128 experts x 64 tokens, K = 3H in 64-column steps.  Warp 0 issues
-// TMA for A and B, warp 1 allocates TMEM and issues the MMAs,
-// warps 4-7 write the scores (+ bias).
+// One CTA: 128 experts x 128 tokens over one half of H, in 64-column steps.  A
+// step brings the tile of x once and the hi, mid and lo tiles of W_r for the same
+// columns; the three terms go into three TMEM accumulators (3 x 128 columns).
+// Warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs (warp-uniform, one
+// elected lane), warps 4-7 write the scores.
 __global__ void __launch_bounds__(256, 1)
 router_tc_kernel(const __grid_constant__ RouterTcArgs a, const __grid_constant__ CUtensorMap mapA,
                  const __grid_constant__ CUtensorMap mapX) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr uint32_t A_BYTES = kBM * kBK * 2, B_BYTES = kRtBN * kBK * 2, STAGE = A_BYTES + B_BYTES;
+    constexpr uint32_t TILE = kBM * kBK * 2;            // 16 KB: 128 rows x 64 bf16
+    static_assert(kRtBN * kBK * 2 == TILE, "x and W_r tiles have the same size");
+    constexpr uint32_t STAGE = 4 * TILE;                // x, then W_r hi, mid, lo
     uint64_t* full = reinterpret_cast<uint64_t*>(base + kRtStages * STAGE);
     uint64_t* empty = full + kRtStages;
     uint64_t* accum = empty + kRtStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(accum + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1) + 1;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kRtBN;
-    const int nK = 3 * a.H / kBK, hsteps = a.H / kBK;
+    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kRtBN, kh = blockIdx.z;
+    const int hsteps = a.H / kBK, s0 = kh * hsteps / kRtSplit, s1 = (kh + 1) * hsteps / kRtSplit, nS = s1 - s0;
     if (tid == 0) {
         for (int s = 0; s < kRtStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         mbar_init(accum, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(tmem_slot, 4 * kRtBN);   // hi, mid, lo accumulators
+    if (warp == 1) tmem_alloc(tmem_slot, 512);   // hi, mid, lo accumulators at 0, 128, 256
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -145,29 +150,32 @@ router_tc_kernel(const __grid_constant__ RouterTcArgs a, const __grid_constant__
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&mapA);
         prefetch_tensormap(&mapX);
-        for (int ks = 0; ks < nK; ++ks) {
-            const int s = ks % kRtStages;
-            if (!mbar_wait(&empty[s], ((ks / kRtStages) & 1) ^ 1, abort_flag, a.status)) break;
+        for (int i = 0; i < nS; ++i) {
+            const int s = i % kRtStages, c = (s0 + i) * kBK;
+            if (!mbar_wait(&empty[s], ((i / kRtStages) & 1) ^ 1, abort_flag, a.status)) break;
             uint8_t* st = base + (size_t)s * STAGE;
             mbar_arrive_expect_tx(&full[s], STAGE);
-            tma_load_2d(st, &mapA, ks * kBK, m0, &full[s]);
-            tma_load_2d(st + A_BYTES, &mapX, (ks % hsteps) * kBK, n0, &full[s]);
+            tma_load_2d(st, &mapX, c, n0, &full[s]);
+            for (int part = 0; part < 3; ++part) tma_load_2d(st + (1 + part) * TILE, &mapA, part * a.H + c, m0, &full[s]);
         }
     } else if (warp == 1) {   // warp-uniform loop, one elected lane issues
         const uint32_t idesc = umma_idesc_bf16(kBM, kRtBN);
         bool ok = true;
-        for (int ks = 0; ks < nK; ++ks) {
-            const int s = ks % kRtStages;
-            if (!(ok = mbar_wait_warp(&full[s], (ks / kRtStages) & 1, abort_flag, a.status))) break;
+        for (int i = 0; i < nS; ++i) {
+            const int s = i % kRtStages;
+            if (!(ok = mbar_wait_warp(&full[s], (i / kRtStages) & 1, abort_flag, a.status))) break;
             tc_fence_after();
-            const uint32_t sa = smem_u32(base + (size_t)s * STAGE);
-            const uint64_t adesc0 = umma_desc_sw128(sa), bdesc0 = umma_desc_sw128(sa + A_BYTES);
+            const uint32_t sb = smem_u32(base + (size_t)s * STAGE);
+            const uint64_t bdesc0 = umma_desc_sw128(sb);
             // one accumulator per term: products of very different magnitude are
             // never summed inside the tensor core, only in fp32 in the epilogue
-            const int part = ks / hsteps, kp = ks % hsteps;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)   // +32 bytes per K=16 slice: +2 in the address field
-                umma_f16_elect(taddr + part * kRtBN, adesc0 + 2 * kk, bdesc0 + 2 * kk, idesc, (kp | kk) != 0);
+            for (int part = 0; part < 3; ++part) {
+                const uint64_t adesc0 = umma_desc_sw128(sb + (1 + part) * TILE);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)   // +32 bytes per K=16 slice: +2 in the address field
+                    umma_f16_elect(taddr + part * kRtBN, adesc0 + 2 * kk, bdesc0 + 2 * kk, idesc, (i | kk) != 0);
+            }
             umma_commit_elect(&empty[s]);
         }
         if (ok) umma_commit_elect(accum);
@@ -175,7 +183,8 @@ router_tc_kernel(const __grid_constant__ RouterTcArgs a, const __grid_constant__
         const int q = warp - 4, e = m0 + q * 32 + lane;
         if (mbar_wait(accum, 0, abort_flag, a.status)) {
             tc_fence_after();
-            const float bias = (e < a.E && a.bias) ? a.bias[e] : 0.f;
+            const float bias = (kh == 0 && e < a.E && a.bias) ? a.bias[e] : 0.f;
+            float* out = a.logits + (size_t)kh * a.T * a.E;
             for (int c0 = 0; c0 < kRtBN; c0 += 16) {
                 uint32_t vh[16], vm[16], vl[16];
                 const uint32_t ta = taddr + ((uint32_t)(q * 32) << 16) + c0;
@@ -187,17 +196,17 @@ router_tc_kernel(const __grid_constant__ RouterTcArgs a, const __grid_constant__
                 for (int j = 0; j < 16; ++j) {
                     const int t = n0 + c0 + j;
                     const float v = __uint_as_float(vh[j]) + (__uint_as_float(vm[j]) + __uint_as_float(vl[j]));
-                    if (e < a.E && t < a.T) a.logits[(size_t)t * a.E + e] = v + bias;
+                    if (e < a.E && t < a.T) out[(size_t)t * a.E + e] = v + bias;
                 }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(taddr, 4 * kRtBN);
+    if (warp == 1) tmem_dealloc(taddr, 512);
 }
 
-size_t router_tc_smem() { return 1024 + (size_t)kRtStages * (kBM * kBK * 2 + kRtBN * kBK * 2) + 2 * kRtStages * 8 + 32; }
+size_t router_tc_smem() { return 1024 + (size_t)kRtStages * 4 * kBM * kBK * 2 + 2 * kRtStages * 8 + 32; }
 
 // ---------------------------------------------------------------------------
 // per-token selection: one warp per token
@@ -207,6 +216,7 @@ constexpr int kTopkWarps = 8;
 // NIT >= ceil(H/256): 16-byte loads of the x row per lane, held in registers.
 template <int NIT>
 __global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 3 : 2) topk_kernel(const float* __restrict__ logits,
+                                                               int nsplit,   // 1 or 2 partial score arrays
                                                                const uint16_t* __restrict__ x,
                                                                const float* __restrict__ g, int T, int H, int E,
                                                                int k, int32_t* __restrict__ idx,
@@ -230,7 +240,11 @@ __global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 3 : 2) topk_kernel
         xv[it] = h < H ? *reinterpret_cast<const uint4*>(x + (size_t)t * H + h) : make_uint4(0, 0, 0, 0);
     }
     float* sc = sc_all + warp * E;
-    for (int e = lane; e < E; e += 32) sc[e] = logits[(size_t)t * E + e];
+    // partial scores added in order; unrolled so that the loads of a row are in flight together
+    const float* l0 = logits + (size_t)t * E;
+    const float* l1 = logits + ((size_t)T + t) * E;
+#pragma unroll 8
+    for (int e = lane; e < E; e += 32) sc[e] = nsplit > 1 ? l0[e] + l1[e] : l0[e];
     __syncwarp();
     select_topk_warp(sc, E, k, idx + (size_t)t * k, w + (size_t)t * k);
     float d = 0.f;
@@ -308,26 +322,27 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
             attr[dev] = router_tc_smem();
         }
         RouterTcArgs ra{L.router_bias, o.logits, T, L.H, L.E, o.status};
-        router_tc_kernel<<<dim3(Epad / kBM, (T + kRtBN - 1) / kRtBN), 256, router_tc_smem(), st>>>(ra, mA, mX);
+        router_tc_kernel<<<dim3(Epad / kBM, (T + kRtBN - 1) / kRtBN, kRtSplit), 256, router_tc_smem(), st>>>(ra, mA, mX);
     } else {
         dim3 grid((L.E + kRE - 1) / kRE, (T + kRT - 1) / kRT);
         router_scores_kernel<<<grid, 256, 0, st>>>(x, L.router_w, L.router_bias, o.logits, T, L.H, L.E);
     }
     trace_mark(st, 1);
+    const int nsplit = o.router_a ? kRtSplit : 1;
     const size_t sm = ((size_t)L.H + (size_t)kTopkWarps * L.E) * sizeof(float);
     const dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
     const int nit = (L.H + 255) / 256;   // H <= 4096
     if (nit <= 2)
-        topk_kernel<2><<<grid, block, sm, st>>>(o.logits, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
+        topk_kernel<2><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
                                                 o.gamma, o.x16, o.status);
     else if (nit <= 4)
-        topk_kernel<4><<<grid, block, sm, st>>>(o.logits, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
+        topk_kernel<4><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
                                                 o.gamma, o.x16, o.status);
     else if (nit <= 8)
-        topk_kernel<8><<<grid, block, sm, st>>>(o.logits, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
+        topk_kernel<8><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
                                                 o.gamma, o.x16, o.status);
     else
-        topk_kernel<16><<<grid, block, sm, st>>>(o.logits, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
+        topk_kernel<16><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
                                                  o.gamma, o.x16, o.status);
     trace_mark(st, 2);
     return cudaGetLastError();
