@@ -15,7 +15,13 @@ static int g_ntrace = 0;
 static int g_traced_kernels = 0;
 
 void trace_mark(cudaStream_t st, int i) {
-    if (g_trace && i < g_ntrace) cudaEventRecordWithFlags(g_trace[i], st, cudaEventRecordExternal);
+    if (!g_trace || i >= g_ntrace) return;
+    // inside a stream capture the event becomes a graph node; outside it is a plain record
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(g_trace[i], st, cudaEventRecordExternal);
+    else
+        cudaEventRecord(g_trace[i], st);
 }
 void trace_kernels(int n) {
     if (g_trace) g_traced_kernels = n;

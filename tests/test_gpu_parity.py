@@ -257,3 +257,27 @@ def test_gpu_workspace_errors(mw, torch):
     assert mw.moe_w4_forward_prefill(ctypes.byref(dl.c), 4, xd.data_ptr(), out.data_ptr(), ws.data_ptr(),
                                      need, st) == mw.MOE_W4_OK
     torch.cuda.synchronize()
+
+
+def test_trace_events_outside_capture(mw, torch):
+    """Kernel timing events recorded around an eager (not captured) call: the call
+    succeeds and every event completes in order."""
+    import ctypes
+    L, x, dl = layer_of(mw, "tiny_T4")
+    n = 9
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in evs])
+    mw._check(mw.moe_w4_set_trace_events(arr, n), "trace")
+    try:
+        out = mw.forward_prefill(dl, mw.tokens_to_device(x))
+        torch.cuda.synchronize()
+        nk = mw.moe_w4_last_traced_kernels()
+    finally:
+        mw.moe_w4_set_trace_events(None, 0)
+    assert nk == 8
+    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(nk)]
+    assert all(t >= 0 for t in times)
+    check_out(to_np_bits(out), O.moe_layer(L, x)["out"])
