@@ -232,10 +232,11 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, m
     p.x16 = o.x16;
     p.hh = at<uint16_t>(workspace, w.hh);
     p.ys = at<uint16_t>(workspace, w.ys);
+    p.xg = p.ys;
     p.max_tiles_gu = w.max_tiles_gu;
     p.max_tiles_dn = w.max_tiles_dn;
     p.status = o.status;
-    trace_kernels(8);
+    trace_kernels(9);
     return launch_status(launch_grouped_ffn(*L, T, x, out, p, stream));
 }
 

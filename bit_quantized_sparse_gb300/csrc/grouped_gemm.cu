@@ -15,7 +15,7 @@
 // rows, listed in a block map.)
 //
 // A tile is 128 weight rows (output features) x up to 128 grouped token rows,
-// reduced over K in 64-column steps (one quantisation group per row per step).
+// reduced over K in 128-column steps (two quantisation groups per row per step).
 // The weights are the M=128 operand ("swap AB"), so an expert with few rows
 // wastes only N columns, and N = rows rounded up to 16.
 //   gate/up:  D_g = Wg * X^T, D_u = Wu * X^T (two accumulators), epilogue
@@ -25,16 +25,18 @@
 // The kernel is persistent (one CTA per SM, tiles strided by the grid) and
 // warp-specialised:
 //   dequantisers  8 warps (gate/up: one thread per matrix row; down: two threads
-//                 per row, half a step each): codes from
-//                 shared memory -> fp16 -> tcgen05.st into an A ring in TMEM;
-//                 for gate/up they also gather the token rows of x16 (the B
-//                 operand) with cp.async a few steps ahead
+//                 per row, one group of the step each): codes from
+//                 shared memory -> fp16 -> tcgen05.st into an A ring in TMEM
 //   epilogue      8 warps, two per TMEM lane quarter: TMEM -> registers ->
 //                 global memory
-//   producer      1 warp, TMA: the step's packed codes (and, for down, the
-//                 contiguous B rows of hh), plus an L2 prefetch of the tile's codes
+//   producer      1 warp, TMA: the step's packed codes and the tile's B rows,
+//                 contiguous in grouped order (gate/up: the token rows copied
+//                 by gather_rows_kernel, or x16 itself for the shared expert;
+//                 down: hh), plus an L2 prefetch of the tile's codes and rows
 //   MMA           1 warp: TMEM allocation and the MMA loop (warp-uniform, one
 //                 elected lane issues tcgen05.mma with A read from tensor memory)
+// gather_rows_kernel first copies the token rows of x16 into grouped order, so
+// that every B row block is one contiguous range for TMA.
 // combine_kernel then sums, per token, its k rows of ys and the shared row in
 // a fixed order.
 #include "common.cuh"
@@ -48,14 +50,14 @@ struct GemmArgs {
     int M;                     // weight-row blocks per row block (tile = row block * M + weight-row block)
     const int32_t* offsets;    // expert group starts
     const int32_t* perm;       // grouped position -> t*k + j
-    const uint16_t* x16;       // [T][H] fp16 copy of the activations (gate/up)
     const float* topk_w;       // [T*k] (down)
     const float* gamma;        // [T] (down)
     const uint16_t* s0r; const uint16_t* b0r; const uint16_t* s1r; const uint16_t* b1r;   // routed
     const uint16_t* s0s; const uint16_t* b0s; const uint16_t* s1s; const uint16_t* b1s;   // shared
     const uint32_t* c0r; const uint32_t* c1r; const uint32_t* c0s; const uint32_t* c1s;   // codes (L2 prefetch)
     uint16_t* out;             // hh [.][I] or ys [.][H]
-    const uint16_t* hh_rows;   // down: the B rows (hh), for the L2 prefetch
+    const uint16_t* b_rows;    // B rows in grouped order (gate/up: xg, down: hh), for the L2 prefetch
+    const uint16_t* b_rows_sh; // the shared group's B rows (gate/up: x16 from row 0, down: hh)
     int E, k, T, H;            // H: row length of x
     int K;                     // reduction length (H or I)
     int rows_e;                // weight rows per expert (I or H)
@@ -63,8 +65,11 @@ struct GemmArgs {
     unsigned int* status;
 };
 
-constexpr uint32_t kCodesBytes = kBM * (kBK / 8) * 4;   // 4 KB of packed codes per matrix per step
-constexpr uint32_t kTileBytes = kBM * kBK * 2;          // 16 KB fp16 tile (A or B)
+constexpr int kGK = 128;                                // reduction columns per pipeline step
+static_assert(kGK == 2 * kGroup, "a step holds two quantisation groups");
+constexpr uint32_t kCodesBytes = kBM * (kGK / 8) * 4;   // 8 KB of packed codes per matrix per step
+constexpr uint32_t kSubBytes = kBN * 64 * 2;            // 16 KB: 128 B rows x 64 fp16 columns, 128-byte swizzle
+constexpr uint32_t kTileBytes = 2 * kSubBytes;          // B tile of one step: two K sub-tiles
 
 // Persistent-kernel geometry: warp roles, ring depths and the TMEM map.
 // The dequantised weights (the A operand) live in tensor memory, written by
@@ -74,7 +79,7 @@ template <bool DUAL>
 struct Geo {
     static constexpr int NMAT = DUAL ? 2 : 1;
     // 8 dequantiser warps: gate/up one thread per (matrix, weight row); down two
-    // threads per weight row, 32 of the step's 64 columns each (more threads in
+    // threads per weight row, one of the step's two groups each (more threads in
     // flight for the one matrix)
     static constexpr int kDeqWarps = 8;
     static constexpr int kDeqWarp0 = 0;                   // warp w reaches TMEM lanes 32*(w%4)..+31, so the
@@ -83,18 +88,19 @@ struct Geo {
     static constexpr int kProdWarp = kEpiWarp0 + kEpiWarps;   // TMA producer
     static constexpr int kMmaWarp = kProdWarp + 1;            // TMEM owner and MMA issuer
     static constexpr int kThreads = 32 * (kMmaWarp + 1);
-    static constexpr int SR = DUAL ? 8 : 10;              // codes (+B) ring in shared memory
+    static constexpr int SR = DUAL ? 4 : 5;               // codes + B ring in shared memory
     static constexpr uint32_t R_STAGE = kTileBytes + NMAT * kCodesBytes;   // B first (1024-aligned)
     static constexpr uint32_t ACC_COLS = NMAT * 128;      // TMEM columns per accumulator buffer
     static constexpr int ACC_BUFS = DUAL ? 1 : 2;
-    static constexpr uint32_t A_COLS = NMAT * (kBK / 2);  // TMEM columns per A stage (16-bit pairs)
+    static constexpr uint32_t A_COLS = NMAT * (kGK / 2);  // TMEM columns per A stage (16-bit pairs)
     static constexpr int SA = (512 - ACC_BUFS * ACC_COLS) / A_COLS;   // A ring in TMEM
     static constexpr uint32_t A_TMEM0 = ACC_BUFS * ACC_COLS;
     static constexpr size_t bytes() {
         return 1024 + (size_t)SR * R_STAGE + 2 * kBN * 4 + (2 * SR + SA + 4) * 8 + 16;
     }
 };
-static_assert(Geo<true>::SA == 4 && Geo<false>::SA == 8, "TMEM map");
+static_assert(Geo<true>::SA == 2 && Geo<false>::SA == 4, "TMEM map");
+static_assert(Geo<true>::bytes() <= 232448 && Geo<false>::bytes() <= 232448, "shared memory per CTA");
 static_assert(Geo<true>::SA <= Geo<true>::SR && Geo<false>::SA <= Geo<false>::SR, "A slots are freed by the stage barriers");
 
 MW4_DEV uint8_t* align1024(uint8_t* p) {
@@ -122,11 +128,12 @@ template <bool DUAL>
 __global__ void __launch_bounds__(Geo<DUAL>::kThreads, 1)
 grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap map0r,
                        const __grid_constant__ CUtensorMap map1r, const __grid_constant__ CUtensorMap map0s,
-                       const __grid_constant__ CUtensorMap map1s, const __grid_constant__ CUtensorMap mapb) {
+                       const __grid_constant__ CUtensorMap map1s, const __grid_constant__ CUtensorMap mapb,
+                       const __grid_constant__ CUtensorMap mapbs) {
     using GG = Geo<DUAL>;
     constexpr int NMAT = GG::NMAT, SR = GG::SR, SA = GG::SA;
     const int ntiles = a.ntiles[0];
-    const int G = a.K / kGroup, nK = a.K / kBK;
+    const int G = a.K / kGroup, nK = a.K / kGK;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align1024(smem_raw);
@@ -170,34 +177,33 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
 
     if (warp == GG::kProdWarp) {
         // ------------------------------------------------------------ TMA producer (warp-uniform)
-        // Per step: the packed codes of each matrix and, for down, the tile's
-        // contiguous B rows of hh (gate/up B rows are gathered by the
-        // dequantisers).
-        if (lane == 0) {
-            prefetch_tensormap(&map0r);
-            prefetch_tensormap(&map0s);
-            if (DUAL) { prefetch_tensormap(&map1r); prefetch_tensormap(&map1s); } else prefetch_tensormap(&mapb);
-        }
+        // Per step: the packed codes of each matrix and the step's 128 columns of the
+        // tile's B rows (two 64-column sub-tiles).
         int gk = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             const TileInfo ti = tile_info(a, t);
             const CUtensorMap* m0 = ti.sh ? &map0s : &map0r;
             const CUtensorMap* m1 = ti.sh ? &map1s : &map1r;
-            if (lane == 0) {   // the tile's packed codes are one contiguous range per matrix
+            const CUtensorMap* mb = ti.sh ? &mapbs : &mapb;
+            // gate/up's shared rows are rows r0.. of x16; every other B row block starts
+            // at its first grouped position
+            const int brow = (DUAL && ti.sh) ? ti.r0 : ti.p0;
+            if (lane == 0) {   // the tile's packed codes are one contiguous range per matrix, so are its B rows
                 prefetch_l2((ti.sh ? a.c0s : a.c0r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
                 if (DUAL) prefetch_l2((ti.sh ? a.c1s : a.c1r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
-                else prefetch_l2(a.hh_rows + (size_t)ti.p0 * a.K, (uint32_t)ti.nrows * a.K * 2);
+                prefetch_l2((ti.sh ? a.b_rows_sh : a.b_rows) + (size_t)brow * a.K, (uint32_t)ti.nrows * a.K * 2);
             }
-            const uint32_t bbytes = DUAL ? 0u : kTileBytes;
             for (int ks = 0; ks < nK; ++ks, ++gk) {
                 const int s = gk % SR;
                 if (!mbar_wait_warp(&r_empty[s], ((gk / SR) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&r_full[s], NMAT * kCodesBytes + bbytes);
-                    tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * (kBK / 8), ti.arow, &r_full[s]);
-                    if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * (kBK / 8), ti.arow, &r_full[s]);
-                    else tma_load_2d(B_of(s), &mapb, ks * kBK, ti.p0, &r_full[s]);
+                    mbar_arrive_expect_tx(&r_full[s], NMAT * kCodesBytes + kTileBytes);
+                    tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * (kGK / 8), ti.arow, &r_full[s]);
+                    if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * (kGK / 8), ti.arow, &r_full[s]);
+                    // the two 64-column halves of the step's B rows
+                    tma_load_2d(B_of(s), mb, ks * kGK, brow, &r_full[s]);
+                    tma_load_2d(B_of(s) + kSubBytes, mb, ks * kGK + 64, brow, &r_full[s]);
                 }
             }
         }
@@ -216,19 +222,20 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
             for (int ks = 0; ks < nK; ++ks, ++gk) {
                 const int sr = gk % SR, sa = gk % SA;
                 // a_full certifies both operands: the dequantisers arrive only after
-                // the step's codes (and, for down, its B rows) landed and, for
-                // gate/up, after their own gathered B rows landed
+                // the step's codes and B rows landed (r_full)
                 ok = mbar_wait_warp(&a_full[sa], (gk / SA) & 1, abort_flag, a.status);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t atm = taddr + GG::A_TMEM0 + sa * GG::A_COLS;
                 const uint64_t bdesc0 = umma_desc_sw128(smem_u32(B_of(sr)));
+                const uint64_t bdesc1 = umma_desc_sw128(smem_u32(B_of(sr) + kSubBytes));
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk) {
+                for (int kk = 0; kk < kGK / 16; ++kk) {
+                    // K=16 slice kk: sub-tile kk/4, +32 bytes per slice within it (+2 in the address field)
+                    const uint64_t bd = (kk < 4 ? bdesc0 : bdesc1) + 2 * (kk & 3);
 #pragma unroll
-                    for (int mat = 0; mat < NMAT; ++mat)   // +32 bytes per K=16 slice: +2 in the address field
-                        umma_f16_ts_elect(dacc + mat * 128, atm + mat * (kBK / 2) + kk * 8, bdesc0 + 2 * kk, idesc,
-                                          (ks | kk) != 0);
+                    for (int mat = 0; mat < NMAT; ++mat)
+                        umma_f16_ts_elect(dacc + mat * 128, atm + mat * (kGK / 2) + kk * 8, bd, idesc, (ks | kk) != 0);
                 }
                 umma_commit_elect(&r_empty[sr]);   // also frees A slot sa (see the dequantiser)
             }
@@ -237,46 +244,11 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     } else if (warp < GG::kEpiWarp0) {
         // ------------------------------------------------------------ dequantisation: one weight row per thread
         const int td = tid - 32 * GG::kDeqWarp0, row = td % 128;
-        const int mat = DUAL ? td / 128 : 0, hsel = DUAL ? -1 : td / 128;   // down: which 32-column half
-        const int sw = (row >> 2) & 1;   // 32-byte swizzle phase of this row's codes
+        const int mat = DUAL ? td / 128 : 0, hsel = DUAL ? -1 : td / 128;   // down: which group of the step
+        const int sw = (row >> 1) & 3;   // 64-byte swizzle phase of this row's codes
         const bool chunked = (G % 8) == 0;
         int gk = 0;
         bool ok = true;
-        // gate/up: these threads also gather the B rows (token rows of x16), kGatherAhead
-        // steps ahead of the step they dequantise; thread td copies half of tile row
-        // td/2 (four 16-byte chunks, 128-byte swizzle).  A stage is reused only after
-        // the MMAs of the step SR earlier, signalled on r_empty.
-        constexpr int kGatherAhead = 4;
-        static_assert(kGatherAhead < SR, "the gather must not wait on a stage the MMA still needs");
-        const int grow = td >> 1, gc0 = (td & 1) * 4;
-        int g_t = blockIdx.x, g_ks = 0, g_gk = 0, g_tok = -1;
-        auto g_setup = [&]() {
-            g_tok = -1;
-            if (g_t < ntiles) {
-                const TileInfo tg = tile_info(a, g_t);
-                if (grow < tg.nrows) g_tok = tg.sh ? tg.r0 + grow : a.perm[tg.p0 + grow] / a.k;
-            }
-        };
-        auto gather_step = [&]() -> bool {   // copies of step g_gk (an empty group past the last tile)
-            if (g_t < ntiles) {
-                const int s = g_gk % SR;
-                if (!mbar_wait(&r_empty[s], ((g_gk / SR) & 1) ^ 1, abort_flag, a.status)) return false;
-                if (g_tok >= 0) {
-                    uint8_t* dst = B_of(s) + grow * 128;
-                    const uint16_t* src = a.x16 + (size_t)g_tok * a.H + g_ks * kBK;
-#pragma unroll
-                    for (int c = gc0; c < gc0 + 4; ++c) cp_async_16(dst + ((c ^ (grow & 7)) << 4), src + c * 8);
-                }
-                ++g_gk;
-                if (++g_ks == nK) { g_ks = 0; g_t += gridDim.x; g_setup(); }
-            }
-            cp_async_commit();
-            return true;
-        };
-        if (DUAL) {
-            g_setup();
-            for (int i = 0; i < kGatherAhead && ok; ++i) ok = gather_step();
-        }
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             const TileInfo ti = tile_info(a, t);
             const uint16_t* sp = (mat == 0 ? (ti.sh ? a.s0s : a.s0r) : (ti.sh ? a.s1s : a.s1r)) + (size_t)(ti.arow + row) * G;
@@ -286,26 +258,23 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 sq = __ldg(reinterpret_cast<const uint4*>(sp));
                 bq = __ldg(reinterpret_cast<const uint4*>(bp));
             }
-            for (int k8 = 0; k8 < nK; k8 += 8) {
-                if (chunked && k8 + 8 < nK) {   // next eight steps' scales and biases
-                    sqn = __ldg(reinterpret_cast<const uint4*>(sp + k8 + 8));
-                    bqn = __ldg(reinterpret_cast<const uint4*>(bp + k8 + 8));
+            for (int k4 = 0; k4 < nK; k4 += 4) {   // four steps = eight groups per scale/bias load
+                if (chunked && k4 + 4 < nK) {
+                    sqn = __ldg(reinterpret_cast<const uint4*>(sp + 2 * (k4 + 4)));
+                    bqn = __ldg(reinterpret_cast<const uint4*>(bp + 2 * (k4 + 4)));
                 }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int ks = k8 + j;
+                for (int j = 0; j < 4; ++j) {
+                    const int ks = k4 + j;
                     if (ks >= nK) break;
-                    uint32_t s16, b16;
+                    uint32_t s2w, b2w;   // the step's two groups, bf16 pairs (low half first)
                     if (chunked) {
-                        const uint32_t sw2 = (j < 2 ? sq.x : j < 4 ? sq.y : j < 6 ? sq.z : sq.w);
-                        const uint32_t bw2 = (j < 2 ? bq.x : j < 4 ? bq.y : j < 6 ? bq.z : bq.w);
-                        s16 = (j & 1) ? (sw2 >> 16) : (sw2 & 0xFFFFu);
-                        b16 = (j & 1) ? (bw2 >> 16) : (bw2 & 0xFFFFu);
+                        s2w = (j == 0 ? sq.x : j == 1 ? sq.y : j == 2 ? sq.z : sq.w);
+                        b2w = (j == 0 ? bq.x : j == 1 ? bq.y : j == 2 ? bq.z : bq.w);
                     } else {
-                        s16 = sp[ks];
-                        b16 = bp[ks];
+                        s2w = (uint32_t)sp[2 * ks] | ((uint32_t)sp[2 * ks + 1] << 16);
+                        b2w = (uint32_t)bp[2 * ks] | ((uint32_t)bp[2 * ks + 1] << 16);
                     }
-                    if (DUAL && !(ok = gather_step())) break;   // B rows of step gk + kGatherAhead
                     const int sr = gk % SR, sa = gk % SA;
                     // A slot sa last served step gk - SA; the commit on r_empty of that
                     // step's stage fires once its MMAs are done (SA <= SR, so that
@@ -313,35 +282,35 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                     ok = mbar_wait(&r_full[sr], (gk / SR) & 1, abort_flag, a.status) &&
                          (gk < SA || mbar_wait(&r_empty[(gk - SA) % SR], ((gk - SA) / SR) & 1, abort_flag, a.status));
                     if (!ok) break;
-                    const uint8_t* cr = C_of(sr, mat) + row * 32;
-                    const float sf = bf16_bits_to_float((uint16_t)s16);
-                    const __half s_h = __float2half_rn(sf), s_h16 = __float2half_rn(sf * 0.0625f);
-                    const __half b_h = __float2half_rn(bf16_bits_to_float((uint16_t)b16));
-                    const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16);
-                    const __half2 b2 = __halves2half2(b_h, b_h);
+                    const uint8_t* cr = C_of(sr, mat) + row * 64;
                     tc_fence_after();   // the MMAs that read this A slot have completed
-                    // this thread's weight row -> its TMEM lane, 32 columns of fp16 pairs, in two halves
+                    // this thread's weight row -> its TMEM lane, 64 columns of fp16 pairs, in quads of 16
                     const uint32_t tdst =
-                        taddr + ((uint32_t)(row & ~31) << 16) + GG::A_TMEM0 + sa * GG::A_COLS + mat * (kBK / 2);
+                        taddr + ((uint32_t)(row & ~31) << 16) + GG::A_TMEM0 + sa * GG::A_COLS + mat * (kGK / 2);
 #pragma unroll
-                    for (int hlf = 0; hlf < 2; ++hlf) {
-                        if (!DUAL && hlf != hsel) continue;
-                        const uint4 w = *reinterpret_cast<const uint4*>(cr + ((hlf ^ sw) << 4));
-                        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-                        uint32_t o[16];
+                    for (int grp = 0; grp < 2; ++grp) {
+                        if (!DUAL && grp != hsel) continue;
+                        const float sf = bf16_bits_to_float((uint16_t)(grp ? (s2w >> 16) : (s2w & 0xFFFFu)));
+                        const __half s_h = __float2half_rn(sf), s_h16 = __float2half_rn(sf * 0.0625f);
+                        const __half b_h = __float2half_rn(bf16_bits_to_float((uint16_t)(grp ? (b2w >> 16) : (b2w & 0xFFFFu))));
+                        const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16);
+                        const __half2 b2 = __halves2half2(b_h, b_h);
 #pragma unroll
-                        for (int wi = 0; wi < 4; ++wi) {
-                            uint32_t q4[4];
-                            dequant8_f16(words[wi], s2, s2_16, b2, q4);
-                            o[4 * wi] = q4[0]; o[4 * wi + 1] = q4[1]; o[4 * wi + 2] = q4[2]; o[4 * wi + 3] = q4[3];
+                        for (int qq = 0; qq < 2; ++qq) {
+                            const int q = 2 * grp + qq;
+                            const uint4 w = *reinterpret_cast<const uint4*>(cr + ((q ^ sw) << 4));
+                            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+                            uint32_t o[16];
+#pragma unroll
+                            for (int wi = 0; wi < 4; ++wi) {
+                                uint32_t q4[4];
+                                dequant8_f16(words[wi], s2, s2_16, b2, q4);
+                                o[4 * wi] = q4[0]; o[4 * wi + 1] = q4[1]; o[4 * wi + 2] = q4[2]; o[4 * wi + 3] = q4[3];
+                            }
+                            tmem_st16(tdst + 16 * q, o);
                         }
-                        tmem_st16(tdst + 16 * hlf, o);
                     }
                     tmem_wait_st();
-                    if (DUAL) {   // this thread's B copies of step gk have landed; hand them to the async proxy
-                        cp_async_wait<kGatherAhead>();
-                        fence_proxy_async_smem();
-                    }
                     tc_fence_before();
                     mbar_arrive(&a_full[sa]);
                     ++gk;
@@ -351,7 +320,6 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 bq = bqn;
             }
         }
-        if (DUAL) cp_async_wait<0>();   // no copy in flight when the CTA leaves
     } else {
         // ------------------------------------------------------------ epilogue: TMEM -> registers -> global
         const int ew = warp - GG::kEpiWarp0, q = ew & 3, half = ew >> 2;
@@ -404,6 +372,28 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     tc_fence_before();
     __syncthreads();
     if (warp == GG::kMmaWarp) tmem_dealloc(taddr, 512);
+}
+
+// xg[p] = x16[perm[p] / k] for the T*k routed grouped positions p: one warp per
+// row, 16-byte loads and stores, eight in flight per lane.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x16,
+                                                          const int32_t* __restrict__ perm,
+                                                          uint16_t* __restrict__ xg, int nrows, int H, int k) {
+    const int p = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (p >= nrows) return;
+    const int t = __ldg(perm + p) / k;
+    const uint4* src = reinterpret_cast<const uint4*>(x16 + (size_t)t * H);
+    uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
+    const int n = H / 8;
+    for (int c0 = lane; c0 < n; c0 += 32 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (c0 + 32 * u < n) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (c0 + 32 * u < n) dst[c0 + 32 * u] = v[u];
+    }
 }
 
 // out[t] = bf16( sum_j ys[inv[t*k + j]] + ys[T*k + t] ) with ys in fp16 and
@@ -470,21 +460,22 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
                                cudaStream_t st) {
     const int H = L.H, I = L.I, E = L.E, k = L.top_k;
     const uint64_t rows_all = (uint64_t)T * k + T;
-    CUtensorMap mg, mu, msg, msu, md, msd, mh;
+    CUtensorMap mg, mu, msg, msu, md, msd, mh, mxg, mx;
     const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
-    const auto SW32 = CU_TENSOR_MAP_SWIZZLE_32B;   // 32-byte code rows: bank-conflict-free per-row reads
-    bool ok = make_map(&mg, U32, 4, L.gate.codes, (uint64_t)E * I, H / 8, kBM, kBK / 8, SW32) &&
-              make_map(&mu, U32, 4, L.up.codes, (uint64_t)E * I, H / 8, kBM, kBK / 8, SW32) &&
-              make_map(&msg, U32, 4, L.sh_gate.codes, I, H / 8, kBM, kBK / 8, SW32) &&
-              make_map(&msu, U32, 4, L.sh_up.codes, I, H / 8, kBM, kBK / 8, SW32) &&
-              make_map(&md, U32, 4, L.down.codes, (uint64_t)E * H, I / 8, kBM, kBK / 8, SW32) &&
-              make_map(&msd, U32, 4, L.sh_down.codes, H, I / 8, kBM, kBK / 8, SW32) &&
-              make_map(&mh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hh, rows_all, I, kBN, kBK,
+    const auto SW64 = CU_TENSOR_MAP_SWIZZLE_64B;   // 64-byte code rows: bank-conflict-free per-row reads
+    constexpr uint32_t cw = kGK / 8;                // code words per row per step
+    bool ok = make_map(&mg, U32, 4, L.gate.codes, (uint64_t)E * I, H / 8, kBM, cw, SW64) &&
+              make_map(&mu, U32, 4, L.up.codes, (uint64_t)E * I, H / 8, kBM, cw, SW64) &&
+              make_map(&msg, U32, 4, L.sh_gate.codes, I, H / 8, kBM, cw, SW64) &&
+              make_map(&msu, U32, 4, L.sh_up.codes, I, H / 8, kBM, cw, SW64) &&
+              make_map(&md, U32, 4, L.down.codes, (uint64_t)E * H, I / 8, kBM, cw, SW64) &&
+              make_map(&msd, U32, 4, L.sh_down.codes, H, I / 8, kBM, cw, SW64) &&
+              make_map(&mh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hh, rows_all, I, kBN, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&mxg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.xg, (uint64_t)T * k, H, kBN, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x16, (uint64_t)T, H, kBN, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B);
-    // x16 rows for tile::gather4: box one row high, 64 columns, 128-byte swizzle
-    CUtensorMap mx;
-    ok = ok && make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x16, (uint64_t)T, H, 1, kBK,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
 
     const size_t sm_gu = Geo<true>::bytes(), sm_dn = Geo<false>::bytes();
@@ -509,7 +500,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     }
 
     GemmArgs a{};
-    a.ntiles = p.ntiles; a.offsets = p.offsets; a.perm = p.perm; a.x16 = p.x16;
+    a.ntiles = p.ntiles; a.offsets = p.offsets; a.perm = p.perm;
     a.topk_w = p.topk_w; a.gamma = p.gamma;
     a.E = E; a.k = k; a.T = T; a.H = H; a.status = p.status;
 
@@ -518,26 +509,29 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     a.s0r = L.gate.scales; a.b0r = L.gate.biases; a.s1r = L.up.scales; a.b1r = L.up.biases;
     a.s0s = L.sh_gate.scales; a.b0s = L.sh_gate.biases; a.s1s = L.sh_up.scales; a.b1s = L.sh_up.biases;
     a.c0r = L.gate.codes; a.c1r = L.up.codes; a.c0s = L.sh_gate.codes; a.c1s = L.sh_up.codes;
-    a.out = p.hh; a.K = H; a.rows_e = I; a.out_cols = I;
+    a.out = p.hh; a.K = H; a.rows_e = I; a.out_cols = I; a.b_rows = p.xg; a.b_rows_sh = p.x16;
     // persistent: one CTA per SM (never more CTAs than the largest tile count)
     const int grid_gu = p.max_tiles_gu < nsm ? p.max_tiles_gu : nsm;
-    grouped_w4_gemm_kernel<true><<<grid_gu, Geo<true>::kThreads, sm_gu, st>>>(a, mg, mu, msg, msu, mx);
+    const int nrg = T * k;
+    gather_rows_kernel<<<(unsigned)((nrg + 7) / 8), 256, 0, st>>>(p.x16, p.perm, p.xg, nrg, H, k);
     trace_mark(st, 6);
+    grouped_w4_gemm_kernel<true><<<grid_gu, Geo<true>::kThreads, sm_gu, st>>>(a, mg, mu, msg, msu, mxg, mx);
+    trace_mark(st, 7);
 
     // down: A = Wd rows (H per expert), K = I, B = hh rows, out = ys [.][H]
     GemmArgs b = a;
     b.M = H / kBM; b.ntiles = p.ntiles + 1;
     b.s0r = L.down.scales; b.b0r = L.down.biases; b.s1r = nullptr; b.b1r = nullptr;
     b.s0s = L.sh_down.scales; b.b0s = L.sh_down.biases; b.s1s = nullptr; b.b1s = nullptr;
-    b.c0r = L.down.codes; b.c1r = nullptr; b.c0s = L.sh_down.codes; b.c1s = nullptr; b.hh_rows = p.hh;
+    b.c0r = L.down.codes; b.c1r = nullptr; b.c0s = L.sh_down.codes; b.c1s = nullptr; b.b_rows = p.hh; b.b_rows_sh = p.hh;
     b.out = p.ys; b.K = I; b.rows_e = H; b.out_cols = H;
     const int grid_dn = p.max_tiles_dn < nsm ? p.max_tiles_dn : nsm;
-    grouped_w4_gemm_kernel<false><<<grid_dn, Geo<false>::kThreads, sm_dn, st>>>(b, md, md, msd, msd, mh);
-    trace_mark(st, 7);
+    grouped_w4_gemm_kernel<false><<<grid_dn, Geo<false>::kThreads, sm_dn, st>>>(b, md, md, msd, msd, mh, mh);
+    trace_mark(st, 8);
 
     const size_t nthr = (size_t)T * (H / 8);
     combine_kernel<<<(unsigned)((nthr + 255) / 256), 256, 0, st>>>(p.ys, p.inv, out, T, H, k);
-    trace_mark(st, 8);
+    trace_mark(st, 9);
     return cudaGetLastError();
 }
 

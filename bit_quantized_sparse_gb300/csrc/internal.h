@@ -89,6 +89,8 @@ struct PrefillWs {
     const uint16_t* x16;  // fp16 [T][H]
     uint16_t* hh;   // fp16 [T*k + T][I]
     uint16_t* ys;   // fp16 [T*k + T][H]
+    uint16_t* xg;   // fp16 [T*k][H]: token rows in grouped order, the gate/up B operand; shares ys's
+                    // memory (read by gate/up only, before down writes ys)
     int max_tiles_gu, max_tiles_dn;
     unsigned int* status;
 };

@@ -264,7 +264,7 @@ def test_trace_events_outside_capture(mw, torch):
     succeeds and every event completes in order."""
     import ctypes
     L, x, dl = layer_of(mw, "tiny_T4")
-    n = 9
+    n = 10
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
     for e in evs:
         e.record()
@@ -277,7 +277,7 @@ def test_trace_events_outside_capture(mw, torch):
         nk = mw.moe_w4_last_traced_kernels()
     finally:
         mw.moe_w4_set_trace_events(None, 0)
-    assert nk == 8
+    assert nk == 9
     times = [evs[i].elapsed_time(evs[i + 1]) for i in range(nk)]
     assert all(t >= 0 for t in times)
     check_out(to_np_bits(out), O.moe_layer(L, x)["out"])
