@@ -85,23 +85,30 @@ struct Geo {
     static constexpr int kDeqWarp0 = 0;                   // warp w reaches TMEM lanes 32*(w%4)..+31, so the
     static constexpr int kEpiWarp0 = kDeqWarp0 + kDeqWarps;   // dequantiser and epilogue groups start at w%4 == 0
     static constexpr int kEpiWarps = 8;                   // two per TMEM lane group, columns interleaved
-    static constexpr int kProdWarp = kEpiWarp0 + kEpiWarps;   // TMA producer
-    static constexpr int kMmaWarp = kProdWarp + 1;            // TMEM owner and MMA issuer
+    static constexpr int kProdWarp = kEpiWarp0 + kEpiWarps;   // TMA producer of the codes
+    static constexpr int kProdBWarp = kProdWarp + 1;          // TMA producer of the B rows
+    static constexpr int kMmaWarp = kProdBWarp + 1;           // TMEM owner and MMA issuer
     static constexpr int kThreads = 32 * (kMmaWarp + 1);
-    static constexpr int SR = DUAL ? 4 : 5;               // codes + B ring in shared memory
-    static constexpr uint32_t R_STAGE = kTileBytes + NMAT * kCodesBytes;   // B first (1024-aligned)
+    // Two rings in shared memory: the codes, freed as soon as the dequantisers
+    // have read a step, and the B rows, freed when the step's MMAs complete.
+    // The codes thus run several steps ahead of the dequantisers, whatever the
+    // MMAs' lag.
+    static constexpr int SC = DUAL ? 4 : 8;
+    static constexpr int SB = 4;
+    static constexpr uint32_t C_STAGE = NMAT * kCodesBytes;
     static constexpr uint32_t ACC_COLS = NMAT * 128;      // TMEM columns per accumulator buffer
     static constexpr int ACC_BUFS = DUAL ? 1 : 2;
     static constexpr uint32_t A_COLS = NMAT * (kGK / 2);  // TMEM columns per A stage (16-bit pairs)
     static constexpr int SA = (512 - ACC_BUFS * ACC_COLS) / A_COLS;   // A ring in TMEM
     static constexpr uint32_t A_TMEM0 = ACC_BUFS * ACC_COLS;
     static constexpr size_t bytes() {
-        return 1024 + (size_t)SR * R_STAGE + 2 * kBN * 4 + (2 * SR + SA + 4) * 8 + 16;
+        return 1024 + (size_t)SB * kTileBytes + (size_t)SC * C_STAGE + 2 * kBN * 4 + (2 * SB + 2 * SC + SA + 4) * 8 +
+               16;
     }
 };
 static_assert(Geo<true>::SA == 2 && Geo<false>::SA == 4, "TMEM map");
 static_assert(Geo<true>::bytes() <= 232448 && Geo<false>::bytes() <= 232448, "shared memory per CTA");
-static_assert(Geo<true>::SA <= Geo<true>::SR && Geo<false>::SA <= Geo<false>::SR, "A slots are freed by the stage barriers");
+static_assert(Geo<true>::SA <= Geo<true>::SB && Geo<false>::SA <= Geo<false>::SB, "A slots are freed by the B-ring barriers");
 
 MW4_DEV uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -131,32 +138,39 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                        const __grid_constant__ CUtensorMap map1s, const __grid_constant__ CUtensorMap mapb,
                        const __grid_constant__ CUtensorMap mapbs) {
     using GG = Geo<DUAL>;
-    constexpr int NMAT = GG::NMAT, SR = GG::SR, SA = GG::SA;
+    constexpr int NMAT = GG::NMAT, SC = GG::SC, SB = GG::SB, SA = GG::SA;
     const int ntiles = a.ntiles[0];
     const int G = a.K / kGroup, nK = a.K / kGK;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align1024(smem_raw);
-    uint8_t* rring = base;
-    auto B_of = [&](int s) { return rring + (size_t)s * GG::R_STAGE; };
+    uint8_t* bring = base;                                   // [SB][kTileBytes], 1024-aligned stages
+    uint8_t* cring = bring + (size_t)SB * kTileBytes;        // [SC][NMAT][kCodesBytes]
+    auto B_of = [&](int s) { return bring + (size_t)s * kTileBytes; };
     auto C_of = [&](int s, int mat) {
-        return reinterpret_cast<const uint8_t*>(rring + (size_t)s * GG::R_STAGE + kTileBytes + mat * kCodesBytes);
+        return reinterpret_cast<const uint8_t*>(cring + (size_t)s * GG::C_STAGE + mat * kCodesBytes);
     };
-    float* col_scale = reinterpret_cast<float*>(rring + (size_t)SR * GG::R_STAGE);   // [2][kBN]
+    float* col_scale = reinterpret_cast<float*>(cring + (size_t)SC * GG::C_STAGE);   // [2][kBN]
     uint64_t* bars = reinterpret_cast<uint64_t*>(col_scale + 2 * kBN);
-    uint64_t* r_full = bars;
-    uint64_t* r_empty = bars + SR;
-    uint64_t* a_full = bars + 2 * SR;
-    uint64_t* acc_full = bars + 2 * SR + SA;
+    uint64_t* c_full = bars;
+    uint64_t* c_empty = c_full + SC;
+    uint64_t* b_full = c_empty + SC;
+    uint64_t* b_empty = b_full + SB;
+    uint64_t* a_full = b_empty + SB;
+    uint64_t* acc_full = a_full + SA;
     uint64_t* acc_empty = acc_full + 2;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_empty + 2);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2) + 1;
 
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     if (tid == 0) {
-        for (int s = 0; s < SR; ++s) {
-            mbar_init(&r_full[s], 1);
-            mbar_init(&r_empty[s], 1);
+        for (int s = 0; s < SC; ++s) {
+            mbar_init(&c_full[s], 1);
+            mbar_init(&c_empty[s], 32 * GG::kDeqWarps);
+        }
+        for (int s = 0; s < SB; ++s) {
+            mbar_init(&b_full[s], 1);
+            mbar_init(&b_empty[s], 1);
         }
         for (int s = 0; s < SA; ++s) {
             mbar_init(&a_full[s], 32 * GG::kDeqWarps);
@@ -176,34 +190,58 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     const uint32_t taddr = *tmem_slot;
 
     if (warp == GG::kProdWarp) {
-        // ------------------------------------------------------------ TMA producer (warp-uniform)
-        // Per step: the packed codes of each matrix and the step's 128 columns of the
-        // tile's B rows (two 64-column sub-tiles).
+        // ------------------------------------------------------------ TMA producer: codes (warp-uniform)
+        // Per step: the packed codes of each matrix (128 weight rows x 16 words).
+        if (lane == 0) {
+            prefetch_tensormap(&map0r);
+            prefetch_tensormap(&map0s);
+            if (DUAL) { prefetch_tensormap(&map1r); prefetch_tensormap(&map1s); }
+        }
         int gk = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
             const TileInfo ti = tile_info(a, t);
             const CUtensorMap* m0 = ti.sh ? &map0s : &map0r;
             const CUtensorMap* m1 = ti.sh ? &map1s : &map1r;
+            if (lane == 0) {   // the tile's packed codes are one contiguous range per matrix
+                prefetch_l2((ti.sh ? a.c0s : a.c0r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
+                if (DUAL) prefetch_l2((ti.sh ? a.c1s : a.c1r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
+            }
+            for (int ks = 0; ks < nK; ++ks, ++gk) {
+                const int s = gk % SC;
+                if (!mbar_wait_warp(&c_empty[s], ((gk / SC) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&c_full[s], NMAT * kCodesBytes);
+                    tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * (kGK / 8), ti.arow, &c_full[s]);
+                    if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * (kGK / 8), ti.arow, &c_full[s]);
+                }
+            }
+        }
+    } else if (warp == GG::kProdBWarp) {
+        // ------------------------------------------------------------ TMA producer: B rows (warp-uniform)
+        // Per step: the step's 128 columns of the tile's B rows (two 64-column
+        // sub-tiles).
+        if (lane == 0) {
+            prefetch_tensormap(&mapb);
+            prefetch_tensormap(&mapbs);
+        }
+        int gk = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const TileInfo ti = tile_info(a, t);
             const CUtensorMap* mb = ti.sh ? &mapbs : &mapb;
             // gate/up's shared rows are rows r0.. of x16; every other B row block starts
             // at its first grouped position
             const int brow = (DUAL && ti.sh) ? ti.r0 : ti.p0;
-            if (lane == 0) {   // the tile's packed codes are one contiguous range per matrix, so are its B rows
-                prefetch_l2((ti.sh ? a.c0s : a.c0r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
-                if (DUAL) prefetch_l2((ti.sh ? a.c1s : a.c1r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
+            if (lane == 0)   // the tile's B rows are one contiguous range
                 prefetch_l2((ti.sh ? a.b_rows_sh : a.b_rows) + (size_t)brow * a.K, (uint32_t)ti.nrows * a.K * 2);
-            }
             for (int ks = 0; ks < nK; ++ks, ++gk) {
-                const int s = gk % SR;
-                if (!mbar_wait_warp(&r_empty[s], ((gk / SR) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                const int s = gk % SB;
+                if (!mbar_wait_warp(&b_empty[s], ((gk / SB) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&r_full[s], NMAT * kCodesBytes + kTileBytes);
-                    tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * (kGK / 8), ti.arow, &r_full[s]);
-                    if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * (kGK / 8), ti.arow, &r_full[s]);
-                    // the two 64-column halves of the step's B rows
-                    tma_load_2d(B_of(s), mb, ks * kGK, brow, &r_full[s]);
-                    tma_load_2d(B_of(s) + kSubBytes, mb, ks * kGK + 64, brow, &r_full[s]);
+                    mbar_arrive_expect_tx(&b_full[s], kTileBytes);
+                    tma_load_2d(B_of(s), mb, ks * kGK, brow, &b_full[s]);
+                    tma_load_2d(B_of(s) + kSubBytes, mb, ks * kGK + 64, brow, &b_full[s]);
                 }
             }
         }
@@ -220,15 +258,15 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
             tc_fence_after();
             const uint32_t dacc = taddr + b * GG::ACC_COLS;
             for (int ks = 0; ks < nK; ++ks, ++gk) {
-                const int sr = gk % SR, sa = gk % SA;
-                // a_full certifies both operands: the dequantisers arrive only after
-                // the step's codes and B rows landed (r_full)
-                ok = mbar_wait_warp(&a_full[sa], (gk / SA) & 1, abort_flag, a.status);
+                const int sb = gk % SB, sa = gk % SA;
+                // A from the dequantisers (a_full), B from the TMA (b_full)
+                ok = mbar_wait_warp(&a_full[sa], (gk / SA) & 1, abort_flag, a.status) &&
+                     mbar_wait_warp(&b_full[sb], (gk / SB) & 1, abort_flag, a.status);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t atm = taddr + GG::A_TMEM0 + sa * GG::A_COLS;
-                const uint64_t bdesc0 = umma_desc_sw128(smem_u32(B_of(sr)));
-                const uint64_t bdesc1 = umma_desc_sw128(smem_u32(B_of(sr) + kSubBytes));
+                const uint64_t bdesc0 = umma_desc_sw128(smem_u32(B_of(sb)));
+                const uint64_t bdesc1 = umma_desc_sw128(smem_u32(B_of(sb) + kSubBytes));
 #pragma unroll
                 for (int kk = 0; kk < kGK / 16; ++kk) {
                     // K=16 slice kk: sub-tile kk/4, +32 bytes per slice within it (+2 in the address field)
@@ -237,7 +275,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                     for (int mat = 0; mat < NMAT; ++mat)
                         umma_f16_ts_elect(dacc + mat * 128, atm + mat * (kGK / 2) + kk * 8, bd, idesc, (ks | kk) != 0);
                 }
-                umma_commit_elect(&r_empty[sr]);   // also frees A slot sa (see the dequantiser)
+                umma_commit_elect(&b_empty[sb]);   // also frees A slot sa (see the dequantiser)
             }
             if (ok) umma_commit_elect(&acc_full[b]);
         }
@@ -275,14 +313,14 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         s2w = (uint32_t)sp[2 * ks] | ((uint32_t)sp[2 * ks + 1] << 16);
                         b2w = (uint32_t)bp[2 * ks] | ((uint32_t)bp[2 * ks + 1] << 16);
                     }
-                    const int sr = gk % SR, sa = gk % SA;
-                    // A slot sa last served step gk - SA; the commit on r_empty of that
-                    // step's stage fires once its MMAs are done (SA <= SR, so that
+                    const int sc = gk % SC, sa = gk % SA;
+                    // A slot sa last served step gk - SA; the commit on b_empty of that
+                    // step's B stage fires once its MMAs are done (SA <= SB, so that
                     // barrier cannot have moved on by a further phase meanwhile)
-                    ok = mbar_wait(&r_full[sr], (gk / SR) & 1, abort_flag, a.status) &&
-                         (gk < SA || mbar_wait(&r_empty[(gk - SA) % SR], ((gk - SA) / SR) & 1, abort_flag, a.status));
+                    ok = mbar_wait(&c_full[sc], (gk / SC) & 1, abort_flag, a.status) &&
+                         (gk < SA || mbar_wait(&b_empty[(gk - SA) % SB], ((gk - SA) / SB) & 1, abort_flag, a.status));
                     if (!ok) break;
-                    const uint8_t* cr = C_of(sr, mat) + row * 64;
+                    const uint8_t* cr = C_of(sc, mat) + row * 64;
                     tc_fence_after();   // the MMAs that read this A slot have completed
                     // this thread's weight row -> its TMEM lane, 64 columns of fp16 pairs, in quads of 16
                     const uint32_t tdst =
@@ -311,6 +349,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         }
                     }
                     tmem_wait_st();
+                    mbar_arrive(&c_empty[sc]);   // this thread's codes of the step are read
                     tc_fence_before();
                     mbar_arrive(&a_full[sa]);
                     ++gk;
