@@ -19,9 +19,10 @@
 // The weights are the M=128 operand ("swap AB"), so an expert with few rows
 // wastes only N columns, and N = rows rounded up to 16.
 //   gate/up:  D_g = Wg * X^T, D_u = Wu * X^T (two accumulators), epilogue
-//             h = silu(D_g) * D_u -> hh[p][i] fp16
-//   down:     D = Wd * H^T, epilogue scales column p by its routing weight
-//             (or the shared gate) -> ys[p][o] fp16
+//             h = w_p * silu(D_g) * D_u -> hh[p][i] fp16, w_p the routing weight
+//             of grouped row p (or the shared gate): the down projection is
+//             linear, so weighting its input weights its output
+//   down:     D = Wd * H^T -> ys[p][o] fp16
 // The kernel is persistent (one CTA per SM, tiles strided by the grid) and
 // warp-specialised:
 //   dequantisers  8 warps (gate/up: one thread per matrix row; down: two threads
@@ -50,8 +51,8 @@ struct GemmArgs {
     int M;                     // weight-row blocks per row block (tile = row block * M + weight-row block)
     const int32_t* offsets;    // expert group starts
     const int32_t* perm;       // grouped position -> t*k + j
-    const float* topk_w;       // [T*k] (down)
-    const float* gamma;        // [T] (down)
+    const float* topk_w;       // [T*k] (gate/up epilogue)
+    const float* gamma;        // [T] (gate/up epilogue)
     const uint16_t* s0r; const uint16_t* b0r; const uint16_t* s1r; const uint16_t* b1r;   // routed
     const uint16_t* s0s; const uint16_t* b0s; const uint16_t* s1s; const uint16_t* b1s;   // shared
     const uint32_t* c0r; const uint32_t* c1r; const uint32_t* c0s; const uint32_t* c1s;   // codes (L2 prefetch)
@@ -366,10 +367,14 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         int it = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const TileInfo ti = tile_info(a, t);
-            const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS;
-            if (!DUAL) {   // per-column output scale of this tile, fetched while the MMAs run
+            const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS, cb = it & 1;
+            // gate/up: the weight of each column of the tile (its routing weight, or the
+            // shared gate) is applied to h, so that the down projection's output needs
+            // none; fetched while the MMAs run (two buffers: a thread writes a buffer
+            // only after every thread has passed the previous tile's barrier)
+            if (DUAL) {
                 if (et < ti.nrows)
-                    col_scale[b * kBN + et] = ti.sh ? a.gamma[ti.r0 + et] : a.topk_w[a.perm[ti.p0 + et]];
+                    col_scale[cb * kBN + et] = ti.sh ? a.gamma[ti.r0 + et] : a.topk_w[a.perm[ti.p0 + et]];
                 asm volatile("bar.sync 2, 256;" ::: "memory");
             }
             if (!mbar_wait(&acc_full[b], use & 1, abort_flag, a.status)) break;
@@ -386,12 +391,22 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 // column n of the tile is grouped row p0 + n: one pointer per chunk, rows
                 // out_cols apart; a full chunk runs without per-element branches
                 uint16_t* op = a.out + (size_t)(ti.p0 + c0) * a.out_cols + ocol;
-                const float* cs = col_scale + b * kBN + c0;
-                bool bad = false;
+                float cs[16];
+                if (DUAL) {
+                    const float4* c4 = reinterpret_cast<const float4*>(col_scale + cb * kBN + c0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float4 f = c4[i];
+                        cs[4 * i] = f.x; cs[4 * i + 1] = f.y; cs[4 * i + 2] = f.z; cs[4 * i + 3] = f.w;
+                    }
+                }
+                // range check on the running maximum of |v| (the values are finite: fp16
+                // operands, fp32 sums far below the fp32 limit)
+                float vmax = 0.f;
                 auto emit = [&](int j) {
-                    const float v = DUAL ? silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j])
-                                         : __uint_as_float(g[j]) * cs[j];
-                    bad |= !(fabsf(v) <= 65504.f);
+                    const float v = DUAL ? silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]) * cs[j]
+                                         : __uint_as_float(g[j]);
+                    vmax = fmaxf(vmax, fabsf(v));
                     op[(size_t)j * a.out_cols] = __half_as_ushort(__float2half_rn(v));
                 };
                 if (c0 + 16 <= ti.nrows) {
@@ -402,7 +417,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                     for (int j = 0; j < 16; ++j)
                         if (j < ti.nrows - c0) emit(j);
                 }
-                if (bad) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
+                if (!(vmax <= 65504.f)) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
             }
             tc_fence_before();
             mbar_arrive(&acc_empty[b]);

@@ -138,12 +138,13 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
 
 /* Layer output for a prefill batch, T >= 1 (section "Dequantise weights
  * during matrix multiplication"): routing as moe_w4_route, then grouped W4
- * GEMMs on the tensor cores (dequantised fp16 tiles in shared memory, fp16
- * activations, fp32 accumulators in tensor memory) with a SwiGLU epilogue, and
- * a weighted un-permute that adds the gated shared expert.  out bf16 [T][H].
- * The activations x, the SwiGLU output and each expert's weighted output must
- * stay within the fp16 range (|v| <= 65504); otherwise the status word gets
- * MOE_W4_STATUS_FP16_RANGE. */
+ * GEMMs on the tensor cores (dequantised fp16 weight tiles and fp32
+ * accumulators in tensor memory, fp16 activations) with a SwiGLU epilogue that
+ * also applies the routing weight (or the shared gate), and an un-permute that
+ * adds each token's k weighted expert outputs and the gated shared expert.
+ * out bf16 [T][H].  The activations x, the weighted SwiGLU output and each
+ * expert's weighted output must stay within the fp16 range (|v| <= 65504);
+ * otherwise the status word gets MOE_W4_STATUS_FP16_RANGE. */
 int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
                            moe_w4_bf16* out, void* workspace, size_t ws_bytes,
                            cudaStream_t stream);
