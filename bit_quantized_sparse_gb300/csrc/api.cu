@@ -54,6 +54,7 @@ WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     w.perm = take(T * k * 4);
     w.inv = take(T * k * 4);
     w.blkinfo = take((size_t)w.max_blocks * sizeof(int4));
+    w.unitinfo = take((size_t)w.max_blocks * sizeof(int4));
     w.ntiles = take(4 * sizeof(int32_t));
     w.hh = take((T * k + T) * I * 2);
     w.ys = take((T * k + T) * H * 2);
@@ -129,6 +130,7 @@ static RouteOut route_ws(void* ws, const WsLayout& w) {
     o.router_a = at<uint16_t>(ws, w.router_a);
     o.x16 = at<uint16_t>(ws, w.x16);
     o.blkinfo = at<int4>(ws, w.blkinfo);
+    o.unitinfo = at<int4>(ws, w.unitinfo);
     o.ntiles = at<int32_t>(ws, w.ntiles);
     o.status = &at<Ctrl>(ws, w.ctrl)->status;
     return o;
@@ -176,7 +178,7 @@ int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x, int32_t* to
     RouteOut o = route_ws(workspace, w);
     o.topk_idx = topk_idx; o.topk_w = topk_w; o.gamma = shared_gamma;
     o.counts = counts; o.offsets = offsets; o.perm = perm; o.inv = inv;
-    o.blkinfo = nullptr; o.x16 = nullptr;
+    o.blkinfo = nullptr; o.unitinfo = nullptr; o.x16 = nullptr;
     if (T == 0) {   // empty batch: zero counts and offsets, nothing else to write
         cudaMemsetAsync(counts, 0, (size_t)L->E * 4, stream);
         return launch_status(cudaMemsetAsync(offsets, 0, (size_t)(L->E + 1) * 4, stream));
@@ -227,7 +229,7 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, m
     if (e == cudaSuccess) e = launch_grouping(*L, T, o, stream);
     if (e != cudaSuccess) return MOE_W4_ERR_LAUNCH;
     PrefillWs p{};
-    p.blkinfo = o.blkinfo; p.ntiles = o.ntiles;
+    p.blkinfo = o.blkinfo; p.unitinfo = o.unitinfo; p.ntiles = o.ntiles;
     p.offsets = o.offsets; p.perm = o.perm; p.inv = o.inv; p.topk_w = o.topk_w; p.gamma = o.gamma;
     p.x16 = o.x16;
     p.hh = at<uint16_t>(workspace, w.hh);

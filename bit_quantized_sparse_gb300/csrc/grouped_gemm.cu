@@ -47,8 +47,9 @@ namespace mw4 {
 
 struct GemmArgs {
     const int4* blkinfo;       // per 128-row block: {group (E = shared), first row, rows, first grouped position}
+    const int4* unitinfo;      // down: units {first row block, row blocks, group, 0}; NULL: one block per unit
     const int32_t* ntiles;     // tile count (device)
-    int M;                     // weight-row blocks per row block (tile = row block * M + weight-row block)
+    int M;                     // weight-row blocks (work item = unit * M + weight-row block)
     const int32_t* offsets;    // expert group starts
     const int32_t* perm;       // grouped position -> t*k + j
     const float* topk_w;       // [T*k] (gate/up epilogue)
@@ -103,27 +104,54 @@ struct Geo {
     static constexpr int SA = (512 - ACC_BUFS * ACC_COLS) / A_COLS;   // A ring in TMEM
     static constexpr uint32_t A_TMEM0 = ACC_BUFS * ACC_COLS;
     static constexpr size_t bytes() {
-        return 1024 + (size_t)SB * kTileBytes + (size_t)SC * C_STAGE + 2 * kBN * 4 + (2 * SB + 2 * SC + SA + 4) * 8 +
-               16;
+        return 1024 + (size_t)SB * kTileBytes + (size_t)SC * C_STAGE + 2 * kBN * 4 +
+               (2 * SB + 2 * SC + 2 * SA + 4) * 8 + 16;
     }
 };
 static_assert(Geo<true>::SA == 2 && Geo<false>::SA == 4, "TMEM map");
 static_assert(Geo<true>::bytes() <= 232448 && Geo<false>::bytes() <= 232448, "shared memory per CTA");
-static_assert(Geo<true>::SA <= Geo<true>::SB && Geo<false>::SA <= Geo<false>::SB, "A slots are freed by the B-ring barriers");
+static_assert(kDownReuseMaxI / kGK <= Geo<false>::SA, "a reused down weight tile holds its whole K in the A ring");
+static_assert(Geo<true>::SA <= Geo<true>::SB, "gate/up A slots are freed by the B-ring barriers");
 
 MW4_DEV uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
 struct TileInfo { int e, m, r0, nrows, p0, arow; bool sh; };
+struct UnitInfo { int b0, nb, m; };
 
-// Tile t = (row block t / M, weight-row block t % M); the row block's record
-// (group, first row, rows, first grouped position) was written by the scan.
-MW4_DEV TileInfo tile_info(const GemmArgs& a, int t) {
-    const int4 bi = __ldg(a.blkinfo + t / a.M);
+// Work item t = (unit t / M, weight-row block t % M).  A unit is a run of row
+// blocks of one group (a single block unless unitinfo is given): its weight
+// tile is dequantised once and multiplied with each of its row blocks.
+MW4_DEV UnitInfo unit_info(const GemmArgs& a, int t) {
+    UnitInfo u;
+    u.m = t % a.M;
+    if (a.unitinfo) {
+        const int4 r = __ldg(a.unitinfo + t / a.M);
+        u.b0 = r.x;
+        u.nb = r.y;
+    } else {
+        u.b0 = t / a.M;
+        u.nb = 1;
+    }
+    return u;
+}
+
+// Unit record of work item t as {first row block, row blocks}: no load when
+// every unit is one block; {0, 0} past the last item.
+MW4_DEV int2 unit_rec(const GemmArgs& a, int t, int ntiles) {
+    if (t >= ntiles) return make_int2(0, 0);
+    if (!a.unitinfo) return make_int2(t / a.M, 1);
+    const int4 r = __ldg(a.unitinfo + t / a.M);
+    return make_int2(r.x, r.y);
+}
+
+// Tile (row block with record bi, weight-row block m); the record (group,
+// first row, rows, first grouped position) was written by the scan.
+MW4_DEV TileInfo tile_from(const GemmArgs& a, int4 bi, int m) {
     TileInfo ti;
     ti.e = bi.x;
-    ti.m = t % a.M;
+    ti.m = m;
     ti.r0 = bi.y;
     ti.nrows = bi.z;
     ti.p0 = bi.w;
@@ -131,6 +159,7 @@ MW4_DEV TileInfo tile_info(const GemmArgs& a, int t) {
     ti.arow = (ti.sh ? 0 : ti.e * a.rows_e) + ti.m * kBM;
     return ti;
 }
+MW4_DEV TileInfo block_info(const GemmArgs& a, int rb, int m) { return tile_from(a, __ldg(a.blkinfo + rb), m); }
 
 template <bool DUAL>
 __global__ void __launch_bounds__(Geo<DUAL>::kThreads, 1)
@@ -158,7 +187,8 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     uint64_t* b_full = c_empty + SC;
     uint64_t* b_empty = b_full + SB;
     uint64_t* a_full = b_empty + SB;
-    uint64_t* acc_full = a_full + SA;
+    uint64_t* a_empty = a_full + SA;
+    uint64_t* acc_full = a_empty + SA;
     uint64_t* acc_empty = acc_full + 2;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_empty + 2);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2) + 1;
@@ -175,6 +205,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         }
         for (int s = 0; s < SA; ++s) {
             mbar_init(&a_full[s], 32 * GG::kDeqWarps);
+            mbar_init(&a_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -201,7 +232,8 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         int gk = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            const TileInfo ti = tile_info(a, t);
+            const UnitInfo u = unit_info(a, t);
+            const TileInfo ti = block_info(a, u.b0, u.m);
             const CUtensorMap* m0 = ti.sh ? &map0s : &map0r;
             const CUtensorMap* m1 = ti.sh ? &map1s : &map1r;
             if (lane == 0) {   // the tile's packed codes are one contiguous range per matrix
@@ -229,56 +261,84 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         int gk = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            const TileInfo ti = tile_info(a, t);
-            const CUtensorMap* mb = ti.sh ? &mapbs : &mapb;
-            // gate/up's shared rows are rows r0.. of x16; every other B row block starts
-            // at its first grouped position
-            const int brow = (DUAL && ti.sh) ? ti.r0 : ti.p0;
-            if (lane == 0)   // the tile's B rows are one contiguous range
-                prefetch_l2((ti.sh ? a.b_rows_sh : a.b_rows) + (size_t)brow * a.K, (uint32_t)ti.nrows * a.K * 2);
-            for (int ks = 0; ks < nK; ++ks, ++gk) {
-                const int s = gk % SB;
-                if (!mbar_wait_warp(&b_empty[s], ((gk / SB) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&b_full[s], kTileBytes);
-                    tma_load_2d(B_of(s), mb, ks * kGK, brow, &b_full[s]);
-                    tma_load_2d(B_of(s) + kSubBytes, mb, ks * kGK + 64, brow, &b_full[s]);
+            const UnitInfo u = unit_info(a, t);
+            for (int r = 0; r < u.nb && ok; ++r) {
+                const TileInfo ti = block_info(a, u.b0 + r, u.m);
+                const CUtensorMap* mb = ti.sh ? &mapbs : &mapb;
+                // gate/up's shared rows are rows r0.. of x16; every other B row block
+                // starts at its first grouped position
+                const int brow = (DUAL && ti.sh) ? ti.r0 : ti.p0;
+                if (lane == 0)   // the tile's B rows are one contiguous range
+                    prefetch_l2((ti.sh ? a.b_rows_sh : a.b_rows) + (size_t)brow * a.K, (uint32_t)ti.nrows * a.K * 2);
+                for (int ks = 0; ks < nK; ++ks, ++gk) {
+                    const int s = gk % SB;
+                    if (!mbar_wait_warp(&b_empty[s], ((gk / SB) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&b_full[s], kTileBytes);
+                        tma_load_2d(B_of(s), mb, ks * kGK, brow, &b_full[s]);
+                        tma_load_2d(B_of(s) + kSubBytes, mb, ks * kGK + 64, brow, &b_full[s]);
+                    }
                 }
             }
         }
     } else if (warp == GG::kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer (warp-uniform, one lane issues)
-        int gk = 0, it = 0;
+        // ga counts A steps (one per K step of a unit), gb B steps (one per K step of
+        // each row block of a unit)
+        // The records are software-pipelined so that no tile waits on a global load:
+        // the unit record two items ahead and, one lane per row block, the row-block
+        // records of the next item are requested while an item runs.
+        int ga = 0, gb = 0, it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
-            const TileInfo ti = tile_info(a, t);
-            const int nmma = ((ti.nrows + 15) / 16) * 16;
-            const uint32_t idesc = umma_idesc_f16(kBM, nmma);
-            const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS;
-            if (!mbar_wait_warp(&acc_empty[b], (use & 1) ^ 1, abort_flag, a.status)) break;
-            tc_fence_after();
-            const uint32_t dacc = taddr + b * GG::ACC_COLS;
-            for (int ks = 0; ks < nK; ++ks, ++gk) {
-                const int sb = gk % SB, sa = gk % SA;
-                // A from the dequantisers (a_full), B from the TMA (b_full)
-                ok = mbar_wait_warp(&a_full[sa], (gk / SA) & 1, abort_flag, a.status) &&
-                     mbar_wait_warp(&b_full[sb], (gk / SB) & 1, abort_flag, a.status);
+        int2 ur_c = unit_rec(a, blockIdx.x, ntiles), ur_n = unit_rec(a, blockIdx.x + gridDim.x, ntiles);
+        int4 blk_c = lane < ur_c.y ? __ldg(a.blkinfo + ur_c.x + lane) : make_int4(0, 0, 0, 0);
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const int2 ur_nn = unit_rec(a, t + 2 * gridDim.x, ntiles);
+            const int4 blk_n = lane < ur_n.y ? __ldg(a.blkinfo + ur_n.x + lane) : make_int4(0, 0, 0, 0);
+            const int um = t % a.M, unb = ur_c.y;
+            for (int r = 0; r < unb && ok; ++r, ++it) {
+                int4 bi;
+                bi.x = __shfl_sync(0xffffffffu, blk_c.x, r);
+                bi.y = __shfl_sync(0xffffffffu, blk_c.y, r);
+                bi.z = __shfl_sync(0xffffffffu, blk_c.z, r);
+                bi.w = __shfl_sync(0xffffffffu, blk_c.w, r);
+                const TileInfo ti = tile_from(a, bi, um);
+                const int nmma = ((ti.nrows + 15) / 16) * 16;
+                const uint32_t idesc = umma_idesc_f16(kBM, nmma);
+                const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS;
+                ok = mbar_wait_warp(&acc_empty[b], (use & 1) ^ 1, abort_flag, a.status);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t atm = taddr + GG::A_TMEM0 + sa * GG::A_COLS;
-                const uint64_t bdesc0 = umma_desc_sw128(smem_u32(B_of(sb)));
-                const uint64_t bdesc1 = umma_desc_sw128(smem_u32(B_of(sb) + kSubBytes));
+                const uint32_t dacc = taddr + b * GG::ACC_COLS;
+                for (int ks = 0; ks < nK; ++ks, ++gb) {
+                    const int sb = gb % SB, ka = ga + ks, sa = ka % SA;
+                    // A from the dequantisers (a_full, waited on by the unit's first row
+                    // block), B from the TMA (b_full)
+                    ok = (r > 0 || mbar_wait_warp(&a_full[sa], (ka / SA) & 1, abort_flag, a.status)) &&
+                         mbar_wait_warp(&b_full[sb], (gb / SB) & 1, abort_flag, a.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t atm = taddr + GG::A_TMEM0 + sa * GG::A_COLS;
+                    const uint64_t bdesc0 = umma_desc_sw128(smem_u32(B_of(sb)));
+                    const uint64_t bdesc1 = umma_desc_sw128(smem_u32(B_of(sb) + kSubBytes));
 #pragma unroll
-                for (int kk = 0; kk < kGK / 16; ++kk) {
-                    // K=16 slice kk: sub-tile kk/4, +32 bytes per slice within it (+2 in the address field)
-                    const uint64_t bd = (kk < 4 ? bdesc0 : bdesc1) + 2 * (kk & 3);
+                    for (int kk = 0; kk < kGK / 16; ++kk) {
+                        // K=16 slice kk: sub-tile kk/4, +32 bytes per slice within it (+2 in the address field)
+                        const uint64_t bd = (kk < 4 ? bdesc0 : bdesc1) + 2 * (kk & 3);
 #pragma unroll
-                    for (int mat = 0; mat < NMAT; ++mat)
-                        umma_f16_ts_elect(dacc + mat * 128, atm + mat * (kGK / 2) + kk * 8, bd, idesc, (ks | kk) != 0);
+                        for (int mat = 0; mat < NMAT; ++mat)
+                            umma_f16_ts_elect(dacc + mat * 128, atm + mat * (kGK / 2) + kk * 8, bd, idesc,
+                                              (ks | kk) != 0);
+                    }
+                    umma_commit_elect(&b_empty[sb]);   // gate/up: also frees A slot sa (see the dequantiser)
+                    if (!DUAL && r == unb - 1) umma_commit_elect(&a_empty[sa]);   // the unit's last use of A slot sa
                 }
-                umma_commit_elect(&b_empty[sb]);   // also frees A slot sa (see the dequantiser)
+                if (ok) umma_commit_elect(&acc_full[b]);
             }
-            if (ok) umma_commit_elect(&acc_full[b]);
+            ga += nK;
+            ur_c = ur_n;
+            ur_n = ur_nn;
+            blk_c = blk_n;
         }
     } else if (warp < GG::kEpiWarp0) {
         // ------------------------------------------------------------ dequantisation: one weight row per thread
@@ -289,7 +349,8 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         int gk = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            const TileInfo ti = tile_info(a, t);
+            const UnitInfo u = unit_info(a, t);
+            const TileInfo ti = block_info(a, u.b0, u.m);   // the unit's group and weight rows
             const uint16_t* sp = (mat == 0 ? (ti.sh ? a.s0s : a.s0r) : (ti.sh ? a.s1s : a.s1r)) + (size_t)(ti.arow + row) * G;
             const uint16_t* bp = (mat == 0 ? (ti.sh ? a.b0s : a.b0r) : (ti.sh ? a.b1s : a.b1r)) + (size_t)(ti.arow + row) * G;
             uint4 sq = make_uint4(0, 0, 0, 0), bq = sq, sqn = sq, bqn = sq;
@@ -315,11 +376,15 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         b2w = (uint32_t)bp[2 * ks] | ((uint32_t)bp[2 * ks + 1] << 16);
                     }
                     const int sc = gk % SC, sa = gk % SA;
-                    // A slot sa last served step gk - SA; the commit on b_empty of that
-                    // step's B stage fires once its MMAs are done (SA <= SB, so that
-                    // barrier cannot have moved on by a further phase meanwhile)
+                    // A slot sa last served A step gk - SA.  Down: a_empty fires once the
+                    // MMAs of every row block of that step's unit are done.  Gate/up (one row
+                    // block per unit, A step = B step): the commit on b_empty of that step
+                    // does (SA <= SB, so that barrier cannot have moved on by a further
+                    // phase meanwhile), and no separate commit is spent.
                     ok = mbar_wait(&c_full[sc], (gk / SC) & 1, abort_flag, a.status) &&
-                         (gk < SA || mbar_wait(&b_empty[(gk - SA) % SB], ((gk - SA) / SB) & 1, abort_flag, a.status));
+                         (DUAL ? (gk < SA || mbar_wait(&b_empty[(gk - SA) % SB], ((gk - SA) / SB) & 1, abort_flag,
+                                                       a.status))
+                               : mbar_wait(&a_empty[sa], ((gk / SA) & 1) ^ 1, abort_flag, a.status));
                     if (!ok) break;
                     const uint8_t* cr = C_of(sc, mat) + row * 64;
                     tc_fence_after();   // the MMAs that read this A slot have completed
@@ -365,62 +430,67 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         const int ew = warp - GG::kEpiWarp0, q = ew & 3, half = ew >> 2;
         const int et = tid - 32 * GG::kEpiWarp0;
         int it = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-            const TileInfo ti = tile_info(a, t);
-            const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS, cb = it & 1;
-            // gate/up: the weight of each column of the tile (its routing weight, or the
-            // shared gate) is applied to h, so that the down projection's output needs
-            // none; fetched while the MMAs run (two buffers: a thread writes a buffer
-            // only after every thread has passed the previous tile's barrier)
-            if (DUAL) {
-                if (et < ti.nrows)
-                    col_scale[cb * kBN + et] = ti.sh ? a.gamma[ti.r0 + et] : a.topk_w[a.perm[ti.p0 + et]];
-                asm volatile("bar.sync 2, 256;" ::: "memory");
-            }
-            if (!mbar_wait(&acc_full[b], use & 1, abort_flag, a.status)) break;
-            tc_fence_after();
-            const uint32_t lane_addr = taddr + b * GG::ACC_COLS + ((uint32_t)(q * 32) << 16);
-            // h is the K operand of the down projection: store it in chunk order
-            const int orow = ti.m * kBM + q * 32 + lane;
-            const int ocol = DUAL ? ((orow & ~7) | chunk_pos_of_col(orow & 7)) : orow;
-            for (int c0 = half * 16; c0 < ti.nrows; c0 += 32) {
-                uint32_t g[16], u[16];
-                tmem_ld16(lane_addr + c0, g);
-                if (DUAL) tmem_ld16(lane_addr + 128 + c0, u);
-                tmem_wait_ld();
-                // column n of the tile is grouped row p0 + n: one pointer per chunk, rows
-                // out_cols apart; a full chunk runs without per-element branches
-                uint16_t* op = a.out + (size_t)(ti.p0 + c0) * a.out_cols + ocol;
-                float cs[16];
+        bool ok = true;
+        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const UnitInfo un = unit_info(a, t);
+            for (int r = 0; r < un.nb; ++r, ++it) {
+                const TileInfo ti = block_info(a, un.b0 + r, un.m);
+                const int b = it % GG::ACC_BUFS, use = it / GG::ACC_BUFS, cb = it & 1;
+                // gate/up: the weight of each column of the tile (its routing weight, or the
+                // shared gate) is applied to h, so that the down projection's output needs
+                // none; fetched while the MMAs run (two buffers: a thread writes a buffer
+                // only after every thread has passed the previous tile's barrier)
                 if (DUAL) {
-                    const float4* c4 = reinterpret_cast<const float4*>(col_scale + cb * kBN + c0);
+                    if (et < ti.nrows)
+                        col_scale[cb * kBN + et] = ti.sh ? a.gamma[ti.r0 + et] : a.topk_w[a.perm[ti.p0 + et]];
+                    asm volatile("bar.sync 2, 256;" ::: "memory");
+                }
+                ok = mbar_wait(&acc_full[b], use & 1, abort_flag, a.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t lane_addr = taddr + b * GG::ACC_COLS + ((uint32_t)(q * 32) << 16);
+                // h is the K operand of the down projection: store it in chunk order
+                const int orow = ti.m * kBM + q * 32 + lane;
+                const int ocol = DUAL ? ((orow & ~7) | chunk_pos_of_col(orow & 7)) : orow;
+                for (int c0 = half * 16; c0 < ti.nrows; c0 += 32) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(lane_addr + c0, g);
+                    if (DUAL) tmem_ld16(lane_addr + 128 + c0, u);
+                    tmem_wait_ld();
+                    // column n of the tile is grouped row p0 + n: one pointer per chunk, rows
+                    // out_cols apart; a full chunk runs without per-element branches
+                    uint16_t* op = a.out + (size_t)(ti.p0 + c0) * a.out_cols + ocol;
+                    float cs[16];
+                    if (DUAL) {
+                        const float4* c4 = reinterpret_cast<const float4*>(col_scale + cb * kBN + c0);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const float4 f = c4[i];
-                        cs[4 * i] = f.x; cs[4 * i + 1] = f.y; cs[4 * i + 2] = f.z; cs[4 * i + 3] = f.w;
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 f = c4[i];
+                            cs[4 * i] = f.x; cs[4 * i + 1] = f.y; cs[4 * i + 2] = f.z; cs[4 * i + 3] = f.w;
+                        }
                     }
-                }
-                // range check on the running maximum of |v| (the values are finite: fp16
-                // operands, fp32 sums far below the fp32 limit)
-                float vmax = 0.f;
-                auto emit = [&](int j) {
-                    const float v = DUAL ? silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]) * cs[j]
-                                         : __uint_as_float(g[j]);
-                    vmax = fmaxf(vmax, fabsf(v));
-                    op[(size_t)j * a.out_cols] = __half_as_ushort(__float2half_rn(v));
-                };
-                if (c0 + 16 <= ti.nrows) {
+                    // range check on the running maximum of |v| (the values are finite: fp16
+                    // operands, fp32 sums far below the fp32 limit)
+                    float vmax = 0.f;
+                    auto emit = [&](int j) {
+                        const float v = DUAL ? silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]) * cs[j]
+                                             : __uint_as_float(g[j]);
+                        vmax = fmaxf(vmax, fabsf(v));
+                        op[(size_t)j * a.out_cols] = __half_as_ushort(__float2half_rn(v));
+                    };
+                    if (c0 + 16 <= ti.nrows) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) emit(j);
-                } else {
+                        for (int j = 0; j < 16; ++j) emit(j);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (j < ti.nrows - c0) emit(j);
+                        for (int j = 0; j < 16; ++j)
+                            if (j < ti.nrows - c0) emit(j);
+                    }
+                    if (!(vmax <= 65504.f)) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
                 }
-                if (!(vmax <= 65504.f)) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
+                tc_fence_before();
+                mbar_arrive(&acc_empty[b]);
             }
-            tc_fence_before();
-            mbar_arrive(&acc_empty[b]);
         }
     }
     tc_fence_before();
@@ -559,7 +629,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     a.E = E; a.k = k; a.T = T; a.H = H; a.status = p.status;
 
     // gate/up: A = Wg, Wu rows (I per expert), K = H, out = hh [.][I]
-    a.blkinfo = p.blkinfo; a.M = I / kBM;
+    a.blkinfo = p.blkinfo; a.unitinfo = nullptr; a.M = I / kBM;
     a.s0r = L.gate.scales; a.b0r = L.gate.biases; a.s1r = L.up.scales; a.b1r = L.up.biases;
     a.s0s = L.sh_gate.scales; a.b0s = L.sh_gate.biases; a.s1s = L.sh_up.scales; a.b1s = L.sh_up.biases;
     a.c0r = L.gate.codes; a.c1r = L.up.codes; a.c0s = L.sh_gate.codes; a.c1s = L.sh_up.codes;
@@ -574,7 +644,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
 
     // down: A = Wd rows (H per expert), K = I, B = hh rows, out = ys [.][H]
     GemmArgs b = a;
-    b.M = H / kBM; b.ntiles = p.ntiles + 1;
+    b.M = H / kBM; b.ntiles = p.ntiles + 1; b.unitinfo = p.unitinfo;
     b.s0r = L.down.scales; b.b0r = L.down.biases; b.s1r = nullptr; b.b1r = nullptr;
     b.s0s = L.sh_down.scales; b.b0s = L.sh_down.biases; b.s1s = nullptr; b.b1s = nullptr;
     b.c0r = L.down.codes; b.c1r = nullptr; b.c0s = L.sh_down.codes; b.c1s = nullptr; b.b_rows = p.hh; b.b_rows_sh = p.hh;

@@ -73,13 +73,14 @@ constexpr int kScanRegChunks = 32;   // chunk counts held in registers (T <= 32 
 
 __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nchunk, int32_t* __restrict__ chunk_base,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                                    int4* __restrict__ blkinfo,
-                                                    int32_t* __restrict__ ntiles, int MI, int MH) {
+                                                    int4* __restrict__ blkinfo, int4* __restrict__ unitinfo,
+                                                    int32_t* __restrict__ ntiles, int MI, int MH, int R) {
     extern __shared__ int sm[];
     int* cnt = sm;               // [E+1]
     int* off = sm + (E + 1);     // [E+1]
     int* blk = off + (E + 1);    // [E+1]
-    int* wt = blk + (E + 1);     // [33]
+    int* uni = blk + (E + 1);    // [E+1]
+    int* wt = uni + (E + 1);     // [33]
     // up to kScanRegChunks chunks: the counts of one expert stay in registers as
     // exclusive prefixes and are written once, offset added, after the scan
     const bool in_regs = nchunk <= kScanRegChunks;
@@ -143,9 +144,20 @@ __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nch
             blkinfo[b] = make_int4(e, r0, min(kBN, rows - r0), p_first + r0);
         }
     }
+    // down units: runs of at most R consecutive row blocks of one group
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        const int nb = ((e < E) ? blk[e + 1] : nblk) - blk[e];
+        uni[e] = (nb + R - 1) / R;
+    }
+    __syncthreads();
+    const int nuni = block_exclusive_scan(uni, E + 1, wt);
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        const int b0 = blk[e], nb = ((e < E) ? blk[e + 1] : nblk) - b0;
+        for (int j = 0; j * R < nb; ++j) unitinfo[uni[e] + j] = make_int4(b0 + j * R, min(R, nb - j * R), e, 0);
+    }
     if (threadIdx.x == 0) {
         ntiles[0] = nblk * MI;
-        ntiles[1] = nblk * MH;
+        ntiles[1] = nuni * MH;
     }
 }
 
@@ -212,9 +224,9 @@ cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cud
     const int nchunk = (T + kChunk - 1) / kChunk;
     chunk_count_kernel<<<nchunk, kChunk, E * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.status);
     trace_mark(st, 3);
-    const size_t scan_sm = (3 * (E + 1) + 33) * sizeof(int);
-    scan_kernel<<<1, 1024, scan_sm, st>>>(T, E, k, nchunk, o.chunk_base, o.counts, o.offsets, o.blkinfo, o.ntiles,
-                                          L.I / kBM, L.H / kBM);
+    const size_t scan_sm = (4 * (E + 1) + 33) * sizeof(int);
+    scan_kernel<<<1, 1024, scan_sm, st>>>(T, E, k, nchunk, o.chunk_base, o.counts, o.offsets, o.blkinfo, o.unitinfo,
+                                          o.ntiles, L.I / kBM, L.H / kBM, down_blocks_per_unit(L.I));
     trace_mark(st, 4);
     assign_kernel<<<nchunk, kChunk, (kAssignWarps * E + kChunk * k) * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.perm,
                                                                      o.inv);

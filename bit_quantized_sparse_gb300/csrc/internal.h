@@ -19,6 +19,12 @@ constexpr int kDecodeMaxT = 16;   // largest decode batch
 constexpr int kFusedClustersPerExpert = 4;   // fused T=1 decode: 16 CTAs per expert in clusters of 4
 constexpr int kRouterRowsPerCta = 256;  // H rows per decode-router CTA
 constexpr int kRouterSplit = 2;         // prefill router: partial score arrays (halves of H)
+// Down projection: one CTA dequantises a 128-row weight tile once and runs it
+// against up to this many 128-row blocks of the same expert, when its whole K
+// (I columns) fits the tensor-memory A ring (kDownReuseMaxI columns).
+constexpr int kDownBlocksPerUnit = 4;
+constexpr int kDownReuseMaxI = 512;
+inline int down_blocks_per_unit(int I) { return I <= kDownReuseMaxI ? kDownBlocksPerUnit : 1; }
 
 struct Ctrl;   // workspace control header (common.cuh)
 
@@ -30,7 +36,7 @@ void trace_kernels(int n);
 // Byte offsets of every region of the workspace (all 256-byte aligned).
 struct WsLayout {
     size_t ctrl, logits, router_a, x16, topk_idx, topk_w, gamma, chunk_base, counts, offsets, perm, inv;
-    size_t blkinfo, ntiles, hh, ys;
+    size_t blkinfo, unitinfo, ntiles, hh, ys;
     size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh, dec_cpart, dec_ybuf;
     size_t total;
     int T_max, nchunk_max, max_blocks, max_tiles_gu, max_tiles_dn;
@@ -50,6 +56,7 @@ struct RouteOut {
     uint16_t* router_a;  // [Epad][3H] bf16 split router weights (tensor-core scores); NULL: CUDA cores
     uint16_t* x16;     // fp16 copy of x written by the top-k kernel (NULL: not needed)
     int4* blkinfo; int32_t* ntiles;   // per-block records [max blocks] and tile counts [2]; NULL: no tile maps
+    int4* unitinfo;                   // down units [max blocks]: {first block, blocks, group, 0}
     unsigned int* status;
 };
 cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* x, const RouteOut& o,
@@ -83,6 +90,7 @@ cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint1
 // ---------------------------------------------------------------------------
 struct PrefillWs {
     const int4* blkinfo;     // per 128-row block of the grouped rows: {group (E = shared), first row, rows, first position}
+    const int4* unitinfo;    // down units: {first row block, row blocks, group, 0}
     const int32_t* ntiles;   // [2] gate/up and down tile counts
     const int32_t* offsets; const int32_t* perm; const int32_t* inv;
     const float* topk_w; const float* gamma;

@@ -37,6 +37,10 @@ MOE_W4_ERR_LAUNCH = -4
 MOE_W4_ERR_DEVICE = -5
 MOE_W4_ERR_ALIGN = -6
 MOE_W4_ERR_SCRATCH = -7
+# bits of the device status word (include/moe_w4.h)
+MOE_W4_STATUS_WAIT_TIMEOUT = 1
+MOE_W4_STATUS_BAD_INDEX = 2
+MOE_W4_STATUS_FP16_RANGE = 4
 DECODE_MAX_T = 16
 
 

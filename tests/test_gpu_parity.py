@@ -259,6 +259,22 @@ def test_gpu_workspace_errors(mw, torch):
     torch.cuda.synchronize()
 
 
+def test_prefill_fp16_range_status(mw, torch):
+    """x within the fp16 range, but large enough that the weighted SwiGLU output
+    is not: the prefill sets MOE_W4_STATUS_FP16_RANGE in the status word; a
+    call on ordinary inputs leaves it clear."""
+    L, x = S.draw_config("tiny_T4")
+    dl = mw.DeviceLayer(L)
+    mw.forward_prefill(dl, mw.tokens_to_device(x))
+    torch.cuda.synchronize()
+    assert dl.status() == 0
+    xf = S.bf16_bits_to_f32(x).astype(np.float64)
+    big = S.f32_to_bf16_bits((xf * (60000.0 / np.abs(xf).max())).astype(np.float32))
+    mw.forward_prefill(dl, mw.tokens_to_device(big))
+    torch.cuda.synchronize()
+    assert dl.status() & mw.MOE_W4_STATUS_FP16_RANGE
+
+
 def test_trace_events_outside_capture(mw, torch):
     """Kernel timing events recorded around an eager (not captured) call: the call
     succeeds and every event completes in order."""
