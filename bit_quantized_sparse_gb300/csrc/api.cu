@@ -64,8 +64,9 @@ WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     w.dec_w = take(Td * k * 4);
     w.dec_gamma = take(Td * 4);
     w.dec_hh = take(Td * (k + 1) * I * 4);
-    w.dec_cpart = take((size_t)kFusedClustersPerExpert * (k + 1) * E * 4);
-    w.dec_ybuf = take((k + 1) * H * 4);
+    w.dec_cpart = take((size_t)kFusedClustersPerExpert * (k + 1) * E * 8);
+    w.dec_hx = take((k + 1) * I * 8);
+    w.dec_ybuf = take((k + 1) * H * 8);
     w.total = o;
     return w;
 }
@@ -149,7 +150,9 @@ size_t moe_w4_workspace_size(const moe_w4_layer* L, int T_max) {
 
 int moe_w4_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream) {
     if (!workspace || ws_bytes < sizeof(Ctrl)) return MOE_W4_ERR_WORKSPACE;
-    return launch_status(cudaMemsetAsync(workspace, 0, sizeof(Ctrl), stream));
+    // the whole workspace: the fused decode's exchange buffers must start with no
+    // call's tag in them
+    return launch_status(cudaMemsetAsync(workspace, 0, ws_bytes, stream));
 }
 
 size_t moe_w4_status_offset(void) { return offsetof(Ctrl, status); }
@@ -207,8 +210,9 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, mo
     d.counter = &at<Ctrl>(workspace, w.ctrl)->decode_counter;
     d.status = &at<Ctrl>(workspace, w.ctrl)->status;
     d.ctrl = at<Ctrl>(workspace, w.ctrl);
-    d.fused_cpart = at<float>(workspace, w.dec_cpart);
-    d.fused_ybuf = at<float>(workspace, w.dec_ybuf);
+    d.fused_cpart = at<uint64_t>(workspace, w.dec_cpart);
+    d.fused_hx = at<uint64_t>(workspace, w.dec_hx);
+    d.fused_ybuf = at<uint64_t>(workspace, w.dec_ybuf);
     trace_mark(stream, 0);
     return launch_status(launch_decode(*L, T, x, out, d, stream));
 }

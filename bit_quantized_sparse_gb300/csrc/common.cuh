@@ -33,6 +33,22 @@ MW4_DEV unsigned int atomic_add_release_gpu(unsigned int* p, unsigned int v) {
     asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
 }
+// Tagged values for cross-CTA exchanges: one 8-byte word, the float's bits in
+// the low half and the writer's call tag in the high half, stored and loaded
+// as single-copy-atomic 8-byte accesses at GPU scope.  A reader that sees its
+// own call's tag has the value: the data is its own ready flag.
+MW4_DEV void st_tagged(uint64_t* p, float v, uint32_t tag) {
+    const uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(w) : "memory");
+}
+MW4_DEV uint64_t ld_tagged(const uint64_t* p) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+MW4_DEV uint32_t tag_of(uint64_t w) { return (uint32_t)(w >> 32); }
+MW4_DEV float val_of(uint64_t w) { return __uint_as_float((uint32_t)w); }
+
 MW4_DEV unsigned int atomic_add_acq_rel_gpu(unsigned int* p, unsigned int v) {
     unsigned int old;
     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");

@@ -16,7 +16,9 @@
 //      cluster are added through distributed shared memory, the cluster sums
 //      are published in global memory and, once all are in (bounded wait: all
 //      CTAs are co-resident), every routed CTA adds them in a fixed order and
-//      selects the top-k.  The shared expert does not wait for the routing: it
+//      selects the top-k.  Every value that crosses CTAs through global memory
+//      is an 8-byte (value, call tag) word, so that a reader waits on the data
+//      itself rather than on a counter and then the data.  The shared expert does not wait for the routing: it
 //      starts loading its weights as soon as its own router reads are done.
 //   2. TMA loads the CTA's slices of the packed codes (128-byte swizzle) and
 //      its scales/biases; the gate/up slices are consumed box by box as they
@@ -27,13 +29,14 @@
 //      positions divided by 16; fp32 accumulation per 64-column group, then
 //      s*(acc - 1024*sum(B)) + b*sum(x).  SwiGLU in fp32.
 //   4. h: every CTA publishes its slice of h in global memory; the 16 CTAs of
-//      an expert wait (bounded) until all 16 slices are in and read all of h.
+//      an expert wait (bounded) until all 16 slices carry the tag and read all of h.
 //   5. down GEMV the same way with h in fp16, scaled by the routing weight
 //      (or the shared gate), written per expert.
-//   6. per block of output rows, the last of the k+1 CTAs to finish adds the
-//      k+1 expert outputs in slot order and writes bf16 out.
-// No step waits on another CTA except the bounded router and h exchanges and
-// the hardware cluster barriers.
+//   6. per block of output rows, the shared expert's CTA (it needs no routing,
+//      so it is usually done first) waits (bounded) for the k routed outputs,
+//      adds the k+1 in slot order and writes bf16 out.
+// No step waits on another CTA except these bounded exchanges and the hardware
+// cluster barriers.
 #include "common.cuh"
 #include "internal.h"
 
@@ -44,11 +47,6 @@ constexpr int kPE = kCS * kFusedClustersPerExpert;       // CTAs per expert (16)
 constexpr int kFThreads = 512;                           // 16 warps
 constexpr int kFWarps = kFThreads / 32;
 constexpr int kMaxSlots = 9;                             // k + 1 <= 9
-// control-header words used by the kernel (Ctrl::pad)
-constexpr int kPadRows = 0;                 // [kPE] combine arrivals per block of output rows
-constexpr int kPadDone = kPadRows + kPE;    // row blocks combined
-constexpr int kPadH = kPadDone + 1;         // [k+1] h slices published per expert
-static_assert(kPadH + kMaxSlots <= 62, "control header");
 
 struct FusedArgs {
     const uint16_t* x;          // [H] bf16
@@ -59,9 +57,9 @@ struct FusedArgs {
     const uint16_t* ds; const uint16_t* db;                                             // routed down s, b
     const uint16_t* sgs; const uint16_t* sgb; const uint16_t* sus; const uint16_t* sub; // shared
     const uint16_t* sds; const uint16_t* sdb;
-    float* cpart;               // [4(k+1)][E] cluster partial scores
-    float* hbuf;                // [k+1][I] h of every expert
-    float* ybuf;                // [k+1][H] weighted expert outputs
+    uint64_t* cpart;            // [4(k+1)][E] cluster partial scores, tagged with the call
+    uint64_t* hx;               // [k+1][I] h of every expert, tagged with the call
+    uint64_t* ybuf;             // [k+1][H] weighted expert outputs, tagged with the call
     int32_t* idx_out;           // [k] (for inspection)
     float* w_out;               // [k]
     float* gamma_out;           // [1]
@@ -296,7 +294,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_dn + 1);
     int* sel_e = reinterpret_cast<int*>(bar_dn + 2);                     // selected expert of this cluster
     float* sel_w = reinterpret_cast<float*>(sel_e + 1);                  // its weight (or gamma)
-    int* last_flag = reinterpret_cast<int*>(sel_e + 2);
+    uint32_t* xtag_s = reinterpret_cast<uint32_t*>(sel_e + 3);            // this call's exchange tag
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // clusters are consecutive blocks: expert slot = block / kPE, CTA ei of the
@@ -335,6 +333,11 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         fence_mbar_init();
     }
     griddep_wait();   // from here on: x, the workspace and its counters
+    // Values crossing CTAs carry this call's tag (the call counter + 1): a reader
+    // polls the data itself instead of a counter and then the data.  CTA 0 advances
+    // the counter once every cluster's router sum carries the tag, i.e. once every
+    // CTA has read it.
+    if (tid == 0) *xtag_s = ld_acquire_u32(&a.ctrl->pad[kCtrlEpochWord]) + 1u;
     if (tid < 2 * E) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) rx[j] = (r_hb + j < r_he) ? bf16_bits_to_float(__ldg(a.x + rh0 + r_hb + j)) : 0.f;
@@ -391,10 +394,8 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             float s = 0.f;
 #pragma unroll
             for (int r = 0; r < kCS; ++r) s += v[r];
-            a.cpart[(size_t)cid * E + e] = s;
+            st_tagged(a.cpart + (size_t)cid * E + e, s, *xtag_s);
         }
-        __syncthreads();
-        if (tid == 0) atomic_add_release_gpu(&a.ctrl->decode_counter, 1u);
     }
     // the shared expert needs no routing: its loads start once its router sums are
     // published, so that issuing them does not delay the exchange everyone waits on
@@ -469,30 +470,40 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     }
     if (!shared_cluster) {
         // ------------------------------------------------------------ 1b. exchange, top-k
-        if (tid == 0) {
-            const uint64_t t0 = globaltimer();
-            while (ld_acquire_u32(&a.ctrl->decode_counter) < (uint32_t)NG) {
-                __nanosleep(20);
-                if (globaltimer() - t0 > kWaitLimitNs) {
-                    raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
-                    *abort_flag = 1;
-                    break;
-                }
-            }
-        }
-        __syncthreads();
-        if (!*abort_flag) {
+        {
+            const uint32_t xtag = *xtag_s;
             for (int e = tid; e < E; e += kFThreads) {   // cluster sums added in cluster order, all loads in flight
                 constexpr int kMaxCl = kMaxSlots * kFusedClustersPerExpert;
-                float v[kMaxCl];
+                uint64_t v[kMaxCl];
 #pragma unroll
-                for (int j = 0; j < kMaxCl; ++j) v[j] = (j < NCL) ? __ldcg(a.cpart + (size_t)j * E + e) : 0.f;
+                for (int j = 0; j < kMaxCl; ++j) v[j] = (j < NCL) ? ld_tagged(a.cpart + (size_t)j * E + e) : 0ull;
+                // re-read the sums that do not carry this call's tag yet (bounded)
+                const uint64_t t0 = globaltimer();
+                while (true) {
+                    bool all = true;
+#pragma unroll
+                    for (int j = 0; j < kMaxCl; ++j)
+                        if (j < NCL && tag_of(v[j]) != xtag) {
+                            all = false;
+                            v[j] = ld_tagged(a.cpart + (size_t)j * E + e);
+                        }
+                    if (all) break;
+                    if (globaltimer() - t0 > kWaitLimitNs) {
+                        raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
                 float s = 0.f;
 #pragma unroll
-                for (int j = 0; j < kMaxCl; ++j) s += v[j];
+                for (int j = 0; j < kMaxCl; ++j) s += (j < NCL) ? val_of(v[j]) : 0.f;
                 logits[e] = s + (a.router_bias ? a.router_bias[e] : 0.f);
             }
             __syncthreads();
+            // every cluster's sum carries the tag, so every CTA has read the counter
+            if (G == 0 && tid == 0 && !*abort_flag) a.ctrl->pad[kCtrlEpochWord] = xtag;
+        }
+        if (!*abort_flag) {
             // one warp selects, weighs and issues the loads of this CTA's expert
             if (warp == 0) {
                 int sidx;
@@ -551,32 +562,42 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     }
     __syncthreads();
     // ---------------------------------------------------------------- 4. h through global memory
-    if (gu_ok)
-        for (int i = tid; i < RG; i += kFThreads) a.hbuf[(size_t)slot * I + ei * RG + i] = silu_f(gsum[i]) * usum[i];
-    __syncthreads();
-    if (tid == 0) {
-        // published even after an abort, so that no CTA of the expert waits in vain
-        atomic_add_release_gpu(&a.ctrl->pad[kPadH + slot], 1u);
-        if (gu_ok) {
+    // this CTA's slice of h, tagged; published even after an abort (as zeros), so
+    // that no CTA of the expert waits in vain
+    {
+        const uint32_t xtag = *xtag_s;
+        for (int i = tid; i < RG; i += kFThreads)
+            st_tagged(a.hx + (size_t)slot * I + ei * RG + i, gu_ok ? silu_f(gsum[i]) * usum[i] : 0.f, xtag);
+    }
+    const bool h_in = gu_ok && !*abort_flag;
+    if (h_in) {
+        // fp16 B fragments of h, laid out like x (odd entries divided by 16), once
+        // all 16 slices carry this call's tag
+        const uint32_t xtag = *xtag_s;
+        for (int i = tid; i < I / 8; i += kFThreads) {
+            const uint64_t* src = a.hx + (size_t)slot * I + i * 8;
+            uint64_t w[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) w[j] = ld_tagged(src + j);
             const uint64_t t0 = globaltimer();
-            while (ld_acquire_u32(&a.ctrl->pad[kPadH + slot]) < (uint32_t)kPE) {
+            while (true) {
+                bool all = true;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (tag_of(w[j]) != xtag) {
+                        all = false;
+                        w[j] = ld_tagged(src + j);
+                    }
+                if (all) break;
                 if (globaltimer() - t0 > kWaitLimitNs) {
                     raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
                     *abort_flag = 1;
                     break;
                 }
             }
-        }
-    }
-    __syncthreads();
-    const bool h_ok = gu_ok && !*abort_flag;
-    if (h_ok) {
-        // fp16 B fragments of h, laid out like x (odd entries divided by 16)
-        for (int i = tid; i < I / 8; i += kFThreads) {
-            const float* src = a.hbuf + (size_t)slot * I + i * 8;
-            const float4 v0 = __ldcg(reinterpret_cast<const float4*>(src));
-            const float4 v1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = val_of(w[j]);
             bool bad = false;
 #pragma unroll
             for (int j = 0; j < 8; ++j) bad |= !(fabsf(v[j]) <= 65504.f);
@@ -589,6 +610,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         }
     }
     __syncthreads();
+    const bool h_ok = h_in && !*abort_flag;
     if (h_ok) {
         for (int gi = tid; gi < I / 64; gi += kFThreads) {
             float sb = 0.f, so = 0.f;
@@ -609,6 +631,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     griddep_launch_dependents();   // the next kernel on the stream may start its prologue
     // RD/16 row tiles x KS splits of the 64-column groups
     const bool dn_ok = __syncthreads_and(h_ok ? mbar_wait(bar_dn, 0, abort_flag, status) : 0);
+    const uint32_t xtag = *xtag_s;
     if (dn_ok) {
         const int ntile = RD / 16, KS = kFWarps / ntile > 0 ? kFWarps / ntile : 1, ngrp = I / 64;
         for (int task = warp; task < ntile * KS; task += kFWarps) {
@@ -627,33 +650,36 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             const int t = i / 16, r = i % 16;
             float v = 0.f;
             for (int ks = 0; ks < KS; ++ks) v += red[(t * KS + ks) * 16 + r];
-            a.ybuf[(size_t)slot * H + ei * RD + i] = v * wsel;
+            st_tagged(a.ybuf + (size_t)slot * H + ei * RD + i, v * wsel, xtag);
         }
+    } else {   // published even after an abort (as zeros), so that the reducer does not wait in vain
+        for (int i = tid; i < RD; i += kFThreads) st_tagged(a.ybuf + (size_t)slot * H + ei * RD + i, 0.f, xtag);
     }
-    // ---------------------------------------------------------------- 6. combine: last of the k+1 CTAs per row block
-    __syncthreads();
-    if (tid == 0) *last_flag = (atomic_add_acq_rel_gpu(&a.ctrl->pad[kPadRows + ei], 1u) == (unsigned)(NC - 1));
-    __syncthreads();
-    if (*last_flag) {
+    // ---------------------------------------------------------------- 6. combine: the shared expert's CTA per row block
+    if (shared_cluster) {
         for (int o = ei * RD + tid; o < (ei + 1) * RD; o += kFThreads) {
-            float v[kMaxSlots];
+            uint64_t v[kMaxSlots];
 #pragma unroll
-            for (int j = 0; j < kMaxSlots; ++j) v[j] = (j < NC) ? __ldcg(a.ybuf + (size_t)j * H + o) : 0.f;
+            for (int j = 0; j < kMaxSlots; ++j) v[j] = (j < NC) ? ld_tagged(a.ybuf + (size_t)j * H + o) : 0ull;
+            const uint64_t t0 = globaltimer();
+            while (true) {
+                bool all = true;
+#pragma unroll
+                for (int j = 0; j < kMaxSlots; ++j)
+                    if (j < NC && tag_of(v[j]) != xtag) {
+                        all = false;
+                        v[j] = ld_tagged(a.ybuf + (size_t)j * H + o);
+                    }
+                if (all) break;
+                if (globaltimer() - t0 > kWaitLimitNs) {
+                    raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
+                    break;
+                }
+            }
             float s = 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxSlots; ++j) s += v[j];
+            for (int j = 0; j < kMaxSlots; ++j) s += (j < NC) ? val_of(v[j]) : 0.f;
             a.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
-        }
-        __syncthreads();
-        if (tid == 0) {
-            a.ctrl->pad[kPadRows + ei] = 0;
-            // the last row block to finish resets the exchange counters for the next
-            // call: by then every CTA has passed both exchanges
-            if (atomicAdd(&a.ctrl->pad[kPadDone], 1u) == (unsigned)(kPE - 1)) {
-                a.ctrl->decode_counter = 0;
-                for (int j = 0; j < NC; ++j) a.ctrl->pad[kPadH + j] = 0;
-                a.ctrl->pad[kPadDone] = 0;
-            }
         }
     }
 }
@@ -772,7 +798,7 @@ cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16
     a.ds = L.down.scales; a.db = L.down.biases;
     a.sgs = L.sh_gate.scales; a.sgb = L.sh_gate.biases; a.sus = L.sh_up.scales; a.sub = L.sh_up.biases;
     a.sds = L.sh_down.scales; a.sdb = L.sh_down.biases;
-    a.cpart = d.fused_cpart; a.hbuf = d.hh; a.ybuf = d.fused_ybuf;
+    a.cpart = d.fused_cpart; a.hx = d.fused_hx; a.ybuf = d.fused_ybuf;
     a.idx_out = d.idx; a.w_out = d.w; a.gamma_out = d.gamma; a.out = out;
     a.ctrl = d.ctrl;
     a.H = H; a.E = E; a.I = I; a.k = k;

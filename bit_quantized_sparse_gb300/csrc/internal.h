@@ -23,6 +23,9 @@ constexpr int kRouterSplit = 2;         // prefill router: partial score arrays 
 // against up to this many 128-row blocks of the same expert, when its whole K
 // (I columns) fits the tensor-memory A ring (kDownReuseMaxI columns).
 constexpr int kDownBlocksPerUnit = 4;
+// Word of the control header's pad[] holding the fused T=1 decode's call
+// counter (the tag of its exchanged values); kept across calls.
+constexpr int kCtrlEpochWord = 61;
 constexpr int kDownReuseMaxI = 512;
 inline int down_blocks_per_unit(int I) { return I <= kDownReuseMaxI ? kDownBlocksPerUnit : 1; }
 
@@ -37,7 +40,7 @@ void trace_kernels(int n);
 struct WsLayout {
     size_t ctrl, logits, router_a, x16, topk_idx, topk_w, gamma, chunk_base, counts, offsets, perm, inv;
     size_t blkinfo, unitinfo, ntiles, hh, ys;
-    size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh, dec_cpart, dec_ybuf;
+    size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh, dec_cpart, dec_hx, dec_ybuf;
     size_t total;
     int T_max, nchunk_max, max_blocks, max_tiles_gu, max_tiles_dn;
 };
@@ -74,10 +77,10 @@ struct DecodeWs {
     float* hh;          // [T][k+1][I]
     unsigned int* counter;
     unsigned int* status;
-    Ctrl* ctrl;         // control header (counters of the fused kernel)
-    float* fused_cpart; // [kFusedClustersPerExpert*(k+1)][E] cluster partial scores (fused T=1 kernel)
-    float* fused_ybuf;  // [k+1][H] weighted expert outputs (fused T=1 kernel); the fused kernel
-                        // exchanges h through hh ([k+1][I] at T=1)
+    Ctrl* ctrl;         // control header (call counter of the fused kernel)
+    uint64_t* fused_cpart; // [kFusedClustersPerExpert*(k+1)][E] tagged cluster partial scores (fused T=1 kernel)
+    uint64_t* fused_hx;    // [k+1][I] tagged h of every expert (fused T=1 kernel)
+    uint64_t* fused_ybuf;  // [k+1][H] tagged weighted expert outputs (fused T=1 kernel)
 };
 bool decode_fused_supported(const moe_w4_layer& L);
 cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,

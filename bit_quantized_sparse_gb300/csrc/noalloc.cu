@@ -30,7 +30,7 @@ static size_t up256n(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Compact decode-only layout inside the fixed array: control header, partial
 // scores, selected experts, weights, shared gate, SwiGLU outputs.
-struct NoallocLayout { size_t ctrl, part, idx, w, gamma, hh, cpart, ybuf, total; };
+struct NoallocLayout { size_t ctrl, part, idx, w, gamma, hh, cpart, hx, ybuf, total; };
 
 static NoallocLayout noalloc_layout(const moe_w4_layer& L, int T) {
     NoallocLayout n{};
@@ -44,8 +44,9 @@ static NoallocLayout noalloc_layout(const moe_w4_layer& L, int T) {
     n.w = take(Tz * k * 4);
     n.gamma = take(Tz * 4);
     n.hh = take(Tz * (k + 1) * I * 4);
-    n.cpart = take((size_t)kFusedClustersPerExpert * (k + 1) * E * 4);
-    n.ybuf = take((k + 1) * H * 4);
+    n.cpart = take((size_t)kFusedClustersPerExpert * (k + 1) * E * 8);
+    n.hx = take((k + 1) * I * 8);
+    n.ybuf = take((k + 1) * H * 8);
     n.total = o;
     return n;
 }
@@ -88,8 +89,12 @@ extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const
     void* base = nullptr;
     if (scratch_address(&base) != cudaSuccess) return MOE_W4_ERR_LAUNCH;
     uint8_t* b = static_cast<uint8_t*>(base);
-    // the completion counter must start at zero; clear the header every call
-    if (cudaMemsetAsync(b + n.ctrl, 0, sizeof(Ctrl), stream) != cudaSuccess) return MOE_W4_ERR_LAUNCH;
+    // the completion counters must start at zero: clear the header every call, up to
+    // the fused decode's call counter, which must keep counting (the exchange
+    // buffers still hold earlier calls' tagged values)
+    if (cudaMemsetAsync(b + n.ctrl, 0, offsetof(Ctrl, pad) + kCtrlEpochWord * sizeof(unsigned int), stream) !=
+        cudaSuccess)
+        return MOE_W4_ERR_LAUNCH;
     DecodeWs d{};
     d.part = reinterpret_cast<float*>(b + n.part);
     d.idx = reinterpret_cast<int32_t*>(b + n.idx);
@@ -99,7 +104,8 @@ extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const
     d.counter = &reinterpret_cast<Ctrl*>(b + n.ctrl)->decode_counter;
     d.status = &reinterpret_cast<Ctrl*>(b + n.ctrl)->status;
     d.ctrl = reinterpret_cast<Ctrl*>(b + n.ctrl);
-    d.fused_cpart = reinterpret_cast<float*>(b + n.cpart);
-    d.fused_ybuf = reinterpret_cast<float*>(b + n.ybuf);
+    d.fused_cpart = reinterpret_cast<uint64_t*>(b + n.cpart);
+    d.fused_hx = reinterpret_cast<uint64_t*>(b + n.hx);
+    d.fused_ybuf = reinterpret_cast<uint64_t*>(b + n.ybuf);
     return launch_decode(*L, T, x, out, d, stream) == cudaSuccess ? MOE_W4_OK : MOE_W4_ERR_LAUNCH;
 }

@@ -97,9 +97,11 @@ enum {
  * activations and a small control header at offset 0. */
 size_t moe_w4_workspace_size(const moe_w4_layer* L, int T_max);
 
-/* Clears the workspace control header (status word and completion counters).
- * Call once after allocating a workspace, before its first use; every later
- * call leaves the header as it found it, except the sticky status word. */
+/* Clears the whole workspace (status word, completion counters, exchange
+ * buffers).  Call once after allocating a workspace, before its first use, and
+ * again after a call reported a device-side error; every later call leaves the
+ * control header as it found it, except the sticky status word and a call
+ * counter of the T=1 decode. */
 int moe_w4_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* Offset in bytes, within the workspace, of the int32 device status word:
