@@ -119,6 +119,9 @@ MW4_DEV uint32_t cluster_id() {
 MW4_DEV void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync, for work in between.
+MW4_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+MW4_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 MW4_DEV float ld_dsmem_f32(const void* local_ptr, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
@@ -400,7 +403,9 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     // the shared expert needs no routing: its loads start once its router sums are
     // published, so that issuing them does not delay the exchange everyone waits on
     if (shared_cluster && warp == 0) issue_loads(E);
-    cluster_sync();   // every peer has read this CTA's partials; the buffers may be reused
+    // this CTA has read its peers' partials; the matching wait (every peer has read
+    // this CTA's, so the buffer may be reused) comes before the gate/up GEMV reuses it
+    cluster_arrive();
     // x for the GEMVs is prepared here, off the router's critical path, while the
     // other CTAs' router sums come in
     // x as fp16 B fragments, one thread per 16-byte entry: entry i (32-column
@@ -528,6 +533,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     __syncthreads();
     const bool run = !*abort_flag;
 
+    cluster_wait();   // every peer has read this CTA's partials: red (= part) may be written
     // ---------------------------------------------------------------- 3. gate/up GEMV
     // 2*RG/16 row tiles (gate, then up) x KS splits of the 64-column groups
     // box 0 also carries the scales/biases; the block agrees on the outcome of the wait
