@@ -35,6 +35,7 @@ PREFILL_KERNELS = ["router_scores", "topk", "chunk_count", "scan", "assign", "ga
                    "combine"]
 DECODE_KERNELS = ["decode_router", "decode_gate_up", "decode_down"]   # the three-kernel path
 DECODE_FUSED = ["decode_fused"]
+SMALL_T = (4, 8)   # multi-row decode batches measured beside the step
 
 
 def parse():
@@ -264,6 +265,31 @@ def run_gpu(args, rank, local_rank, world, dist):
     t_pre = timed(g_pre, args.steps)
     t_dec = timed(g_dec, args.steps)
 
+    # multi-row decode (T = 4 and 8 rows per call, the grouped path): calls
+    # cycling the replica layers over slices of the decode rows; the bytes a call
+    # must move count every distinct expert its rows select once (routing by the
+    # library's own router)
+    small = {}
+    n_small = 32
+    for Tm in SMALL_T:
+        def dec_small(Tm=Tm):
+            for i in range(n_small):
+                o = (i * Tm) % ndec
+                mw._check(mw.moe_w4_forward_decode(ctypes.byref(layers[i % N_REPLICAS].c), Tm,
+                                                   xdec[o:o + Tm].data_ptr(), outdec[o:o + Tm].data_ptr(),
+                                                   ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream),
+                          "decode T>1")
+        with torch.cuda.stream(stream):
+            dec_small()
+        torch.cuda.synchronize()
+        t_small = timed(capture(dec_small), args.steps) / args.steps / n_small
+        distinct = []
+        for i in range(n_small):
+            o = (i * Tm) % ndec
+            cnt = mw.route(layers[i % N_REPLICAS], xdec[o:o + Tm])["counts"]
+            distinct.append(int((cnt > 0).sum().item()))
+        small[Tm] = (t_small, float(np.mean(distinct)))
+
     # per-kernel durations: the library records events around its kernels
     def traced(fn, names):
         n = len(names) + 1
@@ -324,7 +350,7 @@ def run_gpu(args, rank, local_rank, world, dist):
     status = layers[0].status()
     if status != 0:
         raise RuntimeError(f"device status {status}")
-    return dict(c=c, L0=L0, x_np=x_np, xdec_np=xdec_np, t_step=t_step, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e,
+    return dict(c=c, L0=L0, x_np=x_np, xdec_np=xdec_np, t_step=t_step, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e, small=small,
                 clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device))
 
 
@@ -334,6 +360,13 @@ def run_gpu(args, rank, local_rank, world, dist):
 def expert_bytes(H, I):
     w = 3 * H * I
     return w // 2 + 2 * 2 * (w // 64)
+
+
+def decode_bytes_rows(c, T, distinct):
+    """Bytes a decode call of T rows must move: each distinct selected expert
+    once, the shared expert, router weights, shared gate, x and out."""
+    H, E, I = c["H"], c["E"], c["I"]
+    return (distinct + 1) * expert_bytes(H, I) + H * E * 4 + H * 4 + T * H * 2 + T * H * 2
 
 
 def decode_bytes(c, T=1):
@@ -464,6 +497,13 @@ def main():
                         "frac_of_peak": pre_flops / t_chunk / 1e12 / pk["bf16_tflops_sustained"]},
             "decode": {"tok_s": dec_tok_s, "us_per_token": 1e6 * r["t_dec"] / args.steps / ndec,
                        "roofline": roof_dec},
+            "decode_multirow": {f"T{Tm}": {"us_per_call": 1e6 * t, "tok_s": job_value(Tm, world, t),
+                                           "distinct_experts_per_call": dx,
+                                           "bytes_per_call": decode_bytes_rows(c, Tm, dx),
+                                           "hbm_gbs": decode_bytes_rows(c, Tm, dx) / t / 1e9,
+                                           "frac_of_hbm": decode_bytes_rows(c, Tm, dx) / t / 1e9 / pk["hbm_gbs"],
+                                           "path": "grouped tensor-core path (one read per selected expert)"}
+                                for Tm, (t, dx) in r["small"].items()},
             "roofline": roof,
             "kernels_us": {"prefill_4096": {k: 1e6 * v for k, v in r["k_pre"].items()},
                            "decode_T1": {k: 1e6 * v for k, v in r["k_dec"].items()}},

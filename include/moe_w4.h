@@ -131,9 +131,11 @@ int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
                  void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* Layer output for a decode batch, 1 <= T <= 16 (section "Optimise the
- * single-row weight path"): router, fused W4 GEMV for gate/up + SwiGLU, fused
- * W4 GEMV for down weighted by the routing scores plus the gated shared
- * expert.  out bf16 [T][H]. */
+ * single-row weight path").  T = 1: one kernel for the whole layer (router,
+ * W4 GEMVs for gate/up + SwiGLU and for down weighted by the routing scores,
+ * plus the gated shared expert).  T >= 2, or a shape that kernel does not
+ * cover: the grouped path of moe_w4_forward_prefill, which reads each selected
+ * expert once for all rows that chose it.  out bf16 [T][H]. */
 int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
                           moe_w4_bf16* out, void* workspace, size_t ws_bytes,
                           cudaStream_t stream);
@@ -156,8 +158,11 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
  * device memory, a real-time loop that must not wait on an allocator, a
  * memory plan fixed before the layer's shape is known).  The pages have no
  * counterpart: it is a deployment convenience of this library.
- * Same arguments, kernels and results as moe_w4_forward_decode, minus the
- * workspace: the scratch lives in one fixed device array of
+ * Same arguments as moe_w4_forward_decode, minus the workspace, and the same
+ * one-kernel path at T = 1; at T >= 2 it runs per-row CUDA-core GEMVs
+ * (router, gate/up, down kernels) instead of the grouped path, whose buffers
+ * would not fit, with results within the same tolerance of the oracle.  The
+ * scratch lives in one fixed device array of
  * MOE_W4_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library keeps until the process exits.
  *   - Calls needing more scratch than that (large H, E or I, or many tokens)
@@ -166,7 +171,8 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.
- *   - Every call reuses the same array and clears its control header first;
+ *   - Every call reuses the same array and clears its control header first
+ *     (except the T = 1 kernel's call counter);
  *     calls that overlap on the GPU (other streams, other threads) race and
  *     give wrong results: serialise them.
  *   - It never calls cudaMalloc, cudaFree or any allocating routine. */
