@@ -195,6 +195,27 @@ def test_widths_not_multiple_of_256(mw, torch):
     assert dl.status() == 0
 
 
+@pytest.mark.parametrize("H,E,I,k", [(1024, 128, 256, 4), (2048, 64, 1024, 4)])
+def test_other_shapes(mw, torch, H, E, I, k):
+    """Shapes off the benchmark's.  (1024, 128, 256, 4): the one-kernel T=1
+    decode with shapes taken at run time.  (2048, 64, 1024, 4): a down
+    projection whose K (I = 1024) exceeds the tensor-memory A ring, so every
+    down unit is one row block; E = 64 sends T=1 decode to the grouped path.
+    Routing, prefill and decode (1 and 5 rows) against the oracle."""
+    L = S.draw_layer(H, E, I, k, 1.0, seed=40 + k)
+    x = S.draw_tokens(L, 96, seed=41)
+    dl = mw.DeviceLayer(L)
+    xd = mw.tokens_to_device(x)
+    r = mw.route(dl, xd)
+    torch.cuda.synchronize()
+    check_route(r, L, x)
+    ref = O.moe_layer(L, x)["out"]
+    check_out(to_np_bits(mw.forward_prefill(dl, xd)), ref)
+    for a, b in ((0, 1), (5, 6), (10, 15)):
+        check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[a:b]))), ref[a:b])
+    assert dl.status() == 0
+
+
 # ---------------------------------------------------------------------------
 # decode: fused GEMV path
 # ---------------------------------------------------------------------------
