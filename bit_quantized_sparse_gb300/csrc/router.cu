@@ -215,7 +215,7 @@ constexpr int kTopkWarps = 8;
 
 // NIT >= ceil(H/256): 16-byte loads of the x row per lane, held in registers.
 template <int NIT>
-__global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 3 : 2) topk_kernel(const float* __restrict__ logits,
+__global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 4 : 2) topk_kernel(const float* __restrict__ logits,
                                                                int nsplit,   // 1 or 2 partial score arrays
                                                                const uint16_t* __restrict__ x,
                                                                const float* __restrict__ g, int T, int H, int E,
@@ -226,19 +226,22 @@ __global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 3 : 2) topk_kernel
     extern __shared__ float sm_topk[];
     float* gs = sm_topk;                    // [H] shared-expert gate vector, staged once per block
     float* sc_all = sm_topk + H;            // [kTopkWarps][E] scores
+    uint16_t* xs_all = reinterpret_cast<uint16_t*>(sc_all + kTopkWarps * E);   // [kTopkWarps][H] rows of x
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     for (int i = threadIdx.x; i < H / 4; i += blockDim.x)
         reinterpret_cast<float4*>(gs)[i] = reinterpret_cast<const float4*>(g)[i];
     __syncthreads();
     const int t = blockIdx.x * kTopkWarps + warp;
     if (t >= T) return;
-    // the token's row of x is requested first, so that its latency hides behind the selection
-    uint4 xv[NIT];
+    // the token's row of x is requested first, into shared memory (no registers held
+    // across the selection), so that its latency hides behind the selection
+    uint16_t* xs = xs_all + (size_t)warp * H;
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
         const int h = it * 256 + lane * 8;
-        xv[it] = h < H ? *reinterpret_cast<const uint4*>(x + (size_t)t * H + h) : make_uint4(0, 0, 0, 0);
+        if (h < H) cp_async_16(xs + h, x + (size_t)t * H + h);
     }
+    cp_async_commit();
     float* sc = sc_all + warp * E;
     // partial scores added in order; unrolled so that the loads of a row are in flight together
     const float* l0 = logits + (size_t)t * E;
@@ -249,11 +252,13 @@ __global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 3 : 2) topk_kernel
     select_topk_warp(sc, E, k, idx + (size_t)t * k, w + (size_t)t * k);
     float d = 0.f;
     bool fits = true;
+    cp_async_wait<0>();   // each lane reads back only the chunks it copied
 #pragma unroll
     for (int it = 0; it < NIT; ++it) {
         const int h = it * 256 + lane * 8;
         if (h >= H) break;
-        const uint32_t u[4] = {xv[it].x, xv[it].y, xv[it].z, xv[it].w};
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + h);
+        const uint32_t u[4] = {xv.x, xv.y, xv.z, xv.w};
         const float4 g0 = *reinterpret_cast<const float4*>(gs + h), g1 = *reinterpret_cast<const float4*>(gs + h + 4);
         const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         float f[8];
@@ -303,9 +308,33 @@ static bool bf16_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t co
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Dynamic shared memory of topk_kernel: the gate vector, the warps' scores and
+// the warps' rows of x; largest for H = 4096, E = 1024.
+static size_t topk_smem(int H, int E) {
+    return ((size_t)H + (size_t)kTopkWarps * E) * sizeof(float) + (size_t)kTopkWarps * H * 2;
+}
+static cudaError_t topk_smem_attr() {
+    static bool done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (done[dev]) return cudaSuccess;
+    const int mx = (int)topk_smem(4096, 1024);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(topk_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(topk_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
+}
+
 cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* x, const RouteOut& o,
                                   cudaStream_t st) {
     const int Epad = (L.E + kBM - 1) / kBM * kBM;
+    {
+        const cudaError_t e = topk_smem_attr();
+        if (e != cudaSuccess) return e;
+    }
     if (o.router_a) {   // tensor-core path
         router_split_kernel<<<dim3(L.H / 32, Epad / 32), 256, 0, st>>>(L.router_w, L.H, L.E, Epad, o.router_a);
         CUtensorMap mA, mX;
@@ -329,7 +358,7 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
     }
     trace_mark(st, 1);
     const int nsplit = o.router_a ? kRtSplit : 1;
-    const size_t sm = ((size_t)L.H + (size_t)kTopkWarps * L.E) * sizeof(float);
+    const size_t sm = topk_smem(L.H, L.E);
     const dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
     const int nit = (L.H + 255) / 256;   // H <= 4096
     if (nit <= 2)
