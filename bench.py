@@ -49,6 +49,9 @@ def parse():
                     help="step: the timed benchmark; prefill_chunk / decode: run --calls plain library calls on "
                          "one layer of the workload and exit (for profilers)")
     ap.add_argument("--calls", type=int, default=2)
+    ap.add_argument("--no-multirow", action="store_true",
+                    help="skip the multi-row decode measurement (for launch lists that should hold the step's "
+                         "kernels only)")
     return ap.parse_args()
 
 
@@ -271,7 +274,7 @@ def run_gpu(args, rank, local_rank, world, dist):
     # library's own router)
     small = {}
     n_small = 32
-    for Tm in SMALL_T:
+    for Tm in (() if args.no_multirow else SMALL_T):
         def dec_small(Tm=Tm):
             for i in range(n_small):
                 o = (i * Tm) % ndec
