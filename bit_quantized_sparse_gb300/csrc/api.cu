@@ -157,6 +157,12 @@ int moe_w4_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream)
 
 size_t moe_w4_status_offset(void) { return offsetof(Ctrl, status); }
 
+int moe_w4_test_skip_publish(void* workspace, size_t ws_bytes, int on, cudaStream_t stream) {
+    if (!workspace || ws_bytes < sizeof(Ctrl)) return MOE_W4_ERR_WORKSPACE;
+    uint8_t* word = static_cast<uint8_t*>(workspace) + offsetof(Ctrl, pad) + kCtrlInjectWord * sizeof(unsigned int);
+    return launch_status(cudaMemsetAsync(word, on ? 0x5A : 0, sizeof(unsigned int), stream));
+}
+
 int moe_w4_last_traced_kernels(void) { return g_traced_kernels; }
 
 int moe_w4_set_trace_events(cudaEvent_t* events, int n_events) {

@@ -298,6 +298,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     int* sel_e = reinterpret_cast<int*>(bar_dn + 2);                     // selected expert of this cluster
     float* sel_w = reinterpret_cast<float*>(sel_e + 1);                  // its weight (or gamma)
     uint32_t* xtag_s = reinterpret_cast<uint32_t*>(sel_e + 3);            // this call's exchange tag
+    uint32_t* xinj_s = reinterpret_cast<uint32_t*>(sel_e + 4);            // test hook: skip a publish
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // clusters are consecutive blocks: expert slot = block / kPE, CTA ei of the
@@ -340,7 +341,10 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     // polls the data itself instead of a counter and then the data.  CTA 0 advances
     // the counter once every cluster's router sum carries the tag, i.e. once every
     // CTA has read it.
-    if (tid == 0) *xtag_s = ld_acquire_u32(&a.ctrl->pad[kCtrlEpochWord]) + 1u;
+    if (tid == 0) {
+        *xtag_s = ld_acquire_u32(&a.ctrl->pad[kCtrlEpochWord]) + 1u;
+        *xinj_s = ld_acquire_u32(&a.ctrl->pad[kCtrlInjectWord]);
+    }
     if (tid < 2 * E) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) rx[j] = (r_hb + j < r_he) ? bf16_bits_to_float(__ldg(a.x + rh0 + r_hb + j)) : 0.f;
@@ -397,7 +401,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             float s = 0.f;
 #pragma unroll
             for (int r = 0; r < kCS; ++r) s += v[r];
-            st_tagged(a.cpart + (size_t)cid * E + e, s, *xtag_s);
+            if (!(*xinj_s != 0u && cid == 0)) st_tagged(a.cpart + (size_t)cid * E + e, s, *xtag_s);
         }
     }
     // the shared expert needs no routing: its loads start once its router sums are

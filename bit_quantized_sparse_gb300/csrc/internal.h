@@ -26,6 +26,10 @@ constexpr int kDownBlocksPerUnit = 4;
 // Word of the control header's pad[] holding the fused T=1 decode's call
 // counter (the tag of its exchanged values); kept across calls.
 constexpr int kCtrlEpochWord = 61;
+// Word of pad[] that the failure-detection test hook sets (0 in normal use):
+// while it is non-zero, the T=1 kernel's cluster 0 does not publish its router
+// sums, so every routed CTA's bounded wait for them runs out.
+constexpr int kCtrlInjectWord = 60;
 constexpr int kDownReuseMaxI = 512;
 inline int down_blocks_per_unit(int I) { return I <= kDownReuseMaxI ? kDownBlocksPerUnit : 1; }
 

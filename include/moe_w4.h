@@ -183,15 +183,25 @@ int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const moe_w4_bf1
 /* Optional tracing for benchmarks: while set, every forward call records
  * events[0..n_events) (cudaEvent_t, created by the caller) on its stream:
  * event 0 before its first kernel and event i after its i-th kernel, so
- * consecutive events bracket one kernel each (prefill: 8 kernels -- router
- * scores, top-k, chunk counts, scan, assign, grouped gate/up GEMM, grouped
- * down GEMM, combine; decode: 3 -- router, gate/up GEMV, down GEMV).  Extra
+ * consecutive events bracket one kernel each (prefill: 9 kernels -- router
+ * scores, top-k, chunk counts, scan, assign, row gather, grouped gate/up GEMM,
+ * grouped down GEMM, combine; decode of several rows: the same 9; three-kernel
+ * decode: router, gate/up GEMV, down GEMV).  Extra
  * kernels beyond n_events-1 are not traced; a call that launches fewer
  * kernels records its remaining events right after its last kernel (batch-1
  * decode of the supported shapes is one fused kernel).  Events are recorded with
  * cudaEventRecordExternal, so they also fire inside a captured CUDA graph.
  * Pass NULL to stop tracing.  Process-wide setting, not thread-safe. */
 int moe_w4_set_trace_events(cudaEvent_t* events, int n_events);
+
+/* Failure-detection test hook (no production use).  on != 0: the next batch-1
+ * decode calls on this workspace have one cluster skip publishing its router
+ * sums, so the other CTAs' bounded waits for them run out (after about 2 s):
+ * the call completes, its output is not valid, and the status word gets
+ * MOE_W4_STATUS_WAIT_TIMEOUT.  No GPU fault, trap or hang is involved.  on = 0
+ * (or moe_w4_workspace_init, which must follow any device-side error anyway)
+ * turns it off. */
+int moe_w4_test_skip_publish(void* workspace, size_t ws_bytes, int on, cudaStream_t stream);
 
 /* Number of kernels the most recent traced call launched (0 before any). */
 int moe_w4_last_traced_kernels(void);

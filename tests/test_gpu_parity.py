@@ -296,6 +296,31 @@ def test_prefill_fp16_range_status(mw, torch):
     assert dl.status() & mw.MOE_W4_STATUS_FP16_RANGE
 
 
+def test_decode_wait_timeout_is_reported(mw, torch):
+    """Failure detection without a GPU fault: with the test hook on, one cluster
+    of the batch-1 kernel does not publish its router sums, so the other CTAs'
+    bounded waits run out.  The call completes, the status word reports the
+    timeout, the context stays usable, and after re-initialising the workspace
+    the next call matches the oracle."""
+    import ctypes
+    L, x = S.draw_config("decode_T1")
+    dl = mw.DeviceLayer(L)
+    ws = dl.workspace(1)
+    xd = mw.tokens_to_device(x)
+    stream = torch.cuda.current_stream().cuda_stream
+    mw._check(mw.moe_w4_test_skip_publish(ws.data_ptr(), ws.numel(), 1, stream), "hook")
+    out = torch.empty((1, L.H), dtype=torch.bfloat16, device="cuda")
+    mw._check(mw.moe_w4_forward_decode(ctypes.byref(dl.c), 1, xd.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                                       ws.numel(), stream), "decode")
+    torch.cuda.synchronize()   # returns: every wait is bounded
+    assert dl.status() & mw.MOE_W4_STATUS_WAIT_TIMEOUT
+    mw._check(mw.moe_w4_workspace_init(ws.data_ptr(), ws.numel(), stream), "init")
+    torch.cuda.synchronize()
+    assert dl.status() == 0
+    check_out(to_np_bits(mw.forward_decode(dl, xd)), O.moe_layer(L, x)["out"])
+    assert dl.status() == 0
+
+
 def test_trace_events_outside_capture(mw, torch):
     """Kernel timing events recorded around an eager (not captured) call: the call
     succeeds and every event completes in order."""
