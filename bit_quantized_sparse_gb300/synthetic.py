@@ -47,6 +47,10 @@ CONFIGS = {
     # Zipf(1.2)-skewed routing
     "long_T16384": dict(T=16384, H=2048, E=256, top_k=8, I=512, zipf=1.2, seed=4,
                         chunk=4096, decode_steps=64),
+    # the 8-bit affine weight-format variant of the full layer, short prefill
+    "w8_T512": dict(T=512, H=2048, E=256, top_k=8, I=512, zipf=1.0, seed=5, bits=8),
+    # the 8-bit variant of the tiny layer
+    "w8_tiny_T4": dict(T=4, H=256, E=16, top_k=2, I=128, zipf=None, seed=6, bits=8),
 }
 
 
@@ -73,11 +77,12 @@ class W4Layer:
     sh_gate: W4Matrix                  # [I][H/8]
     sh_up: W4Matrix                    # [I][H/8]
     sh_down: W4Matrix                  # [H][I/8]
+    code_bits: int = 4                 # 4 (eight codes per word) or 8 (four codes per word)
 
     def nbytes_expert(self) -> int:
         """Bytes of one expert's three matrices (codes + scales + biases)."""
         w = 3 * self.H * self.I
-        return w // 2 + 2 * 2 * (w // GROUP)
+        return w * self.code_bits // 8 + 2 * 2 * (w // GROUP)
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
@@ -95,15 +100,18 @@ def _streams(seed: int, n: int):
     return [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(n)]
 
 
-def _draw_matrix(rng: np.random.Generator, lead: tuple, rows: int, cols: int) -> W4Matrix:
-    """Codes uniform in [0,15] (a uniform 32-bit word is eight uniform nibbles);
-    s = bf16(|N(0,0.02)|); b = bf16(-8 s + N(0,0.002))."""
-    assert cols % GROUP == 0
-    codes = rng.integers(0, 1 << 32, size=lead + (rows, cols // 8), dtype=np.uint32)
+def _draw_matrix(rng: np.random.Generator, lead: tuple, rows: int, cols: int, bits: int = 4) -> W4Matrix:
+    """4 bits: codes uniform in [0,15] (a uniform 32-bit word is eight uniform
+    nibbles); s = bf16(|N(0,0.02)|); b = bf16(-8 s + N(0,0.002)).  8 bits: codes
+    uniform in [0,255], s = bf16(|N(0,0.02)| / 17), b = bf16(-128 s + N(0,0.002)),
+    so that the weights have about the same spread as the 4-bit ones."""
+    assert cols % GROUP == 0 and bits in (4, 8)
+    codes = rng.integers(0, 1 << 32, size=lead + (rows, cols * bits // 32), dtype=np.uint32)
     shape_g = lead + (rows, cols // GROUP)
-    s_bits = f32_to_bf16_bits(np.abs(rng.normal(0.0, 0.02, size=shape_g)).astype(np.float32))
+    div, mid = (1.0, 8.0) if bits == 4 else (17.0, 128.0)
+    s_bits = f32_to_bf16_bits((np.abs(rng.normal(0.0, 0.02, size=shape_g)) / div).astype(np.float32))
     s = bf16_bits_to_f32(s_bits)
-    b_bits = f32_to_bf16_bits((-8.0 * s + rng.normal(0.0, 0.002, size=shape_g)).astype(np.float32))
+    b_bits = f32_to_bf16_bits((-mid * s + rng.normal(0.0, 0.002, size=shape_g)).astype(np.float32))
     return W4Matrix(codes, s_bits, b_bits)
 
 
@@ -113,19 +121,19 @@ def zipf_bias(E: int, s: float) -> np.ndarray:
     return (-s * np.log(np.arange(1, E + 1, dtype=np.float64))).astype(np.float32)
 
 
-def draw_layer(H: int, E: int, I: int, top_k: int, zipf: Optional[float], seed: int) -> W4Layer:
+def draw_layer(H: int, E: int, I: int, top_k: int, zipf: Optional[float], seed: int, bits: int = 4) -> W4Layer:
     rw, rr, rs = _streams(seed, 3)
-    gate = _draw_matrix(rw, (E,), I, H)
-    up = _draw_matrix(rw, (E,), I, H)
-    down = _draw_matrix(rw, (E,), H, I)
-    sh_gate = _draw_matrix(rs, (), I, H)
-    sh_up = _draw_matrix(rs, (), I, H)
-    sh_down = _draw_matrix(rs, (), H, I)
+    gate = _draw_matrix(rw, (E,), I, H, bits)
+    up = _draw_matrix(rw, (E,), I, H, bits)
+    down = _draw_matrix(rw, (E,), H, I, bits)
+    sh_gate = _draw_matrix(rs, (), I, H, bits)
+    sh_up = _draw_matrix(rs, (), I, H, bits)
+    sh_down = _draw_matrix(rs, (), H, I, bits)
     router_w = rr.normal(0.0, 0.05, size=(H, E)).astype(np.float32)
     shared_gate = rr.normal(0.0, 0.05, size=(H,)).astype(np.float32)
     bias = zipf_bias(E, zipf) if zipf else None
     return W4Layer(H, E, I, top_k, router_w, bias, shared_gate, gate, up, down,
-                   sh_gate, sh_up, sh_down)
+                   sh_gate, sh_up, sh_down, bits)
 
 
 def _screen_ok(x_bits: np.ndarray, layer: W4Layer, margin: float) -> np.ndarray:
@@ -161,12 +169,13 @@ def draw_tokens(layer: W4Layer, T: int, seed: int, stream: int = 0,
 def draw_config(name: str, T: Optional[int] = None, stream: int = 0):
     """Layer and token batch of a named workload; T overrides the batch size."""
     c = CONFIGS[name]
-    layer = draw_layer(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], c["seed"])
+    layer = draw_layer(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], c["seed"], c.get("bits", 4))
     x = draw_tokens(layer, c["T"] if T is None else T, c["seed"], stream)
     return layer, x
 
 
-def draw_layer_torch(H: int, E: int, I: int, top_k: int, zipf: Optional[float], seed: int, device="cuda"):
+def draw_layer_torch(H: int, E: int, I: int, top_k: int, zipf: Optional[float], seed: int, device="cuda",
+                     bits: int = 4):
     """Same recipe as draw_layer, drawn directly on a device with a seeded torch
     generator (fast enough for many layer replicas; the values differ from the
     numpy draw of the same seed).  Returns a W4Layer whose arrays are torch
@@ -176,12 +185,14 @@ def draw_layer_torch(H: int, E: int, I: int, top_k: int, zipf: Optional[float], 
     g = torch.Generator(device=device)
     g.manual_seed(int(seed))
 
+    div, mid = (1.0, 8.0) if bits == 4 else (17.0, 128.0)
+
     def mat(lead, rows, cols):
-        codes = torch.randint(-(1 << 31), 1 << 31, lead + (rows, cols // 8), generator=g, device=device,
+        codes = torch.randint(-(1 << 31), 1 << 31, lead + (rows, cols * bits // 32), generator=g, device=device,
                               dtype=torch.int64).to(torch.int32)
         shape_g = lead + (rows, cols // GROUP)
-        s = (torch.randn(shape_g, generator=g, device=device) * 0.02).abs().to(torch.bfloat16)
-        b = (-8.0 * s.float() + torch.randn(shape_g, generator=g, device=device) * 0.002).to(torch.bfloat16)
+        s = ((torch.randn(shape_g, generator=g, device=device) * 0.02).abs() / div).to(torch.bfloat16)
+        b = (-mid * s.float() + torch.randn(shape_g, generator=g, device=device) * 0.002).to(torch.bfloat16)
         return W4Matrix(codes, s.view(torch.int16), b.view(torch.int16))
 
     gate, up, down = mat((E,), I, H), mat((E,), I, H), mat((E,), H, I)
@@ -189,4 +200,4 @@ def draw_layer_torch(H: int, E: int, I: int, top_k: int, zipf: Optional[float], 
     router_w = torch.randn((H, E), generator=g, device=device) * 0.05
     shared_gate = torch.randn((H,), generator=g, device=device) * 0.05
     bias = torch.from_numpy(zipf_bias(E, zipf)).to(device) if zipf else None
-    return W4Layer(H, E, I, top_k, router_w, bias, shared_gate, gate, up, down, sh_gate, sh_up, sh_down)
+    return W4Layer(H, E, I, top_k, router_w, bias, shared_gate, gate, up, down, sh_gate, sh_up, sh_down, bits)

@@ -32,7 +32,13 @@ The pages leave the arithmetic details open; this oracle takes these readings
   R7  expert FFN is SwiGLU: h = silu(x Wg^T) * (x Wu^T), y = h Wd^T,
       silu(z) = z * sigmoid(z);
   R8  rows of one expert group are ordered by ascending token index;
-  R9  out = sum_j w_j y_{e_j} + gamma * y_shared, rounded once to bf16.
+  R9  out = sum_j w_j y_{e_j} + gamma * y_shared, rounded once to bf16;
+  R10 the 8-bit affine variant (a weight-format variant of the same layer: MLX
+      affine quantisation with group size 64, which the pages quantise encoder
+      layers with at 8 and 4 bits -- "Selective quantisation" section of the
+      page on that model's inference prototype) keeps R1 and R3 with q the
+      unsigned code 0..255, four codes per uint32, lowest input column in the
+      lowest byte.
 
 Everything is float64; the only rounding to bf16 is the final output (and it
 goes float64 -> float32 -> bf16, a double rounding that is far below any
@@ -67,18 +73,22 @@ def f64_to_bf16(x) -> np.ndarray:
 # group-affine 4-bit weights (section "Dequantise weights during matrix
 # multiplication"; readings R1-R3)
 # ----------------------------------------------------------------------------
-def unpack_codes(words: np.ndarray) -> np.ndarray:
-    """uint32 [..., n] -> uint8 codes [..., 8n]; column 8*w + i is nibble i of
-    word w, nibble 0 being the lowest four bits (R2)."""
+def unpack_codes(words: np.ndarray, bits: int = 4) -> np.ndarray:
+    """uint32 [..., n] -> uint8 codes [..., (32/bits) n].  4 bits: column 8*w + i
+    is nibble i of word w, nibble 0 being the lowest four bits (R2); 8 bits:
+    column 4*w + i is byte i of word w, byte 0 the lowest (R10)."""
+    assert bits in (4, 8)
+    per = 32 // bits
+    mask = np.uint32((1 << bits) - 1)
     w = np.asarray(words, dtype=np.uint32)
-    nib = np.stack([(w >> np.uint32(4 * i)) & np.uint32(0xF) for i in range(8)], axis=-1)
-    return nib.reshape(w.shape[:-1] + (w.shape[-1] * 8,)).astype(np.uint8)
+    c = np.stack([(w >> np.uint32(bits * i)) & mask for i in range(per)], axis=-1)
+    return c.reshape(w.shape[:-1] + (w.shape[-1] * per,)).astype(np.uint8)
 
 
-def dequant(codes: np.ndarray, scales: np.ndarray, biases: np.ndarray) -> np.ndarray:
+def dequant(codes: np.ndarray, scales: np.ndarray, biases: np.ndarray, bits: int = 4) -> np.ndarray:
     """Reconstruct a [rows][cols] matrix in float64: w[r, c] = s[r, c//64] * q[r, c]
-    + b[r, c//64] (R1, R3)."""
-    q = unpack_codes(codes).astype(np.float64)
+    + b[r, c//64] (R1, R3; R10 for 8-bit codes)."""
+    q = unpack_codes(codes, bits).astype(np.float64)
     s = np.repeat(bf16_to_f64(scales), GROUP, axis=-1)
     b = np.repeat(bf16_to_f64(biases), GROUP, axis=-1)
     assert q.shape == s.shape == b.shape, (q.shape, s.shape)
@@ -191,31 +201,33 @@ def expert_ffn(xr: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray) -
     return h @ wd.T
 
 
-def _mat(m, e=None):
+def _mat(m, e=None, bits=4):
     if e is None:
-        return dequant(m.codes, m.scales, m.biases)
-    return dequant(m.codes[e], m.scales[e], m.biases[e])
+        return dequant(m.codes, m.scales, m.biases, bits)
+    return dequant(m.codes[e], m.scales[e], m.biases[e], bits)
 
 
 def moe_layer(layer, x_bits: np.ndarray, tokens: Optional[np.ndarray] = None):
     """Whole layer for the rows `tokens` of x (all rows if None).
 
-    `layer` carries H, E, I, top_k, router_w, router_bias, shared_gate and the
-    six W4 matrices (attributes codes/scales/biases) gate, up, down, sh_gate,
-    sh_up, sh_down.  Returns a dict with out (float64), out_bf16 (bits) and the
+    `layer` carries H, E, I, top_k, router_w, router_bias, shared_gate, the
+    six quantised matrices (attributes codes/scales/biases) gate, up, down,
+    sh_gate, sh_up, sh_down and, optionally, code_bits (4 when absent).  Returns a dict with out (float64), out_bf16 (bits) and the
     routing / grouping intermediates of the selected rows.
     """
     x_all = bf16_to_f64(x_bits)
     rows = np.arange(x_all.shape[0]) if tokens is None else np.asarray(tokens)
     x = x_all[rows]
     k = layer.top_k
+    bits = getattr(layer, "code_bits", 4)
     idx, w, gamma, scores = route(x, layer.router_w, layer.router_bias, layer.shared_gate, k)
     out = np.zeros_like(x)
     for e in np.unique(idx):
         sel_t, sel_j = np.nonzero(idx == e)
-        y = expert_ffn(x[sel_t], _mat(layer.gate, e), _mat(layer.up, e), _mat(layer.down, e))
+        y = expert_ffn(x[sel_t], _mat(layer.gate, e, bits), _mat(layer.up, e, bits), _mat(layer.down, e, bits))
         out[sel_t] += w[sel_t, sel_j][:, None] * y
-    y_sh = expert_ffn(x, _mat(layer.sh_gate), _mat(layer.sh_up), _mat(layer.sh_down))
+    y_sh = expert_ffn(x, _mat(layer.sh_gate, None, bits), _mat(layer.sh_up, None, bits),
+                      _mat(layer.sh_down, None, bits))
     out += gamma[:, None] * y_sh
     res = dict(out=out, out_bf16=f64_to_bf16(out), idx=idx, w=w, gamma=gamma, scores=scores)
     if tokens is None:

@@ -58,6 +58,53 @@ def check_group_axis():
     assert got.shape == want.shape and np.array_equal(got, want)
 
 
+def check_dequant8_golden():
+    """8-bit variant: hand-worked words, four codes each, lowest byte first."""
+    n = 0
+    for ln in _lines("dequant8_cases.txt"):
+        tok = ln.split()
+        word = np.array([[int(tok[0], 16)] * 16], dtype=np.uint32)     # one row, 64 columns
+        s = bf(np.array([[float(tok[1])]], np.float32))
+        b = bf(np.array([[float(tok[2])]], np.float32))
+        want = np.array([float(v) for v in tok[3:7]])
+        got = O.dequant(word, s, b, bits=8)
+        assert got.shape == (1, 64)
+        assert np.array_equal(got[0, :4], want), (tok[0], got[0, :4], want)
+        assert np.array_equal(got[0, 60:64], want)
+        n += 1
+    assert n == 6
+
+
+def check_dequant8_group_axis():
+    """8-bit: 2 rows x 128 columns (32 words per row, two groups per row),
+    every code 3: w = 3 s + b of the group (row r, column c // 64)."""
+    codes = np.full((2, 32), 0x03030303, dtype=np.uint32)
+    s = bf(np.array([[1, 2], [4, 8]], np.float32))
+    b = bf(np.array([[0, 0.5], [0.25, 0]], np.float32))
+    got = O.dequant(codes, s, b, bits=8)
+    want = np.array([[3.0] * 64 + [6.5] * 64, [12.25] * 64 + [24.0] * 64])
+    assert got.shape == want.shape and np.array_equal(got, want)
+
+
+def check_formats_agree():
+    """The same codes 0..15 packed eight per word (4 bits) and four per word
+    (8 bits) reconstruct the same matrix: the two unpackings agree on which
+    column each code belongs to."""
+    rng = np.random.default_rng(7)
+    q = rng.integers(0, 16, size=(3, 128)).astype(np.uint32)
+    w4 = np.zeros((3, 16), np.uint32)
+    for i in range(8):
+        w4 |= q[:, i::8] << np.uint32(4 * i)
+    w8 = np.zeros((3, 32), np.uint32)
+    for i in range(4):
+        w8 |= q[:, i::4] << np.uint32(8 * i)
+    s = bf(rng.uniform(0.01, 0.1, size=(3, 2)).astype(np.float32))
+    b = bf(rng.uniform(-1, 1, size=(3, 2)).astype(np.float32))
+    a4, a8 = O.dequant(w4, s, b), O.dequant(w8, s, b, bits=8)
+    assert np.array_equal(a4, a8)
+    assert np.array_equal(O.unpack_codes(w8, 8), q.astype(np.uint8))
+
+
 def check_format_size():
     """Section "Dequantise weights during matrix multiplication": a 35B-parameter
     model shrinks from about 70 GB of bf16 to a 19.4 GB checkpoint.  One bf16
@@ -294,7 +341,8 @@ def check_row_independence():
         assert np.array_equal(part["idx"], full["idx"][a:b])
 
 
-PINS = [check_dequant_golden, check_group_axis, check_format_size, check_router_golden,
+PINS = [check_dequant_golden, check_group_axis, check_dequant8_golden, check_dequant8_group_axis,
+        check_formats_agree, check_format_size, check_router_golden,
         check_router_invariants, check_group_golden, check_group_invariants, check_silu,
         check_structured_ffn, check_layer_golden, check_identical_experts, check_dense_gating,
         check_brute_force_tiny, check_row_independence]
@@ -319,26 +367,46 @@ def test_generator_distribution():
     l = O.router_scores(O.bf16_to_f64(x), L.router_w, L.router_bias)
     lead = -np.sort(-l, axis=1)[:, :L.top_k + 1]
     assert np.all(lead[:, :-1] - lead[:, 1:] >= S.MARGIN)
+    # the 8-bit variant: codes uniform 0..255, s = |N(0, 0.02)| / 17, b = -128 s + N(0, 0.002)
+    L8, _ = S.draw_config("w8_tiny_T4")
+    assert L8.code_bits == 8 and L8.gate.codes.shape[-1] == L8.H // 4
+    q8 = O.unpack_codes(L8.gate.codes, 8).ravel()
+    cnt8 = np.bincount(q8, minlength=256)
+    assert cnt8.min() > 0.6 * q8.size / 256 and cnt8.max() < 1.4 * q8.size / 256
+    s8 = O.bf16_to_f64(L8.gate.scales).ravel()
+    b8 = O.bf16_to_f64(L8.gate.biases).ravel()
+    assert np.all(s8 >= 0) and abs(s8.mean() - 0.02 / 17 * math.sqrt(2 / math.pi)) < 2e-4
+    assert abs(np.std(b8 + 128 * s8) - 0.002) < 5e-4
 
 
 # ---------------------------------------------------------------------------
 # planted mistakes: each broken oracle must fail at least one pin
 # ---------------------------------------------------------------------------
-def _reversed_nibbles(words):
+def _reversed_nibbles(words, bits=4):
+    if bits != 4:
+        return _UNPACK(words, bits)
     w = np.asarray(words, dtype=np.uint32)
     nib = np.stack([(w >> np.uint32(4 * (7 - i))) & np.uint32(0xF) for i in range(8)], axis=-1)
     return nib.reshape(w.shape[:-1] + (w.shape[-1] * 8,)).astype(np.uint8)
 
 
-def _swapped_affine(codes, scales, biases):
-    q = O.unpack_codes(codes).astype(np.float64)
+def _reversed_bytes(words, bits=4):
+    if bits != 8:
+        return _UNPACK(words, bits)
+    w = np.asarray(words, dtype=np.uint32)
+    c = np.stack([(w >> np.uint32(8 * (3 - i))) & np.uint32(0xFF) for i in range(4)], axis=-1)
+    return c.reshape(w.shape[:-1] + (w.shape[-1] * 4,)).astype(np.uint8)
+
+
+def _swapped_affine(codes, scales, biases, bits=4):
+    q = O.unpack_codes(codes, bits).astype(np.float64)
     s = np.repeat(O.bf16_to_f64(scales), 64, axis=-1)
     b = np.repeat(O.bf16_to_f64(biases), 64, axis=-1)
     return b * q + s
 
 
-def _groups_down_rows(codes, scales, biases):
-    q = O.unpack_codes(codes).astype(np.float64)
+def _groups_down_rows(codes, scales, biases, bits=4):
+    q = O.unpack_codes(codes, bits).astype(np.float64)
     s = np.repeat(np.swapaxes(O.bf16_to_f64(scales), -1, -2), 64, axis=-1)   # group index on the wrong axis
     b = np.repeat(np.swapaxes(O.bf16_to_f64(biases), -1, -2), 64, axis=-1)
     return s * q + b
@@ -381,8 +449,11 @@ def _ungated_sigmoid(z):
     return np.ones_like(np.asarray(z, dtype=np.float64)) if np.ndim(z) else 1.0
 
 
+_UNPACK = O.unpack_codes
+
 MUTANTS = [
     ("unpack_codes", _reversed_nibbles),
+    ("unpack_codes", _reversed_bytes),
     ("dequant", _swapped_affine),
     ("dequant", _groups_down_rows),
     ("route", _unrenormalised_route),
