@@ -343,10 +343,25 @@ MW4_DEV uint32_t h2_as_u32(__half2 v) { return *reinterpret_cast<uint32_t*>(&v);
 MW4_DEV uint32_t bf162_as_u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
 
 MW4_DEV int chunk_pos_of_col(int j) { return ((j & 3) << 1) | (j >> 2); }   // inverse of kChunkOrder
+// 8-bit codes: two words per 8 columns, each giving the pairs (c0, c2), (c1, c3),
+// so columns {0,2,1,3,4,6,5,7} sit at positions 0..7; position of column j.
+MW4_DEV int chunk8_pos_of_col(int j) { return (j & 4) | ((j & 1) << 1) | ((j >> 1) & 1); }
 
 // w = s*q + b for eight codes in chunk order; s2 = (s, s), s16 = (s/16, s/16),
 // b2 = (b, b).  q (or 16 q) is recovered exactly and the product and sum are
 // exact inside the fused multiply-add: each weight is rounded to fp16 once.
+// w = s*q + b for the four 8-bit codes of one word (lowest byte first): the fp16
+// pairs (c0, c2) and (c1, c3).  1024 + q is exact in fp16 for q <= 255; each
+// weight is rounded to fp16 once, in the fused multiply-add.
+MW4_DEV void dequant4x8_f16(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[2]) {
+    const uint32_t magic = 0x64006400u;
+    const uint32_t p0 = (w & 0x00FF00FFu) | magic;           // 1024 + (q0, q2)
+    const uint32_t p1 = ((w >> 8) & 0x00FF00FFu) | magic;    // 1024 + (q1, q3)
+    const __half2 k1024 = u32_as_h2(magic);
+    o[0] = h2_as_u32(__hfma2(s2, __hsub2(u32_as_h2(p0), k1024), b2));
+    o[1] = h2_as_u32(__hfma2(s2, __hsub2(u32_as_h2(p1), k1024), b2));
+}
+
 MW4_DEV void dequant8_f16(uint32_t w, __half2 s2, __half2 s16, __half2 b2, uint32_t (&o)[4]) {
     const uint32_t magic = 0x64006400u;
     const uint32_t w8 = w >> 8;

@@ -735,6 +735,7 @@ static FusedKernel fused_kernel_for(const moe_w4_layer& L) {
 }
 
 static bool shape_ok(const moe_w4_layer& L) {
+    if (code_bits_of(L) != 4) return false;   // the mma.sync dot engine unpacks nibbles
     if (L.H % 256 || L.I % 256 || L.H > 4096 || L.I > 2048) return false;   // slices of 16 rows; <= 16 row tiles
     if (L.H / 256 > 16) return false;                                         // gate/up box barriers
     if (L.E < 128 || L.E > 256 || L.E % 32) return false;   // top-k: E/32 warps sort 32 scores each; 2E floats of partials

@@ -69,7 +69,6 @@ struct GemmArgs {
 
 constexpr int kGK = 128;                                // reduction columns per pipeline step
 static_assert(kGK == 2 * kGroup, "a step holds two quantisation groups");
-constexpr uint32_t kCodesBytes = kBM * (kGK / 8) * 4;   // 8 KB of packed codes per matrix per step
 constexpr uint32_t kSubBytes = kBN * 64 * 2;            // 16 KB: 128 B rows x 64 fp16 columns, 128-byte swizzle
 constexpr uint32_t kTileBytes = 2 * kSubBytes;          // B tile of one step: two K sub-tiles
 
@@ -77,9 +76,12 @@ constexpr uint32_t kTileBytes = 2 * kSubBytes;          // B tile of one step: t
 // The dequantised weights (the A operand) live in tensor memory, written by
 // tcgen05.st and read by the MMA from there: no shared-memory round trip and
 // no proxy fence.  TMEM (512 columns) holds the accumulators and an A ring.
-template <bool DUAL>
+template <bool DUAL, int BITS>
 struct Geo {
     static constexpr int NMAT = DUAL ? 2 : 1;
+    // packed codes of one weight row per step (64 B for 4-bit, 128 B for 8-bit codes)
+    static constexpr uint32_t kCodesRowBytes = kGK * BITS / 8;
+    static constexpr uint32_t kCodesBytes = kBM * kCodesRowBytes;   // per matrix per step
     // 8 dequantiser warps: gate/up one thread per (matrix, weight row); down two
     // threads per weight row, one of the step's two groups each (more threads in
     // flight for the one matrix)
@@ -95,7 +97,7 @@ struct Geo {
     // have read a step, and the B rows, freed when the step's MMAs complete.
     // The codes thus run several steps ahead of the dequantisers, whatever the
     // MMAs' lag.
-    static constexpr int SC = DUAL ? 4 : 8;
+    static constexpr int SC = DUAL ? (BITS == 8 ? 3 : 4) : (BITS == 8 ? 6 : 8);
     static constexpr int SB = 4;
     static constexpr uint32_t C_STAGE = NMAT * kCodesBytes;
     static constexpr uint32_t ACC_COLS = NMAT * 128;      // TMEM columns per accumulator buffer
@@ -108,10 +110,11 @@ struct Geo {
                (2 * SB + 2 * SC + 2 * SA + 4) * 8 + 16;
     }
 };
-static_assert(Geo<true>::SA == 2 && Geo<false>::SA == 4, "TMEM map");
-static_assert(Geo<true>::bytes() <= 232448 && Geo<false>::bytes() <= 232448, "shared memory per CTA");
-static_assert(kDownReuseMaxI / kGK <= Geo<false>::SA, "a reused down weight tile holds its whole K in the A ring");
-static_assert(Geo<true>::SA <= Geo<true>::SB, "gate/up A slots are freed by the B-ring barriers");
+static_assert(Geo<true, 4>::SA == 2 && Geo<false, 4>::SA == 4, "TMEM map");
+static_assert(Geo<true, 4>::bytes() <= 232448 && Geo<false, 4>::bytes() <= 232448, "shared memory per CTA");
+static_assert(Geo<true, 8>::bytes() <= 232448 && Geo<false, 8>::bytes() <= 232448, "shared memory per CTA");
+static_assert(kDownReuseMaxI / kGK <= Geo<false, 4>::SA, "a reused down weight tile holds its whole K in the A ring");
+static_assert(Geo<true, 4>::SA <= Geo<true, 4>::SB, "gate/up A slots are freed by the B-ring barriers");
 
 MW4_DEV uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -161,13 +164,15 @@ MW4_DEV TileInfo tile_from(const GemmArgs& a, int4 bi, int m) {
 }
 MW4_DEV TileInfo block_info(const GemmArgs& a, int rb, int m) { return tile_from(a, __ldg(a.blkinfo + rb), m); }
 
-template <bool DUAL>
-__global__ void __launch_bounds__(Geo<DUAL>::kThreads, 1)
+template <bool DUAL, int BITS>
+__global__ void __launch_bounds__(Geo<DUAL, BITS>::kThreads, 1)
 grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap map0r,
                        const __grid_constant__ CUtensorMap map1r, const __grid_constant__ CUtensorMap map0s,
                        const __grid_constant__ CUtensorMap map1s, const __grid_constant__ CUtensorMap mapb,
                        const __grid_constant__ CUtensorMap mapbs) {
-    using GG = Geo<DUAL>;
+    using GG = Geo<DUAL, BITS>;
+    constexpr uint32_t kCodesBytes = GG::kCodesBytes;
+    constexpr int kCodeWords = kGK * BITS / 32;   // code words per row per step
     constexpr int NMAT = GG::NMAT, SC = GG::SC, SB = GG::SB, SA = GG::SA;
     const int ntiles = a.ntiles[0];
     const int G = a.K / kGroup, nK = a.K / kGK;
@@ -237,16 +242,17 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
             const CUtensorMap* m0 = ti.sh ? &map0s : &map0r;
             const CUtensorMap* m1 = ti.sh ? &map1s : &map1r;
             if (lane == 0) {   // the tile's packed codes are one contiguous range per matrix
-                prefetch_l2((ti.sh ? a.c0s : a.c0r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
-                if (DUAL) prefetch_l2((ti.sh ? a.c1s : a.c1r) + (size_t)ti.arow * (a.K / 8), kBM * (a.K / 2));
+                const size_t rw = (size_t)a.K * BITS / 32;   // code words per weight row
+                prefetch_l2((ti.sh ? a.c0s : a.c0r) + (size_t)ti.arow * rw, (uint32_t)(kBM * rw * 4));
+                if (DUAL) prefetch_l2((ti.sh ? a.c1s : a.c1r) + (size_t)ti.arow * rw, (uint32_t)(kBM * rw * 4));
             }
             for (int ks = 0; ks < nK; ++ks, ++gk) {
                 const int s = gk % SC;
                 if (!mbar_wait_warp(&c_empty[s], ((gk / SC) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&c_full[s], NMAT * kCodesBytes);
-                    tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * (kGK / 8), ti.arow, &c_full[s]);
-                    if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * (kGK / 8), ti.arow, &c_full[s]);
+                    tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * kCodeWords, ti.arow, &c_full[s]);
+                    if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * kCodeWords, ti.arow, &c_full[s]);
                 }
             }
         }
@@ -344,7 +350,9 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         // ------------------------------------------------------------ dequantisation: one weight row per thread
         const int td = tid - 32 * GG::kDeqWarp0, row = td % 128;
         const int mat = DUAL ? td / 128 : 0, hsel = DUAL ? -1 : td / 128;   // down: which group of the step
-        const int sw = (row >> 1) & 3;   // 64-byte swizzle phase of this row's codes
+        // swizzle phase of this row's 16-byte code chunks (64-byte rows for 4-bit
+        // codes, 128-byte rows for 8-bit)
+        const int sw = BITS == 8 ? (row & 7) : ((row >> 1) & 3);
         const bool chunked = (G % 8) == 0;
         int gk = 0;
         bool ok = true;
@@ -386,7 +394,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                                                        a.status))
                                : mbar_wait(&a_empty[sa], ((gk / SA) & 1) ^ 1, abort_flag, a.status));
                     if (!ok) break;
-                    const uint8_t* cr = C_of(sc, mat) + row * 64;
+                    const uint8_t* cr = C_of(sc, mat) + row * GG::kCodesRowBytes;
                     tc_fence_after();   // the MMAs that read this A slot have completed
                     // this thread's weight row -> its TMEM lane, 64 columns of fp16 pairs, in quads of 16
                     const uint32_t tdst =
@@ -400,16 +408,32 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16);
                         const __half2 b2 = __halves2half2(b_h, b_h);
 #pragma unroll
-                        for (int qq = 0; qq < 2; ++qq) {
+                        for (int qq = 0; qq < 2; ++qq) {   // 32 columns of the group -> 16 TMEM columns
                             const int q = 2 * grp + qq;
-                            const uint4 w = *reinterpret_cast<const uint4*>(cr + ((q ^ sw) << 4));
-                            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
                             uint32_t o[16];
+                            if (BITS == 8) {   // two 16-byte chunks of four words
 #pragma unroll
-                            for (int wi = 0; wi < 4; ++wi) {
-                                uint32_t q4[4];
-                                dequant8_f16(words[wi], s2, s2_16, b2, q4);
-                                o[4 * wi] = q4[0]; o[4 * wi + 1] = q4[1]; o[4 * wi + 2] = q4[2]; o[4 * wi + 3] = q4[3];
+                                for (int hh2 = 0; hh2 < 2; ++hh2) {
+                                    const int c = 2 * q + hh2;
+                                    const uint4 w = *reinterpret_cast<const uint4*>(cr + ((c ^ sw) << 4));
+                                    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                    for (int wi = 0; wi < 4; ++wi) {
+                                        uint32_t q2[2];
+                                        dequant4x8_f16(words[wi], s2, b2, q2);
+                                        o[8 * hh2 + 2 * wi] = q2[0];
+                                        o[8 * hh2 + 2 * wi + 1] = q2[1];
+                                    }
+                                }
+                            } else {           // one 16-byte chunk of four words
+                                const uint4 w = *reinterpret_cast<const uint4*>(cr + ((q ^ sw) << 4));
+                                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                for (int wi = 0; wi < 4; ++wi) {
+                                    uint32_t q4[4];
+                                    dequant8_f16(words[wi], s2, s2_16, b2, q4);
+                                    o[4 * wi] = q4[0]; o[4 * wi + 1] = q4[1]; o[4 * wi + 2] = q4[2]; o[4 * wi + 3] = q4[3];
+                                }
                             }
                             tmem_st16(tdst + 16 * q, o);
                         }
@@ -451,7 +475,9 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 const uint32_t lane_addr = taddr + b * GG::ACC_COLS + ((uint32_t)(q * 32) << 16);
                 // h is the K operand of the down projection: store it in chunk order
                 const int orow = ti.m * kBM + q * 32 + lane;
-                const int ocol = DUAL ? ((orow & ~7) | chunk_pos_of_col(orow & 7)) : orow;
+                const int ocol = DUAL ? ((orow & ~7) | (BITS == 8 ? chunk8_pos_of_col(orow & 7)
+                                                                  : chunk_pos_of_col(orow & 7)))
+                                      : orow;
                 for (int c0 = half * 16; c0 < ti.nrows; c0 += 32) {
                     uint32_t g[16], u[16];
                     tmem_ld16(lane_addr + c0, g);
@@ -580,20 +606,45 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One grouped GEMM launch (the shared-memory size is raised once per device
+// and instance).
+template <bool DUAL, int BITS>
+static cudaError_t launch_gemm(const GemmArgs& g, int grid, const CUtensorMap& m0r, const CUtensorMap& m1r,
+                               const CUtensorMap& m0s, const CUtensorMap& m1s, const CUtensorMap& mb,
+                               const CUtensorMap& mbs, cudaStream_t st) {
+    using GG = Geo<DUAL, BITS>;
+    static bool set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!set[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(grouped_w4_gemm_kernel<DUAL, BITS>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GG::bytes());
+        if (e != cudaSuccess) return e;
+        set[dev] = true;
+    }
+    grouped_w4_gemm_kernel<DUAL, BITS><<<grid, GG::kThreads, GG::bytes(), st>>>(g, m0r, m1r, m0s, m1s, mb, mbs);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const PrefillWs& p,
                                cudaStream_t st) {
+    const int bits = code_bits_of(L);
     const int H = L.H, I = L.I, E = L.E, k = L.top_k;
     const uint64_t rows_all = (uint64_t)T * k + T;
     CUtensorMap mg, mu, msg, msu, md, msd, mh, mxg, mx;
     const auto U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
-    const auto SW64 = CU_TENSOR_MAP_SWIZZLE_64B;   // 64-byte code rows: bank-conflict-free per-row reads
-    constexpr uint32_t cw = kGK / 8;                // code words per row per step
-    bool ok = make_map(&mg, U32, 4, L.gate.codes, (uint64_t)E * I, H / 8, kBM, cw, SW64) &&
-              make_map(&mu, U32, 4, L.up.codes, (uint64_t)E * I, H / 8, kBM, cw, SW64) &&
-              make_map(&msg, U32, 4, L.sh_gate.codes, I, H / 8, kBM, cw, SW64) &&
-              make_map(&msu, U32, 4, L.sh_up.codes, I, H / 8, kBM, cw, SW64) &&
-              make_map(&md, U32, 4, L.down.codes, (uint64_t)E * H, I / 8, kBM, cw, SW64) &&
-              make_map(&msd, U32, 4, L.sh_down.codes, H, I / 8, kBM, cw, SW64) &&
+    // code rows of one step: 64 bytes (4-bit codes) or 128 bytes (8-bit), swizzled
+    // to match so that the per-row reads are bank-conflict free
+    const auto SWC = bits == 8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const uint32_t cw = kGK * bits / 32;            // code words per row per step
+    const int wH = H * bits / 32, wI = I * bits / 32;   // code words per row of gate/up and of down
+    bool ok = make_map(&mg, U32, 4, L.gate.codes, (uint64_t)E * I, wH, kBM, cw, SWC) &&
+              make_map(&mu, U32, 4, L.up.codes, (uint64_t)E * I, wH, kBM, cw, SWC) &&
+              make_map(&msg, U32, 4, L.sh_gate.codes, I, wH, kBM, cw, SWC) &&
+              make_map(&msu, U32, 4, L.sh_up.codes, I, wH, kBM, cw, SWC) &&
+              make_map(&md, U32, 4, L.down.codes, (uint64_t)E * H, wI, kBM, cw, SWC) &&
+              make_map(&msd, U32, 4, L.sh_down.codes, H, wI, kBM, cw, SWC) &&
               make_map(&mh, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.hh, rows_all, I, kBN, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&mxg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.xg, (uint64_t)T * k, H, kBN, 64,
@@ -602,25 +653,12 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return cudaErrorInvalidValue;
 
-    const size_t sm_gu = Geo<true>::bytes(), sm_dn = Geo<false>::bytes();
     int nsm = 0;
     {
         int dv = 0;
         cudaGetDevice(&dv);
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dv);
         if (nsm <= 0) nsm = 148;
-    }
-    static int set_gu[64] = {}, set_dn[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (set_gu[dev] < (int)sm_gu) {
-        cudaFuncSetAttribute(grouped_w4_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_gu);
-        set_gu[dev] = (int)sm_gu;
-    }
-    if (set_dn[dev] < (int)sm_dn) {
-        cudaFuncSetAttribute(grouped_w4_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_dn);
-        set_dn[dev] = (int)sm_dn;
     }
 
     GemmArgs a{};
@@ -639,7 +677,9 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     const int nrg = T * k;
     gather_rows_kernel<<<(unsigned)((nrg + 7) / 8), 256, 0, st>>>(p.x16, p.perm, p.xg, nrg, H, k);
     trace_mark(st, 6);
-    grouped_w4_gemm_kernel<true><<<grid_gu, Geo<true>::kThreads, sm_gu, st>>>(a, mg, mu, msg, msu, mxg, mx);
+    cudaError_t e = bits == 8 ? launch_gemm<true, 8>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
+                              : launch_gemm<true, 4>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st);
+    if (e != cudaSuccess) return e;
     trace_mark(st, 7);
 
     // down: A = Wd rows (H per expert), K = I, B = hh rows, out = ys [.][H]
@@ -650,7 +690,9 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     b.c0r = L.down.codes; b.c1r = nullptr; b.c0s = L.sh_down.codes; b.c1s = nullptr; b.b_rows = p.hh; b.b_rows_sh = p.hh;
     b.out = p.ys; b.K = I; b.rows_e = H; b.out_cols = H;
     const int grid_dn = p.max_tiles_dn < nsm ? p.max_tiles_dn : nsm;
-    grouped_w4_gemm_kernel<false><<<grid_dn, Geo<false>::kThreads, sm_dn, st>>>(b, md, md, msd, msd, mh, mh);
+    e = bits == 8 ? launch_gemm<false, 8>(b, grid_dn, md, md, msd, msd, mh, mh, st)
+                  : launch_gemm<false, 4>(b, grid_dn, md, md, msd, msd, mh, mh, st);
+    if (e != cudaSuccess) return e;
     trace_mark(st, 8);
 
     const size_t nthr = (size_t)T * (H / 8);

@@ -76,6 +76,7 @@ extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const
     if (!L || L->E < 1 || L->top_k < 1 || L->top_k > 8 || L->top_k > L->E || L->H <= 0 || L->I <= 0)
         return MOE_W4_ERR_INVALID;
     if (L->H % kBM || L->I % kBM || L->H > 4096 || L->I > 4096 || L->E > 1024) return MOE_W4_ERR_UNSUPPORTED;
+    if (L->code_bits != 0 && L->code_bits != 4) return MOE_W4_ERR_UNSUPPORTED;   // per-row GEMVs unpack nibbles
     if (T < 0) return MOE_W4_ERR_INVALID;
     if (T > kDecodeMaxT) return MOE_W4_ERR_UNSUPPORTED;
     if (T == 0) return MOE_W4_OK;

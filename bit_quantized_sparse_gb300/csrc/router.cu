@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 4 : 2) topk_kernel
                                                                const float* __restrict__ g, int T, int H, int E,
                                                                int k, int32_t* __restrict__ idx,
                                                                float* __restrict__ w, float* __restrict__ gamma,
-                                                               uint16_t* __restrict__ x16,
+                                                               uint16_t* __restrict__ x16, int bits,
                                                                unsigned int* status) {
     extern __shared__ float sm_topk[];
     float* gs = sm_topk;                    // [H] shared-expert gate vector, staged once per block
@@ -272,11 +272,19 @@ __global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 4 : 2) topk_kernel
             d = fmaf(f[i], gg[i], d);
             fits = fits && fabsf(f[i]) <= 65504.f;
         }
-        // fp16 copy in chunk order {0,4,1,5,2,6,3,7} (the order the dequantised weights use)
+        // fp16 copy in the K order the dequantised weights use: 4-bit codes
+        // {0,4,1,5,2,6,3,7}, 8-bit codes {0,2,1,3,4,6,5,7} per 8 columns
         if (x16) {
             uint32_t hv[4];
+            if (bits == 8) {
+                hv[0] = h2_as_u32(__floats2half2_rn(f[0], f[2]));
+                hv[1] = h2_as_u32(__floats2half2_rn(f[1], f[3]));
+                hv[2] = h2_as_u32(__floats2half2_rn(f[4], f[6]));
+                hv[3] = h2_as_u32(__floats2half2_rn(f[5], f[7]));
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) hv[i] = h2_as_u32(__floats2half2_rn(f[i], f[i + 4]));
+                for (int i = 0; i < 4; ++i) hv[i] = h2_as_u32(__floats2half2_rn(f[i], f[i + 4]));
+            }
             *reinterpret_cast<uint4*>(x16 + (size_t)t * H + h) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
         }
     }
@@ -363,16 +371,16 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
     const int nit = (L.H + 255) / 256;   // H <= 4096
     if (nit <= 2)
         topk_kernel<2><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                o.gamma, o.x16, o.status);
+                                                o.gamma, o.x16, code_bits_of(L), o.status);
     else if (nit <= 4)
         topk_kernel<4><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                o.gamma, o.x16, o.status);
+                                                o.gamma, o.x16, code_bits_of(L), o.status);
     else if (nit <= 8)
         topk_kernel<8><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                o.gamma, o.x16, o.status);
+                                                o.gamma, o.x16, code_bits_of(L), o.status);
     else
         topk_kernel<16><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                 o.gamma, o.x16, o.status);
+                                                 o.gamma, o.x16, code_bits_of(L), o.status);
     trace_mark(st, 2);
     return cudaGetLastError();
 }

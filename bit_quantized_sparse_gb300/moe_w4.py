@@ -52,7 +52,7 @@ class MoeW4Layer(ctypes.Structure):
     _fields_ = [("H", c_int), ("E", c_int), ("I", c_int), ("top_k", c_int),
                 ("router_w", c_void_p), ("router_bias", c_void_p), ("shared_gate", c_void_p),
                 ("gate", MoeW4Mat), ("up", MoeW4Mat), ("down", MoeW4Mat),
-                ("sh_gate", MoeW4Mat), ("sh_up", MoeW4Mat), ("sh_down", MoeW4Mat)]
+                ("sh_gate", MoeW4Mat), ("sh_up", MoeW4Mat), ("sh_down", MoeW4Mat), ("code_bits", c_int)]
 
 
 _P = ctypes.POINTER(MoeW4Layer)
@@ -148,6 +148,8 @@ class DeviceLayer:
         self.mats = {n: mat(getattr(layer, n)) for n in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")}
         self.c = MoeW4Layer()
         self.c.H, self.c.E, self.c.I, self.c.top_k = self.H, self.E, self.I, self.top_k
+        self.code_bits = int(getattr(layer, "code_bits", 4))
+        self.c.code_bits = self.code_bits
         self.c.router_w = _ptr(self.router_w)
         self.c.router_bias = _ptr(self.router_bias)
         self.c.shared_gate = _ptr(self.shared_gate)

@@ -65,9 +65,17 @@ typedef struct {
 } moe_w4_mat;
 
 /* The layer.  H hidden size, E routed experts, I intermediate size (routed and
- * shared), top_k experts kept per token.
- * Supported: H % 128 == 0, I % 128 == 0, 64 <= H <= 16384, 128 <= I <= 4096,
- * 1 <= E <= 1024, 1 <= top_k <= min(E, 8).  Every pointer 16-byte aligned. */
+ * shared), top_k experts kept per token, code_bits the width of one code.
+ * Supported: H % 128 == 0, I % 128 == 0, 128 <= H <= 4096, 128 <= I <= 4096,
+ * 1 <= E <= 1024, 1 <= top_k <= min(E, 8), code_bits 4 (or 0, read as 4) or 8.
+ * Every pointer 16-byte aligned.
+ * Codes: code_bits = 4: eight per uint32, the lowest column in the lowest
+ * nibble (rows of cols/8 words); code_bits = 8: four per uint32, the lowest
+ * column in the lowest byte (rows of cols/4 words).  Either way a weight is
+ * s * q + b with q the unsigned code and s, b the bf16 scale and bias of its
+ * group of 64 columns.  8-bit layers run the grouped tensor-core path for
+ * every batch size (also T = 1) and are not supported by
+ * moe_w4_forward_decode_noalloc. */
 typedef struct {
     int H, E, I, top_k;
     const float* router_w;     /* [H][E] fp32                                   */
@@ -77,6 +85,8 @@ typedef struct {
     moe_w4_mat down;           /* routed: [E][H][I/8] codes, [E][H][I/64] s, b  */
     moe_w4_mat sh_gate, sh_up; /* shared: [I][H/8] codes, [I][H/64] s, b        */
     moe_w4_mat sh_down;        /* shared: [H][I/8] codes, [H][I/64] s, b        */
+    int code_bits;             /* 4 (or 0) or 8; with 8 the codes arrays hold
+                                  cols/4 words per row instead of cols/8          */
 } moe_w4_layer;
 
 enum {

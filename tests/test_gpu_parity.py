@@ -216,6 +216,30 @@ def test_other_shapes(mw, torch, H, E, I, k):
     assert dl.status() == 0
 
 
+@pytest.mark.parametrize("name", ["w8_tiny_T4", "w8_T512"])
+def test_w8_layer(mw, torch, name):
+    """The 8-bit affine weight-format variant (four codes per word): routing,
+    prefill and decode (1 and 4 rows, both on the grouped path) against the
+    oracle; the allocation-free decode declines it."""
+    import ctypes
+    L, x = S.draw_config(name)
+    assert L.code_bits == 8
+    dl = mw.DeviceLayer(L)
+    xd = mw.tokens_to_device(x)
+    r = mw.route(dl, xd)
+    torch.cuda.synchronize()
+    check_route(r, L, x)
+    ref = O.moe_layer(L, x)["out"]
+    check_out(to_np_bits(mw.forward_prefill(dl, xd)), ref)
+    check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[:1]))), ref[:1])
+    if x.shape[0] >= 8:
+        check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[4:8]))), ref[4:8])
+    out = torch.empty((1, L.H), dtype=torch.bfloat16, device="cuda")
+    assert mw.moe_w4_forward_decode_noalloc(ctypes.byref(dl.c), 1, xd.data_ptr(), out.data_ptr(),
+                                            None) == mw.MOE_W4_ERR_UNSUPPORTED
+    assert dl.status() == 0
+
+
 # ---------------------------------------------------------------------------
 # decode: fused GEMV path
 # ---------------------------------------------------------------------------
