@@ -34,11 +34,19 @@ The pages leave the arithmetic details open; this oracle takes these readings
   R8  rows of one expert group are ordered by ascending token index;
   R9  out = sum_j w_j y_{e_j} + gamma * y_shared, rounded once to bf16;
   R10 the 8-bit affine variant (a weight-format variant of the same layer: MLX
-      affine quantisation with group size 64, which the pages quantise encoder
-      layers with at 8 and 4 bits -- "Selective quantisation" section of the
-      page on that model's inference prototype) keeps R1 and R3 with q the
-      unsigned code 0..255, four codes per uint32, lowest input column in the
-      lowest byte.
+      affine quantisation with group size 64, with which an encoder's linear
+      layers are quantised at 8 and 4 bits in "Engineering investigation: can
+      this MLX port be 10x faster?", section "Selective quantisation") keeps
+      R1 and R3 with q the unsigned code 0..255, four codes per uint32,
+      lowest input column in the lowest byte;
+  R11 the FP8 E4M3 variant (the news item on the lithos-metal pull requests
+      names an "FP8 E4M3 decode" that handles two codes per half2; it gives
+      nothing else) stores each weight's code as one FP8 E4M3 byte, laid out
+      as in R10, and keeps the group scale and bias: w = s*v(q) + b with v(q)
+      the value of the byte in the E4M3 format of "FP8 Formats for Deep
+      Learning" (Micikevicius et al., 2022): sign bit, 4 exponent bits with
+      bias 7, 3 mantissa bits, subnormals at exponent field 0, no infinities,
+      and NaN only at exponent and mantissa fields all ones.
 
 Everything is float64; the only rounding to bf16 is the final output (and it
 goes float64 -> float32 -> bf16, a double rounding that is far below any
@@ -85,10 +93,33 @@ def unpack_codes(words: np.ndarray, bits: int = 4) -> np.ndarray:
     return c.reshape(w.shape[:-1] + (w.shape[-1] * per,)).astype(np.uint8)
 
 
-def dequant(codes: np.ndarray, scales: np.ndarray, biases: np.ndarray, bits: int = 4) -> np.ndarray:
+CODES_UINT = 0      # layer code_format: unsigned integer codes
+CODES_E4M3 = 1      # layer code_format: FP8 E4M3 codes (R11)
+
+
+def e4m3_value(q) -> np.ndarray:
+    """FP8 E4M3 bytes -> float64 (R11).  Fields: sign S = bit 7, exponent
+    field e = bits 6..3, mantissa field m = bits 2..0.  e = 0: (-1)^S m/8 2^-6
+    (subnormal; m = 0 is a signed zero); otherwise (-1)^S (1 + m/8) 2^(e-7);
+    e = 15 with m = 7 is NaN.  The largest finite magnitude is 1.75 * 2^8 = 448."""
+    q = np.asarray(q, dtype=np.uint8).astype(np.int64)
+    sign = np.where(q & 0x80, -1.0, 1.0)
+    e = (q >> 3) & 0xF
+    m = (q & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    return np.where((e == 15) & (q & 0x7 == 7), np.nan, sign * mag)
+
+
+def dequant(codes: np.ndarray, scales: np.ndarray, biases: np.ndarray, bits: int = 4,
+            fmt: int = CODES_UINT) -> np.ndarray:
     """Reconstruct a [rows][cols] matrix in float64: w[r, c] = s[r, c//64] * q[r, c]
-    + b[r, c//64] (R1, R3; R10 for 8-bit codes)."""
-    q = unpack_codes(codes, bits).astype(np.float64)
+    + b[r, c//64] (R1, R3; R10 for 8-bit codes), with q replaced by the E4M3
+    value of the code for FP8 codes (R11)."""
+    if fmt == CODES_E4M3:
+        assert bits == 8
+        q = e4m3_value(unpack_codes(codes, 8))
+    else:
+        q = unpack_codes(codes, bits).astype(np.float64)
     s = np.repeat(bf16_to_f64(scales), GROUP, axis=-1)
     b = np.repeat(bf16_to_f64(biases), GROUP, axis=-1)
     assert q.shape == s.shape == b.shape, (q.shape, s.shape)
@@ -201,10 +232,10 @@ def expert_ffn(xr: np.ndarray, wg: np.ndarray, wu: np.ndarray, wd: np.ndarray) -
     return h @ wd.T
 
 
-def _mat(m, e=None, bits=4):
+def _mat(m, e=None, bits=4, fmt=CODES_UINT):
     if e is None:
-        return dequant(m.codes, m.scales, m.biases, bits)
-    return dequant(m.codes[e], m.scales[e], m.biases[e], bits)
+        return dequant(m.codes, m.scales, m.biases, bits, fmt)
+    return dequant(m.codes[e], m.scales[e], m.biases[e], bits, fmt)
 
 
 def moe_layer(layer, x_bits: np.ndarray, tokens: Optional[np.ndarray] = None):
@@ -212,22 +243,24 @@ def moe_layer(layer, x_bits: np.ndarray, tokens: Optional[np.ndarray] = None):
 
     `layer` carries H, E, I, top_k, router_w, router_bias, shared_gate, the
     six quantised matrices (attributes codes/scales/biases) gate, up, down,
-    sh_gate, sh_up, sh_down and, optionally, code_bits (4 when absent).  Returns a dict with out (float64), out_bf16 (bits) and the
-    routing / grouping intermediates of the selected rows.
+    sh_gate, sh_up, sh_down and, optionally, code_bits (4 when absent) and
+    code_format (CODES_UINT when absent).  Returns a dict with out (float64),
+    out_bf16 (bits) and the routing / grouping intermediates of the selected
+    rows.
     """
     x_all = bf16_to_f64(x_bits)
     rows = np.arange(x_all.shape[0]) if tokens is None else np.asarray(tokens)
     x = x_all[rows]
     k = layer.top_k
-    bits = getattr(layer, "code_bits", 4)
+    f = (getattr(layer, "code_bits", 4), getattr(layer, "code_format", CODES_UINT))
     idx, w, gamma, scores = route(x, layer.router_w, layer.router_bias, layer.shared_gate, k)
     out = np.zeros_like(x)
     for e in np.unique(idx):
         sel_t, sel_j = np.nonzero(idx == e)
-        y = expert_ffn(x[sel_t], _mat(layer.gate, e, bits), _mat(layer.up, e, bits), _mat(layer.down, e, bits))
+        y = expert_ffn(x[sel_t], _mat(layer.gate, e, *f), _mat(layer.up, e, *f), _mat(layer.down, e, *f))
         out[sel_t] += w[sel_t, sel_j][:, None] * y
-    y_sh = expert_ffn(x, _mat(layer.sh_gate, None, bits), _mat(layer.sh_up, None, bits),
-                      _mat(layer.sh_down, None, bits))
+    y_sh = expert_ffn(x, _mat(layer.sh_gate, None, *f), _mat(layer.sh_up, None, *f),
+                      _mat(layer.sh_down, None, *f))
     out += gamma[:, None] * y_sh
     res = dict(out=out, out_bf16=f64_to_bf16(out), idx=idx, w=w, gamma=gamma, scores=scores)
     if tokens is None:

@@ -105,6 +105,93 @@ def check_formats_agree():
     assert np.array_equal(O.unpack_codes(w8, 8), q.astype(np.uint8))
 
 
+def check_e4m3_golden():
+    """FP8 E4M3 code values worked by hand from the format's fields."""
+    n = 0
+    for ln in _lines("e4m3_cases.txt"):
+        code, val = ln.split()
+        got = O.e4m3_value(np.array([int(code, 16)], np.uint8))[0]
+        if val == "nan":
+            assert np.isnan(got), code
+        else:
+            want = float(val)
+            assert got == want and np.signbit(got) == np.signbit(want), (code, got, want)
+        n += 1
+    assert n == 21
+
+
+def check_e4m3_library():
+    """All 256 E4M3 codes against an independent implementation of the same
+    format: PyTorch's float8_e4m3fn type (bytes viewed as that type, widened)."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    codes = np.arange(256, dtype=np.uint8)
+    lib = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_value(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(lib))
+    ok = ~np.isnan(lib)
+    assert np.array_equal(got[ok], lib[ok]) and np.array_equal(np.signbit(got[ok]), np.signbit(lib[ok]))
+
+
+def check_e4m3_monotone():
+    """Invariant of the format: codes 0x00..0x7E are the non-negative finite
+    values in strictly increasing order, and the sign bit only negates."""
+    v = O.e4m3_value(np.arange(0x7F, dtype=np.uint8))
+    assert np.all(np.diff(v) > 0) and v[0] == 0.0 and v[-1] == 448.0
+    neg = O.e4m3_value(np.arange(0x80, 0xFF, dtype=np.uint8))
+    assert np.array_equal(neg, -v)
+
+
+def check_dequant_e4m3_golden():
+    """w = s*v(q) + b for hand-worked words of four E4M3 codes, lowest byte first."""
+    n = 0
+    for ln in _lines("dequant_e4m3_cases.txt"):
+        tok = ln.split()
+        word = np.array([[int(tok[0], 16)] * 16], dtype=np.uint32)     # one row, 64 columns
+        s = bf(np.array([[float(tok[1])]], np.float32))
+        b = bf(np.array([[float(tok[2])]], np.float32))
+        want = np.array([float(v) for v in tok[3:7]])
+        got = O.dequant(word, s, b, bits=8, fmt=O.CODES_E4M3)
+        assert got.shape == (1, 64)
+        assert np.array_equal(got[0, :4], want), (tok[0], got[0, :4], want)
+        assert np.array_equal(got[0, 60:64], want)
+        n += 1
+    assert n == 4
+
+
+def check_e4m3_layer_integers():
+    """A layer whose codes are the E4M3 encodings of integers 0..15 (encoded by
+    PyTorch's float8_e4m3fn, exact for these integers) computes the same output
+    as the unsigned 8-bit layer with those integers as codes: the format only
+    changes how a code is read."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    L, x = S.draw_config("w8_tiny_T4")
+    lut = torch.arange(256, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy().astype(np.uint32)
+
+    def small_ints(m):
+        q = O.unpack_codes(m.codes, 8) & 15                         # integer codes 0..15
+        w_int = np.zeros(m.codes.shape, np.uint32)
+        w_fp8 = np.zeros(m.codes.shape, np.uint32)
+        for i in range(4):
+            w_int |= q[..., i::4].astype(np.uint32) << np.uint32(8 * i)
+            w_fp8 |= lut[q[..., i::4]] << np.uint32(8 * i)
+        return S.W4Matrix(w_int, m.scales, m.biases), S.W4Matrix(w_fp8, m.scales, m.biases)
+
+    names = ("gate", "up", "down", "sh_gate", "sh_up", "sh_down")
+    pairs = {n: small_ints(getattr(L, n)) for n in names}
+    import dataclasses
+    Li = dataclasses.replace(L, **{n: pairs[n][0] for n in names})
+    Lf = dataclasses.replace(L, code_format=S.CODES_E4M3, **{n: pairs[n][1] for n in names})
+    ri, rf = O.moe_layer(Li, x), O.moe_layer(Lf, x)
+    assert np.array_equal(ri["out"], rf["out"])
+    # and the format is really read: the same words read as unsigned bytes differ
+    Lu = dataclasses.replace(Lf, code_format=S.CODES_UINT)
+    assert not np.allclose(O.moe_layer(Lu, x)["out"], rf["out"])
+
+
 def check_format_size():
     """Section "Dequantise weights during matrix multiplication": a 35B-parameter
     model shrinks from about 70 GB of bf16 to a 19.4 GB checkpoint.  One bf16
@@ -342,7 +429,8 @@ def check_row_independence():
 
 
 PINS = [check_dequant_golden, check_group_axis, check_dequant8_golden, check_dequant8_group_axis,
-        check_formats_agree, check_format_size, check_router_golden,
+        check_formats_agree, check_e4m3_golden, check_e4m3_library, check_e4m3_monotone,
+        check_dequant_e4m3_golden, check_e4m3_layer_integers, check_format_size, check_router_golden,
         check_router_invariants, check_group_golden, check_group_invariants, check_silu,
         check_structured_ffn, check_layer_golden, check_identical_experts, check_dense_gating,
         check_brute_force_tiny, check_row_independence]
@@ -398,18 +486,39 @@ def _reversed_bytes(words, bits=4):
     return c.reshape(w.shape[:-1] + (w.shape[-1] * 4,)).astype(np.uint8)
 
 
-def _swapped_affine(codes, scales, biases, bits=4):
+def _swapped_affine(codes, scales, biases, bits=4, fmt=0):
     q = O.unpack_codes(codes, bits).astype(np.float64)
     s = np.repeat(O.bf16_to_f64(scales), 64, axis=-1)
     b = np.repeat(O.bf16_to_f64(biases), 64, axis=-1)
     return b * q + s
 
 
-def _groups_down_rows(codes, scales, biases, bits=4):
+def _groups_down_rows(codes, scales, biases, bits=4, fmt=0):
     q = O.unpack_codes(codes, bits).astype(np.float64)
     s = np.repeat(np.swapaxes(O.bf16_to_f64(scales), -1, -2), 64, axis=-1)   # group index on the wrong axis
     b = np.repeat(np.swapaxes(O.bf16_to_f64(biases), -1, -2), 64, axis=-1)
     return s * q + b
+
+
+_E4M3 = O.e4m3_value
+
+
+def _e4m3_bias_8(q):
+    """E4M3 read with exponent bias 8 (the E5M2-style bias mistake)."""
+    return _E4M3(q) / 2.0
+
+
+def _e4m3_no_subnormals(q):
+    """E4M3 with the implicit leading one also at exponent field 0."""
+    v = _E4M3(q)
+    qq = np.asarray(q, np.uint8).astype(np.int64)
+    sub = ((qq >> 3) & 0xF) == 0
+    return np.where(sub, np.where(qq & 0x80, -1.0, 1.0) * (1.0 + (qq & 7) / 8.0) * 2.0 ** -7, v)
+
+
+def _e4m3_unsigned(q):
+    """E4M3 with the sign bit ignored."""
+    return np.abs(_E4M3(q))
 
 
 def _unrenormalised_route(x, W, bias, g, k):
@@ -454,6 +563,9 @@ _UNPACK = O.unpack_codes
 MUTANTS = [
     ("unpack_codes", _reversed_nibbles),
     ("unpack_codes", _reversed_bytes),
+    ("e4m3_value", _e4m3_bias_8),
+    ("e4m3_value", _e4m3_no_subnormals),
+    ("e4m3_value", _e4m3_unsigned),
     ("dequant", _swapped_affine),
     ("dequant", _groups_down_rows),
     ("route", _unrenormalised_route),
