@@ -36,6 +36,7 @@ PREFILL_KERNELS = ["router_scores", "topk", "chunk_count", "scan", "assign", "ga
 DECODE_KERNELS = ["decode_router", "decode_gate_up", "decode_down"]   # the three-kernel path
 DECODE_FUSED = ["decode_fused"]
 SMALL_T = (4, 8)   # multi-row decode batches measured beside the step
+W8_REPLICAS = 8    # distinct 8-bit layers the 8-bit decode measurement cycles
 
 
 def parse():
@@ -49,9 +50,13 @@ def parse():
                     help="step: the timed benchmark; prefill_chunk / decode: run --calls plain library calls on "
                          "one layer of the workload and exit (for profilers)")
     ap.add_argument("--calls", type=int, default=2)
+    ap.add_argument("--bits", type=int, choices=[4, 8], default=4,
+                    help="code width of the layer a --case run uses")
     ap.add_argument("--no-multirow", action="store_true",
                     help="skip the multi-row decode measurement (for launch lists that should hold the step's "
                          "kernels only)")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the 8-bit weight-format measurement (for launch lists of the step's kernels only)")
     return ap.parse_args()
 
 
@@ -63,14 +68,15 @@ def run_case(args):
     c = S.CONFIGS[WORKLOAD]
     T = c["chunk"] if args.case == "prefill_chunk" else 1
     L0, x = S.draw_config(WORKLOAD, T=T)
-    dl = mw.DeviceLayer(L0)
     xd = mw.tokens_to_device(x)
+    dl = mw.DeviceLayer(L0 if args.bits == 4 else
+                        S.draw_layer_torch(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], seed=2000, bits=8))
     for _ in range(args.calls):
         (mw.forward_prefill if args.case == "prefill_chunk" else mw.forward_decode)(dl, xd)
     torch.cuda.synchronize()
     if dl.status() != 0:
         raise RuntimeError(f"device status {dl.status()}")
-    print(json.dumps({"case": args.case, "calls": args.calls, "T": T, "ok": True}))
+    print(json.dumps({"case": args.case, "bits": args.bits, "calls": args.calls, "T": T, "ok": True}))
 
 
 # ---------------------------------------------------------------------------
@@ -325,6 +331,35 @@ def run_gpu(args, rank, local_rank, world, dist):
     if len(k_dec) == 1:                     # batch-1 decode of this shape is one fused kernel
         k_dec = {DECODE_FUSED[0]: next(iter(k_dec.values()))}
 
+    # 8-bit affine g64 weight-format variant: layers of the same shape with 8-bit
+    # codes (four per word); a 4096-row prefill chunk and batch-1 decode calls
+    # cycling W8_REPLICAS distinct layers (6.8 GB, far above L2)
+    w8 = None
+    if not args.no_variants:
+        l8 = [mw.DeviceLayer(S.draw_layer_torch(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], seed=2000 + r,
+                                                device=device, bits=8), device) for r in range(W8_REPLICAS)]
+        ws8 = l8[0].workspace(chunk)
+
+        def pre8():
+            mw.forward_prefill(l8[0], xc, out=out[:chunk], ws=ws8)
+
+        def dec8():
+            for i in range(n_small):
+                mw._check(mw.moe_w4_forward_decode(ctypes.byref(l8[i % W8_REPLICAS].c), 1, xdec[i:i + 1].data_ptr(),
+                                                   outdec[i:i + 1].data_ptr(), ws8.data_ptr(), ws8.numel(),
+                                                   torch.cuda.current_stream().cuda_stream), "decode w8")
+        with torch.cuda.stream(stream):
+            pre8()
+            dec8()
+        torch.cuda.synchronize()
+        if l8[0].status() != 0:
+            raise RuntimeError(f"device status {l8[0].status()} (8-bit layer)")
+        t8_pre = timed(capture(pre8), args.steps) / args.steps
+        t8_dec = timed(capture(dec8), args.steps) / args.steps / n_small
+        k8_pre = traced(pre8, PREFILL_KERNELS)
+        w8 = dict(t_pre=t8_pre, t_dec=t8_dec, k_pre=k8_pre)
+        del l8, ws8
+
     # end to end through host buffers: copy in, run, copy out, every step
     x_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
     x_host.copy_(x.cpu())
@@ -354,15 +389,16 @@ def run_gpu(args, rank, local_rank, world, dist):
     if status != 0:
         raise RuntimeError(f"device status {status}")
     return dict(c=c, L0=L0, x_np=x_np, xdec_np=xdec_np, t_step=t_step, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e, small=small,
-                clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device))
+                w8=w8, clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device))
 
 
 # ---------------------------------------------------------------------------
 # algorithmic work (per unit) for the roofline
 # ---------------------------------------------------------------------------
-def expert_bytes(H, I):
+def expert_bytes(H, I, bits=4):
+    """Packed codes plus a bf16 scale and bias per 64 weights, for gate, up and down."""
     w = 3 * H * I
-    return w // 2 + 2 * 2 * (w // 64)
+    return w * bits // 8 + 2 * 2 * (w // 64)
 
 
 def decode_bytes_rows(c, T, distinct):
@@ -372,17 +408,35 @@ def decode_bytes_rows(c, T, distinct):
     return (distinct + 1) * expert_bytes(H, I) + H * E * 4 + H * 4 + T * H * 2 + T * H * 2
 
 
-def decode_bytes(c, T=1):
+def decode_bytes(c, T=1, bits=4):
     """Bytes one decode call must move: k+1 experts' packed weights, router
     weights, shared gate, x and out."""
     H, E, I, k = c["H"], c["E"], c["I"], c["top_k"]
-    return (k + 1) * expert_bytes(H, I) + H * E * 4 + H * 4 + T * H * 2 + T * H * 2
+    return (k + 1) * expert_bytes(H, I, bits) + H * E * 4 + H * 4 + T * H * 2 + T * H * 2
 
 
 def gemm_flops(c, T, which):
     H, I, k = c["H"], c["I"], c["top_k"]
     rows = T * k + T
     return 2 * rows * H * 2 * I if which == "gate_up" else 2 * rows * I * H
+
+
+def w8_summary(c, w, chunk, world, pk):
+    """The 8-bit affine g64 layer: prefill chunk against the tensor peak, its
+    two GEMMs, and batch-1 decode against HBM."""
+    fl = {n: gemm_flops(c, chunk, n) for n in ("gate_up", "down")}
+    tf = (fl["gate_up"] + fl["down"]) / w["t_pre"] / 1e12
+    b = decode_bytes(c, 1, bits=8)
+    gk = {n: w["k_pre"].get(f"gemm_{n}") for n in fl}
+    return {"layer": "same shape as the step's layer, 8-bit codes, 8 distinct layers for decode",
+            "prefill": {"ms_per_4096_chunk": 1e3 * w["t_pre"], "tok_s": job_value(chunk, world, w["t_pre"]),
+                        "tensor_tflops": tf, "frac_of_peak": tf / pk["bf16_tflops_sustained"],
+                        "gemm_us": {n: 1e6 * t for n, t in gk.items() if t},
+                        "gemm_frac_of_peak": {n: fl[n] / t / 1e12 / pk["bf16_tflops_sustained"]
+                                              for n, t in gk.items() if t}},
+            "decode_T1": {"us_per_call": 1e6 * w["t_dec"], "bytes_per_call": b, "hbm_gbs": b / w["t_dec"] / 1e9,
+                          "frac_of_hbm": b / w["t_dec"] / 1e9 / pk["hbm_gbs"],
+                          "path": "grouped tensor-core path (the one-kernel decode takes 4-bit codes only)"}}
 
 
 # ---------------------------------------------------------------------------
@@ -507,6 +561,7 @@ def main():
                                            "frac_of_hbm": decode_bytes_rows(c, Tm, dx) / t / 1e9 / pk["hbm_gbs"],
                                            "path": "grouped tensor-core path (one read per selected expert)"}
                                 for Tm, (t, dx) in r["small"].items()},
+            "variant_w8": None if r["w8"] is None else w8_summary(c, r["w8"], chunk, world, pk),
             "roofline": roof,
             "kernels_us": {"prefill_4096": {k: 1e6 * v for k, v in r["k_pre"].items()},
                            "decode_T1": {k: 1e6 * v for k, v in r["k_dec"].items()}},
