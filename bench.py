@@ -36,7 +36,10 @@ PREFILL_KERNELS = ["router_scores", "topk", "chunk_count", "scan", "assign", "ga
 DECODE_KERNELS = ["decode_router", "decode_gate_up", "decode_down"]   # the three-kernel path
 DECODE_FUSED = ["decode_fused"]
 SMALL_T = (4, 8)   # multi-row decode batches measured beside the step
-W8_REPLICAS = 8    # distinct 8-bit layers the 8-bit decode measurement cycles
+W8_REPLICAS = 8    # distinct one-byte-code layers each format-variant decode measurement cycles
+# weight codes: (bits, code_format) -- unsigned 4-bit, unsigned 8-bit, FP8 E4M3
+CODES = {"u4": (4, 0), "u8": (8, 0), "e4m3": (8, 1)}
+VARIANTS = ("u8", "e4m3")   # format variants measured beside the step
 
 
 def parse():
@@ -50,8 +53,8 @@ def parse():
                     help="step: the timed benchmark; prefill_chunk / decode: run --calls plain library calls on "
                          "one layer of the workload and exit (for profilers)")
     ap.add_argument("--calls", type=int, default=2)
-    ap.add_argument("--bits", type=int, choices=[4, 8], default=4,
-                    help="code width of the layer a --case run uses")
+    ap.add_argument("--codes", choices=list(CODES), default="u4",
+                    help="weight codes of the layer a --case run uses")
     ap.add_argument("--no-multirow", action="store_true",
                     help="skip the multi-row decode measurement (for launch lists that should hold the step's "
                          "kernels only)")
@@ -69,14 +72,16 @@ def run_case(args):
     T = c["chunk"] if args.case == "prefill_chunk" else 1
     L0, x = S.draw_config(WORKLOAD, T=T)
     xd = mw.tokens_to_device(x)
-    dl = mw.DeviceLayer(L0 if args.bits == 4 else
-                        S.draw_layer_torch(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], seed=2000, bits=8))
+    bits, fmt = CODES[args.codes]
+    dl = mw.DeviceLayer(L0 if args.codes == "u4" else
+                        S.draw_layer_torch(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], seed=2000, bits=bits,
+                                           fmt=fmt))
     for _ in range(args.calls):
         (mw.forward_prefill if args.case == "prefill_chunk" else mw.forward_decode)(dl, xd)
     torch.cuda.synchronize()
     if dl.status() != 0:
         raise RuntimeError(f"device status {dl.status()}")
-    print(json.dumps({"case": args.case, "bits": args.bits, "calls": args.calls, "T": T, "ok": True}))
+    print(json.dumps({"case": args.case, "codes": args.codes, "calls": args.calls, "T": T, "ok": True}))
 
 
 # ---------------------------------------------------------------------------
@@ -331,13 +336,15 @@ def run_gpu(args, rank, local_rank, world, dist):
     if len(k_dec) == 1:                     # batch-1 decode of this shape is one fused kernel
         k_dec = {DECODE_FUSED[0]: next(iter(k_dec.values()))}
 
-    # 8-bit affine g64 weight-format variant: layers of the same shape with 8-bit
-    # codes (four per word); a 4096-row prefill chunk and batch-1 decode calls
-    # cycling W8_REPLICAS distinct layers (6.8 GB, far above L2)
-    w8 = None
-    if not args.no_variants:
+    # weight-format variants (8-bit affine codes, FP8 E4M3 codes): layers of the
+    # same shape with one-byte codes; a 4096-row prefill chunk and batch-1
+    # decode calls cycling W8_REPLICAS distinct layers (6.8 GB, far above L2)
+    variants = {}
+    for vname in (() if args.no_variants else VARIANTS):
+        bits, fmt = CODES[vname]
         l8 = [mw.DeviceLayer(S.draw_layer_torch(c["H"], c["E"], c["I"], c["top_k"], c["zipf"], seed=2000 + r,
-                                                device=device, bits=8), device) for r in range(W8_REPLICAS)]
+                                                device=device, bits=bits, fmt=fmt), device)
+              for r in range(W8_REPLICAS)]
         ws8 = l8[0].workspace(chunk)
 
         def pre8():
@@ -347,17 +354,17 @@ def run_gpu(args, rank, local_rank, world, dist):
             for i in range(n_small):
                 mw._check(mw.moe_w4_forward_decode(ctypes.byref(l8[i % W8_REPLICAS].c), 1, xdec[i:i + 1].data_ptr(),
                                                    outdec[i:i + 1].data_ptr(), ws8.data_ptr(), ws8.numel(),
-                                                   torch.cuda.current_stream().cuda_stream), "decode w8")
+                                                   torch.cuda.current_stream().cuda_stream), "decode " + vname)
         with torch.cuda.stream(stream):
             pre8()
             dec8()
         torch.cuda.synchronize()
         if l8[0].status() != 0:
-            raise RuntimeError(f"device status {l8[0].status()} (8-bit layer)")
+            raise RuntimeError(f"device status {l8[0].status()} ({vname} layer)")
         t8_pre = timed(capture(pre8), args.steps) / args.steps
         t8_dec = timed(capture(dec8), args.steps) / args.steps / n_small
         k8_pre = traced(pre8, PREFILL_KERNELS)
-        w8 = dict(t_pre=t8_pre, t_dec=t8_dec, k_pre=k8_pre)
+        variants[vname] = dict(t_pre=t8_pre, t_dec=t8_dec, k_pre=k8_pre, bits=bits)
         del l8, ws8
 
     # end to end through host buffers: copy in, run, copy out, every step
@@ -389,7 +396,7 @@ def run_gpu(args, rank, local_rank, world, dist):
     if status != 0:
         raise RuntimeError(f"device status {status}")
     return dict(c=c, L0=L0, x_np=x_np, xdec_np=xdec_np, t_step=t_step, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e, small=small,
-                w8=w8, clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device))
+                variants=variants, clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device))
 
 
 # ---------------------------------------------------------------------------
@@ -421,14 +428,14 @@ def gemm_flops(c, T, which):
     return 2 * rows * H * 2 * I if which == "gate_up" else 2 * rows * I * H
 
 
-def w8_summary(c, w, chunk, world, pk):
-    """The 8-bit affine g64 layer: prefill chunk against the tensor peak, its
-    two GEMMs, and batch-1 decode against HBM."""
+def variant_summary(c, w, chunk, world, pk):
+    """A one-byte-code layer: prefill chunk against the tensor peak, its two
+    GEMMs, and batch-1 decode against HBM."""
     fl = {n: gemm_flops(c, chunk, n) for n in ("gate_up", "down")}
     tf = (fl["gate_up"] + fl["down"]) / w["t_pre"] / 1e12
-    b = decode_bytes(c, 1, bits=8)
+    b = decode_bytes(c, 1, bits=w["bits"])
     gk = {n: w["k_pre"].get(f"gemm_{n}") for n in fl}
-    return {"layer": "same shape as the step's layer, 8-bit codes, 8 distinct layers for decode",
+    return {"layer": f"same shape as the step's layer, {w['bits']}-bit codes, {W8_REPLICAS} distinct layers for decode",
             "prefill": {"ms_per_4096_chunk": 1e3 * w["t_pre"], "tok_s": job_value(chunk, world, w["t_pre"]),
                         "tensor_tflops": tf, "frac_of_peak": tf / pk["bf16_tflops_sustained"],
                         "gemm_us": {n: 1e6 * t for n, t in gk.items() if t},
@@ -515,7 +522,7 @@ def main():
     if dom[1] in ("gemm_gate_up", "gemm_down"):
         f = gemm_flops(c, chunk, "gate_up" if dom[1] == "gemm_gate_up" else "down")
         ach = f / t_dom / 1e12
-        gk = "grouped_w4_gemm_kernel<1>" if dom[1] == "gemm_gate_up" else "grouped_w4_gemm_kernel<0>"
+        gk = "grouped_w4_gemm_kernel<1, 4, 0>" if dom[1] == "gemm_gate_up" else "grouped_w4_gemm_kernel<0, 4, 0>"
         roof = {"kernel": dom[1], "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": measured_traffic(gk),
                 "work_per_launch": f"{f:.4e} FLOP (fp16 operands, fp32 accumulate)",
@@ -561,7 +568,7 @@ def main():
                                            "frac_of_hbm": decode_bytes_rows(c, Tm, dx) / t / 1e9 / pk["hbm_gbs"],
                                            "path": "grouped tensor-core path (one read per selected expert)"}
                                 for Tm, (t, dx) in r["small"].items()},
-            "variant_w8": None if r["w8"] is None else w8_summary(c, r["w8"], chunk, world, pk),
+            "format_variants": {v: variant_summary(c, w, chunk, world, pk) for v, w in r["variants"].items()},
             "roofline": roof,
             "kernels_us": {"prefill_4096": {k: 1e6 * v for k, v in r["k_pre"].items()},
                            "decode_T1": {k: 1e6 * v for k, v in r["k_dec"].items()}},

@@ -85,6 +85,8 @@ static int check_layer(const moe_w4_layer* L) {
     if (L->H <= 0 || L->I <= 0) return MOE_W4_ERR_INVALID;
     if (L->H % kBM || L->I % kBM || L->H > 4096 || L->I > 4096 || L->E > 1024) return MOE_W4_ERR_UNSUPPORTED;
     if (L->code_bits != 0 && L->code_bits != 4 && L->code_bits != 8) return MOE_W4_ERR_UNSUPPORTED;
+    if (L->code_format != MOE_W4_CODES_UINT && L->code_format != MOE_W4_CODES_E4M3) return MOE_W4_ERR_UNSUPPORTED;
+    if (L->code_format == MOE_W4_CODES_E4M3 && L->code_bits != 8) return MOE_W4_ERR_UNSUPPORTED;
     if (!L->router_w || !L->shared_gate) return MOE_W4_ERR_INVALID;
     if (!aligned16(L->router_w) || !aligned16(L->shared_gate) || (L->router_bias && !aligned16(L->router_bias)))
         return MOE_W4_ERR_ALIGN;

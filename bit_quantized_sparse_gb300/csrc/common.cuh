@@ -347,9 +347,6 @@ MW4_DEV int chunk_pos_of_col(int j) { return ((j & 3) << 1) | (j >> 2); }   // i
 // so columns {0,2,1,3,4,6,5,7} sit at positions 0..7; position of column j.
 MW4_DEV int chunk8_pos_of_col(int j) { return (j & 4) | ((j & 1) << 1) | ((j >> 1) & 1); }
 
-// w = s*q + b for eight codes in chunk order; s2 = (s, s), s16 = (s/16, s/16),
-// b2 = (b, b).  q (or 16 q) is recovered exactly and the product and sum are
-// exact inside the fused multiply-add: each weight is rounded to fp16 once.
 // w = s*q + b for the four 8-bit codes of one word (lowest byte first): the fp16
 // pairs (c0, c2) and (c1, c3).  1024 + q is exact in fp16 for q <= 255; each
 // weight is rounded to fp16 once, in the fused multiply-add.
@@ -362,6 +359,25 @@ MW4_DEV void dequant4x8_f16(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[2]
     o[1] = h2_as_u32(__hfma2(s2, __hsub2(u32_as_h2(p1), k1024), b2));
 }
 
+// w = s*v + b for the four FP8 E4M3 codes of one word (lowest byte first), in
+// the pair order of dequant4x8_f16: (c0, c2) and (c1, c3).  A byte permute
+// puts c0, c2 in the low half-word and c1, c3 in the high one; each half-word
+// converts to an fp16 pair (its upper byte to the upper half).  Every E4M3
+// value is exact in fp16, so each weight is rounded to fp16 once, in the fused
+// multiply-add.
+MW4_DEV void dequant_e4m3x4_f16(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[2]) {
+    const uint32_t p = __byte_perm(w, 0u, 0x3120u);   // bytes c0, c2, c1, c3 (low to high)
+    uint32_t v0, v1;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(v0), "=r"(v1) : "r"(p));
+    o[0] = h2_as_u32(__hfma2(s2, u32_as_h2(v0), b2));
+    o[1] = h2_as_u32(__hfma2(s2, u32_as_h2(v1), b2));
+}
+
+// w = s*q + b for eight codes in chunk order; s2 = (s, s), s16 = (s/16, s/16),
+// b2 = (b, b).  q (or 16 q) is recovered exactly and the product and sum are
+// exact inside the fused multiply-add: each weight is rounded to fp16 once.
 MW4_DEV void dequant8_f16(uint32_t w, __half2 s2, __half2 s16, __half2 b2, uint32_t (&o)[4]) {
     const uint32_t magic = 0x64006400u;
     const uint32_t w8 = w >> 8;
@@ -382,7 +398,6 @@ MW4_DEV float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 MW4_DEV float sigmoid_f(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
 
-// Warp top-k with NV scores per lane kept in registers (E <= 32 NV).
 // ---------------------------------------------------------------------------
 // warp-level selection (router)
 // ---------------------------------------------------------------------------

@@ -164,12 +164,14 @@ MW4_DEV TileInfo tile_from(const GemmArgs& a, int4 bi, int m) {
 }
 MW4_DEV TileInfo block_info(const GemmArgs& a, int rb, int m) { return tile_from(a, __ldg(a.blkinfo + rb), m); }
 
-template <bool DUAL, int BITS>
+// E4M3: the 8-bit codes are FP8 E4M3 values instead of unsigned integers.
+template <bool DUAL, int BITS, bool E4M3>
 __global__ void __launch_bounds__(Geo<DUAL, BITS>::kThreads, 1)
 grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap map0r,
                        const __grid_constant__ CUtensorMap map1r, const __grid_constant__ CUtensorMap map0s,
                        const __grid_constant__ CUtensorMap map1s, const __grid_constant__ CUtensorMap mapb,
                        const __grid_constant__ CUtensorMap mapbs) {
+    static_assert(!E4M3 || BITS == 8, "E4M3 codes are one byte each");
     using GG = Geo<DUAL, BITS>;
     constexpr uint32_t kCodesBytes = GG::kCodesBytes;
     constexpr int kCodeWords = kGK * BITS / 32;   // code words per row per step
@@ -420,7 +422,10 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
 #pragma unroll
                                     for (int wi = 0; wi < 4; ++wi) {
                                         uint32_t q2[2];
-                                        dequant4x8_f16(words[wi], s2, b2, q2);
+                                        if (E4M3)
+                                            dequant_e4m3x4_f16(words[wi], s2, b2, q2);
+                                        else
+                                            dequant4x8_f16(words[wi], s2, b2, q2);
                                         o[8 * hh2 + 2 * wi] = q2[0];
                                         o[8 * hh2 + 2 * wi + 1] = q2[1];
                                     }
@@ -608,7 +613,7 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const
 
 // One grouped GEMM launch (the shared-memory size is raised once per device
 // and instance).
-template <bool DUAL, int BITS>
+template <bool DUAL, int BITS, bool E4M3>
 static cudaError_t launch_gemm(const GemmArgs& g, int grid, const CUtensorMap& m0r, const CUtensorMap& m1r,
                                const CUtensorMap& m0s, const CUtensorMap& m1s, const CUtensorMap& mb,
                                const CUtensorMap& mbs, cudaStream_t st) {
@@ -618,18 +623,20 @@ static cudaError_t launch_gemm(const GemmArgs& g, int grid, const CUtensorMap& m
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!set[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(grouped_w4_gemm_kernel<DUAL, BITS>,
+        const cudaError_t e = cudaFuncSetAttribute(grouped_w4_gemm_kernel<DUAL, BITS, E4M3>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GG::bytes());
         if (e != cudaSuccess) return e;
         set[dev] = true;
     }
-    grouped_w4_gemm_kernel<DUAL, BITS><<<grid, GG::kThreads, GG::bytes(), st>>>(g, m0r, m1r, m0s, m1s, mb, mbs);
+    grouped_w4_gemm_kernel<DUAL, BITS, E4M3><<<grid, GG::kThreads, GG::bytes(), st>>>(g, m0r, m1r, m0s, m1s, mb,
+                                                                                     mbs);
     return cudaGetLastError();
 }
 
 cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const PrefillWs& p,
                                cudaStream_t st) {
     const int bits = code_bits_of(L);
+    const bool e4m3 = codes_e4m3(L);   // validated: only with 8-bit codes
     const int H = L.H, I = L.I, E = L.E, k = L.top_k;
     const uint64_t rows_all = (uint64_t)T * k + T;
     CUtensorMap mg, mu, msg, msu, md, msd, mh, mxg, mx;
@@ -677,8 +684,9 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     const int nrg = T * k;
     gather_rows_kernel<<<(unsigned)((nrg + 7) / 8), 256, 0, st>>>(p.x16, p.perm, p.xg, nrg, H, k);
     trace_mark(st, 6);
-    cudaError_t e = bits == 8 ? launch_gemm<true, 8>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
-                              : launch_gemm<true, 4>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st);
+    cudaError_t e = e4m3  ? launch_gemm<true, 8, true>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
+                  : bits == 8 ? launch_gemm<true, 8, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
+                              : launch_gemm<true, 4, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st);
     if (e != cudaSuccess) return e;
     trace_mark(st, 7);
 
@@ -690,8 +698,9 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     b.c0r = L.down.codes; b.c1r = nullptr; b.c0s = L.sh_down.codes; b.c1s = nullptr; b.b_rows = p.hh; b.b_rows_sh = p.hh;
     b.out = p.ys; b.K = I; b.rows_e = H; b.out_cols = H;
     const int grid_dn = p.max_tiles_dn < nsm ? p.max_tiles_dn : nsm;
-    e = bits == 8 ? launch_gemm<false, 8>(b, grid_dn, md, md, msd, msd, mh, mh, st)
-                  : launch_gemm<false, 4>(b, grid_dn, md, md, msd, msd, mh, mh, st);
+    e = e4m3  ? launch_gemm<false, 8, true>(b, grid_dn, md, md, msd, msd, mh, mh, st)
+      : bits == 8 ? launch_gemm<false, 8, false>(b, grid_dn, md, md, msd, msd, mh, mh, st)
+                  : launch_gemm<false, 4, false>(b, grid_dn, md, md, msd, msd, mh, mh, st);
     if (e != cudaSuccess) return e;
     trace_mark(st, 8);
 

@@ -19,12 +19,14 @@ constexpr int kDecodeMaxT = 16;   // largest decode batch
 constexpr int kFusedClustersPerExpert = 4;   // fused T=1 decode: 16 CTAs per expert in clusters of 4
 constexpr int kRouterRowsPerCta = 256;  // H rows per decode-router CTA
 constexpr int kRouterSplit = 2;         // prefill router: partial score arrays (halves of H)
+// Width of one weight code: 4 (also for code_bits = 0) or 8.
+inline int code_bits_of(const moe_w4_layer& L) { return L.code_bits == 8 ? 8 : 4; }
+// FP8 E4M3 codes (one byte each, read as floats) instead of unsigned integers.
+inline bool codes_e4m3(const moe_w4_layer& L) { return L.code_format == MOE_W4_CODES_E4M3; }
+
 // Down projection: one CTA dequantises a 128-row weight tile once and runs it
 // against up to this many 128-row blocks of the same expert, when its whole K
 // (I columns) fits the tensor-memory A ring (kDownReuseMaxI columns).
-// Width of one weight code: 4 (also for code_bits = 0) or 8.
-inline int code_bits_of(const moe_w4_layer& L) { return L.code_bits == 8 ? 8 : 4; }
-
 constexpr int kDownBlocksPerUnit = 4;
 // Word of the control header's pad[] holding the fused T=1 decode's call
 // counter (the tag of its exchanged values); kept across calls.

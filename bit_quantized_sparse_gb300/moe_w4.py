@@ -38,6 +38,8 @@ MOE_W4_ERR_DEVICE = -5
 MOE_W4_ERR_ALIGN = -6
 MOE_W4_ERR_SCRATCH = -7
 # bits of the device status word (include/moe_w4.h)
+MOE_W4_CODES_UINT = 0
+MOE_W4_CODES_E4M3 = 1
 MOE_W4_STATUS_WAIT_TIMEOUT = 1
 MOE_W4_STATUS_BAD_INDEX = 2
 MOE_W4_STATUS_FP16_RANGE = 4
@@ -52,7 +54,8 @@ class MoeW4Layer(ctypes.Structure):
     _fields_ = [("H", c_int), ("E", c_int), ("I", c_int), ("top_k", c_int),
                 ("router_w", c_void_p), ("router_bias", c_void_p), ("shared_gate", c_void_p),
                 ("gate", MoeW4Mat), ("up", MoeW4Mat), ("down", MoeW4Mat),
-                ("sh_gate", MoeW4Mat), ("sh_up", MoeW4Mat), ("sh_down", MoeW4Mat), ("code_bits", c_int)]
+                ("sh_gate", MoeW4Mat), ("sh_up", MoeW4Mat), ("sh_down", MoeW4Mat), ("code_bits", c_int),
+                ("code_format", c_int)]
 
 
 _P = ctypes.POINTER(MoeW4Layer)
@@ -150,6 +153,8 @@ class DeviceLayer:
         self.c.H, self.c.E, self.c.I, self.c.top_k = self.H, self.E, self.I, self.top_k
         self.code_bits = int(getattr(layer, "code_bits", 4))
         self.c.code_bits = self.code_bits
+        self.code_format = int(getattr(layer, "code_format", MOE_W4_CODES_UINT))
+        self.c.code_format = self.code_format
         self.c.router_w = _ptr(self.router_w)
         self.c.router_bias = _ptr(self.router_bias)
         self.c.shared_gate = _ptr(self.shared_gate)

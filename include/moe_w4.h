@@ -75,7 +75,17 @@ typedef struct {
  * s * q + b with q the unsigned code and s, b the bf16 scale and bias of its
  * group of 64 columns.  8-bit layers run the grouped tensor-core path for
  * every batch size (also T = 1) and are not supported by
- * moe_w4_forward_decode_noalloc. */
+ * moe_w4_forward_decode_noalloc.
+ * code_format selects how a code is read (MOE_W4_CODES_*): unsigned integer
+ * codes as above, or FP8 E4M3 codes (code_bits must be 8; same byte layout),
+ * where a weight is s * v(q) + b with v(q) the E4M3 value of the byte: sign
+ * bit 7, exponent field bits 6..3 with bias 7 (field 0: subnormal, m/8 * 2^-6),
+ * mantissa field bits 2..0, no infinities, exponent and mantissa fields all
+ * ones = NaN.  The format variant follows the "FP8 E4M3 decode, two codes per
+ * half2" change listed in "To be verified: lithos-metal adds Apple inference
+ * kernels" (aidaily), section "What was merged within one minute"; the E4M3
+ * encoding is the one of "FP8 Formats for Deep Learning" (2022).  NaN codes
+ * are not checked: they give NaN outputs. */
 typedef struct {
     int H, E, I, top_k;
     const float* router_w;     /* [H][E] fp32                                   */
@@ -87,7 +97,13 @@ typedef struct {
     moe_w4_mat sh_down;        /* shared: [H][I/8] codes, [H][I/64] s, b        */
     int code_bits;             /* 4 (or 0) or 8; with 8 the codes arrays hold
                                   cols/4 words per row instead of cols/8          */
+    int code_format;           /* MOE_W4_CODES_UINT (0) or MOE_W4_CODES_E4M3    */
 } moe_w4_layer;
+
+enum {
+    MOE_W4_CODES_UINT = 0,     /* unsigned integer codes, w = s * q + b         */
+    MOE_W4_CODES_E4M3 = 1      /* FP8 E4M3 codes, w = s * v(q) + b; 8-bit only  */
+};
 
 enum {
     MOE_W4_OK              = 0,

@@ -63,7 +63,8 @@ def test_workspace_size_host_only(mw):
 
 @pytest.mark.parametrize("field,val,code", [
     ("top_k", 0, -1), ("top_k", 9, -1), ("E", 0, -1), ("H", 100, -2), ("I", 192, -2), ("H", 8192, -2),
-    ("E", 2048, -2), ("code_bits", 6, -2), ("code_bits", 16, -2)])
+    ("E", 2048, -2), ("code_bits", 6, -2), ("code_bits", 16, -2), ("code_format", 2, -2),
+    ("code_format", -1, -2), ("code_format", 1, -2)])   # E4M3 codes need code_bits = 8
 def test_bad_shapes_rejected(mw, field, val, code):
     L = _layer(mw)
     setattr(L, field, val)

@@ -216,11 +216,12 @@ def test_other_shapes(mw, torch, H, E, I, k):
     assert dl.status() == 0
 
 
-@pytest.mark.parametrize("name", ["w8_tiny_T4", "w8_T512"])
+@pytest.mark.parametrize("name", ["w8_tiny_T4", "w8_T512", "e4m3_tiny_T4", "e4m3_T512"])
 def test_w8_layer(mw, torch, name):
-    """The 8-bit affine weight-format variant (four codes per word): routing,
-    prefill and decode (1 and 4 rows, both on the grouped path) against the
-    oracle; the allocation-free decode declines it."""
+    """The one-byte weight-format variants (four codes per word; unsigned
+    8-bit affine codes or FP8 E4M3 codes): routing, prefill and decode (1 and 4
+    rows, both on the grouped path) against the oracle; the allocation-free
+    decode declines them."""
     import ctypes
     L, x = S.draw_config(name)
     assert L.code_bits == 8
