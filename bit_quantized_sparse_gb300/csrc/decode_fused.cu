@@ -753,7 +753,7 @@ static bool shape_ok(const moe_w4_layer& L) {
     if (code_bits_of(L) != 4) return false;   // the mma.sync dot engine unpacks nibbles
     if (L.H % 256 || L.I % 256 || L.H > 4096 || L.I > 2048) return false;   // slices of 16 rows; <= 16 row tiles
     if (L.H / 256 > 16) return false;                                         // gate/up box barriers
-    if (L.E < 128 || L.E > 256 || L.E % 32) return false;   // top-k: E/32 warps sort 32 scores each; 2E floats of partials
+    if (L.E < 128 || L.E > 256 || L.E % 32) return false;   // top-k: 8 scores per lane; 2E floats hold the K-split partials
     if (L.top_k + 1 > kMaxSlots) return false;
     if (L.H > 64 * kPE * (L.top_k + 1)) return false;   // <= 64 router rows per CTA (32 per thread)
     const FusedSmem s(L.H, L.E, L.I);

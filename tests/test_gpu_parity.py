@@ -116,6 +116,22 @@ def test_prefill_sampled(mw, torch, name, T):
     assert dl.status() == 0
 
 
+@pytest.mark.parametrize("name", ["w8_T512", "e4m3_T512"])
+def test_byte_codes_prefill_sampled(mw, torch, name):
+    """The one-byte-code layers at the benchmark's chunk size (4096 rows, the
+    size the format-variant measurement times): routing bit-exact, sampled
+    rows against the oracle."""
+    L, x, dl = layer_of(mw, name, 4096)
+    xd = mw.tokens_to_device(x)
+    r = mw.route(dl, xd)
+    torch.cuda.synchronize()
+    check_route(r, L, x)
+    out = to_np_bits(mw.forward_prefill(dl, xd))
+    rows = _sample(x.shape[0], 32, 11)
+    check_out(out[rows], O.moe_layer(L, x, tokens=rows)["out"])
+    assert dl.status() == 0
+
+
 def test_prefill_single_token_and_ragged(mw, torch):
     L, x, dl = layer_of(mw, "prefill_T512")
     for T in (1, 3, 129, 333):
