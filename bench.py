@@ -444,7 +444,7 @@ def variant_summary(c, w, chunk, world, pk):
                                               for n, t in gk.items() if t}},
             "decode_T1": {"us_per_call": 1e6 * w["t_dec"], "bytes_per_call": b, "hbm_gbs": b / w["t_dec"] / 1e9,
                           "frac_of_hbm": b / w["t_dec"] / 1e9 / pk["hbm_gbs"],
-                          "path": "grouped tensor-core path (the one-kernel decode takes 4-bit codes only)"}}
+                          "path": "one-kernel batch-1 decode (decode_fused_kernel, one-byte-code instance)"}}
 
 
 # ---------------------------------------------------------------------------

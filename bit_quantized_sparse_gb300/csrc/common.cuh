@@ -359,18 +359,22 @@ MW4_DEV void dequant4x8_f16(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[2]
     o[1] = h2_as_u32(__hfma2(s2, __hsub2(u32_as_h2(p1), k1024), b2));
 }
 
-// w = s*v + b for the four FP8 E4M3 codes of one word (lowest byte first), in
-// the pair order of dequant4x8_f16: (c0, c2) and (c1, c3).  A byte permute
-// puts c0, c2 in the low half-word and c1, c3 in the high one; each half-word
-// converts to an fp16 pair (its upper byte to the upper half).  Every E4M3
-// value is exact in fp16, so each weight is rounded to fp16 once, in the fused
-// multiply-add.
-MW4_DEV void dequant_e4m3x4_f16(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[2]) {
+// The four FP8 E4M3 codes of one word (lowest byte first) as fp16 pairs in the
+// pair order of dequant4x8_f16: (c0, c2) and (c1, c3).  A byte permute puts c0,
+// c2 in the low half-word and c1, c3 in the high one; each half-word converts
+// to an fp16 pair (its upper byte to the upper half).  Every E4M3 value is
+// exact in fp16.  dequant_e4m3x4_f16 then forms w = s*v + b, each weight
+// rounded to fp16 once, in the fused multiply-add.
+MW4_DEV void e4m3x4_to_f16(uint32_t w, uint32_t& v02, uint32_t& v13) {
     const uint32_t p = __byte_perm(w, 0u, 0x3120u);   // bytes c0, c2, c1, c3 (low to high)
-    uint32_t v0, v1;
     asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
         "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-        : "=r"(v0), "=r"(v1) : "r"(p));
+        : "=r"(v02), "=r"(v13) : "r"(p));
+}
+
+MW4_DEV void dequant_e4m3x4_f16(uint32_t w, __half2 s2, __half2 b2, uint32_t (&o)[2]) {
+    uint32_t v0, v1;
+    e4m3x4_to_f16(w, v0, v1);
     o[0] = h2_as_u32(__hfma2(s2, u32_as_h2(v0), b2));
     o[1] = h2_as_u32(__hfma2(s2, u32_as_h2(v1), b2));
 }

@@ -73,7 +73,7 @@ struct FusedSmem {
     uint32_t gcodes, ucodes, dcodes, gsb, usb, dsb, xperm, xsum, xbs, part, logits, gsum, usum, hperm, hsum,
         hbs, red, misc, total;
     int RG, RD;
-    __host__ __device__ FusedSmem(int H, int E, int I) {
+    __host__ __device__ FusedSmem(int H, int E, int I, int bits) {
         RG = I / kPE;
         RD = H / kPE;
         uint32_t o = 0;
@@ -83,9 +83,9 @@ struct FusedSmem {
             o += bytes;
             return at;
         };
-        gcodes = take(RG * H / 2, 1024);
-        ucodes = take(RG * H / 2, 1024);
-        dcodes = take(RD * I / 2, 1024);
+        gcodes = take(RG * H / 8 * bits, 1024);
+        ucodes = take(RG * H / 8 * bits, 1024);
+        dcodes = take(RD * I / 8 * bits, 1024);
         gsb = take(2 * RG * (H / 64) * 2, 16);   // scales then biases
         usb = take(2 * RG * (H / 64) * 2, 16);
         dsb = take(2 * RD * (I / 64) * 2, 16);
@@ -234,26 +234,76 @@ MW4_DEV void w4_group_mma(const uint8_t* codes, int rows, int r0, int grp, const
     }
 }
 
+// Code formats of the one-kernel decode: unsigned 4-bit, unsigned 8-bit, FP8 E4M3.
+enum : int { kCodeU4 = 0, kCodeU8 = 1, kCodeE4M3 = 2 };
+
+// One warp, one-byte codes: rows [r0, r0+16), one 64-column group = 4 chunks of
+// 16 codes (one 16-byte chunk of 4 words per row, one MMA each); adds the
+// group's dot products of rows r0+g and r0+g+8 to d[0] and d[2].  Lane c takes
+// word c of a chunk: 8-bit codes give fp16 1024 + q for bytes (0, 2) and (1, 3)
+// (one bitwise op per pair, one shift per word), E4M3 codes their exact values;
+// B (`bperm`, 8 bytes per 4-column unit u = chunk * 4 + lane%4) holds the
+// matching activations (x[4u], x[4u+2]), (x[4u+1], x[4u+3]).
+template <bool E4M3>
+MW4_DEV void w8_group_mma(const uint8_t* codes, int rows, int r0, int grp, const uint2* bperm, float (&d)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    constexpr uint32_t M = 0x64006400u;
+    // both rows of the thread share the swizzle phase g; the group's 4 chunks lie
+    // inside one box of 8 chunks
+    const int ch0 = grp * 4;
+    const uint8_t* row0 = codes + (size_t)(ch0 >> 3) * rows * 128 + (r0 + g) * 128 + c * 4;
+    const uint8_t* row1 = row0 + 8 * 128;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const int ch = ch0 + h;
+        const int off = ((ch & 7) ^ g) << 4;
+        const uint32_t wg = *reinterpret_cast<const uint32_t*>(row0 + off);
+        const uint32_t wh = *reinterpret_cast<const uint32_t*>(row1 + off);
+        const uint2 bv = bperm[ch * 4 + c];
+        uint32_t a[4];
+        if (E4M3) {
+            e4m3x4_to_f16(wg, a[0], a[2]);   // (c0, c2), (c1, c3)
+            e4m3x4_to_f16(wh, a[1], a[3]);
+        } else {
+            a[0] = (wg & 0x00FF00FFu) | M;   // bytes 0, 2
+            a[1] = (wh & 0x00FF00FFu) | M;
+            a[2] = ((wg >> 8) & 0x00FF00FFu) | M;   // bytes 1, 3
+            a[3] = ((wh >> 8) & 0x00FF00FFu) | M;
+        }
+        mma_f16_16816(d, a, bv.x, bv.y);
+    }
+}
+
 // Rows r0+g and r0+g+8 dotted with the activation over groups [grp0, grp1):
 // per group w = s*q + b, so the dot is s * (sum of q*value) + b * (sum of
 // values); `bsum` holds per-group sums of the stored B values (for the 1024
 // offset), `tsum` the true sums of the activation.
+// With one-byte codes a TMA box holds 2 groups (128 columns) instead of 4, and
+// `bperm` is read as 8-byte units.
+template <int CODE>
 MW4_DEV bool w4_gemv16(const uint8_t* codes, int rows, int r0, int grp0, int grp1, const uint4* bperm,
                        const float* bsum, const float* tsum, const uint16_t* sc, const uint16_t* bi, int ngrp_row,
                        float& acc0, float& acc1, uint64_t* box_bars, volatile int* abort_flag, unsigned int* status) {
     const int lane = threadIdx.x & 31, g = lane >> 2;
     constexpr int kIn = 4;   // groups in flight: independent MMA chains
+    constexpr int kGpb = CODE == kCodeU4 ? 4 : 2;   // groups per TMA box
     for (int grp = grp0; grp < grp1; grp += kIn) {
-        if (box_bars) {   // 4 groups (256 columns) per TMA box
+        if (box_bars) {
             for (int q = 0; q < kIn; ++q)
-                if (grp + q < grp1 && ((grp + q) & 3) == 0 || (q == 0 && grp + q < grp1))
-                    if (!mbar_wait(&box_bars[(grp + q) >> 2], 0, abort_flag, status)) return false;
+                if (grp + q < grp1 && ((grp + q) % kGpb) == 0 || (q == 0 && grp + q < grp1))
+                    if (!mbar_wait(&box_bars[(grp + q) / kGpb], 0, abort_flag, status)) return false;
         }
         float d[kIn][4];
 #pragma unroll
         for (int q = 0; q < kIn; ++q) {
             d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
-            if (grp + q < grp1) w4_group_mma(codes, rows, r0, grp + q, bperm, d[q]);
+            if (grp + q < grp1) {
+                if (CODE == kCodeU4)
+                    w4_group_mma(codes, rows, r0, grp + q, bperm, d[q]);
+                else
+                    w8_group_mma<CODE == kCodeE4M3>(codes, rows, r0, grp + q, reinterpret_cast<const uint2*>(bperm),
+                                                    d[q]);
+            }
         }
         // every lane of a row group holds the same column sums (B is the same for all n)
 #pragma unroll
@@ -276,14 +326,15 @@ MW4_DEV bool w4_gemv16(const uint8_t* codes, int rows, int r0, int grp0, int grp
 // GEMVs' shared-memory address arithmetic into constants: measured 1.6x faster
 // for the dot-product loops than the same code with run-time strides.  The
 // instance with all four zero takes every shape from the arguments.
-template <int kH, int kI, int kE, int kK>
+template <int kH, int kI, int kE, int kK, int CODE>
 __global__ void __launch_bounds__(kFThreads, 1)
 decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__ CUtensorMap mg,
                     const __grid_constant__ CUtensorMap mu, const __grid_constant__ CUtensorMap md,
                     const __grid_constant__ CUtensorMap msg, const __grid_constant__ CUtensorMap msu,
                     const __grid_constant__ CUtensorMap msd) {
     const int H = kH ? kH : a.H, E = kE ? kE : a.E, I = kI ? kI : a.I, k = kK ? kK : a.k;
-    const FusedSmem L(H, E, I);
+    constexpr int kBits = CODE == kCodeU4 ? 4 : 8;
+    const FusedSmem L(H, E, I, kBits);
     const int RG = L.RG, RD = L.RD;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -305,7 +356,8 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     float* hbs = reinterpret_cast<float*>(sm + L.hbs);
     float* red = reinterpret_cast<float*>(sm + L.red);
     uint8_t* misc = sm + L.misc;
-    const int nbox_gu = H / 256, nbox_dn = I / 256 > 0 ? I / 256 : 1;
+    // TMA boxes of 128-byte code rows: 256 columns of 4-bit codes, 128 of one-byte codes
+    const int nbox_gu = H * kBits / 1024, nbox_dn = I * kBits / 1024 > 0 ? I * kBits / 1024 : 1;
     uint64_t* bar_gu = reinterpret_cast<uint64_t*>(misc);               // [nbox_gu] (<= 16)
     uint64_t* bar_dn = bar_gu + 16;                                      // [1]
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_dn + 1);
@@ -388,7 +440,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             }
         }
         if (lane == 31) {
-            mbar_arrive_expect_tx(bar_dn, (uint32_t)RD * (I / 2) + 2 * dsz);
+            mbar_arrive_expect_tx(bar_dn, (uint32_t)RD * (I * kBits / 8) + 2 * dsz);
             for (int b = 0; b < nbox_dn; ++b) tma_load_2d(dcodes + (size_t)b * RD * 128, MD, b * 32, drow, bar_dn);
             bulk_load(dsb, (sh ? a.sds : a.ds) + dO, dsz, bar_dn);
             bulk_load(dsb + RD * (I / 64), (sh ? a.sdb : a.db) + dO, dsz, bar_dn);
@@ -446,12 +498,18 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         uint32_t q[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float m = (j & 1) ? 0.0625f : 1.0f;
             bad |= !(fabsf(f[j]) <= 65504.f) || !(fabsf(f[j + 4]) <= 65504.f);
-            const __half2 h2 = __floats2half2_rn(f[j] * m, f[j + 4] * m);
+            __half2 h2;
+            if (CODE == kCodeU4) {
+                const float m = (j & 1) ? 0.0625f : 1.0f;
+                h2 = __floats2half2_rn(f[j] * m, f[j + 4] * m);
+            } else {   // 4-column units (x[4u], x[4u+2]), (x[4u+1], x[4u+3])
+                const int b = (j >> 1) * 4 + (j & 1);
+                h2 = __floats2half2_rn(f[b], f[b + 2]);
+            }
             q[j] = h2_as_u32(h2);
             const float2 back = __half22float2(h2);
-            if (j & 1) so += back.x + back.y; else sb += back.x + back.y;
+            if (CODE == kCodeU4 && (j & 1)) so += back.x + back.y; else sb += back.x + back.y;
         }
         reinterpret_cast<uint4*>(xperm)[i] = make_uint4(q[0], q[1], q[2], q[3]);
 #pragma unroll
@@ -459,8 +517,8 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             sb += __shfl_xor_sync(0xffffffffu, sb, off);
             so += __shfl_xor_sync(0xffffffffu, so, off);
         }
-        if ((i & 7) == 0) {
-            xbs[i / 8] = sb + so;
+        if ((i & 7) == 0) {   // E4M3 products carry no 1024 offset
+            xbs[i / 8] = CODE == kCodeE4M3 ? 0.f : sb + so;
             xsum[i / 8] = sb + 16.f * so;
         }
         if (bad) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
@@ -569,7 +627,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             // starts on an early box and, once the last box lands, has one box left
             const int half = ngrp / 2;
             for (int hf = 0; hf < 2; ++hf)
-                w4_gemv16(up ? ucodes : gcodes, RG, r0, hf * half + ks * half / KS, hf * half + (ks + 1) * half / KS,
+                w4_gemv16<CODE>(up ? ucodes : gcodes, RG, r0, hf * half + ks * half / KS, hf * half + (ks + 1) * half / KS,
                           reinterpret_cast<const uint4*>(xperm), xbs, xsum, sb, sb + RG * (H / 64), H / 64, acc0, acc1,
                           bar_gu, abort_flag, status);
             if ((lane & 3) == 0) {
@@ -627,10 +685,18 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
 #pragma unroll
             for (int j = 0; j < 8; ++j) bad |= !(fabsf(v[j]) <= 65504.f);
             if (bad) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
-            const uint32_t q0 = h2_as_u32(__floats2half2_rn(v[0], v[4]));
-            const uint32_t q1 = h2_as_u32(__floats2half2_rn(v[1] * 0.0625f, v[5] * 0.0625f));
-            const uint32_t q2 = h2_as_u32(__floats2half2_rn(v[2], v[6]));
-            const uint32_t q3 = h2_as_u32(__floats2half2_rn(v[3] * 0.0625f, v[7] * 0.0625f));
+            uint32_t q0, q1, q2, q3;
+            if (CODE == kCodeU4) {
+                q0 = h2_as_u32(__floats2half2_rn(v[0], v[4]));
+                q1 = h2_as_u32(__floats2half2_rn(v[1] * 0.0625f, v[5] * 0.0625f));
+                q2 = h2_as_u32(__floats2half2_rn(v[2], v[6]));
+                q3 = h2_as_u32(__floats2half2_rn(v[3] * 0.0625f, v[7] * 0.0625f));
+            } else {   // 4-column units, as for x
+                q0 = h2_as_u32(__floats2half2_rn(v[0], v[2]));
+                q1 = h2_as_u32(__floats2half2_rn(v[1], v[3]));
+                q2 = h2_as_u32(__floats2half2_rn(v[4], v[6]));
+                q3 = h2_as_u32(__floats2half2_rn(v[5], v[7]));
+            }
             reinterpret_cast<uint4*>(hperm)[i] = make_uint4(q0, q1, q2, q3);
         }
     }
@@ -645,10 +711,10 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float2 f = __half22float2(u32_as_h2(u[j]));
-                    if (j & 1) so += f.x + f.y; else sb += f.x + f.y;
+                    if (CODE == kCodeU4 && (j & 1)) so += f.x + f.y; else sb += f.x + f.y;
                 }
             }
-            hbs[gi] = sb + so;
+            hbs[gi] = CODE == kCodeE4M3 ? 0.f : sb + so;   // E4M3 products carry no 1024 offset
             hsum[gi] = sb + 16.f * so;
         }
     }
@@ -662,7 +728,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         for (int task = warp; task < ntile * KS; task += kFWarps) {
             const int t = task / KS, ks = task % KS;
             float acc0 = 0.f, acc1 = 0.f;
-            w4_gemv16(dcodes, RD, t * 16, ks * ngrp / KS, (ks + 1) * ngrp / KS, reinterpret_cast<const uint4*>(hperm),
+            w4_gemv16<CODE>(dcodes, RD, t * 16, ks * ngrp / KS, (ks + 1) * ngrp / KS, reinterpret_cast<const uint4*>(hperm),
                       hbs, hsum, dsb, dsb + RD * (I / 64), I / 64, acc0, acc1, nullptr, abort_flag, status);
             if ((lane & 3) == 0) {
                 red[task * 16 + (lane >> 2)] = acc0;
@@ -729,11 +795,13 @@ static EncodeTiledFn2 encode_fn2() {
 }
 
 // codes [rows][cols/8] uint32, box = 32 words x box_rows, 128-byte swizzle
-static bool codes_map(CUtensorMap* m, const uint32_t* codes, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+static bool codes_map(CUtensorMap* m, const uint32_t* codes, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                      int bits) {
     EncodeTiledFn2 fn = encode_fn2();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {cols / 8, rows};
-    const cuuint64_t strides[1] = {cols / 8 * 4};
+    const uint64_t words = cols * bits / 32;   // code words per row
+    const cuuint64_t dims[2] = {words, rows};
+    const cuuint64_t strides[1] = {words * 4};
     const cuuint32_t box[2] = {32, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(codes), dims, strides, box, estr,
@@ -741,26 +809,36 @@ static bool codes_map(CUtensorMap* m, const uint32_t* codes, uint64_t rows, uint
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The instance for the layer's shape: specialised for the sizes of the pages'
-// layer (H=2048, I=512, E=256, top-8), generic otherwise.
+static int code_of(const moe_w4_layer& L) {
+    return code_bits_of(L) == 4 ? kCodeU4 : (codes_e4m3(L) ? kCodeE4M3 : kCodeU8);
+}
+
+// The instance for the layer's shape and codes: specialised for the sizes of the
+// pages' layer (H=2048, I=512, E=256, top-8), generic otherwise; one-byte codes
+// have the specialised instance only.
 using FusedKernel = void (*)(FusedArgs, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap);
 static FusedKernel fused_kernel_for(const moe_w4_layer& L) {
-    if (L.H == 2048 && L.I == 512 && L.E == 256 && L.top_k == 8) return decode_fused_kernel<2048, 512, 256, 8>;
-    return decode_fused_kernel<0, 0, 0, 0>;
+    const bool spec = L.H == 2048 && L.I == 512 && L.E == 256 && L.top_k == 8;
+    switch (code_of(L)) {
+        case kCodeU4: return spec ? decode_fused_kernel<2048, 512, 256, 8, kCodeU4> : decode_fused_kernel<0, 0, 0, 0, kCodeU4>;
+        case kCodeU8: return spec ? decode_fused_kernel<2048, 512, 256, 8, kCodeU8> : nullptr;
+        default: return spec ? decode_fused_kernel<2048, 512, 256, 8, kCodeE4M3> : nullptr;
+    }
 }
 
 static bool shape_ok(const moe_w4_layer& L) {
-    if (code_bits_of(L) != 4) return false;   // the mma.sync dot engine unpacks nibbles
+    const int bits = code_bits_of(L);
+    if (!fused_kernel_for(L)) return false;
     if (L.H % 256 || L.I % 256 || L.H > 4096 || L.I > 2048) return false;   // slices of 16 rows; <= 16 row tiles
-    if (L.H / 256 > 16) return false;                                         // gate/up box barriers
+    if (L.H * bits / 1024 > 16) return false;                                 // gate/up box barriers
     if (L.E < 128 || L.E > 256 || L.E % 32) return false;   // top-k: 8 scores per lane; 2E floats hold the K-split partials
     if (L.top_k + 1 > kMaxSlots) return false;
     if (L.H > 64 * kPE * (L.top_k + 1)) return false;   // <= 64 router rows per CTA (32 per thread)
-    const FusedSmem s(L.H, L.E, L.I);
+    const FusedSmem s(L.H, L.E, L.I, bits);
     return s.total + 1024 + 1024 <= 227 * 1024;   // + static shared memory of the kernel
 }
 
-static size_t fused_smem(const moe_w4_layer& L) { return FusedSmem(L.H, L.E, L.I).total + 1024; }
+static size_t fused_smem(const moe_w4_layer& L) { return FusedSmem(L.H, L.E, L.I, code_bits_of(L)).total + 1024; }
 
 static cudaLaunchConfig_t fused_config(const moe_w4_layer& L, cudaLaunchAttribute* attr, cudaStream_t st,
                                        bool pdl) {
@@ -812,11 +890,12 @@ bool decode_fused_supported(const moe_w4_layer& L) {
 cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                                 cudaStream_t st) {
     const int H = L.H, E = L.E, I = L.I, k = L.top_k;
-    const int RG = I / kPE, RD = H / kPE;
+    const int RG = I / kPE, RD = H / kPE, b = code_bits_of(L);
     CUtensorMap mg, mu, md, msg, msu, msd;
-    bool ok = codes_map(&mg, L.gate.codes, (uint64_t)E * I, H, RG) && codes_map(&mu, L.up.codes, (uint64_t)E * I, H, RG) &&
-              codes_map(&md, L.down.codes, (uint64_t)E * H, I, RD) && codes_map(&msg, L.sh_gate.codes, I, H, RG) &&
-              codes_map(&msu, L.sh_up.codes, I, H, RG) && codes_map(&msd, L.sh_down.codes, H, I, RD);
+    bool ok = codes_map(&mg, L.gate.codes, (uint64_t)E * I, H, RG, b) &&
+              codes_map(&mu, L.up.codes, (uint64_t)E * I, H, RG, b) &&
+              codes_map(&md, L.down.codes, (uint64_t)E * H, I, RD, b) && codes_map(&msg, L.sh_gate.codes, I, H, RG, b) &&
+              codes_map(&msu, L.sh_up.codes, I, H, RG, b) && codes_map(&msd, L.sh_down.codes, H, I, RD, b);
     if (!ok) return cudaErrorInvalidValue;
     FusedArgs a{};
     a.x = x; a.router_w = L.router_w; a.router_bias = L.router_bias; a.shared_gate = L.shared_gate;

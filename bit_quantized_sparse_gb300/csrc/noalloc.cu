@@ -76,10 +76,15 @@ extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const
     if (!L || L->E < 1 || L->top_k < 1 || L->top_k > 8 || L->top_k > L->E || L->H <= 0 || L->I <= 0)
         return MOE_W4_ERR_INVALID;
     if (L->H % kBM || L->I % kBM || L->H > 4096 || L->I > 4096 || L->E > 1024) return MOE_W4_ERR_UNSUPPORTED;
-    if (L->code_bits != 0 && L->code_bits != 4) return MOE_W4_ERR_UNSUPPORTED;   // per-row GEMVs unpack nibbles
+    if (L->code_bits != 0 && L->code_bits != 4 && L->code_bits != 8) return MOE_W4_ERR_UNSUPPORTED;
+    if (L->code_format != MOE_W4_CODES_UINT && L->code_format != MOE_W4_CODES_E4M3) return MOE_W4_ERR_UNSUPPORTED;
+    if (L->code_format == MOE_W4_CODES_E4M3 && L->code_bits != 8) return MOE_W4_ERR_UNSUPPORTED;
     if (T < 0) return MOE_W4_ERR_INVALID;
     if (T > kDecodeMaxT) return MOE_W4_ERR_UNSUPPORTED;
     if (T == 0) return MOE_W4_OK;
+    // one-byte codes: only the one-kernel batch-1 decode (the per-row GEMVs of
+    // T >= 2 unpack nibbles)
+    if (code_bits_of(*L) == 8 && !(T == 1 && decode_fused_supported(*L))) return MOE_W4_ERR_UNSUPPORTED;
     if (!x || !out || !L->router_w || !L->shared_gate) return MOE_W4_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15) return MOE_W4_ERR_ALIGN;
     const moe_w4_mat* ms[6] = {&L->gate, &L->up, &L->down, &L->sh_gate, &L->sh_up, &L->sh_down};

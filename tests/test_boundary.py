@@ -74,6 +74,17 @@ def test_bad_shapes_rejected(mw, field, val, code):
     assert mw.moe_w4_forward_decode(ctypes.byref(L), 1, ws, ws, ws, 1 << 40, None) == code
 
 
+@pytest.mark.parametrize("bits,fmt,T", [(6, 0, 1), (4, 1, 1), (0, 1, 1), (8, 2, 1), (8, 0, 2), (8, 1, 4)])
+def test_noalloc_code_formats_rejected(mw, bits, fmt, T):
+    """The allocation-free decode refuses code formats it has no kernels for
+    (host checks only, before any device work): unknown widths or formats,
+    E4M3 with 4-bit codes, and one-byte codes at T >= 2."""
+    L = _layer(mw)
+    L.code_bits, L.code_format = bits, fmt
+    ws = 1 << 12
+    assert mw.moe_w4_forward_decode_noalloc(ctypes.byref(L), T, ws, ws, None) == mw.MOE_W4_ERR_UNSUPPORTED
+
+
 def test_bad_arguments_rejected(mw):
     L = _layer(mw)
     p = ctypes.byref(L)

@@ -232,12 +232,33 @@ def test_other_shapes(mw, torch, H, E, I, k):
     assert dl.status() == 0
 
 
+def _traced_decode(mw, torch, dl, x_rows):
+    """One decode call with the library's kernel timing events set: the output
+    (bf16 bits) and the number of kernels the call launched."""
+    import ctypes
+    n = 12
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * n)(*[e.cuda_event for e in evs])
+    mw._check(mw.moe_w4_set_trace_events(arr, n), "trace")
+    try:
+        out = mw.forward_decode(dl, mw.tokens_to_device(x_rows))
+        torch.cuda.synchronize()
+        nk = mw.moe_w4_last_traced_kernels()
+    finally:
+        mw.moe_w4_set_trace_events(None, 0)
+    return to_np_bits(out), nk
+
+
 @pytest.mark.parametrize("name", ["w8_tiny_T4", "w8_T512", "e4m3_tiny_T4", "e4m3_T512"])
 def test_w8_layer(mw, torch, name):
     """The one-byte weight-format variants (four codes per word; unsigned
-    8-bit affine codes or FP8 E4M3 codes): routing, prefill and decode (1 and 4
-    rows, both on the grouped path) against the oracle; the allocation-free
-    decode declines them."""
+    8-bit affine codes or FP8 E4M3 codes): routing, prefill and decode (1 row
+    on the one-kernel path for the full-size layer, 4 rows on the grouped path)
+    against the oracle; the allocation-free decode runs the one-kernel path at
+    T = 1 and declines T >= 2."""
     import ctypes
     L, x = S.draw_config(name)
     assert L.code_bits == 8
@@ -248,12 +269,25 @@ def test_w8_layer(mw, torch, name):
     check_route(r, L, x)
     ref = O.moe_layer(L, x)["out"]
     check_out(to_np_bits(mw.forward_prefill(dl, xd)), ref)
-    check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[:1]))), ref[:1])
+    out1, nk = _traced_decode(mw, torch, dl, x[:1])
+    check_out(out1, ref[:1])
+    # the full-size layer takes the one-kernel batch-1 decode, the tiny one the grouped path
+    assert nk == (1 if L.H == 2048 else 9), nk
     if x.shape[0] >= 8:
         check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[4:8]))), ref[4:8])
-    out = torch.empty((1, L.H), dtype=torch.bfloat16, device="cuda")
-    assert mw.moe_w4_forward_decode_noalloc(ctypes.byref(dl.c), 1, xd.data_ptr(), out.data_ptr(),
-                                            None) == mw.MOE_W4_ERR_UNSUPPORTED
+    # the allocation-free decode: the one-kernel path at T = 1 (full-size layer only);
+    # its T >= 2 kernels unpack nibbles, so one-byte codes are declined there
+    out = torch.empty((4, L.H), dtype=torch.bfloat16, device="cuda")
+    rc1 = mw.moe_w4_forward_decode_noalloc(ctypes.byref(dl.c), 1, xd.data_ptr(), out.data_ptr(), None)
+    if L.H == 2048:
+        assert rc1 == mw.MOE_W4_OK
+        torch.cuda.synchronize()
+        check_out(to_np_bits(out[:1]), ref[:1])
+    else:
+        assert rc1 == mw.MOE_W4_ERR_UNSUPPORTED
+    if x.shape[0] >= 4:
+        assert mw.moe_w4_forward_decode_noalloc(ctypes.byref(dl.c), 4, xd.data_ptr(), out.data_ptr(),
+                                                None) == mw.MOE_W4_ERR_UNSUPPORTED
     assert dl.status() == 0
 
 
