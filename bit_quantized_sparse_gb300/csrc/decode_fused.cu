@@ -417,7 +417,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     }
 
     // ---------------------------------------------------------------- weight loads (routed: after the top-k)
-    // called by all 32 lanes of warp 0: lane b issues box b, lanes 16.. the rest
+    // called by all 32 lanes of warp 0
     auto issue_loads = [&](int e) {
         const bool sh = (e >= E);
         const CUtensorMap* MG = sh ? &msg : &mg;
@@ -427,19 +427,25 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         const int drow = (sh ? 0 : e * H) + ei * RD;
         const uint32_t gsz = RG * (H / 64) * 2, dsz = RD * (I / 64) * 2;
         const size_t go = (size_t)grow * (H / 64), dO = (size_t)drow * (I / 64);
-        if (lane < nbox_gu) {
-            const int b = lane;
-            mbar_arrive_expect_tx(&bar_gu[b], 2u * RG * 128 + (b == 0 ? 4 * gsz : 0));
-            tma_load_2d(gcodes + (size_t)b * RG * 128, MG, b * 32, grow, &bar_gu[b]);
-            tma_load_2d(ucodes + (size_t)b * RG * 128, MU, b * 32, grow, &bar_gu[b]);
-            if (b == 0) {
-                bulk_load(gsb, (sh ? a.sgs : a.gs) + go, gsz, &bar_gu[0]);
-                bulk_load(gsb + RG * (H / 64), (sh ? a.sgb : a.gb) + go, gsz, &bar_gu[0]);
-                bulk_load(usb, (sh ? a.sus : a.us) + go, gsz, &bar_gu[0]);
-                bulk_load(usb + RG * (H / 64), (sh ? a.sub : a.ub) + go, gsz, &bar_gu[0]);
-            }
+        // in the order the GEMVs consume them: the gate/up scales and biases (box 0's
+        // barrier waits for them too), then gate and up of box 0, of box 1, ..., then down
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_gu[0], 2u * RG * 128 + 4 * gsz);
+            bulk_load(gsb, (sh ? a.sgs : a.gs) + go, gsz, &bar_gu[0]);
+            bulk_load(gsb + RG * (H / 64), (sh ? a.sgb : a.gb) + go, gsz, &bar_gu[0]);
+            bulk_load(usb, (sh ? a.sus : a.us) + go, gsz, &bar_gu[0]);
+            bulk_load(usb + RG * (H / 64), (sh ? a.sub : a.ub) + go, gsz, &bar_gu[0]);
         }
-        if (lane == 31) {
+        __syncwarp();
+        for (int p = lane; p < 2 * nbox_gu; p += 32) {   // p = 2 box + matrix
+            const int b = p >> 1;
+            if ((p & 1) == 0 && b != 0) mbar_arrive_expect_tx(&bar_gu[b], 2u * RG * 128);
+            __syncwarp(__activemask());
+            tma_load_2d(((p & 1) ? ucodes : gcodes) + (size_t)b * RG * 128, (p & 1) ? MU : MG, b * 32, grow,
+                        &bar_gu[b]);
+        }
+        __syncwarp();
+        if (lane == 0) {
             mbar_arrive_expect_tx(bar_dn, (uint32_t)RD * (I * kBits / 8) + 2 * dsz);
             for (int b = 0; b < nbox_dn; ++b) tma_load_2d(dcodes + (size_t)b * RD * 128, MD, b * 32, drow, bar_dn);
             bulk_load(dsb, (sh ? a.sds : a.ds) + dO, dsz, bar_dn);
