@@ -708,11 +708,11 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     }
     __syncthreads();
     const bool h_ok = h_in && !*abort_flag;
-    if (h_ok) {
-        for (int gi = tid; gi < I / 64; gi += kFThreads) {
+    if (h_ok) {   // per-64-value group sums of h: one warp per group, lanes 0..7 one 8-value entry each
+        for (int gi = warp; gi < I / 64; gi += kFWarps) {
             float sb = 0.f, so = 0.f;
-            for (int i = gi * 8; i < gi * 8 + 8; ++i) {
-                const uint4 q = reinterpret_cast<const uint4*>(hperm)[i];
+            if (lane < 8) {
+                const uint4 q = reinterpret_cast<const uint4*>(hperm)[gi * 8 + lane];
                 const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -720,8 +720,15 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
                     if (CODE == kCodeU4 && (j & 1)) so += f.x + f.y; else sb += f.x + f.y;
                 }
             }
-            hbs[gi] = CODE == kCodeE4M3 ? 0.f : sb + so;   // E4M3 products carry no 1024 offset
-            hsum[gi] = sb + 16.f * so;
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1) {
+                sb += __shfl_xor_sync(0xffffffffu, sb, off);
+                so += __shfl_xor_sync(0xffffffffu, so, off);
+            }
+            if (lane == 0) {
+                hbs[gi] = CODE == kCodeE4M3 ? 0.f : sb + so;   // E4M3 products carry no 1024 offset
+                hsum[gi] = sb + 16.f * so;
+            }
         }
     }
     // ---------------------------------------------------------------- 5. down GEMV
