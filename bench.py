@@ -368,22 +368,52 @@ def run_gpu(args, rank, local_rank, world, dist):
         variants[vname] = dict(t_pre=t8_pre, t_dec=t8_dec, k_pre=k8_pre, bits=bits)
         del l8, ws8
 
-    # end to end through host buffers: copy in, run, copy out, every step
+    # end to end through host buffers, every step: the step's inputs are copied in
+    # from pinned host memory and its outputs copied back, segment by segment (the
+    # four 4096-row prefill chunks, then the decode rows).  A segment's rows go in
+    # on one copy stream, the segment runs once they are in, and its output goes
+    # out on a second copy stream while the next segment runs.  Events order the
+    # reuse of a device buffer across steps: its copy-in waits for the previous
+    # step's compute on it, and the compute that overwrites an output waits for
+    # the previous step's copy-out.
     x_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
     x_host.copy_(x.cpu())
     xd_host = torch.empty((ndec, H), dtype=torch.bfloat16, pin_memory=True)
     xd_host.copy_(xdec.cpu())
     o_host = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
     od_host = torch.empty((ndec, H), dtype=torch.bfloat16, pin_memory=True)
+    h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    starts = list(range(0, T, chunk))
+    g_seg = [capture(lambda i=i: mw.forward_prefill(layers[0], x[i:i + chunk], out=out[i:i + chunk], ws=ws))
+             for i in starts] + [g_dec]
+    seg_in = [(x[i:i + chunk], x_host[i:i + chunk]) for i in starts] + [(xdec, xd_host)]
+    seg_out = [(o_host[i:i + chunk], out[i:i + chunk]) for i in starts] + [(od_host, outdec)]
+    done_read = [None] * len(g_seg)   # compute finished with the segment's input
+    done_out = [None] * len(g_seg)    # copy-out of the segment's output finished
 
     def e2e_steps(n):
-        with torch.cuda.stream(stream):
-            for _ in range(n):
-                x.copy_(x_host, non_blocking=True)
-                xdec.copy_(xd_host, non_blocking=True)
-                g_step.replay()
-                o_host.copy_(out, non_blocking=True)
-                od_host.copy_(outdec, non_blocking=True)
+        for _ in range(n):
+            arrived = []
+            for sgi, (dst, src) in enumerate(seg_in):
+                with torch.cuda.stream(h2d):
+                    if done_read[sgi] is not None:
+                        h2d.wait_event(done_read[sgi])
+                    dst.copy_(src, non_blocking=True)
+                    arrived.append(torch.cuda.Event())
+                    arrived[-1].record(h2d)
+            for sgi, g in enumerate(g_seg):
+                with torch.cuda.stream(stream):
+                    stream.wait_event(arrived[sgi])
+                    if done_out[sgi] is not None:
+                        stream.wait_event(done_out[sgi])
+                    g.replay()
+                    done_read[sgi] = torch.cuda.Event()
+                    done_read[sgi].record(stream)
+                with torch.cuda.stream(d2h):
+                    d2h.wait_event(done_read[sgi])
+                    seg_out[sgi][0].copy_(seg_out[sgi][1], non_blocking=True)
+                    done_out[sgi] = torch.cuda.Event()
+                    done_out[sgi].record(d2h)
 
     e2e_steps(args.warmup)
     torch.cuda.synchronize()
