@@ -411,35 +411,98 @@ MW4_DEV uint32_t order_key(float v) {
     return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
 }
 
-// Top-k (k <= 8) of E <= 32*NV scores of one warp: lane j holds scores
-// lane + 32 i as keys; each round takes the warp maximum (redux.sync) and, among
-// the lanes holding it, the lowest expert index, so equal scores go to the
-// lower index.  Writes the experts by descending score and their softmax
-// weights (over the selection, relative to the largest score).
+MW4_DEV void sort_desc_ce(uint64_t& a, uint64_t& b) {
+    const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
+    a = hi;
+    b = lo;
+}
+
+// Top-k (k <= 8) of E <= 32*NV (NV in 1, 2, 4, 8) scores in shared memory by one
+// warp, larger score first and the lower expert index on equal scores.  Lane l
+// holds experts l + 32 i as 64-bit words (order-preserving key << 32 | ~index),
+// sorted once in descending order by a sorting network (19 exchanges for 8
+// words), so a lane's best candidate is always its first word.  Each round takes
+// the warp maximum of the keys (redux.sync), the lowest index holding it
+// (redux.sync), and the lane that owns the winner drops its first word.  Absent
+// experts (index >= E) carry key 0 and index 0xffffffff and sort last.  Lane
+// r < k returns the r-th selection (index and score); with fewer than k experts
+// the missing ones read -1.
 template <int NV>
-MW4_DEV void select_topk_warp_n(const float* sc, int E, int k, int32_t* idx_out, float* w_out) {
+MW4_DEV void warp_topk_sorted(const float* sc, int E, int k, int& sel_idx, float& sel_val) {
+    static_assert(NV == 1 || NV == 2 || NV == 4 || NV == 8, "sorting networks for 1, 2, 4 or 8 words");
     const int lane = threadIdx.x & 31;
-    uint32_t key[NV];
-    uint32_t live = 0;   // bit i: score lane + 32 i exists and is not taken
+    uint64_t c[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
-        key[i] = e < E ? order_key(sc[e]) : 0u;
-        if (e < E) live |= 1u << i;
+        c[i] = e < E ? ((uint64_t)order_key(sc[e]) << 32) | (uint32_t)~(uint32_t)e : 0ull;
     }
+    if (NV == 2) sort_desc_ce(c[0], c[NV - 1]);
+    if (NV == 4) {
+        sort_desc_ce(c[0], c[1 % NV]); sort_desc_ce(c[2 % NV], c[3 % NV]);
+        sort_desc_ce(c[0], c[2 % NV]); sort_desc_ce(c[1 % NV], c[3 % NV]);
+        sort_desc_ce(c[1 % NV], c[2 % NV]);
+    }
+    if (NV == 8) {   // Batcher-style network, depth 6
+        sort_desc_ce(c[0], c[2 % NV]); sort_desc_ce(c[1 % NV], c[3 % NV]);
+        sort_desc_ce(c[4 % NV], c[6 % NV]); sort_desc_ce(c[5 % NV], c[7 % NV]);
+        sort_desc_ce(c[0], c[4 % NV]); sort_desc_ce(c[1 % NV], c[5 % NV]);
+        sort_desc_ce(c[2 % NV], c[6 % NV]); sort_desc_ce(c[3 % NV], c[7 % NV]);
+        sort_desc_ce(c[0], c[1 % NV]); sort_desc_ce(c[2 % NV], c[3 % NV]);
+        sort_desc_ce(c[4 % NV], c[5 % NV]); sort_desc_ce(c[6 % NV], c[7 % NV]);
+        sort_desc_ce(c[2 % NV], c[4 % NV]); sort_desc_ce(c[3 % NV], c[5 % NV]);
+        sort_desc_ce(c[1 % NV], c[4 % NV]); sort_desc_ce(c[3 % NV], c[6 % NV]);
+        sort_desc_ce(c[1 % NV], c[2 % NV]); sort_desc_ce(c[3 % NV], c[4 % NV]); sort_desc_ce(c[5 % NV], c[6 % NV]);
+    }
+    sel_idx = -1;
+    sel_val = 0.f;
+    for (int r = 0; r < k; ++r) {
+        const uint32_t hk = (uint32_t)(c[0] >> 32), hix = ~(uint32_t)c[0];
+        const uint32_t wmax = __reduce_max_sync(0xffffffffu, hk);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, hk == wmax ? hix : 0xffffffffu);
+        if (hix == win && win != 0xffffffffu) {
+#pragma unroll
+            for (int i = 0; i + 1 < NV; ++i) c[i] = c[i + 1];
+            c[NV - 1] = 0ull;
+        }
+        if (lane == r && win < (uint32_t)E) { sel_idx = (int)win; sel_val = sc[win]; }
+    }
+}
+
+// Top-k (k <= 8) of E <= 32*NV scores of one warp, larger score first and the
+// lower expert index on equal scores; writes the experts by descending score
+// and their softmax weights (over the selection, relative to the largest
+// score).  NV <= 8 sorts each lane's candidates once (warp_topk_sorted); for
+// larger NV each round takes the warp maximum (redux.sync) of the lanes' best
+// remaining keys and, among the lanes holding it, the lowest expert index.
+template <int NV>
+MW4_DEV void select_topk_warp_n(const float* sc, int E, int k, int32_t* idx_out, float* w_out) {
+    const int lane = threadIdx.x & 31;
     int mine = 0;
     float mval = 0.f;
-    for (int r = 0; r < k; ++r) {
-        uint32_t bk = 0;
-        int bi = 0x7fffffff;
-        bool any = false;
+    if (NV <= 8) {
+        warp_topk_sorted<NV <= 8 ? NV : 8>(sc, E, k, mine, mval);
+    } else {
+        uint32_t key[NV];
+        uint32_t live = 0;   // bit i: score lane + 32 i exists and is not taken
 #pragma unroll
-        for (int i = 0; i < NV; ++i)   // ascending index in the lane: strict > keeps the lower one
-            if (((live >> i) & 1u) && (!any || key[i] > bk)) { bk = key[i]; bi = lane + 32 * i; any = true; }
-        const uint32_t wmax = __reduce_max_sync(0xffffffffu, any ? bk : 0u);
-        const uint32_t win = __reduce_min_sync(0xffffffffu, (any && bk == wmax) ? (uint32_t)bi : 0xffffffffu);
-        if ((int)(win & 31) == lane) live &= ~(1u << (win >> 5));
-        if (lane == r) { mine = (int)win; mval = sc[win]; }
+        for (int i = 0; i < NV; ++i) {
+            const int e = lane + 32 * i;
+            key[i] = e < E ? order_key(sc[e]) : 0u;
+            if (e < E) live |= 1u << i;
+        }
+        for (int r = 0; r < k; ++r) {
+            uint32_t bk = 0;
+            int bi = 0x7fffffff;
+            bool any = false;
+#pragma unroll
+            for (int i = 0; i < NV; ++i)   // ascending index in the lane: strict > keeps the lower one
+                if (((live >> i) & 1u) && (!any || key[i] > bk)) { bk = key[i]; bi = lane + 32 * i; any = true; }
+            const uint32_t wmax = __reduce_max_sync(0xffffffffu, any ? bk : 0u);
+            const uint32_t win = __reduce_min_sync(0xffffffffu, (any && bk == wmax) ? (uint32_t)bi : 0xffffffffu);
+            if ((int)(win & 31) == lane) live &= ~(1u << (win >> 5));
+            if (lane == r) { mine = (int)win; mval = sc[win]; }
+        }
     }
     const float v0 = __shfl_sync(0xffffffffu, mval, 0);
     const float ex = lane < k ? expf(mval - v0) : 0.f;

@@ -135,51 +135,6 @@ MW4_DEV uint32_t ld_acquire_u32(const unsigned int* p) {
     return v;
 }
 
-// Top-k of E <= 256 scores in shared memory by one warp, larger score first and
-// the lower expert index on equal scores.  Lane l holds experts l + 32 i
-// (i < 8) as 64-bit words (order-preserving key << 32 | ~index), sorted once
-// in descending order by a 19-exchange network, so a lane's best candidate is
-// always its first word.  Each round takes the warp maximum of the keys
-// (redux.sync), the lowest index holding it (redux.sync), and the lane that
-// owns the winner drops its first word.  Absent experts (index >= E) carry key
-// 0 and index 0xffffffff and sort last.  Lane r < k returns the r-th selection
-// (index and score); with fewer than k experts the missing ones read -1.
-MW4_DEV void sort_desc_ce(uint64_t& a, uint64_t& b) {
-    const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
-    a = hi;
-    b = lo;
-}
-
-MW4_DEV void warp_topk_sorted(const float* sc, int E, int k, int& sel_idx, float& sel_val) {
-    const int lane = threadIdx.x & 31;
-    uint64_t c[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        c[i] = e < E ? ((uint64_t)order_key(sc[e]) << 32) | (uint32_t)~(uint32_t)e : 0ull;
-    }
-    // Batcher-style network for 8 inputs (depth 6)
-    sort_desc_ce(c[0], c[2]); sort_desc_ce(c[1], c[3]); sort_desc_ce(c[4], c[6]); sort_desc_ce(c[5], c[7]);
-    sort_desc_ce(c[0], c[4]); sort_desc_ce(c[1], c[5]); sort_desc_ce(c[2], c[6]); sort_desc_ce(c[3], c[7]);
-    sort_desc_ce(c[0], c[1]); sort_desc_ce(c[2], c[3]); sort_desc_ce(c[4], c[5]); sort_desc_ce(c[6], c[7]);
-    sort_desc_ce(c[2], c[4]); sort_desc_ce(c[3], c[5]);
-    sort_desc_ce(c[1], c[4]); sort_desc_ce(c[3], c[6]);
-    sort_desc_ce(c[1], c[2]); sort_desc_ce(c[3], c[4]); sort_desc_ce(c[5], c[6]);
-    sel_idx = -1;
-    sel_val = 0.f;
-    for (int r = 0; r < k; ++r) {
-        const uint32_t hk = (uint32_t)(c[0] >> 32), hix = ~(uint32_t)c[0];
-        const uint32_t wmax = __reduce_max_sync(0xffffffffu, hk);
-        const uint32_t win = __reduce_min_sync(0xffffffffu, hk == wmax ? hix : 0xffffffffu);
-        if (hix == win && win != 0xffffffffu) {
-#pragma unroll
-            for (int i = 0; i < 7; ++i) c[i] = c[i + 1];
-            c[7] = 0ull;
-        }
-        if (lane == r && win < (uint32_t)E) { sel_idx = (int)win; sel_val = sc[win]; }
-    }
-}
-
 // --------------------------------------------------------------------------- legacy-MMA dot engine
 MW4_DEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -595,7 +550,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             if (warp == 0) {
                 int sidx;
                 float sval;
-                warp_topk_sorted(logits, E, k, sidx, sval);
+                warp_topk_sorted<8>(logits, E, k, sidx, sval);
                 const int e = __shfl_sync(0xffffffffu, sidx, slot);
                 // the loads first: the routing weight is needed only by the down GEMV
                 if (e < 0 || e >= E) {
