@@ -560,20 +560,30 @@ def main():
                 "peak_note": f"dense bf16 sustained, {pk['source']}; fp16 has the same nominal rate"}
     else:
         b = decode_bytes(c)
-        ach = b / sum(r["k_dec"].values()) / 1e9
         fused_only = len(r["k_dec"]) == 1
+        # one fused launch per call: the decode region of the step is 64 consecutive
+        # launches of this kernel alone, so its average launch duration is that
+        # region's CUDA-event time over the launches (back to back, as in the step;
+        # the traced duration of a launch isolated between events is reported too)
+        t_launch = r["t_dec"] / args.steps / ndec if fused_only else sum(r["k_dec"].values())
+        ach = b / t_launch / 1e9
         roof = {"kernel": "decode_fused_kernel" if fused_only else "decode step", "bound": "hbm", "achieved": ach,
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
                 "traffic": measured_traffic("decode_fused_kernel") if fused_only else None,
                 "work_per_launch": f"{b} B (algorithmic bytes of one batch-1 call)",
+                "us_per_launch": 1e6 * t_launch,
+                "duration": ("decode region of the timed replays: CUDA events around 64 consecutive launches, "
+                             "averaged" if fused_only else "sum of the traced kernels of one call"),
+                "us_isolated_launch": 1e6 * sum(r["k_dec"].values()),
                 "peak_note": f"measured copy bandwidth, {pk['source']}"}
-    t_dec_call = sum(r["k_dec"].values())
     fused = len(r["k_dec"]) == 1
+    t_dec_call = r["t_dec"] / args.steps / ndec if fused else sum(r["k_dec"].values())
     dec_launches = len(r["k_dec"])
     dec_b = decode_bytes(c)
     roof_dec = {"kernel": "decode_fused_kernel" if fused else "decode call (3 kernels)", "bound": "hbm", "achieved": dec_b / t_dec_call / 1e9,
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": dec_b / t_dec_call / 1e9 / pk["hbm_gbs"],
-                "bytes_per_call": dec_b, "us_per_call_kernels": 1e6 * t_dec_call,
+                "bytes_per_call": dec_b, "us_per_call": 1e6 * t_dec_call,
+                "us_isolated_launch": 1e6 * sum(r["k_dec"].values()),
                 "traffic": measured_traffic("decode_fused_kernel") if fused else None,
                 "us_per_call_in_step": 1e6 * r["t_dec"] / args.steps / ndec}
     pre_flops = gemm_flops(c, chunk, "gate_up") + gemm_flops(c, chunk, "down")
