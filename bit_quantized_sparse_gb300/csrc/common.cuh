@@ -437,6 +437,8 @@ MW4_DEV void warp_topk_sorted(const float* sc, int E, int k, int& sel_idx, float
         const int e = lane + 32 * i;
         c[i] = e < E ? ((uint64_t)order_key(sc[e]) << 32) | (uint32_t)~(uint32_t)e : 0ull;
     }
+    // every branch compiles for every NV; indices are taken modulo NV so that the
+    // branches of other widths stay in bounds (only the branch for this NV runs)
     if (NV == 2) sort_desc_ce(c[0], c[NV - 1]);
     if (NV == 4) {
         sort_desc_ce(c[0], c[1 % NV]); sort_desc_ce(c[2 % NV], c[3 % NV]);

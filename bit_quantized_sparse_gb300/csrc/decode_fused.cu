@@ -27,7 +27,10 @@
 //      m16n8k16 with fp16 A = 1024 + q (even nibbles) or 1024 + 16 q (odd
 //      nibbles), one bitwise op per pair, and B = x in fp16 with the odd
 //      positions divided by 16; fp32 accumulation per 64-column group, then
-//      s*(acc - 1024*sum(B)) + b*sum(x).  SwiGLU in fp32.
+//      s*(acc - 1024*sum(B)) + b*sum(x).  SwiGLU in fp32.  The instances for
+//      one-byte codes take 1024 + q (8-bit codes) or the exact E4M3 value (no
+//      offset) for bytes (0, 2) and (1, 3) of a word, with B in matching
+//      4-column units and no division by 16.
 //   4. h: every CTA publishes its slice of h in global memory; the 16 CTAs of
 //      an expert wait (bounded) until all 16 slices carry the tag and read all of h.
 //   5. down GEMV the same way with h in fp16, scaled by the routing weight
@@ -439,9 +442,11 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     cluster_arrive();
     // x for the GEMVs is prepared here, off the router's critical path, while the
     // other CTAs' router sums come in
-    // x as fp16 B fragments, one thread per 16-byte entry: entry i (32-column
-    // block i/4, lane%4 = i%4) holds {x[8i], x[8i+4]}, {x[8i+1], x[8i+5]}/16,
-    // {x[8i+2], x[8i+6]}, {x[8i+3], x[8i+7]}/16; plus the per-64-column group
+    // x as fp16 B fragments, one thread per 16-byte entry: for 4-bit codes
+    // entry i (32-column block i/4, lane%4 = i%4) holds {x[8i], x[8i+4]},
+    // {x[8i+1], x[8i+5]}/16, {x[8i+2], x[8i+6]}, {x[8i+3], x[8i+7]}/16; for
+    // one-byte codes {x[8i], x[8i+2]}, {x[8i+1], x[8i+3]}, {x[8i+4], x[8i+6]},
+    // {x[8i+5], x[8i+7]} (the 4-column units 2i and 2i+1); plus the per-64-column group
     // sums of the stored values (xbs) and of the values the products use
     // (xsum), reduced over the 8 lanes of a group (H/8 is a multiple of 32, so
     // the loop runs whole warps)
@@ -615,8 +620,8 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     }
     const bool h_in = gu_ok && !*abort_flag;
     if (h_in) {
-        // fp16 B fragments of h, laid out like x (odd entries divided by 16), once
-        // all 16 slices carry this call's tag
+        // fp16 B fragments of h, laid out like x, once all 16 slices carry this
+        // call's tag
         const uint32_t xtag = *xtag_s;
         for (int i = tid; i < I / 8; i += kFThreads) {
             const uint64_t* src = a.hx + (size_t)slot * I + i * 8;
