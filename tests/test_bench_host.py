@@ -17,6 +17,26 @@ def test_work_per_unit():
     # 2 * 3 * H * I * (k + 1) FLOP per token = 56.6 MFLOP
     per_tok = (bench.gemm_flops(c, 4096, "gate_up") + bench.gemm_flops(c, 4096, "down")) / 4096
     assert per_tok == 2 * 3 * 2048 * 512 * 9
+    # one-byte codes: 3 * H * I code bytes plus the same scales and biases per expert
+    assert bench.expert_bytes(2048, 512, bits=8) == 3 * 2048 * 512 + 4 * 3 * 2048 * 512 // 64 == 3342336
+    assert bench.decode_bytes(c, 1, bits=8) == 9 * 3342336 + 2048 * 256 * 4 + 2048 * 4 + 2 * 2048 * 2 == 32194560
+    # T rows reading each of `distinct` selected experts once, plus the shared one
+    assert bench.decode_bytes_rows(c, 4, 25) == 26 * 1769472 + 2048 * 256 * 4 + 2048 * 4 + 2 * 4 * 2048 * 2
+
+
+def test_variant_summary_fractions():
+    """The format-variant summary divides the algorithmic work by the measured
+    times and the peaks it is given."""
+    c = dict(H=2048, E=256, I=512, top_k=8)
+    pk = dict(hbm_gbs=6000.0, bf16_tflops_sustained=1500.0)
+    w = dict(t_pre=0.5e-3, t_dec=16e-6, bits=8, k_pre={"gemm_gate_up": 250e-6, "gemm_down": 150e-6})
+    v = bench.variant_summary(c, w, 4096, 1, pk)
+    flops = bench.gemm_flops(c, 4096, "gate_up") + bench.gemm_flops(c, 4096, "down")
+    assert abs(v["prefill"]["tensor_tflops"] - flops / 0.5e-3 / 1e12) < 1e-9
+    assert abs(v["prefill"]["frac_of_peak"] - flops / 0.5e-3 / 1e12 / 1500.0) < 1e-12
+    assert abs(v["prefill"]["gemm_frac_of_peak"]["down"] - bench.gemm_flops(c, 4096, "down") / 150e-6 / 1e12 / 1500.0) < 1e-12
+    assert v["decode_T1"]["bytes_per_call"] == 32194560
+    assert abs(v["decode_T1"]["frac_of_hbm"] - 32194560 / 16e-6 / 1e9 / 6000.0) < 1e-12
 
 
 def _free_port():
