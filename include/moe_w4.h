@@ -73,8 +73,9 @@ typedef struct {
  * nibble (rows of cols/8 words); code_bits = 8: four per uint32, the lowest
  * column in the lowest byte (rows of cols/4 words).  Either way a weight is
  * s * q + b with q the unsigned code and s, b the bf16 scale and bias of its
- * group of 64 columns.  8-bit layers take the one-kernel batch-1 decode only
- * for H = 2048, I = 512, E = 256, top_k = 8 (the grouped tensor-core path
+ * group of 64 columns.  8-bit layers (either code_format below) take the
+ * one-kernel batch-1 decode only for H = 2048, I = 512, E = 256, top_k = 8
+ * (the grouped tensor-core path
  * otherwise, and for every T >= 2); moe_w4_forward_decode_noalloc takes them
  * only where that one-kernel path applies (T = 1, that shape) and returns
  * MOE_W4_ERR_UNSUPPORTED otherwise.
