@@ -465,6 +465,20 @@ def test_generator_distribution():
     b8 = O.bf16_to_f64(L8.gate.biases).ravel()
     assert np.all(s8 >= 0) and abs(s8.mean() - 0.02 / 17 * math.sqrt(2 / math.pi)) < 2e-4
     assert abs(np.std(b8 + 128 * s8) - 0.002) < 5e-4
+    # FP8 E4M3 codes: uniform sign, exponent field 3..10, uniform mantissa; never NaN;
+    # s = |N(0, 0.02)|, b = N(0, 0.002)
+    Lf, _ = S.draw_config("e4m3_tiny_T4")
+    assert Lf.code_bits == 8 and Lf.code_format == S.CODES_E4M3
+    qf = O.unpack_codes(Lf.gate.codes, 8).ravel().astype(np.int64)
+    ef = (qf >> 3) & 15
+    assert ef.min() == 3 and ef.max() == 10
+    assert abs(np.mean(qf >> 7) - 0.5) < 0.05
+    assert np.bincount(qf & 7, minlength=8).min() > 0.8 * qf.size / 8
+    assert not np.any(np.isnan(O.e4m3_value(qf.astype(np.uint8))))
+    sf = O.bf16_to_f64(Lf.gate.scales).ravel()
+    bfv = O.bf16_to_f64(Lf.gate.biases).ravel()
+    assert np.all(sf >= 0) and abs(sf.mean() - 0.02 * math.sqrt(2 / math.pi)) < 2e-3
+    assert abs(np.std(bfv) - 0.002) < 5e-4
 
 
 # ---------------------------------------------------------------------------
