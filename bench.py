@@ -36,7 +36,7 @@ PREFILL_KERNELS = ["router_scores", "topk", "chunk_count", "scan", "assign", "ga
 DECODE_KERNELS = ["decode_router", "decode_gate_up", "decode_down"]   # the three-kernel path
 DECODE_FUSED = ["decode_fused"]
 SMALL_T = (4, 8)   # multi-row decode batches measured beside the step
-CPU_SAMPLE = (4096, 16)   # oracle sample for cpu_baseline: prefill rows, decode rows
+CPU_SAMPLE = (8192, 32)   # oracle sample for cpu_baseline: prefill rows, decode rows
 W8_REPLICAS = 8    # distinct one-byte-code layers each format-variant decode measurement cycles
 # weight codes: (bits, code_format) -- unsigned 4-bit, unsigned 8-bit, FP8 E4M3
 CODES = {"u4": (4, 0), "u8": (8, 0), "e4m3": (8, 1)}
@@ -626,8 +626,8 @@ def main():
         n_pre, n_dec = CPU_SAMPLE
         val, dt = time_oracle(r["L0"], r["x_np"], n_pre, n_dec, r["xdec_np"])
         line["cpu_baseline"] = {"value": val, "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
-                                "sample": f"{n_pre} prefill rows (one chunk) + {n_dec} batch-1 decode rows of the "
-                                          f"workload ({dt:.1f} s)"}
+                                "sample": f"{n_pre} prefill rows (two 4096-row chunks) + {n_dec} batch-1 decode rows "
+                                          f"of the workload ({dt:.1f} s)"}
     if rank == 0:
         print(json.dumps(line))
 
