@@ -54,7 +54,6 @@ tolerance used against it).  Parity pins: see tests/test_oracle_pins.py.
 """
 from __future__ import annotations
 
-import math
 from typing import Optional
 
 import numpy as np
@@ -280,6 +279,3 @@ def bits_per_weight(group_size: int = GROUP, code_bits: int = 4, param_bits: int
 def checkpoint_gb(n_params: float, bits: float) -> float:
     return n_params * bits / 8.0 / 1e9
 
-
-def logistic(z: float) -> float:
-    return 1.0 / (1.0 + math.exp(-z))

@@ -283,6 +283,20 @@ def check_group_golden():
     assert n == 3
 
 
+def check_block_map_golden():
+    """The block list by its exact (expert, first row) entries, hand-worked."""
+    n = 0
+    for ln in _lines("block_map_tiny.txt"):
+        parts = [p.strip() for p in ln.split("|")]
+        B = int(parts[1])
+        counts = np.array([int(v) for v in parts[2].split()])
+        want = [] if parts[3] == "-" else [tuple(int(v) for v in b.split()) for b in parts[3].split(";")]
+        got = [(int(e), int(r)) for e, r in O.block_map(counts, B)]
+        assert got == want, (parts[0], got, want)
+        n += 1
+    assert n == 5
+
+
 def check_group_invariants(seed=1):
     rng = np.random.default_rng(seed)
     for T, E, k in ((1, 4, 2), (37, 16, 4), (200, 64, 8)):
@@ -431,7 +445,7 @@ def check_row_independence():
 PINS = [check_dequant_golden, check_group_axis, check_dequant8_golden, check_dequant8_group_axis,
         check_formats_agree, check_e4m3_golden, check_e4m3_library, check_e4m3_monotone,
         check_dequant_e4m3_golden, check_e4m3_layer_integers, check_format_size, check_router_golden,
-        check_router_invariants, check_group_golden, check_group_invariants, check_silu,
+        check_router_invariants, check_group_golden, check_block_map_golden, check_group_invariants, check_silu,
         check_structured_ffn, check_layer_golden, check_identical_experts, check_dense_gating,
         check_brute_force_tiny, check_row_independence]
 
@@ -572,6 +586,23 @@ def _ungated_sigmoid(z):
     return np.ones_like(np.asarray(z, dtype=np.float64)) if np.ndim(z) else 1.0
 
 
+def _block_map_short_stride(counts, rows_per_block):
+    blocks = []
+    for e, c in enumerate(counts):
+        for r0 in range(0, int(c), max(1, rows_per_block - 1)):
+            blocks.append((e, r0))
+    return blocks
+
+
+def _block_map_row_major(counts, rows_per_block):
+    blocks = []
+    for r0 in range(0, int(max(counts, default=0)), rows_per_block):
+        for e, c in enumerate(counts):
+            if r0 < c:
+                blocks.append((e, r0))
+    return blocks
+
+
 _UNPACK = O.unpack_codes
 
 MUTANTS = [
@@ -587,6 +618,8 @@ MUTANTS = [
     ("expert_ffn", _silu_on_up),
     ("expert_ffn", _down_transposed),
     ("group", _group_by_slot),
+    ("block_map", _block_map_short_stride),
+    ("block_map", _block_map_row_major),
     ("sigmoid", _ungated_sigmoid),
 ]
 
