@@ -106,13 +106,51 @@ def _sample(T, n, seed):
     return np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=n, replace=False)]))
 
 
-@pytest.mark.parametrize("name,T", [("prefill_T4096", None), ("long_T16384", 4096)])
-def test_prefill_sampled(mw, torch, name, T):
-    L, x, dl = layer_of(mw, name, T)
+def test_prefill_T4096_every_row(mw, torch):
+    """The 4K prefill (Zipf(1.0) routing): all 4096 rows against the oracle,
+    element by element."""
+    L, x, dl = layer_of(mw, "prefill_T4096")
     out = to_np_bits(mw.forward_prefill(dl, mw.tokens_to_device(x)))
-    rows = _sample(x.shape[0], 48, 7)
-    ref = O.moe_layer(L, x, tokens=rows)["out"]
-    check_out(out[rows], ref)
+    check_out(out, O.moe_layer(L, x)["out"])
+    assert dl.status() == 0
+
+
+def test_long_prompt_every_row(mw, torch):
+    """The long prompt ("Optimizing on-device inference for Apple Silicon",
+    section "Bound scratch with prompt chunking": chunking bounds the scratch
+    and leaves the output unchanged).  Zipf(1.2) routing, 16384 rows as four
+    4096-row calls sharing one workspace: every row of every chunk against the
+    oracle; one 16384-row call gives the same bytes; then the 64 batch-1 decode
+    rows on the same layer (the one-kernel path), each against the oracle."""
+    c = S.CONFIGS["long_T16384"]
+    L, x, dl = layer_of(mw, "long_T16384")
+    T, chunk = c["T"], c["chunk"]
+    assert x.shape[0] == T
+    xd = mw.tokens_to_device(x)
+    n = dl.workspace_size(chunk)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    mw._check(mw.moe_w4_workspace_init(ws.data_ptr(), n, torch.cuda.current_stream().cuda_stream), "init")
+    parts = [mw.forward_prefill(dl, xd[i:i + chunk], ws=ws).clone() for i in range(0, T, chunk)]
+    whole = mw.forward_prefill(dl, xd)
+    torch.cuda.synchronize()
+    st = int(ws[mw.moe_w4_status_offset():][:4].view(torch.int32).item())
+    assert st == 0 and dl.status() == 0
+    chunked = torch.cat(parts)
+    assert torch.equal(whole.view(torch.int16), chunked.view(torch.int16))
+    ref = O.moe_layer(L, x)["out"]
+    got = to_np_bits(chunked)
+    for i in range(0, T, chunk):
+        check_out(got[i:i + chunk], ref[i:i + chunk])
+    # 64 consecutive batch-1 decode steps, fresh seeded rows (no model feedback)
+    xdec = S.draw_tokens(L, c["decode_steps"], c["seed"], stream=1)
+    outs = [mw.forward_decode(dl, mw.tokens_to_device(xdec[i:i + 1])).clone() for i in range(xdec.shape[0])]
+    torch.cuda.synchronize()
+    got_dec = np.concatenate([to_np_bits(o) for o in outs])
+    ref_dec = O.moe_layer(L, xdec)["out"]
+    for i in range(xdec.shape[0]):
+        check_out(got_dec[i:i + 1], ref_dec[i:i + 1])
+    _, nk = _traced_decode(mw, torch, dl, xdec[:1])
+    assert nk == 1, nk                      # the one-kernel batch-1 decode ran
     assert dl.status() == 0
 
 
