@@ -64,9 +64,9 @@ WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     w.dec_w = take(Td * k * 4);
     w.dec_gamma = take(Td * 4);
     w.dec_hh = take(Td * (k + 1) * I * 4);
-    w.dec_cpart = take((size_t)kFusedClustersPerExpert * (k + 1) * E * 8);
-    w.dec_hx = take((k + 1) * I * 8);
-    w.dec_ybuf = take((k + 1) * H * 8);
+    w.dec_scores = take(fused_scores_bytes(L));
+    w.dec_hx = take(fused_hx_bytes(L));
+    w.dec_hsx = take(fused_hsx_bytes(L));
     w.total = o;
     return w;
 }
@@ -227,11 +227,19 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, mo
     d.counter = &at<Ctrl>(workspace, w.ctrl)->decode_counter;
     d.status = &at<Ctrl>(workspace, w.ctrl)->status;
     d.ctrl = at<Ctrl>(workspace, w.ctrl);
-    d.fused_cpart = at<uint64_t>(workspace, w.dec_cpart);
+    d.fused_scores = at<uint64_t>(workspace, w.dec_scores);
     d.fused_hx = at<uint64_t>(workspace, w.dec_hx);
-    d.fused_ybuf = at<uint64_t>(workspace, w.dec_ybuf);
+    d.fused_hsx = at<uint64_t>(workspace, w.dec_hsx);
     trace_mark(stream, 0);
-    return launch_status(launch_decode(*L, T, x, out, d, stream));
+    if (launch_decode_fused(*L, x, out, d, stream) != cudaSuccess) {
+        // the cooperative launch was refused (the grid cannot be resident at once
+        // on this device or partition): the grouped path
+        cudaGetLastError();
+        return run_grouped(L, T, x, out, workspace, w, stream);
+    }
+    trace_kernels(1);
+    for (int i = 1; i <= 3; ++i) trace_mark(stream, i);
+    return launch_status(cudaGetLastError());
 }
 
 // Routing, grouping and the grouped tensor-core GEMMs over T rows (the

@@ -101,8 +101,10 @@ MW4_DEV uint64_t globaltimer() {
 // Bounded wait on an mbarrier phase.  On timeout it raises
 // MOE_W4_STATUS_WAIT_TIMEOUT, sets the CTA's abort flag and returns false.
 // Any thread that sees the abort flag set also gives up at once.
-MW4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The waiting loop is out of line: it is the rare path, and single-pass kernels
+// run from a cold instruction cache, where every inlined copy costs fetch time.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                   unsigned int* status) {
     const uint64_t t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -113,6 +115,9 @@ MW4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
             return false;
         }
     }
+}
+MW4_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, unsigned int* status) {
+    return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, abort_flag, status);
 }
 
 // mbar_wait run by a whole converged warp; every lane gets lane 0's answer.
@@ -458,6 +463,7 @@ MW4_DEV void warp_topk_sorted(const float* sc, int E, int k, int& sel_idx, float
     }
     sel_idx = -1;
     sel_val = 0.f;
+#pragma unroll 1
     for (int r = 0; r < k; ++r) {
         const uint32_t hk = (uint32_t)(c[0] >> 32), hix = ~(uint32_t)c[0];
         const uint32_t wmax = __reduce_max_sync(0xffffffffu, hk);

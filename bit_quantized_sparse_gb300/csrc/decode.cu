@@ -197,12 +197,14 @@ cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint1
                           cudaStream_t st) {
     const int k = L.top_k;
     if (T == 1 && decode_fused_supported(L)) {   // one launch for the whole layer
-        const cudaError_t e = launch_decode_fused(L, x, out, d, st);
-        trace_kernels(1);
-        trace_mark(st, 1);
-        trace_mark(st, 2);
-        trace_mark(st, 3);
-        return e == cudaSuccess ? cudaGetLastError() : e;
+        if (launch_decode_fused(L, x, out, d, st) == cudaSuccess) {
+            trace_kernels(1);
+            trace_mark(st, 1);
+            trace_mark(st, 2);
+            trace_mark(st, 3);
+            return cudaGetLastError();
+        }
+        cudaGetLastError();   // the cooperative launch was refused: the three kernels below
     }
     static bool attrs_set[64] = {};
     int dev = 0;

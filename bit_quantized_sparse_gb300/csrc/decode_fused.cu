@@ -5,24 +5,25 @@
 // state and traffic" -- gate/up projections fused with the gated activation,
 // the output projection fused with the routing scores and the shared expert.)
 //
-// Grid: (k+1) experts x 16 CTAs, in clusters of 4 (one CTA per SM; the host
-// checks that every cluster fits on the GPU at once).  Expert slot j < k is
-// the j-th selected expert, slot k the shared expert.  CTA i (0..15) of an
-// expert owns gate/up rows [i*I/16, (i+1)*I/16) and down rows
-// [i*H/16, (i+1)*H/16) of it.
+// Grid: (k+1) expert slots x 16 CTAs, one CTA per SM, launched cooperatively
+// (every CTA is resident at once, which the two exchanges below rely on).
+// Slot j < k is the j-th selected expert, slot k the shared expert.  CTA i
+// (0..15) of a slot owns gate/up rows [i*I/16, (i+1)*I/16) of it; each of the
+// 16k routed CTAs also owns output rows [c*DR, (c+1)*DR), DR = H/(16k), of the
+// down projection of all k+1 slots.
 //
-//   1. router: every CTA sums x . W_r over its own 1/(16 (k+1)) slice of the H
-//      rows for all E experts (these loads go out first); the 4 slices of a
-//      cluster are added through distributed shared memory, the cluster sums
-//      are published in global memory and, once all are in (bounded wait: all
-//      CTAs are co-resident), every routed CTA adds them in a fixed order and
-//      selects the top-k.  Every value that crosses CTAs through global memory
-//      is an 8-byte (value, call tag) word, so that a reader waits on the data
-//      itself rather than on a counter and then the data.  The shared expert does not wait for the routing: it
-//      starts loading its weights as soon as its own router reads are done.
-//   2. TMA loads the CTA's slices of the packed codes (128-byte swizzle) and
-//      its scales/biases; the gate/up slices are consumed box by box as they
-//      land.
+//   1. router: CTA c computes complete scores x . W_r[:, e] (+bias) over all H
+//      for its experts e in [c*EPC, (c+1)*EPC) (EPC = E/(16(k+1)) rounded up;
+//      these W_r loads go out first) and publishes them; every CTA also forms
+//      the shared gate sigmoid(x . g) itself.  Every value that crosses CTAs
+//      is an 8-byte (value, call tag) word, so that a reader polls the data
+//      itself rather than a counter and then the data.
+//   2. every routed CTA polls the E scores (bounded wait), one warp selects
+//      the top-k (sorted candidate lists) and at once issues the TMA loads of
+//      the CTA's gate/up slices of its slot's expert and of its down rows of
+//      the k selected experts.  The shared expert needs no routing: its gate/up
+//      slices, and every routed CTA's down rows of it, are requested at kernel
+//      start, before the wait for the preceding kernel.
 //   3. gate/up GEMV on the tensor cores as a dot-product engine: mma.sync
 //      m16n8k16 with fp16 A = 1024 + q (even nibbles) or 1024 + 16 q (odd
 //      nibbles), one bitwise op per pair, and B = x in fp16 with the odd
@@ -31,25 +32,32 @@
 //      one-byte codes take 1024 + q (8-bit codes) or the exact E4M3 value (no
 //      offset) for bytes (0, 2) and (1, 3) of a word, with B in matching
 //      4-column units and no division by 16.
-//   4. h: every CTA publishes its slice of h in global memory; the 16 CTAs of
-//      an expert wait (bounded) until all 16 slices carry the tag and read all of h.
-//   5. down GEMV the same way with h in fp16, scaled by the routing weight
-//      (or the shared gate), written per expert.
-//   6. per block of output rows, the shared expert's CTA (it needs no routing,
-//      so it is usually done first) waits (bounded) for the k routed outputs,
-//      adds the k+1 in slot order and writes bf16 out.
-// No step waits on another CTA except these bounded exchanges and the hardware
-// cluster barriers.
+//   4. h: every CTA publishes its slice of h as fp16 pairs already in the
+//      dot engine's B-operand order; each routed CTA waits (bounded) until the
+//      h of all k+1 slots carries the call's tag.
+//   5. down GEMV of its DR output rows for all k+1 slots, the same dot engine,
+//      each slot's rows scaled by its routing weight (the shared one by the
+//      shared gate) and added in slot order in fp32; the CTA writes its rows of
+//      the bf16 output.  No further exchange.
+// No step waits on another CTA except these two bounded exchanges.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace mw4 {
 
-constexpr int kCS = 4;                                   // CTAs per cluster
-constexpr int kPE = kCS * kFusedClustersPerExpert;       // CTAs per expert (16)
-constexpr int kFThreads = 512;                           // 16 warps
+#ifndef MW4_FUSED_THREADS
+#define MW4_FUSED_THREADS 512
+#endif
+constexpr int kPE = 16;                 // CTAs per expert slot
+constexpr int kFThreads = MW4_FUSED_THREADS;   // warps hide the dot engine's latencies
 constexpr int kFWarps = kFThreads / 32;
-constexpr int kMaxSlots = 9;                             // k + 1 <= 9
+constexpr int kMaxSlots = 9;            // k + 1 <= 9
+constexpr int kRE = 8;                  // router: experts per CTA (one 32-byte sector of a W_r row)
+constexpr int kMaxRouterRows = 4;       // router: H rows per thread, at most
+constexpr int kScoreReplicas = 8;       // copies of the published score partials (readers spread over them)
+constexpr int kHReplicas = 8;           // copies of the published h and its piece sums
 
 struct FusedArgs {
     const uint16_t* x;          // [H] bf16
@@ -60,9 +68,10 @@ struct FusedArgs {
     const uint16_t* ds; const uint16_t* db;                                             // routed down s, b
     const uint16_t* sgs; const uint16_t* sgb; const uint16_t* sus; const uint16_t* sub; // shared
     const uint16_t* sds; const uint16_t* sdb;
-    uint64_t* cpart;            // [4(k+1)][E] cluster partial scores, tagged with the call
-    uint64_t* hx;               // [k+1][I] h of every expert, tagged with the call
-    uint64_t* ybuf;             // [k+1][H] weighted expert outputs, tagged with the call
+    uint64_t* scores;           // [kScoreReplicas][RS][E] partial router scores, tagged with the call
+    uint64_t* hx;               // [kHReplicas][k+1][I/2] h as fp16 pairs in B order, tagged with the call
+    uint64_t* hsx;              // [kHReplicas][k+1][I/16][2] per 16 values of h: sums of the stored B values
+                                // and of h itself, tagged with the call
     int32_t* idx_out;           // [k] (for inspection)
     float* w_out;               // [k]
     float* gamma_out;           // [1]
@@ -71,14 +80,19 @@ struct FusedArgs {
     int H, E, I, k;
 };
 
-// smem carve-up (byte offsets from a 1024-aligned base), computed on both sides
+// smem carve-up (byte offsets from a 1024-aligned base), computed on both sides.
+// After the gate/up GEMV its code slices are dead: h (in B order) and its group
+// sums then live in the gate codes region, the down partial sums in the up one.
 struct FusedSmem {
-    uint32_t gcodes, ucodes, dcodes, gsb, usb, dsb, xperm, xsum, xbs, part, logits, gsum, usum, hperm, hsum,
-        hbs, red, misc, total;
-    int RG, RD;
-    __host__ __device__ FusedSmem(int H, int E, int I, int bits) {
+    uint32_t gcodes, ucodes, dcodes, dslot, gsb, usb, dsb, xperm, xsum, xbs, logits, gred, gsum, usum, wred,
+        misc, total;
+    uint32_t hperm, hsum, hbs, hpiece, dred;   // aliases (see above)
+    uint32_t code_region;              // bytes of one gate/up code region
+    int RG, DR, NS;
+    __host__ __device__ FusedSmem(int H, int E, int I, int k, int bits) {
         RG = I / kPE;
-        RD = H / kPE;
+        DR = H / (kPE * k);
+        NS = k + 1;
         uint32_t o = 0;
         auto take = [&](uint32_t bytes, uint32_t align) {
             o = (o + align - 1) / align * align;
@@ -86,57 +100,38 @@ struct FusedSmem {
             o += bytes;
             return at;
         };
-        gcodes = take(RG * H / 8 * bits, 1024);
-        ucodes = take(RG * H / 8 * bits, 1024);
-        dcodes = take(RD * I / 8 * bits, 1024);
+        code_region = RG * H / 8 * bits;
+        gcodes = take(code_region, 1024);
+        ucodes = take(code_region, 1024);
+        dslot = (DR * I / 8 * bits + 1023) / 1024 * 1024;   // each slot's boxes 1024-aligned (128-byte swizzle)
+        dcodes = take(NS * dslot, 1024);
         gsb = take(2 * RG * (H / 64) * 2, 16);   // scales then biases
         usb = take(2 * RG * (H / 64) * 2, 16);
-        dsb = take(2 * RD * (I / 64) * 2, 16);
+        dsb = take(NS * 2 * DR * (I / 64) * 2, 16);   // per slot: scales [DR][I/64] then biases
         xperm = take(H * 2, 16);
         xsum = take(H / 64 * 4, 16);
         xbs = take(H / 64 * 4, 16);
-        part = take(E * 4, 16);
         logits = take(E * 4, 16);
+        // per (row tile, warp) 16 partial row sums; before the GEMV the polled score
+        // partials [RS][E] (RS * E = 128 k)
+        gred = take((2 * RG * kFWarps > 128 * k ? 2 * RG * kFWarps : 128 * k) * 4, 16);
         gsum = take(RG * 4, 16);
         usum = take(RG * 4, 16);
-        hperm = take(I * 2, 16);
-        hsum = take(I / 64 * 4, 16);
-        hbs = take(I / 64 * 4, 16);
-        red = part;   // K-split partials reuse the score buffers (part, logits: 2E floats) after routing
-        misc = take(256, 16);
+        wred = take(kFWarps * (kRE + 1) * 4, 16);
+        misc = take(512, 16);
         total = o;
+        hperm = gcodes;
+        hsum = gcodes + NS * I * 2;
+        hbs = hsum + NS * (I / 64) * 4;
+        hpiece = hbs + NS * (I / 64) * 4;   // [NS][I/16][2]
+        dred = ucodes;
+    }
+    // the aliased buffers fit their regions
+    __host__ __device__ bool aliases_fit(int I) const {
+        return (uint32_t)(NS * I * 2 + 2 * NS * (I / 64) * 4 + NS * (I / 16) * 2 * 4) <= code_region &&
+               (uint32_t)(NS * (I / 64) * DR * 4) <= code_region;
     }
 };
-
-// --------------------------------------------------------------------------- cluster helpers
-MW4_DEV uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-MW4_DEV uint32_t cluster_id() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-MW4_DEV void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// The two halves of cluster_sync, for work in between.
-MW4_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-MW4_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-MW4_DEV float ld_dsmem_f32(const void* local_ptr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_ptr)), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
-MW4_DEV uint32_t ld_acquire_u32(const unsigned int* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 
 // --------------------------------------------------------------------------- legacy-MMA dot engine
 MW4_DEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -147,12 +142,18 @@ MW4_DEV void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, u
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Codes word `wi` (0-based along the row) of row `row` inside a 128-byte
-// swizzled TMA tile set: boxes of 32 words x `rows` rows, box b at b*rows*128.
-MW4_DEV uint32_t sw_word(const uint8_t* base, int rows, int row, int wi) {
-    const int box = wi >> 5, u = (wi >> 2) & 7, w = wi & 3;
-    return *reinterpret_cast<const uint32_t*>(base + (size_t)box * rows * 128 + row * 128 + ((u ^ (row & 7)) << 4) +
-                                              w * 4);
+MW4_DEV uint32_t ld_acquire_u32(const unsigned int* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+MW4_DEV void st_relaxed_u32(unsigned int* p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+// A tagged word that carries a pair of fp16 values (B-operand order) instead of a float.
+MW4_DEV void st_tagged_u32(uint64_t* p, uint32_t v, uint32_t tag) {
+    const uint64_t w = ((uint64_t)tag << 32) | v;
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(w) : "memory");
 }
 
 // One warp: rows [r0, r0+16) of a swizzled codes tile set, one 64-column
@@ -162,6 +163,8 @@ MW4_DEV uint32_t sw_word(const uint8_t* base, int rows, int row, int wi) {
 // per word); B (`bperm`, 16 bytes per (32-column block, lane%4)) holds the
 // matching activations, the odd positions divided by 16, so that every
 // product is q * value + 1024 * (stored B value).
+// Code tiles are TMA boxes of 32 words x `rows` rows, 128-byte swizzled, box b
+// at b*rows*128.
 MW4_DEV void w4_group_mma(const uint8_t* codes, int rows, int r0, int grp, const uint4* bperm, float (&d)[4]) {
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     constexpr uint32_t M = 0x64006400u;
@@ -232,36 +235,112 @@ MW4_DEV void w8_group_mma(const uint8_t* codes, int rows, int r0, int grp, const
     }
 }
 
+// The B fragments of one 64-column group for this lane (8 words): 4-bit codes
+// the 16-byte entries of its two 32-column blocks, one-byte codes the 8-byte
+// units of its four 16-column chunks.
+template <int CODE>
+MW4_DEV void load_bfrag(const uint4* bperm, int grp, uint32_t (&b)[8]) {
+    const int c = threadIdx.x & 3;
+    if (CODE == kCodeU4) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 v = bperm[(grp * 2 + h) * 4 + c];
+            b[4 * h] = v.x; b[4 * h + 1] = v.y; b[4 * h + 2] = v.z; b[4 * h + 3] = v.w;
+        }
+    } else {
+        const uint2* bp = reinterpret_cast<const uint2*>(bperm);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const uint2 v = bp[(grp * 4 + h) * 4 + c];
+            b[2 * h] = v.x; b[2 * h + 1] = v.y;
+        }
+    }
+}
+
+// group_mma with the B fragments already in registers (load_bfrag).
+template <int CODE>
+MW4_DEV void group_mma_b(const uint8_t* codes, int rows, int r0, int grp, const uint32_t (&b)[8], float (&d)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    constexpr uint32_t M = 0x64006400u;
+    if (CODE == kCodeU4) {
+        const int blk0 = grp * 2;
+        const uint8_t* row0 = codes + (size_t)(blk0 >> 3) * rows * 128 + (r0 + g) * 128 + c * 4;
+        const uint8_t* row1 = row0 + 8 * 128;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int off = (((blk0 + h) & 7) ^ g) << 4;
+            const uint32_t wg = *reinterpret_cast<const uint32_t*>(row0 + off);
+            const uint32_t wh = *reinterpret_cast<const uint32_t*>(row1 + off);
+            uint32_t a[4];
+            a[0] = (wg & 0x000F000Fu) | M;
+            a[1] = (wh & 0x000F000Fu) | M;
+            a[2] = (wg & 0x00F000F0u) | M;
+            a[3] = (wh & 0x00F000F0u) | M;
+            mma_f16_16816(d, a, b[4 * h], b[4 * h + 1]);
+            const uint32_t wg8 = wg >> 8, wh8 = wh >> 8;
+            a[0] = (wg8 & 0x000F000Fu) | M;
+            a[1] = (wh8 & 0x000F000Fu) | M;
+            a[2] = (wg8 & 0x00F000F0u) | M;
+            a[3] = (wh8 & 0x00F000F0u) | M;
+            mma_f16_16816(d, a, b[4 * h + 2], b[4 * h + 3]);
+        }
+    } else {
+        const int ch0 = grp * 4;
+        const uint8_t* row0 = codes + (size_t)(ch0 >> 3) * rows * 128 + (r0 + g) * 128 + c * 4;
+        const uint8_t* row1 = row0 + 8 * 128;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int off = (((ch0 + h) & 7) ^ g) << 4;
+            const uint32_t wg = *reinterpret_cast<const uint32_t*>(row0 + off);
+            const uint32_t wh = *reinterpret_cast<const uint32_t*>(row1 + off);
+            uint32_t a[4];
+            if (CODE == kCodeE4M3) {
+                e4m3x4_to_f16(wg, a[0], a[2]);
+                e4m3x4_to_f16(wh, a[1], a[3]);
+            } else {
+                a[0] = (wg & 0x00FF00FFu) | M;
+                a[1] = (wh & 0x00FF00FFu) | M;
+                a[2] = ((wg >> 8) & 0x00FF00FFu) | M;
+                a[3] = ((wh >> 8) & 0x00FF00FFu) | M;
+            }
+            mma_f16_16816(d, a, b[2 * h], b[2 * h + 1]);
+        }
+    }
+}
+
+template <int CODE>
+MW4_DEV void group_mma(const uint8_t* codes, int rows, int r0, int grp, const uint4* bperm, float (&d)[4]) {
+    if (CODE == kCodeU4)
+        w4_group_mma(codes, rows, r0, grp, bperm, d);
+    else
+        w8_group_mma<CODE == kCodeE4M3>(codes, rows, r0, grp, reinterpret_cast<const uint2*>(bperm), d);
+}
+
 // Rows r0+g and r0+g+8 dotted with the activation over groups [grp0, grp1):
 // per group w = s*q + b, so the dot is s * (sum of q*value) + b * (sum of
 // values); `bsum` holds per-group sums of the stored B values (for the 1024
 // offset), `tsum` the true sums of the activation.
 // With one-byte codes a TMA box holds 2 groups (128 columns) instead of 4, and
 // `bperm` is read as 8-byte units.
+// `box_bars[i]` (if given) completes when groups [i*gpb, (i+1)*gpb) have landed.
 template <int CODE>
 MW4_DEV bool w4_gemv16(const uint8_t* codes, int rows, int r0, int grp0, int grp1, const uint4* bperm,
                        const float* bsum, const float* tsum, const uint16_t* sc, const uint16_t* bi, int ngrp_row,
-                       float& acc0, float& acc1, uint64_t* box_bars, volatile int* abort_flag, unsigned int* status) {
+                       float& acc0, float& acc1, uint64_t* box_bars, int gpb, volatile int* abort_flag,
+                       unsigned int* status) {
     const int lane = threadIdx.x & 31, g = lane >> 2;
     constexpr int kIn = 4;   // groups in flight: independent MMA chains
-    constexpr int kGpb = CODE == kCodeU4 ? 4 : 2;   // groups per TMA box
     for (int grp = grp0; grp < grp1; grp += kIn) {
         if (box_bars) {
             for (int q = 0; q < kIn; ++q)
-                if (grp + q < grp1 && ((grp + q) % kGpb) == 0 || (q == 0 && grp + q < grp1))
-                    if (!mbar_wait(&box_bars[(grp + q) / kGpb], 0, abort_flag, status)) return false;
+                if (grp + q < grp1 && ((grp + q) % gpb) == 0 || (q == 0 && grp + q < grp1))
+                    if (!mbar_wait(&box_bars[(grp + q) / gpb], 0, abort_flag, status)) return false;
         }
         float d[kIn][4];
 #pragma unroll
         for (int q = 0; q < kIn; ++q) {
             d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
-            if (grp + q < grp1) {
-                if (CODE == kCodeU4)
-                    w4_group_mma(codes, rows, r0, grp + q, bperm, d[q]);
-                else
-                    w8_group_mma<CODE == kCodeE4M3>(codes, rows, r0, grp + q, reinterpret_cast<const uint2*>(bperm),
-                                                    d[q]);
-            }
+            if (grp + q < grp1) group_mma<CODE>(codes, rows, r0, grp + q, bperm, d[q]);
         }
         // every lane of a row group holds the same column sums (B is the same for all n)
 #pragma unroll
@@ -280,6 +359,52 @@ MW4_DEV bool w4_gemv16(const uint8_t* codes, int rows, int r0, int grp0, int grp
     return true;
 }
 
+// The four B-operand words of 8 consecutive activation values v[0..7] (an
+// entry of 16 bytes): 4-bit codes (v0, v4), (v1, v5)/16, (v2, v6), (v3, v7)/16;
+// one-byte codes the 4-column units (v0, v2), (v1, v3), (v4, v6), (v5, v7).
+template <int CODE>
+MW4_DEV uint32_t b_word(const float (&v)[8], int m) {
+    if (CODE == kCodeU4) {
+        const int a = m >> 1 ? 2 : 0, o = m & 1;   // m: 0 -> (0,4), 1 -> (1,5)/16, 2 -> (2,6), 3 -> (3,7)/16
+        const float sc = o ? 0.0625f : 1.0f;
+        return h2_as_u32(__floats2half2_rn(v[a + o] * sc, v[a + o + 4] * sc));
+    }
+    const int b = (m >> 1) * 4 + (m & 1);   // m: 0 -> (0,2), 1 -> (1,3), 2 -> (4,6), 3 -> (5,7)
+    return h2_as_u32(__floats2half2_rn(v[b], v[b + 2]));
+}
+
+// Group sums of one 16-byte B entry as stored: `sb` of the pairs that carry
+// the 1024 offset unscaled, `so` of the pairs divided by 16 (4-bit codes).
+template <int CODE>
+MW4_DEV void b_entry_sums(const uint4& q, float& sb, float& so) {
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(u32_as_h2(u[j]));
+        if (CODE == kCodeU4 && (j & 1)) so += f.x + f.y; else sb += f.x + f.y;
+    }
+}
+
+// 3-D tiled load: code rows seen as [box column][row][32 words], so that one copy
+// brings several 128-byte box columns of a row slice (each landing as a 2-D box
+// of `rows` x 128 bytes, one after the other); c2 is the first box column.
+MW4_DEV void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bounded wait on an mbarrier phase that ignores the abort flag: used before
+// exit so that no TMA copy of this CTA is still in flight when it leaves.
+static __device__ __noinline__ void mbar_drain(uint64_t* bar) {
+    if (mbar_try_wait(bar, 0)) return;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, 0))
+        if (globaltimer() - t0 > kWaitLimitNs) return;
+}
+
 // Shape parameters given at compile time (kH, kI, kE, kK non-zero) fold the
 // GEMVs' shared-memory address arithmetic into constants: measured 1.6x faster
 // for the dot-product loops than the same code with run-time strides.  The
@@ -292,8 +417,8 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
                     const __grid_constant__ CUtensorMap msd) {
     const int H = kH ? kH : a.H, E = kE ? kE : a.E, I = kI ? kI : a.I, k = kK ? kK : a.k;
     constexpr int kBits = CODE == kCodeU4 ? 4 : 8;
-    const FusedSmem L(H, E, I, kBits);
-    const int RG = L.RG, RD = L.RD;
+    const FusedSmem L(H, E, I, k, kBits);
+    const int RG = L.RG, DR = L.DR, NS = L.NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* gcodes = sm + L.gcodes;
@@ -305,446 +430,553 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     uint32_t* xperm = reinterpret_cast<uint32_t*>(sm + L.xperm);
     float* xsum = reinterpret_cast<float*>(sm + L.xsum);
     float* xbs = reinterpret_cast<float*>(sm + L.xbs);
-    float* part = reinterpret_cast<float*>(sm + L.part);
     float* logits = reinterpret_cast<float*>(sm + L.logits);
+    float* gred = reinterpret_cast<float*>(sm + L.gred);
     float* gsum = reinterpret_cast<float*>(sm + L.gsum);
     float* usum = reinterpret_cast<float*>(sm + L.usum);
-    uint32_t* hperm = reinterpret_cast<uint32_t*>(sm + L.hperm);
+    float* wred = reinterpret_cast<float*>(sm + L.wred);
+    uint32_t* hperm = reinterpret_cast<uint32_t*>(sm + L.hperm);   // after the gate/up GEMV
     float* hsum = reinterpret_cast<float*>(sm + L.hsum);
+    float* hpiece = reinterpret_cast<float*>(sm + L.hpiece);
     float* hbs = reinterpret_cast<float*>(sm + L.hbs);
-    float* red = reinterpret_cast<float*>(sm + L.red);
+    float* dred = reinterpret_cast<float*>(sm + L.dred);
     uint8_t* misc = sm + L.misc;
-    // TMA boxes of 128-byte code rows: 256 columns of 4-bit codes, 128 of one-byte codes
-    const int nbox_gu = H * kBits / 1024, nbox_dn = I * kBits / 1024 > 0 ? I * kBits / 1024 : 1;
-    uint64_t* bar_gu = reinterpret_cast<uint64_t*>(misc);               // [nbox_gu] (<= 16)
-    uint64_t* bar_dn = bar_gu + 16;                                      // [1]
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_dn + 1);
-    int* sel_e = reinterpret_cast<int*>(bar_dn + 2);                     // selected expert of this cluster
-    float* sel_w = reinterpret_cast<float*>(sel_e + 1);                  // its weight (or gamma)
-    uint32_t* xtag_s = reinterpret_cast<uint32_t*>(sel_e + 3);            // this call's exchange tag
-    uint32_t* xinj_s = reinterpret_cast<uint32_t*>(sel_e + 4);            // test hook: skip a publish
+    // TMA boxes of 128-byte code rows: 256 columns of 4-bit codes, 128 of one-byte codes.
+    // Gate/up slices come in two halves of their box columns (one 3-D copy per matrix
+    // and half, one barrier per half), each slot's down rows in one 3-D copy.
+    const int nbox_gu = H * kBits / 1024, nbox_dn = I * kBits / 1024;
+    uint64_t* bar_gu = reinterpret_cast<uint64_t*>(misc);               // [2] halves of the gate/up slices
+    uint64_t* bar_dn = bar_gu + 2;                                       // routed down rows
+    uint64_t* bar_dsh = bar_dn + 1;                                      // shared expert's down rows
+    uint64_t* bar_sb = bar_dsh + 1;                                      // gate/up scales, biases (warp 0's cp.async)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_sb + 1);
+    int* sel_e = reinterpret_cast<int*>(bar_sb + 2);                     // [kMaxSlots] selected experts
+    float* sel_w = reinterpret_cast<float*>(sel_e + kMaxSlots);          // [kMaxSlots] weights (slot k: gamma)
+    uint32_t* xtag_s = reinterpret_cast<uint32_t*>(sel_w + kMaxSlots);   // this call's exchange tag
+    uint32_t* xinj_s = xtag_s + 1;                                       // test hook: skip a publish
+    int* issued = reinterpret_cast<int*>(xtag_s + 2);   // bits: 0 gate/up codes, 1 down, 2 shared down, 3 gate/up s, b
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // clusters are consecutive blocks: expert slot = block / kPE, CTA ei of the
-    // expert = block % kPE; cluster cid, rank inside the cluster for DSMEM
-    const int rank = (int)cluster_rank(), cid = (int)cluster_id();
     const int G = blockIdx.x, slot = G / kPE, ei = G % kPE;
-    const int NC = k + 1, NG = NC * kPE, NCL = NC * kFusedClustersPerExpert;
-    const bool shared_cluster = (slot == k);
+    const int NG = NS * kPE, NR = k * kPE;        // all CTAs; routed CTAs (also the down CTAs)
+    const bool shared_cta = (slot == k);
+    const bool down_cta = G < NR;
     unsigned int* status = &a.ctrl->status;
+    // Router: with EG = E/8 groups of 8 experts and RS = NR/EG splits of the H rows,
+    // CTA G < EG*RS sums experts [eg*8, eg*8+8) over rows [rs*H/RS, (rs+1)*H/RS)
+    // (eg = G % EG, rs = G / EG): one full 32-byte sector per W_r row it reads.
+    const int EG = E / kRE, RS = NR / EG, r_rows = H / RS;
+    const bool router_cta = G < EG * RS;
+    const int r_eg = G % EG, r_rs = G / EG;
+    constexpr int kRPT = (kH && kE && kK) ? (kH / ((kK * kPE) / (kE / kRE)) + kFThreads - 1) / kFThreads
+                                          : kMaxRouterRows;   // router rows per thread
+    constexpr int kGPT = kH ? (kH + kFThreads - 1) / kFThreads : 8;   // shared-gate rows per thread
+    const int gdrow_sh = G * DR;                  // this CTA's down rows (routed CTAs)
+    const int dchunks = DR * (I / 64) * 2 / 16;   // 16-byte pieces of one slot's down scales (or biases)
 
+    // The barriers first: their initialisation is published with a release fence,
+    // which must not wait for the router loads below.
+    if (tid == 0) {
+        mbar_init(&bar_gu[0], 1);
+        mbar_init(&bar_gu[1], 1);
+        mbar_init(bar_dn, 1);
+        mbar_init(bar_dsh, 1);
+        mbar_init(bar_sb, 1);
+        *abort_flag = 0;
+        *issued = 0;
+        fence_mbar_init();
+    }
     // The kernel may start before the previous kernel on the stream has finished
     // (programmatic dependent launch): until griddep_wait() it touches only
     // weights, its own shared memory and the tensor maps.
-    // The router's loads go out first: thread (e, half) sums half of this CTA's
-    // slice of the H rows for expert e; its W_r column slice is requested before
-    // the wait, the matching x values (the same for the whole warp) after it.
-    const int rh0 = (int)((long)G * H / NG), rh1 = (int)((long)(G + 1) * H / NG);
-    const int rnh = rh1 - rh0, rhalf = rnh / 2;
-    const int r_e = tid % E, r_hb = (tid / E) ? rhalf : 0, r_he = (tid / E) ? rnh : rhalf;
-    float rw[32], rx[32];
-    if (tid < 2 * E) {
+    // Router weights first: thread t holds row r_rs*H/RS + t (+ kFThreads, ...) of W_r
+    // for the CTA's 8 experts, and the shared gate at rows t, t + kFThreads, ...
+    // The loads are unconditional (row indices clamped into range, the surplus
+    // rows' x taken as 0 later), so that nothing before griddep_wait() waits on them.
+    float rw[kRPT][kRE], rg[kGPT];
+    if (router_cta) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const bool in = r_hb + j < r_he;
-            rw[j] = in ? __ldg(a.router_w + (size_t)(rh0 + r_hb + j) * E + r_e) : 0.f;
+        for (int i = 0; i < kRPT; ++i) {
+            const int h = min(r_rs * r_rows + min(tid + i * kFThreads, r_rows - 1), H - 1);
+            const float4* src = reinterpret_cast<const float4*>(a.router_w + (size_t)h * E + r_eg * kRE);
+            const float4 w0 = __ldg(src), w1 = __ldg(src + 1);
+            rw[i][0] = w0.x; rw[i][1] = w0.y; rw[i][2] = w0.z; rw[i][3] = w0.w;
+            rw[i][4] = w1.x; rw[i][5] = w1.y; rw[i][6] = w1.z; rw[i][7] = w1.w;
+        }
+    }
+    float rbias[8];   // warp 0 of a routed CTA: the router bias of experts lane + 32 i
+    if (down_cta) {
+#pragma unroll
+        for (int i = 0; i < kGPT; ++i) rg[i] = __ldg(a.shared_gate + min(tid + i * kFThreads, H - 1));
+        if (warp == 0 && a.router_bias) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rbias[i] = __ldg(a.router_bias + min(lane + 32 * i, E - 1));
         }
     }
     if (tid == 32) {   // the descriptors are fetched once, early, off the critical path
         prefetch_tensormap(&mg); prefetch_tensormap(&mu); prefetch_tensormap(&md);
         prefetch_tensormap(&msg); prefetch_tensormap(&msu); prefetch_tensormap(&msd);
     }
-    if (tid == 0) {
-        for (int b = 0; b < nbox_gu; ++b) mbar_init(&bar_gu[b], 1);
-        mbar_init(bar_dn, 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    griddep_wait();   // from here on: x, the workspace and its counters
-    // Values crossing CTAs carry this call's tag (the call counter + 1): a reader
-    // polls the data itself instead of a counter and then the data.  CTA 0 advances
-    // the counter once every cluster's router sum carries the tag, i.e. once every
-    // CTA has read it.
-    if (tid == 0) {
-        *xtag_s = ld_acquire_u32(&a.ctrl->pad[kCtrlEpochWord]) + 1u;
-        *xinj_s = ld_acquire_u32(&a.ctrl->pad[kCtrlInjectWord]);
-    }
-    if (tid < 2 * E) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) rx[j] = (r_hb + j < r_he) ? bf16_bits_to_float(__ldg(a.x + rh0 + r_hb + j)) : 0.f;
-    }
+    __syncthreads();
 
-    // ---------------------------------------------------------------- weight loads (routed: after the top-k)
-    // called by all 32 lanes of warp 0
-    auto issue_loads = [&](int e) {
+    // ---------------------------------------------------------------- weight loads
+    // gate/up code slices of expert e (E = the shared expert), by one thread: two
+    // halves of the box columns, each half of gate and of up on one barrier
+    auto issue_gateup = [&](int e) {
         const bool sh = (e >= E);
-        const CUtensorMap* MG = sh ? &msg : &mg;
-        const CUtensorMap* MU = sh ? &msu : &mu;
-        const CUtensorMap* MD = sh ? &msd : &md;
         const int grow = (sh ? 0 : e * I) + ei * RG;
-        const int drow = (sh ? 0 : e * H) + ei * RD;
-        const uint32_t gsz = RG * (H / 64) * 2, dsz = RD * (I / 64) * 2;
-        const size_t go = (size_t)grow * (H / 64), dO = (size_t)drow * (I / 64);
-        // in the order the GEMVs consume them: the gate/up scales and biases (box 0's
-        // barrier waits for them too), then gate and up of box 0, of box 1, ..., then down
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bar_gu[0], 2u * RG * 128 + 4 * gsz);
-            bulk_load(gsb, (sh ? a.sgs : a.gs) + go, gsz, &bar_gu[0]);
-            bulk_load(gsb + RG * (H / 64), (sh ? a.sgb : a.gb) + go, gsz, &bar_gu[0]);
-            bulk_load(usb, (sh ? a.sus : a.us) + go, gsz, &bar_gu[0]);
-            bulk_load(usb + RG * (H / 64), (sh ? a.sub : a.ub) + go, gsz, &bar_gu[0]);
-        }
-        __syncwarp();
-        for (int p = lane; p < 2 * nbox_gu; p += 32) {   // p = 2 box + matrix
-            const int b = p >> 1;
-            if ((p & 1) == 0 && b != 0) mbar_arrive_expect_tx(&bar_gu[b], 2u * RG * 128);
-            __syncwarp(__activemask());
-            tma_load_2d(((p & 1) ? ucodes : gcodes) + (size_t)b * RG * 128, (p & 1) ? MU : MG, b * 32, grow,
-                        &bar_gu[b]);
-        }
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bar_dn, (uint32_t)RD * (I * kBits / 8) + 2 * dsz);
-            for (int b = 0; b < nbox_dn; ++b) tma_load_2d(dcodes + (size_t)b * RD * 128, MD, b * 32, drow, bar_dn);
-            bulk_load(dsb, (sh ? a.sds : a.ds) + dO, dsz, bar_dn);
-            bulk_load(dsb + RD * (I / 64), (sh ? a.sdb : a.db) + dO, dsz, bar_dn);
+        const int hb = nbox_gu / 2;
+        const uint32_t gsz = RG * (H / 64) * 2;   // one scale (or bias) slice
+        const size_t go = (size_t)grow * (H / 64);
+        mbar_arrive_expect_tx(bar_sb, 4 * gsz);
+        bulk_load(gsb, (sh ? a.sgs : a.gs) + go, gsz, bar_sb);
+        bulk_load(gsb + RG * (H / 64), (sh ? a.sgb : a.gb) + go, gsz, bar_sb);
+        bulk_load(usb, (sh ? a.sus : a.us) + go, gsz, bar_sb);
+        bulk_load(usb + RG * (H / 64), (sh ? a.sub : a.ub) + go, gsz, bar_sb);
+        for (int h = 0; h < 2; ++h) {
+            mbar_arrive_expect_tx(&bar_gu[h], 2u * hb * RG * 128);
+            tma_load_3d(gcodes + (size_t)h * hb * RG * 128, sh ? &msg : &mg, 0, grow, h * hb, &bar_gu[h]);
+            tma_load_3d(ucodes + (size_t)h * hb * RG * 128, sh ? &msu : &mu, 0, grow, h * hb, &bar_gu[h]);
         }
     };
-
-    // ---------------------------------------------------------------- 1. router partial sums
-    if (tid < 2 * E) {
-        float sum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sum = fmaf(rx[j], rw[j], sum);
-        (tid / E ? logits : part)[r_e] = sum;
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += kFThreads) part[e] += logits[e];
-    __syncthreads();
-    cluster_sync();
-    {   // cluster sum of the partials, ranks in order; CTA r reduces experts [r*E/kCS, (r+1)*E/kCS)
-        const int e0 = rank * E / kCS, e1 = (rank + 1) * E / kCS;
-        for (int e = e0 + tid; e < e1; e += kFThreads) {
-            float v[kCS];
-#pragma unroll
-            for (int r = 0; r < kCS; ++r) v[r] = ld_dsmem_f32(part + e, r);
-            float s = 0.f;
-#pragma unroll
-            for (int r = 0; r < kCS; ++r) s += v[r];
-            if (!(*xinj_s != 0u && cid == 0)) st_tagged(a.cpart + (size_t)cid * E + e, s, *xtag_s);
-        }
-    }
-    // the shared expert needs no routing: its loads start once its router sums are
-    // published, so that issuing them does not delay the exchange everyone waits on
-    if (shared_cluster && warp == 0) issue_loads(E);
-    // this CTA has read its peers' partials; the matching wait (every peer has read
-    // this CTA's, so the buffer may be reused) comes before the gate/up GEMV reuses it
-    cluster_arrive();
-    // x for the GEMVs is prepared here, off the router's critical path, while the
-    // other CTAs' router sums come in
-    // x as fp16 B fragments, one thread per 16-byte entry: for 4-bit codes
-    // entry i (32-column block i/4, lane%4 = i%4) holds {x[8i], x[8i+4]},
-    // {x[8i+1], x[8i+5]}/16, {x[8i+2], x[8i+6]}, {x[8i+3], x[8i+7]}/16; for
-    // one-byte codes {x[8i], x[8i+2]}, {x[8i+1], x[8i+3]}, {x[8i+4], x[8i+6]},
-    // {x[8i+5], x[8i+7]} (the 4-column units 2i and 2i+1); plus the per-64-column group
-    // sums of the stored values (xbs) and of the values the products use
-    // (xsum), reduced over the 8 lanes of a group (H/8 is a multiple of 32, so
-    // the loop runs whole warps)
-    for (int i = tid; i < H / 8; i += kFThreads) {
-        const uint4 v = *reinterpret_cast<const uint4*>(a.x + i * 8);
-        const uint32_t e[4] = {v.x, v.y, v.z, v.w};   // pairs (0,1) (2,3) (4,5) (6,7)
-        float f[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[2 * j] = __uint_as_float(e[j] << 16);
-            f[2 * j + 1] = __uint_as_float(e[j] & 0xFFFF0000u);
-        }
-        float sb = 0.f, so = 0.f;   // sums of the stored even / odd entries
-        bool bad = false;
-        uint32_t q[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            bad |= !(fabsf(f[j]) <= 65504.f) || !(fabsf(f[j + 4]) <= 65504.f);
-            __half2 h2;
-            if (CODE == kCodeU4) {
-                const float m = (j & 1) ? 0.0625f : 1.0f;
-                h2 = __floats2half2_rn(f[j] * m, f[j + 4] * m);
-            } else {   // 4-column units (x[4u], x[4u+2]), (x[4u+1], x[4u+3])
-                const int b = (j >> 1) * 4 + (j & 1);
-                h2 = __floats2half2_rn(f[b], f[b + 2]);
-            }
-            q[j] = h2_as_u32(h2);
-            const float2 back = __half22float2(h2);
-            if (CODE == kCodeU4 && (j & 1)) so += back.x + back.y; else sb += back.x + back.y;
-        }
-        reinterpret_cast<uint4*>(xperm)[i] = make_uint4(q[0], q[1], q[2], q[3]);
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1) {
-            sb += __shfl_xor_sync(0xffffffffu, sb, off);
-            so += __shfl_xor_sync(0xffffffffu, so, off);
-        }
-        if ((i & 7) == 0) {   // E4M3 products carry no 1024 offset
-            xbs[i / 8] = CODE == kCodeE4M3 ? 0.f : sb + so;
-            xsum[i / 8] = sb + 16.f * so;
-        }
-        if (bad) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
-    }
-    __syncthreads();
-    if (shared_cluster) {   // the shared cluster's gate sigmoid(x . g), all threads
-        float d = 0.f;
-        for (int h = tid * 8; h < H; h += kFThreads * 8) {
-            const uint4 v = *reinterpret_cast<const uint4*>(a.x + h);
-            const float4 g0 = *reinterpret_cast<const float4*>(a.shared_gate + h);
-            const float4 g1 = *reinterpret_cast<const float4*>(a.shared_gate + h + 4);
-            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                d = fmaf(__uint_as_float(u[j] << 16), gg[2 * j], d);
-                d = fmaf(__uint_as_float(u[j] & 0xFFFF0000u), gg[2 * j + 1], d);
-            }
-        }
-        d = warp_sum(d);
-        if (lane == 0) gsum[warp] = d;   // gsum is free until the gate/up GEMV
-        __syncthreads();
+    // down code rows [G*DR, (G+1)*DR) of expert e into slot j's region, by one thread
+    auto issue_down = [&](int j, int e, uint64_t* bar) {
+        const int drow = (e >= E ? 0 : e * H) + gdrow_sh;
+        tma_load_3d(dcodes + (size_t)j * L.dslot, e >= E ? &msd : &md, 0, drow, 0, bar);
+    };
+    // the down rows' scales and biases by cp.async, one 16-byte piece per call:
+    // piece c of slot j's down rows of expert e (2 dchunks: s, b)
+    auto sb_down = [&](int j, int e, int c) {
+        const bool sh = (e >= E);
+        const size_t dO = (size_t)((sh ? 0 : e * H) + gdrow_sh) * (I / 64);
+        const int arr = c / dchunks, o = (c % dchunks) * 8;
+        const uint16_t* src = arr == 0 ? (sh ? a.sds : a.ds) : (sh ? a.sdb : a.db);
+        cp_async_16(dsb + (size_t)j * 2 * DR * (I / 64) + arr * DR * (I / 64) + o, src + dO + o);
+    };
+    const uint32_t dn_bytes = (uint32_t)DR * (I * kBits / 8);   // one slot's down code rows
+    if (shared_cta) {   // the shared expert needs no routing: its loads go out now
         if (tid == 0) {
-            float t = 0.f;
-            for (int w = 0; w < kFWarps; ++w) t += gsum[w];
-            *sel_w = 1.0f / (1.0f + expf(-t));
-            *sel_e = E;
-            if (ei == 0) *a.gamma_out = *sel_w;
+            issue_gateup(E);
+            *issued |= 1 | 8;
         }
+    } else {            // routed CTAs: their down rows of the shared expert
+        if (tid == 0) {
+            mbar_arrive_expect_tx(bar_dsh, dn_bytes);
+            issue_down(k, E, bar_dsh);
+            *issued |= 4;
+        }
+        for (int c = tid; c < 2 * dchunks; c += kFThreads) sb_down(k, E, c);
     }
-    if (!shared_cluster) {
-        // ------------------------------------------------------------ 1b. exchange, top-k
-        {
-            const uint32_t xtag = *xtag_s;
-            for (int e = tid; e < E; e += kFThreads) {   // cluster sums added in cluster order, all loads in flight
-                constexpr int kMaxCl = kMaxSlots * kFusedClustersPerExpert;
-                uint64_t v[kMaxCl];
-#pragma unroll
-                for (int j = 0; j < kMaxCl; ++j) v[j] = (j < NCL) ? ld_tagged(a.cpart + (size_t)j * E + e) : 0ull;
-                // re-read the sums that do not carry this call's tag yet (bounded)
-                const uint64_t t0 = globaltimer();
-                while (true) {
-                    bool all = true;
-#pragma unroll
-                    for (int j = 0; j < kMaxCl; ++j)
-                        if (j < NCL && tag_of(v[j]) != xtag) {
-                            all = false;
-                            v[j] = ld_tagged(a.cpart + (size_t)j * E + e);
-                        }
-                    if (all) break;
-                    if (globaltimer() - t0 > kWaitLimitNs) {
-                        raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
-                        *abort_flag = 1;
-                        break;
-                    }
-                }
-                float s = 0.f;
-#pragma unroll
-                for (int j = 0; j < kMaxCl; ++j) s += (j < NCL) ? val_of(v[j]) : 0.f;
-                logits[e] = s + (a.router_bias ? a.router_bias[e] : 0.f);
-            }
-            __syncthreads();
-            // every cluster's sum carries the tag, so every CTA has read the counter
-            if (G == 0 && tid == 0 && !*abort_flag) a.ctrl->pad[kCtrlEpochWord] = xtag;
-        }
-        if (!*abort_flag) {
-            // one warp selects, weighs and issues the loads of this CTA's expert
-            if (warp == 0) {
-                int sidx;
-                float sval;
-                warp_topk_sorted<8>(logits, E, k, sidx, sval);
-                const int e = __shfl_sync(0xffffffffu, sidx, slot);
-                // the loads first: the routing weight is needed only by the down GEMV
-                if (e < 0 || e >= E) {
-                    if (lane == 0) { raise_status(status, MOE_W4_STATUS_BAD_INDEX); *abort_flag = 1; }
-                } else {
-                    issue_loads(e);
-                }
-                const float v0 = __shfl_sync(0xffffffffu, sval, 0);   // the largest selected score
-                const float ex = lane < k ? expf(sval - v0) : 0.f;
-                const float z = warp_sum(ex);
-                const float w = ex / z;   // softmax over the selection
-                const float we = __shfl_sync(0xffffffffu, w, slot);
-                if (lane == 0) { *sel_e = e; *sel_w = we; }
-                if (G == 0 && lane < k) { a.idx_out[lane] = sidx; a.w_out[lane] = w; }
-            }
-        }
-    }
-    __syncthreads();
-    const bool run = !*abort_flag;
+    cp_async_commit();
 
-    cluster_wait();   // every peer has read this CTA's partials: red (= part) may be written
-    // ---------------------------------------------------------------- 3. gate/up GEMV
-    // 2*RG/16 row tiles (gate, then up) x KS splits of the 64-column groups
-    // box 0 also carries the scales/biases; the block agrees on the outcome of the wait
-    const bool gu_ok = __syncthreads_and(run ? mbar_wait(&bar_gu[0], 0, abort_flag, status) : 0);
-    if (gu_ok) {
-        const int ntile = 2 * (RG / 16), KS = kFWarps / ntile > 0 ? kFWarps / ntile : 1, ngrp = H / 64;
-        for (int task = warp; task < ntile * KS; task += kFWarps) {
-            const int t = task / KS, ks = task % KS;
-            const bool up = t >= ntile / 2;
-            const int r0 = (up ? t - ntile / 2 : t) * 16;
-            const uint16_t* sb = up ? usb : gsb;
-            float acc0 = 0.f, acc1 = 0.f;
-            // split ks takes its share of each half of the columns, so that every warp
-            // starts on an early box and, once the last box lands, has one box left
-            const int half = ngrp / 2;
-            for (int hf = 0; hf < 2; ++hf)
-                w4_gemv16<CODE>(up ? ucodes : gcodes, RG, r0, hf * half + ks * half / KS, hf * half + (ks + 1) * half / KS,
-                          reinterpret_cast<const uint4*>(xperm), xbs, xsum, sb, sb + RG * (H / 64), H / 64, acc0, acc1,
-                          bar_gu, abort_flag, status);
-            if ((lane & 3) == 0) {
-                red[task * 16 + (lane >> 2)] = acc0;
-                red[task * 16 + (lane >> 2) + 8] = acc1;
+    griddep_wait();   // from here on: x, the workspace and its counters
+    // Values crossing CTAs carry this call's tag (the call counter + 1, never 0):
+    // a reader polls the data itself.  The counter advances once a routed CTA has
+    // seen every slot's h with the tag (so every CTA has read the counter), or
+    // when a CTA gives up.
+    if (tid == 0) {
+        uint32_t t = ld_acquire_u32(&a.ctrl->pad[kCtrlEpochWord]) + 1u;
+        *xtag_s = t ? t : 1u;
+        *xinj_s = ld_acquire_u32(&a.ctrl->pad[kCtrlInjectWord]);
+    }
+
+    // ---------------------------------------------------------------- 1. router partial scores and the shared gate
+    if (down_cta) {
+        float acc[kRE + 1];
+#pragma unroll
+        for (int c = 0; c <= kRE; ++c) acc[c] = 0.f;
+        if (router_cta) {
+#pragma unroll
+            for (int i = 0; i < kRPT; ++i) {
+                const int hr = tid + i * kFThreads;
+                const float xv = hr < r_rows ? bf16_bits_to_float(__ldg(a.x + r_rs * r_rows + hr)) : 0.f;
+#pragma unroll
+                for (int c = 0; c < kRE; ++c) acc[c] = fmaf(xv, rw[i][c], acc[c]);
             }
         }
-        __syncthreads();
-        for (int i = tid; i < 2 * RG; i += kFThreads) {   // sum the K splits in order
-            const int t = i / 16, r = i % 16;
-            float v = 0.f;
-            for (int ks = 0; ks < KS; ++ks) v += red[(t * KS + ks) * 16 + r];
-            (t < ntile / 2 ? gsum : usum)[(t % (ntile / 2)) * 16 + r] = v;
+#pragma unroll
+        for (int i = 0; i < kGPT; ++i) {
+            const int h = tid + i * kFThreads;
+            const float xv = h < H ? bf16_bits_to_float(__ldg(a.x + h)) : 0.f;
+            acc[kRE] = fmaf(xv, rg[i], acc[kRE]);
+        }
+#pragma unroll
+        for (int c = 0; c <= kRE; ++c) {
+            const float v = warp_sum(acc[c]);
+            if (lane == 0) wred[warp * (kRE + 1) + c] = v;
         }
     }
     __syncthreads();
-    // ---------------------------------------------------------------- 4. h through global memory
-    // this CTA's slice of h, tagged; published even after an abort (as zeros), so
-    // that no CTA of the expert waits in vain
-    {
-        const uint32_t xtag = *xtag_s;
-        for (int i = tid; i < RG; i += kFThreads)
-            st_tagged(a.hx + (size_t)slot * I + ei * RG + i, gu_ok ? silu_f(gsum[i]) * usum[i] : 0.f, xtag);
+    const uint32_t xtag = *xtag_s;
+    if (down_cta && tid <= kRE * kScoreReplicas) {
+        // block sums in warp order: the 8 partial scores, each published to every
+        // replica (thread c + 8 r: expert c, replica r), and the shared gate
+        const int c = tid < kRE * kScoreReplicas ? tid % kRE : kRE;
+        float sum = 0.f;
+        for (int w = 0; w < kFWarps; ++w) sum += wred[w * (kRE + 1) + c];
+        if (c == kRE) {
+            sel_w[k] = 1.0f / (1.0f + expf(-sum));
+            if (G == 0) *a.gamma_out = sel_w[k];
+        } else if (router_cta && !(*xinj_s != 0u && G == 0)) {
+            const int r = tid / kRE;
+            st_tagged(a.scores + ((size_t)r * RS + r_rs) * E + r_eg * kRE + c, sum, xtag);
+        }
     }
-    const bool h_in = gu_ok && !*abort_flag;
-    if (h_in) {
-        // fp16 B fragments of h, laid out like x, once all 16 slices carry this
-        // call's tag
-        const uint32_t xtag = *xtag_s;
-        for (int i = tid; i < I / 8; i += kFThreads) {
-            const uint64_t* src = a.hx + (size_t)slot * I + i * 8;
-            uint64_t w[8];
+
+    // ---------------------------------------------------------------- 2. scores in, top-k, loads (routed CTAs)
+    // warps 0 .. RS-1 each poll one row split's partials of all E experts in this
+    // CTA's replica (bounded wait) and leave them in shared memory; warp 0 then adds
+    // them in split order, selects the top-k and issues the loads
+    if (!shared_cta && warp < RS) {
+        constexpr int kNV = 8;   // E <= 256 scores: lane l holds experts l + 32 i
+        const uint64_t* src = a.scores + ((size_t)(G % kScoreReplicas) * RS + warp) * E;
+        uint64_t v[kNV];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) w[j] = ld_tagged(src + j);
-            const uint64_t t0 = globaltimer();
-            while (true) {
-                bool all = true;
+        for (int i = 0; i < kNV; ++i) v[i] = (lane + 32 * i < E) ? ld_tagged(src + lane + 32 * i) : 0ull;
+        const uint64_t t0 = globaltimer();
+        bool ok = true;
+        for (int it = 1;; ++it) {
+            bool all = true;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (tag_of(w[j]) != xtag) {
-                        all = false;
-                        w[j] = ld_tagged(src + j);
-                    }
-                if (all) break;
-                if (globaltimer() - t0 > kWaitLimitNs) {
-                    raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
-                    *abort_flag = 1;
-                    break;
+            for (int i = 0; i < kNV; ++i)
+                if (lane + 32 * i < E && tag_of(v[i]) != xtag) {
+                    all = false;
+                    v[i] = ld_tagged(src + lane + 32 * i);
+                }
+            if (__all_sync(0xffffffffu, all)) break;
+            if ((it & 15) == 0 && globaltimer() - t0 > kWaitLimitNs) { ok = false; break; }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) { raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT); *abort_flag = 1; }
+        } else {
+            float* part = gred + warp * E;   // gred is free until the gate/up GEMV
+#pragma unroll
+            for (int i = 0; i < kNV; ++i)
+                if (lane + 32 * i < E) part[lane + 32 * i] = val_of(v[i]);
+        }
+        asm volatile("bar.sync 1, %0;" :: "r"(RS * 32) : "memory");   // the polling warps only
+    }
+    int rsel = -1;      // warp 0 of a routed CTA: lane j < k holds the j-th selection
+    float rval = 0.f;   // and its score
+    if (!shared_cta && warp == 0) {
+        if (!*abort_flag) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) {
+                    float sum = 0.f;
+                    for (int r = 0; r < RS; ++r) sum += gred[r * E + e];
+                    logits[e] = sum + (a.router_bias ? rbias[i] : 0.f);
                 }
             }
-            float v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = val_of(w[j]);
+            __syncwarp();
+            int sidx;
+            float sval;
+            warp_topk_sorted<8>(logits, E, k, sidx, sval);
+            const bool bad = __any_sync(0xffffffffu, lane < k && (sidx < 0 || sidx >= E));
+            if (bad) {
+                if (lane == 0) { raise_status(status, MOE_W4_STATUS_BAD_INDEX); *abort_flag = 1; }
+            } else {
+                // what the gate/up GEMV needs first: its code slices and their scales
+                // and biases; the down rows and the routing weights follow once the
+                // block has the selection
+                const int e_mine = __shfl_sync(0xffffffffu, sidx, slot);
+                if (lane == 0) {
+                    issue_gateup(e_mine);
+                    *issued |= 1 | 8;
+                }
+                if (lane < k) sel_e[lane] = sidx;
+                rsel = sidx;
+                rval = sval;
+            }
+        }
+    }
+    if (shared_cta || warp >= RS) {
+        // x as fp16 B fragments, one thread per 16-byte entry (entry i holds the B
+        // words of x[8i .. 8i+7], b_word), plus the per-64-column group sums of the
+        // stored values (xbs) and of the values the products use (xsum), reduced
+        // over the 8 lanes of a group.  Routed CTAs: the warps that do not poll the
+        // scores (H/8 is a multiple of 32, so every warp runs whole iterations).
+        const int t0 = shared_cta ? tid : tid - 32 * RS, nt = shared_cta ? kFThreads : kFThreads - 32 * RS;
+        for (int i = t0; i < H / 8; i += nt) {
+            const uint4 q = *reinterpret_cast<const uint4*>(a.x + i * 8);
+            const uint32_t e[4] = {q.x, q.y, q.z, q.w};   // pairs (0,1) (2,3) (4,5) (6,7)
+            float f[8];
             bool bad = false;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) bad |= !(fabsf(v[j]) <= 65504.f);
-            if (bad) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
-            uint32_t q0, q1, q2, q3;
-            if (CODE == kCodeU4) {
-                q0 = h2_as_u32(__floats2half2_rn(v[0], v[4]));
-                q1 = h2_as_u32(__floats2half2_rn(v[1] * 0.0625f, v[5] * 0.0625f));
-                q2 = h2_as_u32(__floats2half2_rn(v[2], v[6]));
-                q3 = h2_as_u32(__floats2half2_rn(v[3] * 0.0625f, v[7] * 0.0625f));
-            } else {   // 4-column units, as for x
-                q0 = h2_as_u32(__floats2half2_rn(v[0], v[2]));
-                q1 = h2_as_u32(__floats2half2_rn(v[1], v[3]));
-                q2 = h2_as_u32(__floats2half2_rn(v[4], v[6]));
-                q3 = h2_as_u32(__floats2half2_rn(v[5], v[7]));
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] = __uint_as_float(e[j] << 16);
+                f[2 * j + 1] = __uint_as_float(e[j] & 0xFFFF0000u);
             }
-            reinterpret_cast<uint4*>(hperm)[i] = make_uint4(q0, q1, q2, q3);
-        }
-    }
-    __syncthreads();
-    const bool h_ok = h_in && !*abort_flag;
-    if (h_ok) {   // per-64-value group sums of h: one warp per group, lanes 0..7 one 8-value entry each
-        for (int gi = warp; gi < I / 64; gi += kFWarps) {
-            float sb = 0.f, so = 0.f;
-            if (lane < 8) {
-                const uint4 q = reinterpret_cast<const uint4*>(hperm)[gi * 8 + lane];
-                const uint32_t u[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 f = __half22float2(u32_as_h2(u[j]));
-                    if (CODE == kCodeU4 && (j & 1)) so += f.x + f.y; else sb += f.x + f.y;
-                }
-            }
+            for (int j = 0; j < 8; ++j) bad |= !(fabsf(f[j]) <= 65504.f);
+            const uint4 o = make_uint4(b_word<CODE>(f, 0), b_word<CODE>(f, 1), b_word<CODE>(f, 2), b_word<CODE>(f, 3));
+            reinterpret_cast<uint4*>(xperm)[i] = o;
+            float sb = 0.f, so = 0.f;
+            b_entry_sums<CODE>(o, sb, so);
 #pragma unroll
             for (int off = 1; off < 8; off <<= 1) {
                 sb += __shfl_xor_sync(0xffffffffu, sb, off);
                 so += __shfl_xor_sync(0xffffffffu, so, off);
             }
-            if (lane == 0) {
-                hbs[gi] = CODE == kCodeE4M3 ? 0.f : sb + so;   // E4M3 products carry no 1024 offset
-                hsum[gi] = sb + 16.f * so;
+            if ((i & 7) == 0) {   // E4M3 products carry no 1024 offset
+                xbs[i / 8] = CODE == kCodeE4M3 ? 0.f : sb + so;
+                xsum[i / 8] = sb + 16.f * so;
             }
+            if (bad) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
         }
     }
-    // ---------------------------------------------------------------- 5. down GEMV
+    __syncthreads();
+    const bool run = !*abort_flag;
+    if (!shared_cta && run) {
+        if (warp == 0) {   // the selected experts' down rows, then the routing weights
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar_dn, (uint32_t)k * dn_bytes);
+                *issued |= 2;
+            }
+#pragma unroll 1
+            for (int j = 0; j < k; ++j) {
+                const int e = __shfl_sync(0xffffffffu, rsel, j);
+                if (lane == 0) issue_down(j, e, bar_dn);
+            }
+            const float v0 = __shfl_sync(0xffffffffu, rval, 0);   // the largest selected score
+            const float ex = lane < k ? expf(rval - v0) : 0.f;
+            const float z = warp_sum(ex);
+            const float w = ex / z;   // softmax over the selection
+            if (lane < k) sel_w[lane] = w;
+            if (G == 0 && lane < k) { a.idx_out[lane] = rsel; a.w_out[lane] = w; }
+        } else {           // the other warps: the down rows' scales and biases
+            const int ndn = k * 2 * dchunks;
+#pragma unroll 1
+            for (int c = tid - 32; c < ndn; c += kFThreads - 32)
+                sb_down(c / (2 * dchunks), sel_e[c / (2 * dchunks)], c % (2 * dchunks));
+        }
+    }
+    cp_async_commit();
     griddep_launch_dependents();   // the next kernel on the stream may start its prologue
-    // RD/16 row tiles x KS splits of the 64-column groups
-    const bool dn_ok = __syncthreads_and(h_ok ? mbar_wait(bar_dn, 0, abort_flag, status) : 0);
-    const uint32_t xtag = *xtag_s;
-    if (dn_ok) {
-        const int ntile = RD / 16, KS = kFWarps / ntile > 0 ? kFWarps / ntile : 1, ngrp = I / 64;
-        for (int task = warp; task < ntile * KS; task += kFWarps) {
-            const int t = task / KS, ks = task % KS;
-            float acc0 = 0.f, acc1 = 0.f;
-            w4_gemv16<CODE>(dcodes, RD, t * 16, ks * ngrp / KS, (ks + 1) * ngrp / KS, reinterpret_cast<const uint4*>(hperm),
-                      hbs, hsum, dsb, dsb + RD * (I / 64), I / 64, acc0, acc1, nullptr, abort_flag, status);
+
+    // ---------------------------------------------------------------- 3. gate/up GEMV
+    // 2*RG/16 row tiles (gate, then up) x KS splits of the 64-column groups
+    // box 0 also carries the scales/biases; the block agrees on the outcome of the wait
+    const bool gu_ok = __syncthreads_and(run ? mbar_wait(bar_sb, 0, abort_flag, status) : 0);
+    if (gu_ok) {
+        // 2*RG/16 row tiles (gate, then up), every warp on all of them for its own
+        // groups gg = warp, warp + kFWarps, ... (one in each half of the columns with
+        // 32 groups and 16 warps): each group's B fragments are loaded once for all
+        // the tiles, whose MMA chains are independent
+        const int ntile = 2 * (RG / 16), ngrp = H / 64, half = ngrp / 2;
+        constexpr int kTC = 4;   // row tiles per pass
+        for (int t0 = 0; t0 < ntile; t0 += kTC) {
+            float acc[kTC][2];
+#pragma unroll
+            for (int t = 0; t < kTC; ++t) acc[t][0] = acc[t][1] = 0.f;
+            for (int gg = warp; gg < ngrp; gg += kFWarps) {
+                if (!mbar_wait(&bar_gu[gg / half], 0, abort_flag, status)) break;
+                uint32_t bf[8];
+                load_bfrag<CODE>(reinterpret_cast<const uint4*>(xperm), gg, bf);
+                float d[kTC][4];
+#pragma unroll
+                for (int t = 0; t < kTC; ++t) {
+                    d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
+                    const int tt = t0 + t;
+                    if (tt < ntile) {
+                        const bool up = tt >= ntile / 2;
+                        group_mma_b<CODE>(up ? ucodes : gcodes, RG, (up ? tt - ntile / 2 : tt) * 16, gg, bf, d[t]);
+                    }
+                }
+                const float bs = xbs[gg], xs = xsum[gg];
+                const int g = lane >> 2, ngr = H / 64;
+#pragma unroll
+                for (int t = 0; t < kTC; ++t) {
+                    const int tt = t0 + t;
+                    if (tt >= ntile) break;
+                    const bool up = tt >= ntile / 2;
+                    const int r0 = (up ? tt - ntile / 2 : tt) * 16 + g;
+                    const uint16_t* sc = up ? usb : gsb;
+                    const uint16_t* bi = sc + RG * ngr;
+                    acc[t][0] = fmaf(bf16_bits_to_float(sc[r0 * ngr + gg]), d[t][0] - 1024.f * bs,
+                                     fmaf(bf16_bits_to_float(bi[r0 * ngr + gg]), xs, acc[t][0]));
+                    acc[t][1] = fmaf(bf16_bits_to_float(sc[(r0 + 8) * ngr + gg]), d[t][2] - 1024.f * bs,
+                                     fmaf(bf16_bits_to_float(bi[(r0 + 8) * ngr + gg]), xs, acc[t][1]));
+                }
+            }
             if ((lane & 3) == 0) {
-                red[task * 16 + (lane >> 2)] = acc0;
-                red[task * 16 + (lane >> 2) + 8] = acc1;
+#pragma unroll
+                for (int t = 0; t < kTC; ++t)
+                    if (t0 + t < ntile) {
+                        gred[((t0 + t) * kFWarps + warp) * 16 + (lane >> 2)] = acc[t][0];
+                        gred[((t0 + t) * kFWarps + warp) * 16 + (lane >> 2) + 8] = acc[t][1];
+                    }
             }
         }
         __syncthreads();
-        const float wsel = *sel_w;
-        for (int i = tid; i < RD; i += kFThreads) {   // sum the K splits in order
+        for (int i = tid; i < 2 * RG; i += kFThreads) {   // sum the warps' group partials in warp order
             const int t = i / 16, r = i % 16;
             float v = 0.f;
-            for (int ks = 0; ks < KS; ++ks) v += red[(t * KS + ks) * 16 + r];
-            st_tagged(a.ybuf + (size_t)slot * H + ei * RD + i, v * wsel, xtag);
+            for (int w = 0; w < kFWarps; ++w) v += gred[(t * kFWarps + w) * 16 + r];
+            (t < ntile / 2 ? gsum : usum)[(t % (ntile / 2)) * 16 + r] = v;
         }
-    } else {   // published even after an abort (as zeros), so that the reducer does not wait in vain
-        for (int i = tid; i < RD; i += kFThreads) st_tagged(a.ybuf + (size_t)slot * H + ei * RD + i, 0.f, xtag);
     }
-    // ---------------------------------------------------------------- 6. combine: the shared expert's CTA per row block
-    if (shared_cluster) {
-        for (int o = ei * RD + tid; o < (ei + 1) * RD; o += kFThreads) {
-            uint64_t v[kMaxSlots];
+    __syncthreads();
+    // ---------------------------------------------------------------- 4. h exchange
+    // this CTA's RG values of h as RG/2 tagged fp16 pairs in B order (entry q of the
+    // slice = h[8q .. 8q+7]), and per 16 values of h (8 words) the sums of the
+    // stored B values (with the 1024 offset) and of the values the products use;
+    // published even after an abort (as zeros), so that no routed CTA waits in vain
+    const bool gu_done = gu_ok && !*abort_flag;
+    {   // thread t < kHReplicas * RG/2: word t % (RG/2) of the slice, to replica t / (RG/2)
+        const int nwc = RG / 2;   // a multiple of 8, so whole warps and whole 8-word pieces
+        if (tid < kHReplicas * nwc) {
+            const int r = tid / nwc, wi = tid % nwc, q = wi >> 2, m = wi & 3;
+            // word m of entry q holds two of h[8q .. 8q+7] (b_word's pairs)
+            const int j0 = CODE == kCodeU4 ? m : (m >> 1) * 4 + (m & 1);
+            const int j1 = j0 + (CODE == kCodeU4 ? 4 : 2);
+            const float sc = (CODE == kCodeU4 && (m & 1)) ? 0.0625f : 1.0f;
+            const float h0 = gu_done ? silu_f(gsum[q * 8 + j0]) * usum[q * 8 + j0] : 0.f;
+            const float h1 = gu_done ? silu_f(gsum[q * 8 + j1]) * usum[q * 8 + j1] : 0.f;
+            if (r == 0 && !(fabsf(h0) <= 65504.f && fabsf(h1) <= 65504.f)) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
+            const uint32_t wd = h2_as_u32(__floats2half2_rn(h0 * sc, h1 * sc));
+            const float2 f = __half22float2(u32_as_h2(wd));
+            float sb = (CODE == kCodeU4 && (m & 1)) ? 0.f : f.x + f.y;   // stored pairs at full scale
+            float so = (CODE == kCodeU4 && (m & 1)) ? f.x + f.y : 0.f;   // stored pairs divided by 16
 #pragma unroll
-            for (int j = 0; j < kMaxSlots; ++j) v[j] = (j < NC) ? ld_tagged(a.ybuf + (size_t)j * H + o) : 0ull;
-            const uint64_t t0 = globaltimer();
-            while (true) {
-                bool all = true;
+            for (int off = 1; off < 8; off <<= 1) {   // the 8 words of one 16-value piece
+                sb += __shfl_xor_sync(0xffffffffu, sb, off);
+                so += __shfl_xor_sync(0xffffffffu, so, off);
+            }
+            const size_t nw = (size_t)NS * (I / 2), ns2 = (size_t)NS * (I / 16) * 2;
+            st_tagged_u32(a.hx + r * nw + (size_t)slot * (I / 2) + ei * nwc + wi, wd, xtag);
+            if ((wi & 7) == 0) {
+                uint64_t* hs = a.hsx + r * ns2 + ((size_t)slot * (I / 16) + ei * (RG / 16) + wi / 8) * 2;
+                st_tagged(hs, CODE == kCodeE4M3 ? 0.f : sb + so, xtag);   // E4M3 products carry no 1024 offset
+                st_tagged(hs + 1, sb + 16.f * so, xtag);
+            }
+        }
+    }
+    if (down_cta) {
+        // all NS slots' h and its piece sums: thread t polls words t, t + kFThreads, ...
+        // of the two arrays seen as one (bounded wait), then stores h in B order for
+        // the down GEMV and the sums beside it (this CTA's gate codes are dead)
+        const int nw = NS * (I / 2), ns2 = NS * (I / 16) * 2;
+        constexpr int kPer = (kMaxSlots * (2048 / 2 + 2048 / 8) + kFThreads - 1) / kFThreads;   // at most
+        const int per = kI ? (kMaxSlots * (kI / 2 + kI / 8) + kFThreads - 1) / kFThreads : kPer;
+        const uint64_t* hxr = a.hx + (size_t)(G % kHReplicas) * nw;     // this CTA's replica
+        const uint64_t* hsr = a.hsx + (size_t)(G % kHReplicas) * ns2;
+        auto src = [&](int i) { return i < nw ? hxr + i : hsr + (i - nw); };
+        uint64_t w[kPer];
 #pragma unroll
-                for (int j = 0; j < kMaxSlots; ++j)
-                    if (j < NC && tag_of(v[j]) != xtag) {
-                        all = false;
-                        v[j] = ld_tagged(a.ybuf + (size_t)j * H + o);
-                    }
-                if (all) break;
-                if (globaltimer() - t0 > kWaitLimitNs) {
-                    raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
-                    break;
+        for (int j = 0; j < kPer; ++j) {
+            const int i = tid + j * kFThreads;
+            w[j] = (j < per && i < nw + ns2) ? ld_tagged(src(i)) : 0ull;
+        }
+        const uint64_t t0 = globaltimer();
+        for (int it = 1;; ++it) {
+            bool all = true;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                const int i = tid + j * kFThreads;
+                if (j < per && i < nw + ns2 && tag_of(w[j]) != xtag) {
+                    all = false;
+                    w[j] = ld_tagged(src(i));
                 }
             }
-            float s = 0.f;
-#pragma unroll
-            for (int j = 0; j < kMaxSlots; ++j) s += (j < NC) ? val_of(v[j]) : 0.f;
-            a.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+            if (all) break;
+            if ((it & 15) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+                raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
         }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int i = tid + j * kFThreads;
+            if (j < per && i < nw) hperm[i] = (uint32_t)w[j];
+            else if (j < per && i < nw + ns2) hpiece[i - nw] = val_of(w[j]);
+        }
+    }
+    __syncthreads();
+    const bool h_ok = down_cta && gu_done && !*abort_flag;
+    // every slot's h carries the tag, so every CTA has read the call counter
+    if (h_ok && G == 0 && tid == 0) st_relaxed_u32(&a.ctrl->pad[kCtrlEpochWord], xtag);
+    if (h_ok) {   // per-64-value group sums of h: its four 16-value pieces in order
+        for (int gi = tid; gi < NS * (I / 64); gi += kFThreads) {
+            const float* pc = hpiece + 8 * gi;
+            hbs[gi] = ((pc[0] + pc[2]) + pc[4]) + pc[6];
+            hsum[gi] = ((pc[1] + pc[3]) + pc[5]) + pc[7];
+        }
+    }
+    // ---------------------------------------------------------------- 5. down GEMV, weighted sum, output rows
+    cp_async_wait<0>();   // this thread's pieces of the down scales and biases
+    const bool dn_ok = __syncthreads_and(h_ok ? (mbar_wait(bar_dn, 0, abort_flag, status) &&
+                                                 mbar_wait(bar_dsh, 0, abort_flag, status))
+                                              : 0);
+    if (dn_ok) {
+        // units (slot, row tile, group), strided over the warps; each unit's 16 row
+        // sums go to dred[unit][16]
+        const int ngrp = I / 64, ntl = DR / 16, nunit = NS * ntl * ngrp;
+        constexpr int kU = (kMaxSlots * 8 + kFWarps - 1) / kFWarps;   // units per warp in flight (I = 512)
+        for (int u0 = warp; u0 < nunit; u0 += kU * kFWarps) {
+            // branch-free: a unit past the end repeats the last one, its result unstored
+            float d[kU][4];
+            int uj[kU], ugg[kU], utl[kU];
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const int u = min(u0 + q * kFWarps, nunit - 1);
+                uj[q] = u / (ntl * ngrp);
+                utl[q] = (u / ngrp) % ntl;
+                ugg[q] = u % ngrp;
+                d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
+                group_mma<CODE>(dcodes + (size_t)uj[q] * L.dslot, DR, utl[q] * 16, ugg[q],
+                                reinterpret_cast<const uint4*>(hperm) + (size_t)uj[q] * (I / 8), d[q]);
+            }
+            const int g = lane >> 2;
+#pragma unroll
+            for (int q = 0; q < kU; ++q) {
+                const int j = uj[q], gg = ugg[q], r0 = utl[q] * 16 + g;
+                const uint16_t* sc = dsb + (size_t)j * 2 * DR * ngrp;
+                const uint16_t* bi = sc + DR * ngrp;
+                const float bs = hbs[j * ngrp + gg], hs = hsum[j * ngrp + gg];
+                const float v0 = fmaf(bf16_bits_to_float(sc[r0 * ngrp + gg]), d[q][0] - 1024.f * bs,
+                                      bf16_bits_to_float(bi[r0 * ngrp + gg]) * hs);
+                const float v1 = fmaf(bf16_bits_to_float(sc[(r0 + 8) * ngrp + gg]), d[q][2] - 1024.f * bs,
+                                      bf16_bits_to_float(bi[(r0 + 8) * ngrp + gg]) * hs);
+                const int u = u0 + q * kFWarps;
+                if ((lane & 3) == 0 && u < nunit) {
+                    dred[u * 16 + g] = v0;
+                    dred[u * 16 + g + 8] = v1;
+                }
+            }
+        }
+        __syncthreads();
+        // out row r = sum over slots (in order) of the slot's weight times its row sum
+        // over the groups (in order)
+        for (int r = tid; r < DR; r += kFThreads) {
+            const int tl = r / 16, rr = r % 16;
+            float acc = 0.f;
+            for (int j = 0; j < NS; ++j) {
+                float y = 0.f;
+                for (int gg = 0; gg < ngrp; ++gg) y += dred[((j * ntl + tl) * ngrp + gg) * 16 + rr];
+                acc = fmaf(sel_w[j], y, acc);
+            }
+            a.out[gdrow_sh + r] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+        }
+    }
+    // ---------------------------------------------------------------- exit
+    // a CTA that gave up advances the call counter itself (the tags of this call's
+    // words must not be taken for the next call's), and no TMA copy of this CTA
+    // may still be in flight when it leaves
+    __syncthreads();
+    if (tid == 0) {
+        if (*abort_flag) st_relaxed_u32(&a.ctrl->pad[kCtrlEpochWord], xtag);
+        const int is = *issued;
+        if (is & 1) {
+            mbar_drain(&bar_gu[0]);
+            mbar_drain(&bar_gu[1]);
+        }
+        if (is & 2) mbar_drain(bar_dn);
+        if (is & 4) mbar_drain(bar_dsh);
+        if (is & 8) mbar_drain(bar_sb);
     }
 }
 
@@ -757,27 +989,31 @@ typedef CUresult (*EncodeTiledFn2)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 
 static EncodeTiledFn2 encode_fn2() {
     static EncodeTiledFn2 fn = nullptr;
-    if (!fn) {
+    static std::once_flag once;
+    std::call_once(once, [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess && q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<EncodeTiledFn2>(p);
-    }
+    });
     return fn;
 }
 
-// codes [rows][cols/8] uint32, box = 32 words x box_rows, 128-byte swizzle
+// codes [rows][cols/8] uint32 seen as [cols/256 box columns][rows][32 words]
+// (dimension 1 = rows, dimension 2 = box columns 128 bytes apart), box = 32
+// words x box_rows x box_cols; every (row, box column) lands as one 128-byte
+// line, 128-byte swizzled, box column c of the copy at c*box_rows*128.
 static bool codes_map(CUtensorMap* m, const uint32_t* codes, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                      int bits) {
+                      uint32_t box_cols, int bits) {
     EncodeTiledFn2 fn = encode_fn2();
     if (!fn) return false;
     const uint64_t words = cols * bits / 32;   // code words per row
-    const cuuint64_t dims[2] = {words, rows};
-    const cuuint64_t strides[1] = {words * 4};
-    const cuuint32_t box[2] = {32, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(codes), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {32, rows, words / 32};
+    const cuuint64_t strides[2] = {words * 4, 128};
+    const cuuint32_t box[3] = {32, box_rows, box_cols};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t*>(codes), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -800,30 +1036,38 @@ static FusedKernel fused_kernel_for(const moe_w4_layer& L) {
 }
 
 static bool shape_ok(const moe_w4_layer& L) {
-    const int bits = code_bits_of(L);
+    const int bits = code_bits_of(L), k = L.top_k, NG = (k + 1) * kPE;
     if (!fused_kernel_for(L)) return false;
+    if (k < 1 || k + 1 > kMaxSlots) return false;
     if (L.H % 256 || L.I % 256 || L.H > 4096 || L.I > 2048) return false;   // slices of 16 rows; <= 16 row tiles
-    if (L.H * bits / 1024 > 16) return false;                                 // gate/up box barriers
-    if (L.E < 128 || L.E > 256 || L.E % 32) return false;   // top-k: 8 scores per lane; 2E floats hold the K-split partials
-    if (L.top_k + 1 > kMaxSlots) return false;
-    if (L.H > 64 * kPE * (L.top_k + 1)) return false;   // <= 64 router rows per CTA (32 per thread)
-    const FusedSmem s(L.H, L.E, L.I, bits);
-    return s.total + 1024 + 1024 <= 227 * 1024;   // + static shared memory of the kernel
+    if (L.H % (kPE * k * 16)) return false;                                   // down rows per CTA: whole m16 tiles
+    if (L.H * bits / 1024 > 16 || (L.H * bits / 1024) % 2) return false;     // gate/up: two halves of box columns
+    if (L.E < 128 || L.E > 256 || L.E % 32) return false;                     // top-k: 8 scores per lane
+    const int EG = L.E / kRE, NR = k * kPE;                                   // router: 8 experts per CTA
+    if (EG > NR || NR % EG || NR / EG > 8 || L.H % (NR / EG)) return false;   // row splits: at most 8 polling warps
+    if (L.H / (NR / EG) > kMaxRouterRows * kFThreads || L.H > 8 * kFThreads) return false;
+    if (L.I / 64 * (k + 1) > 9 * 8) return false;                             // down units per warp in flight
+    if (L.I > 2048) return false;                                              // h words per thread
+    const FusedSmem s(L.H, L.E, L.I, k, bits);
+    if (!s.aliases_fit(L.I)) return false;
+    return s.total + 1024 <= 227 * 1024;
 }
 
-static size_t fused_smem(const moe_w4_layer& L) { return FusedSmem(L.H, L.E, L.I, code_bits_of(L)).total + 1024; }
+static size_t fused_smem(const moe_w4_layer& L) {
+    return FusedSmem(L.H, L.E, L.I, L.top_k, code_bits_of(L)).total + 1024;
+}
 
-static cudaLaunchConfig_t fused_config(const moe_w4_layer& L, cudaLaunchAttribute* attr, cudaStream_t st,
-                                       bool pdl) {
+// Cooperative launch: every CTA resident at once (the exchanges wait on other
+// CTAs); with programmatic dependent launch the prologue may overlap the
+// previous kernel's tail.
+static cudaLaunchConfig_t fused_config(const moe_w4_layer& L, cudaLaunchAttribute* attr, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((L.top_k + 1) * kPE);
     cfg.blockDim = dim3(kFThreads);
     cfg.dynamicSmemBytes = fused_smem(L);
     cfg.stream = st;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
@@ -831,29 +1075,30 @@ static cudaLaunchConfig_t fused_config(const moe_w4_layer& L, cudaLaunchAttribut
     return cfg;
 }
 
-// The kernel's exchanges wait on other CTAs, so every cluster must be resident
-// at once: the answer of the occupancy calculator is checked (and cached per
-// device and launch shape) before the fused path is taken.
+// The kernel's exchanges wait on other CTAs, so every CTA must be resident at
+// once: the occupancy calculator's answer is checked (and cached per device and
+// launch shape) before the fused path is taken, and the launch itself is
+// cooperative.
 bool decode_fused_supported(const moe_w4_layer& L) {
     if (!shape_ok(L)) return false;
     struct Entry { int dev, k; size_t smem; FusedKernel kern; bool ok; };
     static Entry cache[16] = {};
     static int ncache = 0;
+    static std::mutex mu;   // first calls from several host threads fill the cache one at a time
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     const size_t smem = fused_smem(L);
     const FusedKernel kern = fused_kernel_for(L);
+    std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < ncache; ++i)
         if (cache[i].dev == dev && cache[i].k == L.top_k && cache[i].smem == smem && cache[i].kern == kern)
             return cache[i].ok;
-    bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
-              cudaSuccess;
+    bool ok = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess;
     if (ok) {
-        cudaLaunchAttribute attr[2];
-        const cudaLaunchConfig_t cfg = fused_config(L, attr, nullptr, false);
-        int nclusters = 0;
-        ok = cudaOccupancyMaxActiveClusters(&nclusters, (void*)kern, &cfg) == cudaSuccess &&
-             nclusters >= (L.top_k + 1) * kFusedClustersPerExpert;
+        int per_sm = 0, nsm = 0;
+        ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFThreads, smem) == cudaSuccess &&
+             cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+             per_sm * nsm >= (L.top_k + 1) * kPE;
     }
     cudaGetLastError();   // a refused query leaves no sticky error behind
     if (ncache < 16) cache[ncache++] = Entry{dev, L.top_k, smem, kern, ok};
@@ -863,12 +1108,14 @@ bool decode_fused_supported(const moe_w4_layer& L) {
 cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                                 cudaStream_t st) {
     const int H = L.H, E = L.E, I = L.I, k = L.top_k;
-    const int RG = I / kPE, RD = H / kPE, b = code_bits_of(L);
+    const int RG = I / kPE, DR = H / (kPE * k), b = code_bits_of(L);
+    const uint32_t hbox = H * b / 1024 / 2, dbox = I * b / 1024;   // box columns per copy
     CUtensorMap mg, mu, md, msg, msu, msd;
-    bool ok = codes_map(&mg, L.gate.codes, (uint64_t)E * I, H, RG, b) &&
-              codes_map(&mu, L.up.codes, (uint64_t)E * I, H, RG, b) &&
-              codes_map(&md, L.down.codes, (uint64_t)E * H, I, RD, b) && codes_map(&msg, L.sh_gate.codes, I, H, RG, b) &&
-              codes_map(&msu, L.sh_up.codes, I, H, RG, b) && codes_map(&msd, L.sh_down.codes, H, I, RD, b);
+    bool ok = codes_map(&mg, L.gate.codes, (uint64_t)E * I, H, RG, hbox, b) &&
+              codes_map(&mu, L.up.codes, (uint64_t)E * I, H, RG, hbox, b) &&
+              codes_map(&md, L.down.codes, (uint64_t)E * H, I, DR, dbox, b) &&
+              codes_map(&msg, L.sh_gate.codes, I, H, RG, hbox, b) && codes_map(&msu, L.sh_up.codes, I, H, RG, hbox, b) &&
+              codes_map(&msd, L.sh_down.codes, H, I, DR, dbox, b);
     if (!ok) return cudaErrorInvalidValue;
     FusedArgs a{};
     a.x = x; a.router_w = L.router_w; a.router_bias = L.router_bias; a.shared_gate = L.shared_gate;
@@ -876,14 +1123,25 @@ cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16
     a.ds = L.down.scales; a.db = L.down.biases;
     a.sgs = L.sh_gate.scales; a.sgb = L.sh_gate.biases; a.sus = L.sh_up.scales; a.sub = L.sh_up.biases;
     a.sds = L.sh_down.scales; a.sdb = L.sh_down.biases;
-    a.cpart = d.fused_cpart; a.hx = d.fused_hx; a.ybuf = d.fused_ybuf;
+    a.scores = d.fused_scores; a.hx = d.fused_hx; a.hsx = d.fused_hsx;
     a.idx_out = d.idx; a.w_out = d.w; a.gamma_out = d.gamma; a.out = out;
     a.ctrl = d.ctrl;
     a.H = H; a.E = E; a.I = I; a.k = k;
     cudaLaunchAttribute attr[2];
-    // programmatic dependent launch: the prologue may overlap the previous kernel's tail
-    const cudaLaunchConfig_t cfg = fused_config(L, attr, st, true);   // shared memory opt-in set by the support check
-    return cudaLaunchKernelEx(&cfg, fused_kernel_for(L), a, mg, mu, md, msg, msu, msd);
+    const FusedKernel kern = fused_kernel_for(L);   // shared memory opt-in set by the support check
+    cudaLaunchConfig_t cfg = fused_config(L, attr, st, true);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, mg, mu, md, msg, msu, msd);
+    if (e != cudaSuccess) {   // refused with programmatic dependent launch: cooperative alone
+        cudaGetLastError();
+        cfg = fused_config(L, attr, st, false);
+        e = cudaLaunchKernelEx(&cfg, kern, a, mg, mu, md, msg, msu, msd);
+    }
+    return e;
 }
+
+// Sizes of the fused kernel's exchange buffers (tagged 8-byte words) for a layer.
+size_t fused_scores_bytes(const moe_w4_layer& L) { return (size_t)kScoreReplicas * 128 * L.top_k * 8; }
+size_t fused_hx_bytes(const moe_w4_layer& L) { return (size_t)kHReplicas * (L.top_k + 1) * (L.I / 2) * 8; }
+size_t fused_hsx_bytes(const moe_w4_layer& L) { return (size_t)kHReplicas * (L.top_k + 1) * (L.I / 16) * 2 * 8; }
 
 }  // namespace mw4

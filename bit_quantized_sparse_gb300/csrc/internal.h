@@ -16,7 +16,6 @@ constexpr int kBM = 128;          // weight rows per tensor-core tile
 constexpr int kBN = 128;          // token rows per tensor-core tile
 constexpr int kBK = 64;           // reduction columns per pipeline stage (= one group)
 constexpr int kDecodeMaxT = 16;   // largest decode batch
-constexpr int kFusedClustersPerExpert = 4;   // fused T=1 decode: 16 CTAs per expert in clusters of 4
 constexpr int kRouterRowsPerCta = 256;  // H rows per decode-router CTA
 constexpr int kRouterSplit = 2;         // prefill router: partial score arrays (halves of H)
 // Width of one weight code: 4 (also for code_bits = 0) or 8.
@@ -29,11 +28,12 @@ inline bool codes_e4m3(const moe_w4_layer& L) { return L.code_format == MOE_W4_C
 // (I columns) fits the tensor-memory A ring (kDownReuseMaxI columns).
 constexpr int kDownBlocksPerUnit = 4;
 // Word of the control header's pad[] holding the fused T=1 decode's call
-// counter (the tag of its exchanged values); kept across calls.
+// counter (the tag of its exchanged values is the counter + 1); kept across
+// calls.
 constexpr int kCtrlEpochWord = 61;
 // Word of pad[] that the failure-detection test hook sets (0 in normal use):
-// while it is non-zero, the T=1 kernel's cluster 0 does not publish its router
-// sums, so every routed CTA's bounded wait for them runs out.
+// while it is non-zero, the T=1 kernel's CTA 0 does not publish its router
+// scores, so every routed CTA's bounded wait for them runs out.
 constexpr int kCtrlInjectWord = 60;
 constexpr int kDownReuseMaxI = 512;
 inline int down_blocks_per_unit(int I) { return I <= kDownReuseMaxI ? kDownBlocksPerUnit : 1; }
@@ -49,7 +49,7 @@ void trace_kernels(int n);
 struct WsLayout {
     size_t ctrl, logits, router_a, x16, topk_idx, topk_w, gamma, chunk_base, counts, offsets, perm, inv;
     size_t blkinfo, unitinfo, ntiles, hh, ys;
-    size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh, dec_cpart, dec_hx, dec_ybuf;
+    size_t dec_part, dec_idx, dec_w, dec_gamma, dec_hh, dec_scores, dec_hx, dec_hsx;
     size_t total;
     int T_max, nchunk_max, max_blocks, max_tiles_gu, max_tiles_dn;
 };
@@ -87,13 +87,20 @@ struct DecodeWs {
     unsigned int* counter;
     unsigned int* status;
     Ctrl* ctrl;         // control header (call counter of the fused kernel)
-    uint64_t* fused_cpart; // [kFusedClustersPerExpert*(k+1)][E] tagged cluster partial scores (fused T=1 kernel)
-    uint64_t* fused_hx;    // [k+1][I] tagged h of every expert (fused T=1 kernel)
-    uint64_t* fused_ybuf;  // [k+1][H] tagged weighted expert outputs (fused T=1 kernel)
+    uint64_t* fused_scores; // tagged partial router scores, fused_scores_bytes (fused T=1 kernel)
+    uint64_t* fused_hx;     // tagged h of every slot, fp16 pairs, fused_hx_bytes (fused T=1 kernel)
+    uint64_t* fused_hsx;    // tagged sums of 16-value pieces of h, fused_hsx_bytes (fused T=1 kernel)
 };
 bool decode_fused_supported(const moe_w4_layer& L);
+// One cooperative launch of the fused T=1 kernel; an error means the launch
+// was refused and nothing was enqueued (the caller takes another path).
 cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                                 cudaStream_t st);
+// Bytes of the fused kernel's exchange buffers for a layer: router score
+// partials (replicated), h, and the sums of h's 32-value pieces.
+size_t fused_scores_bytes(const moe_w4_layer& L);
+size_t fused_hx_bytes(const moe_w4_layer& L);
+size_t fused_hsx_bytes(const moe_w4_layer& L);
 cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                           cudaStream_t st);
 

@@ -16,6 +16,8 @@
 // array, so its device address is looked up once per device with
 // cudaGetSymbolAddress (with that device current) and cached; the first call on
 // a device does this set-up.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,12 +27,21 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_W4_NOALLOC_SCRATC
 
 static constexpr int kMaxDevices = 64;
 static void* g_scratch_addr[kMaxDevices] = {};
+static std::mutex g_scratch_mu;   // first calls from several host threads set up the cache one at a time
 
 static size_t up256n(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Compact decode-only layout inside the fixed array: control header, partial
-// scores, selected experts, weights, shared gate, SwiGLU outputs.
-struct NoallocLayout { size_t ctrl, part, idx, w, gamma, hh, cpart, hx, ybuf, total; };
+// Compact decode-only layout inside the fixed array: control header, then the
+// one-kernel T=1 decode's exchange buffers (router score partials, h, sums of
+// h's pieces) at fixed offsets sized for the largest layer that kernel takes
+// (top_k <= 8, I <= 2048), so that no call of another shape or layer ever writes there
+// (the words there carry call tags that must only come from that kernel), then
+// the buffers of the T >= 2 kernels: partial router scores, selected experts,
+// weights, shared gate, SwiGLU outputs.
+constexpr size_t kNoallocScoresBytes = 8 * 128 * 8 * 8;    // replicas x 128 k words, k <= 8
+constexpr size_t kNoallocHxBytes = 8 * 9 * 1024 * 8;       // replicas x (k+1) * I/2 words
+constexpr size_t kNoallocHsxBytes = 8 * 9 * 128 * 2 * 8;   // replicas x (k+1) * I/16 * 2 words
+struct NoallocLayout { size_t ctrl, scores, hx, hsx, part, idx, w, gamma, hh, total; };
 
 static NoallocLayout noalloc_layout(const moe_w4_layer& L, int T) {
     NoallocLayout n{};
@@ -39,14 +50,14 @@ static NoallocLayout noalloc_layout(const moe_w4_layer& L, int T) {
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o += up256n(bytes); return at; };
     n.ctrl = take(sizeof(Ctrl));
+    n.scores = take(kNoallocScoresBytes);
+    n.hx = take(kNoallocHxBytes);
+    n.hsx = take(kNoallocHsxBytes);
     n.part = take(nslice * Tz * E * 4);
     n.idx = take(Tz * k * 4);
     n.w = take(Tz * k * 4);
     n.gamma = take(Tz * 4);
     n.hh = take(Tz * (k + 1) * I * 4);
-    n.cpart = take((size_t)kFusedClustersPerExpert * (k + 1) * E * 8);
-    n.hx = take((k + 1) * I * 8);
-    n.ybuf = take((k + 1) * H * 8);
     n.total = o;
     return n;
 }
@@ -57,6 +68,7 @@ static cudaError_t scratch_address(void** out) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
@@ -90,6 +102,10 @@ extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const
     const moe_w4_mat* ms[6] = {&L->gate, &L->up, &L->down, &L->sh_gate, &L->sh_up, &L->sh_down};
     for (const moe_w4_mat* m : ms)
         if (!m->codes || !m->scales || !m->biases) return MOE_W4_ERR_INVALID;
+    auto mis = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
+    if (mis(L->router_w) || mis(L->shared_gate) || (L->router_bias && mis(L->router_bias))) return MOE_W4_ERR_ALIGN;
+    for (const moe_w4_mat* m : ms)
+        if (mis(m->codes) || mis(m->scales) || mis(m->biases)) return MOE_W4_ERR_ALIGN;
     const NoallocLayout n = noalloc_layout(*L, T);
     if (n.total > (size_t)MOE_W4_NOALLOC_SCRATCH_BYTES) return MOE_W4_ERR_SCRATCH;
     void* base = nullptr;
@@ -110,8 +126,20 @@ extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const
     d.counter = &reinterpret_cast<Ctrl*>(b + n.ctrl)->decode_counter;
     d.status = &reinterpret_cast<Ctrl*>(b + n.ctrl)->status;
     d.ctrl = reinterpret_cast<Ctrl*>(b + n.ctrl);
-    d.fused_cpart = reinterpret_cast<uint64_t*>(b + n.cpart);
+    d.fused_scores = reinterpret_cast<uint64_t*>(b + n.scores);
     d.fused_hx = reinterpret_cast<uint64_t*>(b + n.hx);
-    d.fused_ybuf = reinterpret_cast<uint64_t*>(b + n.ybuf);
+    d.fused_hsx = reinterpret_cast<uint64_t*>(b + n.hsx);
     return launch_decode(*L, T, x, out, d, stream) == cudaSuccess ? MOE_W4_OK : MOE_W4_ERR_LAUNCH;
+}
+
+// Copies the status word of the scratch array (the sticky MOE_W4_STATUS_* bits
+// of the calls since the last one that cleared it) into caller memory.
+extern "C" int moe_w4_noalloc_status(unsigned int* status, cudaStream_t stream) {
+    if (!status) return MOE_W4_ERR_INVALID;
+    void* base = nullptr;
+    if (scratch_address(&base) != cudaSuccess) return MOE_W4_ERR_LAUNCH;
+    const uint8_t* word = static_cast<const uint8_t*>(base) + offsetof(Ctrl, status);
+    return cudaMemcpyAsync(status, word, sizeof(unsigned int), cudaMemcpyDefault, stream) == cudaSuccess
+               ? MOE_W4_OK
+               : MOE_W4_ERR_LAUNCH;
 }

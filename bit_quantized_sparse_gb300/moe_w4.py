@@ -70,6 +70,7 @@ _SIGS = {
     "moe_w4_set_trace_events": (c_int, [c_void_p, c_int]),
     "moe_w4_last_traced_kernels": (c_int, []),
     "moe_w4_forward_decode_noalloc": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p]),
+    "moe_w4_noalloc_status": (c_int, [c_void_p, c_void_p]),
     "moe_w4_test_skip_publish": (c_int, [c_void_p, c_size_t, c_int, c_void_p]),
     "moe_w4_strerror": (c_char_p, [c_int]),
 }
@@ -88,6 +89,7 @@ moe_w4_forward_prefill = _lib.moe_w4_forward_prefill
 moe_w4_set_trace_events = _lib.moe_w4_set_trace_events
 moe_w4_last_traced_kernels = _lib.moe_w4_last_traced_kernels
 moe_w4_forward_decode_noalloc = _lib.moe_w4_forward_decode_noalloc
+moe_w4_noalloc_status = _lib.moe_w4_noalloc_status
 moe_w4_test_skip_publish = _lib.moe_w4_test_skip_publish
 
 

@@ -160,11 +160,16 @@ int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
                  void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* Layer output for a decode batch, 1 <= T <= 16 (section "Optimise the
- * single-row weight path").  T = 1: one kernel for the whole layer (router,
- * W4 GEMVs for gate/up + SwiGLU and for down weighted by the routing scores,
- * plus the gated shared expert).  T >= 2, or a shape that kernel does not
- * cover: the grouped path of moe_w4_forward_prefill, which reads each selected
- * expert once for all rows that chose it.  out bf16 [T][H]. */
+ * single-row weight path").  T = 1: one cooperative kernel for the whole layer
+ * (router, W4 GEMVs for gate/up + SwiGLU and for down weighted by the routing
+ * scores, plus the gated shared expert); its CTAs exchange router scores and h
+ * through the workspace with bounded waits.  T >= 2, a shape that kernel does
+ * not cover, or a device that refuses its cooperative launch: the grouped path
+ * of moe_w4_forward_prefill, which reads each selected expert once for all
+ * rows that chose it.  out bf16 [T][H].  The one-kernel path reads the
+ * weights, router and shared gate before it waits for the kernel that precedes
+ * it on the stream (programmatic dependent launch): they must not be written
+ * by that kernel. */
 int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
                           moe_w4_bf16* out, void* workspace, size_t ws_bytes,
                           cudaStream_t stream);
@@ -209,6 +214,15 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
 int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
                                   moe_w4_bf16* out, cudaStream_t stream);
 
+/* Device status of the allocation-free decode: enqueues on `stream` a copy of
+ * the status word inside the fixed scratch array (the MOE_W4_STATUS_* bits of
+ * the allocation-free calls since the last one, as each call clears it first)
+ * into *status, device or host memory; read it once the stream has passed this
+ * point.  A non-zero word means the last call's output is not valid.  No
+ * counterpart in the pages.  MOE_W4_ERR_INVALID for a NULL pointer,
+ * MOE_W4_ERR_LAUNCH if the copy cannot be enqueued. */
+int moe_w4_noalloc_status(unsigned int* status, cudaStream_t stream);
+
 /* Optional tracing for benchmarks: while set, every forward call records
  * events[0..n_events) (cudaEvent_t, created by the caller) on its stream:
  * event 0 before its first kernel and event i after its i-th kernel, so
@@ -224,8 +238,8 @@ int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const moe_w4_bf1
 int moe_w4_set_trace_events(cudaEvent_t* events, int n_events);
 
 /* Failure-detection test hook (no production use).  on != 0: the next batch-1
- * decode calls on this workspace have one cluster skip publishing its router
- * sums, so the other CTAs' bounded waits for them run out (after about 2 s):
+ * decode calls on this workspace have one CTA skip publishing its router
+ * scores, so the other CTAs' bounded waits for them run out (after about 2 s):
  * the call completes, its output is not valid, and the status word gets
  * MOE_W4_STATUS_WAIT_TIMEOUT.  No GPU fault, trap or hang is involved.  on = 0
  * (or moe_w4_workspace_init, which must follow any device-side error anyway)
