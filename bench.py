@@ -127,29 +127,28 @@ def peaks():
 
 
 def measured_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary table
-    (profiles/traffic.md), or None when the kernel's source files have changed
+    """DRAM bytes per launch of `kernel` from the committed ncu figures
+    (profiles/traffic.json), or None when the kernel's source files have changed
     since that capture (their sha256 no longer matches) or it was never captured."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "traffic.md")
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    for line in open(path):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) < 4 or cells[0] != kernel:
+    for e in json.load(open(path))["kernels"]:
+        if e["kernel"] != kernel:
             continue
         h = hashlib.sha256()
-        for f in cells[1].split():
+        for f in e["sources"]:
             fp = os.path.join(ROOT, "bit_quantized_sparse_gb300", f)
             if not os.path.exists(fp):
                 return None
             h.update(open(fp, "rb").read())
-        return int(cells[3]) if h.hexdigest() == cells[2] else None
+        return int(e["dram_bytes_per_launch"]) if h.hexdigest() == e["sha256"] else None
     return None
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 20 ms while the timed regions run."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -161,7 +160,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -256,29 +255,33 @@ def run_gpu(args, rank, local_rank, world, dist):
 
     g_step, g_pre, g_dec = capture(step), capture(prefill_part), capture(decode_part)
 
-    def timed(g, n):
+    def timed(g, n, per=None):
+        """Seconds for n replays of g (max over ranks), events on the replay stream
+        around each replay; `per`, if given, receives each replay's seconds."""
         for _ in range(args.warmup):
             g.replay()
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
         with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(n):
+            evs[0].record(stream)
+            for i in range(n):
                 g.replay()
-            e1.record(stream)
+                evs[i + 1].record(stream)
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-        return reduce_max(e0.elapsed_time(e1) / 1e3, dist, device)
+        if per is not None:
+            per.extend(evs[i].elapsed_time(evs[i + 1]) / 1e3 for i in range(n))
+        return reduce_max(evs[0].elapsed_time(evs[n]) / 1e3, dist, device)
 
-    with ClockSampler(local_rank) as clk:
-        t_step = timed(g_step, args.steps)
-    clocks = clk.summary()
-    t_pre = timed(g_pre, args.steps)
-    t_dec = timed(g_dec, args.steps)
+    clk = ClockSampler(local_rank).__enter__()   # sampling spans every timed region of the run
+    per_step, per_pre, per_dec = [], [], []
+    t_step = timed(g_step, args.steps, per_step)
+    t_pre = timed(g_pre, args.steps, per_pre)
+    t_dec = timed(g_dec, args.steps, per_dec)
 
     # multi-row decode (T = 4 and 8 rows per call, the grouped path): calls
     # cycling the replica layers over slices of the decode rows; the bytes a call
@@ -423,10 +426,13 @@ def run_gpu(args, rank, local_rank, world, dist):
     e2e_steps(args.steps)
     torch.cuda.synchronize()
     t_e2e = reduce_max(time.perf_counter() - t0, dist, device)
+    clk.__exit__(None, None, None)
+    clocks = clk.summary()
     status = layers[0].status()
     if status != 0:
         raise RuntimeError(f"device status {status}")
     return dict(c=c, L0=L0, x_np=x_np, xdec_np=xdec_np, t_step=t_step, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e, small=small,
+                per_step=per_step, per_pre=per_pre, per_dec=per_dec,
                 variants=variants, clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device))
 
 
@@ -459,6 +465,15 @@ def gemm_flops(c, T, which):
     return 2 * rows * H * 2 * I if which == "gate_up" else 2 * rows * I * H
 
 
+def spread(values, scale=1.0):
+    """Median, 10th and 90th percentile of per-replay times (seconds), scaled."""
+    if not values:
+        return None
+    v = np.sort(np.asarray(values, np.float64)) * scale
+    return {"median": float(np.median(v)), "p10": float(np.percentile(v, 10)), "p90": float(np.percentile(v, 90)),
+            "replays": int(v.size)}
+
+
 def variant_summary(c, w, chunk, world, pk):
     """A one-byte-code layer: prefill chunk against the tensor peak, its two
     GEMMs, and batch-1 decode against HBM."""
@@ -468,10 +483,11 @@ def variant_summary(c, w, chunk, world, pk):
     gk = {n: w["k_pre"].get(f"gemm_{n}") for n in fl}
     return {"layer": f"same shape as the step's layer, {w['bits']}-bit codes, {W8_REPLICAS} distinct layers for decode",
             "prefill": {"ms_per_4096_chunk": 1e3 * w["t_pre"], "tok_s": job_value(chunk, world, w["t_pre"]),
-                        "tensor_tflops": tf, "frac_of_peak": tf / pk["bf16_tflops_sustained"],
+                        "tensor_tflops": tf, "frac_of_burst_peak": tf / pk["bf16_tflops"],
+                        "frac_of_sustained_peak": tf / pk["bf16_tflops_sustained"],
                         "gemm_us": {n: 1e6 * t for n, t in gk.items() if t},
-                        "gemm_frac_of_peak": {n: fl[n] / t / 1e12 / pk["bf16_tflops_sustained"]
-                                              for n, t in gk.items() if t}},
+                        "gemm_frac_of_burst_peak": {n: fl[n] / t / 1e12 / pk["bf16_tflops"]
+                                                    for n, t in gk.items() if t}},
             "decode_T1": {"us_per_call": 1e6 * w["t_dec"], "bytes_per_call": b, "hbm_gbs": b / w["t_dec"] / 1e9,
                           "frac_of_hbm": b / w["t_dec"] / 1e9 / pk["hbm_gbs"],
                           "path": "one-kernel batch-1 decode (decode_fused_kernel, one-byte-code instance)"}}
@@ -554,10 +570,11 @@ def main():
         f = gemm_flops(c, chunk, "gate_up" if dom[1] == "gemm_gate_up" else "down")
         ach = f / t_dom / 1e12
         gk = "grouped_w4_gemm_kernel<1, 4, 0>" if dom[1] == "gemm_gate_up" else "grouped_w4_gemm_kernel<0, 4, 0>"
-        roof = {"kernel": dom[1], "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": measured_traffic(gk),
+        roof = {"kernel": dom[1], "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": measured_traffic(gk),
                 "work_per_launch": f"{f:.4e} FLOP (fp16 operands, fp32 accumulate)",
-                "peak_note": f"dense bf16 sustained, {pk['source']}; fp16 has the same nominal rate"}
+                "peak_note": f"dense bf16 burst (the kernel is timed in short replays), {pk['source']}; fp16 has "
+                             f"the same nominal rate"}
     else:
         b = decode_bytes(c)
         fused_only = len(r["k_dec"]) == 1
@@ -596,12 +613,21 @@ def main():
                                    f"top-8 I=512 shared expert, Zipf(1.2) routing",
                        "l2": f"inputs larger than L2: 455 MB of weights per layer; decode cycles {N_REPLICAS} "
                              f"distinct layers ({N_REPLICAS * 455} MB)",
-                       "parallelism": f"replicas x{world}", "timing": "CUDA graph replay, CUDA events"},
+                       "parallelism": f"replicas x{world}",
+                       "timing": "CUDA graph replay, CUDA events around every replay on the replay stream; "
+                                 "clocks sampled every 20 ms across all timed regions"},
             "prefill": {"tok_s": pre_tok_s, "ms_per_4096_chunk": 1e3 * t_chunk,
                         "tensor_tflops": pre_flops / t_chunk / 1e12,
-                        "frac_of_peak": pre_flops / t_chunk / 1e12 / pk["bf16_tflops_sustained"]},
+                        "frac_of_burst_peak": pre_flops / t_chunk / 1e12 / pk["bf16_tflops"],
+                        "frac_of_sustained_peak": pre_flops / t_chunk / 1e12 / pk["bf16_tflops_sustained"],
+                        "gemm_frac_of_burst_peak": {
+                            n: gemm_flops(c, chunk, n) / r["k_pre"][f"gemm_{n}"] / 1e12 / pk["bf16_tflops"]
+                            for n in ("gate_up", "down") if r["k_pre"].get(f"gemm_{n}")},
+                        "ms_per_4096_chunk_spread": spread(r["per_pre"], 1e3 / (T // chunk))},
             "decode": {"tok_s": dec_tok_s, "us_per_token": 1e6 * r["t_dec"] / args.steps / ndec,
+                       "us_per_token_spread": spread(r["per_dec"], 1e6 / ndec),
                        "roofline": roof_dec},
+            "ms_per_step_spread": spread(r["per_step"], 1e3),
             "decode_multirow": {f"T{Tm}": {"us_per_call": 1e6 * t, "tok_s": job_value(Tm, world, t),
                                            "distinct_experts_per_call": dx,
                                            "bytes_per_call": decode_bytes_rows(c, Tm, dx),

@@ -1,5 +1,6 @@
 """Host-side logic of bench.py: algorithmic work per unit and the multi-rank
 reduction (world size 2 over gloo on the CPU)."""
+import json
 import os
 import socket
 
@@ -28,13 +29,15 @@ def test_variant_summary_fractions():
     """The format-variant summary divides the algorithmic work by the measured
     times and the peaks it is given."""
     c = dict(H=2048, E=256, I=512, top_k=8)
-    pk = dict(hbm_gbs=6000.0, bf16_tflops_sustained=1500.0)
+    pk = dict(hbm_gbs=6000.0, bf16_tflops=1800.0, bf16_tflops_sustained=1500.0)
     w = dict(t_pre=0.5e-3, t_dec=16e-6, bits=8, k_pre={"gemm_gate_up": 250e-6, "gemm_down": 150e-6})
     v = bench.variant_summary(c, w, 4096, 1, pk)
     flops = bench.gemm_flops(c, 4096, "gate_up") + bench.gemm_flops(c, 4096, "down")
     assert abs(v["prefill"]["tensor_tflops"] - flops / 0.5e-3 / 1e12) < 1e-9
-    assert abs(v["prefill"]["frac_of_peak"] - flops / 0.5e-3 / 1e12 / 1500.0) < 1e-12
-    assert abs(v["prefill"]["gemm_frac_of_peak"]["down"] - bench.gemm_flops(c, 4096, "down") / 150e-6 / 1e12 / 1500.0) < 1e-12
+    assert abs(v["prefill"]["frac_of_burst_peak"] - flops / 0.5e-3 / 1e12 / 1800.0) < 1e-12
+    assert abs(v["prefill"]["frac_of_sustained_peak"] - flops / 0.5e-3 / 1e12 / 1500.0) < 1e-12
+    assert abs(v["prefill"]["gemm_frac_of_burst_peak"]["down"]
+               - bench.gemm_flops(c, 4096, "down") / 150e-6 / 1e12 / 1800.0) < 1e-12
     assert v["decode_T1"]["bytes_per_call"] == 32194560
     assert abs(v["decode_T1"]["frac_of_hbm"] - 32194560 / 16e-6 / 1e9 / 6000.0) < 1e-12
 
@@ -79,11 +82,19 @@ def test_measured_traffic_follows_the_sources(tmp_path, monkeypatch):
     (src / "k.cu").write_text("kernel v1\n")
     (tmp_path / "profiles").mkdir()
     digest = hashlib.sha256(b"kernel v1\n").hexdigest()
-    (tmp_path / "profiles" / "traffic.md").write_text(
-        "| kernel | source files | sha256 | dram bytes per launch | from |\n|---|---|---|---|---|\n"
-        f"| my_kernel | csrc/k.cu | {digest} | 12345 | a capture |\n")
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"kernels": [
+        {"kernel": "my_kernel", "sources": ["csrc/k.cu"], "sha256": digest, "dram_bytes_per_launch": 12345,
+         "capture": "a capture"}]}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.measured_traffic("my_kernel") == 12345
     assert bench.measured_traffic("other_kernel") is None
     (src / "k.cu").write_text("kernel v2\n")          # the kernel changed after the capture
     assert bench.measured_traffic("my_kernel") is None
+
+
+def test_spread_percentiles():
+    """Per-replay spread: median and the 10th / 90th percentiles, scaled."""
+    sp = bench.spread([3.0, 1.0, 2.0, 4.0, 5.0], 1e3)
+    assert sp["median"] == 3000.0 and sp["replays"] == 5
+    assert abs(sp["p10"] - 1400.0) < 1e-9 and abs(sp["p90"] - 4600.0) < 1e-9
+    assert bench.spread([]) is None

@@ -434,6 +434,32 @@ def test_decode_wait_timeout_is_reported(mw, torch):
     assert dl.status() == 0
 
 
+def test_decode_after_timeout_without_reinit(mw, torch):
+    """A batch-1 call that gives up its waits still advances the call counter
+    its exchanged words are tagged with: with the test hook turned off again and
+    no workspace re-initialisation, the next call must not take any of the
+    aborted call's words for its own, so it matches the oracle (the sticky
+    status word keeps the earlier timeout bit)."""
+    import ctypes
+    L, x = S.draw_config("decode_T1")
+    dl = mw.DeviceLayer(L)
+    ws = dl.workspace(1)
+    xd = mw.tokens_to_device(x)
+    stream = torch.cuda.current_stream().cuda_stream
+    mw.forward_decode(dl, xd)             # a normal call first: the counter is past 0
+    mw._check(mw.moe_w4_test_skip_publish(ws.data_ptr(), ws.numel(), 1, stream), "hook")
+    out = torch.empty((1, L.H), dtype=torch.bfloat16, device="cuda")
+    mw._check(mw.moe_w4_forward_decode(ctypes.byref(dl.c), 1, xd.data_ptr(), out.data_ptr(), ws.data_ptr(),
+                                       ws.numel(), stream), "decode")
+    mw._check(mw.moe_w4_test_skip_publish(ws.data_ptr(), ws.numel(), 0, stream), "hook off")
+    torch.cuda.synchronize()
+    assert dl.status() & mw.MOE_W4_STATUS_WAIT_TIMEOUT
+    x2 = S.draw_tokens(L, 3, seed=123)
+    for t in range(3):
+        got = to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x2[t:t + 1])))
+        check_out(got, O.moe_layer(L, x2[t:t + 1])["out"])
+
+
 def test_trace_events_outside_capture(mw, torch):
     """Kernel timing events recorded around an eager (not captured) call: the call
     succeeds and every event completes in order."""
