@@ -58,6 +58,7 @@ constexpr int kRE = 8;                  // router: experts per CTA (one 32-byte 
 constexpr int kMaxRouterRows = 4;       // router: H rows per thread, at most
 constexpr int kScoreReplicas = 8;       // copies of the published score partials (readers spread over them)
 constexpr int kHReplicas = 8;           // copies of the published h and its piece sums
+constexpr int kGuParts = 4;             // gate/up code slices arrive in this many parts (one barrier each)
 
 struct FusedArgs {
     const uint16_t* x;          // [H] bf16
@@ -442,11 +443,12 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     float* dred = reinterpret_cast<float*>(sm + L.dred);
     uint8_t* misc = sm + L.misc;
     // TMA boxes of 128-byte code rows: 256 columns of 4-bit codes, 128 of one-byte codes.
-    // Gate/up slices come in two halves of their box columns (one 3-D copy per matrix
-    // and half, one barrier per half), each slot's down rows in one 3-D copy.
+    // Gate/up slices come in kGuParts parts of their box columns (one 3-D copy per
+    // matrix and part, one barrier per part, so the GEMV starts on the first part),
+    // each slot's down rows in one 3-D copy.
     const int nbox_gu = H * kBits / 1024, nbox_dn = I * kBits / 1024;
-    uint64_t* bar_gu = reinterpret_cast<uint64_t*>(misc);               // [2] halves of the gate/up slices
-    uint64_t* bar_dn = bar_gu + 2;                                       // routed down rows
+    uint64_t* bar_gu = reinterpret_cast<uint64_t*>(misc);               // [kGuParts] parts of the gate/up slices
+    uint64_t* bar_dn = bar_gu + kGuParts;                                // routed down rows
     uint64_t* bar_dsh = bar_dn + 1;                                      // shared expert's down rows
     uint64_t* bar_sb = bar_dsh + 1;                                      // gate/up scales, biases (warp 0's cp.async)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_sb + 1);
@@ -477,8 +479,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     // The barriers first: their initialisation is published with a release fence,
     // which must not wait for the router loads below.
     if (tid == 0) {
-        mbar_init(&bar_gu[0], 1);
-        mbar_init(&bar_gu[1], 1);
+        for (int q = 0; q < kGuParts; ++q) mbar_init(&bar_gu[q], 1);
         mbar_init(bar_dn, 1);
         mbar_init(bar_dsh, 1);
         mbar_init(bar_sb, 1);
@@ -525,7 +526,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     auto issue_gateup = [&](int e) {
         const bool sh = (e >= E);
         const int grow = (sh ? 0 : e * I) + ei * RG;
-        const int hb = nbox_gu / 2;
+        const int hb = nbox_gu / kGuParts;   // box columns per part
         const uint32_t gsz = RG * (H / 64) * 2;   // one scale (or bias) slice
         const size_t go = (size_t)grow * (H / 64);
         mbar_arrive_expect_tx(bar_sb, 4 * gsz);
@@ -533,7 +534,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         bulk_load(gsb + RG * (H / 64), (sh ? a.sgb : a.gb) + go, gsz, bar_sb);
         bulk_load(usb, (sh ? a.sus : a.us) + go, gsz, bar_sb);
         bulk_load(usb + RG * (H / 64), (sh ? a.sub : a.ub) + go, gsz, bar_sb);
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kGuParts; ++h) {
             mbar_arrive_expect_tx(&bar_gu[h], 2u * hb * RG * 128);
             tma_load_3d(gcodes + (size_t)h * hb * RG * 128, sh ? &msg : &mg, 0, grow, h * hb, &bar_gu[h]);
             tma_load_3d(ucodes + (size_t)h * hb * RG * 128, sh ? &msu : &mu, 0, grow, h * hb, &bar_gu[h]);
@@ -765,14 +766,14 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         // groups gg = warp, warp + kFWarps, ... (one in each half of the columns with
         // 32 groups and 16 warps): each group's B fragments are loaded once for all
         // the tiles, whose MMA chains are independent
-        const int ntile = 2 * (RG / 16), ngrp = H / 64, half = ngrp / 2;
+        const int ntile = 2 * (RG / 16), ngrp = H / 64;
         constexpr int kTC = 4;   // row tiles per pass
         for (int t0 = 0; t0 < ntile; t0 += kTC) {
             float acc[kTC][2];
 #pragma unroll
             for (int t = 0; t < kTC; ++t) acc[t][0] = acc[t][1] = 0.f;
             for (int gg = warp; gg < ngrp; gg += kFWarps) {
-                if (!mbar_wait(&bar_gu[gg / half], 0, abort_flag, status)) break;
+                if (!mbar_wait(&bar_gu[gg / (ngrp / kGuParts)], 0, abort_flag, status)) break;
                 uint32_t bf[8];
                 load_bfrag<CODE>(reinterpret_cast<const uint4*>(xperm), gg, bf);
                 float d[kTC][4];
@@ -965,14 +966,14 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     // ---------------------------------------------------------------- exit
     // a CTA that gave up advances the call counter itself (the tags of this call's
     // words must not be taken for the next call's), and no TMA copy of this CTA
-    // may still be in flight when it leaves
+    // may still be in flight when it leaves (without an abort every barrier has
+    // already been waited on)
     __syncthreads();
-    if (tid == 0) {
-        if (*abort_flag) st_relaxed_u32(&a.ctrl->pad[kCtrlEpochWord], xtag);
+    if (tid == 0 && *abort_flag) {
+        st_relaxed_u32(&a.ctrl->pad[kCtrlEpochWord], xtag);
         const int is = *issued;
         if (is & 1) {
-            mbar_drain(&bar_gu[0]);
-            mbar_drain(&bar_gu[1]);
+            for (int q = 0; q < kGuParts; ++q) mbar_drain(&bar_gu[q]);
         }
         if (is & 2) mbar_drain(bar_dn);
         if (is & 4) mbar_drain(bar_dsh);
@@ -1041,7 +1042,7 @@ static bool shape_ok(const moe_w4_layer& L) {
     if (k < 1 || k + 1 > kMaxSlots) return false;
     if (L.H % 256 || L.I % 256 || L.H > 4096 || L.I > 2048) return false;   // slices of 16 rows; <= 16 row tiles
     if (L.H % (kPE * k * 16)) return false;                                   // down rows per CTA: whole m16 tiles
-    if (L.H * bits / 1024 > 16 || (L.H * bits / 1024) % 2) return false;     // gate/up: two halves of box columns
+    if (L.H * bits / 1024 > 16 || (L.H * bits / 1024) % kGuParts) return false;   // gate/up: parts of box columns
     if (L.E < 128 || L.E > 256 || L.E % 32) return false;                     // top-k: 8 scores per lane
     const int EG = L.E / kRE, NR = k * kPE;                                   // router: 8 experts per CTA
     if (EG > NR || NR % EG || NR / EG > 8 || L.H % (NR / EG)) return false;   // row splits: at most 8 polling warps
@@ -1109,7 +1110,7 @@ cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16
                                 cudaStream_t st) {
     const int H = L.H, E = L.E, I = L.I, k = L.top_k;
     const int RG = I / kPE, DR = H / (kPE * k), b = code_bits_of(L);
-    const uint32_t hbox = H * b / 1024 / 2, dbox = I * b / 1024;   // box columns per copy
+    const uint32_t hbox = H * b / 1024 / kGuParts, dbox = I * b / 1024;   // box columns per copy
     CUtensorMap mg, mu, md, msg, msu, msd;
     bool ok = codes_map(&mg, L.gate.codes, (uint64_t)E * I, H, RG, hbox, b) &&
               codes_map(&mu, L.up.codes, (uint64_t)E * I, H, RG, hbox, b) &&
