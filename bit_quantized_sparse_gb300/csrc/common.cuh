@@ -404,6 +404,16 @@ MW4_DEV void dequant8_f16(uint32_t w, __half2 s2, __half2 s16, __half2 b2, uint3
 MW4_DEV float bf16_bits_to_float(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
 MW4_DEV float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+// silu(z) = z sigmoid(z) = h + h tanh(h) with h = z/2: one hardware tanh
+// (tanh.approx.f32, relative error about 2^-11, the size of the fp16 rounding the
+// result then gets) instead of an exponential and a reciprocal, which halves the
+// special-function work of the gate/up epilogue.
+MW4_DEV float silu_tanh(float z) {
+    const float h = 0.5f * z;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
 MW4_DEV float sigmoid_f(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
 

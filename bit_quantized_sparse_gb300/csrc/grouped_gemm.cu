@@ -33,7 +33,8 @@
 //   producer      1 warp, TMA: the step's packed codes and the tile's B rows,
 //                 contiguous in grouped order (gate/up: the token rows copied
 //                 by gather_rows_kernel, or x16 itself for the shared expert;
-//                 down: hh), plus an L2 prefetch of the tile's codes and rows
+//                 down: hh); no L2 prefetch of codes or rows (measured slower: the
+//                 prefetches occupy the TMA unit at every tile start)
 //   MMA           1 warp: TMEM allocation and the MMA loop (warp-uniform, one
 //                 elected lane issues tcgen05.mma with A read from tensor memory)
 // gather_rows_kernel first copies the token rows of x16 into grouped order, so
@@ -56,10 +57,7 @@ struct GemmArgs {
     const float* gamma;        // [T] (gate/up epilogue)
     const uint16_t* s0r; const uint16_t* b0r; const uint16_t* s1r; const uint16_t* b1r;   // routed
     const uint16_t* s0s; const uint16_t* b0s; const uint16_t* s1s; const uint16_t* b1s;   // shared
-    const uint32_t* c0r; const uint32_t* c1r; const uint32_t* c0s; const uint32_t* c1s;   // codes (L2 prefetch)
     uint16_t* out;             // hh [.][I] or ys [.][H]
-    const uint16_t* b_rows;    // B rows in grouped order (gate/up: xg, down: hh), for the L2 prefetch
-    const uint16_t* b_rows_sh; // the shared group's B rows (gate/up: x16 from row 0, down: hh)
     int E, k, T, H;            // H: row length of x
     int K;                     // reduction length (H or I)
     int rows_e;                // weight rows per expert (I or H)
@@ -243,11 +241,6 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
             const TileInfo ti = block_info(a, u.b0, u.m);
             const CUtensorMap* m0 = ti.sh ? &map0s : &map0r;
             const CUtensorMap* m1 = ti.sh ? &map1s : &map1r;
-            if (lane == 0) {   // the tile's packed codes are one contiguous range per matrix
-                const size_t rw = (size_t)a.K * BITS / 32;   // code words per weight row
-                prefetch_l2((ti.sh ? a.c0s : a.c0r) + (size_t)ti.arow * rw, (uint32_t)(kBM * rw * 4));
-                if (DUAL) prefetch_l2((ti.sh ? a.c1s : a.c1r) + (size_t)ti.arow * rw, (uint32_t)(kBM * rw * 4));
-            }
             for (int ks = 0; ks < nK; ++ks, ++gk) {
                 const int s = gk % SC;
                 if (!mbar_wait_warp(&c_empty[s], ((gk / SC) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
@@ -276,8 +269,6 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 // gate/up's shared rows are rows r0.. of x16; every other B row block
                 // starts at its first grouped position
                 const int brow = (DUAL && ti.sh) ? ti.r0 : ti.p0;
-                if (lane == 0)   // the tile's B rows are one contiguous range
-                    prefetch_l2((ti.sh ? a.b_rows_sh : a.b_rows) + (size_t)brow * a.K, (uint32_t)ti.nrows * a.K * 2);
                 for (int ks = 0; ks < nK; ++ks, ++gk) {
                     const int s = gk % SB;
                     if (!mbar_wait_warp(&b_empty[s], ((gk / SB) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
@@ -405,8 +396,13 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                     for (int grp = 0; grp < 2; ++grp) {
                         if (!DUAL && grp != hsel) continue;
                         const float sf = bf16_bits_to_float((uint16_t)(grp ? (s2w >> 16) : (s2w & 0xFFFFu)));
+                        const float bf = bf16_bits_to_float((uint16_t)(grp ? (b2w >> 16) : (b2w & 0xFFFFu)));
+                        // the group's rebuilt weights |s q + b| must stay within fp16 (q <= the
+                        // largest code magnitude: 15, 255, or 448 for E4M3)
+                        constexpr float kQmax = BITS == 4 ? 15.f : (E4M3 ? 448.f : 255.f);
+                        if (!(fmaf(fabsf(sf), kQmax, fabsf(bf)) <= 65504.f)) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
                         const __half s_h = __float2half_rn(sf), s_h16 = __float2half_rn(sf * 0.0625f);
-                        const __half b_h = __float2half_rn(bf16_bits_to_float((uint16_t)(grp ? (b2w >> 16) : (b2w & 0xFFFFu))));
+                        const __half b_h = __float2half_rn(bf);
                         const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16);
                         const __half2 b2 = __halves2half2(b_h, b_h);
 #pragma unroll
@@ -504,7 +500,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                     // operands, fp32 sums far below the fp32 limit)
                     float vmax = 0.f;
                     auto emit = [&](int j) {
-                        const float v = DUAL ? silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]) * cs[j]
+                        const float v = DUAL ? silu_tanh(__uint_as_float(g[j])) * __uint_as_float(u[j]) * cs[j]
                                              : __uint_as_float(g[j]);
                         vmax = fmaxf(vmax, fabsf(v));
                         op[(size_t)j * a.out_cols] = __half_as_ushort(__float2half_rn(v));
@@ -677,8 +673,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     a.blkinfo = p.blkinfo; a.unitinfo = nullptr; a.M = I / kBM;
     a.s0r = L.gate.scales; a.b0r = L.gate.biases; a.s1r = L.up.scales; a.b1r = L.up.biases;
     a.s0s = L.sh_gate.scales; a.b0s = L.sh_gate.biases; a.s1s = L.sh_up.scales; a.b1s = L.sh_up.biases;
-    a.c0r = L.gate.codes; a.c1r = L.up.codes; a.c0s = L.sh_gate.codes; a.c1s = L.sh_up.codes;
-    a.out = p.hh; a.K = H; a.rows_e = I; a.out_cols = I; a.b_rows = p.xg; a.b_rows_sh = p.x16;
+    a.out = p.hh; a.K = H; a.rows_e = I; a.out_cols = I;
     // persistent: one CTA per SM (never more CTAs than the largest tile count)
     const int grid_gu = p.max_tiles_gu < nsm ? p.max_tiles_gu : nsm;
     const int nrg = T * k;
@@ -695,7 +690,6 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     b.M = H / kBM; b.ntiles = p.ntiles + 1; b.unitinfo = p.unitinfo;
     b.s0r = L.down.scales; b.b0r = L.down.biases; b.s1r = nullptr; b.b1r = nullptr;
     b.s0s = L.sh_down.scales; b.b0s = L.sh_down.biases; b.s1s = nullptr; b.b1s = nullptr;
-    b.c0r = L.down.codes; b.c1r = nullptr; b.c0s = L.sh_down.codes; b.c1s = nullptr; b.b_rows = p.hh; b.b_rows_sh = p.hh;
     b.out = p.ys; b.K = I; b.rows_e = H; b.out_cols = H;
     const int grid_dn = p.max_tiles_dn < nsm ? p.max_tiles_dn : nsm;
     e = e4m3  ? launch_gemm<false, 8, true>(b, grid_dn, md, md, msd, msd, mh, mh, st)

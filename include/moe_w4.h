@@ -139,8 +139,21 @@ int moe_w4_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream)
 size_t moe_w4_status_offset(void);
 #define MOE_W4_STATUS_WAIT_TIMEOUT 1u  /* a bounded wait gave up              */
 #define MOE_W4_STATUS_BAD_INDEX    2u  /* a routing index was out of range    */
-#define MOE_W4_STATUS_FP16_RANGE   4u  /* a prefill intermediate left the fp16
-                                          range (|v| > 65504): output not finite */
+#define MOE_W4_STATUS_FP16_RANGE   4u  /* a value held in fp16 left its range
+                                          (|v| > 65504): output not valid */
+/* Value ranges.  The tensor-core paths hold activations (x), the weighted
+ * SwiGLU output h, each expert's weighted output and the rebuilt weights
+ * s * q + b (prefill and multi-row decode) in fp16; batch-1 decode holds x and h
+ * in fp16 (with 4-bit codes half of their entries divided by 16) and applies s
+ * and b in fp32.  Inputs must therefore keep these within
+ * the fp16 range: |x| <= 65504; per group |s| * qmax + |b| <= 65504 (qmax = 15
+ * for 4-bit codes, 255 for 8-bit codes, 448 for E4M3); h and the expert outputs
+ * <= 65504 in magnitude.  A kernel that sees a value beyond this sets
+ * MOE_W4_STATUS_FP16_RANGE.  Below the fp16 normal range (6.1e-5) values keep
+ * an absolute precision of 2^-25 rather than 11 significant bits: layers whose
+ * rebuilt weights, h or expert outputs are mostly below it (scales around 1e-6
+ * with unit activations) lose accuracy without any status bit.  Scale and
+ * activation together: scales of 1e3 with activations of 1e-6 are in range. */
 
 /* Routing of T tokens (sections "Qwen creates three different workload
  * shapes" and "Keep expert routing on the GPU").

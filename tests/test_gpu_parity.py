@@ -409,6 +409,64 @@ def test_prefill_fp16_range_status(mw, torch):
     assert dl.status() & mw.MOE_W4_STATUS_FP16_RANGE
 
 
+def _scaled_layer(L, a):
+    """The layer with every scale and bias times 2^a (exact in bf16) and the router
+    and shared-gate weights times 2^a too: with activations times 2^-a the routing
+    scores x . W_r and the shared gate are unchanged bit for bit."""
+    import copy
+    L2 = copy.deepcopy(L)
+    for nm in ("gate", "up", "down", "sh_gate", "sh_up", "sh_down"):
+        m = getattr(L2, nm)
+        for f in ("scales", "biases"):
+            v = S.bf16_bits_to_f32(getattr(m, f)).astype(np.float64) * 2.0 ** a
+            setattr(m, f, S.f32_to_bf16_bits(v.astype(np.float32)))
+    L2.router_w = (L.router_w.astype(np.float64) * 2.0 ** a).astype(np.float32)
+    L2.shared_gate = (L.shared_gate.astype(np.float64) * 2.0 ** a).astype(np.float32)
+    return L2
+
+
+def test_large_scales_small_activations(mw, torch):
+    """Scales of 1e1 .. 4e2 (the generator's times 2^12, exact in bf16) with
+    activations near 6e-5 (times 2^-14), router weights times 2^12 (the same
+    scores): the rebuilt weights, h and the expert outputs (up to about 4e4) stay
+    within fp16, so prefill and a 4-row decode match the oracle and the status
+    word stays clear.  (Batch-1 decode with 4-bit codes holds half of x divided by
+    16 in fp16, below the fp16 normal range at these activations: not run here.)"""
+    L0 = S.draw_layer(2048, 256, 512, 8, 1.0, seed=57)
+    x0 = S.draw_tokens(L0, 40, seed=57)
+    L = _scaled_layer(L0, 12)
+    x = S.f32_to_bf16_bits((S.bf16_bits_to_f32(x0).astype(np.float64) * 2.0 ** -14).astype(np.float32))
+    assert 30 < np.median(S.bf16_bits_to_f32(L.gate.scales)) < 100
+    dl = mw.DeviceLayer(L)
+    xd = mw.tokens_to_device(x)
+    r = mw.route(dl, xd)
+    torch.cuda.synchronize()
+    check_route(r, L, x)
+    ref = O.moe_layer(L, x)["out"]
+    check_out(to_np_bits(mw.forward_prefill(dl, xd)), ref)
+    check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[3:7]))), ref[3:7])
+    assert dl.status() == 0
+
+
+def test_weight_range_status(mw, torch):
+    """One group whose rebuilt weights exceed the fp16 range (scale 2^13, so
+    15 s > 65504) sets MOE_W4_STATUS_FP16_RANGE in the prefill; activations near
+    zero keep every other fp16 value in range, so the bit comes from the weights."""
+    L, _ = S.draw_config("tiny_T4")
+    import copy
+    L2 = copy.deepcopy(L)
+    sc = L2.gate.scales.copy()
+    sc[:, 0, 0] = S.f32_to_bf16_bits(np.array([8192.0], np.float32))[0]   # every expert's row 0, group 0
+    L2.gate.scales = sc
+    L2.sh_gate.scales = L2.sh_gate.scales.copy()
+    L2.sh_gate.scales[0, 0] = sc[0, 0, 0]
+    x = S.draw_tokens(L2, 4, seed=5)
+    dl = mw.DeviceLayer(L2)
+    mw.forward_prefill(dl, mw.tokens_to_device(x))
+    torch.cuda.synchronize()
+    assert dl.status() & mw.MOE_W4_STATUS_FP16_RANGE
+
+
 def test_decode_wait_timeout_is_reported(mw, torch):
     """Failure detection without a GPU fault: with the test hook on, one cluster
     of the batch-1 kernel does not publish its router sums, so the other CTAs'
