@@ -36,6 +36,9 @@ PREFILL_KERNELS = ["router_scores", "topk", "chunk_count", "scan", "assign", "ga
 DECODE_KERNELS = ["decode_router", "decode_gate_up", "decode_down"]   # the three-kernel path
 DECODE_FUSED = ["decode_fused"]
 SMALL_T = (4, 8)   # multi-row decode batches measured beside the step
+# prefill tile choices of the ablation table: (token rows per block, row blocks per down unit); the first is the default
+TILE_CHOICES = ((128, 4), (128, 2), (128, 1), (64, 4), (64, 2), (64, 1), (32, 1))
+ABLATION_T = (512, 2048, 4096)   # prefill sizes of the ablations (2048 rows = 16,384 assignments, 64 per expert)
 CPU_SAMPLE = (8192, 32)   # oracle sample for cpu_baseline: prefill rows, decode rows
 W8_REPLICAS = 8    # distinct one-byte-code layers each format-variant decode measurement cycles
 # weight codes: (bits, code_format) -- unsigned 4-bit, unsigned 8-bit, FP8 E4M3
@@ -61,6 +64,9 @@ def parse():
                          "kernels only)")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the 8-bit weight-format measurement (for launch lists of the step's kernels only)")
+    ap.add_argument("--ablations", action="store_true",
+                    help="also measure the prefill design choices against their alternatives (tile table, "
+                         "host-synchronised routing, router weights split per call); adds an 'ablations' object")
     return ap.parse_args()
 
 
@@ -371,6 +377,8 @@ def run_gpu(args, rank, local_rank, world, dist):
         variants[vname] = dict(t_pre=t8_pre, t_dec=t8_dec, k_pre=k8_pre, bits=bits)
         del l8, ws8
 
+    abl = run_ablations(torch, mw, c, layers[0], x, out, ws, stream, timed, capture, args) if args.ablations else None
+
     # end to end through host buffers, every step: the step's inputs are copied in
     # from pinned host memory and its outputs copied back, segment by segment (the
     # four 4096-row prefill chunks, then the decode rows).  A segment's rows go in
@@ -433,7 +441,69 @@ def run_gpu(args, rank, local_rank, world, dist):
         raise RuntimeError(f"device status {status}")
     return dict(c=c, L0=L0, x_np=x_np, xdec_np=xdec_np, t_step=t_step, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e, small=small,
                 per_step=per_step, per_pre=per_pre, per_dec=per_dec,
-                variants=variants, clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device))
+                variants=variants, clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device),
+                ablations=abl)
+
+
+def run_ablations(torch, mw, c, dl, x, out, ws, stream, timed, capture, args):
+    """The prefill's design choices against their alternatives, on the
+    workload's first layer and the first T rows of its prompt:
+    - tiles: ms per call for each (token rows per block, row blocks per down
+      unit) of TILE_CHOICES (CUDA-graph replays, like the step);
+    - routing: ms per call, eager calls, with the GPU-resident grouping and with
+      the host-synchronised one (moe_w4_ablation_prefill);
+    - router_prep: ms per call (graph replays) with the router weights prepared
+      once and split on every call."""
+    res = {"tiles_ms": {}, "routing_ms": {}, "router_prep_ms": {}}
+    st = lambda: torch.cuda.current_stream().cuda_stream
+
+    def graph_ms(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        return 1e3 * timed(capture(fn), args.steps) / args.steps
+
+    def eager_ms(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fn()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(n):
+                fn()
+            torch.cuda.synchronize()
+        return 1e3 * (time.perf_counter() - t0) / n
+
+    plain = mw.MoeW4Layer.from_buffer_copy(dl.c)
+    plain.router_prep = None
+    for Tm in ABLATION_T:
+        xs, os_ = x[:Tm], out[:Tm]
+        row = {}
+        try:
+            for bn, du in TILE_CHOICES:
+                assert mw.moe_w4_set_tile_override(bn, du) == mw.MOE_W4_OK
+                row[f"bn{bn}_du{du}"] = graph_ms(lambda: mw.forward_prefill(dl, xs, out=os_, ws=ws))
+        finally:
+            mw.moe_w4_set_tile_override(0, 0)
+        res["tiles_ms"][f"T{Tm}"] = row
+
+        def host_routed():
+            mw._check(mw.moe_w4_ablation_prefill(ctypes.byref(dl.c), Tm, xs.data_ptr(), os_.data_ptr(), ws.data_ptr(),
+                                                 ws.numel(), mw.MOE_W4_ABLATE_HOST_ROUTING, st()), "ablation")
+        n = max(args.steps, 5)
+        res["routing_ms"][f"T{Tm}"] = {
+            "gpu_resident_eager": eager_ms(lambda: mw.forward_prefill(dl, xs, out=os_, ws=ws), n),
+            "host_synchronised_eager": eager_ms(host_routed, n),
+            "gpu_resident_graph": graph_ms(lambda: mw.forward_prefill(dl, xs, out=os_, ws=ws))}
+
+        def split_each_call():
+            mw._check(mw.moe_w4_forward_prefill(ctypes.byref(plain), Tm, xs.data_ptr(), os_.data_ptr(), ws.data_ptr(),
+                                                ws.numel(), st()), "prefill")
+        res["router_prep_ms"][f"T{Tm}"] = {"prepared_once": row[f"bn{TILE_CHOICES[0][0]}_du{TILE_CHOICES[0][1]}"],
+                                          "split_every_call": graph_ms(split_each_call)}
+    if dl.status() != 0:
+        raise RuntimeError(f"device status {dl.status()} after the ablations")
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -645,6 +715,7 @@ def main():
             "e2e": {"value": job_value(units, world, r["t_e2e"] / args.steps), "unit": "tok/s",
                     "h2d_bytes_per_step": units * c["H"] * 2, "d2h_bytes_per_step": units * c["H"] * 2},
             "clocks": r["clocks"], "gpu": r["gpu"],
+            **({"ablations": r["ablations"]} if r.get("ablations") else {}),
             "context": {"pages_whole_model_M5_Max": {"prefill_tok_s_4K": 5749.9, "decode_tok_s_4K": 186.6,
                                                     "mlx_lm_prefill": 4737.5, "mlx_lm_decode": 140.9,
                                                     "note": "whole 40-layer model on an Apple M5 Max; context only"}}}

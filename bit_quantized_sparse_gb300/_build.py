@@ -11,7 +11,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_w4.so")
-SOURCES = ["api.cu", "router.cu", "grouping.cu", "decode.cu", "grouped_gemm.cu", "noalloc.cu", "decode_fused.cu"]
+SOURCES = ["api.cu", "router.cu", "grouping.cu", "decode.cu", "grouped_gemm.cu", "noalloc.cu", "decode_fused.cu",
+           "ablation.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]

@@ -1,12 +1,15 @@
 // C ABI of libmoe_w4: argument validation, workspace layout and the three
 // entry points (route, decode, prefill).  Everything is enqueued on the
 // caller's stream; nothing here allocates, frees or synchronises.
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "moe_w4_ablation.h"
 
 namespace mw4 {
 
@@ -29,6 +32,39 @@ void trace_kernels(int n) {
 
 static size_t up256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Tile override: moe_w4_set_tile_override, else MOE_W4_FORCE_TILE (read once).
+static std::atomic<int> g_tile_bn{0}, g_tile_du{0};
+static std::once_flag g_tile_env_once;
+static int set_tile(int bn, int du) {
+    if (bn != 0 && bn != 32 && bn != 64 && bn != 128) return MOE_W4_ERR_INVALID;
+    if (du != 0 && du != 1 && du != 2 && du != 4) return MOE_W4_ERR_INVALID;
+    g_tile_bn.store(bn);
+    g_tile_du.store(du);
+    return MOE_W4_OK;
+}
+static void read_tile_env() {
+    const char* v = std::getenv("MOE_W4_FORCE_TILE");
+    if (!v) return;
+    int bn = 0, du = 0;
+    for (const char* p = v; *p;) {
+        if (!std::strncmp(p, "bn=", 3)) bn = std::atoi(p + 3);
+        else if (!std::strncmp(p, "du=", 3)) du = std::atoi(p + 3);
+        const char* c = std::strchr(p, ',');
+        if (!c) break;
+        p = c + 1;
+    }
+    if (set_tile(bn, du) != MOE_W4_OK) std::fprintf(stderr, "moe_w4: MOE_W4_FORCE_TILE=%s ignored\n", v);
+}
+
+TileCfg tile_cfg(const moe_w4_layer& L, int T) {
+    std::call_once(g_tile_env_once, read_tile_env);
+    TileCfg c{kBN, (int64_t)T * L.top_k >= 64 * (int64_t)L.E ? down_blocks_per_unit(L.I) : 1};
+    const int bn = g_tile_bn.load(), du = g_tile_du.load();
+    if (bn) c.bn = bn;
+    if (du && (du == 1 || L.I <= kDownReuseMaxI)) c.du = du;   // a reused tile keeps its whole K in TMEM
+    return c;
+}
+
 WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     WsLayout w{};
     const size_t E = L.E, k = L.top_k, H = L.H, I = L.I;
@@ -36,7 +72,8 @@ WsLayout ws_layout(const moe_w4_layer& L, int T_max) {
     const size_t Td = T < (size_t)kDecodeMaxT ? T : (size_t)kDecodeMaxT;
     w.T_max = (int)T;
     w.nchunk_max = (int)((T + kChunk - 1) / kChunk);
-    w.max_blocks = (int)((T * k + kBN - 1) / kBN + E + (T + kBN - 1) / kBN);
+    // blocks of kBN rows, or of as few as kMinBN under a tile override
+    w.max_blocks = (int)((T * k + kMinBN - 1) / kMinBN + E + (T + kMinBN - 1) / kMinBN);
     w.max_tiles_gu = w.max_blocks * (int)(I / kBM);
     w.max_tiles_dn = w.max_blocks * (int)(H / kBM);
     size_t o = 0;
@@ -88,7 +125,8 @@ static int check_layer(const moe_w4_layer* L) {
     if (L->code_format != MOE_W4_CODES_UINT && L->code_format != MOE_W4_CODES_E4M3) return MOE_W4_ERR_UNSUPPORTED;
     if (L->code_format == MOE_W4_CODES_E4M3 && L->code_bits != 8) return MOE_W4_ERR_UNSUPPORTED;
     if (!L->router_w || !L->shared_gate) return MOE_W4_ERR_INVALID;
-    if (!aligned16(L->router_w) || !aligned16(L->shared_gate) || (L->router_bias && !aligned16(L->router_bias)))
+    if (!aligned16(L->router_w) || !aligned16(L->shared_gate) || (L->router_bias && !aligned16(L->router_bias)) ||
+        (L->router_prep && !aligned16(L->router_prep)))
         return MOE_W4_ERR_ALIGN;
     const moe_w4_mat* ms[6] = {&L->gate, &L->up, &L->down, &L->sh_gate, &L->sh_up, &L->sh_down};
     for (const moe_w4_mat* m : ms) {
@@ -146,6 +184,20 @@ using namespace mw4;
 
 extern "C" {
 
+size_t moe_w4_router_prep_bytes(const moe_w4_layer* L) {
+    if (check_layer(L) != MOE_W4_OK) return 0;
+    return router_prep_bytes(*L);
+}
+
+int moe_w4_prepare_router(const moe_w4_layer* L, void* dst, size_t dst_bytes, cudaStream_t stream) {
+    const int r = check_layer(L);
+    if (r) return r;
+    if (!dst) return MOE_W4_ERR_INVALID;
+    if (!aligned16(dst)) return MOE_W4_ERR_ALIGN;
+    if (dst_bytes < router_prep_bytes(*L)) return MOE_W4_ERR_WORKSPACE;
+    return launch_status(launch_router_prep(*L, static_cast<uint16_t*>(dst), stream));
+}
+
 size_t moe_w4_workspace_size(const moe_w4_layer* L, int T_max) {
     if (check_layer(L) != MOE_W4_OK || T_max < 0) return 0;
     return ws_layout(*L, T_max).total;
@@ -167,6 +219,11 @@ int moe_w4_test_skip_publish(void* workspace, size_t ws_bytes, int on, cudaStrea
 }
 
 int moe_w4_last_traced_kernels(void) { return g_traced_kernels; }
+
+int moe_w4_set_tile_override(int bn, int du) {
+    std::call_once(g_tile_env_once, read_tile_env);   // the environment first, so that this call wins
+    return set_tile(bn, du);
+}
 
 int moe_w4_set_trace_events(cudaEvent_t* events, int n_events) {
     if (events && n_events < 1) return MOE_W4_ERR_INVALID;
@@ -201,7 +258,7 @@ int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x, int32_t* to
 }
 
 static int run_grouped(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out, void* workspace,
-                       const WsLayout& w, cudaStream_t stream);
+                       const WsLayout& w, cudaStream_t stream, bool host_routing = false);
 
 int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out, void* workspace,
                           size_t ws_bytes, cudaStream_t stream) {
@@ -245,12 +302,14 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, mo
 // Routing, grouping and the grouped tensor-core GEMMs over T rows (the
 // workspace checks already done).
 static int run_grouped(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out, void* workspace,
-                       const WsLayout& w, cudaStream_t stream) {
+                       const WsLayout& w, cudaStream_t stream, bool host_routing) {
     RouteOut o = route_ws(workspace, w);
     trace_mark(stream, 0);
     cudaError_t e = launch_router_prefill(*L, T, x, o, stream);
-    if (e == cudaSuccess) e = launch_grouping(*L, T, o, stream);
+    bool bad = false;
+    if (e == cudaSuccess) e = host_routing ? host_grouping(*L, T, o, stream, &bad) : launch_grouping(*L, T, o, stream);
     if (e != cudaSuccess) return MOE_W4_ERR_LAUNCH;
+    if (bad) return MOE_W4_ERR_DEVICE;
     PrefillWs p{};
     p.blkinfo = o.blkinfo; p.unitinfo = o.unitinfo; p.ntiles = o.ntiles;
     p.offsets = o.offsets; p.perm = o.perm; p.inv = o.inv; p.topk_w = o.topk_w; p.gamma = o.gamma;
@@ -277,6 +336,20 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, m
     WsLayout w;
     if ((r = check_ws(*L, T, workspace, ws_bytes, &w))) return r;
     return run_grouped(L, T, x, out, workspace, w, stream);
+}
+
+int moe_w4_ablation_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out, void* workspace,
+                            size_t ws_bytes, int mode, cudaStream_t stream) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (mode != MOE_W4_ABLATE_HOST_ROUTING) return MOE_W4_ERR_INVALID;
+    if (T < 0) return MOE_W4_ERR_INVALID;
+    if (T == 0) return MOE_W4_OK;
+    if (!x || !out) return MOE_W4_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(out)) return MOE_W4_ERR_ALIGN;
+    WsLayout w;
+    if ((r = check_ws(*L, T, workspace, ws_bytes, &w))) return r;
+    return run_grouped(L, T, x, out, workspace, w, stream, true);
 }
 
 const char* moe_w4_strerror(int status) {

@@ -12,10 +12,9 @@
 // 16k routed CTAs also owns output rows [c*DR, (c+1)*DR), DR = H/(16k), of the
 // down projection of all k+1 slots.
 //
-//   1. router: CTA c computes complete scores x . W_r[:, e] (+bias) over all H
-//      for its experts e in [c*EPC, (c+1)*EPC) (EPC = E/(16(k+1)) rounded up;
-//      these W_r loads go out first) and publishes them; every CTA also forms
-//      the shared gate sigmoid(x . g) itself.  Every value that crosses CTAs
+//   1. router: routed CTA c sums 8 experts' scores x . W_r[:, e] over a
+//      quarter of the H rows (these W_r loads go out first) and publishes the
+//      partials; every CTA also forms the shared gate sigmoid(x . g) itself.  Every value that crosses CTAs
 //      is an 8-byte (value, call tag) word, so that a reader polls the data
 //      itself rather than a counter and then the data.
 //   2. every routed CTA polls the E scores (bounded wait), one warp selects
@@ -82,12 +81,13 @@ struct FusedArgs {
 };
 
 // smem carve-up (byte offsets from a 1024-aligned base), computed on both sides.
-// After the gate/up GEMV its code slices are dead: h (in B order) and its group
-// sums then live in the gate codes region, the down partial sums in the up one.
+// After the gate/up GEMV its code slices are dead: h (in B order) and its
+// 16-value piece sums then live in the gate codes region, the down partial sums
+// and row sums in the up one.
 struct FusedSmem {
     uint32_t gcodes, ucodes, dcodes, dslot, gsb, usb, dsb, xperm, xsum, xbs, logits, gred, gsum, usum, wred,
         misc, total;
-    uint32_t hperm, hsum, hbs, hpiece, dred;   // aliases (see above)
+    uint32_t hperm, hpiece, dred;   // aliases (see above)
     uint32_t code_region;              // bytes of one gate/up code region
     int RG, DR, NS;
     __host__ __device__ FusedSmem(int H, int E, int I, int k, int bits) {
@@ -122,15 +122,13 @@ struct FusedSmem {
         misc = take(512, 16);
         total = o;
         hperm = gcodes;
-        hsum = gcodes + NS * I * 2;
-        hbs = hsum + NS * (I / 64) * 4;
-        hpiece = hbs + NS * (I / 64) * 4;   // [NS][I/16][2]
-        dred = ucodes;
+        hpiece = gcodes + NS * I * 2;   // [NS][I/16][2]
+        dred = ucodes;                  // [NS * (I/64) * DR/16][16], then [NS][DR] row sums
     }
     // the aliased buffers fit their regions
     __host__ __device__ bool aliases_fit(int I) const {
-        return (uint32_t)(NS * I * 2 + 2 * NS * (I / 64) * 4 + NS * (I / 16) * 2 * 4) <= code_region &&
-               (uint32_t)(NS * (I / 64) * DR * 4) <= code_region;
+        return (uint32_t)(NS * I * 2 + NS * (I / 16) * 2 * 4) <= code_region &&
+               (uint32_t)((NS * (I / 64) * DR + NS * DR) * 4) <= code_region;
     }
 };
 
@@ -157,84 +155,8 @@ MW4_DEV void st_tagged_u32(uint64_t* p, uint32_t v, uint32_t tag) {
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(w) : "memory");
 }
 
-// One warp: rows [r0, r0+16) of a swizzled codes tile set, one 64-column
-// group; adds the group's dot products of rows r0+g and r0+g+8 (g = lane/4)
-// to d[0] and d[2].  A holds fp16 1024 + q for the even nibbles of a code
-// byte and 1024 + 16 q for the odd ones (one bitwise op per pair, one shift
-// per word); B (`bperm`, 16 bytes per (32-column block, lane%4)) holds the
-// matching activations, the odd positions divided by 16, so that every
-// product is q * value + 1024 * (stored B value).
-// Code tiles are TMA boxes of 32 words x `rows` rows, 128-byte swizzled, box b
-// at b*rows*128.
-MW4_DEV void w4_group_mma(const uint8_t* codes, int rows, int r0, int grp, const uint4* bperm, float (&d)[4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-    constexpr uint32_t M = 0x64006400u;
-    // both rows of the thread (r0+g, r0+g+8) share the swizzle phase g; a group
-    // (2 blocks of 32 columns) lies inside one box of 8 blocks
-    const int blk0 = grp * 2;
-    const uint8_t* row0 = codes + (size_t)(blk0 >> 3) * rows * 128 + (r0 + g) * 128 + c * 4;
-    const uint8_t* row1 = row0 + 8 * 128;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int blk = blk0 + h;
-        const int off = ((blk & 7) ^ g) << 4;
-        const uint32_t wg = *reinterpret_cast<const uint32_t*>(row0 + off);
-        const uint32_t wh = *reinterpret_cast<const uint32_t*>(row1 + off);
-        const uint4 bv = bperm[blk * 4 + c];
-        uint32_t a[4];
-        a[0] = (wg & 0x000F000Fu) | M;   // nibbles 0, 4
-        a[1] = (wh & 0x000F000Fu) | M;
-        a[2] = (wg & 0x00F000F0u) | M;   // nibbles 1, 5 (x16)
-        a[3] = (wh & 0x00F000F0u) | M;
-        mma_f16_16816(d, a, bv.x, bv.y);
-        const uint32_t wg8 = wg >> 8, wh8 = wh >> 8;
-        a[0] = (wg8 & 0x000F000Fu) | M;  // nibbles 2, 6
-        a[1] = (wh8 & 0x000F000Fu) | M;
-        a[2] = (wg8 & 0x00F000F0u) | M;  // nibbles 3, 7 (x16)
-        a[3] = (wh8 & 0x00F000F0u) | M;
-        mma_f16_16816(d, a, bv.z, bv.w);
-    }
-}
-
 // Code formats of the one-kernel decode: unsigned 4-bit, unsigned 8-bit, FP8 E4M3.
 enum : int { kCodeU4 = 0, kCodeU8 = 1, kCodeE4M3 = 2 };
-
-// One warp, one-byte codes: rows [r0, r0+16), one 64-column group = 4 chunks of
-// 16 codes (one 16-byte chunk of 4 words per row, one MMA each); adds the
-// group's dot products of rows r0+g and r0+g+8 to d[0] and d[2].  Lane c takes
-// word c of a chunk: 8-bit codes give fp16 1024 + q for bytes (0, 2) and (1, 3)
-// (one bitwise op per pair, one shift per word), E4M3 codes their exact values;
-// B (`bperm`, 8 bytes per 4-column unit u = chunk * 4 + lane%4) holds the
-// matching activations (x[4u], x[4u+2]), (x[4u+1], x[4u+3]).
-template <bool E4M3>
-MW4_DEV void w8_group_mma(const uint8_t* codes, int rows, int r0, int grp, const uint2* bperm, float (&d)[4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-    constexpr uint32_t M = 0x64006400u;
-    // both rows of the thread share the swizzle phase g; the group's 4 chunks lie
-    // inside one box of 8 chunks
-    const int ch0 = grp * 4;
-    const uint8_t* row0 = codes + (size_t)(ch0 >> 3) * rows * 128 + (r0 + g) * 128 + c * 4;
-    const uint8_t* row1 = row0 + 8 * 128;
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        const int ch = ch0 + h;
-        const int off = ((ch & 7) ^ g) << 4;
-        const uint32_t wg = *reinterpret_cast<const uint32_t*>(row0 + off);
-        const uint32_t wh = *reinterpret_cast<const uint32_t*>(row1 + off);
-        const uint2 bv = bperm[ch * 4 + c];
-        uint32_t a[4];
-        if (E4M3) {
-            e4m3x4_to_f16(wg, a[0], a[2]);   // (c0, c2), (c1, c3)
-            e4m3x4_to_f16(wh, a[1], a[3]);
-        } else {
-            a[0] = (wg & 0x00FF00FFu) | M;   // bytes 0, 2
-            a[1] = (wh & 0x00FF00FFu) | M;
-            a[2] = ((wg >> 8) & 0x00FF00FFu) | M;   // bytes 1, 3
-            a[3] = ((wh >> 8) & 0x00FF00FFu) | M;
-        }
-        mma_f16_16816(d, a, bv.x, bv.y);
-    }
-}
 
 // The B fragments of one 64-column group for this lane (8 words): 4-bit codes
 // the 16-byte entries of its two 32-column blocks, one-byte codes the 8-byte
@@ -258,106 +180,93 @@ MW4_DEV void load_bfrag(const uint4* bperm, int grp, uint32_t (&b)[8]) {
     }
 }
 
-// group_mma with the B fragments already in registers (load_bfrag).
+// The dot engine: mma.sync m16n8k16 with the weights as A (16 rows x 16
+// columns) and the activation as column 0 of B; per 64-column group
+// w = s*q + b, so a row's dot is s * (sum of q*value) + b * (sum of values),
+// finished in fp32 by the callers.
+// The A fragment of one MMA from a thread's two code words (rows r0+g and
+// r0+g+8, g = lane/4), one bitwise op per register: 4-bit codes give fp16
+// 1024 + q for the even nibbles of a byte and 1024 + 16 q for the odd ones
+// (step 0: nibbles 0,4 and 1,5; step 1, after a shift of the word by 8:
+// nibbles 2,6 and 3,7), so B holds the matching activations with the odd
+// positions divided by 16 and every product is q * value + 1024 * (stored B
+// value); 8-bit codes give 1024 + q for bytes (0, 2) and (1, 3); E4M3 codes
+// their exact values (no offset).
+// Code tiles are TMA boxes of 32 words x `rows` rows, 128-byte swizzled, box b
+// at b*rows*128; a 64-column group lies inside one box.
 template <int CODE>
-MW4_DEV void group_mma_b(const uint8_t* codes, int rows, int r0, int grp, const uint32_t (&b)[8], float (&d)[4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+MW4_DEV void a_frag(uint32_t wg, uint32_t wh, uint32_t (&a)[4]) {
     constexpr uint32_t M = 0x64006400u;
     if (CODE == kCodeU4) {
-        const int blk0 = grp * 2;
-        const uint8_t* row0 = codes + (size_t)(blk0 >> 3) * rows * 128 + (r0 + g) * 128 + c * 4;
-        const uint8_t* row1 = row0 + 8 * 128;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int off = (((blk0 + h) & 7) ^ g) << 4;
-            const uint32_t wg = *reinterpret_cast<const uint32_t*>(row0 + off);
-            const uint32_t wh = *reinterpret_cast<const uint32_t*>(row1 + off);
-            uint32_t a[4];
-            a[0] = (wg & 0x000F000Fu) | M;
-            a[1] = (wh & 0x000F000Fu) | M;
-            a[2] = (wg & 0x00F000F0u) | M;
-            a[3] = (wh & 0x00F000F0u) | M;
-            mma_f16_16816(d, a, b[4 * h], b[4 * h + 1]);
-            const uint32_t wg8 = wg >> 8, wh8 = wh >> 8;
-            a[0] = (wg8 & 0x000F000Fu) | M;
-            a[1] = (wh8 & 0x000F000Fu) | M;
-            a[2] = (wg8 & 0x00F000F0u) | M;
-            a[3] = (wh8 & 0x00F000F0u) | M;
-            mma_f16_16816(d, a, b[4 * h + 2], b[4 * h + 3]);
-        }
+        a[0] = (wg & 0x000F000Fu) | M;
+        a[1] = (wh & 0x000F000Fu) | M;
+        a[2] = (wg & 0x00F000F0u) | M;
+        a[3] = (wh & 0x00F000F0u) | M;
+    } else if (CODE == kCodeE4M3) {
+        e4m3x4_to_f16(wg, a[0], a[2]);
+        e4m3x4_to_f16(wh, a[1], a[3]);
     } else {
-        const int ch0 = grp * 4;
-        const uint8_t* row0 = codes + (size_t)(ch0 >> 3) * rows * 128 + (r0 + g) * 128 + c * 4;
-        const uint8_t* row1 = row0 + 8 * 128;
+        a[0] = (wg & 0x00FF00FFu) | M;
+        a[1] = (wh & 0x00FF00FFu) | M;
+        a[2] = ((wg >> 8) & 0x00FF00FFu) | M;
+        a[3] = ((wh >> 8) & 0x00FF00FFu) | M;
+    }
+}
+
+// NU independent units of one warp, each rows r0[q]..+15 of the codes tile set
+// codes[q] (`rows` rows) against one 64-column group grp[q], adding to d[q] what
+// group_mma adds.  The MMAs are issued step by step across the units, so that
+// consecutive MMAs accumulate into different units: a unit's chain of
+// dependent MMAs (24 cycles each) is covered by the other units' MMAs instead
+// of stalling the warp.  B comes from shared memory per unit (bperm[q]), or,
+// with SHARED_B, from the registers `bsh` (load_bfrag) for every unit.
+template <int CODE, int NU, bool SHARED_B>
+MW4_DEV void units_mma(const uint8_t* const (&codes)[NU], int rows, const int (&r0)[NU], const int (&grp)[NU],
+                       const uint4* const (&bperm)[NU], const uint32_t (&bsh)[8], float (&d)[NU][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    // 4-bit codes: 2 blocks of 32 columns per group, 2 MMAs per block; one-byte
+    // codes: 4 chunks of 16 columns, one MMA each
+    constexpr int kSteps = CODE == kCodeU4 ? 2 : 4;
+    constexpr int kPerBox = CODE == kCodeU4 ? 2 : 4;   // blocks (chunks) per group
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int off = (((ch0 + h) & 7) ^ g) << 4;
-            const uint32_t wg = *reinterpret_cast<const uint32_t*>(row0 + off);
-            const uint32_t wh = *reinterpret_cast<const uint32_t*>(row1 + off);
-            uint32_t a[4];
-            if (CODE == kCodeE4M3) {
-                e4m3x4_to_f16(wg, a[0], a[2]);
-                e4m3x4_to_f16(wh, a[1], a[3]);
+    for (int h = 0; h < kSteps; ++h) {
+        uint32_t wg[NU], wh[NU], b[NU][4];
+#pragma unroll
+        for (int q = 0; q < NU; ++q) {
+            const int bk = grp[q] * kPerBox + h;   // block (chunk) of the group
+            const uint8_t* row0 = codes[q] + (size_t)(bk >> 3) * rows * 128 + (r0[q] + g) * 128 + c * 4 +
+                                  (((bk & 7) ^ g) << 4);
+            wg[q] = *reinterpret_cast<const uint32_t*>(row0);
+            wh[q] = *reinterpret_cast<const uint32_t*>(row0 + 8 * 128);
+            if (SHARED_B) {
+                if (CODE == kCodeU4) {
+                    b[q][0] = bsh[4 * h]; b[q][1] = bsh[4 * h + 1]; b[q][2] = bsh[4 * h + 2]; b[q][3] = bsh[4 * h + 3];
+                } else {
+                    b[q][0] = bsh[2 * h]; b[q][1] = bsh[2 * h + 1];
+                }
+            } else if (CODE == kCodeU4) {
+                const uint4 v = bperm[q][bk * 4 + c];
+                b[q][0] = v.x; b[q][1] = v.y; b[q][2] = v.z; b[q][3] = v.w;
             } else {
-                a[0] = (wg & 0x00FF00FFu) | M;
-                a[1] = (wh & 0x00FF00FFu) | M;
-                a[2] = ((wg >> 8) & 0x00FF00FFu) | M;
-                a[3] = ((wh >> 8) & 0x00FF00FFu) | M;
+                const uint2 v = reinterpret_cast<const uint2*>(bperm[q])[bk * 4 + c];
+                b[q][0] = v.x; b[q][1] = v.y;
             }
-            mma_f16_16816(d, a, b[2 * h], b[2 * h + 1]);
+        }
+#pragma unroll
+        for (int q = 0; q < NU; ++q) {
+            uint32_t a[4];
+            a_frag<CODE>(wg[q], wh[q], a);
+            mma_f16_16816(d[q], a, b[q][0], b[q][1]);
+        }
+        if (CODE == kCodeU4) {
+#pragma unroll
+            for (int q = 0; q < NU; ++q) {
+                uint32_t a[4];
+                a_frag<CODE>(wg[q] >> 8, wh[q] >> 8, a);
+                mma_f16_16816(d[q], a, b[q][2], b[q][3]);
+            }
         }
     }
-}
-
-template <int CODE>
-MW4_DEV void group_mma(const uint8_t* codes, int rows, int r0, int grp, const uint4* bperm, float (&d)[4]) {
-    if (CODE == kCodeU4)
-        w4_group_mma(codes, rows, r0, grp, bperm, d);
-    else
-        w8_group_mma<CODE == kCodeE4M3>(codes, rows, r0, grp, reinterpret_cast<const uint2*>(bperm), d);
-}
-
-// Rows r0+g and r0+g+8 dotted with the activation over groups [grp0, grp1):
-// per group w = s*q + b, so the dot is s * (sum of q*value) + b * (sum of
-// values); `bsum` holds per-group sums of the stored B values (for the 1024
-// offset), `tsum` the true sums of the activation.
-// With one-byte codes a TMA box holds 2 groups (128 columns) instead of 4, and
-// `bperm` is read as 8-byte units.
-// `box_bars[i]` (if given) completes when groups [i*gpb, (i+1)*gpb) have landed.
-template <int CODE>
-MW4_DEV bool w4_gemv16(const uint8_t* codes, int rows, int r0, int grp0, int grp1, const uint4* bperm,
-                       const float* bsum, const float* tsum, const uint16_t* sc, const uint16_t* bi, int ngrp_row,
-                       float& acc0, float& acc1, uint64_t* box_bars, int gpb, volatile int* abort_flag,
-                       unsigned int* status) {
-    const int lane = threadIdx.x & 31, g = lane >> 2;
-    constexpr int kIn = 4;   // groups in flight: independent MMA chains
-    for (int grp = grp0; grp < grp1; grp += kIn) {
-        if (box_bars) {
-            for (int q = 0; q < kIn; ++q)
-                if (grp + q < grp1 && ((grp + q) % gpb) == 0 || (q == 0 && grp + q < grp1))
-                    if (!mbar_wait(&box_bars[(grp + q) / gpb], 0, abort_flag, status)) return false;
-        }
-        float d[kIn][4];
-#pragma unroll
-        for (int q = 0; q < kIn; ++q) {
-            d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
-            if (grp + q < grp1) group_mma<CODE>(codes, rows, r0, grp + q, bperm, d[q]);
-        }
-        // every lane of a row group holds the same column sums (B is the same for all n)
-#pragma unroll
-        for (int q = 0; q < kIn; ++q) {
-            const int gg = grp + q;
-            if (gg >= grp1) break;
-            const float bs = bsum[gg], xs = tsum[gg];
-            const float s0 = bf16_bits_to_float(sc[(r0 + g) * ngrp_row + gg]);
-            const float b0 = bf16_bits_to_float(bi[(r0 + g) * ngrp_row + gg]);
-            const float s1 = bf16_bits_to_float(sc[(r0 + g + 8) * ngrp_row + gg]);
-            const float b1 = bf16_bits_to_float(bi[(r0 + g + 8) * ngrp_row + gg]);
-            acc0 = fmaf(s0, d[q][0] - 1024.f * bs, fmaf(b0, xs, acc0));
-            acc1 = fmaf(s1, d[q][2] - 1024.f * bs, fmaf(b1, xs, acc1));
-        }
-    }
-    return true;
 }
 
 // The four B-operand words of 8 consecutive activation values v[0..7] (an
@@ -437,16 +346,14 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     float* usum = reinterpret_cast<float*>(sm + L.usum);
     float* wred = reinterpret_cast<float*>(sm + L.wred);
     uint32_t* hperm = reinterpret_cast<uint32_t*>(sm + L.hperm);   // after the gate/up GEMV
-    float* hsum = reinterpret_cast<float*>(sm + L.hsum);
     float* hpiece = reinterpret_cast<float*>(sm + L.hpiece);
-    float* hbs = reinterpret_cast<float*>(sm + L.hbs);
     float* dred = reinterpret_cast<float*>(sm + L.dred);
     uint8_t* misc = sm + L.misc;
     // TMA boxes of 128-byte code rows: 256 columns of 4-bit codes, 128 of one-byte codes.
     // Gate/up slices come in kGuParts parts of their box columns (one 3-D copy per
     // matrix and part, one barrier per part, so the GEMV starts on the first part),
     // each slot's down rows in one 3-D copy.
-    const int nbox_gu = H * kBits / 1024, nbox_dn = I * kBits / 1024;
+    const int nbox_gu = H * kBits / 1024;
     uint64_t* bar_gu = reinterpret_cast<uint64_t*>(misc);               // [kGuParts] parts of the gate/up slices
     uint64_t* bar_dn = bar_gu + kGuParts;                                // routed down rows
     uint64_t* bar_dsh = bar_dn + 1;                                      // shared expert's down rows
@@ -460,7 +367,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = blockIdx.x, slot = G / kPE, ei = G % kPE;
-    const int NG = NS * kPE, NR = k * kPE;        // all CTAs; routed CTAs (also the down CTAs)
+    const int NR = k * kPE;                       // routed CTAs (also the down CTAs)
     const bool shared_cta = (slot == k);
     const bool down_cta = G < NR;
     unsigned int* status = &a.ctrl->status;
@@ -763,9 +670,10 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     const bool gu_ok = __syncthreads_and(run ? mbar_wait(bar_sb, 0, abort_flag, status) : 0);
     if (gu_ok) {
         // 2*RG/16 row tiles (gate, then up), every warp on all of them for its own
-        // groups gg = warp, warp + kFWarps, ... (one in each half of the columns with
-        // 32 groups and 16 warps): each group's B fragments are loaded once for all
-        // the tiles, whose MMA chains are independent
+        // groups gg = warp, warp + kFWarps, ...: each group's B fragments are loaded
+        // once for all the tiles, whose MMA chains are independent (fewer groups per
+        // warp measured faster than spreading every part of the columns over all
+        // warps: the per-group work around the MMAs is paid once per group)
         const int ntile = 2 * (RG / 16), ngrp = H / 64;
         constexpr int kTC = 4;   // row tiles per pass
         for (int t0 = 0; t0 < ntile; t0 += kTC) {
@@ -777,15 +685,20 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
                 uint32_t bf[8];
                 load_bfrag<CODE>(reinterpret_cast<const uint4*>(xperm), gg, bf);
                 float d[kTC][4];
+                const uint8_t* tcodes[kTC];
+                int tr0[kTC], tgrp[kTC];
+                const uint4* tnob[kTC];
 #pragma unroll
-                for (int t = 0; t < kTC; ++t) {
+                for (int t = 0; t < kTC; ++t) {   // a tile past the end repeats the last one, unused
                     d[t][0] = d[t][1] = d[t][2] = d[t][3] = 0.f;
-                    const int tt = t0 + t;
-                    if (tt < ntile) {
-                        const bool up = tt >= ntile / 2;
-                        group_mma_b<CODE>(up ? ucodes : gcodes, RG, (up ? tt - ntile / 2 : tt) * 16, gg, bf, d[t]);
-                    }
+                    const int tt = min(t0 + t, ntile - 1);
+                    const bool up = tt >= ntile / 2;
+                    tcodes[t] = up ? ucodes : gcodes;
+                    tr0[t] = (up ? tt - ntile / 2 : tt) * 16;
+                    tgrp[t] = gg;
+                    tnob[t] = nullptr;
                 }
+                units_mma<CODE, kTC, true>(tcodes, RG, tr0, tgrp, tnob, bf, d);
                 const float bs = xbs[gg], xs = xsum[gg];
                 const int g = lane >> 2, ngr = H / 64;
 #pragma unroll
@@ -896,22 +809,14 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             else if (j < per && i < nw + ns2) hpiece[i - nw] = val_of(w[j]);
         }
     }
-    __syncthreads();
-    const bool h_ok = down_cta && gu_done && !*abort_flag;
-    // every slot's h carries the tag, so every CTA has read the call counter
-    if (h_ok && G == 0 && tid == 0) st_relaxed_u32(&a.ctrl->pad[kCtrlEpochWord], xtag);
-    if (h_ok) {   // per-64-value group sums of h: its four 16-value pieces in order
-        for (int gi = tid; gi < NS * (I / 64); gi += kFThreads) {
-            const float* pc = hpiece + 8 * gi;
-            hbs[gi] = ((pc[0] + pc[2]) + pc[4]) + pc[6];
-            hsum[gi] = ((pc[1] + pc[3]) + pc[5]) + pc[7];
-        }
-    }
     // ---------------------------------------------------------------- 5. down GEMV, weighted sum, output rows
     cp_async_wait<0>();   // this thread's pieces of the down scales and biases
-    const bool dn_ok = __syncthreads_and(h_ok ? (mbar_wait(bar_dn, 0, abort_flag, status) &&
-                                                 mbar_wait(bar_dsh, 0, abort_flag, status))
-                                              : 0);
+    const bool dn_ok = __syncthreads_and((down_cta && gu_done) ? (mbar_wait(bar_dn, 0, abort_flag, status) &&
+                                                                  mbar_wait(bar_dsh, 0, abort_flag, status))
+                                                               : 0) &&
+                       !*abort_flag;
+    // every slot's h carries the tag, so every CTA has read the call counter
+    if (dn_ok && G == 0 && tid == 0) st_relaxed_u32(&a.ctrl->pad[kCtrlEpochWord], xtag);
     if (dn_ok) {
         // units (slot, row tile, group), strided over the warps; each unit's 16 row
         // sums go to dred[unit][16]
@@ -921,23 +826,29 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             // branch-free: a unit past the end repeats the last one, its result unstored
             float d[kU][4];
             int uj[kU], ugg[kU], utl[kU];
+            const uint8_t* ucodes_q[kU];
+            const uint4* ub[kU];
+            const uint32_t nob[8] = {};
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
                 const int u = min(u0 + q * kFWarps, nunit - 1);
                 uj[q] = u / (ntl * ngrp);
-                utl[q] = (u / ngrp) % ntl;
+                utl[q] = (u / ngrp) % ntl * 16;
                 ugg[q] = u % ngrp;
                 d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
-                group_mma<CODE>(dcodes + (size_t)uj[q] * L.dslot, DR, utl[q] * 16, ugg[q],
-                                reinterpret_cast<const uint4*>(hperm) + (size_t)uj[q] * (I / 8), d[q]);
+                ucodes_q[q] = dcodes + (size_t)uj[q] * L.dslot;
+                ub[q] = reinterpret_cast<const uint4*>(hperm) + (size_t)uj[q] * (I / 8);
             }
+            units_mma<CODE, kU, false>(ucodes_q, DR, utl, ugg, ub, nob, d);
             const int g = lane >> 2;
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
-                const int j = uj[q], gg = ugg[q], r0 = utl[q] * 16 + g;
+                const int j = uj[q], gg = ugg[q], r0 = utl[q] + g;
                 const uint16_t* sc = dsb + (size_t)j * 2 * DR * ngrp;
                 const uint16_t* bi = sc + DR * ngrp;
-                const float bs = hbs[j * ngrp + gg], hs = hsum[j * ngrp + gg];
+                // per-64-value group sums of h: its four 16-value pieces in order
+                const float* pc = hpiece + 8 * (j * ngrp + gg);
+                const float bs = ((pc[0] + pc[2]) + pc[4]) + pc[6], hs = ((pc[1] + pc[3]) + pc[5]) + pc[7];
                 const float v0 = fmaf(bf16_bits_to_float(sc[r0 * ngrp + gg]), d[q][0] - 1024.f * bs,
                                       bf16_bits_to_float(bi[r0 * ngrp + gg]) * hs);
                 const float v1 = fmaf(bf16_bits_to_float(sc[(r0 + 8) * ngrp + gg]), d[q][2] - 1024.f * bs,
@@ -951,15 +862,19 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
         }
         __syncthreads();
         // out row r = sum over slots (in order) of the slot's weight times its row sum
-        // over the groups (in order)
+        // over the groups (in order): the row sums y[j][r] by one thread each, then
+        // the weighted sums
+        float* ysl = dred + nunit * 16;   // [NS][DR]
+        for (int i = tid; i < NS * DR; i += kFThreads) {
+            const int j = i / DR, r = i % DR, tl = r / 16, rr = r % 16;
+            float y = 0.f;
+            for (int gg = 0; gg < ngrp; ++gg) y += dred[((j * ntl + tl) * ngrp + gg) * 16 + rr];
+            ysl[i] = y;
+        }
+        __syncthreads();
         for (int r = tid; r < DR; r += kFThreads) {
-            const int tl = r / 16, rr = r % 16;
             float acc = 0.f;
-            for (int j = 0; j < NS; ++j) {
-                float y = 0.f;
-                for (int gg = 0; gg < ngrp; ++gg) y += dred[((j * ntl + tl) * ngrp + gg) * 16 + rr];
-                acc = fmaf(sel_w[j], y, acc);
-            }
+            for (int j = 0; j < NS; ++j) acc = fmaf(sel_w[j], ysl[j * DR + r], acc);
             a.out[gdrow_sh + r] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
         }
     }
@@ -1037,7 +952,7 @@ static FusedKernel fused_kernel_for(const moe_w4_layer& L) {
 }
 
 static bool shape_ok(const moe_w4_layer& L) {
-    const int bits = code_bits_of(L), k = L.top_k, NG = (k + 1) * kPE;
+    const int bits = code_bits_of(L), k = L.top_k;
     if (!fused_kernel_for(L)) return false;
     if (k < 1 || k + 1 > kMaxSlots) return false;
     if (L.H % 256 || L.I % 256 || L.H > 4096 || L.I > 2048) return false;   // slices of 16 rows; <= 16 row tiles

@@ -74,7 +74,7 @@ constexpr int kScanRegChunks = 32;   // chunk counts held in registers (T <= 32 
 __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nchunk, int32_t* __restrict__ chunk_base,
                                                     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                     int4* __restrict__ blkinfo, int4* __restrict__ unitinfo,
-                                                    int32_t* __restrict__ ntiles, int MI, int MH, int R) {
+                                                    int32_t* __restrict__ ntiles, int MI, int MH, int R, int BN) {
     extern __shared__ int sm[];
     int* cnt = sm;               // [E+1]
     int* off = sm + (E + 1);     // [E+1]
@@ -110,12 +110,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nch
         }
         cnt[e] = run;
         off[e] = run;
-        blk[e] = (run + kBN - 1) / kBN;
+        blk[e] = (run + BN - 1) / BN;
     }
     if (threadIdx.x == 0) {
         cnt[E] = T;                        // shared expert: every token, in order
         off[E] = T;
-        blk[E] = (T + kBN - 1) / kBN;
+        blk[E] = (T + BN - 1) / BN;
     }
     __syncthreads();
     block_exclusive_scan(off, E + 1, wt);      // off[e] = start of group e; off[E] = T*k
@@ -134,14 +134,14 @@ __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nch
     }
     if (threadIdx.x == 0) offsets[E] = off[E];
     if (blkinfo == nullptr) return;
-    // one record per 128-row block: the GEMMs read their tile's block in one load
+    // one record per block of BN rows (128 unless a tile override is set): the GEMMs read their tile's block in one load
     // (tile = block * M + weight-row block); the shared group (e = E) comes last
     for (int e = threadIdx.x; e <= E; e += blockDim.x) {
         const int b0 = blk[e], b1 = (e < E) ? blk[e + 1] : nblk;
         const int rows = (e < E) ? cnt[e] : T, p_first = (e < E) ? off[e] : T * k;
         for (int b = b0; b < b1; ++b) {
-            const int r0 = (b - b0) * kBN;
-            blkinfo[b] = make_int4(e, r0, min(kBN, rows - r0), p_first + r0);
+            const int r0 = (b - b0) * BN;
+            blkinfo[b] = make_int4(e, r0, min(BN, rows - r0), p_first + r0);
         }
     }
     // down units: runs of at most R consecutive row blocks of one group
@@ -225,8 +225,9 @@ cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cud
     chunk_count_kernel<<<nchunk, kChunk, E * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.status);
     trace_mark(st, 3);
     const size_t scan_sm = (4 * (E + 1) + 33) * sizeof(int);
+    const TileCfg tc = tile_cfg(L, T);
     scan_kernel<<<1, 1024, scan_sm, st>>>(T, E, k, nchunk, o.chunk_base, o.counts, o.offsets, o.blkinfo, o.unitinfo,
-                                          o.ntiles, L.I / kBM, L.H / kBM, down_blocks_per_unit(L.I));
+                                          o.ntiles, L.I / kBM, L.H / kBM, tc.du, tc.bn);
     trace_mark(st, 4);
     assign_kernel<<<nchunk, kChunk, (kAssignWarps * E + kChunk * k) * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.perm,
                                                                      o.inv);

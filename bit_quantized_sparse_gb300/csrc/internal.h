@@ -37,6 +37,18 @@ constexpr int kCtrlEpochWord = 61;
 constexpr int kCtrlInjectWord = 60;
 constexpr int kDownReuseMaxI = 512;
 inline int down_blocks_per_unit(int I) { return I <= kDownReuseMaxI ? kDownBlocksPerUnit : 1; }
+// Smallest token block the grouping may use (a tile override); sizes the block records.
+constexpr int kMinBN = 32;
+
+// Prefill tile choice: token rows per block (the GEMMs' N, at most kBN) and
+// row blocks per down unit.  The default is kBN, and down_blocks_per_unit(I)
+// once the routed rows average at least half a block per expert (T*k >= 64*E),
+// else 1 (measured on GB300 at H=2048, I=512, E=256, top-8: units of 4 blocks
+// 2% slower at T=512, 3-4% faster at T=2048 and 4096).  The environment
+// variable MOE_W4_FORCE_TILE ("bn=64,du=2", either key optional) or
+// moe_w4_set_tile_override replaces it, for ablations.
+struct TileCfg { int bn, du; };
+TileCfg tile_cfg(const moe_w4_layer& L, int T);
 
 struct Ctrl;   // workspace control header (common.cuh)
 
@@ -65,7 +77,7 @@ struct RouteOut {
     int32_t* perm; int32_t* inv;
     int32_t* chunk_base;
     float* logits;       // [kRouterSplit][T][E] partial router scores (tensor-core path), [T][E] otherwise
-    uint16_t* router_a;  // [Epad][3H] bf16 split router weights (tensor-core scores); NULL: CUDA cores
+    uint16_t* router_a;  // [Epad][3H] bf16 split router weights, written per call unless the layer has them
     uint16_t* x16;     // fp16 copy of x written by the top-k kernel (NULL: not needed)
     int4* blkinfo; int32_t* ntiles;   // per-block records [max blocks] and tile counts [2]; NULL: no tile maps
     int4* unitinfo;                   // down units [max blocks]: {first block, blocks, group, 0}
@@ -73,7 +85,14 @@ struct RouteOut {
 };
 cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* x, const RouteOut& o,
                                   cudaStream_t st);
+// Bytes of the split router weights ([Epad][3H] bf16) and their one-time preparation.
+size_t router_prep_bytes(const moe_w4_layer& L);
+cudaError_t launch_router_prep(const moe_w4_layer& L, uint16_t* dst, cudaStream_t st);
 cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cudaStream_t st);
+// The grouping step on the host (ablation.cu): synchronises the stream, copies
+// the top-k indices back, writes the same records as launch_grouping; sets
+// *bad_index (and writes nothing) if an index is out of range.
+cudaError_t host_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cudaStream_t st, bool* bad_index);
 
 // ---------------------------------------------------------------------------
 // decode (decode.cu)

@@ -10,68 +10,6 @@
 namespace mw4 {
 
 // ---------------------------------------------------------------------------
-// scores: 64 tokens x 64 experts per CTA, 32-deep K slices, 4x4 per thread
-// ---------------------------------------------------------------------------
-constexpr int kRT = 64, kRE = 64, kRK = 32;
-
-__global__ void __launch_bounds__(256) router_scores_kernel(const uint16_t* __restrict__ x,
-                                                            const float* __restrict__ Wr,
-                                                            const float* __restrict__ bias,
-                                                            float* __restrict__ logits, int T, int H, int E) {
-    __shared__ float xs[kRK][kRT + 4];
-    __shared__ __align__(16) float ws[kRK][kRE];
-    const int tid = threadIdx.x;
-    const int t0 = blockIdx.y * kRT, e0 = blockIdx.x * kRE;
-    const int ty = tid / 16, tx = tid % 16;
-    float acc[4][4] = {};
-    for (int h0 = 0; h0 < H; h0 += kRK) {
-        {   // x tile: 64 tokens x 32 columns of bf16, one 16-byte load per thread
-            const int t = tid / 4, c = (tid % 4) * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t0 + t < T) v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * H + h0 + c);
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                xs[c + 2 * i][t] = __uint_as_float(u[i] << 16);
-                xs[c + 2 * i + 1][t] = __uint_as_float(u[i] & 0xFFFF0000u);
-            }
-        }
-        {   // W tile: 32 rows x 64 experts fp32
-            const int r = tid / 8, c = (tid % 8) * 8;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = e0 + c + i;
-                ws[r][c + i] = (e < E) ? Wr[(size_t)(h0 + r) * E + e] : 0.f;
-            }
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < kRK; ++kk) {
-            float a[4], b[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
-            const float4 bv = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
-            b[0] = bv.x; b[1] = bv.y; b[2] = bv.z; b[3] = bv.w;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + ty * 4 + i;
-        if (t >= T) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + tx * 4 + j;
-            if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
 // scores on the tensor cores with fp32 accuracy
 // ---------------------------------------------------------------------------
 // W_r (fp32) is split exactly into three bf16 terms, w = hi + mid + lo (8 + 8 +
@@ -336,6 +274,17 @@ static cudaError_t topk_smem_attr() {
     return e;
 }
 
+size_t router_prep_bytes(const moe_w4_layer& L) {
+    const size_t Epad = (size_t)(L.E + kBM - 1) / kBM * kBM;
+    return Epad * 3 * (size_t)L.H * 2;
+}
+
+cudaError_t launch_router_prep(const moe_w4_layer& L, uint16_t* dst, cudaStream_t st) {
+    const int Epad = (L.E + kBM - 1) / kBM * kBM;
+    router_split_kernel<<<dim3(L.H / 32, Epad / 32), 256, 0, st>>>(L.router_w, L.H, L.E, Epad, dst);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* x, const RouteOut& o,
                                   cudaStream_t st) {
     const int Epad = (L.E + kBM - 1) / kBM * kBM;
@@ -343,10 +292,16 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
         const cudaError_t e = topk_smem_attr();
         if (e != cudaSuccess) return e;
     }
-    if (o.router_a) {   // tensor-core path
+    // the split router weights: prepared once per layer (moe_w4_prepare_router),
+    // else split into the workspace on every call
+    const uint16_t* ra = static_cast<const uint16_t*>(L.router_prep);
+    if (!ra) {
         router_split_kernel<<<dim3(L.H / 32, Epad / 32), 256, 0, st>>>(L.router_w, L.H, L.E, Epad, o.router_a);
+        ra = o.router_a;
+    }
+    {
         CUtensorMap mA, mX;
-        if (!bf16_map(&mA, o.router_a, Epad, 3 * (uint64_t)L.H, kBM) || !bf16_map(&mX, x, T, L.H, kRtBN))
+        if (!bf16_map(&mA, ra, Epad, 3 * (uint64_t)L.H, kBM) || !bf16_map(&mX, x, T, L.H, kRtBN))
             return cudaErrorInvalidValue;
         static size_t attr[64] = {};
         int dev = 0;
@@ -358,14 +313,12 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
             if (e != cudaSuccess) return e;
             attr[dev] = router_tc_smem();
         }
-        RouterTcArgs ra{L.router_bias, o.logits, T, L.H, L.E, o.status};
-        router_tc_kernel<<<dim3(Epad / kBM, (T + kRtBN - 1) / kRtBN, kRtSplit), 256, router_tc_smem(), st>>>(ra, mA, mX);
-    } else {
-        dim3 grid((L.E + kRE - 1) / kRE, (T + kRT - 1) / kRT);
-        router_scores_kernel<<<grid, 256, 0, st>>>(x, L.router_w, L.router_bias, o.logits, T, L.H, L.E);
+        RouterTcArgs ra_args{L.router_bias, o.logits, T, L.H, L.E, o.status};
+        router_tc_kernel<<<dim3(Epad / kBM, (T + kRtBN - 1) / kRtBN, kRtSplit), 256, router_tc_smem(), st>>>(ra_args, mA,
+                                                                                                           mX);
     }
     trace_mark(st, 1);
-    const int nsplit = o.router_a ? kRtSplit : 1;
+    const int nsplit = kRtSplit;
     const size_t sm = topk_smem(L.H, L.E);
     const dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
     const int nit = (L.H + 255) / 256;   // H <= 4096

@@ -40,6 +40,7 @@ MOE_W4_ERR_SCRATCH = -7
 # bits of the device status word (include/moe_w4.h)
 MOE_W4_CODES_UINT = 0
 MOE_W4_CODES_E4M3 = 1
+MOE_W4_ABLATE_HOST_ROUTING = 1   # include/moe_w4_ablation.h
 MOE_W4_STATUS_WAIT_TIMEOUT = 1
 MOE_W4_STATUS_BAD_INDEX = 2
 MOE_W4_STATUS_FP16_RANGE = 4
@@ -55,19 +56,23 @@ class MoeW4Layer(ctypes.Structure):
                 ("router_w", c_void_p), ("router_bias", c_void_p), ("shared_gate", c_void_p),
                 ("gate", MoeW4Mat), ("up", MoeW4Mat), ("down", MoeW4Mat),
                 ("sh_gate", MoeW4Mat), ("sh_up", MoeW4Mat), ("sh_down", MoeW4Mat), ("code_bits", c_int),
-                ("code_format", c_int)]
+                ("code_format", c_int), ("router_prep", c_void_p)]
 
 
 _P = ctypes.POINTER(MoeW4Layer)
 _SIGS = {
     "moe_w4_workspace_size": (c_size_t, [_P, c_int]),
+    "moe_w4_router_prep_bytes": (c_size_t, [_P]),
+    "moe_w4_prepare_router": (c_int, [_P, c_void_p, c_size_t, c_void_p]),
     "moe_w4_workspace_init": (c_int, [c_void_p, c_size_t, c_void_p]),
     "moe_w4_status_offset": (c_size_t, []),
     "moe_w4_route": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_w4_forward_decode": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_w4_forward_prefill": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "moe_w4_ablation_prefill": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_int, c_void_p]),
     "moe_w4_set_trace_events": (c_int, [c_void_p, c_int]),
+    "moe_w4_set_tile_override": (c_int, [c_int, c_int]),
     "moe_w4_last_traced_kernels": (c_int, []),
     "moe_w4_forward_decode_noalloc": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_w4_noalloc_status": (c_int, [c_void_p, c_void_p]),
@@ -81,12 +86,16 @@ for _name, (_res, _args) in _SIGS.items():
 EXPORTED = tuple(_SIGS)
 
 moe_w4_workspace_size = _lib.moe_w4_workspace_size
+moe_w4_router_prep_bytes = _lib.moe_w4_router_prep_bytes
+moe_w4_prepare_router = _lib.moe_w4_prepare_router
 moe_w4_workspace_init = _lib.moe_w4_workspace_init
 moe_w4_status_offset = _lib.moe_w4_status_offset
 moe_w4_route = _lib.moe_w4_route
 moe_w4_forward_decode = _lib.moe_w4_forward_decode
 moe_w4_forward_prefill = _lib.moe_w4_forward_prefill
+moe_w4_ablation_prefill = _lib.moe_w4_ablation_prefill
 moe_w4_set_trace_events = _lib.moe_w4_set_trace_events
+moe_w4_set_tile_override = _lib.moe_w4_set_tile_override
 moe_w4_last_traced_kernels = _lib.moe_w4_last_traced_kernels
 moe_w4_forward_decode_noalloc = _lib.moe_w4_forward_decode_noalloc
 moe_w4_noalloc_status = _lib.moe_w4_noalloc_status
@@ -132,7 +141,7 @@ class DeviceLayer:
     Build it from any object with the attributes of synthetic.W4Layer (numpy
     arrays: uint32 codes, uint16 bf16 bit patterns, float32 router)."""
 
-    def __init__(self, layer, device="cuda"):
+    def __init__(self, layer, device="cuda", prepare_router=True):
         torch = _torch()
         self.H, self.E, self.I, self.top_k = int(layer.H), int(layer.E), int(layer.I), int(layer.top_k)
         self.device = torch.device(device)
@@ -162,6 +171,15 @@ class DeviceLayer:
         self.c.shared_gate = _ptr(self.shared_gate)
         for n, (c, s, b) in self.mats.items():
             setattr(self.c, n, MoeW4Mat(c.data_ptr(), s.data_ptr(), b.data_ptr()))
+        # the router weights split once for the tensor-core routing (none for a
+        # layer the library rejects: its calls return the error instead)
+        self.router_prep = None
+        nprep = moe_w4_router_prep_bytes(ctypes.byref(self.c)) if prepare_router else 0
+        if nprep:
+            self.router_prep = torch.empty(nprep, dtype=torch.uint8, device=self.device)
+            _check(moe_w4_prepare_router(ctypes.byref(self.c), self.router_prep.data_ptr(), nprep, _stream()),
+                   "prepare_router")
+            self.c.router_prep = self.router_prep.data_ptr()
         self._ws = None
         self._ws_T = -1
 

@@ -101,6 +101,12 @@ typedef struct {
     int code_bits;             /* 4 (or 0) or 8; with 8 the codes arrays hold
                                   cols/4 words per row instead of cols/8          */
     int code_format;           /* MOE_W4_CODES_UINT (0) or MOE_W4_CODES_E4M3    */
+    const void* router_prep;   /* the router weights as moe_w4_prepare_router
+                                  writes them (moe_w4_router_prep_bytes bytes,
+                                  16-byte aligned), or NULL: the routing of
+                                  every call with T >= 2 then prepares them in
+                                  its workspace first.  Must be rewritten after
+                                  router_w changes.                            */
 } moe_w4_layer;
 
 enum {
@@ -120,6 +126,20 @@ enum {
     MOE_W4_ERR_SCRATCH     = -7  /* moe_w4_forward_decode_noalloc: the call
                                     needs more than the fixed scratch array    */
 };
+
+/* The router weights prepared once per layer for the tensor-core scores of
+ * the routing (prefill, and decode calls with T >= 2): W_r (fp32 [H][E]) split
+ * exactly into three bf16 terms per weight, hi + mid + lo, stored transposed,
+ * [ceil(E/128)*128][3H] bf16, rows past E zero.  The scores are unchanged by
+ * the preparation; it only saves the split on every call.
+ * moe_w4_router_prep_bytes: the size (0 if the layer is invalid).
+ * moe_w4_prepare_router: writes them to `dst` (device memory owned by the
+ * caller, dst_bytes >= that size, 16-byte aligned) on `stream`; reads only
+ * L->router_w, L->H and L->E.  Returns MOE_W4_ERR_INVALID / _ALIGN /
+ * _WORKSPACE (dst too small) or MOE_W4_ERR_LAUNCH.  Store dst in
+ * L->router_prep to use it. */
+size_t moe_w4_router_prep_bytes(const moe_w4_layer* L);
+int moe_w4_prepare_router(const moe_w4_layer* L, void* dst, size_t dst_bytes, cudaStream_t stream);
 
 /* Bytes of workspace needed for calls with up to T_max tokens (0 if the layer
  * is invalid).  The workspace holds routing intermediates, the grouped
@@ -249,6 +269,18 @@ int moe_w4_noalloc_status(unsigned int* status, cudaStream_t stream);
  * cudaEventRecordExternal, so they also fire inside a captured CUDA graph.
  * Pass NULL to stop tracing.  Process-wide setting, not thread-safe. */
 int moe_w4_set_trace_events(cudaEvent_t* events, int n_events);
+
+/* Prefill tile override, for ablations ("Optimizing on-device inference for
+ * Apple Silicon", section "Match tile size to expert load": the tile height is
+ * chosen per workload).  bn: token rows per block of the grouped GEMMs (the
+ * MMA's N), 32, 64 or 128 (the default); du: row blocks of one expert that a
+ * down-projection weight tile is dequantised once for, 1, 2 or 4 (by default 4
+ * where I <= 512 and T * top_k >= 64 * E, else 1; with I > 512 du > 1 is
+ * ignored).  0 restores a default.  The environment variable MOE_W4_FORCE_TILE ("bn=64,du=2", either
+ * key optional) is read once, at the first prefill call or at the first call
+ * of this function, which then replaces it.  Process-wide; takes effect for
+ * calls enqueued afterwards.  Returns MOE_W4_ERR_INVALID for other values. */
+int moe_w4_set_tile_override(int bn, int du);
 
 /* Failure-detection test hook (no production use).  on != 0: the next batch-1
  * decode calls on this workspace have one CTA skip publishing its router

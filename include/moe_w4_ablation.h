@@ -1,0 +1,41 @@
+/* Measurement-only entry point of libmoe_w4: the prefill with one step of the
+ * path replaced by the design the source pages measured against, so that the
+ * gain of the product's design can be re-measured on this GPU.  Not for
+ * production use.
+ *
+ * ("Optimizing on-device inference for Apple Silicon", section "Keep expert
+ * routing on the GPU": a routing step synchronised with the CPU between the
+ * router and the expert GEMMs, against the histogram, scan and scatter kept
+ * on the GPU.)
+ */
+#ifndef MOE_W4_ABLATION_H
+#define MOE_W4_ABLATION_H
+
+#include "moe_w4.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    /* The router and top-k run on the GPU as usual; the stream is then
+     * synchronised, the top-k indices copied to the host, the expert
+     * histogram, scan, positions and block records computed there and copied
+     * back before the grouped GEMMs are enqueued.  Same output as
+     * moe_w4_forward_prefill (the records are identical).  The call blocks the
+     * host until the routing is done and cannot be captured in a CUDA graph. */
+    MOE_W4_ABLATE_HOST_ROUTING = 1
+};
+
+/* moe_w4_forward_prefill with the variant `mode` (MOE_W4_ABLATE_*); same
+ * arguments, layouts and ownership.  Returns MOE_W4_ERR_INVALID for an unknown
+ * mode, MOE_W4_ERR_DEVICE if a top-k index was out of range (nothing written
+ * to `out`), the other codes as moe_w4_forward_prefill. */
+int moe_w4_ablation_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out,
+                            void* workspace, size_t ws_bytes, int mode, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_W4_ABLATION_H */

@@ -8,7 +8,7 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "moe_w4.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("moe_w4.h", "moe_w4_ablation.h")]
 
 
 @pytest.fixture(scope="module")
@@ -21,15 +21,18 @@ def mw():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_w4_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(moe_w4_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("moe_w4_route", "moe_w4_forward_decode", "moe_w4_forward_prefill", "moe_w4_workspace_size",
-              "moe_w4_strerror"):
+              "moe_w4_strerror", "moe_w4_prepare_router", "moe_w4_router_prep_bytes", "moe_w4_set_tile_override",
+              "moe_w4_ablation_prefill"):
         assert n in names
 
 
@@ -111,3 +114,36 @@ def test_bad_arguments_rejected(mw):
 def test_strerror(mw):
     for code in (0, -1, -2, -3, -4, -5, -6, 42):
         assert isinstance(mw.moe_w4_strerror(code), str) and mw.moe_w4_strerror(code)
+
+
+def test_router_prep_host_checks(mw):
+    """The prepared router weights: size, and the host-side refusals (no device work)."""
+    L = _layer(mw)
+    n = mw.moe_w4_router_prep_bytes(ctypes.byref(L))
+    assert n == 256 * 3 * 2048 * 2            # [ceil(E/128)*128][3H] bf16
+    L2 = _layer(mw, E=200)
+    assert mw.moe_w4_router_prep_bytes(ctypes.byref(L2)) == 256 * 3 * 2048 * 2
+    assert mw.moe_w4_router_prep_bytes(None) == 0
+    dst = 1 << 20
+    assert mw.moe_w4_prepare_router(ctypes.byref(L), dst, n - 16, None) == mw.MOE_W4_ERR_WORKSPACE
+    assert mw.moe_w4_prepare_router(ctypes.byref(L), dst + 8, n, None) == mw.MOE_W4_ERR_ALIGN
+    assert mw.moe_w4_prepare_router(ctypes.byref(L), None, n, None) == mw.MOE_W4_ERR_INVALID
+    L.router_prep = dst + 4                   # a misaligned prepared copy is refused by every call
+    ws = 1 << 12
+    assert mw.moe_w4_forward_prefill(ctypes.byref(L), 4, ws, ws, ws, 1 << 40, None) == mw.MOE_W4_ERR_ALIGN
+
+
+def test_tile_override_values(mw):
+    for bn, du in [(32, 1), (64, 2), (128, 4), (0, 0)]:
+        assert mw.moe_w4_set_tile_override(bn, du) == mw.MOE_W4_OK
+    for bn, du in [(16, 0), (96, 0), (256, 0), (0, 3), (0, 8), (-1, 0)]:
+        assert mw.moe_w4_set_tile_override(bn, du) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_set_tile_override(0, 0) == mw.MOE_W4_OK
+
+
+def test_ablation_mode_checked(mw):
+    L = _layer(mw)
+    ws = 1 << 12
+    assert mw.moe_w4_ablation_prefill(ctypes.byref(L), 4, ws, ws, ws, 1 << 40, 7, None) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_ablation_prefill(ctypes.byref(L), 0, ws, ws, ws, 1 << 40, mw.MOE_W4_ABLATE_HOST_ROUTING,
+                                      None) == mw.MOE_W4_OK

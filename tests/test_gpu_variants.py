@@ -1,0 +1,99 @@
+"""GPU: the prefill's optional variants give the product path's results.
+
+- the router weights prepared once per layer (moe_w4_prepare_router) against
+  the split made in the workspace on every call: the same scores, so the
+  same bits out;
+- tile overrides (moe_w4_set_tile_override: token rows per block, row blocks
+  per down unit): every choice against the oracle, and against the default
+  tiles bit for bit (a tile changes which rows share an MMA, not the
+  arithmetic of any output element);
+- the measurement-only host-synchronised grouping (moe_w4_ablation_prefill):
+  identical records, so identical bits out.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle as O
+from bit_quantized_sparse_gb300 import synthetic as S
+from tests import tolerance as TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_quantized_sparse_gb300 import _build
+    _build.build()
+    from bit_quantized_sparse_gb300 import moe_w4 as mw
+    return torch, mw
+
+
+def _bits(torch, t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.fixture(scope="module")
+def case(env):
+    torch, mw = env
+    L, x = S.draw_config("prefill_T512")
+    return L, x, mw.DeviceLayer(L), O.moe_layer(L, x)["out"]
+
+
+def test_router_prep_same_bits(env, case):
+    torch, mw = env
+    L, x, dl, ref = case
+    assert dl.c.router_prep                      # prepared at construction
+    plain = mw.DeviceLayer(L, prepare_router=False)
+    assert not plain.c.router_prep
+    xd = mw.tokens_to_device(x)
+    a = _bits(torch, mw.forward_prefill(dl, xd))
+    b = _bits(torch, mw.forward_prefill(plain, xd))
+    torch.cuda.synchronize()
+    assert np.array_equal(a, b)
+    assert TOL.within(TOL.metrics(O.bf16_to_f64(a), ref))
+    ra, rb = mw.route(dl, xd), mw.route(plain, xd)
+    torch.cuda.synchronize()
+    for k in ra:
+        assert torch.equal(ra[k], rb[k]), k
+    assert dl.status() == 0 and plain.status() == 0
+
+
+@pytest.mark.parametrize("bn,du", [(32, 1), (64, 1), (64, 2), (64, 4), (128, 1), (128, 2)])
+def test_tile_override(env, case, bn, du):
+    torch, mw = env
+    L, x, dl, ref = case
+    xd = mw.tokens_to_device(x)
+    base = _bits(torch, mw.forward_prefill(dl, xd))
+    try:
+        assert mw.moe_w4_set_tile_override(bn, du) == mw.MOE_W4_OK
+        got = _bits(torch, mw.forward_prefill(dl, xd))
+        torch.cuda.synchronize()
+    finally:
+        mw.moe_w4_set_tile_override(0, 0)
+    assert TOL.within(TOL.metrics(O.bf16_to_f64(got), ref))
+    assert np.array_equal(got, base)
+    assert dl.status() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny_T4", "prefill_T512"])
+def test_host_routing_ablation_same_bits(env, name):
+    torch, mw = env
+    L, x = S.draw_config(name)
+    dl = mw.DeviceLayer(L)
+    xd = mw.tokens_to_device(x)
+    T = x.shape[0]
+    ref_bits = _bits(torch, mw.forward_prefill(dl, xd))
+    ws = dl.workspace(T)
+    out = torch.full((T, L.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    r = mw.moe_w4_ablation_prefill(ctypes.byref(dl.c), T, xd.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                   mw.MOE_W4_ABLATE_HOST_ROUTING, st)
+    assert r == mw.MOE_W4_OK
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(torch, out), ref_bits)
+    assert dl.status() == 0
