@@ -453,8 +453,13 @@ def run_ablations(torch, mw, c, dl, x, out, ws, stream, timed, capture, args):
     - routing: ms per call, eager calls, with the GPU-resident grouping and with
       the host-synchronised one (moe_w4_ablation_prefill);
     - router_prep: ms per call (graph replays) with the router weights prepared
-      once and split on every call."""
-    res = {"tiles_ms": {}, "routing_ms": {}, "router_prep_ms": {}}
+      once and split on every call;
+    - dequant: ms per call (graph replays) with the weights rebuilt in the
+      GEMMs' tiles (the product) and with a separate pass that writes every
+      weight in fp16 before the GEMMs read them back."""
+    res = {"tiles_ms": {}, "routing_ms": {}, "router_prep_ms": {}, "dequant_ms": {}}
+    nscr = mw.moe_w4_ablation_scratch_bytes(ctypes.byref(dl.c), mw.MOE_W4_ABLATE_SEPARATE_DEQUANT)
+    scratch = torch.empty(nscr, dtype=torch.uint8, device=x.device)   # every weight in fp16 (1.6 GB)
     st = lambda: torch.cuda.current_stream().cuda_stream
 
     def graph_ms(fn):
@@ -489,7 +494,14 @@ def run_ablations(torch, mw, c, dl, x, out, ws, stream, timed, capture, args):
 
         def host_routed():
             mw._check(mw.moe_w4_ablation_prefill(ctypes.byref(dl.c), Tm, xs.data_ptr(), os_.data_ptr(), ws.data_ptr(),
-                                                 ws.numel(), mw.MOE_W4_ABLATE_HOST_ROUTING, st()), "ablation")
+                                                 ws.numel(), mw.MOE_W4_ABLATE_HOST_ROUTING, None, 0, st()), "ablation")
+
+        def separate_dequant():
+            mw._check(mw.moe_w4_ablation_prefill(ctypes.byref(dl.c), Tm, xs.data_ptr(), os_.data_ptr(), ws.data_ptr(),
+                                                 ws.numel(), mw.MOE_W4_ABLATE_SEPARATE_DEQUANT, scratch.data_ptr(),
+                                                 scratch.numel(), st()), "ablation")
+        res["dequant_ms"][f"T{Tm}"] = {"fused_in_gemm": row[f"bn{TILE_CHOICES[0][0]}_du{TILE_CHOICES[0][1]}"],
+                                      "separate_fp16_pass": graph_ms(separate_dequant)}
         n = max(args.steps, 5)
         res["routing_ms"][f"T{Tm}"] = {
             "gpu_resident_eager": eager_ms(lambda: mw.forward_prefill(dl, xs, out=os_, ws=ws), n),

@@ -62,3 +62,80 @@ cudaError_t host_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cudaS
 }
 
 }  // namespace mw4
+
+namespace mw4 {
+
+// ---------------------------------------------------------------------------
+// Separate dequantisation pass: the layer's weights rebuilt in fp16 in memory,
+// for the grouped GEMMs to read back.  ("Optimizing on-device inference for
+// Apple Silicon", section "Dequantise weights during matrix multiplication":
+// expanding the 4-bit weights to a 16-bit array that the matmul then reads is
+// what the fused dequantisation replaces.)  Each weight is the value the fused
+// dequantisers put in tensor memory (same fp16 roundings), at the same K
+// position (chunk order), so the variant's output equals the product's.
+// ---------------------------------------------------------------------------
+template <int BITS, bool E4M3>
+__global__ void __launch_bounds__(256) f16_weights_kernel(const uint32_t* __restrict__ codes,
+                                                          const uint16_t* __restrict__ sc,
+                                                          const uint16_t* __restrict__ bi, size_t rows, int cols,
+                                                          uint16_t* __restrict__ out, unsigned int* status) {
+    constexpr int kPerWord = 32 / BITS;   // columns per code word
+    const int wpr = cols / kPerWord, G = cols / kGroup;
+    const size_t n = rows * (size_t)wpr;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / wpr;
+        const int col0 = (int)(i % wpr) * kPerWord, g = col0 / kGroup;
+        const float sf = bf16_bits_to_float(sc[r * G + g]), bf = bf16_bits_to_float(bi[r * G + g]);
+        constexpr float kQmax = BITS == 4 ? 15.f : (E4M3 ? 448.f : 255.f);
+        if (!(fmaf(fabsf(sf), kQmax, fabsf(bf)) <= 65504.f)) raise_status(status, MOE_W4_STATUS_FP16_RANGE);
+        const __half s_h = __float2half_rn(sf), s_h16 = __float2half_rn(sf * 0.0625f), b_h = __float2half_rn(bf);
+        const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16), b2 = __halves2half2(b_h, b_h);
+        const uint32_t w = codes[i];
+        uint16_t* dst = out + r * cols + col0;
+        if (BITS == 4) {
+            uint32_t o[4];
+            dequant8_f16(w, s2, s2_16, b2, o);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            uint32_t o[2];
+            if (E4M3)
+                dequant_e4m3x4_f16(w, s2, b2, o);
+            else
+                dequant4x8_f16(w, s2, b2, o);
+            *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
+        }
+    }
+}
+
+size_t f16_weights_bytes(const moe_w4_layer& L) {
+    return 3 * ((size_t)L.E + 1) * (size_t)L.I * (size_t)L.H * 2;
+}
+
+cudaError_t launch_f16_weights(const moe_w4_layer& L, uint16_t* w16, const uint16_t* w16_ptrs[6], unsigned int* status,
+                               cudaStream_t st) {
+    const size_t E = L.E, H = L.H, I = L.I;
+    const moe_w4_mat* ms[6] = {&L.gate, &L.up, &L.down, &L.sh_gate, &L.sh_up, &L.sh_down};
+    const size_t rows[6] = {E * I, E * I, E * H, I, I, H};
+    const int cols[6] = {(int)H, (int)H, (int)I, (int)H, (int)H, (int)I};
+    const int bits = code_bits_of(L);
+    const bool e4m3 = codes_e4m3(L);
+    uint16_t* o = w16;
+    for (int m = 0; m < 6; ++m) {
+        w16_ptrs[m] = o;
+        const size_t words = rows[m] * (size_t)cols[m] * bits / 32;
+        const unsigned grid = (unsigned)std::min<size_t>((words + 255) / 256, 152 * 8);
+        if (bits == 4)
+            f16_weights_kernel<4, false><<<grid, 256, 0, st>>>(ms[m]->codes, ms[m]->scales, ms[m]->biases, rows[m],
+                                                               cols[m], o, status);
+        else if (e4m3)
+            f16_weights_kernel<8, true><<<grid, 256, 0, st>>>(ms[m]->codes, ms[m]->scales, ms[m]->biases, rows[m],
+                                                              cols[m], o, status);
+        else
+            f16_weights_kernel<8, false><<<grid, 256, 0, st>>>(ms[m]->codes, ms[m]->scales, ms[m]->biases, rows[m],
+                                                               cols[m], o, status);
+        o += rows[m] * (size_t)cols[m];
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mw4

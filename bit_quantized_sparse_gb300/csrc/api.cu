@@ -258,7 +258,7 @@ int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x, int32_t* to
 }
 
 static int run_grouped(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out, void* workspace,
-                       const WsLayout& w, cudaStream_t stream, bool host_routing = false);
+                       const WsLayout& w, cudaStream_t stream, int ablate = 0, void* scratch = nullptr);
 
 int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out, void* workspace,
                           size_t ws_bytes, cudaStream_t stream) {
@@ -302,12 +302,20 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, mo
 // Routing, grouping and the grouped tensor-core GEMMs over T rows (the
 // workspace checks already done).
 static int run_grouped(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out, void* workspace,
-                       const WsLayout& w, cudaStream_t stream, bool host_routing) {
+                       const WsLayout& w, cudaStream_t stream, int ablate, void* scratch) {
     RouteOut o = route_ws(workspace, w);
     trace_mark(stream, 0);
-    cudaError_t e = launch_router_prefill(*L, T, x, o, stream);
+    // measurement-only variants (moe_w4_ablation_prefill): the weights rebuilt in
+    // fp16 by a separate pass first, read by the GEMMs with one-block down units
+    const uint16_t* w16[6] = {};
+    const TileCfg one_block{tile_cfg(*L, T).bn, 1};
+    const bool sep = ablate == MOE_W4_ABLATE_SEPARATE_DEQUANT;
+    cudaError_t e = sep ? launch_f16_weights(*L, static_cast<uint16_t*>(scratch), w16, o.status, stream) : cudaSuccess;
+    if (e == cudaSuccess) e = launch_router_prefill(*L, T, x, o, stream);
     bool bad = false;
-    if (e == cudaSuccess) e = host_routing ? host_grouping(*L, T, o, stream, &bad) : launch_grouping(*L, T, o, stream);
+    if (e == cudaSuccess)
+        e = ablate == MOE_W4_ABLATE_HOST_ROUTING ? host_grouping(*L, T, o, stream, &bad)
+                                                  : launch_grouping(*L, T, o, stream, sep ? &one_block : nullptr);
     if (e != cudaSuccess) return MOE_W4_ERR_LAUNCH;
     if (bad) return MOE_W4_ERR_DEVICE;
     PrefillWs p{};
@@ -321,7 +329,7 @@ static int run_grouped(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w
     p.max_tiles_dn = w.max_tiles_dn;
     p.status = o.status;
     trace_kernels(9);
-    return launch_status(launch_grouped_ffn(*L, T, x, out, p, stream));
+    return launch_status(launch_grouped_ffn(*L, T, x, out, p, stream, sep ? w16 : nullptr));
 }
 
 
@@ -338,18 +346,28 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, m
     return run_grouped(L, T, x, out, workspace, w, stream);
 }
 
+size_t moe_w4_ablation_scratch_bytes(const moe_w4_layer* L, int mode) {
+    if (check_layer(L) != MOE_W4_OK) return 0;
+    return mode == MOE_W4_ABLATE_SEPARATE_DEQUANT ? f16_weights_bytes(*L) : 0;
+}
+
 int moe_w4_ablation_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w4_bf16* out, void* workspace,
-                            size_t ws_bytes, int mode, cudaStream_t stream) {
+                            size_t ws_bytes, int mode, void* scratch, size_t scratch_bytes, cudaStream_t stream) {
     int r = check_layer(L);
     if (r) return r;
-    if (mode != MOE_W4_ABLATE_HOST_ROUTING) return MOE_W4_ERR_INVALID;
+    if (mode != MOE_W4_ABLATE_HOST_ROUTING && mode != MOE_W4_ABLATE_SEPARATE_DEQUANT) return MOE_W4_ERR_INVALID;
+    if (mode == MOE_W4_ABLATE_SEPARATE_DEQUANT) {
+        if (!scratch) return MOE_W4_ERR_INVALID;
+        if (!aligned16(scratch)) return MOE_W4_ERR_ALIGN;
+        if (scratch_bytes < f16_weights_bytes(*L)) return MOE_W4_ERR_WORKSPACE;
+    }
     if (T < 0) return MOE_W4_ERR_INVALID;
     if (T == 0) return MOE_W4_OK;
     if (!x || !out) return MOE_W4_ERR_INVALID;
     if (!aligned16(x) || !aligned16(out)) return MOE_W4_ERR_ALIGN;
     WsLayout w;
     if ((r = check_ws(*L, T, workspace, ws_bytes, &w))) return r;
-    return run_grouped(L, T, x, out, workspace, w, stream, true);
+    return run_grouped(L, T, x, out, workspace, w, stream, mode, scratch);
 }
 
 const char* moe_w4_strerror(int status) {

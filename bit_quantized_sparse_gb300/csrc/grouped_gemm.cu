@@ -62,6 +62,7 @@ struct GemmArgs {
     int K;                     // reduction length (H or I)
     int rows_e;                // weight rows per expert (I or H)
     int out_cols;              // I or H
+    int k_order8;              // K order of the one-byte codes (fp16 weights from a separate pass only)
     unsigned int* status;
 };
 
@@ -95,8 +96,11 @@ struct Geo {
     // have read a step, and the B rows, freed when the step's MMAs complete.
     // The codes thus run several steps ahead of the dequantisers, whatever the
     // MMAs' lag.
-    static constexpr int SC = DUAL ? (BITS == 8 ? 3 : 4) : (BITS == 8 ? 6 : 8);
-    static constexpr int SB = 4;
+    // BITS = 16: weights already rebuilt in fp16 by a separate pass (a
+    // measurement-only variant): the "codes" ring holds fp16 A tiles that the
+    // MMAs read from shared memory, and no dequantiser runs
+    static constexpr int SC = BITS == 16 ? (DUAL ? 2 : 3) : DUAL ? (BITS == 8 ? 3 : 4) : (BITS == 8 ? 6 : 8);
+    static constexpr int SB = BITS == 16 ? (DUAL ? 2 : 3) : 4;
     static constexpr uint32_t C_STAGE = NMAT * kCodesBytes;
     static constexpr uint32_t ACC_COLS = NMAT * 128;      // TMEM columns per accumulator buffer
     static constexpr int ACC_BUFS = DUAL ? 1 : 2;
@@ -111,6 +115,7 @@ struct Geo {
 static_assert(Geo<true, 4>::SA == 2 && Geo<false, 4>::SA == 4, "TMEM map");
 static_assert(Geo<true, 4>::bytes() <= 232448 && Geo<false, 4>::bytes() <= 232448, "shared memory per CTA");
 static_assert(Geo<true, 8>::bytes() <= 232448 && Geo<false, 8>::bytes() <= 232448, "shared memory per CTA");
+static_assert(Geo<true, 16>::bytes() <= 232448 && Geo<false, 16>::bytes() <= 232448, "shared memory per CTA");
 static_assert(kDownReuseMaxI / kGK <= Geo<false, 4>::SA, "a reused down weight tile holds its whole K in the A ring");
 static_assert(Geo<true, 4>::SA <= Geo<true, 4>::SB, "gate/up A slots are freed by the B-ring barriers");
 
@@ -170,6 +175,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                        const __grid_constant__ CUtensorMap map1s, const __grid_constant__ CUtensorMap mapb,
                        const __grid_constant__ CUtensorMap mapbs) {
     static_assert(!E4M3 || BITS == 8, "E4M3 codes are one byte each");
+    constexpr bool PRE = BITS == 16;   // fp16 weights from a separate pass: A from shared memory
     using GG = Geo<DUAL, BITS>;
     constexpr uint32_t kCodesBytes = GG::kCodesBytes;
     constexpr int kCodeWords = kGK * BITS / 32;   // code words per row per step
@@ -202,7 +208,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     if (tid == 0) {
         for (int s = 0; s < SC; ++s) {
             mbar_init(&c_full[s], 1);
-            mbar_init(&c_empty[s], 32 * GG::kDeqWarps);
+            mbar_init(&c_empty[s], PRE ? 1 : 32 * GG::kDeqWarps);   // PRE: freed by the MMAs' commit
         }
         for (int s = 0; s < SB; ++s) {
             mbar_init(&b_full[s], 1);
@@ -246,8 +252,16 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 if (!mbar_wait_warp(&c_empty[s], ((gk / SC) & 1) ^ 1, abort_flag, a.status)) { ok = false; break; }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&c_full[s], NMAT * kCodesBytes);
-                    tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * kCodeWords, ti.arow, &c_full[s]);
-                    if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * kCodeWords, ti.arow, &c_full[s]);
+                    if (PRE) {   // two 64-column fp16 sub-tiles per matrix
+                        for (int mat = 0; mat < NMAT; ++mat) {
+                            uint8_t* dst = const_cast<uint8_t*>(C_of(s, mat));
+                            tma_load_2d(dst, mat ? m1 : m0, ks * kGK, ti.arow, &c_full[s]);
+                            tma_load_2d(dst + kSubBytes, mat ? m1 : m0, ks * kGK + 64, ti.arow, &c_full[s]);
+                        }
+                    } else {
+                        tma_load_2d(const_cast<uint8_t*>(C_of(s, 0)), m0, ks * kCodeWords, ti.arow, &c_full[s]);
+                        if (DUAL) tma_load_2d(const_cast<uint8_t*>(C_of(s, 1)), m1, ks * kCodeWords, ti.arow, &c_full[s]);
+                    }
                 }
             }
         }
@@ -310,10 +324,12 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 tc_fence_after();
                 const uint32_t dacc = taddr + b * GG::ACC_COLS;
                 for (int ks = 0; ks < nK; ++ks, ++gb) {
-                    const int sb = gb % SB, ka = ga + ks, sa = ka % SA;
+                    const int sb = gb % SB, ka = ga + ks, sa = ka % SA, sc = gb % SC;
                     // A from the dequantisers (a_full, waited on by the unit's first row
-                    // block), B from the TMA (b_full)
-                    ok = (r > 0 || mbar_wait_warp(&a_full[sa], (ka / SA) & 1, abort_flag, a.status)) &&
+                    // block), or PRE from the TMA into the codes ring (c_full; one row block
+                    // per unit, so A steps are B steps); B from the TMA (b_full)
+                    ok = (PRE ? mbar_wait_warp(&c_full[sc], (gb / SC) & 1, abort_flag, a.status)
+                              : (r > 0 || mbar_wait_warp(&a_full[sa], (ka / SA) & 1, abort_flag, a.status))) &&
                          mbar_wait_warp(&b_full[sb], (gb / SB) & 1, abort_flag, a.status);
                     if (!ok) break;
                     tc_fence_after();
@@ -325,12 +341,20 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         // K=16 slice kk: sub-tile kk/4, +32 bytes per slice within it (+2 in the address field)
                         const uint64_t bd = (kk < 4 ? bdesc0 : bdesc1) + 2 * (kk & 3);
 #pragma unroll
-                        for (int mat = 0; mat < NMAT; ++mat)
-                            umma_f16_ts_elect(dacc + mat * 128, atm + mat * (kGK / 2) + kk * 8, bd, idesc,
-                                              (ks | kk) != 0);
+                        for (int mat = 0; mat < NMAT; ++mat) {
+                            if (PRE) {
+                                const uint8_t* at = C_of(sc, mat) + (kk < 4 ? 0 : kSubBytes);
+                                umma_f16_elect(dacc + mat * 128, umma_desc_sw128(smem_u32(at)) + 2 * (kk & 3), bd,
+                                               idesc, (ks | kk) != 0);
+                            } else {
+                                umma_f16_ts_elect(dacc + mat * 128, atm + mat * (kGK / 2) + kk * 8, bd, idesc,
+                                                  (ks | kk) != 0);
+                            }
+                        }
                     }
                     umma_commit_elect(&b_empty[sb]);   // gate/up: also frees A slot sa (see the dequantiser)
-                    if (!DUAL && r == unb - 1) umma_commit_elect(&a_empty[sa]);   // the unit's last use of A slot sa
+                    if (PRE) umma_commit_elect(&c_empty[sc]);
+                    else if (!DUAL && r == unb - 1) umma_commit_elect(&a_empty[sa]);   // the unit's last use of A slot sa
                 }
                 if (ok) umma_commit_elect(&acc_full[b]);
             }
@@ -341,113 +365,115 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
         }
     } else if (warp < GG::kEpiWarp0) {
         // ------------------------------------------------------------ dequantisation: one weight row per thread
-        const int td = tid - 32 * GG::kDeqWarp0, row = td % 128;
-        const int mat = DUAL ? td / 128 : 0, hsel = DUAL ? -1 : td / 128;   // down: which group of the step
-        // swizzle phase of this row's 16-byte code chunks (64-byte rows for 4-bit
-        // codes, 128-byte rows for 8-bit)
-        const int sw = BITS == 8 ? (row & 7) : ((row >> 1) & 3);
-        const bool chunked = (G % 8) == 0;
-        int gk = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-            const UnitInfo u = unit_info(a, t);
-            const TileInfo ti = block_info(a, u.b0, u.m);   // the unit's group and weight rows
-            const uint16_t* sp = (mat == 0 ? (ti.sh ? a.s0s : a.s0r) : (ti.sh ? a.s1s : a.s1r)) + (size_t)(ti.arow + row) * G;
-            const uint16_t* bp = (mat == 0 ? (ti.sh ? a.b0s : a.b0r) : (ti.sh ? a.b1s : a.b1r)) + (size_t)(ti.arow + row) * G;
-            uint4 sq = make_uint4(0, 0, 0, 0), bq = sq, sqn = sq, bqn = sq;
-            if (chunked) {
-                sq = __ldg(reinterpret_cast<const uint4*>(sp));
-                bq = __ldg(reinterpret_cast<const uint4*>(bp));
-            }
-            for (int k4 = 0; k4 < nK; k4 += 4) {   // four steps = eight groups per scale/bias load
-                if (chunked && k4 + 4 < nK) {
-                    sqn = __ldg(reinterpret_cast<const uint4*>(sp + 2 * (k4 + 4)));
-                    bqn = __ldg(reinterpret_cast<const uint4*>(bp + 2 * (k4 + 4)));
+        if constexpr (!PRE) {   // PRE: the weights are fp16 already
+            const int td = tid - 32 * GG::kDeqWarp0, row = td % 128;
+            const int mat = DUAL ? td / 128 : 0, hsel = DUAL ? -1 : td / 128;   // down: which group of the step
+            // swizzle phase of this row's 16-byte code chunks (64-byte rows for 4-bit
+            // codes, 128-byte rows for 8-bit)
+            const int sw = BITS == 8 ? (row & 7) : ((row >> 1) & 3);
+            const bool chunked = (G % 8) == 0;
+            int gk = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const UnitInfo u = unit_info(a, t);
+                const TileInfo ti = block_info(a, u.b0, u.m);   // the unit's group and weight rows
+                const uint16_t* sp = (mat == 0 ? (ti.sh ? a.s0s : a.s0r) : (ti.sh ? a.s1s : a.s1r)) + (size_t)(ti.arow + row) * G;
+                const uint16_t* bp = (mat == 0 ? (ti.sh ? a.b0s : a.b0r) : (ti.sh ? a.b1s : a.b1r)) + (size_t)(ti.arow + row) * G;
+                uint4 sq = make_uint4(0, 0, 0, 0), bq = sq, sqn = sq, bqn = sq;
+                if (chunked) {
+                    sq = __ldg(reinterpret_cast<const uint4*>(sp));
+                    bq = __ldg(reinterpret_cast<const uint4*>(bp));
                 }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int ks = k4 + j;
-                    if (ks >= nK) break;
-                    uint32_t s2w, b2w;   // the step's two groups, bf16 pairs (low half first)
-                    if (chunked) {
-                        s2w = (j == 0 ? sq.x : j == 1 ? sq.y : j == 2 ? sq.z : sq.w);
-                        b2w = (j == 0 ? bq.x : j == 1 ? bq.y : j == 2 ? bq.z : bq.w);
-                    } else {
-                        s2w = (uint32_t)sp[2 * ks] | ((uint32_t)sp[2 * ks + 1] << 16);
-                        b2w = (uint32_t)bp[2 * ks] | ((uint32_t)bp[2 * ks + 1] << 16);
+                for (int k4 = 0; k4 < nK; k4 += 4) {   // four steps = eight groups per scale/bias load
+                    if (chunked && k4 + 4 < nK) {
+                        sqn = __ldg(reinterpret_cast<const uint4*>(sp + 2 * (k4 + 4)));
+                        bqn = __ldg(reinterpret_cast<const uint4*>(bp + 2 * (k4 + 4)));
                     }
-                    const int sc = gk % SC, sa = gk % SA;
-                    // A slot sa last served A step gk - SA.  Down: a_empty fires once the
-                    // MMAs of every row block of that step's unit are done.  Gate/up (one row
-                    // block per unit, A step = B step): the commit on b_empty of that step
-                    // does (SA <= SB, so that barrier cannot have moved on by a further
-                    // phase meanwhile), and no separate commit is spent.
-                    ok = mbar_wait(&c_full[sc], (gk / SC) & 1, abort_flag, a.status) &&
-                         (DUAL ? (gk < SA || mbar_wait(&b_empty[(gk - SA) % SB], ((gk - SA) / SB) & 1, abort_flag,
-                                                       a.status))
-                               : mbar_wait(&a_empty[sa], ((gk / SA) & 1) ^ 1, abort_flag, a.status));
-                    if (!ok) break;
-                    const uint8_t* cr = C_of(sc, mat) + row * GG::kCodesRowBytes;
-                    tc_fence_after();   // the MMAs that read this A slot have completed
-                    // this thread's weight row -> its TMEM lane, 64 columns of fp16 pairs, in quads of 16
-                    const uint32_t tdst =
-                        taddr + ((uint32_t)(row & ~31) << 16) + GG::A_TMEM0 + sa * GG::A_COLS + mat * (kGK / 2);
-#pragma unroll
-                    for (int grp = 0; grp < 2; ++grp) {
-                        if (!DUAL && grp != hsel) continue;
-                        const float sf = bf16_bits_to_float((uint16_t)(grp ? (s2w >> 16) : (s2w & 0xFFFFu)));
-                        const float bf = bf16_bits_to_float((uint16_t)(grp ? (b2w >> 16) : (b2w & 0xFFFFu)));
-                        // the group's rebuilt weights |s q + b| must stay within fp16 (q <= the
-                        // largest code magnitude: 15, 255, or 448 for E4M3)
-                        constexpr float kQmax = BITS == 4 ? 15.f : (E4M3 ? 448.f : 255.f);
-                        if (!(fmaf(fabsf(sf), kQmax, fabsf(bf)) <= 65504.f)) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
-                        const __half s_h = __float2half_rn(sf), s_h16 = __float2half_rn(sf * 0.0625f);
-                        const __half b_h = __float2half_rn(bf);
-                        const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16);
-                        const __half2 b2 = __halves2half2(b_h, b_h);
-#pragma unroll
-                        for (int qq = 0; qq < 2; ++qq) {   // 32 columns of the group -> 16 TMEM columns
-                            const int q = 2 * grp + qq;
-                            uint32_t o[16];
-                            if (BITS == 8) {   // two 16-byte chunks of four words
-#pragma unroll
-                                for (int hh2 = 0; hh2 < 2; ++hh2) {
-                                    const int c = 2 * q + hh2;
-                                    const uint4 w = *reinterpret_cast<const uint4*>(cr + ((c ^ sw) << 4));
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int ks = k4 + j;
+                        if (ks >= nK) break;
+                        uint32_t s2w, b2w;   // the step's two groups, bf16 pairs (low half first)
+                        if (chunked) {
+                            s2w = (j == 0 ? sq.x : j == 1 ? sq.y : j == 2 ? sq.z : sq.w);
+                            b2w = (j == 0 ? bq.x : j == 1 ? bq.y : j == 2 ? bq.z : bq.w);
+                        } else {
+                            s2w = (uint32_t)sp[2 * ks] | ((uint32_t)sp[2 * ks + 1] << 16);
+                            b2w = (uint32_t)bp[2 * ks] | ((uint32_t)bp[2 * ks + 1] << 16);
+                        }
+                        const int sc = gk % SC, sa = gk % SA;
+                        // A slot sa last served A step gk - SA.  Down: a_empty fires once the
+                        // MMAs of every row block of that step's unit are done.  Gate/up (one row
+                        // block per unit, A step = B step): the commit on b_empty of that step
+                        // does (SA <= SB, so that barrier cannot have moved on by a further
+                        // phase meanwhile), and no separate commit is spent.
+                        ok = mbar_wait(&c_full[sc], (gk / SC) & 1, abort_flag, a.status) &&
+                             (DUAL ? (gk < SA || mbar_wait(&b_empty[(gk - SA) % SB], ((gk - SA) / SB) & 1, abort_flag,
+                                                           a.status))
+                                   : mbar_wait(&a_empty[sa], ((gk / SA) & 1) ^ 1, abort_flag, a.status));
+                        if (!ok) break;
+                        const uint8_t* cr = C_of(sc, mat) + row * GG::kCodesRowBytes;
+                        tc_fence_after();   // the MMAs that read this A slot have completed
+                        // this thread's weight row -> its TMEM lane, 64 columns of fp16 pairs, in quads of 16
+                        const uint32_t tdst =
+                            taddr + ((uint32_t)(row & ~31) << 16) + GG::A_TMEM0 + sa * GG::A_COLS + mat * (kGK / 2);
+    #pragma unroll
+                        for (int grp = 0; grp < 2; ++grp) {
+                            if (!DUAL && grp != hsel) continue;
+                            const float sf = bf16_bits_to_float((uint16_t)(grp ? (s2w >> 16) : (s2w & 0xFFFFu)));
+                            const float bf = bf16_bits_to_float((uint16_t)(grp ? (b2w >> 16) : (b2w & 0xFFFFu)));
+                            // the group's rebuilt weights |s q + b| must stay within fp16 (q <= the
+                            // largest code magnitude: 15, 255, or 448 for E4M3)
+                            constexpr float kQmax = BITS == 4 ? 15.f : (E4M3 ? 448.f : 255.f);
+                            if (!(fmaf(fabsf(sf), kQmax, fabsf(bf)) <= 65504.f)) raise_status(a.status, MOE_W4_STATUS_FP16_RANGE);
+                            const __half s_h = __float2half_rn(sf), s_h16 = __float2half_rn(sf * 0.0625f);
+                            const __half b_h = __float2half_rn(bf);
+                            const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16);
+                            const __half2 b2 = __halves2half2(b_h, b_h);
+    #pragma unroll
+                            for (int qq = 0; qq < 2; ++qq) {   // 32 columns of the group -> 16 TMEM columns
+                                const int q = 2 * grp + qq;
+                                uint32_t o[16];
+                                if (BITS == 8) {   // two 16-byte chunks of four words
+    #pragma unroll
+                                    for (int hh2 = 0; hh2 < 2; ++hh2) {
+                                        const int c = 2 * q + hh2;
+                                        const uint4 w = *reinterpret_cast<const uint4*>(cr + ((c ^ sw) << 4));
+                                        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+    #pragma unroll
+                                        for (int wi = 0; wi < 4; ++wi) {
+                                            uint32_t q2[2];
+                                            if (E4M3)
+                                                dequant_e4m3x4_f16(words[wi], s2, b2, q2);
+                                            else
+                                                dequant4x8_f16(words[wi], s2, b2, q2);
+                                            o[8 * hh2 + 2 * wi] = q2[0];
+                                            o[8 * hh2 + 2 * wi + 1] = q2[1];
+                                        }
+                                    }
+                                } else {           // one 16-byte chunk of four words
+                                    const uint4 w = *reinterpret_cast<const uint4*>(cr + ((q ^ sw) << 4));
                                     const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
+    #pragma unroll
                                     for (int wi = 0; wi < 4; ++wi) {
-                                        uint32_t q2[2];
-                                        if (E4M3)
-                                            dequant_e4m3x4_f16(words[wi], s2, b2, q2);
-                                        else
-                                            dequant4x8_f16(words[wi], s2, b2, q2);
-                                        o[8 * hh2 + 2 * wi] = q2[0];
-                                        o[8 * hh2 + 2 * wi + 1] = q2[1];
+                                        uint32_t q4[4];
+                                        dequant8_f16(words[wi], s2, s2_16, b2, q4);
+                                        o[4 * wi] = q4[0]; o[4 * wi + 1] = q4[1]; o[4 * wi + 2] = q4[2]; o[4 * wi + 3] = q4[3];
                                     }
                                 }
-                            } else {           // one 16-byte chunk of four words
-                                const uint4 w = *reinterpret_cast<const uint4*>(cr + ((q ^ sw) << 4));
-                                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                                for (int wi = 0; wi < 4; ++wi) {
-                                    uint32_t q4[4];
-                                    dequant8_f16(words[wi], s2, s2_16, b2, q4);
-                                    o[4 * wi] = q4[0]; o[4 * wi + 1] = q4[1]; o[4 * wi + 2] = q4[2]; o[4 * wi + 3] = q4[3];
-                                }
+                                tmem_st16(tdst + 16 * q, o);
                             }
-                            tmem_st16(tdst + 16 * q, o);
                         }
+                        tmem_wait_st();
+                        mbar_arrive(&c_empty[sc]);   // this thread's codes of the step are read
+                        tc_fence_before();
+                        mbar_arrive(&a_full[sa]);
+                        ++gk;
                     }
-                    tmem_wait_st();
-                    mbar_arrive(&c_empty[sc]);   // this thread's codes of the step are read
-                    tc_fence_before();
-                    mbar_arrive(&a_full[sa]);
-                    ++gk;
+                    if (!ok) break;
+                    sq = sqn;
+                    bq = bqn;
                 }
-                if (!ok) break;
-                sq = sqn;
-                bq = bqn;
             }
         }
     } else {
@@ -476,8 +502,8 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 const uint32_t lane_addr = taddr + b * GG::ACC_COLS + ((uint32_t)(q * 32) << 16);
                 // h is the K operand of the down projection: store it in chunk order
                 const int orow = ti.m * kBM + q * 32 + lane;
-                const int ocol = DUAL ? ((orow & ~7) | (BITS == 8 ? chunk8_pos_of_col(orow & 7)
-                                                                  : chunk_pos_of_col(orow & 7)))
+                const bool ko8 = PRE ? a.k_order8 != 0 : BITS == 8;   // the layer's codes, not the fp16 copy
+                const int ocol = DUAL ? ((orow & ~7) | (ko8 ? chunk8_pos_of_col(orow & 7) : chunk_pos_of_col(orow & 7)))
                                       : orow;
                 for (int c0 = half * 16; c0 < ti.nrows; c0 += 32) {
                     uint32_t g[16], u[16];
@@ -630,7 +656,7 @@ static cudaError_t launch_gemm(const GemmArgs& g, int grid, const CUtensorMap& m
 }
 
 cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const PrefillWs& p,
-                               cudaStream_t st) {
+                               cudaStream_t st, const uint16_t* const* w16) {
     const int bits = code_bits_of(L);
     const bool e4m3 = codes_e4m3(L);   // validated: only with 8-bit codes
     const int H = L.H, I = L.I, E = L.E, k = L.top_k;
@@ -654,6 +680,15 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
                        CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x16, (uint64_t)T, H, kBN, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B);
+    if (w16) {   // fp16 weights from the separate pass: 64-column boxes, as the B tiles
+        const auto F16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+        ok = ok && make_map(&mg, F16, 2, w16[0], (uint64_t)E * I, H, kBM, 64, SW) &&
+             make_map(&mu, F16, 2, w16[1], (uint64_t)E * I, H, kBM, 64, SW) &&
+             make_map(&md, F16, 2, w16[2], (uint64_t)E * H, I, kBM, 64, SW) &&
+             make_map(&msg, F16, 2, w16[3], I, H, kBM, 64, SW) && make_map(&msu, F16, 2, w16[4], I, H, kBM, 64, SW) &&
+             make_map(&msd, F16, 2, w16[5], H, I, kBM, 64, SW);
+    }
     if (!ok) return cudaErrorInvalidValue;
 
     int nsm = 0;
@@ -667,7 +702,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     GemmArgs a{};
     a.ntiles = p.ntiles; a.offsets = p.offsets; a.perm = p.perm;
     a.topk_w = p.topk_w; a.gamma = p.gamma;
-    a.E = E; a.k = k; a.T = T; a.H = H; a.status = p.status;
+    a.E = E; a.k = k; a.T = T; a.H = H; a.status = p.status; a.k_order8 = bits == 8;
 
     // gate/up: A = Wg, Wu rows (I per expert), K = H, out = hh [.][I]
     a.blkinfo = p.blkinfo; a.unitinfo = nullptr; a.M = I / kBM;
@@ -679,7 +714,8 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     const int nrg = T * k;
     gather_rows_kernel<<<(unsigned)((nrg + 7) / 8), 256, 0, st>>>(p.x16, p.perm, p.xg, nrg, H, k);
     trace_mark(st, 6);
-    cudaError_t e = e4m3  ? launch_gemm<true, 8, true>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
+    cudaError_t e = w16   ? launch_gemm<true, 16, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
+                  : e4m3  ? launch_gemm<true, 8, true>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
                   : bits == 8 ? launch_gemm<true, 8, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
                               : launch_gemm<true, 4, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st);
     if (e != cudaSuccess) return e;
@@ -687,12 +723,13 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
 
     // down: A = Wd rows (H per expert), K = I, B = hh rows, out = ys [.][H]
     GemmArgs b = a;
-    b.M = H / kBM; b.ntiles = p.ntiles + 1; b.unitinfo = p.unitinfo;
+    b.M = H / kBM; b.ntiles = p.ntiles + 1; b.unitinfo = p.unitinfo;   // fp16 weights: one-block units (du = 1)
     b.s0r = L.down.scales; b.b0r = L.down.biases; b.s1r = nullptr; b.b1r = nullptr;
     b.s0s = L.sh_down.scales; b.b0s = L.sh_down.biases; b.s1s = nullptr; b.b1s = nullptr;
     b.out = p.ys; b.K = I; b.rows_e = H; b.out_cols = H;
     const int grid_dn = p.max_tiles_dn < nsm ? p.max_tiles_dn : nsm;
-    e = e4m3  ? launch_gemm<false, 8, true>(b, grid_dn, md, md, msd, msd, mh, mh, st)
+    e = w16   ? launch_gemm<false, 16, false>(b, grid_dn, md, md, msd, msd, mh, mh, st)
+      : e4m3  ? launch_gemm<false, 8, true>(b, grid_dn, md, md, msd, msd, mh, mh, st)
       : bits == 8 ? launch_gemm<false, 8, false>(b, grid_dn, md, md, msd, msd, mh, mh, st)
                   : launch_gemm<false, 4, false>(b, grid_dn, md, md, msd, msd, mh, mh, st);
     if (e != cudaSuccess) return e;

@@ -219,13 +219,13 @@ __global__ void __launch_bounds__(kChunk) assign_kernel(const int32_t* __restric
     }
 }
 
-cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cudaStream_t st) {
+cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cudaStream_t st, const TileCfg* force) {
     const int E = L.E, k = L.top_k;
     const int nchunk = (T + kChunk - 1) / kChunk;
     chunk_count_kernel<<<nchunk, kChunk, E * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.status);
     trace_mark(st, 3);
     const size_t scan_sm = (4 * (E + 1) + 33) * sizeof(int);
-    const TileCfg tc = tile_cfg(L, T);
+    const TileCfg tc = force ? *force : tile_cfg(L, T);
     scan_kernel<<<1, 1024, scan_sm, st>>>(T, E, k, nchunk, o.chunk_base, o.counts, o.offsets, o.blkinfo, o.unitinfo,
                                           o.ntiles, L.I / kBM, L.H / kBM, tc.du, tc.bn);
     trace_mark(st, 4);

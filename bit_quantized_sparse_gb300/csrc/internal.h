@@ -88,7 +88,9 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
 // Bytes of the split router weights ([Epad][3H] bf16) and their one-time preparation.
 size_t router_prep_bytes(const moe_w4_layer& L);
 cudaError_t launch_router_prep(const moe_w4_layer& L, uint16_t* dst, cudaStream_t st);
-cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cudaStream_t st);
+// `force` (optional) replaces the tile choice (an ablation needs one-block down units).
+cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cudaStream_t st,
+                            const TileCfg* force = nullptr);
 // The grouping step on the host (ablation.cu): synchronises the stream, copies
 // the top-k indices back, writes the same records as launch_grouping; sets
 // *bad_index (and writes nothing) if an index is out of range.
@@ -141,6 +143,14 @@ struct PrefillWs {
     unsigned int* status;
 };
 cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out,
-                               const PrefillWs& p, cudaStream_t st);
+                               const PrefillWs& p, cudaStream_t st,
+                               const uint16_t* const* w16 = nullptr);
+// The measurement-only separate dequantisation pass (ablation.cu): every weight
+// of the layer's six matrices rebuilt in fp16, in the K order of the fused
+// dequantisers, into w16 (moe_w4_ablation_scratch_bytes); w16_ptrs receives the
+// six matrices' starts (gate, up, down, shared gate, shared up, shared down).
+size_t f16_weights_bytes(const moe_w4_layer& L);
+cudaError_t launch_f16_weights(const moe_w4_layer& L, uint16_t* w16, const uint16_t* w16_ptrs[6], unsigned int* status,
+                               cudaStream_t st);
 
 }  // namespace mw4

@@ -37,10 +37,11 @@ MOE_W4_ERR_LAUNCH = -4
 MOE_W4_ERR_DEVICE = -5
 MOE_W4_ERR_ALIGN = -6
 MOE_W4_ERR_SCRATCH = -7
-# bits of the device status word (include/moe_w4.h)
 MOE_W4_CODES_UINT = 0
 MOE_W4_CODES_E4M3 = 1
-MOE_W4_ABLATE_HOST_ROUTING = 1   # include/moe_w4_ablation.h
+MOE_W4_ABLATE_HOST_ROUTING = 1       # include/moe_w4_ablation.h
+MOE_W4_ABLATE_SEPARATE_DEQUANT = 2
+# bits of the device status word (include/moe_w4.h)
 MOE_W4_STATUS_WAIT_TIMEOUT = 1
 MOE_W4_STATUS_BAD_INDEX = 2
 MOE_W4_STATUS_FP16_RANGE = 4
@@ -70,7 +71,9 @@ _SIGS = {
                              c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_w4_forward_decode": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "moe_w4_forward_prefill": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
-    "moe_w4_ablation_prefill": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_int, c_void_p]),
+    "moe_w4_ablation_prefill": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_int, c_void_p,
+                                        c_size_t, c_void_p]),
+    "moe_w4_ablation_scratch_bytes": (c_size_t, [_P, c_int]),
     "moe_w4_set_trace_events": (c_int, [c_void_p, c_int]),
     "moe_w4_set_tile_override": (c_int, [c_int, c_int]),
     "moe_w4_last_traced_kernels": (c_int, []),
@@ -94,6 +97,7 @@ moe_w4_route = _lib.moe_w4_route
 moe_w4_forward_decode = _lib.moe_w4_forward_decode
 moe_w4_forward_prefill = _lib.moe_w4_forward_prefill
 moe_w4_ablation_prefill = _lib.moe_w4_ablation_prefill
+moe_w4_ablation_scratch_bytes = _lib.moe_w4_ablation_scratch_bytes
 moe_w4_set_trace_events = _lib.moe_w4_set_trace_events
 moe_w4_set_tile_override = _lib.moe_w4_set_tile_override
 moe_w4_last_traced_kernels = _lib.moe_w4_last_traced_kernels

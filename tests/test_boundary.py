@@ -144,6 +144,14 @@ def test_tile_override_values(mw):
 def test_ablation_mode_checked(mw):
     L = _layer(mw)
     ws = 1 << 12
-    assert mw.moe_w4_ablation_prefill(ctypes.byref(L), 4, ws, ws, ws, 1 << 40, 7, None) == mw.MOE_W4_ERR_INVALID
-    assert mw.moe_w4_ablation_prefill(ctypes.byref(L), 0, ws, ws, ws, 1 << 40, mw.MOE_W4_ABLATE_HOST_ROUTING,
-                                      None) == mw.MOE_W4_OK
+    f = mw.moe_w4_ablation_prefill
+    assert f(ctypes.byref(L), 4, ws, ws, ws, 1 << 40, 7, None, 0, None) == mw.MOE_W4_ERR_INVALID
+    assert f(ctypes.byref(L), 0, ws, ws, ws, 1 << 40, mw.MOE_W4_ABLATE_HOST_ROUTING, None, 0, None) == mw.MOE_W4_OK
+    # the separate dequantisation pass needs a scratch for every weight in fp16
+    n = mw.moe_w4_ablation_scratch_bytes(ctypes.byref(L), mw.MOE_W4_ABLATE_SEPARATE_DEQUANT)
+    assert n == 3 * 257 * 512 * 2048 * 2
+    assert mw.moe_w4_ablation_scratch_bytes(ctypes.byref(L), mw.MOE_W4_ABLATE_HOST_ROUTING) == 0
+    sep = mw.MOE_W4_ABLATE_SEPARATE_DEQUANT
+    assert f(ctypes.byref(L), 4, ws, ws, ws, 1 << 40, sep, None, n, None) == mw.MOE_W4_ERR_INVALID
+    assert f(ctypes.byref(L), 4, ws, ws, ws, 1 << 40, sep, ws + 8, n, None) == mw.MOE_W4_ERR_ALIGN
+    assert f(ctypes.byref(L), 4, ws, ws, ws, 1 << 40, sep, ws, n - 16, None) == mw.MOE_W4_ERR_WORKSPACE

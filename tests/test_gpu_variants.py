@@ -7,8 +7,10 @@
   per down unit): every choice against the oracle, and against the default
   tiles bit for bit (a tile changes which rows share an MMA, not the
   arithmetic of any output element);
-- the measurement-only host-synchronised grouping (moe_w4_ablation_prefill):
-  identical records, so identical bits out.
+- the measurement-only variants of moe_w4_ablation_prefill: the
+  host-synchronised grouping (identical records) and the separate fp16
+  dequantisation pass (identical fp16 weights in the same K order): identical
+  bits out.
 """
 import ctypes
 
@@ -92,7 +94,36 @@ def test_host_routing_ablation_same_bits(env, name):
     out = torch.full((T, L.H), float("nan"), dtype=torch.bfloat16, device="cuda")
     st = torch.cuda.current_stream().cuda_stream
     r = mw.moe_w4_ablation_prefill(ctypes.byref(dl.c), T, xd.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(),
-                                   mw.MOE_W4_ABLATE_HOST_ROUTING, st)
+                                   mw.MOE_W4_ABLATE_HOST_ROUTING, None, 0, st)
+    assert r == mw.MOE_W4_OK
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(torch, out), ref_bits)
+    assert dl.status() == 0
+
+
+@pytest.mark.parametrize("name,bits,fmt", [("tiny_T4", 4, 0), ("prefill_T512", 4, 0), ("w8", 8, 0), ("w8", 8, 1)])
+def test_separate_dequant_ablation_same_bits(env, name, bits, fmt):
+    """Weights rebuilt in fp16 by a separate pass and read back by the GEMMs
+    from shared memory: the same fp16 weights in the same K order as the fused
+    dequantisers put in tensor memory, so the same bits out."""
+    torch, mw = env
+    if name == "w8":   # one-byte codes: a smaller layer (several tiles, ragged expert blocks)
+        L = S.draw_layer(512, 64, 256, 4, 1.0, seed=31, bits=bits, fmt=fmt)
+        x = S.draw_tokens(L, 200, 31)
+    else:
+        L, x = S.draw_config(name)
+    dl = mw.DeviceLayer(L)
+    xd = mw.tokens_to_device(x)
+    T = x.shape[0]
+    ref_bits = _bits(torch, mw.forward_prefill(dl, xd))
+    ws = dl.workspace(T)
+    mode = mw.MOE_W4_ABLATE_SEPARATE_DEQUANT
+    n = mw.moe_w4_ablation_scratch_bytes(ctypes.byref(dl.c), mode)
+    scratch = torch.empty(n, dtype=torch.uint8, device="cuda")
+    out = torch.full((T, L.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    r = mw.moe_w4_ablation_prefill(ctypes.byref(dl.c), T, xd.data_ptr(), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                                   mode, scratch.data_ptr(), n, st)
     assert r == mw.MOE_W4_OK
     torch.cuda.synchronize()
     assert np.array_equal(_bits(torch, out), ref_bits)
