@@ -220,6 +220,26 @@ int moe_w4_test_skip_publish(void* workspace, size_t ws_bytes, int on, cudaStrea
 
 int moe_w4_last_traced_kernels(void) { return g_traced_kernels; }
 
+int moe_w4_test_block_records(const moe_w4_layer* L, int T, const void* workspace, size_t ws_bytes, int32_t* dst,
+                              size_t dst_bytes, cudaStream_t stream) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (T < 1 || !dst) return MOE_W4_ERR_INVALID;
+    WsLayout w;
+    if ((r = check_ws(*L, T, const_cast<void*>(workspace), ws_bytes, &w))) return r;
+    const size_t rec = (size_t)w.max_blocks * sizeof(int4);
+    if (dst_bytes < 2 * sizeof(int32_t) + rec) return MOE_W4_ERR_WORKSPACE;
+    const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+    cudaError_t e = cudaMemcpyAsync(dst, ws + w.ntiles, 2 * sizeof(int32_t), cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst + 2, ws + w.blkinfo, rec, cudaMemcpyDeviceToDevice, stream);
+    return launch_status(e);
+}
+
+size_t moe_w4_test_block_records_bytes(const moe_w4_layer* L, int T) {
+    if (check_layer(L) != MOE_W4_OK || T < 1) return 0;
+    return 2 * sizeof(int32_t) + (size_t)ws_layout(*L, T).max_blocks * sizeof(int4);
+}
+
 int moe_w4_set_tile_override(int bn, int du) {
     std::call_once(g_tile_env_once, read_tile_env);   // the environment first, so that this call wins
     return set_tile(bn, du);

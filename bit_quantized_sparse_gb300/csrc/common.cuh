@@ -59,6 +59,23 @@ MW4_DEV void raise_status(unsigned int* status, unsigned int bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Debug builds (MW4_DEBUG_CHECKS, libmoe_w4_debug.so): an index read from the
+// routing records (a position, a block or unit record) is checked against its
+// range before use; out of range raises MOE_W4_STATUS_BAD_INDEX and the index
+// is clamped into range, so the access stays inside its buffer.  In the
+// product build the checks compile away.
+MW4_DEV int checked_index(int v, int lo, int hi_excl, unsigned int* status) {
+#ifdef MW4_DEBUG_CHECKS
+    if (v < lo || v >= hi_excl) {
+        raise_status(status, MOE_W4_STATUS_BAD_INDEX);
+        return v < lo ? lo : hi_excl - 1;
+    }
+#else
+    (void)lo; (void)hi_excl; (void)status;
+#endif
+    return v;
+}
+
 // ---------------------------------------------------------------------------
 // shared-memory addresses
 // ---------------------------------------------------------------------------

@@ -63,6 +63,7 @@ struct GemmArgs {
     int rows_e;                // weight rows per expert (I or H)
     int out_cols;              // I or H
     int k_order8;              // K order of the one-byte codes (fp16 weights from a separate pass only)
+    int max_blocks;            // capacity of the block (and unit) records (debug-build bounds)
     unsigned int* status;
 };
 
@@ -129,13 +130,22 @@ struct UnitInfo { int b0, nb, m; };
 // Work item t = (unit t / M, weight-row block t % M).  A unit is a run of row
 // blocks of one group (a single block unless unitinfo is given): its weight
 // tile is dequantised once and multiplied with each of its row blocks.
+// A unit record {first row block, row blocks} (checked in debug builds: at
+// most kDownBlocksPerUnit blocks, inside the block records).
+MW4_DEV int2 checked_unit(const GemmArgs& a, int b0, int nb) {
+    nb = checked_index(nb, 1, kDownBlocksPerUnit + 1, a.status);
+    b0 = checked_index(b0, 0, a.max_blocks - nb + 1, a.status);
+    return make_int2(b0, nb);
+}
+
 MW4_DEV UnitInfo unit_info(const GemmArgs& a, int t) {
     UnitInfo u;
     u.m = t % a.M;
     if (a.unitinfo) {
         const int4 r = __ldg(a.unitinfo + t / a.M);
-        u.b0 = r.x;
-        u.nb = r.y;
+        const int2 c = checked_unit(a, r.x, r.y);
+        u.b0 = c.x;
+        u.nb = c.y;
     } else {
         u.b0 = t / a.M;
         u.nb = 1;
@@ -149,18 +159,21 @@ MW4_DEV int2 unit_rec(const GemmArgs& a, int t, int ntiles) {
     if (t >= ntiles) return make_int2(0, 0);
     if (!a.unitinfo) return make_int2(t / a.M, 1);
     const int4 r = __ldg(a.unitinfo + t / a.M);
-    return make_int2(r.x, r.y);
+    return checked_unit(a, r.x, r.y);
 }
 
 // Tile (row block with record bi, weight-row block m); the record (group,
 // first row, rows, first grouped position) was written by the scan.
 MW4_DEV TileInfo tile_from(const GemmArgs& a, int4 bi, int m) {
     TileInfo ti;
-    ti.e = bi.x;
+    ti.e = checked_index(bi.x, 0, a.E + 1, a.status);
     ti.m = m;
-    ti.r0 = bi.y;
-    ti.nrows = bi.z;
-    ti.p0 = bi.w;
+    // the rows it names lie inside the group's grouped positions: routed [0, T*k),
+    // shared [T*k, T*k + T)
+    const int lo = ti.e == a.E ? a.T * a.k : 0, hi = ti.e == a.E ? a.T * a.k + a.T : a.T * a.k;
+    ti.nrows = checked_index(bi.z, 1, min(kBN, hi - lo) + 1, a.status);
+    ti.r0 = checked_index(bi.y, 0, hi - lo - ti.nrows + 1, a.status);
+    ti.p0 = checked_index(bi.w, lo, hi - ti.nrows + 1, a.status);
     ti.sh = (ti.e == a.E);
     ti.arow = (ti.sh ? 0 : ti.e * a.rows_e) + ti.m * kBM;
     return ti;
@@ -180,7 +193,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     constexpr uint32_t kCodesBytes = GG::kCodesBytes;
     constexpr int kCodeWords = kGK * BITS / 32;   // code words per row per step
     constexpr int NMAT = GG::NMAT, SC = GG::SC, SB = GG::SB, SA = GG::SA;
-    const int ntiles = a.ntiles[0];
+    const int ntiles = checked_index(a.ntiles[0], 0, a.max_blocks * a.M + 1, a.status);
     const int G = a.K / kGroup, nK = a.K / kGK;
 
     extern __shared__ uint8_t smem_raw[];
@@ -493,7 +506,9 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                 // only after every thread has passed the previous tile's barrier)
                 if (DUAL) {
                     if (et < ti.nrows)
-                        col_scale[cb * kBN + et] = ti.sh ? a.gamma[ti.r0 + et] : a.topk_w[a.perm[ti.p0 + et]];
+                        col_scale[cb * kBN + et] =
+                            ti.sh ? a.gamma[ti.r0 + et]
+                                  : a.topk_w[checked_index(a.perm[ti.p0 + et], 0, a.T * a.k, a.status)];
                     asm volatile("bar.sync 2, 256;" ::: "memory");
                 }
                 ok = mbar_wait(&acc_full[b], use & 1, abort_flag, a.status);
@@ -555,10 +570,11 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
 // row, 16-byte loads and stores, eight in flight per lane.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x16,
                                                           const int32_t* __restrict__ perm,
-                                                          uint16_t* __restrict__ xg, int nrows, int H, int k) {
+                                                          uint16_t* __restrict__ xg, int nrows, int H, int k,
+                                                          unsigned int* status) {
     const int p = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
     if (p >= nrows) return;
-    const int t = __ldg(perm + p) / k;
+    const int t = checked_index(__ldg(perm + p), 0, nrows, status) / k;
     const uint4* src = reinterpret_cast<const uint4*>(x16 + (size_t)t * H);
     uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)p * H);
     const int n = H / 8;
@@ -577,14 +593,14 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 // the sum in fp32, slots in order then the shared row; 8 columns per thread.
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ ys,
                                                       const int32_t* __restrict__ inv, uint16_t* __restrict__ out,
-                                                      int T, int H, int k) {
+                                                      int T, int H, int k, unsigned int* status) {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int per_row = H / 8;
     if (i >= (size_t)T * per_row) return;
     const int t = (int)(i / per_row), c = (int)(i % per_row) * 8;
     float acc[8] = {};
     for (int j = 0; j <= k; ++j) {
-        const size_t p = (j < k) ? (size_t)inv[(size_t)t * k + j] : (size_t)T * k + t;
+        const size_t p = (j < k) ? (size_t)checked_index(inv[(size_t)t * k + j], 0, T * k, status) : (size_t)T * k + t;
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(ys + p * H + c));
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -703,6 +719,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     a.ntiles = p.ntiles; a.offsets = p.offsets; a.perm = p.perm;
     a.topk_w = p.topk_w; a.gamma = p.gamma;
     a.E = E; a.k = k; a.T = T; a.H = H; a.status = p.status; a.k_order8 = bits == 8;
+    a.max_blocks = p.max_tiles_gu / (I / kBM);
 
     // gate/up: A = Wg, Wu rows (I per expert), K = H, out = hh [.][I]
     a.blkinfo = p.blkinfo; a.unitinfo = nullptr; a.M = I / kBM;
@@ -712,7 +729,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     // persistent: one CTA per SM (never more CTAs than the largest tile count)
     const int grid_gu = p.max_tiles_gu < nsm ? p.max_tiles_gu : nsm;
     const int nrg = T * k;
-    gather_rows_kernel<<<(unsigned)((nrg + 7) / 8), 256, 0, st>>>(p.x16, p.perm, p.xg, nrg, H, k);
+    gather_rows_kernel<<<(unsigned)((nrg + 7) / 8), 256, 0, st>>>(p.x16, p.perm, p.xg, nrg, H, k, p.status);
     trace_mark(st, 6);
     cudaError_t e = w16   ? launch_gemm<true, 16, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
                   : e4m3  ? launch_gemm<true, 8, true>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
@@ -736,7 +753,7 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     trace_mark(st, 8);
 
     const size_t nthr = (size_t)T * (H / 8);
-    combine_kernel<<<(unsigned)((nthr + 255) / 256), 256, 0, st>>>(p.ys, p.inv, out, T, H, k);
+    combine_kernel<<<(unsigned)((nthr + 255) / 256), 256, 0, st>>>(p.ys, p.inv, out, T, H, k, p.status);
     trace_mark(st, 9);
     return cudaGetLastError();
 }

@@ -172,7 +172,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(int T, int E, int k, int nch
 constexpr int kAssignWarps = kChunk / 32;
 __global__ void __launch_bounds__(kChunk) assign_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                                         const int32_t* __restrict__ chunk_base,
-                                                        int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+                                                        int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                                                        unsigned int* status) {
     extern __shared__ int sm_assign[];
     int* running = sm_assign;                       // [kAssignWarps][E]
     int* sel = sm_assign + kAssignWarps * E;        // [kChunk * k] the chunk's selections
@@ -213,6 +214,7 @@ __global__ void __launch_bounds__(kChunk) assign_kernel(const int32_t* __restric
         if (e >= 0 && (same & lt_mask) == 0) run_w[e] += __popc(same);   // group leader
         __syncwarp();
         if (e >= 0) {
+            pos = checked_index(pos, 0, T * k, status);
             perm[pos] = t * k + j;
             inv[(size_t)t * k + j] = pos;
         }
@@ -230,7 +232,7 @@ cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cud
                                           o.ntiles, L.I / kBM, L.H / kBM, tc.du, tc.bn);
     trace_mark(st, 4);
     assign_kernel<<<nchunk, kChunk, (kAssignWarps * E + kChunk * k) * sizeof(int), st>>>(o.topk_idx, T, E, k, o.chunk_base, o.perm,
-                                                                     o.inv);
+                                                                     o.inv, o.status);
     trace_mark(st, 5);
     return cudaGetLastError();
 }

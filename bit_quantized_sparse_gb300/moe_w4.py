@@ -22,9 +22,13 @@ from typing import Optional
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe_w4.so")
+# MOE_W4_DEBUG=1 selects the build with device-side bounds checks (and host-side
+# error messages on stderr); build it with `python -m bit_quantized_sparse_gb300._build --debug`
+DEBUG = os.environ.get("MOE_W4_DEBUG", "") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libmoe_w4_debug.so" if DEBUG else "libmoe_w4.so")
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m bit_quantized_sparse_gb300._build`")
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m bit_quantized_sparse_gb300._build"
+                      f"{' --debug' if DEBUG else ''}`")
 _lib = ctypes.CDLL(LIB_PATH)
 
 c_int, c_size_t, c_void_p, c_char_p = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
@@ -80,6 +84,8 @@ _SIGS = {
     "moe_w4_forward_decode_noalloc": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_w4_noalloc_status": (c_int, [c_void_p, c_void_p]),
     "moe_w4_test_skip_publish": (c_int, [c_void_p, c_size_t, c_int, c_void_p]),
+    "moe_w4_test_block_records_bytes": (c_size_t, [_P, c_int]),
+    "moe_w4_test_block_records": (c_int, [_P, c_int, c_void_p, c_size_t, c_void_p, c_size_t, c_void_p]),
     "moe_w4_strerror": (c_char_p, [c_int]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -104,6 +110,8 @@ moe_w4_last_traced_kernels = _lib.moe_w4_last_traced_kernels
 moe_w4_forward_decode_noalloc = _lib.moe_w4_forward_decode_noalloc
 moe_w4_noalloc_status = _lib.moe_w4_noalloc_status
 moe_w4_test_skip_publish = _lib.moe_w4_test_skip_publish
+moe_w4_test_block_records_bytes = _lib.moe_w4_test_block_records_bytes
+moe_w4_test_block_records = _lib.moe_w4_test_block_records
 
 
 def moe_w4_strerror(status: int) -> str:

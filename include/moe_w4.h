@@ -291,6 +291,21 @@ int moe_w4_set_tile_override(int bn, int du);
  * turns it off. */
 int moe_w4_test_skip_publish(void* workspace, size_t ws_bytes, int on, cudaStream_t stream);
 
+/* Test hook: the block records of the last prefill (or multi-row decode) call
+ * enqueued on `workspace` for T tokens, copied on `stream` to `dst` (device
+ * memory, at least moe_w4_test_block_records_bytes(L, T) bytes): two int32
+ * tile counts (gate/up blocks x I/128, down units x H/128), then one record of
+ * four int32 per block of grouped rows: expert (E for the shared expert's
+ * group), first row within the expert's group, rows, first grouped position.
+ * Blocks are listed expert by expert, routed experts first; only the first
+ * (tile count 0) / (I/128) records are meaningful.  ("Optimizing on-device
+ * inference for Apple Silicon", section "Keep expert routing on the GPU": the
+ * list of fixed-size blocks the grouped product processes.)  Returns
+ * MOE_W4_ERR_INVALID / _WORKSPACE or MOE_W4_ERR_LAUNCH. */
+size_t moe_w4_test_block_records_bytes(const moe_w4_layer* L, int T);
+int moe_w4_test_block_records(const moe_w4_layer* L, int T, const void* workspace, size_t ws_bytes,
+                              int32_t* dst, size_t dst_bytes, cudaStream_t stream);
+
 /* Number of kernels the most recent traced call launched (0 before any). */
 int moe_w4_last_traced_kernels(void);
 

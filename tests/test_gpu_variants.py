@@ -128,3 +128,45 @@ def test_separate_dequant_ablation_same_bits(env, name, bits, fmt):
     torch.cuda.synchronize()
     assert np.array_equal(_bits(torch, out), ref_bits)
     assert dl.status() == 0
+
+
+@pytest.mark.parametrize("name,bn", [("tiny_T4", 0), ("prefill_T512", 0), ("prefill_T512", 64),
+                                     ("prefill_T4096", 0)])
+def test_block_records_match_oracle_block_map(env, name, bn):
+    """The GPU's block list against the oracle's block map: routed experts'
+    blocks (expert, first row) exactly as oracle.block_map lists them for the
+    block height in use, each with rows min(bn, count - first row) and first
+    grouped position offsets[e] + first row; then the shared expert's blocks
+    over all T tokens at positions T*k + first row."""
+    torch, mw = env
+    L, x = S.draw_config(name)
+    dl = mw.DeviceLayer(L)
+    T = x.shape[0]
+    xd = mw.tokens_to_device(x)
+    ws = dl.workspace(T)
+    try:
+        assert mw.moe_w4_set_tile_override(bn, 0) == mw.MOE_W4_OK
+        mw.forward_prefill(dl, xd, ws=ws)
+        n = mw.moe_w4_test_block_records_bytes(ctypes.byref(dl.c), T)
+        rec = torch.zeros(n // 4, dtype=torch.int32, device="cuda")
+        st = torch.cuda.current_stream().cuda_stream
+        assert mw.moe_w4_test_block_records(ctypes.byref(dl.c), T, ws.data_ptr(), ws.numel(), rec.data_ptr(), n,
+                                            st) == mw.MOE_W4_OK
+        torch.cuda.synchronize()
+    finally:
+        mw.moe_w4_set_tile_override(0, 0)
+    rec = rec.cpu().numpy()
+    B = bn or 128
+    nblk = int(rec[0]) // (L.I // 128)
+    blocks = rec[2:2 + 4 * nblk].reshape(nblk, 4)
+    idx, _, _, _ = O.route(O.bf16_to_f64(x), L.router_w, L.router_bias, L.shared_gate, L.top_k)
+    counts, offsets, _, _ = O.group(idx, L.E)
+    routed = blocks[blocks[:, 0] < L.E]
+    assert [(int(e), int(r)) for e, r, _, _ in routed] == [(int(e), int(r)) for e, r in O.block_map(counts, B)]
+    for e, r0, rows, p0 in routed:
+        assert rows == min(B, counts[e] - r0) and p0 == offsets[e] + r0
+    shared = blocks[blocks[:, 0] == L.E]
+    assert [int(r) for r in shared[:, 1]] == list(range(0, T, B))
+    for _, r0, rows, p0 in shared:
+        assert rows == min(B, T - r0) and p0 == T * L.top_k + r0
+    assert len(routed) + len(shared) == nblk
