@@ -31,8 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "W4g64 MoE layer tok/s at T=1 & T=4096; % of HBM / bf16 TC roofline"
 WORKLOAD = "long_T16384"
 N_REPLICAS = 16
-PREFILL_KERNELS = ["router_scores", "topk", "chunk_count", "scan", "assign", "gather_rows", "gemm_gate_up", "gemm_down",
-                   "combine"]
+PREFILL_KERNELS = ["router_scores", "topk", "group", "gather_rows", "gemm_gate_up", "gemm_down", "combine"]
 DECODE_KERNELS = ["decode_router", "decode_gate_up", "decode_down"]   # the three-kernel path
 DECODE_FUSED = ["decode_fused"]
 SMALL_T = (4, 8)   # multi-row decode batches measured beside the step

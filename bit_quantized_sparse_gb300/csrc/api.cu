@@ -348,7 +348,7 @@ static int run_grouped(const moe_w4_layer* L, int T, const moe_w4_bf16* x, moe_w
     p.max_tiles_gu = w.max_tiles_gu;
     p.max_tiles_dn = w.max_tiles_dn;
     p.status = o.status;
-    trace_kernels(9);
+    trace_kernels(7);
     return launch_status(launch_grouped_ffn(*L, T, x, out, p, stream, sep ? w16 : nullptr));
 }
 

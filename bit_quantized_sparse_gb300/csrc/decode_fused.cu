@@ -58,6 +58,8 @@ constexpr int kMaxRouterRows = 4;       // router: H rows per thread, at most
 constexpr int kScoreReplicas = 8;       // copies of the published score partials (readers spread over them)
 constexpr int kHReplicas = 8;           // copies of the published h and its piece sums
 constexpr int kGuParts = 4;             // gate/up code slices arrive in this many parts (one barrier each)
+constexpr int kDnUnits = (kMaxSlots * 8 + kFWarps - 1) / kFWarps;   // down units per warp and pass
+constexpr int kDnUnitWords = 40;        // a down unit's h: 32 words (64 fp16 values), 8 piece sums
 
 struct FusedArgs {
     const uint16_t* x;          // [H] bf16
@@ -81,13 +83,13 @@ struct FusedArgs {
 };
 
 // smem carve-up (byte offsets from a 1024-aligned base), computed on both sides.
-// After the gate/up GEMV its code slices are dead: h (in B order) and its
-// 16-value piece sums then live in the gate codes region, the down partial sums
-// and row sums in the up one.
+// After the gate/up GEMV its code slices are dead: each warp's copy of the h
+// (in B order) and 16-value piece sums of its down units then lives in the gate
+// codes region, the down partial sums and row sums in the up one.
 struct FusedSmem {
     uint32_t gcodes, ucodes, dcodes, dslot, gsb, usb, dsb, xperm, xsum, xbs, logits, gred, gsum, usum, wred,
         misc, total;
-    uint32_t hperm, hpiece, dred;   // aliases (see above)
+    uint32_t hwarp, dred;   // aliases (see above)
     uint32_t code_region;              // bytes of one gate/up code region
     int RG, DR, NS;
     __host__ __device__ FusedSmem(int H, int E, int I, int k, int bits) {
@@ -121,13 +123,12 @@ struct FusedSmem {
         wred = take(kFWarps * (kRE + 1) * 4, 16);
         misc = take(512, 16);
         total = o;
-        hperm = gcodes;
-        hpiece = gcodes + NS * I * 2;   // [NS][I/16][2]
+        hwarp = gcodes;                 // [warp][kDnUnits * kDnUnitWords]
         dred = ucodes;                  // [NS * (I/64) * DR/16][16], then [NS][DR] row sums
     }
     // the aliased buffers fit their regions
     __host__ __device__ bool aliases_fit(int I) const {
-        return (uint32_t)(NS * I * 2 + NS * (I / 16) * 2 * 4) <= code_region &&
+        return (uint32_t)(kFWarps * kDnUnits * kDnUnitWords * 4) <= code_region &&
                (uint32_t)((NS * (I / 64) * DR + NS * DR) * 4) <= code_region;
     }
 };
@@ -218,8 +219,9 @@ MW4_DEV void a_frag(uint32_t wg, uint32_t wh, uint32_t (&a)[4]) {
 // group_mma adds.  The MMAs are issued step by step across the units, so that
 // consecutive MMAs accumulate into different units: a unit's chain of
 // dependent MMAs (24 cycles each) is covered by the other units' MMAs instead
-// of stalling the warp.  B comes from shared memory per unit (bperm[q]), or,
-// with SHARED_B, from the registers `bsh` (load_bfrag) for every unit.
+// of stalling the warp.  B comes from shared memory per unit (bperm[q]: the
+// unit's group, 8 entries of 16 bytes), or, with SHARED_B, from the registers
+// `bsh` (load_bfrag) for every unit.
 template <int CODE, int NU, bool SHARED_B>
 MW4_DEV void units_mma(const uint8_t* const (&codes)[NU], int rows, const int (&r0)[NU], const int (&grp)[NU],
                        const uint4* const (&bperm)[NU], const uint32_t (&bsh)[8], float (&d)[NU][4]) {
@@ -245,10 +247,10 @@ MW4_DEV void units_mma(const uint8_t* const (&codes)[NU], int rows, const int (&
                     b[q][0] = bsh[2 * h]; b[q][1] = bsh[2 * h + 1];
                 }
             } else if (CODE == kCodeU4) {
-                const uint4 v = bperm[q][bk * 4 + c];
+                const uint4 v = bperm[q][h * 4 + c];
                 b[q][0] = v.x; b[q][1] = v.y; b[q][2] = v.z; b[q][3] = v.w;
             } else {
-                const uint2 v = reinterpret_cast<const uint2*>(bperm[q])[bk * 4 + c];
+                const uint2 v = reinterpret_cast<const uint2*>(bperm[q])[h * 4 + c];
                 b[q][0] = v.x; b[q][1] = v.y;
             }
         }
@@ -345,8 +347,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
     float* gsum = reinterpret_cast<float*>(sm + L.gsum);
     float* usum = reinterpret_cast<float*>(sm + L.usum);
     float* wred = reinterpret_cast<float*>(sm + L.wred);
-    uint32_t* hperm = reinterpret_cast<uint32_t*>(sm + L.hperm);   // after the gate/up GEMV
-    float* hpiece = reinterpret_cast<float*>(sm + L.hpiece);
+    uint32_t* hwarp = reinterpret_cast<uint32_t*>(sm + L.hwarp);   // after the gate/up GEMV
     float* dred = reinterpret_cast<float*>(sm + L.dred);
     uint8_t* misc = sm + L.misc;
     // TMA boxes of 128-byte code rows: 256 columns of 4-bit codes, 128 of one-byte codes.
@@ -681,7 +682,8 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
 #pragma unroll
             for (int t = 0; t < kTC; ++t) acc[t][0] = acc[t][1] = 0.f;
             for (int gg = warp; gg < ngrp; gg += kFWarps) {
-                if (!mbar_wait(&bar_gu[gg / (ngrp / kGuParts)], 0, abort_flag, status)) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(&bar_gu[gg / (ngrp / kGuParts)], 0, abort_flag, status)))
+                    break;   // warp-uniform: the MMAs need the whole warp
                 uint32_t bf[8];
                 load_bfrag<CODE>(reinterpret_cast<const uint4*>(xperm), gg, bf);
                 float d[kTC][4];
@@ -732,6 +734,7 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             (t < ntile / 2 ? gsum : usum)[(t % (ntile / 2)) * 16 + r] = v;
         }
     }
+    cp_async_wait<0>();   // this thread's pieces of the down scales and biases (read after the barrier)
     __syncthreads();
     // ---------------------------------------------------------------- 4. h exchange
     // this CTA's RG values of h as RG/2 tagged fp16 pairs in B order (entry q of the
@@ -768,78 +771,81 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
             }
         }
     }
-    if (down_cta) {
-        // all NS slots' h and its piece sums: thread t polls words t, t + kFThreads, ...
-        // of the two arrays seen as one (bounded wait), then stores h in B order for
-        // the down GEMV and the sums beside it (this CTA's gate codes are dead)
-        const int nw = NS * (I / 2), ns2 = NS * (I / 16) * 2;
-        constexpr int kPer = (kMaxSlots * (2048 / 2 + 2048 / 8) + kFThreads - 1) / kFThreads;   // at most
-        const int per = kI ? (kMaxSlots * (kI / 2 + kI / 8) + kFThreads - 1) / kFThreads : kPer;
-        const uint64_t* hxr = a.hx + (size_t)(G % kHReplicas) * nw;     // this CTA's replica
-        const uint64_t* hsr = a.hsx + (size_t)(G % kHReplicas) * ns2;
-        auto src = [&](int i) { return i < nw ? hxr + i : hsr + (i - nw); };
-        uint64_t w[kPer];
+    // ---------------------------------------------------------------- 5. h in, down GEMV, weighted sum, output rows
+    // Units (slot, row tile, group) in slot-major order; warp w takes the contiguous
+    // units [w*nunit/16, (w+1)*nunit/16), so most warps need one slot's h.  Each warp
+    // polls only the h words and piece sums of its own units (bounded wait) and
+    // starts its MMAs as soon as they carry the call's tag: the down products of the
+    // slots that publish early overlap the wait for the late ones.  Each unit's 16
+    // row sums go to dred[unit][16].
+    const int ngrp = I / 64, ntl = DR / 16, nunit = NS * ntl * ngrp;
+    constexpr int kU = kDnUnits;                                  // units per pass (I = 512: every unit of the warp)
+    constexpr int kUW = kDnUnitWords;
+    constexpr int kPW = (kU * kUW + 31) / 32;                     // polled words per lane and pass
+    // (every branch below is warp-uniform: the MMAs need the whole warp)
+    if (__all_sync(0xffffffffu, down_cta && gu_done && !*abort_flag)) {
+        const int ua = warp * nunit / kFWarps, ub = (warp + 1) * nunit / kFWarps;
+        const bool w_ok = __all_sync(0xffffffffu, mbar_wait(bar_dn, 0, abort_flag, status) &&
+                                                      mbar_wait(bar_dsh, 0, abort_flag, status));
+        const uint64_t* hxr = a.hx + (size_t)(G % kHReplicas) * NS * (I / 2);      // this CTA's replica
+        const uint64_t* hsr = a.hsx + (size_t)(G % kHReplicas) * NS * (I / 16) * 2;
+        uint32_t* wh = hwarp + warp * (kU * kUW);                                  // this warp's h and sums
+        for (int u0 = ua; w_ok && u0 < ub; u0 += kU) {
+            const int nu = min(kU, ub - u0), nwords = nu * kUW;
+            // word i of the pass: unit u0 + i / kUW, its h word (i % kUW < 32) or piece sum
+            auto src = [&](int i) {
+                const int u = u0 + i / kUW, k2 = i % kUW, j = u / (ntl * ngrp), gg = u % ngrp;
+                return k2 < 32 ? hxr + (size_t)j * (I / 2) + gg * 32 + k2
+                               : hsr + ((size_t)j * (I / 16) + gg * 4) * 2 + (k2 - 32);
+            };
+            uint64_t w[kPW];
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int i = tid + j * kFThreads;
-            w[j] = (j < per && i < nw + ns2) ? ld_tagged(src(i)) : 0ull;
-        }
-        const uint64_t t0 = globaltimer();
-        for (int it = 1;; ++it) {
-            bool all = true;
+            for (int m = 0; m < kPW; ++m) {
+                const int i = lane + 32 * m;
+                w[m] = i < nwords ? ld_tagged(src(i)) : 0ull;
+            }
+            const uint64_t t0 = globaltimer();
+            for (int it = 1;; ++it) {
+                bool all = true;
 #pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                const int i = tid + j * kFThreads;
-                if (j < per && i < nw + ns2 && tag_of(w[j]) != xtag) {
-                    all = false;
-                    w[j] = ld_tagged(src(i));
+                for (int m = 0; m < kPW; ++m) {
+                    const int i = lane + 32 * m;
+                    if (i < nwords && tag_of(w[m]) != xtag) {
+                        all = false;
+                        w[m] = ld_tagged(src(i));
+                    }
+                }
+                if (all) break;
+                if ((it & 15) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+                    raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
                 }
             }
-            if (all) break;
-            if ((it & 15) == 0 && globaltimer() - t0 > kWaitLimitNs) {
-                raise_status(status, MOE_W4_STATUS_WAIT_TIMEOUT);
-                *abort_flag = 1;
-                break;
-            }
-        }
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int i = tid + j * kFThreads;
-            if (j < per && i < nw) hperm[i] = (uint32_t)w[j];
-            else if (j < per && i < nw + ns2) hpiece[i - nw] = val_of(w[j]);
-        }
-    }
-    // ---------------------------------------------------------------- 5. down GEMV, weighted sum, output rows
-    cp_async_wait<0>();   // this thread's pieces of the down scales and biases
-    const bool dn_ok = __syncthreads_and((down_cta && gu_done) ? (mbar_wait(bar_dn, 0, abort_flag, status) &&
-                                                                  mbar_wait(bar_dsh, 0, abort_flag, status))
-                                                               : 0) &&
-                       !*abort_flag;
-    // every slot's h carries the tag, so every CTA has read the call counter
-    if (dn_ok && G == 0 && tid == 0) st_relaxed_u32(&a.ctrl->pad[kCtrlEpochWord], xtag);
-    if (dn_ok) {
-        // units (slot, row tile, group), strided over the warps; each unit's 16 row
-        // sums go to dred[unit][16]
-        const int ngrp = I / 64, ntl = DR / 16, nunit = NS * ntl * ngrp;
-        constexpr int kU = (kMaxSlots * 8 + kFWarps - 1) / kFWarps;   // units per warp in flight (I = 512)
-        for (int u0 = warp; u0 < nunit; u0 += kU * kFWarps) {
-            // branch-free: a unit past the end repeats the last one, its result unstored
+            for (int m = 0; m < kPW; ++m) {
+                const int i = lane + 32 * m;
+                if (i < nwords) wh[i] = (uint32_t)w[m];   // h pairs, or the float bits of a piece sum
+            }
+            __syncwarp();
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            // branch-free: a unit past the warp's range repeats its last one, unstored
             float d[kU][4];
             int uj[kU], ugg[kU], utl[kU];
             const uint8_t* ucodes_q[kU];
-            const uint4* ub[kU];
+            const uint4* ub4[kU];
             const uint32_t nob[8] = {};
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
-                const int u = min(u0 + q * kFWarps, nunit - 1);
+                const int qq = min(q, nu - 1), u = u0 + qq;
                 uj[q] = u / (ntl * ngrp);
                 utl[q] = (u / ngrp) % ntl * 16;
                 ugg[q] = u % ngrp;
                 d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
                 ucodes_q[q] = dcodes + (size_t)uj[q] * L.dslot;
-                ub[q] = reinterpret_cast<const uint4*>(hperm) + (size_t)uj[q] * (I / 8);
+                ub4[q] = reinterpret_cast<const uint4*>(wh + qq * kUW);
             }
-            units_mma<CODE, kU, false>(ucodes_q, DR, utl, ugg, ub, nob, d);
+            units_mma<CODE, kU, false>(ucodes_q, DR, utl, ugg, ub4, nob, d);
             const int g = lane >> 2;
 #pragma unroll
             for (int q = 0; q < kU; ++q) {
@@ -847,20 +853,27 @@ decode_fused_kernel(const __grid_constant__ FusedArgs a, const __grid_constant__
                 const uint16_t* sc = dsb + (size_t)j * 2 * DR * ngrp;
                 const uint16_t* bi = sc + DR * ngrp;
                 // per-64-value group sums of h: its four 16-value pieces in order
-                const float* pc = hpiece + 8 * (j * ngrp + gg);
+                const float* pc = reinterpret_cast<const float*>(wh + min(q, nu - 1) * kUW + 32);
                 const float bs = ((pc[0] + pc[2]) + pc[4]) + pc[6], hs = ((pc[1] + pc[3]) + pc[5]) + pc[7];
                 const float v0 = fmaf(bf16_bits_to_float(sc[r0 * ngrp + gg]), d[q][0] - 1024.f * bs,
                                       bf16_bits_to_float(bi[r0 * ngrp + gg]) * hs);
                 const float v1 = fmaf(bf16_bits_to_float(sc[(r0 + 8) * ngrp + gg]), d[q][2] - 1024.f * bs,
                                       bf16_bits_to_float(bi[(r0 + 8) * ngrp + gg]) * hs);
-                const int u = u0 + q * kFWarps;
-                if ((lane & 3) == 0 && u < nunit) {
+                const int u = u0 + q;
+                if ((lane & 3) == 0 && q < nu) {
                     dred[u * 16 + g] = v0;
                     dred[u * 16 + g + 8] = v1;
                 }
             }
+            __syncwarp();   // this pass's h is read before the next pass overwrites it
         }
-        __syncthreads();
+    }
+    __syncthreads();
+    const bool dn_ok = down_cta && gu_done && !*abort_flag;
+    // every slot's h carried the tag for one of this CTA's warps, so every CTA has read
+    // the call counter
+    if (dn_ok && G == 0 && tid == 0) st_relaxed_u32(&a.ctrl->pad[kCtrlEpochWord], xtag);
+    if (dn_ok) {
         // out row r = sum over slots (in order) of the slot's weight times its row sum
         // over the groups (in order): the row sums y[j][r] by one thread each, then
         // the weighted sums

@@ -730,13 +730,13 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     const int grid_gu = p.max_tiles_gu < nsm ? p.max_tiles_gu : nsm;
     const int nrg = T * k;
     gather_rows_kernel<<<(unsigned)((nrg + 7) / 8), 256, 0, st>>>(p.x16, p.perm, p.xg, nrg, H, k, p.status);
-    trace_mark(st, 6);
+    trace_mark(st, 4);
     cudaError_t e = w16   ? launch_gemm<true, 16, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
                   : e4m3  ? launch_gemm<true, 8, true>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
                   : bits == 8 ? launch_gemm<true, 8, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
                               : launch_gemm<true, 4, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st);
     if (e != cudaSuccess) return e;
-    trace_mark(st, 7);
+    trace_mark(st, 5);
 
     // down: A = Wd rows (H per expert), K = I, B = hh rows, out = ys [.][H]
     GemmArgs b = a;
@@ -750,11 +750,11 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
       : bits == 8 ? launch_gemm<false, 8, false>(b, grid_dn, md, md, msd, msd, mh, mh, st)
                   : launch_gemm<false, 4, false>(b, grid_dn, md, md, msd, msd, mh, mh, st);
     if (e != cudaSuccess) return e;
-    trace_mark(st, 8);
+    trace_mark(st, 6);
 
     const size_t nthr = (size_t)T * (H / 8);
     combine_kernel<<<(unsigned)((nthr + 255) / 256), 256, 0, st>>>(p.ys, p.inv, out, T, H, k, p.status);
-    trace_mark(st, 9);
+    trace_mark(st, 7);
     return cudaGetLastError();
 }
 

@@ -75,7 +75,7 @@ struct RouteOut {
     int32_t* counts;   // [E] routed (tile maps also need the shared group)
     int32_t* offsets;  // [E+1]
     int32_t* perm; int32_t* inv;
-    int32_t* chunk_base;
+    int32_t* chunk_base;   // [chunks][E] assignments per (chunk of kChunk tokens, expert), counted by top-k
     float* logits;       // [kRouterSplit][T][E] partial router scores (tensor-core path), [T][E] otherwise
     uint16_t* router_a;  // [Epad][3H] bf16 split router weights, written per call unless the layer has them
     uint16_t* x16;     // fp16 copy of x written by the top-k kernel (NULL: not needed)

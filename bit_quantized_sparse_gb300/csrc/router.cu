@@ -50,6 +50,8 @@ struct RouterTcArgs {
     const float* bias;
     float* logits;   // [kRtSplit][T][E] partial scores (the bias goes into the first)
     int T, H, E;
+    int32_t* hist;   // the grouping's histogram, zeroed here before the top-k kernel counts (or NULL)
+    int hist_n;      // its ints
     unsigned int* status;
 };
 
@@ -73,6 +75,11 @@ router_tc_kernel(const __grid_constant__ RouterTcArgs a, const __grid_constant__
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1) + 1;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kRtBN, kh = blockIdx.z;
+    if (a.hist) {   // every CTA zeroes its share of the histogram
+        const int nblk = gridDim.x * gridDim.y * gridDim.z;
+        const int b = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        for (int i = b * blockDim.x + tid; i < a.hist_n; i += nblk * blockDim.x) a.hist[i] = 0;
+    }
     const int hsteps = a.H / kBK, s0 = kh * hsteps / kRtSplit, s1 = (kh + 1) * hsteps / kRtSplit, nS = s1 - s0;
     if (tid == 0) {
         for (int s = 0; s < kRtStages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -160,7 +167,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 4 : 2) topk_kernel
                                                                int k, int32_t* __restrict__ idx,
                                                                float* __restrict__ w, float* __restrict__ gamma,
                                                                uint16_t* __restrict__ x16, int bits,
-                                                               unsigned int* status) {
+                                                               int32_t* __restrict__ hist, unsigned int* status) {
     extern __shared__ float sm_topk[];
     float* gs = sm_topk;                    // [H] shared-expert gate vector, staged once per block
     float* sc_all = sm_topk + H;            // [kTopkWarps][E] scores
@@ -188,6 +195,9 @@ __global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 4 : 2) topk_kernel
     for (int e = lane; e < E; e += 32) sc[e] = nsplit > 1 ? l0[e] + l1[e] : l0[e];
     __syncwarp();
     select_topk_warp(sc, E, k, idx + (size_t)t * k, w + (size_t)t * k);
+    // the grouping's histogram: assignments per (chunk of kChunk tokens, expert)
+    // (each lane reads back the selection it wrote)
+    if (hist && lane < k) atomicAdd(&hist[(size_t)(t / kChunk) * E + idx[(size_t)t * k + lane]], 1);
     float d = 0.f;
     bool fits = true;
     cp_async_wait<0>();   // each lane reads back only the chunks it copied
@@ -313,7 +323,9 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
             if (e != cudaSuccess) return e;
             attr[dev] = router_tc_smem();
         }
-        RouterTcArgs ra_args{L.router_bias, o.logits, T, L.H, L.E, o.status};
+        // the grouping's per-chunk histogram, zeroed by this kernel, counted by the top-k kernel
+        RouterTcArgs ra_args{L.router_bias, o.logits, T, L.H, L.E, o.chunk_base,
+                             ((T + kChunk - 1) / kChunk) * L.E, o.status};
         router_tc_kernel<<<dim3(Epad / kBM, (T + kRtBN - 1) / kRtBN, kRtSplit), 256, router_tc_smem(), st>>>(ra_args, mA,
                                                                                                            mX);
     }
@@ -324,16 +336,16 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
     const int nit = (L.H + 255) / 256;   // H <= 4096
     if (nit <= 2)
         topk_kernel<2><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                o.gamma, o.x16, code_bits_of(L), o.status);
+                                                o.gamma, o.x16, code_bits_of(L), o.chunk_base, o.status);
     else if (nit <= 4)
         topk_kernel<4><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                o.gamma, o.x16, code_bits_of(L), o.status);
+                                                o.gamma, o.x16, code_bits_of(L), o.chunk_base, o.status);
     else if (nit <= 8)
         topk_kernel<8><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                o.gamma, o.x16, code_bits_of(L), o.status);
+                                                o.gamma, o.x16, code_bits_of(L), o.chunk_base, o.status);
     else
         topk_kernel<16><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                 o.gamma, o.x16, code_bits_of(L), o.status);
+                                                 o.gamma, o.x16, code_bits_of(L), o.chunk_base, o.status);
     trace_mark(st, 2);
     return cudaGetLastError();
 }
