@@ -546,12 +546,17 @@ def gemm_flops(c, T, which):
     return 2 * rows * H * 2 * I if which == "gate_up" else 2 * rows * I * H
 
 
-def spread(values, scale=1.0):
-    """Median, 10th and 90th percentile of per-replay times (seconds), scaled."""
+def spread(values, scale=1.0, n_boot=2000, seed=0):
+    """Median, 10th and 90th percentile of per-replay times (seconds), scaled,
+    and a 95% bootstrap confidence interval of the median (percentile method,
+    n_boot resamples of the replays with replacement, seeded)."""
     if not values:
         return None
     v = np.sort(np.asarray(values, np.float64)) * scale
+    rng = np.random.default_rng(seed)
+    meds = np.median(v[rng.integers(0, v.size, size=(n_boot, v.size))], axis=1)
     return {"median": float(np.median(v)), "p10": float(np.percentile(v, 10)), "p90": float(np.percentile(v, 90)),
+            "median_ci95": [float(np.percentile(meds, 2.5)), float(np.percentile(meds, 97.5))],
             "replays": int(v.size)}
 
 

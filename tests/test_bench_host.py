@@ -98,3 +98,18 @@ def test_spread_percentiles():
     assert sp["median"] == 3000.0 and sp["replays"] == 5
     assert abs(sp["p10"] - 1400.0) < 1e-9 and abs(sp["p90"] - 4600.0) < 1e-9
     assert bench.spread([]) is None
+
+
+def test_spread_bootstrap_interval():
+    """The median's bootstrap interval holds the median, lies inside the sample's
+    range, is reproducible (seeded) and narrows as the replays grow."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    small = list(rng.normal(1.0, 0.1, 20))
+    big = list(rng.normal(1.0, 0.1, 2000))
+    a, b = bench.spread(small), bench.spread(small)
+    assert a["median_ci95"] == b["median_ci95"]
+    lo, hi = a["median_ci95"]
+    assert min(small) <= lo <= a["median"] <= hi <= max(small)
+    lo2, hi2 = bench.spread(big)["median_ci95"]
+    assert hi2 - lo2 < hi - lo
