@@ -344,6 +344,10 @@ def run_gpu(args, rank, local_rank, world, dist):
         torch.cuda.current_stream().cuda_stream), "decode"), DECODE_KERNELS)
     if len(k_dec) == 1:                     # batch-1 decode of this shape is one fused kernel
         k_dec = {DECODE_FUSED[0]: next(iter(k_dec.values()))}
+    # a multi-row decode call (4 rows, the grouped path): where its time goes
+    k_dec4 = {} if args.no_multirow else traced(lambda: mw._check(mw.moe_w4_forward_decode(
+        ctypes.byref(layers[1].c), 4, xdec[:4].data_ptr(), outdec[:4].data_ptr(), ws.data_ptr(), ws.numel(),
+        torch.cuda.current_stream().cuda_stream), "decode T=4"), PREFILL_KERNELS)
 
     # weight-format variants (8-bit affine codes, FP8 E4M3 codes): layers of the
     # same shape with one-byte codes; a 4096-row prefill chunk and batch-1
@@ -440,7 +444,8 @@ def run_gpu(args, rank, local_rank, world, dist):
         raise RuntimeError(f"device status {status}")
     return dict(c=c, L0=L0, x_np=x_np, xdec_np=xdec_np, t_step=t_step, t_pre=t_pre, t_dec=t_dec, t_e2e=t_e2e, small=small,
                 per_step=per_step, per_pre=per_pre, per_dec=per_dec,
-                variants=variants, clocks=clocks, k_pre=k_pre, k_dec=k_dec, gpu=torch.cuda.get_device_name(device),
+                variants=variants, clocks=clocks, k_pre=k_pre, k_dec=k_dec, k_dec4=k_dec4,
+                gpu=torch.cuda.get_device_name(device),
                 ablations=abl)
 
 
@@ -724,7 +729,8 @@ def main():
             "format_variants": {v: variant_summary(c, w, chunk, world, pk) for v, w in r["variants"].items()},
             "roofline": roof,
             "kernels_us": {"prefill_4096": {k: 1e6 * v for k, v in r["k_pre"].items()},
-                           "decode_T1": {k: 1e6 * v for k, v in r["k_dec"].items()}},
+                           "decode_T1": {k: 1e6 * v for k, v in r["k_dec"].items()},
+                           **({"decode_T4": {k: 1e6 * v for k, v in r["k_dec4"].items()}} if r["k_dec4"] else {})},
             "kernel_share": {f"{a}:{b}": v / total for (a, b), v in sorted(share.items(), key=lambda kv: -kv[1])},
             "gpu_launches": args.steps * (4 * len(PREFILL_KERNELS) + ndec * dec_launches),
             "decode_path": "one fused kernel (decode_fused_kernel)" if fused else "three kernels",
