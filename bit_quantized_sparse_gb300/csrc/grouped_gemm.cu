@@ -598,11 +598,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     const int per_row = H / 8;
     if (i >= (size_t)T * per_row) return;
     const int t = (int)(i / per_row), c = (int)(i % per_row) * 8;
-    float acc[8] = {};
-    for (int j = 0; j <= k; ++j) {
+    // all k + 1 rows requested before the first is added (k <= 8), then added in order
+    uint4 v[9];
+#pragma unroll
+    for (int j = 0; j < 9; ++j) {
+        if (j > k) break;
         const size_t p = (j < k) ? (size_t)checked_index(inv[(size_t)t * k + j], 0, T * k, status) : (size_t)T * k + t;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(ys + p * H + c));
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        v[j] = __ldg(reinterpret_cast<const uint4*>(ys + p * H + c));
+    }
+    float acc[8] = {};
+#pragma unroll
+    for (int j = 0; j < 9; ++j) {
+        if (j > k) break;
+        const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float2 f = __half22float2(u32_as_h2(u[q]));
