@@ -16,6 +16,7 @@
 // array, so its device address is looked up once per device with
 // cudaGetSymbolAddress (with that device current) and cached; the first call on
 // a device does this set-up.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -27,6 +28,7 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_W4_NOALLOC_SCRATC
 
 static constexpr int kMaxDevices = 64;
 static void* g_scratch_addr[kMaxDevices] = {};
+static std::atomic<int> g_noalloc_skip_publish{0};   // test hook (moe_w4_noalloc_test_skip_publish)
 static std::mutex g_scratch_mu;   // first calls from several host threads set up the cache one at a time
 
 static size_t up256n(size_t v) { return (v + 255) & ~size_t(255); }
@@ -117,6 +119,10 @@ extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const
     if (cudaMemsetAsync(b + n.ctrl, 0, offsetof(Ctrl, pad) + kCtrlEpochWord * sizeof(unsigned int), stream) !=
         cudaSuccess)
         return MOE_W4_ERR_LAUNCH;
+    if (g_noalloc_skip_publish.load() &&   // failure-detection test hook: one CTA skips its router publish
+        cudaMemsetAsync(b + n.ctrl + offsetof(Ctrl, pad) + kCtrlInjectWord * sizeof(unsigned int), 0x5A,
+                        sizeof(unsigned int), stream) != cudaSuccess)
+        return MOE_W4_ERR_LAUNCH;
     DecodeWs d{};
     d.part = reinterpret_cast<float*>(b + n.part);
     d.idx = reinterpret_cast<int32_t*>(b + n.idx);
@@ -142,4 +148,9 @@ extern "C" int moe_w4_noalloc_status(unsigned int* status, cudaStream_t stream) 
     return cudaMemcpyAsync(status, word, sizeof(unsigned int), cudaMemcpyDefault, stream) == cudaSuccess
                ? MOE_W4_OK
                : MOE_W4_ERR_LAUNCH;
+}
+
+extern "C" int moe_w4_noalloc_test_skip_publish(int on) {
+    g_noalloc_skip_publish.store(on ? 1 : 0);
+    return MOE_W4_OK;
 }

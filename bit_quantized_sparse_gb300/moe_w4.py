@@ -83,6 +83,7 @@ _SIGS = {
     "moe_w4_last_traced_kernels": (c_int, []),
     "moe_w4_forward_decode_noalloc": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_w4_noalloc_status": (c_int, [c_void_p, c_void_p]),
+    "moe_w4_noalloc_test_skip_publish": (c_int, [c_int]),
     "moe_w4_test_skip_publish": (c_int, [c_void_p, c_size_t, c_int, c_void_p]),
     "moe_w4_test_block_records_bytes": (c_size_t, [_P, c_int]),
     "moe_w4_test_block_records": (c_int, [_P, c_int, c_void_p, c_size_t, c_void_p, c_size_t, c_void_p]),
@@ -109,6 +110,7 @@ moe_w4_set_tile_override = _lib.moe_w4_set_tile_override
 moe_w4_last_traced_kernels = _lib.moe_w4_last_traced_kernels
 moe_w4_forward_decode_noalloc = _lib.moe_w4_forward_decode_noalloc
 moe_w4_noalloc_status = _lib.moe_w4_noalloc_status
+moe_w4_noalloc_test_skip_publish = _lib.moe_w4_noalloc_test_skip_publish
 moe_w4_test_skip_publish = _lib.moe_w4_test_skip_publish
 moe_w4_test_block_records_bytes = _lib.moe_w4_test_block_records_bytes
 moe_w4_test_block_records = _lib.moe_w4_test_block_records

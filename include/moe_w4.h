@@ -256,6 +256,16 @@ int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const moe_w4_bf1
  * MOE_W4_ERR_LAUNCH if the copy cannot be enqueued. */
 int moe_w4_noalloc_status(unsigned int* status, cudaStream_t stream);
 
+/* Failure-detection test hook for moe_w4_forward_decode_noalloc (no
+ * production use; process-wide).  on != 0: the following one-kernel batch-1
+ * calls have one CTA skip publishing its router scores, so the other CTAs'
+ * bounded waits run out (after about 2 s): the call completes, its output is
+ * not valid, and the status word (moe_w4_noalloc_status) gets
+ * MOE_W4_STATUS_WAIT_TIMEOUT.  The aborting CTAs advance the call counter, so
+ * the next call is valid.  No GPU fault, trap or hang is involved.  on = 0
+ * turns it off.  Always returns MOE_W4_OK. */
+int moe_w4_noalloc_test_skip_publish(int on);
+
 /* Optional tracing for benchmarks: while set, every forward call records
  * events[0..n_events) (cudaEvent_t, created by the caller) on its stream:
  * event 0 before its first kernel and event i after its i-th kernel, so

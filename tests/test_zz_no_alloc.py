@@ -119,3 +119,32 @@ def test_noalloc_rejects_oversized_calls(env):
     fn = _fn(mw)
     assert fn(ctypes.byref(c), 16, p, p, None) == mw.MOE_W4_ERR_SCRATCH
     assert "scratch" in mw.moe_w4_strerror(mw.MOE_W4_ERR_SCRATCH)
+
+
+def test_noalloc_wait_timeout_then_valid_call(env):
+    """Failure detection on the allocation-free path, without a fault: with the
+    test hook on, one CTA of the batch-1 kernel skips publishing its router
+    scores, the others' bounded waits run out (about 2 s) and the status word
+    reports MOE_W4_STATUS_WAIT_TIMEOUT; the aborting CTAs advance the call
+    counter, so the next call (hook off) is right with a clear status."""
+    torch, mw = env
+    fn = _fn(mw)
+    stream = torch.cuda.current_stream().cuda_stream
+    L, x = S.draw_config("decode_T1", T=2)
+    dl = mw.DeviceLayer(L)
+    xd = mw.tokens_to_device(x)
+    ref = O.moe_layer(L, x)["out"]
+    out = torch.full((1, L.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    try:
+        assert mw.moe_w4_noalloc_test_skip_publish(1) == mw.MOE_W4_OK
+        assert fn(ctypes.byref(dl.c), 1, xd[:1].data_ptr(), out.data_ptr(), stream) == mw.MOE_W4_OK
+        torch.cuda.synchronize()
+    finally:
+        mw.moe_w4_noalloc_test_skip_publish(0)
+    assert _status(torch, mw) & mw.MOE_W4_STATUS_WAIT_TIMEOUT
+    for i in range(2):
+        assert fn(ctypes.byref(dl.c), 1, xd[i:i + 1].data_ptr(), out.data_ptr(), stream) == mw.MOE_W4_OK
+        torch.cuda.synchronize()
+        m = TOL.metrics(O.bf16_to_f64(_bits(torch, out)), ref[i:i + 1])
+        assert TOL.within(m), (i, m)
+        assert _status(torch, mw) == 0, i
