@@ -34,7 +34,9 @@ N_REPLICAS = 16
 PREFILL_KERNELS = ["router_scores", "topk", "group", "gather_rows", "gemm_gate_up", "gemm_down", "combine"]
 DECODE_KERNELS = ["decode_router", "decode_gate_up", "decode_down"]   # the three-kernel path
 DECODE_FUSED = ["decode_fused"]
-SMALL_T = (4, 8)   # multi-row decode batches measured beside the step
+SMALL_T = (2, 4, 6, 8)   # multi-row decode batches measured beside the step
+MULTIROW_PATHS = {1: "one-kernel batch-1 decode once per row (decode_fused_kernel, T launches)",
+                  2: "grouped tensor-core path (one read per selected expert)"}
 # prefill tile choices of the ablation table: (token rows per block, row blocks per down unit); the first is the default
 TILE_CHOICES = ((128, 4), (128, 2), (128, 1), (64, 4), (64, 2), (64, 1), (32, 1))
 ABLATION_T = (512, 2048, 4096)   # prefill sizes of the ablations (2048 rows = 16,384 assignments, 64 per expert)
@@ -288,16 +290,19 @@ def run_gpu(args, rank, local_rank, world, dist):
     t_pre = timed(g_pre, args.steps, per_pre)
     t_dec = timed(g_dec, args.steps, per_dec)
 
-    # multi-row decode (T = 4 and 8 rows per call, the grouped path): calls
-    # cycling the replica layers over slices of the decode rows; the bytes a call
-    # must move count every distinct expert its rows select once (routing by the
-    # library's own router)
+    # multi-row decode (T = 2, 4 and 8 rows per call): calls cycling the replica
+    # layers over slices of the decode rows; the bytes a call must move count
+    # every distinct expert its rows select once (routing by the library's own
+    # router).  Each size is also timed on the path the library did not choose
+    # (the row limit of moe_w4_set_decode_fused_rows moved past it), which is
+    # the measurement behind that limit.
     small = {}
     n_small = 32
-    for Tm in (() if args.no_multirow else SMALL_T):
-        def dec_small(Tm=Tm):
+
+    def time_small(Tm):
+        def dec_small():
             for i in range(n_small):
-                o = (i * Tm) % ndec
+                o = (i * Tm) % (ndec - ndec % Tm)   # whole slices of Tm rows inside the decode rows
                 mw._check(mw.moe_w4_forward_decode(ctypes.byref(layers[i % N_REPLICAS].c), Tm,
                                                    xdec[o:o + Tm].data_ptr(), outdec[o:o + Tm].data_ptr(),
                                                    ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream),
@@ -305,13 +310,25 @@ def run_gpu(args, rank, local_rank, world, dist):
         with torch.cuda.stream(stream):
             dec_small()
         torch.cuda.synchronize()
-        t_small = timed(capture(dec_small), args.steps) / args.steps / n_small
+        return timed(capture(dec_small), args.steps) / args.steps / n_small
+
+    for Tm in (() if args.no_multirow else SMALL_T):
+        t_small = time_small(Tm)
+        path = mw.decode_path(layers[0], Tm)
+        t_alt = None
+        if mw.decode_path(layers[0], 1) == mw.MOE_W4_PATH_FUSED_ROWS:   # both paths exist for this layer
+            mw._check(mw.moe_w4_set_decode_fused_rows(1 if path == mw.MOE_W4_PATH_FUSED_ROWS else mw.DECODE_MAX_T),
+                      "row limit")
+            try:
+                t_alt = time_small(Tm)
+            finally:
+                mw._check(mw.moe_w4_set_decode_fused_rows(0), "row limit")
         distinct = []
         for i in range(n_small):
-            o = (i * Tm) % ndec
+            o = (i * Tm) % (ndec - ndec % Tm)   # whole slices of Tm rows inside the decode rows
             cnt = mw.route(layers[i % N_REPLICAS], xdec[o:o + Tm])["counts"]
             distinct.append(int((cnt > 0).sum().item()))
-        small[Tm] = (t_small, float(np.mean(distinct)))
+        small[Tm] = (t_small, float(np.mean(distinct)), path, t_alt)
 
     # per-kernel durations: the library records events around its kernels
     def traced(fn, names):
@@ -344,10 +361,13 @@ def run_gpu(args, rank, local_rank, world, dist):
         torch.cuda.current_stream().cuda_stream), "decode"), DECODE_KERNELS)
     if len(k_dec) == 1:                     # batch-1 decode of this shape is one fused kernel
         k_dec = {DECODE_FUSED[0]: next(iter(k_dec.values()))}
-    # a multi-row decode call (4 rows, the grouped path): where its time goes
+    # a multi-row decode call (4 rows): where its time goes (one fused kernel per
+    # row, or the grouped path's kernels)
+    names4 = ([f"decode_fused_row{i}" for i in range(4)]
+              if mw.decode_path(layers[1], 4) == mw.MOE_W4_PATH_FUSED_ROWS else PREFILL_KERNELS)
     k_dec4 = {} if args.no_multirow else traced(lambda: mw._check(mw.moe_w4_forward_decode(
         ctypes.byref(layers[1].c), 4, xdec[:4].data_ptr(), outdec[:4].data_ptr(), ws.data_ptr(), ws.numel(),
-        torch.cuda.current_stream().cuda_stream), "decode T=4"), PREFILL_KERNELS)
+        torch.cuda.current_stream().cuda_stream), "decode T=4"), names4)
 
     # weight-format variants (8-bit affine codes, FP8 E4M3 codes): layers of the
     # same shape with one-byte codes; a 4096-row prefill chunk and batch-1
@@ -724,8 +744,9 @@ def main():
                                            "bytes_per_call": decode_bytes_rows(c, Tm, dx),
                                            "hbm_gbs": decode_bytes_rows(c, Tm, dx) / t / 1e9,
                                            "frac_of_hbm": decode_bytes_rows(c, Tm, dx) / t / 1e9 / pk["hbm_gbs"],
-                                           "path": "grouped tensor-core path (one read per selected expert)"}
-                                for Tm, (t, dx) in r["small"].items()},
+                                           "path": MULTIROW_PATHS[p],
+                                           "other_path_us_per_call": None if ta is None else 1e6 * ta}
+                                for Tm, (t, dx, p, ta) in r["small"].items()},
             "format_variants": {v: variant_summary(c, w, chunk, world, pk) for v, w in r["variants"].items()},
             "roofline": roof,
             "kernels_us": {"prefill_4096": {k: 1e6 * v for k, v in r["k_pre"].items()},

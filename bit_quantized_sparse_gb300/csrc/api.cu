@@ -56,6 +56,16 @@ static void read_tile_env() {
     if (set_tile(bn, du) != MOE_W4_OK) std::fprintf(stderr, "moe_w4: MOE_W4_FORCE_TILE=%s ignored\n", v);
 }
 
+// Decode calls of up to this many rows run row by row through the fused
+// batch-1 kernel, when it covers the layer; larger calls take the grouped path.
+// The crossover, measured on the benchmark's layer (H=2048, E=256, top-8,
+// I=512; CUDA-graph replays over 16 distinct layers, us per call):
+//   rows           2    3    4    5    6    7    8
+//   row by row    25   37   49   61   73   85   97
+//   grouped       56   60   61   62   69   74   82
+static std::atomic<int> g_fused_rows{kDecodeFusedRows};
+int decode_fused_rows_max() { return g_fused_rows.load(); }
+
 TileCfg tile_cfg(const moe_w4_layer& L, int T) {
     std::call_once(g_tile_env_once, read_tile_env);
     TileCfg c{kBN, (int64_t)T * L.top_k >= 64 * (int64_t)L.E ? down_blocks_per_unit(L.I) : 1};
@@ -245,6 +255,21 @@ int moe_w4_set_tile_override(int bn, int du) {
     return set_tile(bn, du);
 }
 
+int moe_w4_set_decode_fused_rows(int max_rows) {
+    if (max_rows < 0 || max_rows > kDecodeMaxT) return MOE_W4_ERR_INVALID;
+    g_fused_rows.store(max_rows ? max_rows : kDecodeFusedRows);
+    return MOE_W4_OK;
+}
+
+int moe_w4_decode_path(const moe_w4_layer* L, int T, int* path) {
+    int r = check_layer(L);
+    if (r) return r;
+    if (!path || T < 1) return MOE_W4_ERR_INVALID;
+    if (T > kDecodeMaxT) return MOE_W4_ERR_UNSUPPORTED;
+    *path = T <= decode_fused_rows_max() && decode_fused_supported(*L) ? MOE_W4_PATH_FUSED_ROWS : MOE_W4_PATH_GROUPED;
+    return MOE_W4_OK;
+}
+
 int moe_w4_set_trace_events(cudaEvent_t* events, int n_events) {
     if (events && n_events < 1) return MOE_W4_ERR_INVALID;
     g_trace = events;
@@ -290,11 +315,12 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, mo
     if (!aligned16(x) || !aligned16(out)) return MOE_W4_ERR_ALIGN;
     WsLayout w;
     if ((r = check_ws(*L, T, workspace, ws_bytes, &w))) return r;
-    // Several rows (or a shape the one-kernel T=1 path does not cover): the
-    // grouped path reads each selected expert once for all the rows that chose
-    // it, on the tensor cores (measured 2-5x faster than per-row GEMVs at
-    // T = 2..16).
-    if (T > 1 || !decode_fused_supported(*L)) return run_grouped(L, T, x, out, workspace, w, stream);
+    // A few rows: one fused batch-1 kernel per row (each reads its 9 experts;
+    // their latency, not their bytes, sets the time at these sizes).  More rows,
+    // or a shape that kernel does not cover: the grouped path, which reads each
+    // selected expert once for all the rows that chose it, on the tensor cores.
+    if (T > decode_fused_rows_max() || !decode_fused_supported(*L))
+        return run_grouped(L, T, x, out, workspace, w, stream);
     DecodeWs d{};
     d.part = at<float>(workspace, w.dec_part);
     d.idx = at<int32_t>(workspace, w.dec_idx);
@@ -307,16 +333,12 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, mo
     d.fused_scores = at<uint64_t>(workspace, w.dec_scores);
     d.fused_hx = at<uint64_t>(workspace, w.dec_hx);
     d.fused_hsx = at<uint64_t>(workspace, w.dec_hsx);
-    trace_mark(stream, 0);
-    if (launch_decode_fused(*L, x, out, d, stream) != cudaSuccess) {
-        // the cooperative launch was refused (the grid cannot be resident at once
-        // on this device or partition): the grouped path
-        cudaGetLastError();
-        return run_grouped(L, T, x, out, workspace, w, stream);
-    }
-    trace_kernels(1);
-    for (int i = 1; i <= 3; ++i) trace_mark(stream, i);
-    return launch_status(cudaGetLastError());
+    const int done = launch_decode_fused_rows(*L, T, x, out, d, stream);
+    if (done == T) return launch_status(cudaGetLastError());
+    // a cooperative launch was refused (the grid cannot be resident at once on
+    // this device or partition): the rows not yet enqueued take the grouped path
+    const size_t H = (size_t)L->H;
+    return run_grouped(L, T - done, x + done * H, out + done * H, workspace, w, stream);
 }
 
 // Routing, grouping and the grouped tensor-core GEMMs over T rows (the

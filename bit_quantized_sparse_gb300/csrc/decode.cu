@@ -7,7 +7,9 @@
 // gated activation; output projection fused with the routing scores and the
 // shared expert's result.)
 //
-// Three kernels on one stream, no host round trip:
+// The allocation-free entry point runs these when the fused batch-1 kernel
+// does not cover the layer (or its cooperative launch is refused).  Three
+// kernels on one stream, no host round trip:
 //   1. decode_router_kernel  partial scores over 256-row slices of W_r; the
 //      last CTA to finish (atomic ticket, no spinning) reduces them in a fixed
 //      order, selects the top-k, the softmax weights and the shared gate.
@@ -196,15 +198,12 @@ __global__ void __launch_bounds__(kDN_Warps * 32) decode_down_kernel(moe_w4_laye
 cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                           cudaStream_t st) {
     const int k = L.top_k;
-    if (T == 1 && decode_fused_supported(L)) {   // one launch for the whole layer
-        if (launch_decode_fused(L, x, out, d, st) == cudaSuccess) {
-            trace_kernels(1);
-            trace_mark(st, 1);
-            trace_mark(st, 2);
-            trace_mark(st, 3);
-            return cudaGetLastError();
-        }
-        cudaGetLastError();   // the cooperative launch was refused: the three kernels below
+    if (decode_fused_supported(L)) {   // one launch per row for the whole layer
+        const int done = launch_decode_fused_rows(L, T, x, out, d, st);
+        if (done == T) return cudaGetLastError();
+        // refused: at the first row, the three kernels below; later (the same
+        // launch went through just before), an error for the caller
+        if (done > 0) return cudaErrorLaunchFailure;
     }
     static bool attrs_set[64] = {};
     int dev = 0;

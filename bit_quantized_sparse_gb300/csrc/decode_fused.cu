@@ -1034,18 +1034,24 @@ bool decode_fused_supported(const moe_w4_layer& L) {
     return ok;
 }
 
-cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
-                                cudaStream_t st) {
+// The six code tensor maps of a layer (routed and shared gate, up, down).
+struct FusedMaps { CUtensorMap mg, mu, md, msg, msu, msd; };
+
+static bool fused_maps(const moe_w4_layer& L, FusedMaps* m) {
     const int H = L.H, E = L.E, I = L.I, k = L.top_k;
     const int RG = I / kPE, DR = H / (kPE * k), b = code_bits_of(L);
     const uint32_t hbox = H * b / 1024 / kGuParts, dbox = I * b / 1024;   // box columns per copy
-    CUtensorMap mg, mu, md, msg, msu, msd;
-    bool ok = codes_map(&mg, L.gate.codes, (uint64_t)E * I, H, RG, hbox, b) &&
-              codes_map(&mu, L.up.codes, (uint64_t)E * I, H, RG, hbox, b) &&
-              codes_map(&md, L.down.codes, (uint64_t)E * H, I, DR, dbox, b) &&
-              codes_map(&msg, L.sh_gate.codes, I, H, RG, hbox, b) && codes_map(&msu, L.sh_up.codes, I, H, RG, hbox, b) &&
-              codes_map(&msd, L.sh_down.codes, H, I, DR, dbox, b);
-    if (!ok) return cudaErrorInvalidValue;
+    return codes_map(&m->mg, L.gate.codes, (uint64_t)E * I, H, RG, hbox, b) &&
+           codes_map(&m->mu, L.up.codes, (uint64_t)E * I, H, RG, hbox, b) &&
+           codes_map(&m->md, L.down.codes, (uint64_t)E * H, I, DR, dbox, b) &&
+           codes_map(&m->msg, L.sh_gate.codes, I, H, RG, hbox, b) &&
+           codes_map(&m->msu, L.sh_up.codes, I, H, RG, hbox, b) &&
+           codes_map(&m->msd, L.sh_down.codes, H, I, DR, dbox, b);
+}
+
+// One batch-1 call: x [H] -> out [H], routing into d.idx, d.w, d.gamma.
+static cudaError_t launch_fused_row(const moe_w4_layer& L, const FusedMaps& m, const uint16_t* x, uint16_t* out,
+                                    const DecodeWs& d, cudaStream_t st) {
     FusedArgs a{};
     a.x = x; a.router_w = L.router_w; a.router_bias = L.router_bias; a.shared_gate = L.shared_gate;
     a.gs = L.gate.scales; a.gb = L.gate.biases; a.us = L.up.scales; a.ub = L.up.biases;
@@ -1055,17 +1061,52 @@ cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16
     a.scores = d.fused_scores; a.hx = d.fused_hx; a.hsx = d.fused_hsx;
     a.idx_out = d.idx; a.w_out = d.w; a.gamma_out = d.gamma; a.out = out;
     a.ctrl = d.ctrl;
-    a.H = H; a.E = E; a.I = I; a.k = k;
+    a.H = L.H; a.E = L.E; a.I = L.I; a.k = L.top_k;
     cudaLaunchAttribute attr[2];
     const FusedKernel kern = fused_kernel_for(L);   // shared memory opt-in set by the support check
     cudaLaunchConfig_t cfg = fused_config(L, attr, st, true);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, mg, mu, md, msg, msu, msd);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, m.mg, m.mu, m.md, m.msg, m.msu, m.msd);
     if (e != cudaSuccess) {   // refused with programmatic dependent launch: cooperative alone
         cudaGetLastError();
         cfg = fused_config(L, attr, st, false);
-        e = cudaLaunchKernelEx(&cfg, kern, a, mg, mu, md, msg, msu, msd);
+        e = cudaLaunchKernelEx(&cfg, kern, a, m.mg, m.mu, m.md, m.msg, m.msu, m.msd);
     }
     return e;
+}
+
+cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
+                                cudaStream_t st) {
+    FusedMaps m;
+    if (!fused_maps(L, &m)) return cudaErrorInvalidValue;
+    return launch_fused_row(L, m, x, out, d, st);
+}
+
+// Rows 0..T-1 one after another, each a complete batch-1 call on the stream
+// (row t's routing at d.idx + t*k, d.w + t*k, d.gamma + t).  Consecutive calls
+// overlap only through programmatic dependent launch, so each row still sees
+// the exchange buffers as the previous row left them.  Returns the rows
+// launched: fewer than T when a launch was refused or the tensor maps could
+// not be built (0 then means nothing was launched).  Trace events: one before
+// each row, then the rest after the last.
+int launch_decode_fused_rows(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
+                             cudaStream_t st) {
+    FusedMaps m;
+    if (!fused_maps(L, &m)) return 0;
+    const size_t k = (size_t)L.top_k, H = (size_t)L.H;
+    for (int t = 0; t < T; ++t) {
+        DecodeWs dt = d;
+        dt.idx = d.idx + t * k;
+        dt.w = d.w + t * k;
+        dt.gamma = d.gamma + t;
+        trace_mark(st, t);
+        if (launch_fused_row(L, m, x + t * H, out + t * H, dt, st) != cudaSuccess) {
+            cudaGetLastError();
+            return t;
+        }
+    }
+    trace_kernels(T);
+    for (int i = T; i < T + 4; ++i) trace_mark(st, i);
+    return T;
 }
 
 // Sizes of the fused kernel's exchange buffers (tagged 8-byte words) for a layer.

@@ -193,6 +193,8 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
     constexpr uint32_t kCodesBytes = GG::kCodesBytes;
     constexpr int kCodeWords = kGK * BITS / 32;   // code words per row per step
     constexpr int NMAT = GG::NMAT, SC = GG::SC, SB = GG::SB, SA = GG::SA;
+    griddep_wait();               // programmatic dependent launch: nothing is touched before the
+    griddep_launch_dependents();  // previous kernel has completed; the next one may be scheduled
     const int ntiles = checked_index(a.ntiles[0], 0, a.max_blocks * a.M + 1, a.status);
     const int G = a.K / kGroup, nK = a.K / kGK;
 
@@ -573,6 +575,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
                                                           uint16_t* __restrict__ xg, int nrows, int H, int k,
                                                           unsigned int* status) {
     const int p = blockIdx.x * 8 + threadIdx.x / 32, lane = threadIdx.x % 32;
+    griddep_wait();               // programmatic dependent launch: nothing is touched before the
+    griddep_launch_dependents();  // previous kernel has completed; the next one may be scheduled
     if (p >= nrows) return;
     const int t = checked_index(__ldg(perm + p), 0, nrows, status) / k;
     const uint4* src = reinterpret_cast<const uint4*>(x16 + (size_t)t * H);
@@ -596,6 +600,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       int T, int H, int k, unsigned int* status) {
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int per_row = H / 8;
+    griddep_wait();               // programmatic dependent launch: nothing is touched before the
+    griddep_launch_dependents();  // previous kernel has completed; the next one may be scheduled
     if (i >= (size_t)T * per_row) return;
     const int t = (int)(i / per_row), c = (int)(i % per_row) * 8;
     // all k + 1 rows requested before the first is added (k <= 8), then added in order
@@ -662,7 +668,7 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const
 template <bool DUAL, int BITS, bool E4M3>
 static cudaError_t launch_gemm(const GemmArgs& g, int grid, const CUtensorMap& m0r, const CUtensorMap& m1r,
                                const CUtensorMap& m0s, const CUtensorMap& m1s, const CUtensorMap& mb,
-                               const CUtensorMap& mbs, cudaStream_t st) {
+                               const CUtensorMap& mbs, cudaStream_t st, bool pdl) {
     using GG = Geo<DUAL, BITS>;
     static bool set[64] = {};
     int dev = 0;
@@ -674,9 +680,8 @@ static cudaError_t launch_gemm(const GemmArgs& g, int grid, const CUtensorMap& m
         if (e != cudaSuccess) return e;
         set[dev] = true;
     }
-    grouped_w4_gemm_kernel<DUAL, BITS, E4M3><<<grid, GG::kThreads, GG::bytes(), st>>>(g, m0r, m1r, m0s, m1s, mb,
-                                                                                     mbs);
-    return cudaGetLastError();
+    return launch_pdl(pdl, grouped_w4_gemm_kernel<DUAL, BITS, E4M3>, dim3(grid), dim3(GG::kThreads), GG::bytes(), st, g, m0r,
+                      m1r, m0s, m1s, mb, mbs);
 }
 
 cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const PrefillWs& p,
@@ -737,12 +742,14 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     // persistent: one CTA per SM (never more CTAs than the largest tile count)
     const int grid_gu = p.max_tiles_gu < nsm ? p.max_tiles_gu : nsm;
     const int nrg = T * k;
-    gather_rows_kernel<<<(unsigned)((nrg + 7) / 8), 256, 0, st>>>(p.x16, p.perm, p.xg, nrg, H, k, p.status);
+    cudaError_t e = launch_pdl(pdl_for(T), gather_rows_kernel, dim3((unsigned)((nrg + 7) / 8)), dim3(256), 0, st, p.x16, p.perm,
+                               p.xg, nrg, H, k, p.status);
+    if (e != cudaSuccess) return e;
     trace_mark(st, 4);
-    cudaError_t e = w16   ? launch_gemm<true, 16, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
-                  : e4m3  ? launch_gemm<true, 8, true>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
-                  : bits == 8 ? launch_gemm<true, 8, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st)
-                              : launch_gemm<true, 4, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st);
+    e = w16   ? launch_gemm<true, 16, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st, pdl_for(T))
+                  : e4m3  ? launch_gemm<true, 8, true>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st, pdl_for(T))
+                  : bits == 8 ? launch_gemm<true, 8, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st, pdl_for(T))
+                              : launch_gemm<true, 4, false>(a, grid_gu, mg, mu, msg, msu, mxg, mx, st, pdl_for(T));
     if (e != cudaSuccess) return e;
     trace_mark(st, 5);
 
@@ -753,15 +760,17 @@ cudaError_t launch_grouped_ffn(const moe_w4_layer& L, int T, const uint16_t* x, 
     b.s0s = L.sh_down.scales; b.b0s = L.sh_down.biases; b.s1s = nullptr; b.b1s = nullptr;
     b.out = p.ys; b.K = I; b.rows_e = H; b.out_cols = H;
     const int grid_dn = p.max_tiles_dn < nsm ? p.max_tiles_dn : nsm;
-    e = w16   ? launch_gemm<false, 16, false>(b, grid_dn, md, md, msd, msd, mh, mh, st)
-      : e4m3  ? launch_gemm<false, 8, true>(b, grid_dn, md, md, msd, msd, mh, mh, st)
-      : bits == 8 ? launch_gemm<false, 8, false>(b, grid_dn, md, md, msd, msd, mh, mh, st)
-                  : launch_gemm<false, 4, false>(b, grid_dn, md, md, msd, msd, mh, mh, st);
+    e = w16   ? launch_gemm<false, 16, false>(b, grid_dn, md, md, msd, msd, mh, mh, st, pdl_for(T))
+      : e4m3  ? launch_gemm<false, 8, true>(b, grid_dn, md, md, msd, msd, mh, mh, st, pdl_for(T))
+      : bits == 8 ? launch_gemm<false, 8, false>(b, grid_dn, md, md, msd, msd, mh, mh, st, pdl_for(T))
+                  : launch_gemm<false, 4, false>(b, grid_dn, md, md, msd, msd, mh, mh, st, pdl_for(T));
     if (e != cudaSuccess) return e;
     trace_mark(st, 6);
 
     const size_t nthr = (size_t)T * (H / 8);
-    combine_kernel<<<(unsigned)((nthr + 255) / 256), 256, 0, st>>>(p.ys, p.inv, out, T, H, k, p.status);
+    e = launch_pdl(pdl_for(T), combine_kernel, dim3((unsigned)((nthr + 255) / 256)), dim3(256), 0, st, p.ys, p.inv, out, T, H, k,
+                   p.status);
+    if (e != cudaSuccess) return e;
     trace_mark(st, 7);
     return cudaGetLastError();
 }

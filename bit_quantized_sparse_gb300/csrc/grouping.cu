@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kChunk) group_kernel(const int32_t* __restrict
                                                        int4* __restrict__ blkinfo, int4* __restrict__ unitinfo,
                                                        int32_t* __restrict__ ntiles, int MI, int MH, int R, int BN,
                                                        unsigned int* status) {
+    griddep_wait();               // programmatic dependent launch: nothing is touched before the
+    griddep_launch_dependents();  // previous kernel has completed; the next one may be scheduled
     extern __shared__ int sm_group[];
     int* off = sm_group;                     // [E+1] totals, then their exclusive scan
     int* start = off + (E + 1);              // [E] this chunk's start inside each group
@@ -233,9 +235,10 @@ cudaError_t launch_grouping(const moe_w4_layer& L, int T, const RouteOut& o, cud
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    group_kernel<<<nchunk, kChunk, sm, st>>>(o.topk_idx, T, E, k, nchunk, o.chunk_base, o.counts, o.offsets, o.perm,
-                                             o.inv, o.blkinfo, o.unitinfo, o.ntiles, L.I / kBM, L.H / kBM, tc.du,
-                                             tc.bn, o.status);
+    const cudaError_t e = launch_pdl(pdl_for(T), group_kernel, dim3(nchunk), dim3(kChunk), sm, st, o.topk_idx, T, E, k, nchunk,
+                                     o.chunk_base, o.counts, o.offsets, o.perm, o.inv, o.blkinfo, o.unitinfo, o.ntiles,
+                                     L.I / kBM, L.H / kBM, tc.du, tc.bn, o.status);
+    if (e != cudaSuccess) return e;
     trace_mark(st, 3);
     return cudaGetLastError();
 }

@@ -10,12 +10,46 @@
 
 namespace mw4 {
 
+// Launch with programmatic dependent launch allowed when `pdl` is set: the
+// kernel may be scheduled while the previous kernel on the stream finishes, so
+// it must call griddep_wait() before it touches any memory (every kernel
+// launched this way does so first; without the attribute that wait returns at
+// once).  A refused attribute falls back to a plain launch.
+template <typename... P, typename... A>
+cudaError_t launch_pdl(bool pdl, void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       const A&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess && pdl) {
+        cudaGetLastError();
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelEx(&cfg, kern, args...);
+    }
+    return e;
+}
+
 constexpr int kGroup = 64;        // weights per scale/bias group
 constexpr int kChunk = 128;       // tokens per grouping chunk
 constexpr int kBM = 128;          // weight rows per tensor-core tile
 constexpr int kBN = 128;          // token rows per tensor-core tile
 constexpr int kBK = 64;           // reduction columns per pipeline stage (= one group)
 constexpr int kDecodeMaxT = 16;   // largest decode batch
+// Calls of at most this many rows chain their kernels with programmatic
+// dependent launch (measured on H=2048, E=256, top-8, I=512: 8 rows 85.9 ->
+// 81.8 us per call; a 4096-row chunk 0.386 -> 0.396 ms, so larger calls launch
+// plainly).
+constexpr int kPdlMaxT = 16;
+inline bool pdl_for(int T) { return T <= kPdlMaxT; }
+constexpr int kDecodeFusedRows = 5;   // default: decode calls of up to 5 rows run row by row (fused kernel)
 constexpr int kRouterRowsPerCta = 256;  // H rows per decode-router CTA
 constexpr int kRouterSplit = 2;         // prefill router: partial score arrays (halves of H)
 // Width of one weight code: 4 (also for code_bits = 0) or 8.
@@ -117,11 +151,22 @@ bool decode_fused_supported(const moe_w4_layer& L);
 // was refused and nothing was enqueued (the caller takes another path).
 cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                                 cudaStream_t st);
+// T rows as T consecutive launches of that kernel (row t's routing at
+// d.idx + t*k, d.w + t*k, d.gamma + t); returns the rows launched, fewer than
+// T only when a launch was refused (nothing enqueued for the rest).
+int launch_decode_fused_rows(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
+                             cudaStream_t st);
+// Decode calls of at most this many rows run row by row through the fused
+// kernel when it covers the layer (moe_w4_set_decode_fused_rows overrides it).
+int decode_fused_rows_max();
 // Bytes of the fused kernel's exchange buffers for a layer: router score
 // partials (replicated), h, and the sums of h's 32-value pieces.
 size_t fused_scores_bytes(const moe_w4_layer& L);
 size_t fused_hx_bytes(const moe_w4_layer& L);
 size_t fused_hsx_bytes(const moe_w4_layer& L);
+// The allocation-free decode: row by row through the fused kernel when it
+// covers the layer, else (or when its first launch is refused) the three
+// CUDA-core kernels of decode.cu.
 cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                           cudaStream_t st);
 

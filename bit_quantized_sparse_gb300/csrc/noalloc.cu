@@ -96,9 +96,9 @@ extern "C" int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const
     if (T < 0) return MOE_W4_ERR_INVALID;
     if (T > kDecodeMaxT) return MOE_W4_ERR_UNSUPPORTED;
     if (T == 0) return MOE_W4_OK;
-    // one-byte codes: only the one-kernel batch-1 decode (the per-row GEMVs of
-    // T >= 2 unpack nibbles)
-    if (code_bits_of(*L) == 8 && !(T == 1 && decode_fused_supported(*L))) return MOE_W4_ERR_UNSUPPORTED;
+    // one-byte codes: only the one-kernel batch-1 decode, row by row (the
+    // CUDA-core GEMVs of the fallback unpack nibbles)
+    if (code_bits_of(*L) == 8 && !decode_fused_supported(*L)) return MOE_W4_ERR_UNSUPPORTED;
     if (!x || !out || !L->router_w || !L->shared_gate) return MOE_W4_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 15) return MOE_W4_ERR_ALIGN;
     const moe_w4_mat* ms[6] = {&L->gate, &L->up, &L->down, &L->sh_gate, &L->sh_up, &L->sh_down};

@@ -75,6 +75,8 @@ router_tc_kernel(const __grid_constant__ RouterTcArgs a, const __grid_constant__
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1) + 1;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kRtBN, kh = blockIdx.z;
+    griddep_wait();               // programmatic dependent launch: nothing is touched before the
+    griddep_launch_dependents();  // previous kernel has completed; the next one may be scheduled
     if (a.hist) {   // every CTA zeroes its share of the histogram
         const int nblk = gridDim.x * gridDim.y * gridDim.z;
         const int b = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
@@ -173,6 +175,8 @@ __global__ void __launch_bounds__(kTopkWarps * 32, NIT <= 8 ? 4 : 2) topk_kernel
     float* sc_all = sm_topk + H;            // [kTopkWarps][E] scores
     uint16_t* xs_all = reinterpret_cast<uint16_t*>(sc_all + kTopkWarps * E);   // [kTopkWarps][H] rows of x
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    griddep_wait();               // programmatic dependent launch: nothing is touched before the
+    griddep_launch_dependents();  // previous kernel has completed; the next one may be scheduled
     for (int i = threadIdx.x; i < H / 4; i += blockDim.x)
         reinterpret_cast<float4*>(gs)[i] = reinterpret_cast<const float4*>(g)[i];
     __syncthreads();
@@ -326,26 +330,20 @@ cudaError_t launch_router_prefill(const moe_w4_layer& L, int T, const uint16_t* 
         // the grouping's per-chunk histogram, zeroed by this kernel, counted by the top-k kernel
         RouterTcArgs ra_args{L.router_bias, o.logits, T, L.H, L.E, o.chunk_base,
                              ((T + kChunk - 1) / kChunk) * L.E, o.status};
-        router_tc_kernel<<<dim3(Epad / kBM, (T + kRtBN - 1) / kRtBN, kRtSplit), 256, router_tc_smem(), st>>>(ra_args, mA,
-                                                                                                           mX);
+        const cudaError_t e = launch_pdl(pdl_for(T), router_tc_kernel, dim3(Epad / kBM, (T + kRtBN - 1) / kRtBN, kRtSplit),
+                                         dim3(256), router_tc_smem(), st, ra_args, mA, mX);
+        if (e != cudaSuccess) return e;
     }
     trace_mark(st, 1);
     const int nsplit = kRtSplit;
     const size_t sm = topk_smem(L.H, L.E);
     const dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(kTopkWarps * 32);
     const int nit = (L.H + 255) / 256;   // H <= 4096
-    if (nit <= 2)
-        topk_kernel<2><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                o.gamma, o.x16, code_bits_of(L), o.chunk_base, o.status);
-    else if (nit <= 4)
-        topk_kernel<4><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                o.gamma, o.x16, code_bits_of(L), o.chunk_base, o.status);
-    else if (nit <= 8)
-        topk_kernel<8><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                o.gamma, o.x16, code_bits_of(L), o.chunk_base, o.status);
-    else
-        topk_kernel<16><<<grid, block, sm, st>>>(o.logits, nsplit, x, L.shared_gate, T, L.H, L.E, L.top_k, o.topk_idx, o.topk_w,
-                                                 o.gamma, o.x16, code_bits_of(L), o.chunk_base, o.status);
+    auto topk = nit <= 2 ? topk_kernel<2> : nit <= 4 ? topk_kernel<4> : nit <= 8 ? topk_kernel<8> : topk_kernel<16>;
+    const cudaError_t e = launch_pdl(pdl_for(T), topk, grid, block, sm, st, o.logits, nsplit, x, L.shared_gate, T, L.H, L.E,
+                                     L.top_k, o.topk_idx, o.topk_w, o.gamma, o.x16, code_bits_of(L), o.chunk_base,
+                                     o.status);
+    if (e != cudaSuccess) return e;
     trace_mark(st, 2);
     return cudaGetLastError();
 }

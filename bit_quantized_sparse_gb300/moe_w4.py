@@ -50,6 +50,8 @@ MOE_W4_STATUS_WAIT_TIMEOUT = 1
 MOE_W4_STATUS_BAD_INDEX = 2
 MOE_W4_STATUS_FP16_RANGE = 4
 DECODE_MAX_T = 16
+MOE_W4_PATH_FUSED_ROWS = 1           # moe_w4_decode_path
+MOE_W4_PATH_GROUPED = 2
 
 
 class MoeW4Mat(ctypes.Structure):
@@ -80,6 +82,8 @@ _SIGS = {
     "moe_w4_ablation_scratch_bytes": (c_size_t, [_P, c_int]),
     "moe_w4_set_trace_events": (c_int, [c_void_p, c_int]),
     "moe_w4_set_tile_override": (c_int, [c_int, c_int]),
+    "moe_w4_set_decode_fused_rows": (c_int, [c_int]),
+    "moe_w4_decode_path": (c_int, [_P, c_int, ctypes.POINTER(c_int)]),
     "moe_w4_last_traced_kernels": (c_int, []),
     "moe_w4_forward_decode_noalloc": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_w4_noalloc_status": (c_int, [c_void_p, c_void_p]),
@@ -107,6 +111,8 @@ moe_w4_ablation_prefill = _lib.moe_w4_ablation_prefill
 moe_w4_ablation_scratch_bytes = _lib.moe_w4_ablation_scratch_bytes
 moe_w4_set_trace_events = _lib.moe_w4_set_trace_events
 moe_w4_set_tile_override = _lib.moe_w4_set_tile_override
+moe_w4_set_decode_fused_rows = _lib.moe_w4_set_decode_fused_rows
+moe_w4_decode_path = _lib.moe_w4_decode_path
 moe_w4_last_traced_kernels = _lib.moe_w4_last_traced_kernels
 moe_w4_forward_decode_noalloc = _lib.moe_w4_forward_decode_noalloc
 moe_w4_noalloc_status = _lib.moe_w4_noalloc_status
@@ -250,6 +256,13 @@ def forward_decode(layer: DeviceLayer, x, out=None, stream=None):
     _check(moe_w4_forward_decode(ctypes.byref(layer.c), T, _ptr(x), _ptr(out), ws.data_ptr(), ws.numel(),
                                  _stream(stream)), "moe_w4_forward_decode")
     return out
+
+
+def decode_path(layer: DeviceLayer, T: int) -> int:
+    """MOE_W4_PATH_FUSED_ROWS or MOE_W4_PATH_GROUPED: the path moe_w4_forward_decode takes for T rows."""
+    p = c_int(0)
+    _check(moe_w4_decode_path(ctypes.byref(layer.c), int(T), ctypes.byref(p)), "moe_w4_decode_path")
+    return p.value
 
 
 def forward_prefill(layer: DeviceLayer, x, out=None, stream=None, ws=None):

@@ -75,10 +75,10 @@ typedef struct {
  * s * q + b with q the unsigned code and s, b the bf16 scale and bias of its
  * group of 64 columns.  8-bit layers (either code_format below) take the
  * one-kernel batch-1 decode only for H = 2048, I = 512, E = 256, top_k = 8
- * (the grouped tensor-core path
- * otherwise, and for every T >= 2); moe_w4_forward_decode_noalloc takes them
- * only where that one-kernel path applies (T = 1, that shape) and returns
- * MOE_W4_ERR_UNSUPPORTED otherwise.
+ * (the grouped tensor-core path otherwise, and for decode calls of more rows
+ * than moe_w4_set_decode_fused_rows); moe_w4_forward_decode_noalloc takes
+ * them only where that one-kernel path applies (that shape, any T) and
+ * returns MOE_W4_ERR_UNSUPPORTED otherwise.
  * code_format selects how a code is read (MOE_W4_CODES_*): unsigned integer
  * codes as above, or FP8 E4M3 codes (code_bits must be 8; same byte layout),
  * where a weight is s * v(q) + b with v(q) the E4M3 value of the byte: sign
@@ -104,8 +104,8 @@ typedef struct {
     const void* router_prep;   /* the router weights as moe_w4_prepare_router
                                   writes them (moe_w4_router_prep_bytes bytes,
                                   16-byte aligned), or NULL: the routing of
-                                  every call with T >= 2 then prepares them in
-                                  its workspace first.  Must be rewritten after
+                                  every call on the grouped path then prepares
+                                  them in its workspace first.  Must be rewritten after
                                   router_w changes.                            */
 } moe_w4_layer;
 
@@ -128,7 +128,7 @@ enum {
 };
 
 /* The router weights prepared once per layer for the tensor-core scores of
- * the routing (prefill, and decode calls with T >= 2): W_r (fp32 [H][E]) split
+ * the routing (prefill, and decode calls on the grouped path): W_r (fp32 [H][E]) split
  * exactly into three bf16 terms per weight, hi + mid + lo, stored transposed,
  * [ceil(E/128)*128][3H] bf16, rows past E zero.  The scores are unchanged by
  * the preparation; it only saves the split on every call.
@@ -163,8 +163,10 @@ size_t moe_w4_status_offset(void);
                                           (|v| > 65504): output not valid */
 /* Value ranges.  The tensor-core paths hold activations (x), the weighted
  * SwiGLU output h, each expert's weighted output and the rebuilt weights
- * s * q + b (prefill and multi-row decode) in fp16; batch-1 decode holds x and h
- * in fp16 (with 4-bit codes half of their entries divided by 16) and applies s
+ * s * q + b (prefill and decode on the grouped path) in fp16; the one-kernel
+ * batch-1 decode (also used row by row for small decode calls) holds x and h
+ * in fp16 (with 4-bit codes half of their entries divided by 16, so x should
+ * stay above about 1e-3 in magnitude for full precision there) and applies s
  * and b in fp32.  Inputs must therefore keep these within
  * the fp16 range: |x| <= 65504; per group |s| * qmax + |b| <= 65504 (qmax = 15
  * for 4-bit codes, 255 for 8-bit codes, 448 for E4M3); h and the expert outputs
@@ -193,19 +195,40 @@ int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
                  void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* Layer output for a decode batch, 1 <= T <= 16 (section "Optimise the
- * single-row weight path").  T = 1: one cooperative kernel for the whole layer
- * (router, W4 GEMVs for gate/up + SwiGLU and for down weighted by the routing
- * scores, plus the gated shared expert); its CTAs exchange router scores and h
- * through the workspace with bounded waits.  T >= 2, a shape that kernel does
- * not cover, or a device that refuses its cooperative launch: the grouped path
- * of moe_w4_forward_prefill, which reads each selected expert once for all
- * rows that chose it.  out bf16 [T][H].  The one-kernel path reads the
- * weights, router and shared gate before it waits for the kernel that precedes
- * it on the stream (programmatic dependent launch): they must not be written
- * by that kernel. */
+ * single-row weight path").  One row: one cooperative kernel for the whole
+ * layer (router, W4 GEMVs for gate/up + SwiGLU and for down weighted by the
+ * routing scores, plus the gated shared expert); its CTAs exchange router
+ * scores and h through the workspace with bounded waits.  Up to
+ * moe_w4_set_decode_fused_rows rows (5 by default): that kernel once per row,
+ * in row order.  More rows, a shape that kernel does not cover, or a device
+ * that refuses its cooperative launch: the grouped path of
+ * moe_w4_forward_prefill, which reads each selected expert once for all rows
+ * that chose it (moe_w4_decode_path tells which path a call takes).  out bf16
+ * [T][H].  The one-kernel path reads the weights, router and shared gate
+ * before it waits for the kernel that precedes it on the stream (programmatic
+ * dependent launch): they must not be written by that kernel. */
 int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
                           moe_w4_bf16* out, void* workspace, size_t ws_bytes,
                           cudaStream_t stream);
+
+/* The path moe_w4_forward_decode takes for T rows of layer L, into *path:
+ * MOE_W4_PATH_FUSED_ROWS (the one-kernel batch-1 decode, once per row) or
+ * MOE_W4_PATH_GROUPED (routing, grouping and grouped GEMMs; a refused
+ * cooperative launch also ends there).  Host query on the current device.
+ * Returns MOE_W4_ERR_INVALID (invalid layer, NULL path, T < 1),
+ * MOE_W4_ERR_UNSUPPORTED (T > 16) or the layer checks' codes. */
+#define MOE_W4_PATH_FUSED_ROWS 1
+#define MOE_W4_PATH_GROUPED    2
+int moe_w4_decode_path(const moe_w4_layer* L, int T, int* path);
+
+/* Largest decode call (rows) that runs row by row through the one-kernel
+ * batch-1 path, 1..16; 0 restores the default, 5 (measured on H=2048, E=256,
+ * top-8, I=512: about 12.3 us per row back to back; the grouped path takes
+ * 56, 61, 62 and 69 us at 2, 4, 5 and 6 rows).  1 keeps only single rows
+ * there.
+ * Process-wide; takes effect for calls enqueued afterwards.  Returns
+ * MOE_W4_ERR_INVALID outside 0..16. */
+int moe_w4_set_decode_fused_rows(int max_rows);
 
 /* Layer output for a prefill batch, T >= 1 (section "Dequantise weights
  * during matrix multiplication"): routing as moe_w4_route, then grouped W4
@@ -225,10 +248,12 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
  * device memory, a real-time loop that must not wait on an allocator, a
  * memory plan fixed before the layer's shape is known).  The pages have no
  * counterpart: it is a deployment convenience of this library.
- * Same arguments as moe_w4_forward_decode, minus the workspace, and the same
- * one-kernel path at T = 1; at T >= 2 it runs per-row CUDA-core GEMVs
- * (router, gate/up, down kernels) instead of the grouped path, whose buffers
- * would not fit, with results within the same tolerance of the oracle.  The
+ * Same arguments as moe_w4_forward_decode, minus the workspace.  Where the
+ * one-kernel batch-1 path covers the layer it runs that kernel once per row,
+ * for every T (the grouped path's buffers would not fit); elsewhere, or when
+ * its cooperative launch is refused, per-row CUDA-core GEMVs (router, gate/up,
+ * down kernels; 4-bit codes only), with results within the same tolerance of
+ * the oracle.  The
  * scratch lives in one fixed device array of
  * MOE_W4_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library keeps until the process exits.
@@ -239,7 +264,7 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
  *     that device current) and caches it; make that first call before any
  *     stream capture.
  *   - Every call reuses the same array and clears its control header first
- *     (except the T = 1 kernel's call counter);
+ *     (except the one-kernel path's call counter);
  *     calls that overlap on the GPU (other streams, other threads) race and
  *     give wrong results: serialise them.
  *   - It never calls cudaMalloc, cudaFree or any allocating routine. */
@@ -257,8 +282,9 @@ int moe_w4_forward_decode_noalloc(const moe_w4_layer* L, int T, const moe_w4_bf1
 int moe_w4_noalloc_status(unsigned int* status, cudaStream_t stream);
 
 /* Failure-detection test hook for moe_w4_forward_decode_noalloc (no
- * production use; process-wide).  on != 0: the following one-kernel batch-1
- * calls have one CTA skip publishing its router scores, so the other CTAs'
+ * production use; process-wide).  on != 0: in the following calls every
+ * launch of the one-kernel batch-1 path (one per row) has one CTA skip
+ * publishing its router scores, so the other CTAs'
  * bounded waits run out (after about 2 s): the call completes, its output is
  * not valid, and the status word (moe_w4_noalloc_status) gets
  * MOE_W4_STATUS_WAIT_TIMEOUT.  The aborting CTAs advance the call counter, so
@@ -269,13 +295,13 @@ int moe_w4_noalloc_test_skip_publish(int on);
 /* Optional tracing for benchmarks: while set, every forward call records
  * events[0..n_events) (cudaEvent_t, created by the caller) on its stream:
  * event 0 before its first kernel and event i after its i-th kernel, so
- * consecutive events bracket one kernel each (prefill: 9 kernels -- router
- * scores, top-k, chunk counts, scan, assign, row gather, grouped gate/up GEMM,
- * grouped down GEMM, combine; decode of several rows: the same 9; three-kernel
- * decode: router, gate/up GEMV, down GEMV).  Extra
- * kernels beyond n_events-1 are not traced; a call that launches fewer
- * kernels records its remaining events right after its last kernel (batch-1
- * decode of the supported shapes is one fused kernel).  Events are recorded with
+ * consecutive events bracket one kernel each (prefill: 7 kernels -- router
+ * scores, top-k, grouping, row gather, grouped gate/up GEMM, grouped down
+ * GEMM, combine; decode on the grouped path: the same 7; decode row by row:
+ * one fused kernel per row; three-kernel decode: router, gate/up GEMV, down
+ * GEMV).  Extra kernels beyond n_events-1 are not traced; a call that
+ * launches fewer kernels records its remaining events right after its last
+ * kernel.  Events are recorded with
  * cudaEventRecordExternal, so they also fire inside a captured CUDA graph.
  * Pass NULL to stop tracing.  Process-wide setting, not thread-safe. */
 int moe_w4_set_trace_events(cudaEvent_t* events, int n_events);

@@ -81,11 +81,28 @@ def test_bad_shapes_rejected(mw, field, val, code):
 def test_noalloc_code_formats_rejected(mw, bits, fmt, T):
     """The allocation-free decode refuses code formats it has no kernels for
     (host checks only, before any device work): unknown widths or formats,
-    E4M3 with 4-bit codes, and one-byte codes at T >= 2."""
-    L = _layer(mw)
+    E4M3 with 4-bit codes, and one-byte codes on a shape the one-kernel path
+    does not cover (H=1024, E=128, I=256, top-4), at any T."""
+    L = _layer(mw, H=1024, E=128, I=256, k=4)
     L.code_bits, L.code_format = bits, fmt
     ws = 1 << 12
     assert mw.moe_w4_forward_decode_noalloc(ctypes.byref(L), T, ws, ws, None) == mw.MOE_W4_ERR_UNSUPPORTED
+
+
+def test_decode_path_query(mw):
+    """moe_w4_decode_path (a host query, no device work): argument checks, and
+    a valid call names one of the two paths.  The row limit accepts 0..16."""
+    L = _layer(mw)
+    p = ctypes.c_int(-1)
+    assert mw.moe_w4_decode_path(None, 2, ctypes.byref(p)) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_decode_path(ctypes.byref(L), 2, None) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_decode_path(ctypes.byref(L), 0, ctypes.byref(p)) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_decode_path(ctypes.byref(L), 17, ctypes.byref(p)) == mw.MOE_W4_ERR_UNSUPPORTED
+    assert mw.moe_w4_decode_path(ctypes.byref(L), 2, ctypes.byref(p)) == mw.MOE_W4_OK
+    assert p.value in (mw.MOE_W4_PATH_FUSED_ROWS, mw.MOE_W4_PATH_GROUPED)
+    assert mw.moe_w4_set_decode_fused_rows(-1) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_set_decode_fused_rows(17) == mw.MOE_W4_ERR_INVALID
+    assert mw.moe_w4_set_decode_fused_rows(0) == mw.MOE_W4_OK
 
 
 def test_bad_arguments_rejected(mw):

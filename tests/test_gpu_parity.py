@@ -293,10 +293,11 @@ def _traced_decode(mw, torch, dl, x_rows):
 @pytest.mark.parametrize("name", ["w8_tiny_T4", "w8_T512", "e4m3_tiny_T4", "e4m3_T512"])
 def test_w8_layer(mw, torch, name):
     """The one-byte weight-format variants (four codes per word; unsigned
-    8-bit affine codes or FP8 E4M3 codes): routing, prefill and decode (1 row
-    on the one-kernel path for the full-size layer, 4 rows on the grouped path)
-    against the oracle; the allocation-free decode runs the one-kernel path at
-    T = 1 and declines T >= 2."""
+    8-bit affine codes or FP8 E4M3 codes): routing, prefill and decode (1 and 4
+    rows: the one-kernel path, once per row, for the full-size layer; the
+    grouped path for the tiny one) against the oracle; the allocation-free
+    decode runs the one-kernel path for the full-size layer at T = 1 and 4 and
+    declines the tiny layer, whose fallback kernels unpack nibbles."""
     import ctypes
     L, x = S.draw_config(name)
     assert L.code_bits == 8
@@ -313,19 +314,20 @@ def test_w8_layer(mw, torch, name):
     assert nk == (1 if L.H == 2048 else 7), nk   # grouped path: router, top-k, grouping, gather, 2 GEMMs, combine
     if x.shape[0] >= 8:
         check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[4:8]))), ref[4:8])
-    # the allocation-free decode: the one-kernel path at T = 1 (full-size layer only);
-    # its T >= 2 kernels unpack nibbles, so one-byte codes are declined there
+    # the allocation-free decode: the one-kernel path, once per row (full-size
+    # layer only); its fallback kernels unpack nibbles, so the tiny layer's
+    # one-byte codes are declined
     out = torch.empty((4, L.H), dtype=torch.bfloat16, device="cuda")
-    rc1 = mw.moe_w4_forward_decode_noalloc(ctypes.byref(dl.c), 1, xd.data_ptr(), out.data_ptr(), None)
-    if L.H == 2048:
-        assert rc1 == mw.MOE_W4_OK
-        torch.cuda.synchronize()
-        check_out(to_np_bits(out[:1]), ref[:1])
-    else:
-        assert rc1 == mw.MOE_W4_ERR_UNSUPPORTED
-    if x.shape[0] >= 4:
-        assert mw.moe_w4_forward_decode_noalloc(ctypes.byref(dl.c), 4, xd.data_ptr(), out.data_ptr(),
-                                                None) == mw.MOE_W4_ERR_UNSUPPORTED
+    for T in (1, 4):
+        if x.shape[0] < T:
+            continue
+        rc = mw.moe_w4_forward_decode_noalloc(ctypes.byref(dl.c), T, xd.data_ptr(), out.data_ptr(), None)
+        if L.H == 2048:
+            assert rc == mw.MOE_W4_OK
+            torch.cuda.synchronize()
+            check_out(to_np_bits(out[:T]), ref[:T])
+        else:
+            assert rc == mw.MOE_W4_ERR_UNSUPPORTED
     assert dl.status() == 0
 
 
@@ -353,6 +355,36 @@ def test_decode_single_tokens(mw, torch, name):
     torch.cuda.synchronize()
     got = np.concatenate([to_np_bits(o) for o in outs])
     check_out(got, O.moe_layer(L, xs)["out"])
+    assert dl.status() == 0
+
+
+@pytest.mark.parametrize("T", [2, 3, 5])
+def test_decode_rows_fused(mw, torch, T):
+    """Decode calls of a few rows run the one-kernel batch-1 decode once per
+    row: moe_w4_decode_path says so, the trace counts T kernels, and the output
+    equals the rows' separate batch-1 calls bit for bit and the oracle within
+    the layer tolerance.  With the row limit set to 1 the same call takes the
+    grouped path (7 kernels), also within the tolerance; 6 rows take it by
+    default."""
+    L, x, dl = layer_of(mw, "decode_T1", 16)
+    ref = O.moe_layer(L, x[:T])["out"]
+    assert mw.decode_path(dl, T) == mw.MOE_W4_PATH_FUSED_ROWS
+    assert mw.decode_path(dl, 6) == mw.MOE_W4_PATH_GROUPED
+    rows, nk = _traced_decode(mw, torch, dl, x[:T])
+    assert nk == T, nk
+    check_out(rows, ref)
+    singles = np.concatenate([to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[t:t + 1])))
+                              for t in range(T)])
+    assert np.array_equal(rows, singles)
+    assert mw.moe_w4_set_decode_fused_rows(1) == mw.MOE_W4_OK
+    try:
+        assert mw.decode_path(dl, T) == mw.MOE_W4_PATH_GROUPED
+        grouped, nk = _traced_decode(mw, torch, dl, x[:T])
+    finally:
+        assert mw.moe_w4_set_decode_fused_rows(0) == mw.MOE_W4_OK
+    assert nk == 7, nk   # router, top-k, grouping, gather, 2 GEMMs, combine
+    check_out(grouped, ref)
+    assert mw.decode_path(dl, T) == mw.MOE_W4_PATH_FUSED_ROWS
     assert dl.status() == 0
 
 
@@ -429,9 +461,11 @@ def test_large_scales_small_activations(mw, torch):
     """Scales of 1e1 .. 4e2 (the generator's times 2^12, exact in bf16) with
     activations near 6e-5 (times 2^-14), router weights times 2^12 (the same
     scores): the rebuilt weights, h and the expert outputs (up to about 4e4) stay
-    within fp16, so prefill and a 4-row decode match the oracle and the status
-    word stays clear.  (Batch-1 decode with 4-bit codes holds half of x divided by
-    16 in fp16, below the fp16 normal range at these activations: not run here.)"""
+    within fp16, so prefill and a 4-row decode on the grouped path match the
+    oracle and the status word stays clear.  (The one-kernel batch-1 decode, which
+    by default also takes calls of up to 5 rows, holds half of x divided by 16 in
+    fp16 with 4-bit codes, below the fp16 normal range at these activations: not
+    run here.)"""
     L0 = S.draw_layer(2048, 256, 512, 8, 1.0, seed=57)
     x0 = S.draw_tokens(L0, 40, seed=57)
     L = _scaled_layer(L0, 12)
@@ -444,7 +478,12 @@ def test_large_scales_small_activations(mw, torch):
     check_route(r, L, x)
     ref = O.moe_layer(L, x)["out"]
     check_out(to_np_bits(mw.forward_prefill(dl, xd)), ref)
-    check_out(to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[3:7]))), ref[3:7])
+    assert mw.moe_w4_set_decode_fused_rows(1) == mw.MOE_W4_OK
+    try:
+        got = to_np_bits(mw.forward_decode(dl, mw.tokens_to_device(x[3:7])))
+    finally:
+        assert mw.moe_w4_set_decode_fused_rows(0) == mw.MOE_W4_OK
+    check_out(got, ref[3:7])
     assert dl.status() == 0
 
 
