@@ -428,6 +428,21 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                                    : mbar_wait(&a_empty[sa], ((gk / SA) & 1) ^ 1, abort_flag, a.status));
                         if (!ok) break;
                         const uint8_t* cr = C_of(sc, mat) + row * GG::kCodesRowBytes;
+                        // the step's code chunks, all requested before the first tensor-memory
+                        // store (which orders later shared-memory loads behind it)
+                        constexpr int kCPQ = BITS == 8 ? 2 : 1;   // 16-byte chunks per 32 columns
+                        uint4 wc[2][2][kCPQ];
+#pragma unroll
+                        for (int grp = 0; grp < 2; ++grp) {
+                            if (!DUAL && grp != hsel) continue;
+#pragma unroll
+                            for (int qq = 0; qq < 2; ++qq)
+#pragma unroll
+                                for (int hh2 = 0; hh2 < kCPQ; ++hh2) {
+                                    const int c = kCPQ * (2 * grp + qq) + hh2;
+                                    wc[grp][qq][hh2] = *reinterpret_cast<const uint4*>(cr + ((c ^ sw) << 4));
+                                }
+                        }
                         tc_fence_after();   // the MMAs that read this A slot have completed
                         // this thread's weight row -> its TMEM lane, 64 columns of fp16 pairs, in quads of 16
                         const uint32_t tdst =
@@ -452,8 +467,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                                 if (BITS == 8) {   // two 16-byte chunks of four words
     #pragma unroll
                                     for (int hh2 = 0; hh2 < 2; ++hh2) {
-                                        const int c = 2 * q + hh2;
-                                        const uint4 w = *reinterpret_cast<const uint4*>(cr + ((c ^ sw) << 4));
+                                        const uint4 w = wc[grp][qq][hh2 % kCPQ];
                                         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
     #pragma unroll
                                         for (int wi = 0; wi < 4; ++wi) {
@@ -467,7 +481,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                                         }
                                     }
                                 } else {           // one 16-byte chunk of four words
-                                    const uint4 w = *reinterpret_cast<const uint4*>(cr + ((q ^ sw) << 4));
+                                    const uint4 w = wc[grp][qq][0];
                                     const uint32_t words[4] = {w.x, w.y, w.z, w.w};
     #pragma unroll
                                     for (int wi = 0; wi < 4; ++wi) {
