@@ -423,22 +423,22 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         // does (SA <= SB, so that barrier cannot have moved on by a further
                         // phase meanwhile), and no separate commit is spent.
                         if constexpr (DUAL) {
+                            // gate/up: the codes and the A slot first, then the step's code chunks
+                            // requested together (a tensor-memory store orders later shared-memory
+                            // loads behind it), then each quad rebuilt and stored in turn (measured
+                            // faster than rebuilding any part of the step before the slot wait)
                             ok = mbar_wait(&c_full[sc], (gk / SC) & 1, abort_flag, a.status) &&
-                                 (DUAL ? (gk < SA || mbar_wait(&b_empty[(gk - SA) % SB], ((gk - SA) / SB) & 1, abort_flag,
-                                                               a.status))
-                                       : mbar_wait(&a_empty[sa], ((gk / SA) & 1) ^ 1, abort_flag, a.status));
+                                 (gk < SA || mbar_wait(&b_empty[(gk - SA) % SB], ((gk - SA) / SB) & 1, abort_flag,
+                                                       a.status));
                             if (!ok) break;
                             const uint8_t* cr = C_of(sc, mat) + row * GG::kCodesRowBytes;
-                            // the step's code chunks, all requested before the first tensor-memory
-                            // store (which orders later shared-memory loads behind it)
                             constexpr int kCPQ = BITS == 8 ? 2 : 1;   // 16-byte chunks per 32 columns
                             uint4 wc[2][2][kCPQ];
-    #pragma unroll
+#pragma unroll
                             for (int grp = 0; grp < 2; ++grp) {
-                                if (!DUAL && grp != hsel) continue;
-    #pragma unroll
+#pragma unroll
                                 for (int qq = 0; qq < 2; ++qq)
-    #pragma unroll
+#pragma unroll
                                     for (int hh2 = 0; hh2 < kCPQ; ++hh2) {
                                         const int c = kCPQ * (2 * grp + qq) + hh2;
                                         wc[grp][qq][hh2] = *reinterpret_cast<const uint4*>(cr + ((c ^ sw) << 4));
@@ -448,9 +448,8 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                             // this thread's weight row -> its TMEM lane, 64 columns of fp16 pairs, in quads of 16
                             const uint32_t tdst =
                                 taddr + ((uint32_t)(row & ~31) << 16) + GG::A_TMEM0 + sa * GG::A_COLS + mat * (kGK / 2);
-        #pragma unroll
+    #pragma unroll
                             for (int grp = 0; grp < 2; ++grp) {
-                                if (!DUAL && grp != hsel) continue;
                                 const float sf = bf16_bits_to_float((uint16_t)(grp ? (s2w >> 16) : (s2w & 0xFFFFu)));
                                 const float bf = bf16_bits_to_float((uint16_t)(grp ? (b2w >> 16) : (b2w & 0xFFFFu)));
                                 // the group's rebuilt weights |s q + b| must stay within fp16 (q <= the
@@ -461,16 +460,16 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                                 const __half b_h = __float2half_rn(bf);
                                 const __half2 s2 = __halves2half2(s_h, s_h), s2_16 = __halves2half2(s_h16, s_h16);
                                 const __half2 b2 = __halves2half2(b_h, b_h);
-        #pragma unroll
+    #pragma unroll
                                 for (int qq = 0; qq < 2; ++qq) {   // 32 columns of the group -> 16 TMEM columns
                                     const int q = 2 * grp + qq;
                                     uint32_t o[16];
                                     if (BITS == 8) {   // two 16-byte chunks of four words
-        #pragma unroll
+    #pragma unroll
                                         for (int hh2 = 0; hh2 < 2; ++hh2) {
                                             const uint4 w = wc[grp][qq][hh2 % kCPQ];
                                             const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-        #pragma unroll
+    #pragma unroll
                                             for (int wi = 0; wi < 4; ++wi) {
                                                 uint32_t q2[2];
                                                 if (E4M3)
@@ -484,7 +483,7 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                                     } else {           // one 16-byte chunk of four words
                                         const uint4 w = wc[grp][qq][0];
                                         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-        #pragma unroll
+    #pragma unroll
                                         for (int wi = 0; wi < 4; ++wi) {
                                             uint32_t q4[4];
                                             dequant8_f16(words[wi], s2, s2_16, b2, q4);
@@ -497,7 +496,6 @@ grouped_w4_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant
                         } else {
                             // down: the step rebuilt in registers first, while the MMAs of the
                             // previous unit may still read A slot sa, then stored once it is free
-                            // (gate/up, whose thread holds twice the weights, measured slower so)
                             if (!(ok = mbar_wait(&c_full[sc], (gk / SC) & 1, abort_flag, a.status))) break;
                             const uint8_t* cr = C_of(sc, mat) + row * GG::kCodesRowBytes;
                             constexpr int kCPQ = BITS == 8 ? 2 : 1;   // 16-byte chunks per 32 columns
