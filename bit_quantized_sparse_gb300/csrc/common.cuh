@@ -167,48 +167,11 @@ MW4_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint
         :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
-// Four rows of a 2D map (box one row high) at column c0 from rows r0..r3, to
-// four consecutive box rows at dst (128-byte aligned); swizzling follows the
-// shared-memory address, as for any tiled copy.
-MW4_DEV void tma_gather4(void* dst, const CUtensorMap* map, int c0, int r0, int r1, int r2, int r3, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-           "r"(smem_u32(bar))
-        : "memory");
-}
 // Contiguous global -> shared copy; size and both addresses multiples of 16.
 MW4_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
-}
-// The same two loads with an L2 cache policy (createpolicy): data read once per
-// call is marked evict-first so that it does not displace what stays hot in
-// L2 between calls (the kernel's instructions among it).
-MW4_DEV uint64_t l2_policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-MW4_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;"
-        :: "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)),
-           "l"(policy)
-        : "memory");
-}
-MW4_DEV void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-        :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
-}
-// Pull a contiguous global range into L2 (no completion tracking); size a
-// multiple of 16 bytes.
-MW4_DEV void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
 }
 MW4_DEV void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -268,20 +231,6 @@ MW4_DEV uint32_t umma_idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread (kind::f16: the
-// instruction descriptor selects fp16 or bf16 operands).
-MW4_DEV void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{.reg .pred p; setp.ne.b32 p, %4, 0;"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;}"
-        :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
-}
-// Arrive on `bar` once every MMA issued so far by this thread has completed.
-MW4_DEV void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 :: "r"(smem_u32(bar)) : "memory");
-}
-
 // Warp-level issue: the whole (converged) warp executes these with the same
 // operands and one elected lane issues the instruction.  Keeping the loop that
 // feeds tcgen05.mma warp-uniform, rather than running it in one lane of a
@@ -319,18 +268,6 @@ MW4_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 MW4_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x 32 consecutive 32-bit columns; thread t of the warp writes lane
-// (base lane + t).  Follow with tmem_wait_st before signalling a consumer.
-MW4_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-           "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-           "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-           "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
 MW4_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
@@ -339,15 +276,6 @@ MW4_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
         : "memory");
 }
 MW4_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// D[tmem] (+)= A[tmem] * B[smem]^T: A is 128 lanes (rows) x K/2 columns of
-// 16-bit pairs; issued by one thread.
-MW4_DEV void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{.reg .pred p; setp.ne.b32 p, %4, 0;"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}"
-        :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
-}
 
 // ---------------------------------------------------------------------------
 // 4-bit code unpacking to fp16 (exact), in "chunk order"
@@ -431,7 +359,6 @@ MW4_DEV float silu_tanh(float z) {
     asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
     return fmaf(h, t, h);
 }
-MW4_DEV float sigmoid_f(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
 
 // ---------------------------------------------------------------------------

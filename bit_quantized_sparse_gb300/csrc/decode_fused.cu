@@ -1074,13 +1074,6 @@ static cudaError_t launch_fused_row(const moe_w4_layer& L, const FusedMaps& m, c
     return e;
 }
 
-cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
-                                cudaStream_t st) {
-    FusedMaps m;
-    if (!fused_maps(L, &m)) return cudaErrorInvalidValue;
-    return launch_fused_row(L, m, x, out, d, st);
-}
-
 // Rows 0..T-1 one after another, each a complete batch-1 call on the stream
 // (row t's routing at d.idx + t*k, d.w + t*k, d.gamma + t).  Consecutive calls
 // overlap only through programmatic dependent launch, so each row still sees

@@ -147,13 +147,10 @@ struct DecodeWs {
     uint64_t* fused_hsx;    // tagged sums of 16-value pieces of h, fused_hsx_bytes (fused T=1 kernel)
 };
 bool decode_fused_supported(const moe_w4_layer& L);
-// One cooperative launch of the fused T=1 kernel; an error means the launch
-// was refused and nothing was enqueued (the caller takes another path).
-cudaError_t launch_decode_fused(const moe_w4_layer& L, const uint16_t* x, uint16_t* out, const DecodeWs& d,
-                                cudaStream_t st);
-// T rows as T consecutive launches of that kernel (row t's routing at
-// d.idx + t*k, d.w + t*k, d.gamma + t); returns the rows launched, fewer than
-// T only when a launch was refused (nothing enqueued for the rest).
+// T rows as T consecutive cooperative launches of the fused batch-1 kernel
+// (row t's routing at d.idx + t*k, d.w + t*k, d.gamma + t); returns the rows
+// launched, fewer than T only when a launch was refused (nothing enqueued for
+// the rest; the caller takes another path).
 int launch_decode_fused_rows(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
                              cudaStream_t st);
 // Decode calls of at most this many rows run row by row through the fused
