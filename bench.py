@@ -480,7 +480,9 @@ def run_ablations(torch, mw, c, dl, x, out, ws, stream, timed, capture, args):
       once and split on every call;
     - dequant: ms per call (graph replays) with the weights rebuilt in the
       GEMMs' tiles (the product) and with a separate pass that writes every
-      weight in fp16 before the GEMMs read them back."""
+      weight in fp16 before the GEMMs read them back;
+    - paired: each alternative against the product path in alternating
+      rounds, with the median ratio and its bootstrap confidence interval."""
     res = {"tiles_ms": {}, "routing_ms": {}, "router_prep_ms": {}, "dequant_ms": {}}
     nscr = mw.moe_w4_ablation_scratch_bytes(ctypes.byref(dl.c), mw.MOE_W4_ABLATE_SEPARATE_DEQUANT)
     scratch = torch.empty(nscr, dtype=torch.uint8, device=x.device)   # every weight in fp16 (1.6 GB)
@@ -503,8 +505,52 @@ def run_ablations(torch, mw, c, dl, x, out, ws, stream, timed, capture, args):
             torch.cuda.synchronize()
         return 1e3 * (time.perf_counter() - t0) / n
 
+    def paired_graphs(fa, fb, rounds):
+        """A and B captured as graphs, then replayed in alternating rounds (A
+        first in even rounds, B first in odd ones), each replay between its own
+        events on the replay stream."""
+        gs = []
+        for fn in (fa, fb):
+            with torch.cuda.stream(stream):
+                fn()
+            torch.cuda.synchronize()
+            gs.append(capture(fn))
+        for g in gs:
+            for _ in range(args.warmup):
+                g.replay()
+        torch.cuda.synchronize()
+        ts = ([], [])
+        for i in range(rounds):
+            for j in ((0, 1) if i % 2 == 0 else (1, 0)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    gs[j].replay()
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                ts[j].append(e0.elapsed_time(e1) / 1e3)
+        return paired_ratio(*ts)
+
+    def paired_eager(fa, fb, rounds):
+        """The same with eager calls (host wall clock, synchronised per call)."""
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fa()
+                fb()
+            torch.cuda.synchronize()
+            ts = ([], [])
+            for i in range(rounds):
+                for j in ((0, 1) if i % 2 == 0 else (1, 0)):
+                    t0 = time.perf_counter()
+                    (fa, fb)[j]()
+                    torch.cuda.synchronize()
+                    ts[j].append(time.perf_counter() - t0)
+        return paired_ratio(*ts)
+
     plain = mw.MoeW4Layer.from_buffer_copy(dl.c)
     plain.router_prep = None
+    res["paired"] = {}
+    rounds = max(2 * args.steps, 20)
     for Tm in ABLATION_T:
         xs, os_ = x[:Tm], out[:Tm]
         row = {}
@@ -537,6 +583,22 @@ def run_ablations(torch, mw, c, dl, x, out, ws, stream, timed, capture, args):
                                                 ws.numel(), st()), "prefill")
         res["router_prep_ms"][f"T{Tm}"] = {"prepared_once": row[f"bn{TILE_CHOICES[0][0]}_du{TILE_CHOICES[0][1]}"],
                                           "split_every_call": graph_ms(split_each_call)}
+
+        # the same comparisons as paired, interleaved rounds: A is always the product path
+        def product():
+            mw.forward_prefill(dl, xs, out=os_, ws=ws)
+
+        def bn64():
+            assert mw.moe_w4_set_tile_override(64, 0) == mw.MOE_W4_OK
+            try:
+                mw.forward_prefill(dl, xs, out=os_, ws=ws)
+            finally:
+                mw.moe_w4_set_tile_override(0, 0)
+        res["paired"][f"T{Tm}"] = {
+            "separate_fp16_pass_vs_fused": paired_graphs(product, separate_dequant, rounds),
+            "host_synchronised_vs_gpu_resident_eager": paired_eager(product, host_routed, rounds),
+            "split_every_call_vs_prepared_once": paired_graphs(product, split_each_call, rounds),
+            "bn64_vs_default_tile": paired_graphs(product, bn64, rounds)}
     if dl.status() != 0:
         raise RuntimeError(f"device status {dl.status()} after the ablations")
     return res
@@ -583,6 +645,21 @@ def spread(values, scale=1.0, n_boot=2000, seed=0):
     return {"median": float(np.median(v)), "p10": float(np.percentile(v, 10)), "p90": float(np.percentile(v, 90)),
             "median_ci95": [float(np.percentile(meds, 2.5)), float(np.percentile(meds, 97.5))],
             "replays": int(v.size)}
+
+
+def paired_ratio(a_s, b_s, n_boot=2000, seed=0):
+    """Paired comparison of two implementations timed in alternating rounds
+    (per-round seconds of A and of B, same length): the median of each in ms,
+    and the median of the per-round ratios B/A with a 95% bootstrap confidence
+    interval (percentile method, rounds resampled with replacement, seeded)."""
+    a = np.asarray(a_s, np.float64)
+    b = np.asarray(b_s, np.float64)
+    r = b / a
+    rng = np.random.default_rng(seed)
+    meds = np.median(r[rng.integers(0, r.size, size=(n_boot, r.size))], axis=1)
+    return {"a_ms": 1e3 * float(np.median(a)), "b_ms": 1e3 * float(np.median(b)),
+            "ratio_median": float(np.median(r)),
+            "ratio_ci95": [float(np.percentile(meds, 2.5)), float(np.percentile(meds, 97.5))], "rounds": int(r.size)}
 
 
 def variant_summary(c, w, chunk, world, pk):

@@ -113,3 +113,20 @@ def test_spread_bootstrap_interval():
     assert min(small) <= lo <= a["median"] <= hi <= max(small)
     lo2, hi2 = bench.spread(big)["median_ci95"]
     assert hi2 - lo2 < hi - lo
+
+
+def test_paired_ratio():
+    """Paired rounds: an alternative that always takes twice as long gives a ratio
+    of exactly 2 with a degenerate interval; with noise the interval holds the
+    median ratio, is reproducible, and the per-arm medians are in ms."""
+    import numpy as np
+    p = bench.paired_ratio([1e-3, 2e-3, 3e-3], [2e-3, 4e-3, 6e-3])
+    assert p["ratio_median"] == 2.0 and p["ratio_ci95"] == [2.0, 2.0] and p["rounds"] == 3
+    assert p["a_ms"] == 2.0 and p["b_ms"] == 4.0
+    rng = np.random.default_rng(3)
+    a = rng.normal(1.0, 0.05, 40)
+    b = a * 1.3 + rng.normal(0.0, 0.02, 40)
+    q, q2 = bench.paired_ratio(a, b), bench.paired_ratio(a, b)
+    assert q["ratio_ci95"] == q2["ratio_ci95"]
+    lo, hi = q["ratio_ci95"]
+    assert lo <= q["ratio_median"] <= hi and 1.2 < lo and hi < 1.4
