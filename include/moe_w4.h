@@ -327,7 +327,7 @@ int moe_w4_set_tile_override(int bn, int du);
  * turns it off. */
 int moe_w4_test_skip_publish(void* workspace, size_t ws_bytes, int on, cudaStream_t stream);
 
-/* Test hook: the block records of the last prefill (or multi-row decode) call
+/* Test hook: the block records of the last prefill (or grouped-path decode) call
  * enqueued on `workspace` for T tokens, copied on `stream` to `dst` (device
  * memory, at least moe_w4_test_block_records_bytes(L, T) bytes): two int32
  * tile counts (gate/up blocks x I/128, down units x H/128), then one record of
