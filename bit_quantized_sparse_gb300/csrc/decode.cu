@@ -195,15 +195,22 @@ __global__ void __launch_bounds__(kDN_Warps * 32) decode_down_kernel(moe_w4_laye
     }
 }
 
-cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d,
+cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d_in,
                           cudaStream_t st) {
     const int k = L.top_k;
+    DecodeWs d = d_in;
     if (decode_fused_supported(L)) {   // one launch per row for the whole layer
         const int done = launch_decode_fused_rows(L, T, x, out, d, st);
         if (done == T) return cudaGetLastError();
-        // refused: at the first row, the three kernels below; later (the same
-        // launch went through just before), an error for the caller
-        if (done > 0) return cudaErrorLaunchFailure;
+        // a launch was refused (the grid cannot be resident at once): the rows not
+        // yet enqueued take the three kernels below, which read 4-bit codes only
+        if (code_bits_of(L) != 4) return cudaErrorNotSupported;
+        x += (size_t)done * L.H;
+        out += (size_t)done * L.H;
+        d.idx += (size_t)done * k;
+        d.w += (size_t)done * k;
+        d.gamma += done;
+        T -= done;
     }
     static bool attrs_set[64] = {};
     int dev = 0;

@@ -252,8 +252,8 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x,
  * one-kernel batch-1 path covers the layer it runs that kernel once per row,
  * for every T (the grouped path's buffers would not fit); elsewhere, or when
  * its cooperative launch is refused, per-row CUDA-core GEMVs (router, gate/up,
- * down kernels; 4-bit codes only), with results within the same tolerance of
- * the oracle.  The
+ * down kernels; 4-bit codes only: a refused launch with one-byte codes returns
+ * MOE_W4_ERR_LAUNCH), with results within the same tolerance of the oracle.  The
  * scratch lives in one fixed device array of
  * MOE_W4_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library keeps until the process exits.
