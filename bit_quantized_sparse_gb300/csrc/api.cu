@@ -209,7 +209,7 @@ int moe_w4_prepare_router(const moe_w4_layer* L, void* dst, size_t dst_bytes, cu
 }
 
 size_t moe_w4_workspace_size(const moe_w4_layer* L, int T_max) {
-    if (check_layer(L) != MOE_W4_OK || T_max < 0) return 0;
+    if (check_layer(L) != MOE_W4_OK || T_max < 0 || T_max > MOE_W4_MAX_TOKENS) return 0;
     return ws_layout(*L, T_max).total;
 }
 
@@ -235,6 +235,7 @@ int moe_w4_test_block_records(const moe_w4_layer* L, int T, const void* workspac
     int r = check_layer(L);
     if (r) return r;
     if (T < 1 || !dst) return MOE_W4_ERR_INVALID;
+    if (T > MOE_W4_MAX_TOKENS) return MOE_W4_ERR_UNSUPPORTED;
     WsLayout w;
     if ((r = check_ws(*L, T, const_cast<void*>(workspace), ws_bytes, &w))) return r;
     const size_t rec = (size_t)w.max_blocks * sizeof(int4);
@@ -246,7 +247,7 @@ int moe_w4_test_block_records(const moe_w4_layer* L, int T, const void* workspac
 }
 
 size_t moe_w4_test_block_records_bytes(const moe_w4_layer* L, int T) {
-    if (check_layer(L) != MOE_W4_OK || T < 1) return 0;
+    if (check_layer(L) != MOE_W4_OK || T < 1 || T > MOE_W4_MAX_TOKENS) return 0;
     return 2 * sizeof(int32_t) + (size_t)ws_layout(*L, T).max_blocks * sizeof(int4);
 }
 
@@ -283,6 +284,7 @@ int moe_w4_route(const moe_w4_layer* L, int T, const moe_w4_bf16* x, int32_t* to
     int r = check_layer(L);
     if (r) return r;
     if (T < 0) return MOE_W4_ERR_INVALID;
+    if (T > MOE_W4_MAX_TOKENS) return MOE_W4_ERR_UNSUPPORTED;
     if (!topk_idx || !topk_w || !shared_gamma || !counts || !offsets || !perm || !inv)
         return MOE_W4_ERR_INVALID;
     if (T > 0 && !x) return MOE_W4_ERR_INVALID;
@@ -380,6 +382,7 @@ int moe_w4_forward_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, m
     int r = check_layer(L);
     if (r) return r;
     if (T < 0) return MOE_W4_ERR_INVALID;
+    if (T > MOE_W4_MAX_TOKENS) return MOE_W4_ERR_UNSUPPORTED;
     if (T == 0) return MOE_W4_OK;
     if (!x || !out) return MOE_W4_ERR_INVALID;
     if (!aligned16(x) || !aligned16(out)) return MOE_W4_ERR_ALIGN;
@@ -404,6 +407,7 @@ int moe_w4_ablation_prefill(const moe_w4_layer* L, int T, const moe_w4_bf16* x, 
         if (scratch_bytes < f16_weights_bytes(*L)) return MOE_W4_ERR_WORKSPACE;
     }
     if (T < 0) return MOE_W4_ERR_INVALID;
+    if (T > MOE_W4_MAX_TOKENS) return MOE_W4_ERR_UNSUPPORTED;
     if (T == 0) return MOE_W4_OK;
     if (!x || !out) return MOE_W4_ERR_INVALID;
     if (!aligned16(x) || !aligned16(out)) return MOE_W4_ERR_ALIGN;

@@ -50,6 +50,7 @@ MOE_W4_STATUS_WAIT_TIMEOUT = 1
 MOE_W4_STATUS_BAD_INDEX = 2
 MOE_W4_STATUS_FP16_RANGE = 4
 DECODE_MAX_T = 16
+MAX_TOKENS = 1 << 22                 # MOE_W4_MAX_TOKENS
 MOE_W4_PATH_FUSED_ROWS = 1           # moe_w4_decode_path
 MOE_W4_PATH_GROUPED = 2
 

@@ -141,9 +141,17 @@ enum {
 size_t moe_w4_router_prep_bytes(const moe_w4_layer* L);
 int moe_w4_prepare_router(const moe_w4_layer* L, void* dst, size_t dst_bytes, cudaStream_t stream);
 
+/* Largest token count of one routing or prefill call (longer prompts are
+ * chunked by the caller, as the benchmark's 4096-row chunks are): the kernels
+ * index the T * (top_k + 1) grouped rows with 32-bit integers and tile the
+ * tokens over at most 65535 router CTAs.  Larger T returns
+ * MOE_W4_ERR_UNSUPPORTED (moe_w4_workspace_size: 0). */
+#define MOE_W4_MAX_TOKENS (1 << 22)
+
 /* Bytes of workspace needed for calls with up to T_max tokens (0 if the layer
- * is invalid).  The workspace holds routing intermediates, the grouped
- * activations and a small control header at offset 0. */
+ * is invalid or T_max is outside 0..MOE_W4_MAX_TOKENS).  The workspace holds
+ * routing intermediates, the grouped activations and a small control header at
+ * offset 0. */
 size_t moe_w4_workspace_size(const moe_w4_layer* L, int T_max);
 
 /* Clears the whole workspace (status word, completion counters, exchange
@@ -177,7 +185,7 @@ size_t moe_w4_status_offset(void);
  * with unit activations) lose accuracy without any status bit.  Scale and
  * activation together: scales of 1e3 with activations of 1e-6 are in range. */
 
-/* Routing of T tokens (sections "Qwen creates three different workload
+/* Routing of T tokens, 0 <= T <= MOE_W4_MAX_TOKENS (sections "Qwen creates three different workload
  * shapes" and "Keep expert routing on the GPU").
  *   x         bf16  [T][H]
  *   topk_idx  int32 [T][top_k]  selected experts, by descending score
@@ -230,7 +238,7 @@ int moe_w4_decode_path(const moe_w4_layer* L, int T, int* path);
  * MOE_W4_ERR_INVALID outside 0..16. */
 int moe_w4_set_decode_fused_rows(int max_rows);
 
-/* Layer output for a prefill batch, T >= 1 (section "Dequantise weights
+/* Layer output for a prefill batch, 1 <= T <= MOE_W4_MAX_TOKENS (section "Dequantise weights
  * during matrix multiplication"): routing as moe_w4_route, then grouped W4
  * GEMMs on the tensor cores (dequantised fp16 weight tiles and fp32
  * accumulators in tensor memory, fp16 activations) with a SwiGLU epilogue that

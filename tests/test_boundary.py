@@ -89,6 +89,22 @@ def test_noalloc_code_formats_rejected(mw, bits, fmt, T):
     assert mw.moe_w4_forward_decode_noalloc(ctypes.byref(L), T, ws, ws, None) == mw.MOE_W4_ERR_UNSUPPORTED
 
 
+def test_token_count_cap(mw):
+    """Routing and prefill take at most MOE_W4_MAX_TOKENS rows (32-bit row
+    indices, at most 65535 router CTAs along the tokens): one more is refused on
+    the host, before any device work, and sizes no workspace."""
+    L = _layer(mw)
+    p = ctypes.byref(L)
+    a = 1 << 12
+    big = mw.MAX_TOKENS + 1
+    assert mw.moe_w4_workspace_size(p, mw.MAX_TOKENS) > 0
+    assert mw.moe_w4_workspace_size(p, big) == 0
+    assert mw.moe_w4_forward_prefill(p, big, a, a, a, 1 << 62, None) == mw.MOE_W4_ERR_UNSUPPORTED
+    z = [a] * 7
+    assert mw.moe_w4_route(p, big, a, *z, a, 1 << 62, None) == mw.MOE_W4_ERR_UNSUPPORTED
+    assert mw.moe_w4_test_block_records_bytes(p, big) == 0
+
+
 def test_decode_path_query(mw):
     """moe_w4_decode_path (a host query, no device work): argument checks, and
     a valid call names one of the two paths.  The row limit accepts 0..16."""
