@@ -66,6 +66,15 @@ static void read_tile_env() {
 static std::atomic<int> g_fused_rows{kDecodeFusedRows};
 int decode_fused_rows_max() { return g_fused_rows.load(); }
 
+// Test hook (moe_w4_test_refuse_fused_after): at most this many rows of a call
+// go through the one-kernel path before it behaves as if the next cooperative
+// launch were refused; negative: off.
+static std::atomic<int> g_test_fused_allow{-1};
+int test_fused_rows_allowed(int T) {
+    const int a = g_test_fused_allow.load();
+    return a < 0 || a > T ? T : a;
+}
+
 TileCfg tile_cfg(const moe_w4_layer& L, int T) {
     std::call_once(g_tile_env_once, read_tile_env);
     TileCfg c{kBN, (int64_t)T * L.top_k >= 64 * (int64_t)L.E ? down_blocks_per_unit(L.I) : 1};
@@ -262,6 +271,11 @@ int moe_w4_set_decode_fused_rows(int max_rows) {
     return MOE_W4_OK;
 }
 
+int moe_w4_test_refuse_fused_after(int rows) {
+    g_test_fused_allow.store(rows < 0 ? -1 : rows);
+    return MOE_W4_OK;
+}
+
 int moe_w4_decode_path(const moe_w4_layer* L, int T, int* path) {
     int r = check_layer(L);
     if (r) return r;
@@ -335,7 +349,7 @@ int moe_w4_forward_decode(const moe_w4_layer* L, int T, const moe_w4_bf16* x, mo
     d.fused_scores = at<uint64_t>(workspace, w.dec_scores);
     d.fused_hx = at<uint64_t>(workspace, w.dec_hx);
     d.fused_hsx = at<uint64_t>(workspace, w.dec_hsx);
-    const int done = launch_decode_fused_rows(*L, T, x, out, d, stream);
+    const int done = launch_decode_fused_rows(*L, test_fused_rows_allowed(T), x, out, d, stream);
     if (done == T) return launch_status(cudaGetLastError());
     // a cooperative launch was refused (the grid cannot be resident at once on
     // this device or partition): the rows not yet enqueued take the grouped path

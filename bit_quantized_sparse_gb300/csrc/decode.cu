@@ -200,7 +200,7 @@ cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint1
     const int k = L.top_k;
     DecodeWs d = d_in;
     if (decode_fused_supported(L)) {   // one launch per row for the whole layer
-        const int done = launch_decode_fused_rows(L, T, x, out, d, st);
+        const int done = launch_decode_fused_rows(L, test_fused_rows_allowed(T), x, out, d, st);
         if (done == T) return cudaGetLastError();
         // a launch was refused (the grid cannot be resident at once): the rows not
         // yet enqueued take the three kernels below, which read 4-bit codes only

@@ -85,6 +85,7 @@ _SIGS = {
     "moe_w4_set_tile_override": (c_int, [c_int, c_int]),
     "moe_w4_set_decode_fused_rows": (c_int, [c_int]),
     "moe_w4_decode_path": (c_int, [_P, c_int, ctypes.POINTER(c_int)]),
+    "moe_w4_test_refuse_fused_after": (c_int, [c_int]),
     "moe_w4_last_traced_kernels": (c_int, []),
     "moe_w4_forward_decode_noalloc": (c_int, [_P, c_int, c_void_p, c_void_p, c_void_p]),
     "moe_w4_noalloc_status": (c_int, [c_void_p, c_void_p]),
@@ -114,6 +115,7 @@ moe_w4_set_trace_events = _lib.moe_w4_set_trace_events
 moe_w4_set_tile_override = _lib.moe_w4_set_tile_override
 moe_w4_set_decode_fused_rows = _lib.moe_w4_set_decode_fused_rows
 moe_w4_decode_path = _lib.moe_w4_decode_path
+moe_w4_test_refuse_fused_after = _lib.moe_w4_test_refuse_fused_after
 moe_w4_last_traced_kernels = _lib.moe_w4_last_traced_kernels
 moe_w4_forward_decode_noalloc = _lib.moe_w4_forward_decode_noalloc
 moe_w4_noalloc_status = _lib.moe_w4_noalloc_status

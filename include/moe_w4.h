@@ -335,6 +335,16 @@ int moe_w4_set_tile_override(int bn, int du);
  * turns it off. */
 int moe_w4_test_skip_publish(void* workspace, size_t ws_bytes, int on, cudaStream_t stream);
 
+/* Failure-detection test hook (no production use; process-wide): rows >= 0
+ * makes every following decode call (moe_w4_forward_decode and
+ * moe_w4_forward_decode_noalloc) launch the one-kernel batch-1 path for at
+ * most `rows` of its rows and then take the fallback it takes when a
+ * cooperative launch is refused: the grouped path for the remaining rows (the
+ * per-row CUDA-core kernels in the allocation-free decode, or
+ * MOE_W4_ERR_LAUNCH there for one-byte codes).  Nothing is launched and
+ * refused for real.  rows < 0 turns it off.  Always returns MOE_W4_OK. */
+int moe_w4_test_refuse_fused_after(int rows);
+
 /* Test hook: the block records of the last prefill (or grouped-path decode) call
  * enqueued on `workspace` for T tokens, copied on `stream` to `dst` (device
  * memory, at least moe_w4_test_block_records_bytes(L, T) bytes): two int32

@@ -388,6 +388,25 @@ def test_decode_rows_fused(mw, torch, T):
     assert dl.status() == 0
 
 
+@pytest.mark.parametrize("allow", [0, 1])
+def test_decode_refused_launch_falls_back(mw, torch, allow):
+    """A refused cooperative launch of the one-kernel decode (simulated on the
+    host by moe_w4_test_refuse_fused_after: nothing is refused for real) sends
+    the rows not yet enqueued to the grouped path: a 3-row call with 0 or 1 rows
+    allowed on the one-kernel path ends on the grouped path's 7 kernels and
+    matches the oracle with a clear status."""
+    L, x, dl = layer_of(mw, "decode_T1", 16)
+    ref = O.moe_layer(L, x[:3])["out"]
+    assert mw.moe_w4_test_refuse_fused_after(allow) == mw.MOE_W4_OK
+    try:
+        got, nk = _traced_decode(mw, torch, dl, x[:3])
+    finally:
+        mw.moe_w4_test_refuse_fused_after(-1)
+    assert nk == 7, nk
+    check_out(got, ref)
+    assert dl.status() == 0
+
+
 def test_decode_matches_prefill(mw, torch):
     L, x, dl = layer_of(mw, "decode_T1", 16)
     xd = mw.tokens_to_device(x)

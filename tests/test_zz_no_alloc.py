@@ -148,3 +148,32 @@ def test_noalloc_wait_timeout_then_valid_call(env):
         m = TOL.metrics(O.bf16_to_f64(_bits(torch, out)), ref[i:i + 1])
         assert TOL.within(m), (i, m)
         assert _status(torch, mw) == 0, i
+
+
+def test_noalloc_refused_launch_falls_back(env):
+    """A refused cooperative launch of the one-kernel path in the allocation-free
+    decode (simulated on the host by moe_w4_test_refuse_fused_after): with 1 of
+    3 rows allowed, the other two take the CUDA-core kernels and the output
+    matches the oracle with a clear status; one-byte codes, which those kernels
+    cannot read, return MOE_W4_ERR_LAUNCH instead."""
+    torch, mw = env
+    fn = _fn(mw)
+    stream = torch.cuda.current_stream().cuda_stream
+    for name, ok in (("decode_T1", True), ("w8_T512", False)):
+        L, x = S.draw_config(name, T=3)
+        dl = mw.DeviceLayer(L)
+        xd = mw.tokens_to_device(x)
+        out = torch.full((3, L.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        assert mw.moe_w4_test_refuse_fused_after(1) == mw.MOE_W4_OK
+        try:
+            rc = fn(ctypes.byref(dl.c), 3, xd.data_ptr(), out.data_ptr(), stream)
+            torch.cuda.synchronize()
+        finally:
+            mw.moe_w4_test_refuse_fused_after(-1)
+        if ok:
+            assert rc == mw.MOE_W4_OK
+            m = TOL.metrics(O.bf16_to_f64(_bits(torch, out)), O.moe_layer(L, x)["out"])
+            assert TOL.within(m), m
+            assert _status(torch, mw) == 0
+        else:
+            assert rc == mw.MOE_W4_ERR_LAUNCH
