@@ -69,6 +69,7 @@ int decode_fused_rows_max() { return g_fused_rows.load(); }
 // Test hook (moe_w4_test_refuse_fused_after): at most this many rows of a call
 // go through the one-kernel path before it behaves as if the next cooperative
 // launch were refused; negative: off.
+// (also used by the allocation-free decode in decode.cu)
 static std::atomic<int> g_test_fused_allow{-1};
 int test_fused_rows_allowed(int T) {
     const int a = g_test_fused_allow.load();

@@ -195,6 +195,11 @@ __global__ void __launch_bounds__(kDN_Warps * 32) decode_down_kernel(moe_w4_laye
     }
 }
 
+// The rows of a T-row call that may go through the one-kernel path (T unless
+// the moe_w4_test_refuse_fused_after hook is on; defined with it in api.cu); the
+// rest take the fallback of a refused cooperative launch.
+int test_fused_rows_allowed(int T);
+
 cudaError_t launch_decode(const moe_w4_layer& L, int T, const uint16_t* x, uint16_t* out, const DecodeWs& d_in,
                           cudaStream_t st) {
     const int k = L.top_k;

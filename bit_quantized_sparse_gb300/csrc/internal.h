@@ -156,10 +156,6 @@ int launch_decode_fused_rows(const moe_w4_layer& L, int T, const uint16_t* x, ui
 // Decode calls of at most this many rows run row by row through the fused
 // kernel when it covers the layer (moe_w4_set_decode_fused_rows overrides it).
 int decode_fused_rows_max();
-// The rows of a T-row call that may go through the one-kernel path (T unless
-// the moe_w4_test_refuse_fused_after hook is on); the rest take the fallback as
-// after a refused cooperative launch.
-int test_fused_rows_allowed(int T);
 // Bytes of the fused kernel's exchange buffers for a layer: router score
 // partials (replicated), h, and the sums of h's 32-value pieces.
 size_t fused_scores_bytes(const moe_w4_layer& L);
