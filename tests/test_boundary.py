@@ -89,6 +89,18 @@ def test_noalloc_code_formats_rejected(mw, bits, fmt, T):
     assert mw.moe_w4_forward_decode_noalloc(ctypes.byref(L), T, ws, ws, None) == mw.MOE_W4_ERR_UNSUPPORTED
 
 
+def test_workspace_size_grows_with_tokens(mw):
+    """The workspace a call needs never shrinks as the token count grows (a
+    workspace sized for T_max serves every smaller call), for the benchmark's
+    layer and a small one, across the chunk and block boundaries."""
+    for shape in ((2048, 256, 512, 8), (256, 16, 128, 2)):
+        L = _layer(mw, *shape)
+        sizes = [mw.moe_w4_workspace_size(ctypes.byref(L), t)
+                 for t in (0, 1, 2, 15, 16, 17, 127, 128, 129, 4095, 4096, 4097, 16384)]
+        assert all(a <= b for a, b in zip(sizes, sizes[1:])), sizes
+        assert sizes[0] > 0   # the control header and the batch-1 decode's exchange buffers
+
+
 def test_token_count_cap(mw):
     """Routing and prefill take at most MOE_W4_MAX_TOKENS rows (32-bit row
     indices, at most 65535 router CTAs along the tokens): one more is refused on
